@@ -1,0 +1,24 @@
+"""fp64 CPU oracle for paged GQA decode attention — TEST INFRASTRUCTURE.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It shares no code with the CUDA
+library (``paged_gqa_decode_kvd_gb300``) and neither imports the other.
+
+Parity pins (all in ``tests/test_oracle.py``, run with ``-m "not gpu"``):
+e4m3 decode/encode, row quantise, the paged gather, decode attention, the
+split-free softmax statistics and the importance-score update are each pinned
+to something other than the oracle itself; no function here is "parity
+unpinned".
+"""
+
+from .oracle import (  # noqa: F401
+    build,
+    lib_path,
+    e4m3_decode,
+    e4m3_encode,
+    quantize_rows,
+    OraclePool,
+    decode,
+    score_update,
+    decode_dense_inputs,
+)

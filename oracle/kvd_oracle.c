@@ -1,0 +1,240 @@
+/*
+ * kvd_oracle.c — plain, slow, fp64 CPU oracle for paged GQA decode attention.
+ *
+ * TEST INFRASTRUCTURE.  Only the test suite, the smoke check and the CPU
+ * baseline leg of the benchmark may load this library.  It shares no code,
+ * header, table or constant with the CUDA library and is written straight
+ * from the definitions on the pages:
+ *
+ *  - FP8 E4M3 storage (1 sign, 4 exponent, 3 mantissa bits, max 448; store
+ *    x / scale, multiply the scale back on read): page "LLM에서 KV 캐시는
+ *    얼마나 생길까" (froggydisk.github.io/kv-cache-per-request), section
+ *    "KV 캐시를 줄이는 기법", FP8 format table and the paragraph after it.
+ *  - Paged cache: fixed 16-token blocks and a per-request block table that
+ *    maps the request's j-th block to a physical block; the kernel walks the
+ *    table in order, so scattered blocks give the same result: same page and
+ *    section, PagedAttention paragraphs and the block-table example.
+ *  - Decode attention per query head: softmax(q·Kᵀ/√d_h)·V, with groups of
+ *    query heads sharing one KV head (GQA): same page, section "KV 캐시란".
+ *  - Cumulative importance score
+ *      s_i(t) = s_i(t-1) + (1/|L|) Σ_ℓ (1/H) Σ_h α_{ℓ,h}(t)[i]:
+ *    page "기술 요약: 모든 사고가 HBM 을 필요로 하는 것은 아님"
+ *    (gist.science/ko/paper/2605.09490), section "2. 중요도 점수화".
+ *
+ * Everything is fp64 except the FP8 quantise step, whose scale and x/scale
+ * division are single-precision IEEE operations (the scale is an fp32 value
+ * per (token, KV head)); the code choice is decided in that precision.
+ *
+ * Layout of the oracle's own pool (unrelated to the CUDA library's layout):
+ * values  [num_blocks][n_kv][block_size][d_h]   (fp64, or e4m3 codes)
+ * scales  [num_blocks][n_kv][block_size]        (fp32, FP8 mode only)
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define KVDO_OK 0
+#define KVDO_ERR_INDEX 1   /* a block id or slot outside the pool */
+#define KVDO_ERR_EMPTY 2   /* a head attends to no valid position */
+
+/* ------------------------------------------------------------------ e4m3 */
+
+/* Value of an E4M3 code: sign, 4-bit exponent with bias 7, 3-bit mantissa.
+ * Exponent field 0 holds subnormals m·2^-9; S.1111.111 is NaN and there is
+ * no infinity, so the largest finite magnitude is 1.75·2^8 = 448. */
+double kvdo_e4m3_decode(uint8_t code) {
+    int sign = code >> 7;
+    int e = (code >> 3) & 0xF;
+    int m = code & 0x7;
+    double v;
+    if (e == 0xF && m == 0x7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);
+    else
+        v = ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* Nearest E4M3 code to y: the enumeration of all 127 non-negative finite
+ * codes picks the closest value, a tie goes to the code with an even
+ * mantissa, and magnitudes beyond 448 saturate to 448. */
+uint8_t kvdo_e4m3_encode(float y) {
+    if (isnan(y)) return 0x7F;
+    int neg = signbit(y) ? 1 : 0;
+    double a = fabs((double)y);
+    int best = 0;
+    double best_d = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        double d = fabs(a - kvdo_e4m3_decode((uint8_t)c));
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    if (a > 448.0) best = 0x7E;
+    return (uint8_t)((neg << 7) | best);
+}
+
+void kvdo_e4m3_decode_array(const uint8_t* codes, int64_t n, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = kvdo_e4m3_decode(codes[i]);
+}
+
+void kvdo_e4m3_encode_array(const float* y, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = kvdo_e4m3_encode(y[i]);
+}
+
+/* One (token, KV head) row of d values: scale = absmax/448 in fp32 (1 when
+ * the row is all zero), code_i = e4m3(x_i / scale) with an fp32 division. */
+void kvdo_quantize_row(const float* x, int d, uint8_t* codes, float* scale_out) {
+    float amax = 0.0f;
+    for (int i = 0; i < d; ++i) {
+        float a = fabsf(x[i]);
+        if (a > amax) amax = a;
+    }
+    float scale = (amax == 0.0f) ? 1.0f : amax / 448.0f;
+    for (int i = 0; i < d; ++i) {
+        float y = x[i] / scale;
+        codes[i] = kvdo_e4m3_encode(y);
+    }
+    *scale_out = scale;
+}
+
+void kvdo_quantize_rows(const float* x, int64_t rows, int d, uint8_t* codes, float* scales) {
+    for (int64_t r = 0; r < rows; ++r) kvdo_quantize_row(x + r * d, d, codes + r * d, scales + r);
+}
+
+/* ----------------------------------------------------------- paged cache */
+
+/* Write N new tokens into the pool.  Token n goes to slot slot_mapping[n] =
+ * physical_block·block_size + offset (negative: skipped).  k_new, v_new are
+ * [N][n_kv][d_h].  BF16 mode (fp8 == 0) stores the values; FP8 mode stores
+ * per-(token, head) codes and scales for K and V separately. */
+int kvdo_append(int n_kv, int d_h, int block_size, int64_t num_blocks, int fp8,
+                const float* k_new, const float* v_new, const int64_t* slot_mapping, int64_t N,
+                double* k_pool, double* v_pool,
+                uint8_t* k_codes, uint8_t* v_codes, float* k_scales, float* v_scales) {
+    for (int64_t n = 0; n < N; ++n) {
+        int64_t slot = slot_mapping[n];
+        if (slot < 0) continue;
+        int64_t blk = slot / block_size;
+        int64_t off = slot % block_size;
+        if (blk >= num_blocks) return KVDO_ERR_INDEX;
+        for (int h = 0; h < n_kv; ++h) {
+            const float* ks = k_new + (n * n_kv + h) * d_h;
+            const float* vs = v_new + (n * n_kv + h) * d_h;
+            int64_t row = (blk * n_kv + h) * block_size + off;
+            if (!fp8) {
+                for (int i = 0; i < d_h; ++i) {
+                    k_pool[row * d_h + i] = ks[i];
+                    v_pool[row * d_h + i] = vs[i];
+                }
+            } else {
+                kvdo_quantize_row(ks, d_h, k_codes + row * d_h, k_scales + row);
+                kvdo_quantize_row(vs, d_h, v_codes + row * d_h, v_scales + row);
+            }
+        }
+    }
+    return KVDO_OK;
+}
+
+/* Read back an FP8 pool as values: code value times its row's scale. */
+void kvdo_dequant_pool(const uint8_t* codes, const float* scales, int64_t rows, int d_h, double* out) {
+    for (int64_t r = 0; r < rows; ++r)
+        for (int i = 0; i < d_h; ++i)
+            out[r * d_h + i] = kvdo_e4m3_decode(codes[r * d_h + i]) * (double)scales[r];
+}
+
+/* ------------------------------------------------------ decode attention */
+
+/* One decode step of GQA attention for B requests over the paged pool.
+ *
+ * q          [B][n_q][d_h]
+ * k_pool, v_pool  [num_blocks][n_kv][block_size][d_h] values
+ * block_table [B][max_blocks]: logical block j of request b -> physical block
+ * seq_lens   [B]: attended positions 0 .. seq_lens[b]-1
+ * retain     [num_blocks] or NULL: bit o of retain[p] clear = slot o of block
+ *            p is evicted and takes no part (its logit is -inf)
+ * Query head h reads KV head h / (n_q / n_kv) (consecutive groups).
+ *
+ * Outputs: out [B][n_q][d_h] = Σ_t α_t V_t; lse [B][n_q] = log Σ_t exp(l_t);
+ * alpha (optional) [B][n_q][alpha_stride] = softmax weights per position;
+ * logits (optional) [B][n_q][alpha_stride] = l_t (-inf where evicted).
+ */
+int kvdo_decode(int n_q, int n_kv, int d_h, int block_size, int64_t num_blocks,
+                const double* q, const double* k_pool, const double* v_pool,
+                const int32_t* block_table, int max_blocks, const int32_t* seq_lens, int B,
+                const uint16_t* retain, double softmax_scale,
+                double* out, double* lse, double* alpha, double* logits, int64_t alpha_stride) {
+    int g = n_q / n_kv;
+    int status = KVDO_OK;
+    for (int b = 0; b < B; ++b) {
+        int ctx = seq_lens[b];
+        if (ctx < 0 || ctx > max_blocks * block_size) return KVDO_ERR_INDEX;
+        double* l = (double*)malloc(sizeof(double) * (size_t)(ctx > 0 ? ctx : 1));
+        for (int h = 0; h < n_q; ++h) {
+            int kvh = h / g;
+            const double* qh = q + ((int64_t)b * n_q + h) * d_h;
+            double m = -INFINITY;
+            /* logits through the block table */
+            for (int t = 0; t < ctx; ++t) {
+                int32_t p = block_table[(int64_t)b * max_blocks + t / block_size];
+                int o = t % block_size;
+                if (p < 0 || p >= num_blocks) { free(l); return KVDO_ERR_INDEX; }
+                if (retain && !((retain[p] >> o) & 1u)) { l[t] = -INFINITY; continue; }
+                const double* kt = k_pool + (((int64_t)p * n_kv + kvh) * block_size + o) * d_h;
+                double dot = 0.0;
+                for (int i = 0; i < d_h; ++i) dot += qh[i] * kt[i];
+                l[t] = softmax_scale * dot;
+                if (l[t] > m) m = l[t];
+            }
+            double* oh = out + ((int64_t)b * n_q + h) * d_h;
+            for (int i = 0; i < d_h; ++i) oh[i] = 0.0;
+            if (logits)
+                for (int t = 0; t < ctx; ++t) logits[((int64_t)b * n_q + h) * alpha_stride + t] = l[t];
+            if (m == -INFINITY) {      /* nothing to attend to */
+                lse[(int64_t)b * n_q + h] = -INFINITY;
+                if (alpha)
+                    for (int t = 0; t < ctx; ++t) alpha[((int64_t)b * n_q + h) * alpha_stride + t] = 0.0;
+                status = KVDO_ERR_EMPTY;
+                continue;
+            }
+            /* softmax */
+            double sum = 0.0;
+            for (int t = 0; t < ctx; ++t) sum += exp(l[t] - m);
+            lse[(int64_t)b * n_q + h] = m + log(sum);
+            for (int t = 0; t < ctx; ++t) {
+                double a = exp(l[t] - m) / sum;
+                if (alpha) alpha[((int64_t)b * n_q + h) * alpha_stride + t] = a;
+                if (a == 0.0) continue;
+                int32_t p = block_table[(int64_t)b * max_blocks + t / block_size];
+                int o = t % block_size;
+                const double* vt = v_pool + (((int64_t)p * n_kv + kvh) * block_size + o) * d_h;
+                for (int i = 0; i < d_h; ++i) oh[i] += a * vt[i];
+            }
+        }
+        free(l);
+    }
+    return status;
+}
+
+/* ------------------------------------------------------- importance score */
+
+/* One decode step's update of the cumulative importance score:
+ * s[b][i] += (1/L) Σ_ℓ (1/H) Σ_h alpha[ℓ][b][h][i] for i < seq_lens[b],
+ * with alpha [L][B][H][stride] and s [B][stride]. */
+void kvdo_score_update(const double* alpha, int L, int B, int H, const int32_t* seq_lens,
+                       int64_t stride, double* s) {
+    for (int b = 0; b < B; ++b) {
+        for (int i = 0; i < seq_lens[b]; ++i) {
+            double over_layers = 0.0;
+            for (int ly = 0; ly < L; ++ly) {
+                double over_heads = 0.0;
+                for (int h = 0; h < H; ++h)
+                    over_heads += alpha[(((int64_t)ly * B + b) * H + h) * stride + i];
+                over_layers += over_heads / H;
+            }
+            s[(int64_t)b * stride + i] += over_layers / L;
+        }
+    }
+}

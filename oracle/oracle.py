@@ -1,0 +1,210 @@
+"""ctypes wrapper over the C oracle (``kvd_oracle.c``) — TEST INFRASTRUCTURE.
+
+Every array crossing into C is a contiguous numpy array of the C type.  The
+oracle owns its pool (``OraclePool``) in its own plain layout
+[num_blocks][n_kv][block_size][d_h]; it never reads the CUDA library's pool.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kvd_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "libkvd_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ERR_INDEX = 1
+ERR_EMPTY = 2
+
+
+def lib_path() -> str:
+    return _LIB
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no fast-math, no FMA contraction)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
+               "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+            lib.kvdo_e4m3_decode.restype = f64
+            lib.kvdo_e4m3_decode.argtypes = [ctypes.c_uint8]
+            lib.kvdo_e4m3_encode.restype = ctypes.c_uint8
+            lib.kvdo_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.kvdo_e4m3_decode_array.argtypes = [P, i64, P]
+            lib.kvdo_e4m3_encode_array.argtypes = [P, i64, P]
+            lib.kvdo_quantize_rows.argtypes = [P, i64, i32, P, P]
+            lib.kvdo_append.restype = i32
+            lib.kvdo_append.argtypes = [i32, i32, i32, i64, i32, P, P, P, i64, P, P, P, P, P, P]
+            lib.kvdo_dequant_pool.argtypes = [P, P, i64, i32, P]
+            lib.kvdo_decode.restype = i32
+            lib.kvdo_decode.argtypes = [i32, i32, i32, i32, i64, P, P, P, P, i32, P, i32, P, f64,
+                                        P, P, P, P, i64]
+            lib.kvdo_score_update.argtypes = [P, i32, i32, i32, P, i64, P]
+            _lib = lib
+    return _lib
+
+
+def _c(a, dtype):
+    return np.asarray(a, dtype=dtype, order="C")
+
+
+def _p(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """float64 value of each uint8 E4M3 code."""
+    c = _c(codes, np.uint8)
+    out = np.empty(c.shape, np.float64)
+    _load().kvdo_e4m3_decode_array(_p(c), c.size, _p(out))
+    return out
+
+
+def e4m3_encode(y) -> np.ndarray:
+    """Nearest (ties to even) saturating E4M3 code of each float32 value."""
+    a = _c(y, np.float32)
+    out = np.empty(a.shape, np.uint8)
+    _load().kvdo_e4m3_encode_array(_p(a), a.size, _p(out))
+    return out
+
+
+def quantize_rows(x) -> tuple[np.ndarray, np.ndarray]:
+    """Per-row absmax FP8 quantise of float32 [..., d]: (codes [..., d] uint8, scales [...] float32)."""
+    a = _c(x, np.float32)
+    d = a.shape[-1]
+    rows = a.size // d
+    codes = np.empty(a.shape, np.uint8)
+    scales = np.empty(a.shape[:-1], np.float32)
+    _load().kvdo_quantize_rows(_p(a), rows, d, _p(codes), _p(scales))
+    return codes, scales
+
+
+class OraclePool:
+    """The oracle's own paged pool for one layer: [num_blocks][n_kv][block_size][d_h]."""
+
+    def __init__(self, num_blocks: int, n_kv: int, d_h: int, block_size: int = 16, fp8: bool = False):
+        self.num_blocks, self.n_kv, self.d_h, self.block_size, self.fp8 = num_blocks, n_kv, d_h, block_size, fp8
+        shape = (num_blocks, n_kv, block_size, d_h)
+        if fp8:
+            self.k_codes = np.zeros(shape, np.uint8)
+            self.v_codes = np.zeros(shape, np.uint8)
+            self.k_scales = np.ones(shape[:-1], np.float32)
+            self.v_scales = np.ones(shape[:-1], np.float32)
+            self.k = self.v = None
+        else:
+            self.k = np.zeros(shape, np.float64)
+            self.v = np.zeros(shape, np.float64)
+            self.k_codes = self.v_codes = self.k_scales = self.v_scales = None
+
+    def append(self, k_new, v_new, slot_mapping) -> int:
+        """Write tokens: k_new, v_new float32 [N][n_kv][d_h] (bf16 values), slot_mapping int64 [N]."""
+        k = _c(k_new, np.float32)
+        v = _c(v_new, np.float32)
+        s = _c(slot_mapping, np.int64)
+        return _load().kvdo_append(self.n_kv, self.d_h, self.block_size, self.num_blocks, int(self.fp8),
+                                   _p(k), _p(v), _p(s), s.size,
+                                   _p(self.k), _p(self.v), _p(self.k_codes), _p(self.v_codes),
+                                   _p(self.k_scales), _p(self.v_scales))
+
+    def values(self) -> tuple[np.ndarray, np.ndarray]:
+        """fp64 K and V as read by attention (FP8: code value × row scale)."""
+        if not self.fp8:
+            return self.k, self.v
+        rows = self.num_blocks * self.n_kv * self.block_size
+        kd = np.empty(self.k_codes.shape, np.float64)
+        vd = np.empty(self.v_codes.shape, np.float64)
+        lib = _load()
+        lib.kvdo_dequant_pool(_p(self.k_codes), _p(self.k_scales), rows, self.d_h, _p(kd))
+        lib.kvdo_dequant_pool(_p(self.v_codes), _p(self.v_scales), rows, self.d_h, _p(vd))
+        return kd, vd
+
+
+def decode(pool: OraclePool, q, n_q: int, block_table, seq_lens, retain=None, softmax_scale=None,
+           want_alpha: bool = False, want_logits: bool = False, kv_values=None):
+    """fp64 decode attention.  Returns dict(out [B][n_q][d_h], lse [B][n_q], status[, alpha, logits])."""
+    qd = _c(q, np.float64)
+    B = qd.shape[0]
+    bt = _c(block_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    rt = None if retain is None else _c(np.asarray(retain) & 0xFFFF, np.uint16)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / np.sqrt(pool.d_h)
+    kv, vv = pool.values() if kv_values is None else kv_values
+    kv = _c(kv, np.float64)
+    vv = _c(vv, np.float64)
+    out = np.zeros((B, n_q, pool.d_h), np.float64)
+    lse = np.zeros((B, n_q), np.float64)
+    stride = int(sl.max()) if sl.size else 0
+    alpha = np.zeros((B, n_q, stride), np.float64) if want_alpha else None
+    logits = np.full((B, n_q, stride), -np.inf, np.float64) if want_logits else None
+    st = _load().kvdo_decode(n_q, pool.n_kv, pool.d_h, pool.block_size, pool.num_blocks,
+                             _p(qd), _p(kv), _p(vv), _p(bt), bt.shape[1], _p(sl), B, _p(rt),
+                             float(softmax_scale), _p(out), _p(lse), _p(alpha), _p(logits), stride)
+    res = {"out": out, "lse": lse, "status": st}
+    if want_alpha:
+        res["alpha"] = alpha
+    if want_logits:
+        res["logits"] = logits
+    return res
+
+
+def score_update(s, alpha_layers, seq_lens) -> np.ndarray:
+    """One step of s_i += (1/L) Σ_ℓ (1/H) Σ_h α; alpha_layers [L][B][H][stride], s [B][stride] (updated copy)."""
+    a = _c(alpha_layers, np.float64)
+    L, B, H, stride = a.shape
+    out = _c(s, np.float64).copy()
+    assert out.shape == (B, stride)
+    sl = _c(seq_lens, np.int32)
+    _load().kvdo_score_update(_p(a), L, B, H, _p(sl), stride, _p(out))
+    return out
+
+
+def decode_dense_inputs(k_logical, v_logical, q, seq_lens, n_q, evicted=None, fp8=False, softmax_scale=None):
+    """Run the oracle on logical (unpaged) K/V by paging them into an identity-ordered pool.
+
+    k_logical, v_logical: list over requests of float32 [ctx_b][n_kv][d_h] (bf16 values);
+    evicted: optional list over requests of position arrays.  Used for sampled checks of
+    large workloads, where only the sampled requests are regenerated on the host.
+    """
+    bs = 16
+    n_kv, d_h = k_logical[0].shape[1], k_logical[0].shape[2]
+    nblk = [-(-int(c) // bs) for c in seq_lens]
+    nb = sum(nblk)
+    bt = np.full((len(seq_lens), max(nblk)), -1, np.int32)
+    pool = OraclePool(nb, n_kv, d_h, bs, fp8)
+    off = 0
+    retain = None
+    if evicted is not None:
+        retain = np.full(nb, 0xFFFF, np.int64)
+    for b, c in enumerate(seq_lens):
+        bt[b, :nblk[b]] = np.arange(off, off + nblk[b])
+        slots = np.arange(c, dtype=np.int64) + off * bs
+        pool.append(k_logical[b], v_logical[b], slots)
+        if evicted is not None:
+            for pos in np.asarray(evicted[b]).tolist():
+                retain[off + pos // bs] &= ~(1 << (pos % bs))
+        off += nblk[b]
+    return decode(pool, q, n_q, bt, seq_lens, retain, softmax_scale, want_alpha=True, want_logits=True)

@@ -1,0 +1,359 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: values the
+pages print (tests/golden), library routines (torch's float8_e4m3fn cast,
+scaled_dot_product_attention, scipy's logsumexp), closed forms and invariants.
+"""
+
+import os
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import logsumexp
+
+import oracle
+from kvd_inputs import gen
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _bf16(x):
+    """float32 values rounded to bf16 and widened back (inputs are bf16 tensors)."""
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16).float().numpy()
+
+
+# ------------------------------------------------------------------ e4m3 codec
+
+def test_e4m3_page_vectors():
+    for line in open(os.path.join(GOLDEN, "e4m3_page_vectors.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        kind, x, y = line.split()
+        x, y = float(x), float(y)
+        if kind in ("round", "max"):
+            assert oracle.e4m3_decode(oracle.e4m3_encode(np.float32(x))) == y
+        elif kind == "spacing":
+            c = int(oracle.e4m3_encode(np.float32(x)))
+            assert oracle.e4m3_decode(np.uint8(c + 1)) - oracle.e4m3_decode(np.uint8(c)) == y
+    # nothing above the largest finite value
+    assert oracle.e4m3_decode(np.uint8(0x7E)) == 448.0
+    assert np.isnan(oracle.e4m3_decode(np.uint8(0x7F)))
+
+
+def test_e4m3_decode_all_codes_match_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ours[ok], ref[ok])
+    assert np.array_equal(np.signbit(ours[ok]), np.signbit(ref[ok]))
+
+
+def test_e4m3_decode_format_closed_forms():
+    d = oracle.e4m3_decode(np.arange(127, dtype=np.uint8))
+    assert np.all(np.diff(d) > 0)                 # monotone over non-negative codes
+    assert d[1] == 2.0 ** -9                      # smallest subnormal m·2^-9
+    assert d[8] == 2.0 ** -6                      # smallest normal 2^(1-7)
+    assert d[0x38] == 1.0                         # exponent field 7 = bias
+    assert d[0x7E] == 448.0
+
+
+def _e4m3_test_values():
+    r = _rng(1)
+    mag = np.exp2(r.uniform(-12, 10, 200000)).astype(np.float32)
+    sgn = np.where(r.random(mag.size) < 0.5, -1, 1).astype(np.float32)
+    vals = [mag * sgn]
+    # exact midpoints between neighbouring codes (ties) and the codes themselves
+    d = oracle.e4m3_decode(np.arange(127, dtype=np.uint8))
+    mids = ((d[1:] + d[:-1]) / 2).astype(np.float32)
+    vals += [mids, -mids, d.astype(np.float32), np.array([0.0, -0.0, 448, 449, 464, 465, 1e6, -1e6,
+                                                           np.inf, -np.inf], np.float32)]
+    return np.concatenate(vals)
+
+
+def test_e4m3_encode_matches_torch_cast():
+    y = _e4m3_test_values()
+    ours = oracle.e4m3_encode(y)
+    ref = torch.from_numpy(np.clip(y, -448, 448)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+
+
+def test_e4m3_encode_is_nearest_within_half_spacing():
+    y = _e4m3_test_values()
+    y = y[np.isfinite(y) & (np.abs(y) <= 448)]
+    back = oracle.e4m3_decode(oracle.e4m3_encode(y))
+    a = np.abs(y.astype(np.float64))
+    # spacing of e4m3 around a: 2^-9 below 2^-6, else 2^(floor(log2 a) - 3)
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -6)))
+    spacing = np.exp2(e - 3)
+    assert np.all(np.abs(back - y) <= spacing / 2)
+
+
+def test_quantize_rows_properties():
+    r = _rng(2)
+    x = _bf16(r.standard_normal((400, 128)).astype(np.float32) * np.exp2(r.uniform(-8, 8, (400, 1))))
+    x[3] = 0.0
+    codes, scales = oracle.quantize_rows(x)
+    assert scales[3] == 1.0 and not codes[3].any()
+    amax = np.abs(x).max(axis=1)
+    nz = amax > 0
+    # scale is the fp32 value nearest absmax/448, so absmax/scale lands on the largest code
+    assert np.allclose(scales[nz], amax[nz] / 448.0, rtol=2 ** -23, atol=0)
+    rows_max = np.abs(oracle.e4m3_decode(codes)).max(axis=1)
+    assert np.all(rows_max[nz] == 448.0)
+    # read-back error within half an e4m3 spacing of x/scale, times the scale
+    back = oracle.e4m3_decode(codes) * scales[:, None].astype(np.float64)
+    y = np.abs(x / scales[:, None])
+    e = np.floor(np.log2(np.maximum(y, 2.0 ** -6)))
+    bound = np.exp2(e - 3) / 2 * scales[:, None] * (1 + 2 ** -20)
+    assert np.all(np.abs(back - x) <= bound + 1e-300)
+    # the code step itself is torch's float8 cast of the fp32 quotient
+    qt = (torch.from_numpy(x) / torch.from_numpy(scales)[:, None]).clamp(-448, 448)
+    assert np.array_equal(codes, qt.to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+
+
+# ------------------------------------------------------------ paged attention
+
+def _dense_sdpa(q, k, v, scale, keep=None):
+    """torch fp64 scaled_dot_product_attention over one request's logical K/V.
+
+    q [n_q][d], k/v [ctx][n_kv][d]; query heads map to KV heads in consecutive groups."""
+    n_q, n_kv = q.shape[0], k.shape[1]
+    g = n_q // n_kv
+    qt = torch.from_numpy(np.asarray(q, np.float64))[None, :, None, :]          # [1, n_q, 1, d]
+    kt = torch.from_numpy(np.asarray(k, np.float64)).permute(1, 0, 2).repeat_interleave(g, 0)[None]
+    vt = torch.from_numpy(np.asarray(v, np.float64)).permute(1, 0, 2).repeat_interleave(g, 0)[None]
+    mask = None
+    if keep is not None:
+        mask = torch.from_numpy(np.asarray(keep, bool))[None, None, None, :].expand(1, n_q, 1, -1)
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=scale)
+    return o[0, :, 0, :].numpy()
+
+
+def _page_example():
+    tables = {}
+    for line in open(os.path.join(GOLDEN, "block_table_example.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        name, rest = line.split(":")
+        pairs = [tuple(map(int, p.split("->"))) for p in rest.split()]
+        assert [j for j, _ in pairs] == list(range(len(pairs)))
+        tables[name] = [p for _, p in pairs]
+    return tables
+
+
+def _make_requests(seed, lens, n_kv, d_h, n_q):
+    r = _rng(seed)
+    ks = [_bf16(r.standard_normal((c, n_kv, d_h))) for c in lens]
+    vs = [_bf16(r.standard_normal((c, n_kv, d_h))) for c in lens]
+    q = _bf16(r.standard_normal((len(lens), n_q, d_h)))
+    return q, ks, vs
+
+
+def _paged(tables, lens, ks, vs, num_blocks, n_kv, d_h, fp8=False):
+    pool = oracle.OraclePool(num_blocks, n_kv, d_h, 16, fp8)
+    bt = np.full((len(tables), max(len(t) for t in tables)), -1, np.int32)
+    for b, t in enumerate(tables):
+        bt[b, :len(t)] = t
+        pos = np.arange(lens[b])
+        slots = np.asarray(t, np.int64)[pos // 16] * 16 + pos % 16
+        assert pool.append(ks[b], vs[b], slots) == 0
+    return pool, bt
+
+
+def test_page_block_table_example_matches_dense_attention():
+    tabs = _page_example()
+    tables = [tabs["A"], tabs["B"], tabs["C"]]
+    lens = [20, 90, 33]                       # last blocks partly filled
+    n_q, n_kv, d_h = 8, 2, 32
+    q, ks, vs = _make_requests(3, lens, n_kv, d_h, n_q)
+    pool, bt = _paged(tables, lens, ks, vs, 11, n_kv, d_h)
+    scale = 1 / np.sqrt(d_h)
+    res = oracle.decode(pool, q, n_q, bt, lens, softmax_scale=scale, want_alpha=True)
+    assert res["status"] == 0
+    for b in range(3):
+        ref = _dense_sdpa(q[b], ks[b], vs[b], scale)
+        np.testing.assert_allclose(res["out"][b], ref, rtol=1e-12, atol=1e-13)
+        assert np.allclose(res["alpha"][b, :, :lens[b]].sum(-1), 1.0, atol=1e-13)
+
+
+def test_lse_matches_logsumexp_and_alpha_is_softmax():
+    lens = [37, 64, 1]
+    n_q, n_kv, d_h = 4, 4, 16
+    q, ks, vs = _make_requests(4, lens, n_kv, d_h, n_q)
+    tables = [[0, 1, 2], [3, 4, 5, 6], [7]]
+    pool, bt = _paged(tables, lens, ks, vs, 8, n_kv, d_h)
+    res = oracle.decode(pool, q, n_q, bt, lens, want_alpha=True, want_logits=True)
+    for b, c in enumerate(lens):
+        lg = np.einsum("hd,thd->ht", q[b].astype(np.float64), ks[b].astype(np.float64)) / np.sqrt(d_h)
+        np.testing.assert_allclose(res["logits"][b, :, :c], lg, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(res["lse"][b], logsumexp(lg, axis=-1), rtol=1e-13)
+        np.testing.assert_allclose(res["alpha"][b, :, :c],
+                                   torch.softmax(torch.from_numpy(lg), -1).numpy(), rtol=1e-12, atol=1e-15)
+
+
+def test_permuting_physical_blocks_is_bitwise_invariant():
+    lens = [100, 250]
+    n_q, n_kv, d_h = 8, 2, 64
+    q, ks, vs = _make_requests(5, lens, n_kv, d_h, n_q)
+    nblk = [7, 16]
+    nb = 40
+    base = [list(range(0, 7)), list(range(7, 23))]
+    pool, bt = _paged(base, lens, ks, vs, nb, n_kv, d_h)
+    ref = oracle.decode(pool, q, n_q, bt, lens)
+    for seed in range(3):
+        perm = gen.permutation(gen.stream_key(seed, "relabel"), nb).numpy()
+        tables = [[int(perm[p]) for p in t] for t in base]
+        pool2, bt2 = _paged(tables, lens, ks, vs, nb, n_kv, d_h)
+        res = oracle.decode(pool2, q, n_q, bt2, lens)
+        assert np.array_equal(res["out"], ref["out"]) and np.array_equal(res["lse"], ref["lse"])
+    assert sum(nblk) == 23
+
+
+def test_shared_blocks_serve_two_requests():
+    # request 1 reuses request 0's first three physical blocks (a shared prefix)
+    n_q, n_kv, d_h = 4, 1, 32
+    r = _rng(6)
+    prefix_k = _bf16(r.standard_normal((48, n_kv, d_h)))
+    prefix_v = _bf16(r.standard_normal((48, n_kv, d_h)))
+    tail = [_bf16(r.standard_normal((10, n_kv, d_h))) for _ in range(4)]
+    ks = [np.concatenate([prefix_k, tail[0]]), np.concatenate([prefix_k, tail[1]])]
+    vs = [np.concatenate([prefix_v, tail[2]]), np.concatenate([prefix_v, tail[3]])]
+    q = _bf16(r.standard_normal((2, n_q, d_h)))
+    pool = oracle.OraclePool(6, n_kv, d_h)
+    pos = np.arange(58)
+    pool.append(ks[0], vs[0], np.array([2, 0, 4, 5])[pos // 16] * 16 + pos % 16)
+    pool.append(tail[1], tail[3], 1 * 16 + np.arange(10))
+    bt = np.array([[2, 0, 4, 5], [2, 0, 4, 1]], np.int32)
+    res = oracle.decode(pool, q, n_q, bt, [58, 58])
+    for b in range(2):
+        np.testing.assert_allclose(res["out"][b], _dense_sdpa(q[b], ks[b], vs[b], 1 / np.sqrt(d_h)),
+                                   rtol=1e-12, atol=1e-13)
+
+
+def test_identical_keys_give_mean_of_values():
+    n_q, n_kv, d_h, c = 4, 2, 16, 45
+    r = _rng(7)
+    k1 = _bf16(r.standard_normal((1, n_kv, d_h)))
+    ks = [np.repeat(k1, c, axis=0)]
+    vs = [_bf16(r.standard_normal((c, n_kv, d_h)))]
+    q = _bf16(r.standard_normal((1, n_q, d_h)))
+    pool, bt = _paged([[3, 1, 0]], [c], ks, vs, 4, n_kv, d_h)
+    res = oracle.decode(pool, q, n_q, bt, [c])
+    for h in range(n_q):
+        np.testing.assert_allclose(res["out"][0, h], vs[0][:, h // 2].astype(np.float64).mean(0), rtol=1e-12,
+                                   atol=1e-14)
+
+
+def test_one_dominant_logit_selects_its_value():
+    n_q, n_kv, d_h, c = 2, 1, 16, 40
+    r = _rng(8)
+    ks = [np.zeros((c, n_kv, d_h), np.float32)]
+    ks[0][17, 0, :] = 64.0                    # q·k = 64·64·d/√d  ≫ every other logit (0)
+    vs = [_bf16(r.standard_normal((c, n_kv, d_h)))]
+    q = np.full((1, n_q, d_h), 64.0, np.float32)
+    pool, bt = _paged([[0, 1, 2]], [c], ks, vs, 3, n_kv, d_h)
+    res = oracle.decode(pool, q, n_q, bt, [c])
+    for h in range(n_q):
+        assert np.array_equal(res["out"][0, h], vs[0][17, 0].astype(np.float64))
+
+
+def test_masked_attention_equals_compacted_table():
+    """Only evicted slots change the result: masking them equals dropping them (offloading Prop. 1)."""
+    n_q, n_kv, d_h, c = 4, 2, 32, 150
+    q, ks, vs = _make_requests(9, [c], n_kv, d_h, n_q)
+    evict = np.array([5, 17, 18, 40, 41, 42, 99, 130])
+    keep = np.setdiff1d(np.arange(c), evict)
+    tables = [list(range(10))]
+    pool, bt = _paged(tables, [c], ks, vs, 10, n_kv, d_h)
+    retain = np.full(10, 0xFFFF, np.int64)
+    for p in evict:
+        retain[p // 16] &= ~(1 << (p % 16))
+    res = oracle.decode(pool, q, n_q, bt, [c], retain=retain, want_alpha=True)
+    assert np.all(res["alpha"][0][:, evict] == 0)
+    ck = [ks[0][keep]]
+    cv = [vs[0][keep]]
+    pool2, bt2 = _paged([list(range(9))], [keep.size], ck, cv, 9, n_kv, d_h)
+    res2 = oracle.decode(pool2, q, n_q, bt2, [keep.size])
+    assert np.array_equal(res["out"], res2["out"])
+    assert np.array_equal(res["lse"], res2["lse"])
+    np.testing.assert_allclose(res["out"][0], _dense_sdpa(q[0], ks[0], vs[0], 1 / np.sqrt(d_h),
+                                                          keep=np.isin(np.arange(c), keep)), rtol=1e-12, atol=1e-13)
+
+
+def test_fp8_pool_reads_back_dequantised_values():
+    lens = [70, 33]
+    n_q, n_kv, d_h = 8, 2, 64
+    q, ks, vs = _make_requests(10, lens, n_kv, d_h, n_q)
+    ks[0][:, 1, 5] *= 20.0                     # an outlier channel
+    tables = [[4, 0, 2, 6, 1], [3, 5, 7]]
+    pool, bt = _paged(tables, lens, ks, vs, 8, n_kv, d_h, fp8=True)
+    res = oracle.decode(pool, q, n_q, bt, lens)
+    for b, c in enumerate(lens):
+        # dequantise through torch's float8 type: value(code) × per-(token, head) scale
+        kc, kscale = oracle.quantize_rows(ks[b])
+        vc, vscale = oracle.quantize_rows(vs[b])
+        kd = torch.from_numpy(kc).view(torch.float8_e4m3fn).double().numpy() * kscale[..., None]
+        vd = torch.from_numpy(vc).view(torch.float8_e4m3fn).double().numpy() * vscale[..., None]
+        np.testing.assert_allclose(res["out"][b], _dense_sdpa(q[b], kd, vd, 1 / np.sqrt(d_h)), rtol=1e-12,
+                                   atol=1e-13)
+        # and stays within FP8 rounding of the unquantised attention
+        np.testing.assert_allclose(res["out"][b], _dense_sdpa(q[b], ks[b], vs[b], 1 / np.sqrt(d_h)), atol=0.1)
+
+
+def test_bad_block_id_and_empty_attention_are_reported():
+    n_q, n_kv, d_h = 2, 1, 16
+    q, ks, vs = _make_requests(11, [20], n_kv, d_h, n_q)
+    pool, bt = _paged([[0, 1]], [20], ks, vs, 2, n_kv, d_h)
+    bad = bt.copy()
+    bad[0, 1] = 7
+    assert oracle.decode(pool, q, n_q, bad, [20])["status"] == oracle.oracle.ERR_INDEX
+    res = oracle.decode(pool, q, n_q, bt, [20], retain=np.array([0, 0]))
+    assert res["status"] == oracle.oracle.ERR_EMPTY
+    assert np.all(res["out"] == 0) and np.all(np.isneginf(res["lse"]))
+
+
+# ------------------------------------------------------------- score update
+
+def test_score_update_closed_forms():
+    L, B, H, S = 3, 2, 4, 12
+    seq = np.array([12, 9], np.int32)
+    # one-hot alphas: layer l, head h puts all weight on position l·H + h
+    a = np.zeros((L, B, H, S))
+    for ly in range(L):
+        for h in range(H):
+            for b in range(B):
+                a[ly, b, h, (ly * H + h) % seq[b]] = 1.0
+    s = oracle.score_update(np.zeros((B, S)), a, seq)
+    np.testing.assert_allclose(s[0], np.full(12, 1.0 / (L * H)), rtol=1e-15)
+    assert np.isclose(s[1].sum(), 1.0, rtol=1e-15)
+    assert np.all(s[1, 9:] == 0)               # positions beyond the context are untouched
+
+
+def test_score_sum_grows_by_one_per_step_and_single_head_is_softmax():
+    n_q, n_kv, d_h = 4, 2, 32
+    lens = [50, 77]
+    s = np.zeros((2, 80))
+    L = 2
+    for step in range(3):
+        alphas = []
+        for ly in range(L):
+            q, ks, vs = _make_requests(100 + 10 * step + ly, lens, n_kv, d_h, n_q)
+            res = oracle.decode_dense_inputs(ks, vs, q, lens, n_q)
+            a = np.zeros((2, n_q, 80))
+            a[:, :, :res["alpha"].shape[2]] = res["alpha"]
+            alphas.append(a)
+        s = oracle.score_update(s, np.stack(alphas), lens)
+        np.testing.assert_allclose(s.sum(axis=1), step + 1, rtol=1e-13)
+    # L = 1, H = 1: the update is the softmax itself
+    q, ks, vs = _make_requests(200, [30], 1, 16, 1)
+    res = oracle.decode_dense_inputs(ks, vs, q, [30], 1)
+    s1 = oracle.score_update(np.zeros((1, 30)), res["alpha"][None], [30])
+    lg = (q[0, 0].astype(np.float64) @ ks[0][:, 0].astype(np.float64).T) / 4.0
+    np.testing.assert_allclose(s1[0], torch.softmax(torch.from_numpy(lg), 0).numpy(), rtol=1e-12)
