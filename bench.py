@@ -1,0 +1,423 @@
+"""Benchmark: paged GQA decode attention steps on GB300 through the C ABI.
+
+One step = one decode step of every layer of the workload: per layer, append the
+new token's K/V of every request (kvd_append_kv), then paged decode attention with
+split-KV and the log-sum-exp combine (kvd_decode_attn).  Layers run in order, as in
+a model where layer ℓ+1's query depends on layer ℓ.  The L-layer step is captured
+once as a CUDA graph and replayed.
+
+Prints one JSON line.  `value` is the closed-form K/V bytes attended per step,
+2·L·n_kv·d_h·w_kv per token (FP8 scales excluded), divided by the step time, in GB/s,
+with every input resident in HBM.  Default workload: Llama-3.1-8B shape, 32 layers,
+batch 32, context 8,192, BF16 KV (34.4 GB of KV per step, far larger than L2).
+
+`--impl reference` times the fp64 CPU oracle instead, on a bounded sample.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn KV HBM GB/s and % of GB300 HBM peak; attention steps/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------- analytic
+def kv_bytes_per_token(L: int, n_kv: int, d_h: int, w_kv: float) -> float:
+    """2·L·n_kv·d_h·w_kv: K and V of every layer and KV head."""
+    return 2 * L * n_kv * d_h * w_kv
+
+
+def traffic_crossover_tokens(params: float, w_p: float, batch: int, per_token: float) -> float:
+    """Context s* where per-step KV bytes b·s·per_token equal the weight bytes P·w_p."""
+    return params * w_p / (batch * per_token)
+
+
+def kv_speedup(weight_bytes: float, kv_bytes: float, c: float) -> float:
+    """Memory-bound step-time ratio when the KV bytes shrink by c: (W + KV) / (W + KV/c)."""
+    return (weight_bytes + kv_bytes) / (weight_bytes + kv_bytes / c)
+
+
+def decode_intensity(g: int, w_kv: float) -> float:
+    """Long-context FLOP per KV byte of GQA decode: 2 FLOP per (q, k) and (p, v) element, g heads."""
+    return 2 * g / w_kv
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+# ------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            import tempfile
+
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.gpu)], stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self) -> dict:
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for ln in open(self.path):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower() == "active"})
+        pw = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "samples": len(rows), "reasons": reasons}
+
+
+# --------------------------------------------------------------- dist setup
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ the GPU arm
+class Step:
+    """Device-resident state of one workload and its L-layer decode step."""
+
+    def __init__(self, w, dev, num_splits: int = 0):
+        import torch
+
+        import paged_gqa_decode_kvd_gb300 as kvd
+
+        self.w, self.dev, self.kvd = w, dev, kvd
+        self.L = w.L
+        self.fp8 = w.kv_dtype != "bf16"
+        self.pool = kvd.KVPool(w.L, w.n_kv, w.num_blocks(), kvd.KVD_FP8_E4M3 if self.fp8 else kvd.KVD_BF16,
+                               device=dev)
+        bt = w.block_table()
+        self.bt_cpu = bt
+        self.bt = bt.to(dev)
+        lens = w.seq_lens(0)
+        self.lens = lens
+        self.max_len = max(lens)
+        self.seq = torch.tensor(lens, dtype=torch.int32, device=dev)
+        ret = w.retain_mask(bt)
+        self.retain = None
+        if ret is not None:
+            import numpy as np
+
+            self.retain = torch.from_numpy(ret.numpy().astype(np.uint16).view(np.int16)).to(dev)
+        # prefill every layer's cache through the append entry point (setup, untimed)
+        for layer in range(w.L):
+            for b in range(w.batch):
+                n = lens[b] - 1
+                if n > 0:
+                    k, v = w.kv(layer, b, 0, n, dev)
+                    kvd.kvd_append_kv(self.pool.handle, layer, k.contiguous(), v.contiguous(),
+                                      w.slot_mapping(b, 0, n, bt).to(dev))
+        # per-step inputs: the new token of every request (position len-1) and q, for every layer
+        pos = w.append_pos(0)
+        self.slots = torch.cat([w.slot_mapping(b, pos[b], pos[b] + 1, bt) for b in range(w.batch)]).to(dev)
+        kn, vn = [], []
+        for layer in range(w.L):
+            ks, vs = zip(*[w.kv(layer, b, pos[b], pos[b] + 1, dev) for b in range(w.batch)])
+            kn.append(torch.cat(ks))
+            vn.append(torch.cat(vs))
+        self.k_new = torch.stack(kn).contiguous()          # [L][B][n_kv][128]
+        self.v_new = torch.stack(vn).contiguous()
+        self.q = torch.stack([w.q(layer, 0, dev) for layer in range(w.L)]).contiguous()   # [L][B][n_q][128]
+        self.out = torch.empty(w.L, w.batch, w.n_q, 128, dtype=torch.bfloat16, device=dev)
+        self.splits, nbytes = kvd.kvd_decode_workspace_bytes(self.pool.handle, w.n_q, w.batch, self.max_len,
+                                                             num_splits)
+        self.num_splits = self.splits
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.launches_per_step = 3 * w.L
+        torch.cuda.synchronize()
+        err = kvd.kvd_get_device_error(self.pool.handle)
+        if err:
+            raise RuntimeError(f"device error during setup: {kvd.status_string(err)}")
+
+    def run(self, stream=None):
+        kvd = self.kvd
+        for layer in range(self.L):
+            kvd.kvd_append_kv(self.pool.handle, layer, self.k_new[layer], self.v_new[layer], self.slots, stream)
+            kvd.kvd_decode_attn(self.pool.handle, layer, self.q[layer], self.bt, self.seq, self.max_len, self.ws,
+                                self.out[layer], num_splits=self.num_splits, retain_mask=self.retain, stream=stream)
+
+    def decode_only(self, layer, stream=None):
+        self.kvd.kvd_decode_attn(self.pool.handle, layer, self.q[layer], self.bt, self.seq, self.max_len, self.ws,
+                                 None, num_splits=self.num_splits, retain_mask=self.retain, stream=stream)
+
+    def capture(self):
+        import torch
+
+        s = torch.cuda.Stream(device=self.dev)
+        s.wait_stream(torch.cuda.current_stream(self.dev))
+        with torch.cuda.stream(s):
+            self.run()
+        torch.cuda.current_stream(self.dev).wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run()
+        torch.cuda.synchronize()
+        return g
+
+
+def gpu_arm(args, w, rank, world, local):
+    import torch
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks = measured_peaks()
+    st = Step(w, dev, args.num_splits)
+    kv_bytes = w.kv_bytes_per_step()
+    graph = st.capture()
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        barrier(world)
+        t0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ms = t0.elapsed_time(t1)
+    ms_max = max_over_ranks(ms, world)
+    ms_per_step = ms_max / args.steps
+    value = kv_bytes * world / (ms_per_step * 1e-3) / 1e9
+    err = st.kvd.kvd_get_device_error(st.pool.handle)
+    if err:
+        raise RuntimeError(f"device error after timed steps: {st.kvd.status_string(err)}")
+
+    # per-launch time of the decode kernel alone (partials only, no combine), same stream
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(st.L)]
+    durs = []
+    for rep in range(max(1, min(args.steps, 3))):
+        for layer in range(st.L):
+            ev[layer][0].record(stream)
+            st.decode_only(layer)
+            ev[layer][1].record(stream)
+        torch.cuda.synchronize()
+        durs += [a.elapsed_time(b) for a, b in ev]
+    dec_ms = statistics.mean(durs)
+    layer_bytes = kv_bytes / w.L
+    achieved = layer_bytes / (dec_ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": args.traffic,
+            "kernel": "kvd::decode_kernel", "peak_source": peaks["source"] + " (copy, MEASURED_PEAKS.json hbm_gbs)",
+            "bytes_per_launch": layer_bytes, "launch_ms": round(dec_ms, 5)}
+
+    # end to end: per-step inputs from pinned host memory, outputs back to pinned host memory
+    h_q = st.q.cpu().pin_memory()
+    h_k = st.k_new.cpu().pin_memory()
+    h_v = st.v_new.cpu().pin_memory()
+    h_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    e2e_steps = max(1, min(args.steps, 10))
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        st.q.copy_(h_q, non_blocking=True)
+        st.k_new.copy_(h_k, non_blocking=True)
+        st.v_new.copy_(h_v, non_blocking=True)
+        graph.replay()
+        h_out.copy_(st.out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
+    h2d = (h_q.numel() * h_q.element_size() + h_k.numel() * h_k.element_size() + h_v.numel() * h_v.element_size())
+    d2h = h_out.numel() * h_out.element_size()
+    e2e = {"value": round(kv_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8_e4m3",
+        "data": "synthetic (seeded counter-hash generator)",
+        "config": {"workload": f"{w.name}: {w.description}", "layers": w.L, "batch": w.batch, "n_q": w.n_q,
+                   "n_kv": w.n_kv, "d_h": w.d_h, "context": w.seq_lens(0)[:4] if w.batch > 4 else w.seq_lens(0),
+                   "kv_bytes_per_step": kv_bytes, "num_splits": st.splits, "seed": w.seed,
+                   "l2": "inputs larger than L2 (KV pool streamed every step)", "parallelism": f"replicas x{world}"},
+        "steps_per_s": round(1e3 / ms_per_step, 2),
+        "hbm_frac_of_measured": round(value / world / peaks["hbm_gbs"], 4),
+        "hbm_frac_of_datasheet_8tbs": round(value / world / 8000.0, 4),
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": st.launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+    return line
+
+
+# ------------------------------------------------------------------ the CPU oracle arm
+def cpu_baseline(w, budget_s: float = 15.0) -> dict:
+    """Time the fp64 oracle (as it stands, one thread) on a bounded sample of the workload.
+
+    The sample is one (layer 0, request 0) unit of the workload — append of its context
+    into the oracle's pool, then decode of all its query heads — repeated until
+    `budget_s` seconds of oracle time are spent; the rate is scaled by KV bytes."""
+    import numpy as np
+
+    import oracle
+
+    oracle.build()
+    n = w.seq_lens(0)[0]
+    k, v = w.kv(0, 0, 0, n)
+    kf, vf = k.float().numpy(), v.float().numpy()
+    q = w.q(0, 0)[0:1].float().numpy()
+    nblk = -(-n // 16)
+    pos = np.arange(n)
+    slots = (pos // 16) * 16 + pos % 16
+    table = np.arange(nblk, dtype=np.int32)[None, :]
+    t_used, units = 0.0, 0
+    while t_used < budget_s or units == 0:
+        t0 = time.perf_counter()
+        pool = oracle.OraclePool(nblk, w.n_kv, w.d_h, 16, w.kv_dtype != "bf16")
+        pool.append(kf, vf, slots)
+        oracle.decode(pool, q, w.n_q, table, [n])
+        t_used += time.perf_counter() - t0
+        units += 1
+    bytes_done = kv_bytes_per_token(1, w.n_kv, w.d_h, w.w_kv) * n * units
+    gbs = bytes_done / t_used / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{units} x one (layer, request) unit of {w.name}: {n} tokens, {w.n_q} query heads "
+                      f"(append + decode, fp64, one thread), {t_used:.1f} s, scaled by KV bytes",
+            "steps_per_s": round(gbs * 1e9 / w.kv_bytes_per_step(), 6)}
+
+
+def reference_arm(args, w, rank, world):
+    if rank != 0:
+        return None
+    budget = max(2.0, args.cpu_budget / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_baseline(w, budget_s=budget)
+    vals = [cpu_baseline(w, budget_s=budget) for _ in range(args.steps)]
+    gbs = statistics.mean(v["value"] for v in vals)
+    ms = w.kv_bytes_per_step() / (gbs * 1e9) * 1e3
+    return {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded counter-hash generator)",
+            "config": {"workload": f"{w.name}: {w.description}", "layers": w.L, "batch": w.batch,
+                       "kv_bytes_per_step": w.kv_bytes_per_step(), "seed": w.seed},
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": vals[0]["sample"]},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="llama8b")
+    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram bytes read+write per decode launch from an ncu capture of the current kernel")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    from kvd_inputs import get
+
+    rank, world, local = dist_env()
+    w = get(args.workload, args.seed)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if args.impl == "gb300" else "gloo")
+    if args.impl == "reference":
+        line = reference_arm(args, w, rank, world)
+    else:
+        line = gpu_arm(args, w, rank, world, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

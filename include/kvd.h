@@ -1,0 +1,191 @@
+/*
+ * kvd.h — C ABI of the paged GQA decode-attention library for GB300 (sm_103a).
+ *
+ * One decode step of grouped-query attention over a paged KV cache: every
+ * request holds its keys and values in fixed 16-token blocks reached through
+ * a per-request block table, the new token's K/V is appended first, and each
+ * query head attends softmax(q·Kᵀ/√d_h)·V over the request's context.  Groups
+ * of g = n_q / n_kv query heads share one KV head.
+ *   Paged blocks, block table, append-then-attend and FP8 storage: page
+ *   "LLM에서 KV 캐시는 얼마나 생길까" (froggydisk.github.io/kv-cache-per-request),
+ *   sections "KV 캐시란" (q/k/v heads, √128 scaling, prefill/decode append)
+ *   and "KV 캐시를 줄이는 기법" (16-token blocks, block tables, FP8 E4M3).
+ *   Bytes per token 2·L·n_kv·d_h·w_kv: page "The KV Cache Is the New Memory
+ *   Wall" (jaehun.me/posts/paper-2609-30854v1), background (paper §2.1, Tab. 1).
+ *   Importance score s_i: page "기술 요약: 모든 사고가 HBM 을 필요로 하는 것은
+ *   아님" (gist.science/ko/paper/2605.09490), section "2. 중요도 점수화".
+ *
+ * Conventions for every entry point
+ *  - Device pointers are caller-owned CUDA device memory; the library never
+ *    frees them.  The library itself allocates only the pool handle (host)
+ *    and a 4-byte device error word inside kvd_pool_create.
+ *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *    stream.  Calls are asynchronous: the return status covers argument
+ *    validation and kernel launch only.
+ *  - Kernels never trap.  A problem found on the device (a block id outside
+ *    the pool, a sequence length outside [1, max_blocks_per_seq·16], a bounded
+ *    wait that ran out) records the first error code in the pool's error word;
+ *    the affected work item is treated as empty.  Read it with
+ *    kvd_get_device_error.
+ *  - Supported set: d_h = 128, block_size = 16, 1 ≤ g ≤ 8, batch ≤ 2048.
+ *    Anything else valid returns KVD_ERR_UNSUPPORTED before any launch.
+ *
+ * Pool layout (per layer ℓ, physical block p, KV head h)
+ *  - One record of 2·16·128 elements: the K tile, then the V tile, at byte
+ *    offset ((ℓ·num_blocks + p)·n_kv + h)·record_bytes, record_bytes = 8192
+ *    (BF16) or 4096 (FP8).  A tile holds token t ∈ [0,16) (slot offset within
+ *    the block) × dim d ∈ [0,128), permuted into tensor-core fragment order:
+ *      K tile: i = d/16, c = d%16, lane = 4·(t%8) + (c%8)/2,
+ *              e = (c%2) + 2·(t/8) + 4·(c/8)
+ *      V tile: i = d/16, r = d%16, lane = 4·(r%8) + (t%8)/2,
+ *              e = (t%2) + 2·(r/8) + 4·(t/8)
+ *      BF16 element index within the tile: (i·32 + lane)·8 + e
+ *      FP8  byte index within the tile:   ((i/2)·32 + lane)·16 + (i%2)·8 + e
+ *  - FP8 scales: fp32 [L][num_blocks][n_kv][2][16] (index 0 = K, 1 = V; the
+ *    last index is the slot offset t).
+ *  - The pool is written only through kvd_append_kv.
+ */
+#ifndef KVD_H
+#define KVD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KVD_API __attribute__((visibility("default")))
+#else
+#define KVD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KVD_OK = 0,
+    KVD_ERR_INVALID = 1,      /* bad argument: null pointer, negative size, index out of range */
+    KVD_ERR_UNSUPPORTED = 2,  /* valid but outside the supported set (see above) */
+    KVD_ERR_NOMEM = 3,        /* a caller buffer is smaller than required */
+    KVD_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
+    KVD_ERR_OOB = 5,          /* device-detected: block id or sequence length out of range */
+    KVD_ERR_TIMEOUT = 6       /* device-detected: a bounded wait inside a kernel ran out */
+} kvd_status;
+
+typedef enum {
+    KVD_BF16 = 0,             /* w_kv = 2 bytes */
+    KVD_FP8_E4M3 = 1,         /* w_kv = 1 byte, plus a per-(token, KV head) fp32 scale for K and for V */
+    KVD_F32 = 2               /* output only (full-precision check output) */
+} kvd_dtype;
+
+typedef struct {
+    int32_t num_layers;       /* L */
+    int32_t n_kv;             /* KV heads per layer */
+    int32_t d_h;              /* head dimension; 128 */
+    int32_t block_size;       /* tokens per block; 16 */
+    int64_t num_blocks;       /* physical blocks per layer */
+    int32_t kv_dtype;         /* KVD_BF16 or KVD_FP8_E4M3 */
+} kvd_pool_desc;
+
+typedef struct kvd_pool kvd_pool;  /* opaque */
+
+/* Readable name of a status code (static string). */
+KVD_API const char* kvd_status_string(kvd_status s);
+
+/* Bytes the pool needs: kv_bytes = L·num_blocks·n_kv·2·block_size·d_h·w_kv, i.e. the
+ * closed form 2·L·n_kv·d_h·w_kv bytes per token times num_blocks·block_size tokens;
+ * scale_bytes = L·num_blocks·n_kv·2·block_size·4 for FP8, else 0.  Host only. */
+KVD_API kvd_status kvd_pool_bytes(const kvd_pool_desc* desc, size_t* kv_bytes, size_t* scale_bytes);
+
+/* Wrap caller memory as a pool.  kv_mem (kv_len bytes) and scale_mem (scale_len bytes,
+ * NULL for BF16) are device buffers aligned to 16 bytes and at least kvd_pool_bytes large,
+ * else KVD_ERR_NOMEM / KVD_ERR_INVALID.  Allocates the handle and a 4-byte device error
+ * word on the current device (KVD_ERR_CUDA if that fails).  *out is set on success. */
+KVD_API kvd_status kvd_pool_create(const kvd_pool_desc* desc, void* kv_mem, size_t kv_len,
+                           void* scale_mem, size_t scale_len, kvd_pool** out);
+
+/* Free the handle and its error word (not the caller's pool memory).  NULL is a no-op. */
+KVD_API void kvd_pool_destroy(kvd_pool* pool);
+
+/* Decode-step append ("reshape and cache").  Token n's keys k_new[n][h][:] and values
+ * v_new[n][h][:] (bf16, [n_tokens][n_kv][d_h], device) are written for every KV head h of
+ * `layer` at slot s = slot_mapping[n] (int64, device) = physical_block·16 + offset;
+ * s < 0 skips the token.  FP8 pools store per (token, head) and separately for K and V:
+ * scale = fp32(absmax/448) (1 when the row is zero), code = e4m3 round-to-nearest-even,
+ * saturating, of the fp32 quotient x/scale.  n_tokens = 0 is a no-op.  A slot beyond the
+ * pool sets KVD_ERR_OOB on the device and that token is skipped. */
+KVD_API kvd_status kvd_append_kv(kvd_pool* pool, int layer, const void* k_new, const void* v_new,
+                         const int64_t* slot_mapping, int n_tokens, void* stream);
+
+/* The split plan: number of KV splits (CTAs) kvd_decode_attn uses for this shape when
+ * num_splits = 0, and the workspace bytes it needs.  Host only (queries the device's SM
+ * count and the kernel's occupancy through the pool's device). */
+KVD_API kvd_status kvd_decode_workspace_bytes(const kvd_pool* pool, int n_q, int batch, int max_seq_len,
+                                      int num_splits, int* splits_out, size_t* bytes_out);
+
+/* Paged GQA decode attention for one layer.
+ *  q            bf16 [batch][n_q][d_h], device
+ *  block_table  int32 [batch][max_blocks_per_seq], device; entry j of request b is the
+ *               physical block of its logical block j (entries past the context unread)
+ *  seq_lens     int32 [batch], device; positions 0 .. seq_lens[b]-1 are attended (the
+ *               append of this step included); must be in [1, max_blocks_per_seq·16]
+ *  max_seq_len  host upper bound on seq_lens, used only for the split plan
+ *  num_splits   0 = automatic; else the number of KV splits: the flattened sequence of
+ *               (request, KV head, block) work is cut into num_splits equal contiguous
+ *               ranges, one CTA each; partial results are merged by log-sum-exp
+ *  retain_mask  uint16 [num_blocks] or NULL; bit o of retain_mask[p] clear = slot o of
+ *               physical block p is evicted (logit −inf, weight 0) in every layer
+ *  softmax_scale  multiplies q·k (1/√d_h for the plain definition)
+ *  workspace    device scratch of workspace_bytes ≥ kvd_decode_workspace_bytes; layout:
+ *               part_o f32 [S + U][g][d_h], part_lse f32 [S + U][g], unit_first int32 [U],
+ *               unit_count int32 [U], each region starting on a 256-byte boundary, where
+ *               U = batch·n_kv units and S the split count
+ *  out          [batch][n_q][d_h] in out_dtype (KVD_BF16 rounds to nearest even, or KVD_F32);
+ *               NULL = write only the partials and unit tables into the workspace and launch
+ *               no combine (merge later with kvd_combine_splits; lse_out is then unused)
+ *  lse_out      f32 [batch][n_q] natural-log log-sum-exp of the logits, or NULL
+ *  logits_out   f32 [batch][n_q][logits_stride] or NULL: the scaled logit q·k·scale of
+ *               every attended position (−inf where evicted), input of kvd_accum_scores
+ * Query head h reads KV head h / g.  A head with no retained position gets out = 0 and
+ * lse = −inf. */
+KVD_API kvd_status kvd_decode_attn(const kvd_pool* pool, int layer, const void* q, int n_q,
+                           const int32_t* block_table, int max_blocks_per_seq,
+                           const int32_t* seq_lens, int batch, int max_seq_len, int num_splits,
+                           const uint16_t* retain_mask, float softmax_scale,
+                           void* workspace, size_t workspace_bytes,
+                           void* out, int out_dtype, float* lse_out,
+                           float* logits_out, int64_t logits_stride, void* stream);
+
+/* Merge split partials by log-sum-exp.  For unit u = b·n_kv + h/g and head h:
+ * LSE = log Σ_s exp(lse_s), out = Σ_s exp(lse_s − LSE)·o_s over the unit_count[u] slots
+ * starting at unit_first[u] of part_o f32 [slots][g][d_h] and part_lse f32 [slots][g]
+ * (device).  Slots with lse = −inf are skipped; a unit with none (or count 0) yields
+ * out = 0, lse = −inf.  out in out_dtype (KVD_BF16 or KVD_F32), lse_out may be NULL. */
+KVD_API kvd_status kvd_combine_splits(const float* part_o, const float* part_lse,
+                              const int32_t* unit_first, const int32_t* unit_count,
+                              int batch, int n_q, int n_kv, int d_h,
+                              void* out, int out_dtype, float* lse_out, void* stream);
+
+/* Score epilogue: scores[b][t] += inv_LH · Σ_h exp(logits[b][h][t] − lse[b][h]) for
+ * t < seq_lens[b], i.e. this layer's share (1/(L·H))·Σ_h α_h[t] of the cumulative
+ * importance score update.  logits f32 [batch][n_q][logits_stride], lse f32 [batch][n_q]
+ * (both as written by kvd_decode_attn), scores f32 [batch][scores_stride]; all device.
+ * Heads with lse = −inf add nothing. */
+KVD_API kvd_status kvd_accum_scores(const float* logits, int64_t logits_stride, const float* lse,
+                            const int32_t* seq_lens, int batch, int n_q, float inv_LH,
+                            float* scores, int64_t scores_stride, void* stream);
+
+/* Synchronise `stream`, return the pool's device error word in *code (KVD_OK if none) and
+ * clear it. */
+KVD_API kvd_status kvd_get_device_error(kvd_pool* pool, void* stream, int32_t* code);
+
+/* Self-test of the bounded wait: launches one CTA that waits on an mbarrier nothing will
+ * complete, with a limit of timeout_ns nanoseconds; the kernel then records
+ * KVD_ERR_TIMEOUT in the pool's error word and returns.  Lets a caller check that device
+ * waits give up and report instead of hanging. */
+KVD_API kvd_status kvd_selftest_wait_timeout(kvd_pool* pool, int64_t timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVD_H */

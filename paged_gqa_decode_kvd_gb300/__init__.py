@@ -1,0 +1,65 @@
+"""Paged GQA decode attention for GB300 (sm_103a).
+
+The computation lives in ``libkvd.so`` (hand-written CUDA behind a C ABI,
+``include/kvd.h``); this package is its Python binding plus a small owner of
+pool memory.  Importing it does not touch the GPU; the first call that needs
+the library loads it and fails loudly if it is missing or cannot be built.
+"""
+
+from __future__ import annotations
+
+from ._lib import (  # noqa: F401
+    KVD_BF16,
+    KVD_F32,
+    KVD_FP8_E4M3,
+    KVD_OK,
+    KVD_ERR_CUDA,
+    KVD_ERR_INVALID,
+    KVD_ERR_NOMEM,
+    KVD_ERR_OOB,
+    KVD_ERR_TIMEOUT,
+    KVD_ERR_UNSUPPORTED,
+    SYMBOLS,
+    KvdError,
+    kvd_accum_scores,
+    kvd_append_kv,
+    kvd_combine_splits,
+    kvd_decode_attn,
+    kvd_decode_workspace_bytes,
+    kvd_get_device_error,
+    kvd_pool_bytes,
+    kvd_pool_create,
+    kvd_pool_destroy,
+    kvd_selftest_wait_timeout,
+    lib_path,
+    load,
+    status_string,
+)
+
+
+class KVPool:
+    """Device memory for a paged KV pool (torch allocations) plus its library handle."""
+
+    def __init__(self, num_layers: int, n_kv: int, num_blocks: int, kv_dtype: int = KVD_BF16, device="cuda"):
+        import torch
+
+        self.num_layers, self.n_kv, self.num_blocks, self.kv_dtype = num_layers, n_kv, num_blocks, kv_dtype
+        kv_bytes, sc_bytes = kvd_pool_bytes(num_layers, n_kv, num_blocks, kv_dtype)
+        self.kv = torch.empty(kv_bytes, dtype=torch.uint8, device=device)
+        self.scales = torch.empty(sc_bytes // 4, dtype=torch.float32, device=device) if sc_bytes else None
+        self.handle = kvd_pool_create(num_layers, n_kv, num_blocks, kv_dtype, self.kv, self.scales)
+
+    @property
+    def record_bytes(self) -> int:
+        return 2 * 16 * 128 * (2 if self.kv_dtype == KVD_BF16 else 1)
+
+    def close(self):
+        if self.handle is not None:
+            kvd_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,173 @@
+"""ctypes binding of libkvd.so — argument marshalling only.
+
+Every function here has the name of the C entry point it calls and does
+nothing but turn torch tensors into device pointers, pick the current CUDA
+stream and raise ``KvdError`` on a non-OK status.  All computation happens in
+the CUDA kernels behind the C ABI; there is no fallback path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+KVD_OK, KVD_ERR_INVALID, KVD_ERR_UNSUPPORTED, KVD_ERR_NOMEM, KVD_ERR_CUDA, KVD_ERR_OOB, KVD_ERR_TIMEOUT = range(7)
+KVD_BF16, KVD_FP8_E4M3, KVD_F32 = 0, 1, 2
+
+SYMBOLS = [
+    "kvd_status_string", "kvd_pool_bytes", "kvd_pool_create", "kvd_pool_destroy", "kvd_append_kv",
+    "kvd_decode_workspace_bytes", "kvd_decode_attn", "kvd_combine_splits", "kvd_accum_scores",
+    "kvd_get_device_error", "kvd_selftest_wait_timeout",
+]
+
+
+class KvdError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: {msg} (status {status})")
+        self.status = status
+
+
+class PoolDesc(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int32), ("n_kv", ctypes.c_int32), ("d_h", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int64), ("kv_dtype", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libkvd.so")
+
+
+def load(build_if_missing: bool = True):
+    """Load libkvd.so (building it first if absent).  Raises if it cannot be built or loaded."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if build_if_missing:
+        from . import build as _build
+        _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libkvd.so not found at {path}; build it with paged_gqa_decode_kvd_gb300.build")
+    lib = ctypes.CDLL(path)
+    P, i32, i64, sz, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+    lib.kvd_status_string.restype = ctypes.c_char_p
+    lib.kvd_status_string.argtypes = [i32]
+    lib.kvd_pool_bytes.restype = i32
+    lib.kvd_pool_bytes.argtypes = [ctypes.POINTER(PoolDesc), ctypes.POINTER(sz), ctypes.POINTER(sz)]
+    lib.kvd_pool_create.restype = i32
+    lib.kvd_pool_create.argtypes = [ctypes.POINTER(PoolDesc), P, sz, P, sz, ctypes.POINTER(P)]
+    lib.kvd_pool_destroy.restype = None
+    lib.kvd_pool_destroy.argtypes = [P]
+    lib.kvd_append_kv.restype = i32
+    lib.kvd_append_kv.argtypes = [P, i32, P, P, P, i32, P]
+    lib.kvd_decode_workspace_bytes.restype = i32
+    lib.kvd_decode_workspace_bytes.argtypes = [P, i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(sz)]
+    lib.kvd_decode_attn.restype = i32
+    lib.kvd_decode_attn.argtypes = [P, i32, P, i32, P, i32, P, i32, i32, i32, P, f32, P, sz, P, i32, P, P, i64, P]
+    lib.kvd_combine_splits.restype = i32
+    lib.kvd_combine_splits.argtypes = [P, P, P, P, i32, i32, i32, i32, P, i32, P, P]
+    lib.kvd_accum_scores.restype = i32
+    lib.kvd_accum_scores.argtypes = [P, i64, P, P, i32, i32, f32, P, i64, P]
+    lib.kvd_get_device_error.restype = i32
+    lib.kvd_get_device_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
+    lib.kvd_selftest_wait_timeout.restype = i32
+    lib.kvd_selftest_wait_timeout.argtypes = [P, i64, P]
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().kvd_status_string(status).decode()
+
+
+def _check(fn: str, status: int):
+    if status != KVD_OK:
+        raise KvdError(fn, status, status_string(status))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def kvd_pool_bytes(num_layers: int, n_kv: int, num_blocks: int, kv_dtype: int, d_h: int = 128, block_size: int = 16):
+    """(kv_bytes, scale_bytes) of a pool; host only."""
+    d = PoolDesc(num_layers, n_kv, d_h, block_size, num_blocks, kv_dtype)
+    kv, sc = ctypes.c_size_t(), ctypes.c_size_t()
+    _check("kvd_pool_bytes", load().kvd_pool_bytes(ctypes.byref(d), ctypes.byref(kv), ctypes.byref(sc)))
+    return kv.value, sc.value
+
+
+def kvd_pool_create(num_layers, n_kv, num_blocks, kv_dtype, kv_mem, scale_mem=None, d_h=128, block_size=16):
+    """Wrap device tensors (uint8 / float32, caller-owned) as a pool; returns the handle (c_void_p)."""
+    d = PoolDesc(num_layers, n_kv, d_h, block_size, num_blocks, kv_dtype)
+    h = ctypes.c_void_p()
+    kv_len = kv_mem.numel() * kv_mem.element_size()
+    sc_len = 0 if scale_mem is None else scale_mem.numel() * scale_mem.element_size()
+    _check("kvd_pool_create", load().kvd_pool_create(ctypes.byref(d), _ptr(kv_mem), kv_len, _ptr(scale_mem),
+                                                     sc_len, ctypes.byref(h)))
+    return h
+
+
+def kvd_pool_destroy(handle):
+    load().kvd_pool_destroy(handle)
+
+
+def kvd_append_kv(handle, layer, k_new, v_new, slot_mapping, stream=None):
+    n = 0 if k_new is None else k_new.shape[0]
+    _check("kvd_append_kv", load().kvd_append_kv(handle, layer, _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), n,
+                                                 _stream(stream)))
+
+
+def kvd_decode_workspace_bytes(handle, n_q, batch, max_seq_len, num_splits=0):
+    s, b = ctypes.c_int(), ctypes.c_size_t()
+    _check("kvd_decode_workspace_bytes",
+           load().kvd_decode_workspace_bytes(handle, n_q, batch, max_seq_len, num_splits, ctypes.byref(s),
+                                             ctypes.byref(b)))
+    return s.value, b.value
+
+
+def kvd_decode_attn(handle, layer, q, block_table, seq_lens, max_seq_len, workspace, out, num_splits=0,
+                    retain_mask=None, softmax_scale=None, lse_out=None, logits_out=None, stream=None):
+    batch, n_q, d_h = q.shape
+    if softmax_scale is None:
+        softmax_scale = d_h ** -0.5
+    out_dtype = KVD_F32 if out is not None and out.element_size() == 4 else KVD_BF16
+    lstride = 0 if logits_out is None else logits_out.shape[-1]
+    _check("kvd_decode_attn", load().kvd_decode_attn(
+        handle, layer, _ptr(q), n_q, _ptr(block_table), block_table.shape[1], _ptr(seq_lens), batch,
+        int(max_seq_len), int(num_splits), _ptr(retain_mask), float(softmax_scale), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), out_dtype, _ptr(lse_out), _ptr(logits_out),
+        lstride, _stream(stream)))
+
+
+def kvd_combine_splits(part_o, part_lse, unit_first, unit_count, batch, n_q, n_kv, out, lse_out=None, stream=None):
+    out_dtype = KVD_F32 if out.element_size() == 4 else KVD_BF16
+    _check("kvd_combine_splits", load().kvd_combine_splits(
+        _ptr(part_o), _ptr(part_lse), _ptr(unit_first), _ptr(unit_count), batch, n_q, n_kv, 128, _ptr(out),
+        out_dtype, _ptr(lse_out), _stream(stream)))
+
+
+def kvd_accum_scores(logits, lse, seq_lens, inv_LH, scores, stream=None):
+    batch, n_q, lstride = logits.shape
+    _check("kvd_accum_scores", load().kvd_accum_scores(
+        _ptr(logits), lstride, _ptr(lse), _ptr(seq_lens), batch, n_q, float(inv_LH), _ptr(scores),
+        scores.shape[-1], _stream(stream)))
+
+
+def kvd_get_device_error(handle, stream=None) -> int:
+    c = ctypes.c_int32()
+    _check("kvd_get_device_error", load().kvd_get_device_error(handle, _stream(stream), ctypes.byref(c)))
+    return c.value
+
+
+def kvd_selftest_wait_timeout(handle, timeout_ns, stream=None):
+    _check("kvd_selftest_wait_timeout", load().kvd_selftest_wait_timeout(handle, int(timeout_ns), _stream(stream)))

@@ -1,0 +1,325 @@
+// kvd_api.cu — the exported C ABI: argument checks, split plan, launches, error word.
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "../../include/kvd.h"
+#include "kvd_common.cuh"
+#include "kvd_internal.h"
+
+struct kvd_pool {
+    kvd_pool_desc desc;
+    uint8_t* kv;
+    float* scales;
+    int32_t* err;
+    int device;
+    int num_sms;
+    size_t layer_kv_bytes;
+    size_t layer_scale_bytes;
+};
+
+namespace {
+
+constexpr int kMinBlocksPerSplit = 16;  // smallest per-CTA share the planner creates
+
+bool mul_ok(size_t a, size_t b, size_t* out) {
+    if (a != 0 && b > SIZE_MAX / a) return false;
+    *out = a * b;
+    return true;
+}
+
+kvd_status check_desc(const kvd_pool_desc* d) {
+    if (!d) return KVD_ERR_INVALID;
+    if (d->num_layers < 1 || d->n_kv < 1 || d->num_blocks < 1 || d->d_h < 1 || d->block_size < 1)
+        return KVD_ERR_INVALID;
+    if (d->kv_dtype != KVD_BF16 && d->kv_dtype != KVD_FP8_E4M3) return KVD_ERR_INVALID;
+    if (d->d_h != kvd::kDh || d->block_size != kvd::kBs) return KVD_ERR_UNSUPPORTED;
+    return KVD_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct WsLayout {
+    size_t part_o, part_lse, unit_first, unit_count, total;
+};
+
+WsLayout ws_layout(int units, int nsplit, int g) {
+    WsLayout w;
+    const size_t slots = static_cast<size_t>(units) + static_cast<size_t>(nsplit);
+    size_t o = 0;
+    w.part_o = o;
+    o = align256(o + slots * g * kvd::kDh * sizeof(float));
+    w.part_lse = o;
+    o = align256(o + slots * g * sizeof(float));
+    w.unit_first = o;
+    o = align256(o + static_cast<size_t>(units) * sizeof(int32_t));
+    w.unit_count = o;
+    o = align256(o + static_cast<size_t>(units) * sizeof(int32_t));
+    w.total = o;
+    return w;
+}
+
+// Split count: enough CTAs to fill every SM at the kernel's occupancy, but no CTA
+// with fewer than kMinBlocksPerSplit blocks of the (upper-bound) total work.
+int plan_splits(const kvd_pool* pool, int batch, int max_seq_len) {
+    const bool fp8 = pool->desc.kv_dtype == KVD_FP8_E4M3;
+    const int64_t nblk = (static_cast<int64_t>(max_seq_len) + kvd::kBs - 1) / kvd::kBs;
+    const int64_t total = nblk * batch * pool->desc.n_kv;
+    const int64_t by_work = (total + kMinBlocksPerSplit - 1) / kMinBlocksPerSplit;
+    const int64_t by_sms = static_cast<int64_t>(pool->num_sms) * kvd::decode_ctas_per_sm(fp8, batch);
+    int64_t s = by_work < by_sms ? by_work : by_sms;
+    return static_cast<int>(s < 1 ? 1 : s);
+}
+
+kvd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVD_OK : KVD_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* kvd_status_string(kvd_status s) {
+    switch (s) {
+        case KVD_OK: return "ok";
+        case KVD_ERR_INVALID: return "invalid argument";
+        case KVD_ERR_UNSUPPORTED: return "unsupported shape or type";
+        case KVD_ERR_NOMEM: return "buffer too small";
+        case KVD_ERR_CUDA: return "CUDA error";
+        case KVD_ERR_OOB: return "device-detected index out of range";
+        case KVD_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+kvd_status kvd_pool_bytes(const kvd_pool_desc* desc, size_t* kv_bytes, size_t* scale_bytes) {
+    kvd_status st = check_desc(desc);
+    if (st != KVD_OK) return st;
+    if (!kv_bytes || !scale_bytes) return KVD_ERR_INVALID;
+    const size_t w = desc->kv_dtype == KVD_BF16 ? 2 : 1;
+    size_t per_block = 0, rows = 0, total = 0;
+    // 2 (K and V) · block_size · d_h · w_kv bytes per (layer, block, KV head)
+    if (!mul_ok(2 * static_cast<size_t>(desc->block_size) * desc->d_h, w, &per_block)) return KVD_ERR_INVALID;
+    if (!mul_ok(static_cast<size_t>(desc->num_layers), static_cast<size_t>(desc->num_blocks), &rows)) return KVD_ERR_INVALID;
+    if (!mul_ok(rows, static_cast<size_t>(desc->n_kv), &rows)) return KVD_ERR_INVALID;
+    if (!mul_ok(rows, per_block, &total)) return KVD_ERR_INVALID;
+    *kv_bytes = total;
+    *scale_bytes = 0;
+    if (desc->kv_dtype == KVD_FP8_E4M3) {
+        size_t sb = 0;
+        if (!mul_ok(rows, 2 * static_cast<size_t>(desc->block_size) * sizeof(float), &sb)) return KVD_ERR_INVALID;
+        *scale_bytes = sb;
+    }
+    return KVD_OK;
+}
+
+kvd_status kvd_pool_create(const kvd_pool_desc* desc, void* kv_mem, size_t kv_len, void* scale_mem,
+                           size_t scale_len, kvd_pool** out) {
+    if (!out) return KVD_ERR_INVALID;
+    *out = nullptr;
+    size_t need_kv = 0, need_sc = 0;
+    kvd_status st = kvd_pool_bytes(desc, &need_kv, &need_sc);
+    if (st != KVD_OK) return st;
+    if (!kv_mem || !aligned16(kv_mem)) return KVD_ERR_INVALID;
+    if (kv_len < need_kv) return KVD_ERR_NOMEM;
+    if (desc->kv_dtype == KVD_FP8_E4M3) {
+        if (!scale_mem || !aligned16(scale_mem)) return KVD_ERR_INVALID;
+        if (scale_len < need_sc) return KVD_ERR_NOMEM;
+    }
+    kvd_pool* p = new (std::nothrow) kvd_pool;
+    if (!p) return KVD_ERR_NOMEM;
+    p->desc = *desc;
+    p->kv = static_cast<uint8_t*>(kv_mem);
+    p->scales = desc->kv_dtype == KVD_FP8_E4M3 ? static_cast<float*>(scale_mem) : nullptr;
+    p->layer_kv_bytes = need_kv / desc->num_layers;
+    p->layer_scale_bytes = need_sc / desc->num_layers;
+    p->err = nullptr;
+    if (cudaGetDevice(&p->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess ||
+        cudaMalloc(&p->err, sizeof(int32_t)) != cudaSuccess || cudaMemset(p->err, 0, sizeof(int32_t)) != cudaSuccess) {
+        if (p->err) cudaFree(p->err);
+        delete p;
+        cudaGetLastError();
+        return KVD_ERR_CUDA;
+    }
+    *out = p;
+    return KVD_OK;
+}
+
+void kvd_pool_destroy(kvd_pool* pool) {
+    if (!pool) return;
+    if (pool->err) cudaFree(pool->err);
+    delete pool;
+}
+
+kvd_status kvd_append_kv(kvd_pool* pool, int layer, const void* k_new, const void* v_new,
+                         const int64_t* slot_mapping, int n_tokens, void* stream) {
+    if (!pool || layer < 0 || layer >= pool->desc.num_layers || n_tokens < 0) return KVD_ERR_INVALID;
+    if (n_tokens == 0) return KVD_OK;
+    if (!k_new || !v_new || !slot_mapping) return KVD_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(k_new) & 7u) || (reinterpret_cast<uintptr_t>(v_new) & 7u)) return KVD_ERR_INVALID;
+    kvd::AppendParams p;
+    p.k_new = static_cast<const uint16_t*>(k_new);
+    p.v_new = static_cast<const uint16_t*>(v_new);
+    p.slot_mapping = slot_mapping;
+    p.kv = pool->kv + static_cast<size_t>(layer) * pool->layer_kv_bytes;
+    p.scales = pool->scales ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(pool->scales) +
+                                                        static_cast<size_t>(layer) * pool->layer_scale_bytes)
+                            : nullptr;
+    p.err = pool->err;
+    p.n_tokens = n_tokens;
+    p.num_blocks = pool->desc.num_blocks;
+    p.n_kv = pool->desc.n_kv;
+    return cuda_status(kvd::launch_append(p, pool->desc.kv_dtype == KVD_FP8_E4M3, static_cast<cudaStream_t>(stream)));
+}
+
+static kvd_status check_decode_shape(const kvd_pool* pool, int n_q, int batch, int max_seq_len) {
+    if (!pool || n_q < 1 || batch < 0 || max_seq_len < 1) return KVD_ERR_INVALID;
+    if (n_q % pool->desc.n_kv != 0) return KVD_ERR_INVALID;
+    const int g = n_q / pool->desc.n_kv;
+    if (g > kvd::kMaxG || batch > kvd::kMaxBatch) return KVD_ERR_UNSUPPORTED;
+    return KVD_OK;
+}
+
+kvd_status kvd_decode_workspace_bytes(const kvd_pool* pool, int n_q, int batch, int max_seq_len, int num_splits,
+                                      int* splits_out, size_t* bytes_out) {
+    kvd_status st = check_decode_shape(pool, n_q, batch, max_seq_len);
+    if (st != KVD_OK) return st;
+    if (num_splits < 0 || !bytes_out) return KVD_ERR_INVALID;
+    const int S = num_splits > 0 ? num_splits : plan_splits(pool, batch, max_seq_len);
+    const WsLayout w = ws_layout(batch * pool->desc.n_kv, S, n_q / pool->desc.n_kv);
+    if (splits_out) *splits_out = S;
+    *bytes_out = w.total;
+    return KVD_OK;
+}
+
+kvd_status kvd_decode_attn(const kvd_pool* pool, int layer, const void* q, int n_q, const int32_t* block_table,
+                           int max_blocks_per_seq, const int32_t* seq_lens, int batch, int max_seq_len,
+                           int num_splits, const uint16_t* retain_mask, float softmax_scale, void* workspace,
+                           size_t workspace_bytes, void* out, int out_dtype, float* lse_out, float* logits_out,
+                           int64_t logits_stride, void* stream) {
+    kvd_status st = check_decode_shape(pool, n_q, batch, max_seq_len);
+    if (st != KVD_OK) return st;
+    if (layer < 0 || layer >= pool->desc.num_layers || num_splits < 0 || max_blocks_per_seq < 1) return KVD_ERR_INVALID;
+    if (out_dtype != KVD_BF16 && out_dtype != KVD_F32) return KVD_ERR_INVALID;
+    if (batch == 0) return KVD_OK;
+    if (!q || !block_table || !seq_lens || !workspace) return KVD_ERR_INVALID;
+    if (logits_out && logits_stride < 1) return KVD_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(q) & 3u) || (reinterpret_cast<uintptr_t>(out) & 15u) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return KVD_ERR_INVALID;
+    const int g = n_q / pool->desc.n_kv;
+    const int U = batch * pool->desc.n_kv;
+    const int S = num_splits > 0 ? num_splits : plan_splits(pool, batch, max_seq_len);
+    const WsLayout w = ws_layout(U, S, g);
+    if (workspace_bytes < w.total) return KVD_ERR_NOMEM;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const bool fp8 = pool->desc.kv_dtype == KVD_FP8_E4M3;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    kvd::DecodeParams p;
+    p.kv = pool->kv + static_cast<size_t>(layer) * pool->layer_kv_bytes;
+    p.scales = fp8 ? reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(pool->scales) +
+                                                    static_cast<size_t>(layer) * pool->layer_scale_bytes)
+                   : nullptr;
+    p.q = static_cast<const uint16_t*>(q);
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.retain = retain_mask;
+    p.part_o = reinterpret_cast<float*>(ws + w.part_o);
+    p.part_lse = reinterpret_cast<float*>(ws + w.part_lse);
+    p.unit_first = reinterpret_cast<int32_t*>(ws + w.unit_first);
+    p.unit_count = reinterpret_cast<int32_t*>(ws + w.unit_count);
+    p.logits = logits_out;
+    p.logits_stride = logits_stride;
+    p.err = pool->err;
+    p.num_blocks = pool->desc.num_blocks;
+    p.max_blocks = max_blocks_per_seq;
+    p.B = batch;
+    p.n_kv = pool->desc.n_kv;
+    p.g = g;
+    p.n_q = n_q;
+    p.nsplit = S;
+    p.scale_log2 = softmax_scale * kvd::kLog2e;
+    cudaError_t e = kvd::launch_decode(p, fp8, s);
+    if (e != cudaSuccess) return KVD_ERR_CUDA;
+    if (!out) return KVD_OK;  // partials only: the caller merges them with kvd_combine_splits
+
+    kvd::CombineParams c;
+    c.part_o = p.part_o;
+    c.part_lse = p.part_lse;
+    c.unit_first = p.unit_first;
+    c.unit_count = p.unit_count;
+    c.out = out;
+    c.lse_out = lse_out;
+    c.B = batch;
+    c.n_q = n_q;
+    c.n_kv = pool->desc.n_kv;
+    c.g = g;
+    c.out_f32 = out_dtype == KVD_F32;
+    return cuda_status(kvd::launch_combine(c, s));
+}
+
+kvd_status kvd_combine_splits(const float* part_o, const float* part_lse, const int32_t* unit_first,
+                              const int32_t* unit_count, int batch, int n_q, int n_kv, int d_h, void* out,
+                              int out_dtype, float* lse_out, void* stream) {
+    if (batch < 0 || n_q < 1 || n_kv < 1 || n_q % n_kv != 0) return KVD_ERR_INVALID;
+    if (out_dtype != KVD_BF16 && out_dtype != KVD_F32) return KVD_ERR_INVALID;
+    if (d_h != kvd::kDh || n_q / n_kv > kvd::kMaxG) return KVD_ERR_UNSUPPORTED;
+    if (batch == 0) return KVD_OK;
+    if (!part_o || !part_lse || !unit_first || !unit_count || !out) return KVD_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(part_o) & 15u) || (reinterpret_cast<uintptr_t>(out) & 15u)) return KVD_ERR_INVALID;
+    kvd::CombineParams c;
+    c.part_o = part_o;
+    c.part_lse = part_lse;
+    c.unit_first = unit_first;
+    c.unit_count = unit_count;
+    c.out = out;
+    c.lse_out = lse_out;
+    c.B = batch;
+    c.n_q = n_q;
+    c.n_kv = n_kv;
+    c.g = n_q / n_kv;
+    c.out_f32 = out_dtype == KVD_F32;
+    return cuda_status(kvd::launch_combine(c, static_cast<cudaStream_t>(stream)));
+}
+
+kvd_status kvd_accum_scores(const float* logits, int64_t logits_stride, const float* lse, const int32_t* seq_lens,
+                            int batch, int n_q, float inv_LH, float* scores, int64_t scores_stride, void* stream) {
+    if (batch < 0 || n_q < 1 || logits_stride < 1 || scores_stride < 1) return KVD_ERR_INVALID;
+    if (batch == 0) return KVD_OK;
+    if (!logits || !lse || !seq_lens || !scores) return KVD_ERR_INVALID;
+    if (batch > 65535) return KVD_ERR_UNSUPPORTED;
+    kvd::ScoreParams p;
+    p.logits = logits;
+    p.logits_stride = logits_stride;
+    p.lse = lse;
+    p.seq_lens = seq_lens;
+    p.scores = scores;
+    p.scores_stride = scores_stride;
+    p.B = batch;
+    p.n_q = n_q;
+    p.inv_LH = inv_LH;
+    return cuda_status(kvd::launch_scores(p, static_cast<cudaStream_t>(stream)));
+}
+
+kvd_status kvd_get_device_error(kvd_pool* pool, void* stream, int32_t* code) {
+    if (!pool || !code) return KVD_ERR_INVALID;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t h = 0;
+    if (cudaMemcpyAsync(&h, pool->err, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess) return KVD_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KVD_ERR_CUDA;
+    if (cudaMemsetAsync(pool->err, 0, sizeof(int32_t), s) != cudaSuccess) return KVD_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KVD_ERR_CUDA;
+    *code = h;
+    return KVD_OK;
+}
+
+kvd_status kvd_selftest_wait_timeout(kvd_pool* pool, int64_t timeout_ns, void* stream) {
+    if (!pool || timeout_ns < 1 || timeout_ns > 10000000000ll) return KVD_ERR_INVALID;
+    return cuda_status(kvd::launch_wait_timeout(pool->err, timeout_ns, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

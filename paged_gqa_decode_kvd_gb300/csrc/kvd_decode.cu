@@ -1,0 +1,568 @@
+// kvd_decode.cu — paged GQA decode attention, split-KV, for sm_103a.
+//
+// What it computes (per request b, query head h, KV head h/g):
+//   l_t = softmax_scale · q_h · K_t  for every attended position t (−inf if evicted),
+//   out_h = Σ_t softmax(l)_t · V_t,   lse_h = log Σ_t exp(l_t);
+// the K/V of position t come from physical block block_table[b][t/16], slot
+// t%16 (page "LLM에서 KV 캐시는 얼마나 생길까", section "KV 캐시를 줄이는 기법":
+// the kernel follows the block table, so scattered blocks give the same result;
+// section "KV 캐시란": scores scaled by 1/√128, softmax, weighted sum of V).
+//
+// How (GB300 design):
+//  * Work = the flattened sequence of (request, KV head, logical block); it is
+//    cut into `nsplit` equal contiguous ranges, one CTA each, so every CTA
+//    streams the same number of blocks whatever the length mix.  A CTA writes
+//    one partial (o, lse) per unit segment it touches into slot u + cta, and
+//    the combine kernel merges the partials of each unit by log-sum-exp.
+//  * One producer warp reads the block table (32 entries per coalesced load)
+//    and issues 1-D bulk copies (TMA engine) of each (block, KV head) record —
+//    K tile + V tile, 8 KiB BF16 or 4 KiB FP8 (+128 B of scales) — into a ring
+//    of shared-memory stages guarded by mbarriers.
+//  * NCW consumer warps take stages round-robin.  The record is stored in
+//    tensor-core fragment order, so each lane's 16-byte shared loads are the
+//    A operands of mma.m16n8k16 directly: S^T = K·Q^T (16 tokens × g heads,
+//    the g query heads of the group share every K load), online softmax in
+//    fp32 (exp2 domain), P^T built with movmatrix, O^T += V^T·P^T.
+//  * FP8: codes convert exactly to f16; the K scale multiplies the fp32 logit,
+//    the V scale folds into p before it is rounded to f16 for the MMA.
+//  * Every mbarrier wait is bounded (%globaltimer); a timeout records
+//    KVD_ERR_TIMEOUT and the CTA drains its copies and returns.
+#include "kvd_common.cuh"
+#include "kvd_internal.h"
+
+namespace kvd {
+
+constexpr int kNcw = 4;                    // consumer warps per CTA
+constexpr int kThreads = (kNcw + 1) * 32;  // + 1 producer warp
+constexpr int kStages = 6;
+constexpr int kMergeStride = 132;          // floats per head row in the merge buffer (bank spread)
+constexpr int kMergeFloats = kMaxG * kMergeStride + 2 * kMaxG;
+constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s
+
+template <bool FP8>
+struct Cfg {
+    static constexpr int kTile = FP8 ? kTileFp8 : kTileBf16;
+    static constexpr int kRecord = 2 * kTile;
+    static constexpr int kStage = FP8 ? kRecord + 2 * kBs * 4 : kRecord;
+};
+
+struct Smem {
+    int ring_off, full_off, empty_off, meta_off, merge_off, pref_off, abort_off, total;
+};
+
+template <bool FP8>
+__host__ __device__ inline Smem smem_layout(int batch) {
+    Smem s;
+    int o = 0;
+    s.ring_off = o;
+    o += kStages * Cfg<FP8>::kStage;
+    s.full_off = o;
+    o += kStages * 8;
+    s.empty_off = o;
+    o += kStages * 8;
+    s.meta_off = o;
+    o += kStages * 4;
+    o = (o + 15) & ~15;
+    s.merge_off = o;
+    o += kNcw * kMergeFloats * 4;
+    s.pref_off = o;
+    o += (batch + 1) * 4;
+    s.abort_off = o;
+    o += 4;
+    s.total = (o + 127) & ~127;
+    return s;
+}
+
+struct Segment {
+    int b, kvh;
+    int j0, j1;       // logical block range of this CTA's piece of the unit
+    int nblk;         // blocks of the whole unit (n_b)
+    int64_t end;      // flattened index one past this piece
+    int64_t unit_end; // flattened index one past the unit
+};
+
+// Unit holding flattened block index x: units are ordered (b, kvh); unit (b, kvh)
+// covers [n_kv·pref[b] + kvh·n_b, n_kv·pref[b] + (kvh+1)·n_b).
+__device__ __forceinline__ Segment find_segment(const int* pref, int B, int n_kv, int64_t x, int64_t hi) {
+    int lo = 0, up = B - 1;
+    while (lo < up) {
+        const int mid = (lo + up + 1) >> 1;
+        if (static_cast<int64_t>(n_kv) * pref[mid] <= x) lo = mid;
+        else up = mid - 1;
+    }
+    Segment s;
+    s.b = lo;
+    s.nblk = pref[lo + 1] - pref[lo];
+    const int64_t base = static_cast<int64_t>(n_kv) * pref[lo];
+    s.kvh = static_cast<int>((x - base) / s.nblk);
+    const int64_t ustart = base + static_cast<int64_t>(s.kvh) * s.nblk;
+    s.unit_end = ustart + s.nblk;
+    s.end = s.unit_end < hi ? s.unit_end : hi;
+    s.j0 = static_cast<int>(x - ustart);
+    s.j1 = static_cast<int>(s.end - ustart);
+    return s;
+}
+
+template <bool FP8>
+__global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const Smem L = smem_layout<FP8>(p.B);
+    uint8_t* ring = smem + L.ring_off;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full_off);
+    uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty_off);
+    int* meta = reinterpret_cast<int*>(smem + L.meta_off);
+    float* merge = reinterpret_cast<float*>(smem + L.merge_off);
+    int* pref = reinterpret_cast<int*>(smem + L.pref_off);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_off);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int cta = blockIdx.x;
+
+    // ---- plan: blocks per request, prefix sums, this CTA's range -----------------
+    for (int b = tid; b < p.B; b += kThreads) {
+        const int len = p.seq_lens[b];
+        int n = (len + kBs - 1) / kBs;
+        if (len < 1 || n > p.max_blocks) {
+            n = 0;
+            if (cta == 0) report(p.err, KVD_ERR_OOB);
+        }
+        pref[b + 1] = n;
+    }
+    if (tid == 0) {
+        pref[0] = 0;
+        *abort_flag = 0;
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (warp == 0) {  // inclusive scan of pref[1..B]
+        const int per = (p.B + 31) / 32;
+        const int a = 1 + lane * per;
+        const int e = min(p.B + 1, a + per);
+        int run = 0;
+        for (int i = a; i < e; ++i) run += pref[i];
+        int incl = run;
+        #pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int acc = incl - run;
+        for (int i = a; i < e; ++i) {
+            acc += pref[i];
+            pref[i] = acc;
+        }
+    }
+    __syncthreads();
+
+    const int64_t T = static_cast<int64_t>(p.n_kv) * pref[p.B];
+    const int64_t chunk = (T + p.nsplit - 1) / p.nsplit;
+    const int64_t lo = chunk * cta;
+    const int64_t hi = (lo + chunk < T) ? lo + chunk : T;
+
+    // Units with no block: no CTA covers them, so CTA 0 marks them empty.
+    if (cta == 0) {
+        const int U = p.B * p.n_kv;
+        for (int u = tid; u < U; u += kThreads) {
+            const int b = u / p.n_kv;
+            if (pref[b + 1] == pref[b]) {
+                p.unit_first[u] = 0;
+                p.unit_count[u] = 0;
+            }
+        }
+    }
+
+    if (warp == kNcw) {
+        // =========================== producer warp ===========================
+        const uint64_t policy = policy_evict_first();
+        uint32_t k = 0;
+        bool aborted = false;
+        for (int64_t x = lo; x < hi && !aborted;) {
+            const Segment sg = find_segment(pref, p.B, p.n_kv, x, hi);
+            const int32_t* bt = p.block_table + static_cast<int64_t>(sg.b) * p.max_blocks;
+            const int len = p.seq_lens[sg.b];
+            for (int jb = sg.j0; jb < sg.j1 && !aborted; jb += 32) {
+                const int j = jb + lane;
+                int phys = -1;
+                uint32_t vm = 0;
+                if (j < sg.j1) {
+                    phys = bt[j];
+                    if (phys >= 0 && phys < p.num_blocks) {
+                        const int valid = len - j * kBs;
+                        vm = valid >= kBs ? 0xFFFFu : ((1u << valid) - 1u);
+                        if (p.retain) vm &= p.retain[phys];
+                        vm |= 1u << 16;
+                    } else {
+                        report(p.err, KVD_ERR_OOB);
+                    }
+                }
+                const int cnt = min(32, sg.j1 - jb);
+                for (int i = 0; i < cnt; ++i) {
+                    const int ph = __shfl_sync(kFull, phys, i);
+                    const uint32_t m = __shfl_sync(kFull, vm, i);
+                    const int s = k % kStages;
+                    const uint32_t par = (k / kStages) & 1u;
+                    int ok = 1;
+                    if (lane == 0) {
+                        ok = mbar_wait(&empty[s], par ^ 1u, abort_flag, kWaitNs);
+                        if (ok) {
+                            meta[s] = static_cast<int>(m);
+                            if (m >> 16) {
+                                const uint8_t* rec =
+                                    p.kv + (static_cast<int64_t>(ph) * p.n_kv + sg.kvh) * Cfg<FP8>::kRecord;
+                                uint8_t* dst = ring + s * Cfg<FP8>::kStage;
+                                mbar_arrive_expect_tx(&full[s], Cfg<FP8>::kStage);
+                                bulk_g2s(dst, rec, Cfg<FP8>::kRecord, &full[s], policy);
+                                if constexpr (FP8) {
+                                    const float* sc = p.scales + (static_cast<int64_t>(ph) * p.n_kv + sg.kvh) * (2 * kBs);
+                                    bulk_g2s(dst + Cfg<FP8>::kRecord, sc, 2 * kBs * 4, &full[s], policy);
+                                }
+                            } else {
+                                mbar_arrive(&full[s]);
+                            }
+                        } else {
+                            report(p.err, KVD_ERR_TIMEOUT);
+                            *abort_flag = 1;
+                        }
+                    }
+                    ok = __shfl_sync(kFull, ok, 0);
+                    if (!ok) {
+                        aborted = true;
+                        break;
+                    }
+                    ++k;
+                }
+            }
+            x = sg.end;
+        }
+        // Drain: every issued copy must land before the CTA may exit.
+        if (lane == 0) {
+            const uint32_t first = k > static_cast<uint32_t>(kStages) ? k - kStages : 0u;
+            for (uint32_t kk = first; kk < k; ++kk)
+                if (!mbar_wait(&full[kk % kStages], (kk / kStages) & 1u, nullptr, kWaitNs))
+                    report(p.err, KVD_ERR_TIMEOUT);
+        }
+        return;
+    }
+
+    // ============================ consumer warps ============================
+    const int gid = lane >> 2;   // token row (S^T) / dim row (O^T) within an 8-row group
+    const int tq = lane & 3;     // head pair 2tq, 2tq+1
+    const int h0 = 2 * tq, h1 = 2 * tq + 1;
+    const int g = p.g;
+    uint32_t k = 0;
+    for (int64_t x = lo; x < hi;) {
+        const Segment sg = find_segment(pref, p.B, p.n_kv, x, hi);
+        const int nseg = sg.j1 - sg.j0;
+        const int len = p.seq_lens[sg.b];
+        const int u = sg.b * p.n_kv + sg.kvh;
+
+        // Q^T fragments (B operand): head gid, dims 16i + 2tq + {0,1,8,9}.
+        uint32_t qf[8][2];
+        {
+            const uint16_t* qh = p.q + (static_cast<int64_t>(sg.b) * p.n_q + sg.kvh * g + gid) * kDh;
+            #pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                uint32_t lo2 = 0, hi2 = 0;
+                if (gid < g) {
+                    lo2 = *reinterpret_cast<const uint32_t*>(qh + 16 * i + 2 * tq);
+                    hi2 = *reinterpret_cast<const uint32_t*>(qh + 16 * i + 2 * tq + 8);
+                }
+                if constexpr (FP8) {  // bf16 -> f16 (exact inside the f16 range)
+                    const __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&lo2);
+                    const __nv_bfloat162 c = *reinterpret_cast<__nv_bfloat162*>(&hi2);
+                    lo2 = pack_f16(__low2float(a), __high2float(a));
+                    hi2 = pack_f16(__low2float(c), __high2float(c));
+                }
+                qf[i][0] = lo2;
+                qf[i][1] = hi2;
+            }
+        }
+
+        float m0 = -INFINITY, m1 = -INFINITY;   // running max (log2 domain), heads h0, h1
+        float s0 = 0.f, s1 = 0.f;               // running sum of p (this lane's tokens)
+        float o[8][4];
+        #pragma unroll
+        for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+        float* lg0 = nullptr;
+        float* lg1 = nullptr;
+        if (p.logits) {
+            const int64_t rowb = static_cast<int64_t>(sg.b) * p.n_q + sg.kvh * g;
+            lg0 = h0 < g ? p.logits + (rowb + h0) * p.logits_stride : nullptr;
+            lg1 = h1 < g ? p.logits + (rowb + h1) * p.logits_stride : nullptr;
+        }
+
+        for (int kk = warp; kk < nseg; kk += kNcw) {
+            const uint32_t kg = k + kk;
+            const int s = kg % kStages;
+            if (!mbar_wait(&full[s], (kg / kStages) & 1u, abort_flag, kWaitNs)) {
+                if (lane == 0) {
+                    report(p.err, KVD_ERR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            const uint32_t m = static_cast<uint32_t>(meta[s]);
+            if (!(m >> 16)) {  // bad block id: reported by the producer, treated as empty
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+                continue;
+            }
+            const uint8_t* st = ring + s * Cfg<FP8>::kStage;
+            const int j = sg.j0 + kk;
+
+            // ---- S^T = K · Q^T  (16 tokens × 8 heads) ----
+            float ca[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
+            float fk0, fk1, fv0 = 1.f, fv1 = 1.f;
+            if constexpr (!FP8) {
+                const uint4* kt = reinterpret_cast<const uint4*>(st);
+                #pragma unroll
+                for (int i = 0; i < 8; i += 2) {
+                    const uint4 a0 = kt[i * 32 + lane];
+                    const uint4 a1 = kt[(i + 1) * 32 + lane];
+                    const uint32_t fa[4] = {a0.x, a0.y, a0.z, a0.w};
+                    const uint32_t fb[4] = {a1.x, a1.y, a1.z, a1.w};
+                    mma_bf16(ca, fa, qf[i][0], qf[i][1]);
+                    mma_bf16(cb, fb, qf[i + 1][0], qf[i + 1][1]);
+                }
+                fk0 = fk1 = p.scale_log2;
+            } else {
+                const uint4* kt = reinterpret_cast<const uint4*>(st);
+                #pragma unroll
+                for (int u4 = 0; u4 < 4; ++u4) {
+                    const uint4 w = kt[u4 * 32 + lane];
+                    const uint32_t fa[4] = {e4m3x2_to_f16x2(w.x & 0xffff), e4m3x2_to_f16x2(w.x >> 16),
+                                            e4m3x2_to_f16x2(w.y & 0xffff), e4m3x2_to_f16x2(w.y >> 16)};
+                    const uint32_t fb[4] = {e4m3x2_to_f16x2(w.z & 0xffff), e4m3x2_to_f16x2(w.z >> 16),
+                                            e4m3x2_to_f16x2(w.w & 0xffff), e4m3x2_to_f16x2(w.w >> 16)};
+                    mma_f16(ca, fa, qf[2 * u4][0], qf[2 * u4][1]);
+                    mma_f16(cb, fb, qf[2 * u4 + 1][0], qf[2 * u4 + 1][1]);
+                }
+                const float* sc = reinterpret_cast<const float*>(st + Cfg<FP8>::kRecord);
+                fk0 = sc[gid] * p.scale_log2;
+                fk1 = sc[gid + 8] * p.scale_log2;
+                fv0 = sc[kBs + gid];
+                fv1 = sc[kBs + gid + 8];
+            }
+            const bool v0 = (m >> gid) & 1u;        // token gid
+            const bool v1 = (m >> (gid + 8)) & 1u;  // token gid + 8
+            float l0 = v0 ? (ca[0] + cb[0]) * fk0 : -INFINITY;  // (gid,   h0)
+            float l1 = v0 ? (ca[1] + cb[1]) * fk0 : -INFINITY;  // (gid,   h1)
+            float l2 = v1 ? (ca[2] + cb[2]) * fk1 : -INFINITY;  // (gid+8, h0)
+            float l3 = v1 ? (ca[3] + cb[3]) * fk1 : -INFINITY;  // (gid+8, h1)
+
+            if (p.logits) {
+                const int t0 = j * kBs + gid, t1 = t0 + 8;
+                const int64_t lim = len < p.logits_stride ? len : p.logits_stride;
+                if (lg0) {
+                    if (t0 < lim) lg0[t0] = l0 * kLn2;
+                    if (t1 < lim) lg0[t1] = l2 * kLn2;
+                }
+                if (lg1) {
+                    if (t0 < lim) lg1[t0] = l1 * kLn2;
+                    if (t1 < lim) lg1[t1] = l3 * kLn2;
+                }
+            }
+
+            // ---- online softmax (exp2 domain), heads h0 and h1 ----
+            float bm0 = fmaxf(l0, l2), bm1 = fmaxf(l1, l3);
+            #pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, off));
+                bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, off));
+            }
+            const float n0 = fmaxf(m0, bm0), n1 = fmaxf(m1, bm1);
+            const float z0 = n0 == -INFINITY ? 0.f : n0;
+            const float z1 = n1 == -INFINITY ? 0.f : n1;
+            const float c0 = ex2(m0 - z0), c1 = ex2(m1 - z1);   // 0 when m was −inf
+            const float p0 = ex2(l0 - z0), p1 = ex2(l1 - z1), p2 = ex2(l2 - z0), p3 = ex2(l3 - z1);
+            s0 = s0 * c0 + (p0 + p2);
+            s1 = s1 * c1 + (p1 + p3);
+            m0 = n0;
+            m1 = n1;
+            if (__any_sync(kFull, c0 != 1.f || c1 != 1.f)) {
+                #pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    o[i][0] *= c0;
+                    o[i][1] *= c1;
+                    o[i][2] *= c0;
+                    o[i][3] *= c1;
+                }
+            }
+
+            // ---- P^T fragment: rows = tokens, cols = heads -> transpose ----
+            uint32_t pb0, pb1;
+            if constexpr (!FP8) {
+                pb0 = movmatrix_t(pack_bf16(p0, p1));
+                pb1 = movmatrix_t(pack_bf16(p2, p3));
+            } else {
+                const float w0 = v0 ? fv0 : 0.f, w1 = v1 ? fv1 : 0.f;
+                pb0 = movmatrix_t(pack_f16(p0 * w0, p1 * w0));
+                pb1 = movmatrix_t(pack_f16(p2 * w1, p3 * w1));
+            }
+
+            // ---- O^T += V^T · P^T ----
+            const bool partial = (m & 0xFFFFu) != 0xFFFFu;
+            // halves of this lane's V fragment that belong to invalid tokens are zeroed,
+            // so garbage (NaN) in unused slots cannot reach the output through 0·NaN
+            uint32_t zlo = 0xFFFFFFFFu, zhi = 0xFFFFFFFFu;
+            if (partial) {
+                const int ta = 2 * tq;
+                zlo = (((m >> ta) & 1u) ? 0x0000FFFFu : 0u) | (((m >> (ta + 1)) & 1u) ? 0xFFFF0000u : 0u);
+                zhi = (((m >> (ta + 8)) & 1u) ? 0x0000FFFFu : 0u) | (((m >> (ta + 9)) & 1u) ? 0xFFFF0000u : 0u);
+            }
+            if constexpr (!FP8) {
+                const uint4* vt = reinterpret_cast<const uint4*>(st + Cfg<FP8>::kTile);
+                uint4 vv[8];
+                #pragma unroll
+                for (int i = 0; i < 8; ++i) vv[i] = vt[i * 32 + lane];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+                #pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t fa[4] = {vv[i].x & zlo, vv[i].y & zlo, vv[i].z & zhi, vv[i].w & zhi};
+                    mma_bf16(o[i], fa, pb0, pb1);
+                }
+            } else {
+                const uint4* vt = reinterpret_cast<const uint4*>(st + Cfg<FP8>::kTile);
+                uint4 vv[4];
+                #pragma unroll
+                for (int i = 0; i < 4; ++i) vv[i] = vt[i * 32 + lane];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+                #pragma unroll
+                for (int u4 = 0; u4 < 4; ++u4) {
+                    const uint32_t fa[4] = {e4m3x2_to_f16x2(vv[u4].x & 0xffff) & zlo, e4m3x2_to_f16x2(vv[u4].x >> 16) & zlo,
+                                            e4m3x2_to_f16x2(vv[u4].y & 0xffff) & zhi, e4m3x2_to_f16x2(vv[u4].y >> 16) & zhi};
+                    const uint32_t fb[4] = {e4m3x2_to_f16x2(vv[u4].z & 0xffff) & zlo, e4m3x2_to_f16x2(vv[u4].z >> 16) & zlo,
+                                            e4m3x2_to_f16x2(vv[u4].w & 0xffff) & zhi, e4m3x2_to_f16x2(vv[u4].w >> 16) & zhi};
+                    mma_f16(o[2 * u4], fa, pb0, pb1);
+                    mma_f16(o[2 * u4 + 1], fb, pb0, pb1);
+                }
+            }
+        }
+        k += nseg;
+
+        // ---- merge the consumer warps' states, write this unit piece's partial ----
+        #pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            s0 += __shfl_xor_sync(kFull, s0, off);
+            s1 += __shfl_xor_sync(kFull, s1, off);
+        }
+        float* mb = merge + warp * kMergeFloats;
+        #pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int d0 = 16 * i + gid, d1 = d0 + 8;
+            mb[h0 * kMergeStride + d0] = o[i][0];
+            mb[h1 * kMergeStride + d0] = o[i][1];
+            mb[h0 * kMergeStride + d1] = o[i][2];
+            mb[h1 * kMergeStride + d1] = o[i][3];
+        }
+        if (gid == 0) {
+            mb[kMaxG * kMergeStride + h0] = m0;
+            mb[kMaxG * kMergeStride + h1] = m1;
+            mb[kMaxG * kMergeStride + kMaxG + h0] = s0;
+            mb[kMaxG * kMergeStride + kMaxG + h1] = s1;
+        }
+        named_barrier(1, kNcw * 32);
+        const int slot = u + cta;
+        for (int idx = tid; idx < g * kDh; idx += kNcw * 32) {
+            const int h = idx / kDh, d = idx % kDh;
+            float M = -INFINITY;
+            #pragma unroll
+            for (int w = 0; w < kNcw; ++w) M = fmaxf(M, merge[w * kMergeFloats + kMaxG * kMergeStride + h]);
+            float Ls = 0.f, acc = 0.f;
+            if (M != -INFINITY) {
+                #pragma unroll
+                for (int w = 0; w < kNcw; ++w) {
+                    const float* mw = merge + w * kMergeFloats;
+                    const float e = ex2(mw[kMaxG * kMergeStride + h] - M);
+                    Ls += mw[kMaxG * kMergeStride + kMaxG + h] * e;
+                    acc += mw[h * kMergeStride + d] * e;
+                }
+            }
+            const bool any = Ls > 0.f;
+            p.part_o[(static_cast<int64_t>(slot) * g + h) * kDh + d] = any ? acc / Ls : 0.f;
+            if (d == 0) p.part_lse[static_cast<int64_t>(slot) * g + h] = any ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+        }
+        if (sg.j0 == 0 && tid == 0) {
+            const int64_t c_last = (sg.unit_end - 1) / chunk;
+            p.unit_first[u] = slot;
+            p.unit_count[u] = static_cast<int>(c_last - cta + 1);
+        }
+        named_barrier(1, kNcw * 32);
+        x = sg.end;
+    }
+}
+
+size_t decode_smem_bytes(bool fp8, int batch) {
+    return fp8 ? smem_layout<true>(batch).total : smem_layout<false>(batch).total;
+}
+
+template <bool FP8>
+static cudaError_t ensure_smem_attr();
+
+template <bool FP8>
+static int ctas_per_sm_impl(int batch) {
+    const int smem = smem_layout<FP8>(batch).total;
+    if (ensure_smem_attr<FP8>() != cudaSuccess) return 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<FP8>, kThreads, smem) != cudaSuccess)
+        return 1;
+    return n > 0 ? n : 1;
+}
+
+int decode_ctas_per_sm(bool fp8, int batch) { return fp8 ? ctas_per_sm_impl<true>(batch) : ctas_per_sm_impl<false>(batch); }
+
+// Raise the kernel's dynamic shared-memory limit once per device to the largest
+// layout any batch size can need (batch ≤ kMaxBatch).
+template <bool FP8>
+static cudaError_t ensure_smem_attr() {
+    static int done_for_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (done_for_device == dev) return cudaSuccess;
+    e = cudaFuncSetAttribute(decode_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_layout<FP8>(kMaxBatch).total);
+    if (e == cudaSuccess) done_for_device = dev;
+    return e;
+}
+
+cudaError_t launch_decode(const DecodeParams& p, bool fp8, cudaStream_t stream) {
+    const size_t smem = decode_smem_bytes(fp8, p.B);
+    cudaError_t e = fp8 ? ensure_smem_attr<true>() : ensure_smem_attr<false>();
+    if (e != cudaSuccess) return e;
+    if (fp8)
+        decode_kernel<true><<<p.nsplit, kThreads, smem, stream>>>(p);
+    else
+        decode_kernel<false><<<p.nsplit, kThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- wait self-test
+__global__ void wait_timeout_kernel(int32_t* err, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // nothing arrives on `bar`: the wait must give up and report
+        if (!mbar_wait(&bar, 0, nullptr, limit_ns)) report(err, KVD_ERR_TIMEOUT);
+    }
+}
+
+cudaError_t launch_wait_timeout(int32_t* err, int64_t timeout_ns, cudaStream_t stream) {
+    wait_timeout_kernel<<<1, 32, 0, stream>>>(err, static_cast<uint64_t>(timeout_ns));
+    return cudaGetLastError();
+}
+
+}  // namespace kvd

@@ -1,0 +1,79 @@
+// kvd_internal.h — kernel parameter blocks and launchers (host <-> device, not exported).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kvd {
+
+struct AppendParams {
+    const uint16_t* k_new;       // bf16 bits [n_tokens][n_kv][128]
+    const uint16_t* v_new;
+    const int64_t* slot_mapping; // [n_tokens]
+    uint8_t* kv;                 // this layer's tile records
+    float* scales;               // this layer's scales (FP8) or null
+    int32_t* err;
+    int64_t n_tokens;
+    int64_t num_blocks;
+    int n_kv;
+};
+
+struct DecodeParams {
+    const uint8_t* kv;           // this layer's tile records
+    const float* scales;         // this layer's scales [num_blocks][n_kv][2][16] (FP8) or null
+    const uint16_t* q;           // bf16 bits [B][n_q][128]
+    const int32_t* block_table;  // [B][max_blocks]
+    const int32_t* seq_lens;     // [B]
+    const uint16_t* retain;      // [num_blocks] or null
+    float* part_o;               // [S + U][g][128]
+    float* part_lse;             // [S + U][g]
+    int32_t* unit_first;         // [U]
+    int32_t* unit_count;         // [U]
+    float* logits;               // [B][n_q][logits_stride] or null
+    int64_t logits_stride;
+    int32_t* err;
+    int64_t num_blocks;
+    int max_blocks;
+    int B;
+    int n_kv;
+    int g;
+    int n_q;
+    int nsplit;
+    float scale_log2;            // softmax_scale * log2(e)
+};
+
+struct CombineParams {
+    const float* part_o;
+    const float* part_lse;
+    const int32_t* unit_first;
+    const int32_t* unit_count;
+    void* out;
+    float* lse_out;
+    int B;
+    int n_q;
+    int n_kv;
+    int g;
+    int out_f32;
+};
+
+struct ScoreParams {
+    const float* logits;
+    int64_t logits_stride;
+    const float* lse;
+    const int32_t* seq_lens;
+    float* scores;
+    int64_t scores_stride;
+    int B;
+    int n_q;
+    float inv_LH;
+};
+
+cudaError_t launch_append(const AppendParams& p, bool fp8, cudaStream_t stream);
+size_t decode_smem_bytes(bool fp8, int batch);
+int decode_ctas_per_sm(bool fp8, int batch);
+cudaError_t launch_decode(const DecodeParams& p, bool fp8, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+cudaError_t launch_scores(const ScoreParams& p, cudaStream_t stream);
+cudaError_t launch_wait_timeout(int32_t* err, int64_t timeout_ns, cudaStream_t stream);
+
+}  // namespace kvd

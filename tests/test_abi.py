@@ -1,0 +1,87 @@
+"""The C-ABI library on the host: it loads, exports what include/kvd.h declares, sizes
+pools by the closed form, and rejects bad arguments before touching a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_gqa_decode_kvd_gb300 as kvd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "kvd.h")).read()
+    return sorted(set(re.findall(r"KVD_API\s+[\w\s\*]*?\b(kvd_\w+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = kvd.load()
+    names = _declared()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(kvd.SYMBOLS) == names
+
+
+def test_pool_bytes_closed_form_matches_pages():
+    rows = [ln.split() for ln in open(os.path.join(GOLDEN, "kv_bytes.txt")) if ln.strip() and not ln.startswith("#")]
+    models = {"8B": (32, 8, 128), "70B": (80, 8, 128)}
+    for r in rows:
+        if r[0] == "per_token":
+            _, model, layers, kvh, dh, w, want = r
+            dtype = kvd.KVD_BF16 if w == "2" else kvd.KVD_FP8_E4M3
+            kv, _ = kvd.kvd_pool_bytes(int(layers), int(kvh), 1, dtype)   # one block = 16 tokens
+            assert kv // 16 == int(want)
+        else:
+            _, tokens, gib8, gib70 = r
+            for model, want in (("8B", gib8), ("70B", gib70)):
+                L, nkv, dh = models[model]
+                kv, _ = kvd.kvd_pool_bytes(L, nkv, int(tokens) // 16, kvd.KVD_BF16)
+                assert abs(kv / 2 ** 30 - float(want)) <= 0.005 + 1e-12   # the page prints two decimals
+
+
+def test_fp8_scale_bytes():
+    kv, sc = kvd.kvd_pool_bytes(80, 8, 8192, kvd.KVD_FP8_E4M3)
+    assert kv == 80 * 8192 * 16 * 8 * 128 * 2       # 1 byte per element, K and V
+    assert sc == 80 * 8192 * 8 * 2 * 16 * 4         # one fp32 per (token, head) for K and V
+
+
+def test_bad_descriptors_are_rejected():
+    with pytest.raises(kvd.KvdError) as e:
+        kvd.kvd_pool_bytes(32, 8, 16, kvd.KVD_BF16, d_h=64)
+    assert e.value.status == kvd.KVD_ERR_UNSUPPORTED
+    with pytest.raises(kvd.KvdError) as e:
+        kvd.kvd_pool_bytes(32, 8, 16, kvd.KVD_BF16, block_size=32)
+    assert e.value.status == kvd.KVD_ERR_UNSUPPORTED
+    for bad in [dict(num_layers=0), dict(n_kv=0), dict(num_blocks=0), dict(kv_dtype=7)]:
+        args = dict(num_layers=2, n_kv=8, num_blocks=16, kv_dtype=kvd.KVD_BF16)
+        args.update(bad)
+        with pytest.raises(kvd.KvdError) as e:
+            kvd.kvd_pool_bytes(**args)
+        assert e.value.status == kvd.KVD_ERR_INVALID
+
+
+def test_null_arguments_fail_before_any_launch():
+    lib = kvd.load()
+    P = ctypes.c_void_p
+    d = kvd._lib.PoolDesc(2, 8, 128, 16, 64, kvd.KVD_BF16)
+    h = P()
+    assert lib.kvd_pool_create(ctypes.byref(d), None, 1 << 20, None, 0, ctypes.byref(h)) == kvd.KVD_ERR_INVALID
+    assert lib.kvd_pool_create(ctypes.byref(d), P(16), 10, None, 0, ctypes.byref(h)) == kvd.KVD_ERR_NOMEM
+    assert lib.kvd_pool_create(ctypes.byref(d), P(8), 1 << 30, None, 0, ctypes.byref(h)) == kvd.KVD_ERR_INVALID
+    assert lib.kvd_decode_attn(None, 0, None, 32, None, 1, None, 1, 1, 0, None, 0.1, None, 0, None, 0,
+                               None, None, 0, None) == kvd.KVD_ERR_INVALID
+    assert lib.kvd_append_kv(None, 0, None, None, None, 1, None) == kvd.KVD_ERR_INVALID
+    assert lib.kvd_combine_splits(None, None, None, None, 1, 32, 8, 64, None, 0, None, None) == \
+        kvd.KVD_ERR_UNSUPPORTED
+    assert lib.kvd_combine_splits(None, None, None, None, 1, 72, 8, 128, None, 0, None, None) == \
+        kvd.KVD_ERR_UNSUPPORTED                      # g = 9 > 8
+    assert lib.kvd_combine_splits(None, None, None, None, 0, 32, 8, 128, None, 0, None, None) == kvd.KVD_OK
+    assert lib.kvd_accum_scores(None, 16, None, None, 1, 4, 1.0, None, 16, None) == kvd.KVD_ERR_INVALID
+    assert lib.kvd_get_device_error(None, None, None) == kvd.KVD_ERR_INVALID
+    assert lib.kvd_selftest_wait_timeout(None, 1000, None) == kvd.KVD_ERR_INVALID
+    assert kvd.status_string(kvd.KVD_ERR_OOB) == "device-detected index out of range"
