@@ -301,7 +301,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
         for (int kk = warp; kk < nseg; kk += kNcw) {
             const uint32_t kg = k + kk;
             const int s = kg % kStages;
-            if (!mbar_wait(&full[s], (kg / kStages) & 1u, abort_flag, kWaitNs)) {
+            // every lane observes the phase (acquire); the outcome is made warp-uniform so a
+            // timeout racing with completion cannot split the warp before the MMAs
+            const bool got = mbar_wait(&full[s], (kg / kStages) & 1u, abort_flag, kWaitNs);
+            if (!__all_sync(kFull, got)) {
                 if (lane == 0) {
                     report(p.err, KVD_ERR_TIMEOUT);
                     *abort_flag = 1;
