@@ -65,12 +65,12 @@ WsLayout ws_layout(int units, int nsplit, int g) {
 
 // Split count: enough CTAs to fill every SM at the kernel's occupancy, but no CTA
 // with fewer than kMinBlocksPerSplit blocks of the (upper-bound) total work.
-int plan_splits(const kvd_pool* pool, int batch, int max_seq_len) {
+int plan_splits(const kvd_pool* pool, int batch, int max_seq_len, int g) {
     const bool fp8 = pool->desc.kv_dtype == KVD_FP8_E4M3;
     const int64_t nblk = (static_cast<int64_t>(max_seq_len) + kvd::kBs - 1) / kvd::kBs;
     const int64_t total = nblk * batch * pool->desc.n_kv;
     const int64_t by_work = (total + kMinBlocksPerSplit - 1) / kMinBlocksPerSplit;
-    const int64_t by_sms = static_cast<int64_t>(pool->num_sms) * kvd::decode_ctas_per_sm(fp8, batch);
+    const int64_t by_sms = static_cast<int64_t>(pool->num_sms) * kvd::decode_ctas_per_sm(fp8, batch, g);
     int64_t s = by_work < by_sms ? by_work : by_sms;
     return static_cast<int>(s < 1 ? 1 : s);
 }
@@ -188,7 +188,7 @@ kvd_status kvd_decode_workspace_bytes(const kvd_pool* pool, int n_q, int batch, 
     kvd_status st = check_decode_shape(pool, n_q, batch, max_seq_len);
     if (st != KVD_OK) return st;
     if (num_splits < 0 || !bytes_out) return KVD_ERR_INVALID;
-    const int S = num_splits > 0 ? num_splits : plan_splits(pool, batch, max_seq_len);
+    const int S = num_splits > 0 ? num_splits : plan_splits(pool, batch, max_seq_len, n_q / pool->desc.n_kv);
     const WsLayout w = ws_layout(batch * pool->desc.n_kv, S, n_q / pool->desc.n_kv);
     if (splits_out) *splits_out = S;
     *bytes_out = w.total;
@@ -212,7 +212,7 @@ kvd_status kvd_decode_attn(const kvd_pool* pool, int layer, const void* q, int n
         return KVD_ERR_INVALID;
     const int g = n_q / pool->desc.n_kv;
     const int U = batch * pool->desc.n_kv;
-    const int S = num_splits > 0 ? num_splits : plan_splits(pool, batch, max_seq_len);
+    const int S = num_splits > 0 ? num_splits : plan_splits(pool, batch, max_seq_len, g);
     const WsLayout w = ws_layout(U, S, g);
     if (workspace_bytes < w.total) return KVD_ERR_NOMEM;
     uint8_t* ws = static_cast<uint8_t*>(workspace);

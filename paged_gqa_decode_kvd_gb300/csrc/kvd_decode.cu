@@ -34,16 +34,23 @@ namespace kvd {
 
 constexpr int kNcw = 4;                    // consumer warps per CTA
 constexpr int kThreads = (kNcw + 1) * 32;  // + 1 producer warp
-constexpr int kStages = 6;
 constexpr int kMergeStride = 132;          // floats per head row in the merge buffer (bank spread)
-constexpr int kMergeFloats = kMaxG * kMergeStride + 2 * kMaxG;
 constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s
+
+// Floats of one warp's merge area: O [g][kMergeStride], then m [kMaxG], then l [kMaxG].
+__host__ __device__ inline int merge_floats(int g) { return g * kMergeStride + 2 * kMaxG; }
 
 template <bool FP8>
 struct Cfg {
     static constexpr int kTile = FP8 ? kTileFp8 : kTileBf16;
     static constexpr int kRecord = 2 * kTile;
     static constexpr int kStage = FP8 ? kRecord + 2 * kBs * 4 : kRecord;
+    // Stage k%kStages is consumed by warp (k - segment start) % kNcw.  With kStages a
+    // multiple of kNcw every reuse of a stage inside a segment belongs to the same warp,
+    // and across segments the merge barrier orders it, so a consumer never waits on a
+    // phase whose predecessor is still incomplete (mbarrier parity cannot alias).
+    static constexpr int kStages = FP8 ? 12 : 8;
+    static_assert(kStages % kNcw == 0, "stages must be a multiple of the consumer warps");
 };
 
 struct Smem {
@@ -51,7 +58,8 @@ struct Smem {
 };
 
 template <bool FP8>
-__host__ __device__ inline Smem smem_layout(int batch) {
+__host__ __device__ inline Smem smem_layout(int batch, int g) {
+    constexpr int kStages = Cfg<FP8>::kStages;
     Smem s;
     int o = 0;
     s.ring_off = o;
@@ -64,7 +72,7 @@ __host__ __device__ inline Smem smem_layout(int batch) {
     o += kStages * 4;
     o = (o + 15) & ~15;
     s.merge_off = o;
-    o += kNcw * kMergeFloats * 4;
+    o += kNcw * merge_floats(g) * 4;
     s.pref_off = o;
     o += (batch + 1) * 4;
     s.abort_off = o;
@@ -106,7 +114,9 @@ __device__ __forceinline__ Segment find_segment(const int* pref, int B, int n_kv
 template <bool FP8>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    const Smem L = smem_layout<FP8>(p.B);
+    constexpr int kStages = Cfg<FP8>::kStages;
+    const Smem L = smem_layout<FP8>(p.B, p.g);
+    const int kMergeFloats = merge_floats(p.g);
     uint8_t* ring = smem + L.ring_off;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full_off);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty_off);
@@ -462,16 +472,20 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
         #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int d0 = 16 * i + gid, d1 = d0 + 8;
-            mb[h0 * kMergeStride + d0] = o[i][0];
-            mb[h1 * kMergeStride + d0] = o[i][1];
-            mb[h0 * kMergeStride + d1] = o[i][2];
-            mb[h1 * kMergeStride + d1] = o[i][3];
+            if (h0 < g) {
+                mb[h0 * kMergeStride + d0] = o[i][0];
+                mb[h0 * kMergeStride + d1] = o[i][2];
+            }
+            if (h1 < g) {
+                mb[h1 * kMergeStride + d0] = o[i][1];
+                mb[h1 * kMergeStride + d1] = o[i][3];
+            }
         }
         if (gid == 0) {
-            mb[kMaxG * kMergeStride + h0] = m0;
-            mb[kMaxG * kMergeStride + h1] = m1;
-            mb[kMaxG * kMergeStride + kMaxG + h0] = s0;
-            mb[kMaxG * kMergeStride + kMaxG + h1] = s1;
+            mb[g * kMergeStride + h0] = m0;
+            mb[g * kMergeStride + h1] = m1;
+            mb[g * kMergeStride + kMaxG + h0] = s0;
+            mb[g * kMergeStride + kMaxG + h1] = s1;
         }
         named_barrier(1, kNcw * 32);
         const int slot = u + cta;
@@ -479,14 +493,14 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
             const int h = idx / kDh, d = idx % kDh;
             float M = -INFINITY;
             #pragma unroll
-            for (int w = 0; w < kNcw; ++w) M = fmaxf(M, merge[w * kMergeFloats + kMaxG * kMergeStride + h]);
+            for (int w = 0; w < kNcw; ++w) M = fmaxf(M, merge[w * kMergeFloats + g * kMergeStride + h]);
             float Ls = 0.f, acc = 0.f;
             if (M != -INFINITY) {
                 #pragma unroll
                 for (int w = 0; w < kNcw; ++w) {
                     const float* mw = merge + w * kMergeFloats;
-                    const float e = ex2(mw[kMaxG * kMergeStride + h] - M);
-                    Ls += mw[kMaxG * kMergeStride + kMaxG + h] * e;
+                    const float e = ex2(mw[g * kMergeStride + h] - M);
+                    Ls += mw[g * kMergeStride + kMaxG + h] * e;
                     acc += mw[h * kMergeStride + d] * e;
                 }
             }
@@ -504,16 +518,16 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
     }
 }
 
-size_t decode_smem_bytes(bool fp8, int batch) {
-    return fp8 ? smem_layout<true>(batch).total : smem_layout<false>(batch).total;
+size_t decode_smem_bytes(bool fp8, int batch, int g) {
+    return fp8 ? smem_layout<true>(batch, g).total : smem_layout<false>(batch, g).total;
 }
 
 template <bool FP8>
 static cudaError_t ensure_smem_attr();
 
 template <bool FP8>
-static int ctas_per_sm_impl(int batch) {
-    const int smem = smem_layout<FP8>(batch).total;
+static int ctas_per_sm_impl(int batch, int g) {
+    const int smem = smem_layout<FP8>(batch, g).total;
     if (ensure_smem_attr<FP8>() != cudaSuccess) return 1;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<FP8>, kThreads, smem) != cudaSuccess)
@@ -521,7 +535,9 @@ static int ctas_per_sm_impl(int batch) {
     return n > 0 ? n : 1;
 }
 
-int decode_ctas_per_sm(bool fp8, int batch) { return fp8 ? ctas_per_sm_impl<true>(batch) : ctas_per_sm_impl<false>(batch); }
+int decode_ctas_per_sm(bool fp8, int batch, int g) {
+    return fp8 ? ctas_per_sm_impl<true>(batch, g) : ctas_per_sm_impl<false>(batch, g);
+}
 
 // Raise the kernel's dynamic shared-memory limit once per device to the largest
 // layout any batch size can need (batch ≤ kMaxBatch).
@@ -533,13 +549,13 @@ static cudaError_t ensure_smem_attr() {
     if (e != cudaSuccess) return e;
     if (done_for_device == dev) return cudaSuccess;
     e = cudaFuncSetAttribute(decode_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_layout<FP8>(kMaxBatch).total);
+                             smem_layout<FP8>(kMaxBatch, kMaxG).total);
     if (e == cudaSuccess) done_for_device = dev;
     return e;
 }
 
 cudaError_t launch_decode(const DecodeParams& p, bool fp8, cudaStream_t stream) {
-    const size_t smem = decode_smem_bytes(fp8, p.B);
+    const size_t smem = decode_smem_bytes(fp8, p.B, p.g);
     cudaError_t e = fp8 ? ensure_smem_attr<true>() : ensure_smem_attr<false>();
     if (e != cudaSuccess) return e;
     if (fp8)

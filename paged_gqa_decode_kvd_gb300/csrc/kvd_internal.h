@@ -69,8 +69,8 @@ struct ScoreParams {
 };
 
 cudaError_t launch_append(const AppendParams& p, bool fp8, cudaStream_t stream);
-size_t decode_smem_bytes(bool fp8, int batch);
-int decode_ctas_per_sm(bool fp8, int batch);
+size_t decode_smem_bytes(bool fp8, int batch, int g);
+int decode_ctas_per_sm(bool fp8, int batch, int g);
 cudaError_t launch_decode(const DecodeParams& p, bool fp8, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 cudaError_t launch_scores(const ScoreParams& p, cudaStream_t stream);
