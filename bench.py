@@ -238,13 +238,11 @@ def gpu_arm(args, w, rank, world, local):
     graph = st.capture()
     stream = torch.cuda.current_stream(dev)
 
-    for _ in range(args.warmup):
-        graph.replay()
-    torch.cuda.synchronize()
-    barrier(world)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
+        for _ in range(args.warmup):
+            graph.replay()
         torch.cuda.synchronize()
         barrier(world)
         t0.record(stream)
@@ -385,8 +383,8 @@ def reference_arm(args, w, rank, world):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="llama8b")
     ap.add_argument("--num-splits", type=int, default=0)
