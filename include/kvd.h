@@ -155,6 +155,33 @@ KVD_API kvd_status kvd_decode_attn(const kvd_pool* pool, int layer, const void* 
                            void* out, int out_dtype, float* lse_out,
                            float* logits_out, int64_t logits_stride, void* stream);
 
+/* Size of the fixed device scratch array used by kvd_decode_attn_noalloc: 16 MiB, held on
+ * every GPU that loads the library until the process exits. */
+#define KVD_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* kvd_decode_attn for callers that may not allocate device memory (for example a host
+ * framework whose own allocator owns all device memory, or a latency-critical loop that
+ * cannot take cudaMalloc's implicit synchronisation).  The pages describe no such entry
+ * point; it has no counterpart in them.
+ * Same arguments and results as kvd_decode_attn, minus the workspace: the split partials
+ * go to a file-scope device array of KVD_NOALLOC_SCRATCH_BYTES bytes inside the library.
+ * It allocates nothing (no cudaMalloc, no cudaFree, no allocating library routine).
+ *  - A shape whose workspace (kvd_decode_workspace_bytes) exceeds KVD_NOALLOC_SCRATCH_BYTES
+ *    is rejected with KVD_ERR_NOMEM before any launch; `out` may not be NULL.
+ *  - The first call on a device, with that device current, looks up the array's device
+ *    address (cudaGetSymbolAddress) once for that device; make that first call before any
+ *    stream capture begins.
+ *  - Every call on a device shares the one array, and it keeps the previous call's
+ *    contents; every partial and unit-table entry is written before it is read, so nothing
+ *    needs clearing.  Calls whose kernels overlap on the GPU (e.g. on two streams at once)
+ *    race on the array: serialise them. */
+KVD_API kvd_status kvd_decode_attn_noalloc(const kvd_pool* pool, int layer, const void* q, int n_q,
+                                           const int32_t* block_table, int max_blocks_per_seq,
+                                           const int32_t* seq_lens, int batch, int max_seq_len, int num_splits,
+                                           const uint16_t* retain_mask, float softmax_scale,
+                                           void* out, int out_dtype, float* lse_out,
+                                           float* logits_out, int64_t logits_stride, void* stream);
+
 /* Merge split partials by log-sum-exp.  For unit u = b·n_kv + h/g and head h:
  * LSE = log Σ_s exp(lse_s), out = Σ_s exp(lse_s − LSE)·o_s over the unit_count[u] slots
  * starting at unit_first[u] of part_o f32 [slots][g][d_h] and part_lse f32 [slots][g]

@@ -20,11 +20,13 @@ from ._lib import (  # noqa: F401
     KVD_ERR_TIMEOUT,
     KVD_ERR_UNSUPPORTED,
     SYMBOLS,
+    NOALLOC_SCRATCH_BYTES,
     KvdError,
     kvd_accum_scores,
     kvd_append_kv,
     kvd_combine_splits,
     kvd_decode_attn,
+    kvd_decode_attn_noalloc,
     kvd_decode_workspace_bytes,
     kvd_get_device_error,
     kvd_pool_bytes,

@@ -17,8 +17,9 @@ KVD_BF16, KVD_FP8_E4M3, KVD_F32 = 0, 1, 2
 SYMBOLS = [
     "kvd_status_string", "kvd_pool_bytes", "kvd_pool_create", "kvd_pool_destroy", "kvd_append_kv",
     "kvd_decode_workspace_bytes", "kvd_decode_attn", "kvd_combine_splits", "kvd_accum_scores",
-    "kvd_get_device_error", "kvd_selftest_wait_timeout",
+    "kvd_get_device_error", "kvd_selftest_wait_timeout", "kvd_decode_attn_noalloc",
 ]
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class KvdError(RuntimeError):
@@ -74,6 +75,8 @@ def load(build_if_missing: bool = True):
     lib.kvd_get_device_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
     lib.kvd_selftest_wait_timeout.restype = i32
     lib.kvd_selftest_wait_timeout.argtypes = [P, i64, P]
+    lib.kvd_decode_attn_noalloc.restype = i32
+    lib.kvd_decode_attn_noalloc.argtypes = [P, i32, P, i32, P, i32, P, i32, i32, i32, P, f32, P, i32, P, P, i64, P]
     _lib = lib
     return lib
 
@@ -171,3 +174,17 @@ def kvd_get_device_error(handle, stream=None) -> int:
 
 def kvd_selftest_wait_timeout(handle, timeout_ns, stream=None):
     _check("kvd_selftest_wait_timeout", load().kvd_selftest_wait_timeout(handle, int(timeout_ns), _stream(stream)))
+
+
+def kvd_decode_attn_noalloc(handle, layer, q, block_table, seq_lens, max_seq_len, out, num_splits=0,
+                            retain_mask=None, softmax_scale=None, lse_out=None, logits_out=None, stream=None):
+    """kvd_decode_attn without a workspace argument: the library's fixed device scratch array is used."""
+    batch, n_q, d_h = q.shape
+    if softmax_scale is None:
+        softmax_scale = d_h ** -0.5
+    out_dtype = KVD_F32 if out is not None and out.element_size() == 4 else KVD_BF16
+    lstride = 0 if logits_out is None else logits_out.shape[-1]
+    _check("kvd_decode_attn_noalloc", load().kvd_decode_attn_noalloc(
+        handle, layer, _ptr(q), n_q, _ptr(block_table), block_table.shape[1], _ptr(seq_lens), batch,
+        int(max_seq_len), int(num_splits), _ptr(retain_mask), float(softmax_scale), _ptr(out), out_dtype,
+        _ptr(lse_out), _ptr(logits_out), lstride, _stream(stream)))

@@ -1,0 +1,64 @@
+// kvd_noalloc.cu — decode attention that allocates nothing: its split scratch lives in a
+// fixed-size array in the library's own device image.
+//
+// Some callers may not allocate device memory themselves: a host framework that owns
+// every byte of device memory through its own arena and forbids raw allocations by
+// plugins, or a latency-critical serving loop that cannot afford cudaMalloc's implicit
+// device synchronisation.  kvd_decode_attn_noalloc lets them run decode attention with
+// only their inputs and outputs.  The scratch array below is created when the library's
+// device code is loaded on a GPU and stays resident on every GPU that loads the library
+// until the process exits.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/kvd.h"
+
+namespace {
+
+// Split partials and unit tables of one kvd_decode_attn call (its "workspace").
+__device__ __align__(256) unsigned char g_noalloc_scratch[KVD_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once per device.
+kvd_status scratch_for_current_device(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KVD_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return KVD_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return KVD_ERR_CUDA;
+        }
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return KVD_OK;
+}
+
+}  // namespace
+
+extern "C" kvd_status kvd_decode_attn_noalloc(const kvd_pool* pool, int layer, const void* q, int n_q,
+                                              const int32_t* block_table, int max_blocks_per_seq,
+                                              const int32_t* seq_lens, int batch, int max_seq_len, int num_splits,
+                                              const uint16_t* retain_mask, float softmax_scale, void* out,
+                                              int out_dtype, float* lse_out, float* logits_out,
+                                              int64_t logits_stride, void* stream) {
+    if (!out && batch > 0) return KVD_ERR_INVALID;  // the partials would be unreachable
+    int splits = 0;
+    size_t need = 0;
+    kvd_status st = kvd_decode_workspace_bytes(pool, n_q, batch, max_seq_len, num_splits, &splits, &need);
+    if (st != KVD_OK) return st;
+    if (need > static_cast<size_t>(KVD_NOALLOC_SCRATCH_BYTES)) return KVD_ERR_NOMEM;
+    void* scratch = nullptr;
+    st = scratch_for_current_device(&scratch);
+    if (st != KVD_OK) return st;
+    return kvd_decode_attn(pool, layer, q, n_q, block_table, max_blocks_per_seq, seq_lens, batch, max_seq_len,
+                           splits, retain_mask, softmax_scale, scratch, static_cast<size_t>(KVD_NOALLOC_SCRATCH_BYTES),
+                           out, out_dtype, lse_out, logits_out, logits_stride, stream);
+}
