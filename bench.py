@@ -80,20 +80,29 @@ class ClockSampler:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.out = open(self.path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
-                 "-i", str(self.gpu)], stdout=self.out, stderr=subprocess.DEVNULL)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                   "-i", str(self.gpu)]
+            import shutil
+
+            if shutil.which("stdbuf"):      # line-buffer so no sample is lost when the sampler stops
+                cmd = ["stdbuf", "-oL"] + cmd
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
         except Exception:
             self.proc = None
         return self
 
     def __exit__(self, *a):
         if self.proc is not None:
-            self.proc.terminate()
+            import signal
+
+            time.sleep(0.25)
+            self.proc.send_signal(signal.SIGINT)
             try:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
+                self.proc.wait()
             self.out.close()
 
     def summary(self) -> dict:
@@ -102,7 +111,7 @@ class ClockSampler:
         rows = []
         for ln in open(self.path):
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) >= 9:
+            if len(parts) >= 8:
                 rows.append(parts)
         os.unlink(self.path)
         if not rows:
@@ -145,9 +154,15 @@ def barrier(world: int):
 
 # ------------------------------------------------------------------ the GPU arm
 class Step:
-    """Device-resident state of one workload and its L-layer decode step."""
+    """Device-resident state of one workload and its L-layer decode step.
+
+    A workload with `steps` > 1 (the tiered one) grows every request's context by one
+    token per decode step; step t appends position ctx0 + t.  One CUDA graph is captured
+    per step index and the timed loop cycles through them.  With scores on, each layer
+    also writes its logits and adds its share of the importance score."""
 
     def __init__(self, w, dev, num_splits: int = 0):
+        import numpy as np
         import torch
 
         import paged_gqa_decode_kvd_gb300 as kvd
@@ -158,58 +173,79 @@ class Step:
         self.pool = kvd.KVPool(w.L, w.n_kv, w.num_blocks(), kvd.KVD_FP8_E4M3 if self.fp8 else kvd.KVD_BF16,
                                device=dev)
         bt = w.block_table()
-        self.bt_cpu = bt
         self.bt = bt.to(dev)
-        lens = w.seq_lens(0)
-        self.lens = lens
-        self.max_len = max(lens)
-        self.seq = torch.tensor(lens, dtype=torch.int32, device=dev)
+        self.nsteps = w.steps
+        self.lens = [w.seq_lens(t) for t in range(self.nsteps)]
+        self.max_len = max(max(x) for x in self.lens)
         ret = w.retain_mask(bt)
         self.retain = None
         if ret is not None:
-            import numpy as np
-
             self.retain = torch.from_numpy(ret.numpy().astype(np.uint16).view(np.int16)).to(dev)
-        # prefill every layer's cache through the append entry point (setup, untimed)
+        # prefill: every position before step 0's append, every layer (setup, untimed)
+        first = [c - 1 for c in self.lens[0]]
         for layer in range(w.L):
             for b in range(w.batch):
-                n = lens[b] - 1
-                if n > 0:
-                    k, v = w.kv(layer, b, 0, n, dev)
+                if first[b] > 0:
+                    k, v = w.kv(layer, b, 0, first[b], dev)
                     kvd.kvd_append_kv(self.pool.handle, layer, k.contiguous(), v.contiguous(),
-                                      w.slot_mapping(b, 0, n, bt).to(dev))
-        # per-step inputs: the new token of every request (position len-1) and q, for every layer
-        pos = w.append_pos(0)
-        self.slots = torch.cat([w.slot_mapping(b, pos[b], pos[b] + 1, bt) for b in range(w.batch)]).to(dev)
-        kn, vn = [], []
-        for layer in range(w.L):
-            ks, vs = zip(*[w.kv(layer, b, pos[b], pos[b] + 1, dev) for b in range(w.batch)])
-            kn.append(torch.cat(ks))
-            vn.append(torch.cat(vs))
-        self.k_new = torch.stack(kn).contiguous()          # [L][B][n_kv][128]
-        self.v_new = torch.stack(vn).contiguous()
-        self.q = torch.stack([w.q(layer, 0, dev) for layer in range(w.L)]).contiguous()   # [L][B][n_q][128]
+                                      w.slot_mapping(b, 0, first[b], bt).to(dev))
+        # per-step inputs: the appended token of every request, q, context lengths
+        self.seq, self.slots, self.k_new, self.v_new, self.q = [], [], [], [], []
+        for t in range(self.nsteps):
+            pos = w.append_pos(t)
+            self.seq.append(torch.tensor(self.lens[t], dtype=torch.int32, device=dev))
+            self.slots.append(torch.cat([w.slot_mapping(b, pos[b], pos[b] + 1, bt) for b in range(w.batch)]).to(dev))
+            kn, vn = [], []
+            for layer in range(w.L):
+                ks, vs = zip(*[w.kv(layer, b, pos[b], pos[b] + 1, dev) for b in range(w.batch)])
+                kn.append(torch.cat(ks))
+                vn.append(torch.cat(vs))
+            self.k_new.append(torch.stack(kn).contiguous())        # [L][B][n_kv][128]
+            self.v_new.append(torch.stack(vn).contiguous())
+            self.q.append(torch.stack([w.q(layer, t, dev) for layer in range(w.L)]).contiguous())
         self.out = torch.empty(w.L, w.batch, w.n_q, 128, dtype=torch.bfloat16, device=dev)
         self.splits, nbytes = kvd.kvd_decode_workspace_bytes(self.pool.handle, w.n_q, w.batch, self.max_len,
                                                              num_splits)
-        self.num_splits = self.splits
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-        self.launches_per_step = 3 * w.L
+        self.scores = None
+        if w.scores:
+            self.lse = torch.empty(w.batch, w.n_q, dtype=torch.float32, device=dev)
+            self.logits = torch.empty(w.batch, w.n_q, self.max_len, dtype=torch.float32, device=dev)
+            self.scores = torch.zeros(w.batch, self.max_len, dtype=torch.float32, device=dev)
+        self.launches_per_step = (4 if w.scores else 3) * w.L
         torch.cuda.synchronize()
         err = kvd.kvd_get_device_error(self.pool.handle)
         if err:
             raise RuntimeError(f"device error during setup: {kvd.status_string(err)}")
 
-    def run(self, stream=None):
-        kvd = self.kvd
-        for layer in range(self.L):
-            kvd.kvd_append_kv(self.pool.handle, layer, self.k_new[layer], self.v_new[layer], self.slots, stream)
-            kvd.kvd_decode_attn(self.pool.handle, layer, self.q[layer], self.bt, self.seq, self.max_len, self.ws,
-                                self.out[layer], num_splits=self.num_splits, retain_mask=self.retain, stream=stream)
+    def kv_bytes(self, t: int) -> int:
+        w = self.w
+        return int(2 * w.L * w.n_kv * w.d_h * w.w_kv * sum(self.lens[t]))
 
-    def decode_only(self, layer, stream=None):
-        self.kvd.kvd_decode_attn(self.pool.handle, layer, self.q[layer], self.bt, self.seq, self.max_len, self.ws,
-                                 None, num_splits=self.num_splits, retain_mask=self.retain, stream=stream)
+    def scale_bytes(self, t: int) -> int:
+        w = self.w
+        return 0 if w.kv_dtype == "bf16" else int(2 * w.L * w.n_kv * 4 * sum(self.lens[t]))
+
+    def run(self, t: int = 0, stream=None):
+        kvd, w = self.kvd, self.w
+        inv = 1.0 / (w.L * w.n_q)
+        for layer in range(self.L):
+            kvd.kvd_append_kv(self.pool.handle, layer, self.k_new[t][layer], self.v_new[t][layer], self.slots[t],
+                              stream)
+            if self.scores is None:
+                kvd.kvd_decode_attn(self.pool.handle, layer, self.q[t][layer], self.bt, self.seq[t], self.max_len,
+                                    self.ws, self.out[layer], num_splits=self.splits, retain_mask=self.retain,
+                                    stream=stream)
+            else:
+                kvd.kvd_decode_attn(self.pool.handle, layer, self.q[t][layer], self.bt, self.seq[t], self.max_len,
+                                    self.ws, self.out[layer], num_splits=self.splits, retain_mask=self.retain,
+                                    lse_out=self.lse, logits_out=self.logits, stream=stream)
+                kvd.kvd_accum_scores(self.logits, self.lse, self.seq[t], inv, self.scores, stream=stream)
+
+    def decode_only(self, layer, t: int = 0, stream=None):
+        self.kvd.kvd_decode_attn(self.pool.handle, layer, self.q[t][layer], self.bt, self.seq[t], self.max_len,
+                                 self.ws, None, num_splits=self.splits, retain_mask=self.retain,
+                                 logits_out=None if self.scores is None else self.logits, stream=stream)
 
     def capture(self):
         import torch
@@ -217,14 +253,17 @@ class Step:
         s = torch.cuda.Stream(device=self.dev)
         s.wait_stream(torch.cuda.current_stream(self.dev))
         with torch.cuda.stream(s):
-            self.run()
+            self.run(0)
         torch.cuda.current_stream(self.dev).wait_stream(s)
         torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            self.run()
+        graphs = []
+        for t in range(self.nsteps):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.run(t)
+            graphs.append(g)
         torch.cuda.synchronize()
-        return g
+        return graphs
 
 
 def gpu_arm(args, w, rank, world, local):
@@ -234,20 +273,21 @@ def gpu_arm(args, w, rank, world, local):
     torch.cuda.set_device(dev)
     peaks = measured_peaks()
     st = Step(w, dev, args.num_splits)
-    kv_bytes = w.kv_bytes_per_step()
-    graph = st.capture()
+    graphs = st.capture()
     stream = torch.cuda.current_stream(dev)
+    # closed-form KV bytes of the timed steps (step t of the workload = graph t % steps)
+    kv_bytes = sum(st.kv_bytes(t % st.nsteps) for t in range(args.steps)) / args.steps
 
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
-        for _ in range(args.warmup):
-            graph.replay()
+        for i in range(args.warmup):
+            graphs[i % st.nsteps].replay()
         torch.cuda.synchronize()
         barrier(world)
         t0.record(stream)
-        for _ in range(args.steps):
-            graph.replay()
+        for i in range(args.steps):
+            graphs[i % st.nsteps].replay()
         t1.record(stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -270,7 +310,9 @@ def gpu_arm(args, w, rank, world, local):
         torch.cuda.synchronize()
         durs += [a.elapsed_time(b) for a, b in ev]
     dec_ms = statistics.mean(durs)
-    layer_bytes = kv_bytes / w.L
+    # algorithmic bytes one decode launch must read: the K/V elements of every attended
+    # position, plus for FP8 the per-(token, head) K and V scales
+    layer_bytes = (st.kv_bytes(0) + st.scale_bytes(0)) / w.L
     achieved = layer_bytes / (dec_ms * 1e-3) / 1e9
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": args.traffic,
@@ -278,9 +320,9 @@ def gpu_arm(args, w, rank, world, local):
             "bytes_per_launch": layer_bytes, "launch_ms": round(dec_ms, 5)}
 
     # end to end: per-step inputs from pinned host memory, outputs back to pinned host memory
-    h_q = st.q.cpu().pin_memory()
-    h_k = st.k_new.cpu().pin_memory()
-    h_v = st.v_new.cpu().pin_memory()
+    h_q = st.q[0].cpu().pin_memory()
+    h_k = st.k_new[0].cpu().pin_memory()
+    h_v = st.v_new[0].cpu().pin_memory()
     h_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
     e2e_steps = max(1, min(args.steps, 10))
     torch.cuda.synchronize()
@@ -289,17 +331,17 @@ def gpu_arm(args, w, rank, world, local):
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
-        st.q.copy_(h_q, non_blocking=True)
-        st.k_new.copy_(h_k, non_blocking=True)
-        st.v_new.copy_(h_v, non_blocking=True)
-        graph.replay()
+        st.q[0].copy_(h_q, non_blocking=True)
+        st.k_new[0].copy_(h_k, non_blocking=True)
+        st.v_new[0].copy_(h_v, non_blocking=True)
+        graphs[0].replay()
         h_out.copy_(st.out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
     h2d = (h_q.numel() * h_q.element_size() + h_k.numel() * h_k.element_size() + h_v.numel() * h_v.element_size())
     d2h = h_out.numel() * h_out.element_size()
-    e2e = {"value": round(kv_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+    e2e = {"value": round(st.kv_bytes(0) * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
 
     line = {
@@ -309,7 +351,9 @@ def gpu_arm(args, w, rank, world, local):
         "data": "synthetic (seeded counter-hash generator)",
         "config": {"workload": f"{w.name}: {w.description}", "layers": w.L, "batch": w.batch, "n_q": w.n_q,
                    "n_kv": w.n_kv, "d_h": w.d_h, "context": w.seq_lens(0)[:4] if w.batch > 4 else w.seq_lens(0),
-                   "kv_bytes_per_step": kv_bytes, "num_splits": st.splits, "seed": w.seed,
+                   "kv_bytes_per_step": kv_bytes, "fp8_scale_bytes_per_step": st.scale_bytes(0),
+                   "num_splits": st.splits, "seed": w.seed,
+                   "decode_steps_cycled": st.nsteps, "scores": bool(w.scores),
                    "l2": "inputs larger than L2 (KV pool streamed every step)", "parallelism": f"replicas x{world}"},
         "steps_per_s": round(1e3 / ms_per_step, 2),
         "hbm_frac_of_measured": round(value / world / peaks["hbm_gbs"], 4),
@@ -388,6 +432,7 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="llama8b")
     ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling captures)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -401,6 +446,9 @@ def main(argv=None):
 
     rank, world, local = dist_env()
     w = get(args.workload, args.seed)
+    if args.layers:
+        w.L = args.layers
+        w.description += f" [reduced to {args.layers} layers for profiling]"
     if world > 1:
         import torch.distributed as dist
 

@@ -31,18 +31,19 @@
  *    Anything else valid returns KVD_ERR_UNSUPPORTED before any launch.
  *
  * Pool layout (per layer ℓ, physical block p, KV head h)
- *  - One record of 2·16·128 elements: the K tile, then the V tile, at byte
- *    offset ((ℓ·num_blocks + p)·n_kv + h)·record_bytes, record_bytes = 8192
- *    (BF16) or 4096 (FP8).  A tile holds token t ∈ [0,16) (slot offset within
- *    the block) × dim d ∈ [0,128), permuted into tensor-core fragment order:
+ *  - One record per (ℓ, p, h) at byte offset ((ℓ·num_blocks + p)·n_kv + h)·record_bytes:
+ *    the K tile, then the V tile (2·16·128 elements), then for FP8 the 32 fp32
+ *    scales [2][16] (index 0 = K, 1 = V; last index = slot offset t).
+ *    record_bytes = 8192 (BF16) or 4096 + 128 = 4224 (FP8), so one (block, head)
+ *    is a single contiguous, 16-byte aligned copy.  A tile holds token t ∈ [0,16)
+ *    (slot offset within the block) × dim d ∈ [0,128), permuted into tensor-core
+ *    fragment order:
  *      K tile: i = d/16, c = d%16, lane = 4·(t%8) + (c%8)/2,
  *              e = (c%2) + 2·(t/8) + 4·(c/8)
  *      V tile: i = d/16, r = d%16, lane = 4·(r%8) + (t%8)/2,
  *              e = (t%2) + 2·(r/8) + 4·(t/8)
  *      BF16 element index within the tile: (i·32 + lane)·8 + e
  *      FP8  byte index within the tile:   ((i/2)·32 + lane)·16 + (i%2)·8 + e
- *  - FP8 scales: fp32 [L][num_blocks][n_kv][2][16] (index 0 = K, 1 = V; the
- *    last index is the slot offset t).
  *  - The pool is written only through kvd_append_kv.
  */
 #ifndef KVD_H
@@ -91,17 +92,17 @@ typedef struct kvd_pool kvd_pool;  /* opaque */
 /* Readable name of a status code (static string). */
 KVD_API const char* kvd_status_string(kvd_status s);
 
-/* Bytes the pool needs: kv_bytes = L·num_blocks·n_kv·2·block_size·d_h·w_kv, i.e. the
- * closed form 2·L·n_kv·d_h·w_kv bytes per token times num_blocks·block_size tokens;
- * scale_bytes = L·num_blocks·n_kv·2·block_size·4 for FP8, else 0.  Host only. */
-KVD_API kvd_status kvd_pool_bytes(const kvd_pool_desc* desc, size_t* kv_bytes, size_t* scale_bytes);
+/* Bytes of a pool.  kv_bytes = L·num_blocks·n_kv·2·block_size·d_h·w_kv, the closed form
+ * 2·L·n_kv·d_h·w_kv bytes per token times num_blocks·block_size tokens (K and V elements
+ * only); pool_bytes = kv_bytes plus, for FP8, L·num_blocks·n_kv·2·block_size·4 bytes of
+ * scales: the size of the buffer kvd_pool_create needs.  Host only. */
+KVD_API kvd_status kvd_pool_bytes(const kvd_pool_desc* desc, size_t* pool_bytes, size_t* kv_bytes);
 
-/* Wrap caller memory as a pool.  kv_mem (kv_len bytes) and scale_mem (scale_len bytes,
- * NULL for BF16) are device buffers aligned to 16 bytes and at least kvd_pool_bytes large,
- * else KVD_ERR_NOMEM / KVD_ERR_INVALID.  Allocates the handle and a 4-byte device error
- * word on the current device (KVD_ERR_CUDA if that fails).  *out is set on success. */
-KVD_API kvd_status kvd_pool_create(const kvd_pool_desc* desc, void* kv_mem, size_t kv_len,
-                           void* scale_mem, size_t scale_len, kvd_pool** out);
+/* Wrap caller memory as a pool.  mem is a device buffer of len ≥ pool_bytes bytes,
+ * 16-byte aligned (else KVD_ERR_NOMEM / KVD_ERR_INVALID).  Allocates the handle and a
+ * 4-byte device error word on the current device (KVD_ERR_CUDA if that fails).  *out is
+ * set on success. */
+KVD_API kvd_status kvd_pool_create(const kvd_pool_desc* desc, void* mem, size_t len, kvd_pool** out);
 
 /* Free the handle and its error word (not the caller's pool memory).  NULL is a no-op. */
 KVD_API void kvd_pool_destroy(kvd_pool* pool);

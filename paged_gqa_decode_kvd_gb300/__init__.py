@@ -46,14 +46,14 @@ class KVPool:
         import torch
 
         self.num_layers, self.n_kv, self.num_blocks, self.kv_dtype = num_layers, n_kv, num_blocks, kv_dtype
-        kv_bytes, sc_bytes = kvd_pool_bytes(num_layers, n_kv, num_blocks, kv_dtype)
-        self.kv = torch.empty(kv_bytes, dtype=torch.uint8, device=device)
-        self.scales = torch.empty(sc_bytes // 4, dtype=torch.float32, device=device) if sc_bytes else None
-        self.handle = kvd_pool_create(num_layers, n_kv, num_blocks, kv_dtype, self.kv, self.scales)
+        pool_bytes, self.kv_bytes = kvd_pool_bytes(num_layers, n_kv, num_blocks, kv_dtype)
+        self.mem = torch.empty(pool_bytes, dtype=torch.uint8, device=device)
+        self.handle = kvd_pool_create(num_layers, n_kv, num_blocks, kv_dtype, self.mem)
 
     @property
     def record_bytes(self) -> int:
-        return 2 * 16 * 128 * (2 if self.kv_dtype == KVD_BF16 else 1)
+        """Bytes of one (layer, block, KV head) record: K tile, V tile and (FP8) 32 fp32 scales."""
+        return 8192 if self.kv_dtype == KVD_BF16 else 4096 + 128
 
     def close(self):
         if self.handle is not None:

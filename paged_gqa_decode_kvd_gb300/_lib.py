@@ -58,7 +58,7 @@ def load(build_if_missing: bool = True):
     lib.kvd_pool_bytes.restype = i32
     lib.kvd_pool_bytes.argtypes = [ctypes.POINTER(PoolDesc), ctypes.POINTER(sz), ctypes.POINTER(sz)]
     lib.kvd_pool_create.restype = i32
-    lib.kvd_pool_create.argtypes = [ctypes.POINTER(PoolDesc), P, sz, P, sz, ctypes.POINTER(P)]
+    lib.kvd_pool_create.argtypes = [ctypes.POINTER(PoolDesc), P, sz, ctypes.POINTER(P)]
     lib.kvd_pool_destroy.restype = None
     lib.kvd_pool_destroy.argtypes = [P]
     lib.kvd_append_kv.restype = i32
@@ -102,21 +102,19 @@ def _stream(stream):
 
 
 def kvd_pool_bytes(num_layers: int, n_kv: int, num_blocks: int, kv_dtype: int, d_h: int = 128, block_size: int = 16):
-    """(kv_bytes, scale_bytes) of a pool; host only."""
+    """(pool_bytes, kv_bytes) of a pool: buffer size to allocate, and closed-form K/V bytes; host only."""
     d = PoolDesc(num_layers, n_kv, d_h, block_size, num_blocks, kv_dtype)
-    kv, sc = ctypes.c_size_t(), ctypes.c_size_t()
-    _check("kvd_pool_bytes", load().kvd_pool_bytes(ctypes.byref(d), ctypes.byref(kv), ctypes.byref(sc)))
-    return kv.value, sc.value
+    pool, kv = ctypes.c_size_t(), ctypes.c_size_t()
+    _check("kvd_pool_bytes", load().kvd_pool_bytes(ctypes.byref(d), ctypes.byref(pool), ctypes.byref(kv)))
+    return pool.value, kv.value
 
 
-def kvd_pool_create(num_layers, n_kv, num_blocks, kv_dtype, kv_mem, scale_mem=None, d_h=128, block_size=16):
-    """Wrap device tensors (uint8 / float32, caller-owned) as a pool; returns the handle (c_void_p)."""
+def kvd_pool_create(num_layers, n_kv, num_blocks, kv_dtype, mem, d_h=128, block_size=16):
+    """Wrap a caller-owned device tensor (any dtype, pool_bytes long) as a pool; returns the handle (c_void_p)."""
     d = PoolDesc(num_layers, n_kv, d_h, block_size, num_blocks, kv_dtype)
     h = ctypes.c_void_p()
-    kv_len = kv_mem.numel() * kv_mem.element_size()
-    sc_len = 0 if scale_mem is None else scale_mem.numel() * scale_mem.element_size()
-    _check("kvd_pool_create", load().kvd_pool_create(ctypes.byref(d), _ptr(kv_mem), kv_len, _ptr(scale_mem),
-                                                     sc_len, ctypes.byref(h)))
+    n = mem.numel() * mem.element_size()
+    _check("kvd_pool_create", load().kvd_pool_create(ctypes.byref(d), _ptr(mem), n, ctypes.byref(h)))
     return h
 
 

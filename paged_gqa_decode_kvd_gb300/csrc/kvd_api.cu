@@ -11,13 +11,11 @@
 
 struct kvd_pool {
     kvd_pool_desc desc;
-    uint8_t* kv;
-    float* scales;
+    uint8_t* mem;
     int32_t* err;
     int device;
     int num_sms;
-    size_t layer_kv_bytes;
-    size_t layer_scale_bytes;
+    size_t layer_bytes;
 };
 
 namespace {
@@ -94,10 +92,10 @@ const char* kvd_status_string(kvd_status s) {
     return "unknown status";
 }
 
-kvd_status kvd_pool_bytes(const kvd_pool_desc* desc, size_t* kv_bytes, size_t* scale_bytes) {
+kvd_status kvd_pool_bytes(const kvd_pool_desc* desc, size_t* pool_bytes, size_t* kv_bytes) {
     kvd_status st = check_desc(desc);
     if (st != KVD_OK) return st;
-    if (!kv_bytes || !scale_bytes) return KVD_ERR_INVALID;
+    if (!kv_bytes || !pool_bytes) return KVD_ERR_INVALID;
     const size_t w = desc->kv_dtype == KVD_BF16 ? 2 : 1;
     size_t per_block = 0, rows = 0, total = 0;
     // 2 (K and V) · block_size · d_h · w_kv bytes per (layer, block, KV head)
@@ -106,35 +104,29 @@ kvd_status kvd_pool_bytes(const kvd_pool_desc* desc, size_t* kv_bytes, size_t* s
     if (!mul_ok(rows, static_cast<size_t>(desc->n_kv), &rows)) return KVD_ERR_INVALID;
     if (!mul_ok(rows, per_block, &total)) return KVD_ERR_INVALID;
     *kv_bytes = total;
-    *scale_bytes = 0;
+    *pool_bytes = total;
     if (desc->kv_dtype == KVD_FP8_E4M3) {
         size_t sb = 0;
         if (!mul_ok(rows, 2 * static_cast<size_t>(desc->block_size) * sizeof(float), &sb)) return KVD_ERR_INVALID;
-        *scale_bytes = sb;
+        if (total > SIZE_MAX - sb) return KVD_ERR_INVALID;
+        *pool_bytes = total + sb;
     }
     return KVD_OK;
 }
 
-kvd_status kvd_pool_create(const kvd_pool_desc* desc, void* kv_mem, size_t kv_len, void* scale_mem,
-                           size_t scale_len, kvd_pool** out) {
+kvd_status kvd_pool_create(const kvd_pool_desc* desc, void* mem, size_t len, kvd_pool** out) {
     if (!out) return KVD_ERR_INVALID;
     *out = nullptr;
-    size_t need_kv = 0, need_sc = 0;
-    kvd_status st = kvd_pool_bytes(desc, &need_kv, &need_sc);
+    size_t need = 0, kv = 0;
+    kvd_status st = kvd_pool_bytes(desc, &need, &kv);
     if (st != KVD_OK) return st;
-    if (!kv_mem || !aligned16(kv_mem)) return KVD_ERR_INVALID;
-    if (kv_len < need_kv) return KVD_ERR_NOMEM;
-    if (desc->kv_dtype == KVD_FP8_E4M3) {
-        if (!scale_mem || !aligned16(scale_mem)) return KVD_ERR_INVALID;
-        if (scale_len < need_sc) return KVD_ERR_NOMEM;
-    }
+    if (!mem || !aligned16(mem)) return KVD_ERR_INVALID;
+    if (len < need) return KVD_ERR_NOMEM;
     kvd_pool* p = new (std::nothrow) kvd_pool;
     if (!p) return KVD_ERR_NOMEM;
     p->desc = *desc;
-    p->kv = static_cast<uint8_t*>(kv_mem);
-    p->scales = desc->kv_dtype == KVD_FP8_E4M3 ? static_cast<float*>(scale_mem) : nullptr;
-    p->layer_kv_bytes = need_kv / desc->num_layers;
-    p->layer_scale_bytes = need_sc / desc->num_layers;
+    p->mem = static_cast<uint8_t*>(mem);
+    p->layer_bytes = need / desc->num_layers;
     p->err = nullptr;
     if (cudaGetDevice(&p->device) != cudaSuccess ||
         cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess ||
@@ -164,10 +156,7 @@ kvd_status kvd_append_kv(kvd_pool* pool, int layer, const void* k_new, const voi
     p.k_new = static_cast<const uint16_t*>(k_new);
     p.v_new = static_cast<const uint16_t*>(v_new);
     p.slot_mapping = slot_mapping;
-    p.kv = pool->kv + static_cast<size_t>(layer) * pool->layer_kv_bytes;
-    p.scales = pool->scales ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(pool->scales) +
-                                                        static_cast<size_t>(layer) * pool->layer_scale_bytes)
-                            : nullptr;
+    p.kv = pool->mem + static_cast<size_t>(layer) * pool->layer_bytes;
     p.err = pool->err;
     p.n_tokens = n_tokens;
     p.num_blocks = pool->desc.num_blocks;
@@ -220,10 +209,7 @@ kvd_status kvd_decode_attn(const kvd_pool* pool, int layer, const void* q, int n
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     kvd::DecodeParams p;
-    p.kv = pool->kv + static_cast<size_t>(layer) * pool->layer_kv_bytes;
-    p.scales = fp8 ? reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(pool->scales) +
-                                                    static_cast<size_t>(layer) * pool->layer_scale_bytes)
-                   : nullptr;
+    p.kv = pool->mem + static_cast<size_t>(layer) * pool->layer_bytes;
     p.q = static_cast<const uint16_t*>(q);
     p.block_table = block_table;
     p.seq_lens = seq_lens;

@@ -38,7 +38,7 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
     const int64_t rec = (blk * p.n_kv + h);
 
     if constexpr (!FP8) {
-        __nv_bfloat16* ktile = reinterpret_cast<__nv_bfloat16*>(p.kv) + rec * (2 * kBs * kDh);
+        __nv_bfloat16* ktile = reinterpret_cast<__nv_bfloat16*>(p.kv + rec * kRecordBf16);
         __nv_bfloat16* vtile = ktile + kBs * kDh;
         #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
         }
         const float ks = (kmax == 0.f) ? 1.f : __fdiv_rn(kmax, 448.f);
         const float vs = (vmax == 0.f) ? 1.f : __fdiv_rn(vmax, 448.f);
-        uint8_t* ktile = p.kv + rec * (2 * kTileFp8);
+        uint8_t* ktile = p.kv + rec * kRecordFp8;
         uint8_t* vtile = ktile + kTileFp8;
         #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
             vtile[fp8_tile_index(i, fl, fe)] = vc;
         }
         if (lane == 0) {
-            float* sc = p.scales + rec * (2 * kBs);
+            float* sc = reinterpret_cast<float*>(ktile + 2 * kTileFp8);
             sc[t] = ks;
             sc[kBs + t] = vs;
         }

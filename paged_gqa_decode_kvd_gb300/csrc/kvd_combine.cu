@@ -15,7 +15,8 @@
 
 namespace kvd {
 
-// One warp per (request, query head); lane l owns dims 4l..4l+3.
+// One warp per (request, query head); lane l owns dims 4l..4l+3.  Split weights are
+// computed 32 slots at a time, one per lane, and broadcast for the accumulation.
 __global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
     const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -26,25 +27,39 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
     const int hg = h % p.g;
     const int first = p.unit_first[u];
     const int cnt = p.unit_count[u];
+    const float* lse_col = p.part_lse + hg;      // slot s: lse_col[s * g]
 
     float M = -INFINITY;
-    for (int s = 0; s < cnt; ++s) M = fmaxf(M, p.part_lse[static_cast<int64_t>(first + s) * p.g + hg]);
+    for (int s = lane; s < cnt; s += 32) M = fmaxf(M, lse_col[static_cast<int64_t>(first + s) * p.g]);
+    #pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float lse = -INFINITY;
     if (M != -INFINITY) {
         float Ls = 0.f;
-        for (int s = 0; s < cnt; ++s) {
-            const int64_t row = static_cast<int64_t>(first + s) * p.g + hg;
-            const float ls = p.part_lse[row];
-            if (ls == -INFINITY) continue;
-            const float w = expf(ls - M);
+        for (int s0 = 0; s0 < cnt; s0 += 32) {
+            const int s = s0 + lane;
+            float w = 0.f;
+            if (s < cnt) {
+                const float ls = lse_col[static_cast<int64_t>(first + s) * p.g];
+                w = ls == -INFINITY ? 0.f : expf(ls - M);
+            }
             Ls += w;
-            const float4 v = reinterpret_cast<const float4*>(p.part_o + row * kDh)[lane];
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-            acc.z += w * v.z;
-            acc.w += w * v.w;
+            const int n = min(32, cnt - s0);
+            #pragma unroll 4
+            for (int j = 0; j < n; ++j) {
+                const float wj = __shfl_sync(kFull, w, j);
+                const int64_t row = static_cast<int64_t>(first + s0 + j) * p.g + hg;
+                const float4 v = reinterpret_cast<const float4*>(p.part_o + row * kDh)[lane];
+                acc.x += wj * v.x;
+                acc.y += wj * v.y;
+                acc.z += wj * v.z;
+                acc.w += wj * v.w;
+            }
         }
+        #pragma unroll
+        for (int off = 16; off > 0; off >>= 1) Ls += __shfl_xor_sync(kFull, Ls, off);
         const float inv = 1.f / Ls;
         acc.x *= inv;
         acc.y *= inv;

@@ -19,6 +19,9 @@ constexpr int kMaxG = 8;          // query heads per KV head (one MMA n-tile)
 constexpr int kMaxBatch = 2048;
 constexpr int kTileBf16 = kBs * kDh * 2;   // 4096 bytes
 constexpr int kTileFp8 = kBs * kDh;        // 2048 bytes
+constexpr int kScaleBytes = 2 * kBs * 4;   // FP8 record tail: K and V scales per slot
+constexpr int kRecordBf16 = 2 * kTileBf16;                 // 8192 bytes
+constexpr int kRecordFp8 = 2 * kTileFp8 + kScaleBytes;     // 4224 bytes
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned kFull = 0xffffffffu;
@@ -150,10 +153,13 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
 }
-// Two E4M3 codes (low byte = lower element) -> f16x2, exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
-    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v), __NV_E4M3);
-    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// Two E4M3 codes (low byte = lower element) -> f16x2 in one instruction; exact, since
+// every E4M3 value is an f16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
+    uint32_t r;
+    const uint16_t v = static_cast<uint16_t>(v16);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+    return r;
 }
 
 __device__ __forceinline__ void named_barrier(int id, int threads) {

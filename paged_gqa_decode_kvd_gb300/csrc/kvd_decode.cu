@@ -37,14 +37,15 @@ constexpr int kThreads = (kNcw + 1) * 32;  // + 1 producer warp
 constexpr int kMergeStride = 132;          // floats per head row in the merge buffer (bank spread)
 constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s
 
-// Floats of one warp's merge area: O [g][kMergeStride], then m [kMaxG], then l [kMaxG].
+// Floats of one merge slot: O [g][kMergeStride], then m [kMaxG], then l [kMaxG].  Two
+// slots suffice for the register tree merge of the four consumer warps.
 __host__ __device__ inline int merge_floats(int g) { return g * kMergeStride + 2 * kMaxG; }
 
 template <bool FP8>
 struct Cfg {
     static constexpr int kTile = FP8 ? kTileFp8 : kTileBf16;
-    static constexpr int kRecord = 2 * kTile;
-    static constexpr int kStage = FP8 ? kRecord + 2 * kBs * 4 : kRecord;
+    static constexpr int kRecord = FP8 ? kRecordFp8 : kRecordBf16;   // one bulk copy per (block, head)
+    static constexpr int kStage = kRecord;
     // Stage k%kStages is consumed by warp (k - segment start) % kNcw.  With kStages a
     // multiple of kNcw every reuse of a stage inside a segment belongs to the same warp,
     // and across segments the merge barrier orders it, so a consumer never waits on a
@@ -72,7 +73,7 @@ __host__ __device__ inline Smem smem_layout(int batch, int g) {
     o += kStages * 4;
     o = (o + 15) & ~15;
     s.merge_off = o;
-    o += kNcw * merge_floats(g) * 4;
+    o += 2 * merge_floats(g) * 4;
     s.pref_off = o;
     o += (batch + 1) * 4;
     s.abort_off = o;
@@ -116,7 +117,6 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int kStages = Cfg<FP8>::kStages;
     const Smem L = smem_layout<FP8>(p.B, p.g);
-    const int kMergeFloats = merge_floats(p.g);
     uint8_t* ring = smem + L.ring_off;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full_off);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty_off);
@@ -226,12 +226,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
                                 const uint8_t* rec =
                                     p.kv + (static_cast<int64_t>(ph) * p.n_kv + sg.kvh) * Cfg<FP8>::kRecord;
                                 uint8_t* dst = ring + s * Cfg<FP8>::kStage;
-                                mbar_arrive_expect_tx(&full[s], Cfg<FP8>::kStage);
+                                mbar_arrive_expect_tx(&full[s], Cfg<FP8>::kRecord);
                                 bulk_g2s(dst, rec, Cfg<FP8>::kRecord, &full[s], policy);
-                                if constexpr (FP8) {
-                                    const float* sc = p.scales + (static_cast<int64_t>(ph) * p.n_kv + sg.kvh) * (2 * kBs);
-                                    bulk_g2s(dst + Cfg<FP8>::kRecord, sc, 2 * kBs * 4, &full[s], policy);
-                                }
                             } else {
                                 mbar_arrive(&full[s]);
                             }
@@ -357,7 +353,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
                     mma_f16(ca, fa, qf[2 * u4][0], qf[2 * u4][1]);
                     mma_f16(cb, fb, qf[2 * u4 + 1][0], qf[2 * u4 + 1][1]);
                 }
-                const float* sc = reinterpret_cast<const float*>(st + Cfg<FP8>::kRecord);
+                const float* sc = reinterpret_cast<const float*>(st + 2 * kTileFp8);
                 fk0 = sc[gid] * p.scale_log2;
                 fk1 = sc[gid + 8] * p.scale_log2;
                 fv0 = sc[kBs + gid];
@@ -462,58 +458,93 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
         }
         k += nseg;
 
-        // ---- merge the consumer warps' states, write this unit piece's partial ----
+        // ---- merge the consumer warps' states (register tree: 3+2 -> 1+0, then 1 -> 0) ----
         #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
             s0 += __shfl_xor_sync(kFull, s0, off);
             s1 += __shfl_xor_sync(kFull, s1, off);
         }
-        float* mb = merge + warp * kMergeFloats;
-        #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int d0 = 16 * i + gid, d1 = d0 + 8;
-            if (h0 < g) {
-                mb[h0 * kMergeStride + d0] = o[i][0];
-                mb[h0 * kMergeStride + d1] = o[i][2];
-            }
-            if (h1 < g) {
-                mb[h1 * kMergeStride + d0] = o[i][1];
-                mb[h1 * kMergeStride + d1] = o[i][3];
-            }
-        }
-        if (gid == 0) {
-            mb[g * kMergeStride + h0] = m0;
-            mb[g * kMergeStride + h1] = m1;
-            mb[g * kMergeStride + kMaxG + h0] = s0;
-            mb[g * kMergeStride + kMaxG + h1] = s1;
-        }
-        named_barrier(1, kNcw * 32);
-        const int slot = u + cta;
-        for (int idx = tid; idx < g * kDh; idx += kNcw * 32) {
-            const int h = idx / kDh, d = idx % kDh;
-            float M = -INFINITY;
+        const int MF = merge_floats(g);
+        auto publish = [&](float* mb) {
             #pragma unroll
-            for (int w = 0; w < kNcw; ++w) M = fmaxf(M, merge[w * kMergeFloats + g * kMergeStride + h]);
-            float Ls = 0.f, acc = 0.f;
-            if (M != -INFINITY) {
-                #pragma unroll
-                for (int w = 0; w < kNcw; ++w) {
-                    const float* mw = merge + w * kMergeFloats;
-                    const float e = ex2(mw[g * kMergeStride + h] - M);
-                    Ls += mw[g * kMergeStride + kMaxG + h] * e;
-                    acc += mw[h * kMergeStride + d] * e;
+            for (int i = 0; i < 8; ++i) {
+                const int d0 = 16 * i + gid, d1 = d0 + 8;
+                if (h0 < g) {
+                    mb[h0 * kMergeStride + d0] = o[i][0];
+                    mb[h0 * kMergeStride + d1] = o[i][2];
+                }
+                if (h1 < g) {
+                    mb[h1 * kMergeStride + d0] = o[i][1];
+                    mb[h1 * kMergeStride + d1] = o[i][3];
                 }
             }
-            const bool any = Ls > 0.f;
-            p.part_o[(static_cast<int64_t>(slot) * g + h) * kDh + d] = any ? acc / Ls : 0.f;
-            if (d == 0) p.part_lse[static_cast<int64_t>(slot) * g + h] = any ? (M + log2f(Ls)) * kLn2 : -INFINITY;
-        }
-        if (sg.j0 == 0 && tid == 0) {
-            const int64_t c_last = (sg.unit_end - 1) / chunk;
-            p.unit_first[u] = slot;
-            p.unit_count[u] = static_cast<int>(c_last - cta + 1);
-        }
+            if (gid == 0) {
+                mb[g * kMergeStride + h0] = m0;
+                mb[g * kMergeStride + h1] = m1;
+                mb[g * kMergeStride + kMaxG + h0] = s0;
+                mb[g * kMergeStride + kMaxG + h1] = s1;
+            }
+        };
+        auto fold = [&](const float* mb) {
+            const float mo0 = mb[g * kMergeStride + h0], mo1 = mb[g * kMergeStride + h1];
+            const float so0 = mb[g * kMergeStride + kMaxG + h0], so1 = mb[g * kMergeStride + kMaxG + h1];
+            const float M0 = fmaxf(m0, mo0), M1 = fmaxf(m1, mo1);
+            const float z0 = M0 == -INFINITY ? 0.f : M0, z1 = M1 == -INFINITY ? 0.f : M1;
+            const float a0 = ex2(m0 - z0), b0 = ex2(mo0 - z0);   // 0 for a -inf side
+            const float a1 = ex2(m1 - z1), b1 = ex2(mo1 - z1);
+            s0 = s0 * a0 + so0 * b0;
+            s1 = s1 * a1 + so1 * b1;
+            m0 = M0;
+            m1 = M1;
+            #pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int d0 = 16 * i + gid, d1 = d0 + 8;
+                const float p00 = h0 < g ? mb[h0 * kMergeStride + d0] : 0.f;
+                const float p02 = h0 < g ? mb[h0 * kMergeStride + d1] : 0.f;
+                const float p11 = h1 < g ? mb[h1 * kMergeStride + d0] : 0.f;
+                const float p13 = h1 < g ? mb[h1 * kMergeStride + d1] : 0.f;
+                o[i][0] = o[i][0] * a0 + p00 * b0;
+                o[i][2] = o[i][2] * a0 + p02 * b0;
+                o[i][1] = o[i][1] * a1 + p11 * b1;
+                o[i][3] = o[i][3] * a1 + p13 * b1;
+            }
+        };
+        if (warp >= 2) publish(merge + (warp - 2) * MF);
         named_barrier(1, kNcw * 32);
+        if (warp < 2) fold(merge + warp * MF);
+        named_barrier(1, kNcw * 32);
+        if (warp == 1) publish(merge);
+        named_barrier(1, kNcw * 32);
+        if (warp == 0) {
+            fold(merge);
+            // this unit piece's partial: o normalised over its own positions, and its lse
+            const int slot = u + cta;
+            const float i0 = s0 > 0.f ? 1.f / s0 : 0.f, i1 = s1 > 0.f ? 1.f / s1 : 0.f;
+            float* po = p.part_o + static_cast<int64_t>(slot) * g * kDh;
+            #pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int d0 = 16 * i + gid, d1 = d0 + 8;
+                if (h0 < g) {
+                    po[h0 * kDh + d0] = o[i][0] * i0;
+                    po[h0 * kDh + d1] = o[i][2] * i0;
+                }
+                if (h1 < g) {
+                    po[h1 * kDh + d0] = o[i][1] * i1;
+                    po[h1 * kDh + d1] = o[i][3] * i1;
+                }
+            }
+            if (gid == 0) {
+                float* pl = p.part_lse + static_cast<int64_t>(slot) * g;
+                if (h0 < g) pl[h0] = s0 > 0.f ? (m0 + log2f(s0)) * kLn2 : -INFINITY;
+                if (h1 < g) pl[h1] = s1 > 0.f ? (m1 + log2f(s1)) * kLn2 : -INFINITY;
+            }
+            if (sg.j0 == 0 && lane == 0) {
+                const int64_t c_last = (sg.unit_end - 1) / chunk;
+                p.unit_first[u] = slot;
+                p.unit_count[u] = static_cast<int>(c_last - cta + 1);
+            }
+        }
+        named_barrier(1, kNcw * 32);   // the buffer is free again for the next segment
         x = sg.end;
     }
 }

@@ -10,8 +10,7 @@ struct AppendParams {
     const uint16_t* k_new;       // bf16 bits [n_tokens][n_kv][128]
     const uint16_t* v_new;
     const int64_t* slot_mapping; // [n_tokens]
-    uint8_t* kv;                 // this layer's tile records
-    float* scales;               // this layer's scales (FP8) or null
+    uint8_t* kv;                 // this layer's records
     int32_t* err;
     int64_t n_tokens;
     int64_t num_blocks;
@@ -19,8 +18,7 @@ struct AppendParams {
 };
 
 struct DecodeParams {
-    const uint8_t* kv;           // this layer's tile records
-    const float* scales;         // this layer's scales [num_blocks][n_kv][2][16] (FP8) or null
+    const uint8_t* kv;           // this layer's records (FP8: scales inline after the tiles)
     const uint16_t* q;           // bf16 bits [B][n_q][128]
     const int32_t* block_table;  // [B][max_blocks]
     const int32_t* seq_lens;     // [B]

@@ -36,10 +36,8 @@ def dtype_code(w: Workload) -> int:
 
 def make_pool(w: Workload, layers: int | None = None, poison: bool = True) -> kvd.KVPool:
     pool = kvd.KVPool(layers or w.L, w.n_kv, w.num_blocks(), dtype_code(w))
-    if poison:   # NaN everywhere first: slots never written must never reach an output
-        pool.kv.fill_(0xFF)
-        if pool.scales is not None:
-            pool.scales.fill_(float("nan"))
+    if poison:   # NaN everywhere first (codes, bf16 values, fp32 scales): unwritten slots must never leak
+        pool.mem.fill_(0xFF)
     return pool
 
 
@@ -112,16 +110,17 @@ def read_record(pool: kvd.KVPool, layer: int, block: int, head: int):
     fp8 = pool.kv_dtype == kvd.KVD_FP8_E4M3
     rb = pool.record_bytes
     off = ((layer * pool.num_blocks + block) * pool.n_kv + head) * rb
-    raw = pool.kv[off:off + rb].cpu()
+    raw = pool.mem[off:off + rb].cpu()
     if fp8:
-        kt, vt = raw[:rb // 2].numpy(), raw[rb // 2:].numpy()
+        kt, vt = raw[:2048].numpy(), raw[2048:4096].numpy()
         return kt[_tile_perm("k", True)], vt[_tile_perm("v", True)]
     vals = raw.view(torch.bfloat16)
-    kt, vt = vals[:rb // 4], vals[rb // 4:]
+    kt, vt = vals[:2048], vals[2048:]
     return kt[torch.from_numpy(_tile_perm("k", False))], vt[torch.from_numpy(_tile_perm("v", False))]
 
 
 def read_scales(pool: kvd.KVPool, layer: int, block: int, head: int):
-    base = ((layer * pool.num_blocks + block) * pool.n_kv + head) * 32
-    s = pool.scales[base:base + 32].cpu().numpy()
+    """(K scales, V scales) [16] fp32 stored after the tiles of an FP8 record."""
+    off = ((layer * pool.num_blocks + block) * pool.n_kv + head) * pool.record_bytes + 4096
+    s = pool.mem[off:off + 128].cpu().view(torch.float32).numpy()
     return s[:16], s[16:]

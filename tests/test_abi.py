@@ -34,20 +34,22 @@ def test_pool_bytes_closed_form_matches_pages():
         if r[0] == "per_token":
             _, model, layers, kvh, dh, w, want = r
             dtype = kvd.KVD_BF16 if w == "2" else kvd.KVD_FP8_E4M3
-            kv, _ = kvd.kvd_pool_bytes(int(layers), int(kvh), 1, dtype)   # one block = 16 tokens
+            _, kv = kvd.kvd_pool_bytes(int(layers), int(kvh), 1, dtype)   # one block = 16 tokens
             assert kv // 16 == int(want)
         else:
             _, tokens, gib8, gib70 = r
             for model, want in (("8B", gib8), ("70B", gib70)):
                 L, nkv, dh = models[model]
-                kv, _ = kvd.kvd_pool_bytes(L, nkv, int(tokens) // 16, kvd.KVD_BF16)
+                _, kv = kvd.kvd_pool_bytes(L, nkv, int(tokens) // 16, kvd.KVD_BF16)
                 assert abs(kv / 2 ** 30 - float(want)) <= 0.005 + 1e-12   # the page prints two decimals
 
 
 def test_fp8_scale_bytes():
-    kv, sc = kvd.kvd_pool_bytes(80, 8, 8192, kvd.KVD_FP8_E4M3)
-    assert kv == 80 * 8192 * 16 * 8 * 128 * 2       # 1 byte per element, K and V
-    assert sc == 80 * 8192 * 8 * 2 * 16 * 4         # one fp32 per (token, head) for K and V
+    pool, kv = kvd.kvd_pool_bytes(80, 8, 8192, kvd.KVD_FP8_E4M3)
+    assert kv == 80 * 8192 * 16 * 8 * 128 * 2                  # 1 byte per element, K and V
+    assert pool - kv == 80 * 8192 * 8 * 2 * 16 * 4             # one fp32 per (token, head) for K and V
+    pool, kv = kvd.kvd_pool_bytes(32, 8, 16384, kvd.KVD_BF16)
+    assert pool == kv == 32 * 8192 * 131072 // 8192 * 8192     # 32 GiB: 128 KiB per token
 
 
 def test_bad_descriptors_are_rejected():
@@ -70,9 +72,9 @@ def test_null_arguments_fail_before_any_launch():
     P = ctypes.c_void_p
     d = kvd._lib.PoolDesc(2, 8, 128, 16, 64, kvd.KVD_BF16)
     h = P()
-    assert lib.kvd_pool_create(ctypes.byref(d), None, 1 << 20, None, 0, ctypes.byref(h)) == kvd.KVD_ERR_INVALID
-    assert lib.kvd_pool_create(ctypes.byref(d), P(16), 10, None, 0, ctypes.byref(h)) == kvd.KVD_ERR_NOMEM
-    assert lib.kvd_pool_create(ctypes.byref(d), P(8), 1 << 30, None, 0, ctypes.byref(h)) == kvd.KVD_ERR_INVALID
+    assert lib.kvd_pool_create(ctypes.byref(d), None, 1 << 20, ctypes.byref(h)) == kvd.KVD_ERR_INVALID
+    assert lib.kvd_pool_create(ctypes.byref(d), P(16), 10, ctypes.byref(h)) == kvd.KVD_ERR_NOMEM
+    assert lib.kvd_pool_create(ctypes.byref(d), P(8), 1 << 30, ctypes.byref(h)) == kvd.KVD_ERR_INVALID
     assert lib.kvd_decode_attn(None, 0, None, 32, None, 1, None, 1, 1, 0, None, 0.1, None, 0, None, 0,
                                None, None, 0, None) == kvd.KVD_ERR_INVALID
     assert lib.kvd_append_kv(None, 0, None, None, None, 1, None) == kvd.KVD_ERR_INVALID
