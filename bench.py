@@ -1,10 +1,11 @@
 """Benchmark: paged GQA decode attention steps on GB300 through the C ABI.
 
-One step = one decode step of every layer of the workload: per layer, append the
-new token's K/V of every request (kvd_append_kv), then paged decode attention with
-split-KV and the log-sum-exp combine (kvd_decode_attn).  Layers run in order, as in
-a model where layer ℓ+1's query depends on layer ℓ.  The L-layer step is captured
-once as a CUDA graph and replayed.
+One step = one decode step of every layer of the workload: per layer one
+kvd_decode_attn launch that appends the new token's K/V of every request, runs paged
+decode attention with split-KV and merges the splits (plus, for the tiered workload,
+the score epilogue kvd_accum_scores).  Layers run in order, as in a model where layer
+ℓ+1's query depends on layer ℓ.  The L-layer step is captured as a CUDA graph and
+replayed.
 
 Prints one JSON line.  `value` is the closed-form K/V bytes attended per step,
 2·L·n_kv·d_h·w_kv per token (FP8 scales excluded), divided by the step time, in GB/s,
@@ -212,7 +213,7 @@ class Step:
             self.lse = torch.empty(w.batch, w.n_q, dtype=torch.float32, device=dev)
             self.logits = torch.empty(w.batch, w.n_q, self.max_len, dtype=torch.float32, device=dev)
             self.scores = torch.zeros(w.batch, self.max_len, dtype=torch.float32, device=dev)
-        self.launches_per_step = (4 if w.scores else 3) * w.L
+        self.launches_per_step = (2 if w.scores else 1) * w.L
         torch.cuda.synchronize()
         err = kvd.kvd_get_device_error(self.pool.handle)
         if err:
@@ -226,26 +227,21 @@ class Step:
         w = self.w
         return 0 if w.kv_dtype == "bf16" else int(2 * w.L * w.n_kv * 4 * sum(self.lens[t]))
 
+    def layer_call(self, layer: int, t: int = 0, stream=None):
+        """One layer's decode: fused append of the new token, attention, split merge (one launch)."""
+        scores = self.scores is not None
+        self.kvd.kvd_decode_attn(self.pool.handle, layer, self.q[t][layer], self.bt, self.seq[t], self.max_len,
+                                 self.ws, self.out[layer], num_splits=self.splits, retain_mask=self.retain,
+                                 lse_out=self.lse if scores else None, logits_out=self.logits if scores else None,
+                                 k_new=self.k_new[t][layer], v_new=self.v_new[t][layer], stream=stream)
+
     def run(self, t: int = 0, stream=None):
         kvd, w = self.kvd, self.w
         inv = 1.0 / (w.L * w.n_q)
         for layer in range(self.L):
-            kvd.kvd_append_kv(self.pool.handle, layer, self.k_new[t][layer], self.v_new[t][layer], self.slots[t],
-                              stream)
-            if self.scores is None:
-                kvd.kvd_decode_attn(self.pool.handle, layer, self.q[t][layer], self.bt, self.seq[t], self.max_len,
-                                    self.ws, self.out[layer], num_splits=self.splits, retain_mask=self.retain,
-                                    stream=stream)
-            else:
-                kvd.kvd_decode_attn(self.pool.handle, layer, self.q[t][layer], self.bt, self.seq[t], self.max_len,
-                                    self.ws, self.out[layer], num_splits=self.splits, retain_mask=self.retain,
-                                    lse_out=self.lse, logits_out=self.logits, stream=stream)
+            self.layer_call(layer, t, stream)
+            if self.scores is not None:
                 kvd.kvd_accum_scores(self.logits, self.lse, self.seq[t], inv, self.scores, stream=stream)
-
-    def decode_only(self, layer, t: int = 0, stream=None):
-        self.kvd.kvd_decode_attn(self.pool.handle, layer, self.q[t][layer], self.bt, self.seq[t], self.max_len,
-                                 self.ws, None, num_splits=self.splits, retain_mask=self.retain,
-                                 logits_out=None if self.scores is None else self.logits, stream=stream)
 
     def capture(self):
         import torch
@@ -299,13 +295,13 @@ def gpu_arm(args, w, rank, world, local):
     if err:
         raise RuntimeError(f"device error after timed steps: {st.kvd.status_string(err)}")
 
-    # per-launch time of the decode kernel alone (partials only, no combine), same stream
+    # per-launch time of the dominant kernel: the fused decode launch each layer makes, same stream
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(st.L)]
     durs = []
     for rep in range(max(1, min(args.steps, 3))):
         for layer in range(st.L):
             ev[layer][0].record(stream)
-            st.decode_only(layer)
+            st.layer_call(layer)
             ev[layer][1].record(stream)
         torch.cuda.synchronize()
         durs += [a.elapsed_time(b) for a, b in ev]

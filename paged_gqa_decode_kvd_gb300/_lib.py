@@ -11,7 +11,8 @@ from __future__ import annotations
 import ctypes
 import os
 
-KVD_OK, KVD_ERR_INVALID, KVD_ERR_UNSUPPORTED, KVD_ERR_NOMEM, KVD_ERR_CUDA, KVD_ERR_OOB, KVD_ERR_TIMEOUT = range(7)
+(KVD_OK, KVD_ERR_INVALID, KVD_ERR_UNSUPPORTED, KVD_ERR_NOMEM, KVD_ERR_CUDA, KVD_ERR_OOB, KVD_ERR_TIMEOUT,
+ KVD_ERR_STATE) = range(8)
 KVD_BF16, KVD_FP8_E4M3, KVD_F32 = 0, 1, 2
 
 SYMBOLS = [
@@ -66,7 +67,8 @@ def load(build_if_missing: bool = True):
     lib.kvd_decode_workspace_bytes.restype = i32
     lib.kvd_decode_workspace_bytes.argtypes = [P, i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(sz)]
     lib.kvd_decode_attn.restype = i32
-    lib.kvd_decode_attn.argtypes = [P, i32, P, i32, P, i32, P, i32, i32, i32, P, f32, P, sz, P, i32, P, P, i64, P]
+    lib.kvd_decode_attn.argtypes = [P, i32, P, i32, P, P, P, i32, P, i32, i32, i32, P, f32, P, sz, P, i32, P, P, i64,
+                                    P]
     lib.kvd_combine_splits.restype = i32
     lib.kvd_combine_splits.argtypes = [P, P, P, P, i32, i32, i32, i32, P, i32, P, P]
     lib.kvd_accum_scores.restype = i32
@@ -76,7 +78,8 @@ def load(build_if_missing: bool = True):
     lib.kvd_selftest_wait_timeout.restype = i32
     lib.kvd_selftest_wait_timeout.argtypes = [P, i64, P]
     lib.kvd_decode_attn_noalloc.restype = i32
-    lib.kvd_decode_attn_noalloc.argtypes = [P, i32, P, i32, P, i32, P, i32, i32, i32, P, f32, P, i32, P, P, i64, P]
+    lib.kvd_decode_attn_noalloc.argtypes = [P, i32, P, i32, P, P, P, i32, P, i32, i32, i32, P, f32, P, i32, P, P,
+                                            i64, P]
     _lib = lib
     return lib
 
@@ -137,14 +140,16 @@ def kvd_decode_workspace_bytes(handle, n_q, batch, max_seq_len, num_splits=0):
 
 
 def kvd_decode_attn(handle, layer, q, block_table, seq_lens, max_seq_len, workspace, out, num_splits=0,
-                    retain_mask=None, softmax_scale=None, lse_out=None, logits_out=None, stream=None):
+                    retain_mask=None, softmax_scale=None, lse_out=None, logits_out=None, k_new=None, v_new=None,
+                    stream=None):
     batch, n_q, d_h = q.shape
     if softmax_scale is None:
         softmax_scale = d_h ** -0.5
     out_dtype = KVD_F32 if out is not None and out.element_size() == 4 else KVD_BF16
     lstride = 0 if logits_out is None else logits_out.shape[-1]
     _check("kvd_decode_attn", load().kvd_decode_attn(
-        handle, layer, _ptr(q), n_q, _ptr(block_table), block_table.shape[1], _ptr(seq_lens), batch,
+        handle, layer, _ptr(q), n_q, _ptr(k_new), _ptr(v_new), _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), batch,
         int(max_seq_len), int(num_splits), _ptr(retain_mask), float(softmax_scale), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(out), out_dtype, _ptr(lse_out), _ptr(logits_out),
         lstride, _stream(stream)))
@@ -175,7 +180,8 @@ def kvd_selftest_wait_timeout(handle, timeout_ns, stream=None):
 
 
 def kvd_decode_attn_noalloc(handle, layer, q, block_table, seq_lens, max_seq_len, out, num_splits=0,
-                            retain_mask=None, softmax_scale=None, lse_out=None, logits_out=None, stream=None):
+                            retain_mask=None, softmax_scale=None, lse_out=None, logits_out=None, k_new=None,
+                            v_new=None, stream=None):
     """kvd_decode_attn without a workspace argument: the library's fixed device scratch array is used."""
     batch, n_q, d_h = q.shape
     if softmax_scale is None:
@@ -183,6 +189,7 @@ def kvd_decode_attn_noalloc(handle, layer, q, block_table, seq_lens, max_seq_len
     out_dtype = KVD_F32 if out is not None and out.element_size() == 4 else KVD_BF16
     lstride = 0 if logits_out is None else logits_out.shape[-1]
     _check("kvd_decode_attn_noalloc", load().kvd_decode_attn_noalloc(
-        handle, layer, _ptr(q), n_q, _ptr(block_table), block_table.shape[1], _ptr(seq_lens), batch,
+        handle, layer, _ptr(q), n_q, _ptr(k_new), _ptr(v_new), _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), batch,
         int(max_seq_len), int(num_splits), _ptr(retain_mask), float(softmax_scale), _ptr(out), out_dtype,
         _ptr(lse_out), _ptr(logits_out), lstride, _stream(stream)))

@@ -30,61 +30,9 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
         if (lane == 0) report(p.err, KVD_ERR_OOB);
         return;
     }
-    const int64_t row = (n * p.n_kv + h) * kDh + lane * 4;
-    const uint2 kraw = *reinterpret_cast<const uint2*>(p.k_new + row);
-    const uint2 vraw = *reinterpret_cast<const uint2*>(p.v_new + row);
-    const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(&kraw);
-    const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(&vraw);
-    const int64_t rec = (blk * p.n_kv + h);
-
-    if constexpr (!FP8) {
-        __nv_bfloat16* ktile = reinterpret_cast<__nv_bfloat16*>(p.kv + rec * kRecordBf16);
-        __nv_bfloat16* vtile = ktile + kBs * kDh;
-        #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int d = lane * 4 + j;
-            int fl, fe;
-            int i = k_frag_i(t, d, &fl, &fe);
-            ktile[bf16_tile_index(i, fl, fe)] = kb[j];
-            i = v_frag_i(t, d, &fl, &fe);
-            vtile[bf16_tile_index(i, fl, fe)] = vb[j];
-        }
-    } else {
-        float kx[4], vx[4];
-        float kmax = 0.f, vmax = 0.f;
-        #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            kx[j] = __bfloat162float(kb[j]);
-            vx[j] = __bfloat162float(vb[j]);
-            kmax = fmaxf(kmax, fabsf(kx[j]));
-            vmax = fmaxf(vmax, fabsf(vx[j]));
-        }
-        #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            kmax = fmaxf(kmax, __shfl_xor_sync(kFull, kmax, o));
-            vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, o));
-        }
-        const float ks = (kmax == 0.f) ? 1.f : __fdiv_rn(kmax, 448.f);
-        const float vs = (vmax == 0.f) ? 1.f : __fdiv_rn(vmax, 448.f);
-        uint8_t* ktile = p.kv + rec * kRecordFp8;
-        uint8_t* vtile = ktile + kTileFp8;
-        #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int d = lane * 4 + j;
-            const uint8_t kc = __nv_cvt_float_to_fp8(__fdiv_rn(kx[j], ks), __NV_SATFINITE, __NV_E4M3);
-            const uint8_t vc = __nv_cvt_float_to_fp8(__fdiv_rn(vx[j], vs), __NV_SATFINITE, __NV_E4M3);
-            int fl, fe;
-            int i = k_frag_i(t, d, &fl, &fe);
-            ktile[fp8_tile_index(i, fl, fe)] = kc;
-            i = v_frag_i(t, d, &fl, &fe);
-            vtile[fp8_tile_index(i, fl, fe)] = vc;
-        }
-        if (lane == 0) {
-            float* sc = reinterpret_cast<float*>(ktile + 2 * kTileFp8);
-            sc[t] = ks;
-            sc[kBs + t] = vs;
-        }
-    }
+    const int64_t row = (n * p.n_kv + h) * kDh;
+    uint8_t* record = p.kv + (blk * p.n_kv + h) * (FP8 ? kRecordFp8 : kRecordBf16);
+    write_token<FP8>(record, t, p.k_new + row, p.v_new + row, lane);
 }
 
 cudaError_t launch_append(const AppendParams& p, bool fp8, cudaStream_t stream) {

@@ -162,6 +162,72 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
     return r;
 }
 
+// Write one token's K and V rows (128 bf16 each) into slot t of a pool record, by one
+// warp: lane l holds dims 4l..4l+3.  BF16 records store the values in fragment order;
+// FP8 records store e4m3(x / scale) with scale = fp32(absmax/448) (1 for a zero row),
+// per K and per V, the scales after the two tiles.
+template <bool FP8>
+__device__ __forceinline__ void write_token(uint8_t* record, int t, const uint16_t* krow, const uint16_t* vrow,
+                                            int lane) {
+    const uint2 kraw = *reinterpret_cast<const uint2*>(krow + lane * 4);
+    const uint2 vraw = *reinterpret_cast<const uint2*>(vrow + lane * 4);
+    const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(&kraw);
+    const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(&vraw);
+    if constexpr (!FP8) {
+        __nv_bfloat16* ktile = reinterpret_cast<__nv_bfloat16*>(record);
+        __nv_bfloat16* vtile = ktile + kBs * kDh;
+        #pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int d = lane * 4 + j;
+            int fl, fe;
+            int i = k_frag_i(t, d, &fl, &fe);
+            ktile[bf16_tile_index(i, fl, fe)] = kb[j];
+            i = v_frag_i(t, d, &fl, &fe);
+            vtile[bf16_tile_index(i, fl, fe)] = vb[j];
+        }
+    } else {
+        float kx[4], vx[4];
+        float kmax = 0.f, vmax = 0.f;
+        #pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            kx[j] = __bfloat162float(kb[j]);
+            vx[j] = __bfloat162float(vb[j]);
+            kmax = fmaxf(kmax, fabsf(kx[j]));
+            vmax = fmaxf(vmax, fabsf(vx[j]));
+        }
+        #pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            kmax = fmaxf(kmax, __shfl_xor_sync(kFull, kmax, o));
+            vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, o));
+        }
+        const float ks = (kmax == 0.f) ? 1.f : __fdiv_rn(kmax, 448.f);
+        const float vs = (vmax == 0.f) ? 1.f : __fdiv_rn(vmax, 448.f);
+        uint8_t* ktile = record;
+        uint8_t* vtile = record + kTileFp8;
+        #pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int d = lane * 4 + j;
+            const uint8_t kc = __nv_cvt_float_to_fp8(__fdiv_rn(kx[j], ks), __NV_SATFINITE, __NV_E4M3);
+            const uint8_t vc = __nv_cvt_float_to_fp8(__fdiv_rn(vx[j], vs), __NV_SATFINITE, __NV_E4M3);
+            int fl, fe;
+            int i = k_frag_i(t, d, &fl, &fe);
+            ktile[fp8_tile_index(i, fl, fe)] = kc;
+            i = v_frag_i(t, d, &fl, &fe);
+            vtile[fp8_tile_index(i, fl, fe)] = vc;
+        }
+        if (lane == 0) {
+            float* sc = reinterpret_cast<float*>(record + 2 * kTileFp8);
+            sc[t] = ks;
+            sc[kBs + t] = vs;
+        }
+    }
+}
+
+// Make this thread's generic-proxy global writes visible to its later bulk copies.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_barrier(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }

@@ -50,12 +50,12 @@ struct Cfg {
     // multiple of kNcw every reuse of a stage inside a segment belongs to the same warp,
     // and across segments the merge barrier orders it, so a consumer never waits on a
     // phase whose predecessor is still incomplete (mbarrier parity cannot alias).
-    static constexpr int kStages = FP8 ? 12 : 8;
+    static constexpr int kStages = 8;
     static_assert(kStages % kNcw == 0, "stages must be a multiple of the consumer warps");
 };
 
 struct Smem {
-    int ring_off, full_off, empty_off, meta_off, merge_off, pref_off, abort_off, total;
+    int ring_off, full_off, empty_off, meta_off, merge_off, pref_off, abort_off, flag_off, total;
 };
 
 template <bool FP8>
@@ -77,6 +77,8 @@ __host__ __device__ inline Smem smem_layout(int batch, int g) {
     s.pref_off = o;
     o += (batch + 1) * 4;
     s.abort_off = o;
+    o += 4;
+    s.flag_off = o;
     o += 4;
     s.total = (o + 127) & ~127;
     return s;
@@ -112,8 +114,56 @@ __device__ __forceinline__ Segment find_segment(const int* pref, int B, int n_kv
     return s;
 }
 
+__device__ __forceinline__ void store_out(const DecodeParams& p, int64_t idx, float v) {
+    if (p.out_f32) {
+        static_cast<float*>(p.out)[idx] = v;
+    } else {
+        const __nv_bfloat16 h = __float2bfloat16_rn(v);
+        static_cast<__nv_bfloat16*>(p.out)[idx] = h;
+    }
+}
+
+// Log-sum-exp merge of unit u's `nseg` partials (slots first .. first+nseg-1) by the four
+// consumer warps of the CTA that finished last: warp w takes heads w and w+4, lane l the
+// float4 column 4l..4l+3.  Partials written by other SMs are read through L2 (ld.cg).
+__device__ __noinline__ void combine_unit(const DecodeParams& p, int u, int b, int kvh, int first, int nseg,
+                                          int warp, int lane) {
+    const int g = p.g;
+    for (int h = warp; h < g; h += kNcw) {
+        float M = -INFINITY;
+        for (int s = lane; s < nseg; s += 32)
+            M = fmaxf(M, __ldcg(p.part_lse + static_cast<int64_t>(first + s) * g + h));
+        #pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float Ls = 0.f;
+        if (M != -INFINITY) {
+            #pragma unroll 8
+            for (int s = 0; s < nseg; ++s) {
+                const int64_t row = static_cast<int64_t>(first + s) * g + h;
+                const float ls = __ldcg(p.part_lse + row);
+                const float w = ls == -INFINITY ? 0.f : expf(ls - M);
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + row * kDh) + lane);
+                Ls += w;
+                acc.x += w * v.x;
+                acc.y += w * v.y;
+                acc.z += w * v.z;
+                acc.w += w * v.w;
+            }
+        }
+        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+        const int64_t orow = static_cast<int64_t>(b) * p.n_q + kvh * g + h;
+        store_out(p, orow * kDh + 4 * lane + 0, acc.x * inv);
+        store_out(p, orow * kDh + 4 * lane + 1, acc.y * inv);
+        store_out(p, orow * kDh + 4 * lane + 2, acc.z * inv);
+        store_out(p, orow * kDh + 4 * lane + 3, acc.w * inv);
+        if (p.lse_out && lane == 0) p.lse_out[orow] = Ls > 0.f ? M + logf(Ls) : -INFINITY;
+    }
+    (void)u;
+}
+
 template <bool FP8>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int kStages = Cfg<FP8>::kStages;
     const Smem L = smem_layout<FP8>(p.B, p.g);
@@ -124,6 +174,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
     float* merge = reinterpret_cast<float*>(smem + L.merge_off);
     int* pref = reinterpret_cast<int*>(smem + L.pref_off);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_off);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L.flag_off);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -185,6 +236,18 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
                 p.unit_count[u] = 0;
             }
         }
+        if (p.out) {   // fused combine: units with no block get out = 0, lse = -inf here
+            for (int uu = warp; uu < U; uu += kNcw + 1) {
+                const int b = uu / p.n_kv;
+                if (pref[b + 1] != pref[b]) continue;
+                const int64_t row0 = static_cast<int64_t>(b) * p.n_q + (uu % p.n_kv) * p.g;
+                for (int r = lane; r < p.g * kDh; r += 32) {
+                    if (p.out_f32) static_cast<float*>(p.out)[row0 * kDh + r] = 0.f;
+                    else static_cast<uint16_t*>(p.out)[row0 * kDh + r] = 0;
+                }
+                if (p.lse_out && lane < p.g) p.lse_out[row0 + lane] = -INFINITY;
+            }
+        }
     }
 
     if (warp == kNcw) {
@@ -196,6 +259,19 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
             const Segment sg = find_segment(pref, p.B, p.n_kv, x, hi);
             const int32_t* bt = p.block_table + static_cast<int64_t>(sg.b) * p.max_blocks;
             const int len = p.seq_lens[sg.b];
+            if (p.k_new && sg.j1 == sg.nblk) {
+                // Fused append: this CTA owns the unit's last block, so it writes the new token
+                // (position len-1) into the pool before it bulk-copies that block.
+                const int pos = len - 1;
+                const int ph = bt[pos / kBs];
+                if (ph >= 0 && ph < p.num_blocks) {
+                    const int64_t row = (static_cast<int64_t>(sg.b) * p.n_kv + sg.kvh) * kDh;
+                    uint8_t* rec = const_cast<uint8_t*>(p.kv) + (static_cast<int64_t>(ph) * p.n_kv + sg.kvh) * Cfg<FP8>::kRecord;
+                    write_token<FP8>(rec, pos % kBs, p.k_new + row, p.v_new + row, lane);
+                    fence_proxy_async_global();
+                }
+                __syncwarp();
+            }
             for (int jb = sg.j0; jb < sg.j1 && !aborted; jb += 32) {
                 const int j = jb + lane;
                 int phys = -1;
@@ -515,33 +591,80 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
         named_barrier(1, kNcw * 32);
         if (warp == 1) publish(merge);
         named_barrier(1, kNcw * 32);
+        const bool fused = p.out != nullptr;
+        const bool whole = sg.j0 == 0 && sg.end == sg.unit_end;   // the unit lies in this CTA alone
+        const int64_t c_first = (sg.unit_end - sg.nblk) / chunk;
+        const int64_t c_last = (sg.unit_end - 1) / chunk;
         if (warp == 0) {
             fold(merge);
-            // this unit piece's partial: o normalised over its own positions, and its lse
-            const int slot = u + cta;
             const float i0 = s0 > 0.f ? 1.f / s0 : 0.f, i1 = s1 > 0.f ? 1.f / s1 : 0.f;
-            float* po = p.part_o + static_cast<int64_t>(slot) * g * kDh;
-            #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int d0 = 16 * i + gid, d1 = d0 + 8;
-                if (h0 < g) {
-                    po[h0 * kDh + d0] = o[i][0] * i0;
-                    po[h0 * kDh + d1] = o[i][2] * i0;
+            const float ls0 = s0 > 0.f ? (m0 + log2f(s0)) * kLn2 : -INFINITY;
+            const float ls1 = s1 > 0.f ? (m1 + log2f(s1)) * kLn2 : -INFINITY;
+            if (fused && whole) {
+                // final output straight from registers
+                const int64_t orow = static_cast<int64_t>(sg.b) * p.n_q + sg.kvh * g;
+                #pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int d0 = 16 * i + gid, d1 = d0 + 8;
+                    if (h0 < g) {
+                        store_out(p, (orow + h0) * kDh + d0, o[i][0] * i0);
+                        store_out(p, (orow + h0) * kDh + d1, o[i][2] * i0);
+                    }
+                    if (h1 < g) {
+                        store_out(p, (orow + h1) * kDh + d0, o[i][1] * i1);
+                        store_out(p, (orow + h1) * kDh + d1, o[i][3] * i1);
+                    }
                 }
-                if (h1 < g) {
-                    po[h1 * kDh + d0] = o[i][1] * i1;
-                    po[h1 * kDh + d1] = o[i][3] * i1;
+                if (p.lse_out && gid == 0) {
+                    if (h0 < g) p.lse_out[orow + h0] = ls0;
+                    if (h1 < g) p.lse_out[orow + h1] = ls1;
+                }
+            } else {
+                // this unit piece's partial: o normalised over its own positions, and its lse
+                const int slot = u + cta;
+                float* po = p.part_o + static_cast<int64_t>(slot) * g * kDh;
+                #pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int d0 = 16 * i + gid, d1 = d0 + 8;
+                    if (h0 < g) {
+                        po[h0 * kDh + d0] = o[i][0] * i0;
+                        po[h0 * kDh + d1] = o[i][2] * i0;
+                    }
+                    if (h1 < g) {
+                        po[h1 * kDh + d0] = o[i][1] * i1;
+                        po[h1 * kDh + d1] = o[i][3] * i1;
+                    }
+                }
+                if (gid == 0) {
+                    float* pl = p.part_lse + static_cast<int64_t>(slot) * g;
+                    if (h0 < g) pl[h0] = ls0;
+                    if (h1 < g) pl[h1] = ls1;
+                }
+                if (sg.j0 == 0 && lane == 0) {
+                    p.unit_first[u] = slot;
+                    p.unit_count[u] = static_cast<int>(c_last - cta + 1);
+                }
+                if (fused) {
+                    // publish the partial, then count it; the CTA that completes the count merges
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int nseg = static_cast<int>(c_last - c_first + 1);
+                        const int old = atomicAdd(&p.unit_counter[u], 1);
+                        if (old >= nseg) report(p.err, KVD_ERR_STATE);
+                        const bool last = old == nseg - 1;
+                        if (last) p.unit_counter[u] = 0;   // leave the counter zero for the next call
+                        *last_flag = last ? 1 : 0;
+                    }
                 }
             }
-            if (gid == 0) {
-                float* pl = p.part_lse + static_cast<int64_t>(slot) * g;
-                if (h0 < g) pl[h0] = s0 > 0.f ? (m0 + log2f(s0)) * kLn2 : -INFINITY;
-                if (h1 < g) pl[h1] = s1 > 0.f ? (m1 + log2f(s1)) * kLn2 : -INFINITY;
-            }
-            if (sg.j0 == 0 && lane == 0) {
-                const int64_t c_last = (sg.unit_end - 1) / chunk;
-                p.unit_first[u] = slot;
-                p.unit_count[u] = static_cast<int>(c_last - cta + 1);
+        }
+        if (fused && !whole) {
+            named_barrier(1, kNcw * 32);
+            if (*last_flag) {
+                __threadfence();
+                combine_unit(p, u, sg.b, sg.kvh, static_cast<int>(u + c_first), static_cast<int>(c_last - c_first + 1),
+                             warp, lane);
             }
         }
         named_barrier(1, kNcw * 32);   // the buffer is free again for the next segment

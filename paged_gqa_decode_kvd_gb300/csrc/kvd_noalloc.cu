@@ -43,7 +43,8 @@ kvd_status scratch_for_current_device(void** out) {
 
 }  // namespace
 
-extern "C" kvd_status kvd_decode_attn_noalloc(const kvd_pool* pool, int layer, const void* q, int n_q,
+extern "C" kvd_status kvd_decode_attn_noalloc(kvd_pool* pool, int layer, const void* q, int n_q,
+                                              const void* k_new, const void* v_new,
                                               const int32_t* block_table, int max_blocks_per_seq,
                                               const int32_t* seq_lens, int batch, int max_seq_len, int num_splits,
                                               const uint16_t* retain_mask, float softmax_scale, void* out,
@@ -58,7 +59,8 @@ extern "C" kvd_status kvd_decode_attn_noalloc(const kvd_pool* pool, int layer, c
     void* scratch = nullptr;
     st = scratch_for_current_device(&scratch);
     if (st != KVD_OK) return st;
-    return kvd_decode_attn(pool, layer, q, n_q, block_table, max_blocks_per_seq, seq_lens, batch, max_seq_len,
+    return kvd_decode_attn(pool, layer, q, n_q, k_new, v_new, block_table, max_blocks_per_seq, seq_lens, batch,
+                           max_seq_len,
                            splits, retain_mask, softmax_scale, scratch, static_cast<size_t>(KVD_NOALLOC_SCRATCH_BYTES),
                            out, out_dtype, lse_out, logits_out, logits_stride, stream);
 }

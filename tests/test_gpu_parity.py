@@ -329,3 +329,69 @@ def test_cuda_graph_replay_matches_eager(cuda_device):
     graph.replay()
     torch.cuda.synchronize()
     assert np.array_equal(out.cpu().numpy(), eager["out"])
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_fused_append_equals_separate_append(cuda_device, kv_dtype):
+    """k_new/v_new passed to kvd_decode_attn write the same pool bytes and give the same output
+    as kvd_append_kv followed by kvd_decode_attn."""
+    lens = [300, 17, 1, 4096, 16, 33]
+    w = _custom(f"fused_{kv_dtype}", 16, 4, lens, kv_dtype=kv_dtype, seed=5)
+    dev = cuda_device
+    bt, bt_d, seq, seq_d, _ = H.device_inputs(w, dev)
+    prefix = [c - 1 for c in lens]
+    pos = w.append_pos(0)
+    ks, vs = zip(*[w.kv(0, b, pos[b], pos[b] + 1, dev) for b in range(w.batch)])
+    k_new, v_new = torch.cat(ks).contiguous(), torch.cat(vs).contiguous()
+    slots = torch.cat([w.slot_mapping(b, pos[b], pos[b] + 1, bt) for b in range(w.batch)]).to(dev)
+    q = w.q(0, 0, dev)
+    outs = []
+    pools = []
+    for fused in (False, True):
+        pool = H.make_pool(w)
+        H.fill_layer(pool, w, 0, bt, prefix, dev)
+        if not fused:
+            kvd.kvd_append_kv(pool.handle, 0, k_new, v_new, slots)
+        S, ws = H.workspace(pool, w.n_q, w.batch, max(lens), 7, dev)
+        out = torch.empty(w.batch, w.n_q, 128, dtype=torch.float32, device=dev)
+        kvd.kvd_decode_attn(pool.handle, 0, q, bt_d, seq_d, max(lens), ws, out, num_splits=7,
+                            k_new=k_new if fused else None, v_new=v_new if fused else None)
+        assert kvd.kvd_get_device_error(pool.handle) == 0
+        outs.append(out.cpu())
+        pools.append(pool)
+    assert torch.equal(outs[0], outs[1])
+    assert torch.equal(pools[0].mem, pools[1].mem)
+    ref = H.oracle_layer(w, 0, bt, lens)
+    H.assert_out_close(outs[1].numpy(), ref["out"])
+
+
+def test_fused_combine_matches_standalone_combine(cuda_device):
+    """The in-kernel merge (last CTA of each unit) equals kvd_combine_splits on the partials."""
+    w = _custom("fusedcomb", 32, 8, [5000, 77, 2048, 700])
+    dev = cuda_device
+    bt, bt_d, seq, seq_d, _ = H.device_inputs(w, dev)
+    pool = H.make_pool(w)
+    H.fill_layer(pool, w, 0, bt, w.seq_lens(), dev)
+    q = w.q(0, 0, dev)
+    for splits in (5, 0, 300):
+        S, ws = H.workspace(pool, w.n_q, w.batch, 5000, splits, dev)
+        fused = torch.empty(w.batch, w.n_q, 128, dtype=torch.float32, device=dev)
+        flse = torch.empty(w.batch, w.n_q, dtype=torch.float32, device=dev)
+        kvd.kvd_decode_attn(pool.handle, 0, q, bt_d, seq_d, 5000, ws, fused, num_splits=splits, lse_out=flse)
+        kvd.kvd_decode_attn(pool.handle, 0, q, bt_d, seq_d, 5000, ws, None, num_splits=splits)
+        U, g = w.batch * w.n_kv, w.g
+        slots = U + S
+        a256 = lambda x: (x + 255) // 256 * 256
+        o_po, o_pl = 0, a256(slots * g * 128 * 4)
+        o_uf = o_pl + a256(slots * g * 4)
+        o_uc = o_uf + a256(U * 4)
+        po = ws[o_po:o_pl].view(torch.float32)
+        pl = ws[o_pl:o_pl + slots * g * 4].view(torch.float32)
+        uf = ws[o_uf:o_uf + U * 4].view(torch.int32)
+        uc = ws[o_uc:o_uc + U * 4].view(torch.int32)
+        sep = torch.empty_like(fused)
+        slse = torch.empty_like(flse)
+        kvd.kvd_combine_splits(po, pl, uf, uc, w.batch, w.n_q, w.n_kv, sep, slse)
+        assert kvd.kvd_get_device_error(pool.handle) == 0
+        np.testing.assert_allclose(fused.cpu().numpy(), sep.cpu().numpy(), rtol=1e-5, atol=1e-6)
+        np.testing.assert_allclose(flse.cpu().numpy(), slse.cpu().numpy(), rtol=1e-6, atol=1e-5)
