@@ -235,6 +235,24 @@ class Step:
                                  lse_out=self.lse if scores else None, logits_out=self.logits if scores else None,
                                  k_new=self.k_new[t][layer], v_new=self.v_new[t][layer], stream=stream)
 
+    def decode_kernel_only(self, layer: int, t: int = 0, stream=None):
+        """The layer's decode kernel alone (fused append, partials, no merge launch)."""
+        scores = self.scores is not None
+        self.kvd.kvd_decode_attn(self.pool.handle, layer, self.q[t][layer], self.bt, self.seq[t], self.max_len,
+                                 self.ws, None, num_splits=self.splits, retain_mask=self.retain,
+                                 logits_out=self.logits if scores else None,
+                                 k_new=self.k_new[t][layer], v_new=self.v_new[t][layer], stream=stream)
+
+    def capture_decode_only(self):
+        import torch
+
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for layer in range(self.L):
+                self.decode_kernel_only(layer)
+        torch.cuda.synchronize()
+        return g
+
     def run(self, t: int = 0, stream=None):
         kvd, w = self.kvd, self.w
         inv = 1.0 / (w.L * w.n_q)
@@ -295,19 +313,20 @@ def gpu_arm(args, w, rank, world, local):
     if err:
         raise RuntimeError(f"device error after timed steps: {st.kvd.status_string(err)}")
 
-    # per-launch time of the dominant kernel: the fused decode launch each layer makes, same stream
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(st.L)]
-    durs = []
-    for rep in range(max(1, min(args.steps, 3))):
-        for layer in range(st.L):
-            ev[layer][0].record(stream)
-            st.layer_call(layer)
-            ev[layer][1].record(stream)
-        torch.cuda.synchronize()
-        durs += [a.elapsed_time(b) for a, b in ev]
-    dec_ms = statistics.mean(durs)
-    # algorithmic bytes one decode launch must read: the K/V elements of every attended
-    # position, plus for FP8 the per-(token, head) K and V scales
+    # per-launch time of the dominant kernel (the decode kernel), from a graph of its L
+    # launches alone replayed on the same stream, so host enqueue time cannot inflate it
+    dgraph = st.capture_decode_only()
+    dgraph.replay()
+    torch.cuda.synchronize()
+    reps = max(3, min(50, args.steps // 4))
+    d0 = torch.cuda.Event(enable_timing=True)
+    d1 = torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for _ in range(reps):
+        dgraph.replay()
+    d1.record(stream)
+    torch.cuda.synchronize()
+    dec_ms = d0.elapsed_time(d1) / (reps * st.L)
     layer_bytes = (st.kv_bytes(0) + st.scale_bytes(0)) / w.L
     achieved = layer_bytes / (dec_ms * 1e-3) / 1e9
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",

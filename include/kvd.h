@@ -17,10 +17,8 @@
  *
  * Conventions for every entry point
  *  - Device pointers are caller-owned CUDA device memory; the library never
- *    frees them.  The library itself allocates only, inside kvd_pool_create, the
- *    pool handle (host) and one small device block holding the error word and
- *    the per-unit split counters (256 + 2048·n_kv·4 bytes; zero between calls).
- *    Calls on one pool must not run concurrently on different streams.
+ *    frees them.  The library itself allocates only the pool handle (host) and a
+ *    4-byte device error word inside kvd_pool_create.
  *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
  *    stream.  Calls are asynchronous: the return status covers argument
  *    validation and kernel launch only.
@@ -28,7 +26,7 @@
  *    the pool, a sequence length outside [1, max_blocks_per_seq·16], a bounded
  *    wait that ran out) records the first error code in the pool's error word;
  *    the affected work item is treated as empty.  Read it with
- *    kvd_get_device_error, which also resets the split counters after an error.
+ *    kvd_get_device_error.
  *  - Supported set: d_h = 128, block_size = 16, 1 ≤ g ≤ 8, batch ≤ 2048.
  *    Anything else valid returns KVD_ERR_UNSUPPORTED before any launch.
  *
@@ -71,8 +69,7 @@ typedef enum {
     KVD_ERR_NOMEM = 3,        /* a caller buffer is smaller than required */
     KVD_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
     KVD_ERR_OOB = 5,          /* device-detected: block id or sequence length out of range */
-    KVD_ERR_TIMEOUT = 6,      /* device-detected: a bounded wait inside a kernel ran out */
-    KVD_ERR_STATE = 7         /* device-detected: workspace counters were not zero at entry */
+    KVD_ERR_TIMEOUT = 6       /* device-detected: a bounded wait inside a kernel ran out */
 } kvd_status;
 
 typedef enum {
@@ -102,12 +99,12 @@ KVD_API const char* kvd_status_string(kvd_status s);
 KVD_API kvd_status kvd_pool_bytes(const kvd_pool_desc* desc, size_t* pool_bytes, size_t* kv_bytes);
 
 /* Wrap caller memory as a pool.  mem is a device buffer of len ≥ pool_bytes bytes,
- * 16-byte aligned (else KVD_ERR_NOMEM / KVD_ERR_INVALID).  Allocates the handle and the
- * device error word + split counters on the current device (KVD_ERR_CUDA if that
- * fails).  *out is set on success. */
+ * 16-byte aligned (else KVD_ERR_NOMEM / KVD_ERR_INVALID).  Allocates the handle and a
+ * 4-byte device error word on the current device (KVD_ERR_CUDA if that fails).  *out is
+ * set on success. */
 KVD_API kvd_status kvd_pool_create(const kvd_pool_desc* desc, void* mem, size_t len, kvd_pool** out);
 
-/* Free the handle and its device state (not the caller's pool memory).  NULL is a no-op. */
+/* Free the handle and its error word (not the caller's pool memory).  NULL is a no-op. */
 KVD_API void kvd_pool_destroy(kvd_pool* pool);
 
 /* Decode-step append ("reshape and cache").  Token n's keys k_new[n][h][:] and values
@@ -126,7 +123,7 @@ KVD_API kvd_status kvd_append_kv(kvd_pool* pool, int layer, const void* k_new, c
 KVD_API kvd_status kvd_decode_workspace_bytes(const kvd_pool* pool, int n_q, int batch, int max_seq_len,
                                       int num_splits, int* splits_out, size_t* bytes_out);
 
-/* Paged GQA decode attention for one layer, in one kernel launch.
+/* Paged GQA decode attention for one layer (the decode kernel, then the split merge).
  *  q            bf16 [batch][n_q][d_h], device
  *  k_new, v_new bf16 [batch][n_kv][d_h] or both NULL: the fused decode-step append.  The
  *               token at position seq_lens[b]-1 of request b — slot
@@ -140,15 +137,15 @@ KVD_API kvd_status kvd_decode_workspace_bytes(const kvd_pool* pool, int n_q, int
  *  max_seq_len  host upper bound on seq_lens, used only for the split plan
  *  num_splits   0 = automatic; else the number of KV splits: the flattened sequence of
  *               (request, KV head, block) work is cut into num_splits equal contiguous
- *               ranges, one CTA each; partial results are merged by log-sum-exp inside the
- *               same launch (the CTA that finishes a unit's last piece merges the unit)
+ *               ranges, one CTA each; partial results are merged by log-sum-exp (a unit
+ *               that lies inside one CTA is finished by that CTA directly)
  *  retain_mask  uint16 [num_blocks] or NULL; bit o of retain_mask[p] clear = slot o of
  *               physical block p is evicted (logit −inf, weight 0) in every layer
  *  softmax_scale  multiplies q·k (1/√d_h for the plain definition)
  *  workspace    device scratch of workspace_bytes ≥ kvd_decode_workspace_bytes, no
  *               initialisation needed; layout: part_o f32 [S + U][g][d_h], part_lse f32
- *               [S + U][g], unit_first int32 [U], unit_count int32 [U], each region on a
- *               256-byte boundary (U = batch·n_kv units, S the split count)
+ *               [S + U][g], unit_first int32 [U], unit_count int32 [U] (−1 = output already
+ *               final), each region on a 256-byte boundary (U = batch·n_kv, S splits)
  *  out          [batch][n_q][d_h] in out_dtype (KVD_BF16 rounds to nearest even, or KVD_F32);
  *               NULL = write only the partials and unit tables into the workspace (merge
  *               them later with kvd_combine_splits; lse_out is then unused)
@@ -198,7 +195,8 @@ KVD_API kvd_status kvd_decode_attn_noalloc(kvd_pool* pool, int layer, const void
  * LSE = log Σ_s exp(lse_s), out = Σ_s exp(lse_s − LSE)·o_s over the unit_count[u] slots
  * starting at unit_first[u] of part_o f32 [slots][g][d_h] and part_lse f32 [slots][g]
  * (device).  Slots with lse = −inf are skipped; a unit with none (or count 0) yields
- * out = 0, lse = −inf.  out in out_dtype (KVD_BF16 or KVD_F32), lse_out may be NULL. */
+ * out = 0, lse = −inf; a unit with count < 0 is left untouched (already final).  out in
+ * out_dtype (KVD_BF16 or KVD_F32), lse_out may be NULL. */
 KVD_API kvd_status kvd_combine_splits(const float* part_o, const float* part_lse,
                               const int32_t* unit_first, const int32_t* unit_count,
                               int batch, int n_q, int n_kv, int d_h,

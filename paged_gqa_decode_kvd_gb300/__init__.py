@@ -17,7 +17,6 @@ from ._lib import (  # noqa: F401
     KVD_ERR_INVALID,
     KVD_ERR_NOMEM,
     KVD_ERR_OOB,
-    KVD_ERR_STATE,
     KVD_ERR_TIMEOUT,
     KVD_ERR_UNSUPPORTED,
     SYMBOLS,

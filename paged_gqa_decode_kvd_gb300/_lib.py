@@ -11,8 +11,7 @@ from __future__ import annotations
 import ctypes
 import os
 
-(KVD_OK, KVD_ERR_INVALID, KVD_ERR_UNSUPPORTED, KVD_ERR_NOMEM, KVD_ERR_CUDA, KVD_ERR_OOB, KVD_ERR_TIMEOUT,
- KVD_ERR_STATE) = range(8)
+KVD_OK, KVD_ERR_INVALID, KVD_ERR_UNSUPPORTED, KVD_ERR_NOMEM, KVD_ERR_CUDA, KVD_ERR_OOB, KVD_ERR_TIMEOUT = range(7)
 KVD_BF16, KVD_FP8_E4M3, KVD_F32 = 0, 1, 2
 
 SYMBOLS = [

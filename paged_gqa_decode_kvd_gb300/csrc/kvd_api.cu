@@ -12,8 +12,7 @@
 struct kvd_pool {
     kvd_pool_desc desc;
     uint8_t* mem;
-    int32_t* err;       // device error word, followed (256 B later) by the per-unit split counters
-    int32_t* counters;  // [kMaxBatch * n_kv], zero between calls
+    int32_t* err;       // device error word
     int device;
     int num_sms;
     size_t layer_bytes;
@@ -89,7 +88,6 @@ const char* kvd_status_string(kvd_status s) {
         case KVD_ERR_CUDA: return "CUDA error";
         case KVD_ERR_OOB: return "device-detected index out of range";
         case KVD_ERR_TIMEOUT: return "device wait timed out";
-        case KVD_ERR_STATE: return "workspace counters not zero at entry";
     }
     return "unknown status";
 }
@@ -130,7 +128,7 @@ kvd_status kvd_pool_create(const kvd_pool_desc* desc, void* mem, size_t len, kvd
     p->mem = static_cast<uint8_t*>(mem);
     p->layer_bytes = need / desc->num_layers;
     p->err = nullptr;
-    const size_t state_bytes = 256 + static_cast<size_t>(kvd::kMaxBatch) * desc->n_kv * sizeof(int32_t);
+    const size_t state_bytes = sizeof(int32_t);
     if (cudaGetDevice(&p->device) != cudaSuccess ||
         cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess ||
         cudaMalloc(&p->err, state_bytes) != cudaSuccess || cudaMemset(p->err, 0, state_bytes) != cudaSuccess) {
@@ -139,7 +137,6 @@ kvd_status kvd_pool_create(const kvd_pool_desc* desc, void* mem, size_t len, kvd
         cudaGetLastError();
         return KVD_ERR_CUDA;
     }
-    p->counters = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(p->err) + 256);
     *out = p;
     return KVD_OK;
 }
@@ -223,7 +220,6 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     p.out = out;
     p.lse_out = out ? lse_out : nullptr;
     p.out_f32 = out_dtype == KVD_F32;
-    p.unit_counter = pool->counters;
     p.block_table = block_table;
     p.seq_lens = seq_lens;
     p.retain = retain_mask;
@@ -242,9 +238,23 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     p.n_q = n_q;
     p.nsplit = S;
     p.scale_log2 = softmax_scale * kvd::kLog2e;
-    // One launch: the split combine is fused (the last CTA of each unit merges its
-    // partials), as is the append when k_new/v_new are given.
-    return cuda_status(kvd::launch_decode(p, fp8, s));
+    cudaError_t e = kvd::launch_decode(p, fp8, s);
+    if (e != cudaSuccess) return KVD_ERR_CUDA;
+    if (!out) return KVD_OK;  // partials only: the caller merges them with kvd_combine_splits
+
+    kvd::CombineParams c;
+    c.part_o = p.part_o;
+    c.part_lse = p.part_lse;
+    c.unit_first = p.unit_first;
+    c.unit_count = p.unit_count;
+    c.out = out;
+    c.lse_out = lse_out;
+    c.B = batch;
+    c.n_q = n_q;
+    c.n_kv = pool->desc.n_kv;
+    c.g = g;
+    c.out_f32 = out_dtype == KVD_F32;
+    return cuda_status(kvd::launch_combine(c, s));
 }
 
 kvd_status kvd_combine_splits(const float* part_o, const float* part_lse, const int32_t* unit_first,
@@ -296,9 +306,7 @@ kvd_status kvd_get_device_error(kvd_pool* pool, void* stream, int32_t* code) {
     int32_t h = 0;
     if (cudaMemcpyAsync(&h, pool->err, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess) return KVD_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return KVD_ERR_CUDA;
-    // clear the word; after a device error also the split counters an aborted call may have left
-    const size_t n = h ? 256 + static_cast<size_t>(kvd::kMaxBatch) * pool->desc.n_kv * sizeof(int32_t) : sizeof(int32_t);
-    if (cudaMemsetAsync(pool->err, 0, n, s) != cudaSuccess) return KVD_ERR_CUDA;
+    if (cudaMemsetAsync(pool->err, 0, sizeof(int32_t), s) != cudaSuccess) return KVD_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return KVD_ERR_CUDA;
     *code = h;
     return KVD_OK;

@@ -15,74 +15,87 @@
 
 namespace kvd {
 
-// One warp per (request, query head); lane l owns dims 4l..4l+3.  Split weights are
-// computed 32 slots at a time, one per lane, and broadcast for the accumulation.
-__global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
-    const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (wid >= static_cast<int64_t>(p.B) * p.n_q) return;
-    const int b = static_cast<int>(wid / p.n_q);
-    const int h = static_cast<int>(wid % p.n_q);
+// One CTA of four warps per (request, query head).  Warp w merges slots s ≡ w (mod 4)
+// with lane l owning dims 4l..4l+3 (eight slots in flight per warp), then the four warps'
+// sums are added.  A unit whose output the decode kernel already wrote (count < 0) is
+// skipped; a unit with no partial (count 0) gets out = 0 and lse = −inf.
+constexpr int kCombineWarps = 4;
+
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const CombineParams p) {
+    __shared__ float s_max[kCombineWarps];
+    __shared__ float s_sum[kCombineWarps];
+    __shared__ float4 s_acc[kCombineWarps][32];
+    const int bh = blockIdx.x;
+    const int b = bh / p.n_q;
+    const int h = bh % p.n_q;
     const int u = b * p.n_kv + h / p.g;
     const int hg = h % p.g;
-    const int first = p.unit_first[u];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     const int cnt = p.unit_count[u];
+    if (cnt < 0) return;
+    const int first = p.unit_first[u];
     const float* lse_col = p.part_lse + hg;      // slot s: lse_col[s * g]
 
     float M = -INFINITY;
-    for (int s = lane; s < cnt; s += 32) M = fmaxf(M, lse_col[static_cast<int64_t>(first + s) * p.g]);
+    for (int s = threadIdx.x; s < cnt; s += kCombineWarps * 32)
+        M = fmaxf(M, lse_col[static_cast<int64_t>(first + s) * p.g]);
     #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+    if (lane == 0) s_max[warp] = M;
+    __syncthreads();
+    M = fmaxf(fmaxf(s_max[0], s_max[1]), fmaxf(s_max[2], s_max[3]));
 
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float lse = -INFINITY;
+    float Ls = 0.f;
     if (M != -INFINITY) {
-        float Ls = 0.f;
-        for (int s0 = 0; s0 < cnt; s0 += 32) {
-            const int s = s0 + lane;
-            float w = 0.f;
-            if (s < cnt) {
-                const float ls = lse_col[static_cast<int64_t>(first + s) * p.g];
-                w = ls == -INFINITY ? 0.f : expf(ls - M);
-            }
+        #pragma unroll 8
+        for (int s = warp; s < cnt; s += kCombineWarps) {
+            const int64_t row = static_cast<int64_t>(first + s) * p.g + hg;
+            const float ls = p.part_lse[row];
+            const float4 v = reinterpret_cast<const float4*>(p.part_o + row * kDh)[lane];
+            const float w = ls == -INFINITY ? 0.f : expf(ls - M);
             Ls += w;
-            const int n = min(32, cnt - s0);
-            #pragma unroll 4
-            for (int j = 0; j < n; ++j) {
-                const float wj = __shfl_sync(kFull, w, j);
-                const int64_t row = static_cast<int64_t>(first + s0 + j) * p.g + hg;
-                const float4 v = reinterpret_cast<const float4*>(p.part_o + row * kDh)[lane];
-                acc.x += wj * v.x;
-                acc.y += wj * v.y;
-                acc.z += wj * v.z;
-                acc.w += wj * v.w;
-            }
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
         }
-        #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) Ls += __shfl_xor_sync(kFull, Ls, off);
-        const float inv = 1.f / Ls;
-        acc.x *= inv;
-        acc.y *= inv;
-        acc.z *= inv;
-        acc.w *= inv;
-        lse = M + logf(Ls);
     }
+    s_acc[warp][lane] = acc;
+    if (lane == 0) s_sum[warp] = Ls;
+    __syncthreads();
+    if (warp != 0) return;
+    float4 t = s_acc[0][lane];
+    float L = s_sum[0];
+    #pragma unroll
+    for (int w = 1; w < kCombineWarps; ++w) {
+        const float4 v = s_acc[w][lane];
+        t.x += v.x;
+        t.y += v.y;
+        t.z += v.z;
+        t.w += v.w;
+        L += s_sum[w];
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    t.x *= inv;
+    t.y *= inv;
+    t.z *= inv;
+    t.w *= inv;
     const int64_t orow = static_cast<int64_t>(b) * p.n_q + h;
     if (p.out_f32) {
-        reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * kDh)[lane] = acc;
+        reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * kDh)[lane] = t;
     } else {
         uint2 v;
-        v.x = pack_bf16(acc.x, acc.y);
-        v.y = pack_bf16(acc.z, acc.w);
+        v.x = pack_bf16(t.x, t.y);
+        v.y = pack_bf16(t.z, t.w);
         reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + orow * kDh)[lane] = v;
     }
-    if (p.lse_out && lane == 0) p.lse_out[orow] = lse;
+    if (p.lse_out && lane == 0) p.lse_out[orow] = L > 0.f ? M + logf(L) : -INFINITY;
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
-    const int64_t threads = static_cast<int64_t>(p.B) * p.n_q * 32;
-    const int blk = 256;
-    combine_kernel<<<static_cast<unsigned>((threads + blk - 1) / blk), blk, 0, stream>>>(p);
+    combine_kernel<<<static_cast<unsigned>(p.B * p.n_q), kCombineWarps * 32, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

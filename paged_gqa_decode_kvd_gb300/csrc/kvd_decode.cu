@@ -123,45 +123,6 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, int64_t idx, fl
     }
 }
 
-// Log-sum-exp merge of unit u's `nseg` partials (slots first .. first+nseg-1) by the four
-// consumer warps of the CTA that finished last: warp w takes heads w and w+4, lane l the
-// float4 column 4l..4l+3.  Partials written by other SMs are read through L2 (ld.cg).
-__device__ __noinline__ void combine_unit(const DecodeParams& p, int u, int b, int kvh, int first, int nseg,
-                                          int warp, int lane) {
-    const int g = p.g;
-    for (int h = warp; h < g; h += kNcw) {
-        float M = -INFINITY;
-        for (int s = lane; s < nseg; s += 32)
-            M = fmaxf(M, __ldcg(p.part_lse + static_cast<int64_t>(first + s) * g + h));
-        #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        float Ls = 0.f;
-        if (M != -INFINITY) {
-            #pragma unroll 8
-            for (int s = 0; s < nseg; ++s) {
-                const int64_t row = static_cast<int64_t>(first + s) * g + h;
-                const float ls = __ldcg(p.part_lse + row);
-                const float w = ls == -INFINITY ? 0.f : expf(ls - M);
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + row * kDh) + lane);
-                Ls += w;
-                acc.x += w * v.x;
-                acc.y += w * v.y;
-                acc.z += w * v.z;
-                acc.w += w * v.w;
-            }
-        }
-        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-        const int64_t orow = static_cast<int64_t>(b) * p.n_q + kvh * g + h;
-        store_out(p, orow * kDh + 4 * lane + 0, acc.x * inv);
-        store_out(p, orow * kDh + 4 * lane + 1, acc.y * inv);
-        store_out(p, orow * kDh + 4 * lane + 2, acc.z * inv);
-        store_out(p, orow * kDh + 4 * lane + 3, acc.w * inv);
-        if (p.lse_out && lane == 0) p.lse_out[orow] = Ls > 0.f ? M + logf(Ls) : -INFINITY;
-    }
-    (void)u;
-}
-
 template <bool FP8>
 __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -174,7 +135,6 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
     float* merge = reinterpret_cast<float*>(smem + L.merge_off);
     int* pref = reinterpret_cast<int*>(smem + L.pref_off);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_off);
-    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L.flag_off);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -234,18 +194,6 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
             if (pref[b + 1] == pref[b]) {
                 p.unit_first[u] = 0;
                 p.unit_count[u] = 0;
-            }
-        }
-        if (p.out) {   // fused combine: units with no block get out = 0, lse = -inf here
-            for (int uu = warp; uu < U; uu += kNcw + 1) {
-                const int b = uu / p.n_kv;
-                if (pref[b + 1] != pref[b]) continue;
-                const int64_t row0 = static_cast<int64_t>(b) * p.n_q + (uu % p.n_kv) * p.g;
-                for (int r = lane; r < p.g * kDh; r += 32) {
-                    if (p.out_f32) static_cast<float*>(p.out)[row0 * kDh + r] = 0.f;
-                    else static_cast<uint16_t*>(p.out)[row0 * kDh + r] = 0;
-                }
-                if (p.lse_out && lane < p.g) p.lse_out[row0 + lane] = -INFINITY;
             }
         }
     }
@@ -591,17 +539,15 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
         named_barrier(1, kNcw * 32);
         if (warp == 1) publish(merge);
         named_barrier(1, kNcw * 32);
-        const bool fused = p.out != nullptr;
-        const bool whole = sg.j0 == 0 && sg.end == sg.unit_end;   // the unit lies in this CTA alone
-        const int64_t c_first = (sg.unit_end - sg.nblk) / chunk;
-        const int64_t c_last = (sg.unit_end - 1) / chunk;
+        // A unit that lies in this CTA alone is final here: write the output straight from
+        // registers and mark it done (unit_count = -1) so the combine kernel skips it.
+        const bool whole = p.out != nullptr && sg.j0 == 0 && sg.end == sg.unit_end;
         if (warp == 0) {
             fold(merge);
             const float i0 = s0 > 0.f ? 1.f / s0 : 0.f, i1 = s1 > 0.f ? 1.f / s1 : 0.f;
             const float ls0 = s0 > 0.f ? (m0 + log2f(s0)) * kLn2 : -INFINITY;
             const float ls1 = s1 > 0.f ? (m1 + log2f(s1)) * kLn2 : -INFINITY;
-            if (fused && whole) {
-                // final output straight from registers
+            if (whole) {
                 const int64_t orow = static_cast<int64_t>(sg.b) * p.n_q + sg.kvh * g;
                 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -618,6 +564,10 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
                 if (p.lse_out && gid == 0) {
                     if (h0 < g) p.lse_out[orow + h0] = ls0;
                     if (h1 < g) p.lse_out[orow + h1] = ls1;
+                }
+                if (lane == 0) {
+                    p.unit_first[u] = u + cta;
+                    p.unit_count[u] = -1;
                 }
             } else {
                 // this unit piece's partial: o normalised over its own positions, and its lse
@@ -642,29 +592,8 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
                 }
                 if (sg.j0 == 0 && lane == 0) {
                     p.unit_first[u] = slot;
-                    p.unit_count[u] = static_cast<int>(c_last - cta + 1);
+                    p.unit_count[u] = static_cast<int>((sg.unit_end - 1) / chunk - cta + 1);
                 }
-                if (fused) {
-                    // publish the partial, then count it; the CTA that completes the count merges
-                    __threadfence();
-                    __syncwarp();
-                    if (lane == 0) {
-                        const int nseg = static_cast<int>(c_last - c_first + 1);
-                        const int old = atomicAdd(&p.unit_counter[u], 1);
-                        if (old >= nseg) report(p.err, KVD_ERR_STATE);
-                        const bool last = old == nseg - 1;
-                        if (last) p.unit_counter[u] = 0;   // leave the counter zero for the next call
-                        *last_flag = last ? 1 : 0;
-                    }
-                }
-            }
-        }
-        if (fused && !whole) {
-            named_barrier(1, kNcw * 32);
-            if (*last_flag) {
-                __threadfence();
-                combine_unit(p, u, sg.b, sg.kvh, static_cast<int>(u + c_first), static_cast<int>(c_last - c_first + 1),
-                             warp, lane);
             }
         }
         named_barrier(1, kNcw * 32);   // the buffer is free again for the next segment

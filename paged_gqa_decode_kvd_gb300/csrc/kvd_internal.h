@@ -22,10 +22,9 @@ struct DecodeParams {
     const uint16_t* q;           // bf16 bits [B][n_q][128]
     const uint16_t* k_new;       // fused append: bf16 [B][n_kv][128] new token, or null
     const uint16_t* v_new;
-    void* out;                   // fused combine: [B][n_q][128] output, or null (partials only)
+    void* out;                   // [B][n_q][128] output for units that lie in one CTA, or null
     float* lse_out;              // [B][n_q] or null
     int out_f32;
-    int32_t* unit_counter;       // [U], zero between calls
     const int32_t* block_table;  // [B][max_blocks]
     const int32_t* seq_lens;     // [B]
     const uint16_t* retain;      // [num_blocks] or null
