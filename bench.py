@@ -213,7 +213,7 @@ class Step:
             self.lse = torch.empty(w.batch, w.n_q, dtype=torch.float32, device=dev)
             self.logits = torch.empty(w.batch, w.n_q, self.max_len, dtype=torch.float32, device=dev)
             self.scores = torch.zeros(w.batch, self.max_len, dtype=torch.float32, device=dev)
-        self.launches_per_step = (2 if w.scores else 1) * w.L
+        self.launches_per_step = (3 if w.scores else 2) * w.L   # decode + combine (+ scores)
         torch.cuda.synchronize()
         err = kvd.kvd_get_device_error(self.pool.handle)
         if err:
