@@ -254,6 +254,7 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     c.n_kv = pool->desc.n_kv;
     c.g = g;
     c.out_f32 = out_dtype == KVD_F32;
+    c.slots_hint = S / U + 2;
     return cuda_status(kvd::launch_combine(c, s));
 }
 
@@ -278,6 +279,7 @@ kvd_status kvd_combine_splits(const float* part_o, const float* part_lse, const 
     c.n_kv = n_kv;
     c.g = n_q / n_kv;
     c.out_f32 = out_dtype == KVD_F32;
+    c.slots_hint = 64;   // counts unknown on the host: assume many partials per unit
     return cuda_status(kvd::launch_combine(c, static_cast<cudaStream_t>(stream)));
 }
 

@@ -15,15 +15,18 @@
 
 namespace kvd {
 
-// One CTA of four warps per (request, query head).  Warp w merges slots s ≡ w (mod 4)
-// with lane l owning dims 4l..4l+3 (eight slots in flight per warp), then the four warps'
-// sums are added.  A unit whose output the decode kernel already wrote (count < 0) is
-// skipped; a unit with no partial (count 0) gets out = 0 and lse = −inf.
-constexpr int kCombineWarps = 4;
+// One CTA of W warps (W = blockDim.x/32 ≤ 16, chosen from the expected partials per unit)
+// per (request, query head).  Warp w folds slots s ≡ w (mod W) in one online pass
+// (running max, rescaled sum and accumulator; lane l owns dims 4l..4l+3), then warp 0
+// merges the warps' states: a unit split 76 ways takes about one memory round trip with
+// W = 16, while two or three partials need a single warp.  A unit whose output the decode
+// kernel already wrote (count < 0) is skipped; a unit with no partial (count 0) gets
+// out = 0 and lse = −inf.
+constexpr int kCombineWarps = 16;
 
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const CombineParams p) {
-    __shared__ float s_max[kCombineWarps];
-    __shared__ float s_sum[kCombineWarps];
+    __shared__ float s_m[kCombineWarps];
+    __shared__ float s_l[kCombineWarps];
     __shared__ float4 s_acc[kCombineWarps][32];
     const int bh = blockIdx.x;
     const int b = bh / p.n_q;
@@ -32,50 +35,50 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
     const int hg = h % p.g;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int nw = blockDim.x >> 5;
     const int cnt = p.unit_count[u];
     if (cnt < 0) return;
     const int first = p.unit_first[u];
-    const float* lse_col = p.part_lse + hg;      // slot s: lse_col[s * g]
 
-    float M = -INFINITY;
-    for (int s = threadIdx.x; s < cnt; s += kCombineWarps * 32)
-        M = fmaxf(M, lse_col[static_cast<int64_t>(first + s) * p.g]);
-    #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-    if (lane == 0) s_max[warp] = M;
-    __syncthreads();
-    M = fmaxf(fmaxf(s_max[0], s_max[1]), fmaxf(s_max[2], s_max[3]));
-
+    float m = -INFINITY, l = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float Ls = 0.f;
-    if (M != -INFINITY) {
-        #pragma unroll 8
-        for (int s = warp; s < cnt; s += kCombineWarps) {
-            const int64_t row = static_cast<int64_t>(first + s) * p.g + hg;
-            const float ls = p.part_lse[row];
-            const float4 v = reinterpret_cast<const float4*>(p.part_o + row * kDh)[lane];
-            const float w = ls == -INFINITY ? 0.f : expf(ls - M);
-            Ls += w;
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-            acc.z += w * v.z;
-            acc.w += w * v.w;
-        }
+    #pragma unroll 4
+    for (int s = warp; s < cnt; s += nw) {
+        const int64_t row = static_cast<int64_t>(first + s) * p.g + hg;
+        const float ls = p.part_lse[row];
+        const float4 v = reinterpret_cast<const float4*>(p.part_o + row * kDh)[lane];
+        if (ls == -INFINITY) continue;
+        const float mn = fmaxf(m, ls);
+        const float a = expf(m - mn);          // 0 while m is -inf
+        const float w = expf(ls - mn);
+        l = l * a + w;
+        acc.x = acc.x * a + w * v.x;
+        acc.y = acc.y * a + w * v.y;
+        acc.z = acc.z * a + w * v.z;
+        acc.w = acc.w * a + w * v.w;
+        m = mn;
     }
     s_acc[warp][lane] = acc;
-    if (lane == 0) s_sum[warp] = Ls;
+    if (lane == 0) {
+        s_m[warp] = m;
+        s_l[warp] = l;
+    }
     __syncthreads();
     if (warp != 0) return;
-    float4 t = s_acc[0][lane];
-    float L = s_sum[0];
-    #pragma unroll
-    for (int w = 1; w < kCombineWarps; ++w) {
-        const float4 v = s_acc[w][lane];
-        t.x += v.x;
-        t.y += v.y;
-        t.z += v.z;
-        t.w += v.w;
-        L += s_sum[w];
+    float M = -INFINITY;
+    for (int w = 0; w < nw; ++w) M = fmaxf(M, s_m[w]);
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+    float L = 0.f;
+    if (M != -INFINITY) {
+        for (int w = 0; w < nw; ++w) {
+            const float e = expf(s_m[w] - M);  // 0 for a warp that saw nothing
+            const float4 v = s_acc[w][lane];
+            L += s_l[w] * e;
+            t.x += v.x * e;
+            t.y += v.y * e;
+            t.z += v.z * e;
+            t.w += v.w * e;
+        }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     t.x *= inv;
@@ -95,7 +98,11 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
-    combine_kernel<<<static_cast<unsigned>(p.B * p.n_q), kCombineWarps * 32, 0, stream>>>(p);
+    // about four partials per warp: expected partials per unit ≈ splits / units + 2
+    const int expect = (p.slots_hint > 0 ? p.slots_hint : 1);
+    int warps = 1;
+    while (warps < kCombineWarps && warps * 4 < expect) warps <<= 1;
+    combine_kernel<<<static_cast<unsigned>(p.B * p.n_q), warps * 32, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

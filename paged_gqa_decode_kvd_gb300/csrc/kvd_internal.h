@@ -57,6 +57,7 @@ struct CombineParams {
     int n_kv;
     int g;
     int out_f32;
+    int slots_hint;              // expected partials per unit (sizes the combine CTA), 0 = unknown
 };
 
 struct ScoreParams {
