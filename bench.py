@@ -1,9 +1,9 @@
 """Benchmark: paged GQA decode attention steps on GB300 through the C ABI.
 
 One step = one decode step of every layer of the workload: per layer one
-kvd_decode_attn launch that appends the new token's K/V of every request, runs paged
-decode attention with split-KV and merges the splits (plus, for the tiered workload,
-the score epilogue kvd_accum_scores).  Layers run in order, as in a model where layer
+kvd_decode_attn call: the decode kernel appends the new token's K/V of every request
+and runs paged decode attention with split-KV; a second launch merges the splits (and,
+for the tiered workload, adds the layer's share of the importance score).  Layers run in order, as in a model where layer
 ℓ+1's query depends on layer ℓ.  The L-layer step is captured as a CUDA graph and
 replayed.
 
@@ -213,7 +213,7 @@ class Step:
             self.lse = torch.empty(w.batch, w.n_q, dtype=torch.float32, device=dev)
             self.logits = torch.empty(w.batch, w.n_q, self.max_len, dtype=torch.float32, device=dev)
             self.scores = torch.zeros(w.batch, self.max_len, dtype=torch.float32, device=dev)
-        self.launches_per_step = (3 if w.scores else 2) * w.L   # decode + combine (+ scores)
+        self.launches_per_step = 2 * w.L   # decode kernel + merge (with the fused score update)
         torch.cuda.synchronize()
         err = kvd.kvd_get_device_error(self.pool.handle)
         if err:
@@ -233,7 +233,9 @@ class Step:
         self.kvd.kvd_decode_attn(self.pool.handle, layer, self.q[t][layer], self.bt, self.seq[t], self.max_len,
                                  self.ws, self.out[layer], num_splits=self.splits, retain_mask=self.retain,
                                  lse_out=self.lse if scores else None, logits_out=self.logits if scores else None,
-                                 k_new=self.k_new[t][layer], v_new=self.v_new[t][layer], stream=stream)
+                                 k_new=self.k_new[t][layer], v_new=self.v_new[t][layer],
+                                 scores=self.scores if scores else None, inv_LH=1.0 / (self.w.L * self.w.n_q),
+                                 stream=stream)
 
     def decode_kernel_only(self, layer: int, t: int = 0, stream=None):
         """The layer's decode kernel alone (fused append, partials, no merge launch)."""
@@ -254,12 +256,8 @@ class Step:
         return g
 
     def run(self, t: int = 0, stream=None):
-        kvd, w = self.kvd, self.w
-        inv = 1.0 / (w.L * w.n_q)
         for layer in range(self.L):
             self.layer_call(layer, t, stream)
-            if self.scores is not None:
-                kvd.kvd_accum_scores(self.logits, self.lse, self.seq[t], inv, self.scores, stream=stream)
 
     def capture(self):
         import torch

@@ -89,6 +89,15 @@ typedef struct {
 
 typedef struct kvd_pool kvd_pool;  /* opaque */
 
+/* Optional score epilogue of kvd_decode_attn: adds this layer's share of the cumulative
+ * importance score, scores[b][t] += inv_LH · Σ_h α_h[t], exactly as kvd_accum_scores would
+ * from the call's logits and final LSE, but inside the call's merge launch. */
+typedef struct {
+    float* scores;            /* f32 [batch][scores_stride], device, caller-owned, accumulated */
+    int64_t scores_stride;    /* ≥ every seq_lens[b] */
+    float inv_LH;             /* 1/(L·H): L layers and H = n_q query heads per step */
+} kvd_scores_desc;
+
 /* Readable name of a status code (static string). */
 KVD_API const char* kvd_status_string(kvd_status s);
 
@@ -152,6 +161,8 @@ KVD_API kvd_status kvd_decode_workspace_bytes(const kvd_pool* pool, int n_q, int
  *  lse_out      f32 [batch][n_q] natural-log log-sum-exp of the logits, or NULL
  *  logits_out   f32 [batch][n_q][logits_stride] or NULL: the scaled logit q·k·scale of
  *               every attended position (−inf where evicted), input of kvd_accum_scores
+ *  scores_epilogue  NULL, or the score update to fuse into the merge launch (needs out and
+ *               logits_out; n_q ≤ 256)
  * Query head h reads KV head h / g.  A head with no retained position gets out = 0 and
  * lse = −inf. */
 KVD_API kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q,
@@ -161,7 +172,8 @@ KVD_API kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int
                            const uint16_t* retain_mask, float softmax_scale,
                            void* workspace, size_t workspace_bytes,
                            void* out, int out_dtype, float* lse_out,
-                           float* logits_out, int64_t logits_stride, void* stream);
+                           float* logits_out, int64_t logits_stride,
+                           const kvd_scores_desc* scores_epilogue, void* stream);
 
 /* Size of the fixed device scratch array used by kvd_decode_attn_noalloc: 16 MiB, held on
  * every GPU that loads the library until the process exits. */
@@ -189,7 +201,8 @@ KVD_API kvd_status kvd_decode_attn_noalloc(kvd_pool* pool, int layer, const void
                                            const int32_t* seq_lens, int batch, int max_seq_len, int num_splits,
                                            const uint16_t* retain_mask, float softmax_scale,
                                            void* out, int out_dtype, float* lse_out,
-                                           float* logits_out, int64_t logits_stride, void* stream);
+                                           float* logits_out, int64_t logits_stride,
+                                           const kvd_scores_desc* scores_epilogue, void* stream);
 
 /* Merge split partials by log-sum-exp.  For unit u = b·n_kv + h/g and head h:
  * LSE = log Σ_s exp(lse_s), out = Σ_s exp(lse_s − LSE)·o_s over the unit_count[u] slots

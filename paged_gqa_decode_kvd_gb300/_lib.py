@@ -28,6 +28,10 @@ class KvdError(RuntimeError):
         self.status = status
 
 
+class ScoresDesc(ctypes.Structure):
+    _fields_ = [("scores", ctypes.c_void_p), ("scores_stride", ctypes.c_int64), ("inv_LH", ctypes.c_float)]
+
+
 class PoolDesc(ctypes.Structure):
     _fields_ = [("num_layers", ctypes.c_int32), ("n_kv", ctypes.c_int32), ("d_h", ctypes.c_int32),
                 ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int64), ("kv_dtype", ctypes.c_int32)]
@@ -67,7 +71,7 @@ def load(build_if_missing: bool = True):
     lib.kvd_decode_workspace_bytes.argtypes = [P, i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(sz)]
     lib.kvd_decode_attn.restype = i32
     lib.kvd_decode_attn.argtypes = [P, i32, P, i32, P, P, P, i32, P, i32, i32, i32, P, f32, P, sz, P, i32, P, P, i64,
-                                    P]
+                                    P, P]
     lib.kvd_combine_splits.restype = i32
     lib.kvd_combine_splits.argtypes = [P, P, P, P, i32, i32, i32, i32, P, i32, P, P]
     lib.kvd_accum_scores.restype = i32
@@ -78,7 +82,7 @@ def load(build_if_missing: bool = True):
     lib.kvd_selftest_wait_timeout.argtypes = [P, i64, P]
     lib.kvd_decode_attn_noalloc.restype = i32
     lib.kvd_decode_attn_noalloc.argtypes = [P, i32, P, i32, P, P, P, i32, P, i32, i32, i32, P, f32, P, i32, P, P,
-                                            i64, P]
+                                            i64, P, P]
     _lib = lib
     return lib
 
@@ -138,9 +142,15 @@ def kvd_decode_workspace_bytes(handle, n_q, batch, max_seq_len, num_splits=0):
     return s.value, b.value
 
 
+def _scores_desc(scores, inv_LH):
+    if scores is None:
+        return None
+    return ctypes.byref(ScoresDesc(scores.data_ptr(), scores.shape[-1], float(inv_LH)))
+
+
 def kvd_decode_attn(handle, layer, q, block_table, seq_lens, max_seq_len, workspace, out, num_splits=0,
                     retain_mask=None, softmax_scale=None, lse_out=None, logits_out=None, k_new=None, v_new=None,
-                    stream=None):
+                    scores=None, inv_LH=None, stream=None):
     batch, n_q, d_h = q.shape
     if softmax_scale is None:
         softmax_scale = d_h ** -0.5
@@ -151,7 +161,7 @@ def kvd_decode_attn(handle, layer, q, block_table, seq_lens, max_seq_len, worksp
         _ptr(seq_lens), batch,
         int(max_seq_len), int(num_splits), _ptr(retain_mask), float(softmax_scale), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(out), out_dtype, _ptr(lse_out), _ptr(logits_out),
-        lstride, _stream(stream)))
+        lstride, _scores_desc(scores, inv_LH), _stream(stream)))
 
 
 def kvd_combine_splits(part_o, part_lse, unit_first, unit_count, batch, n_q, n_kv, out, lse_out=None, stream=None):
@@ -180,7 +190,7 @@ def kvd_selftest_wait_timeout(handle, timeout_ns, stream=None):
 
 def kvd_decode_attn_noalloc(handle, layer, q, block_table, seq_lens, max_seq_len, out, num_splits=0,
                             retain_mask=None, softmax_scale=None, lse_out=None, logits_out=None, k_new=None,
-                            v_new=None, stream=None):
+                            v_new=None, scores=None, inv_LH=None, stream=None):
     """kvd_decode_attn without a workspace argument: the library's fixed device scratch array is used."""
     batch, n_q, d_h = q.shape
     if softmax_scale is None:
@@ -191,4 +201,4 @@ def kvd_decode_attn_noalloc(handle, layer, q, block_table, seq_lens, max_seq_len
         handle, layer, _ptr(q), n_q, _ptr(k_new), _ptr(v_new), _ptr(block_table), block_table.shape[1],
         _ptr(seq_lens), batch,
         int(max_seq_len), int(num_splits), _ptr(retain_mask), float(softmax_scale), _ptr(out), out_dtype,
-        _ptr(lse_out), _ptr(logits_out), lstride, _stream(stream)))
+        _ptr(lse_out), _ptr(logits_out), lstride, _scores_desc(scores, inv_LH), _stream(stream)))

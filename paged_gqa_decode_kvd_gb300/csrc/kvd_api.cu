@@ -190,7 +190,7 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
                            int max_seq_len,
                            int num_splits, const uint16_t* retain_mask, float softmax_scale, void* workspace,
                            size_t workspace_bytes, void* out, int out_dtype, float* lse_out, float* logits_out,
-                           int64_t logits_stride, void* stream) {
+                           int64_t logits_stride, const kvd_scores_desc* scores_epilogue, void* stream) {
     kvd_status st = check_decode_shape(pool, n_q, batch, max_seq_len);
     if (st != KVD_OK) return st;
     if (layer < 0 || layer >= pool->desc.num_layers || num_splits < 0 || max_blocks_per_seq < 1) return KVD_ERR_INVALID;
@@ -200,6 +200,10 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     if ((k_new == nullptr) != (v_new == nullptr)) return KVD_ERR_INVALID;
     if ((reinterpret_cast<uintptr_t>(k_new) & 7u) || (reinterpret_cast<uintptr_t>(v_new) & 7u)) return KVD_ERR_INVALID;
     if (logits_out && logits_stride < 1) return KVD_ERR_INVALID;
+    if (scores_epilogue) {
+        if (!out || !logits_out || !scores_epilogue->scores || scores_epilogue->scores_stride < 1) return KVD_ERR_INVALID;
+        if (n_q > 256 || batch > 65535) return KVD_ERR_UNSUPPORTED;
+    }
     if ((reinterpret_cast<uintptr_t>(q) & 3u) || (reinterpret_cast<uintptr_t>(out) & 15u) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return KVD_ERR_INVALID;
@@ -255,7 +259,18 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     c.g = g;
     c.out_f32 = out_dtype == KVD_F32;
     c.slots_hint = S / U + 2;
-    return cuda_status(kvd::launch_combine(c, s));
+    if (!scores_epilogue) return cuda_status(kvd::launch_combine(c, s));
+    kvd::ScoreParams sp;
+    sp.logits = logits_out;
+    sp.logits_stride = logits_stride;
+    sp.lse = nullptr;
+    sp.seq_lens = seq_lens;
+    sp.scores = scores_epilogue->scores;
+    sp.scores_stride = scores_epilogue->scores_stride;
+    sp.B = batch;
+    sp.n_q = n_q;
+    sp.inv_LH = scores_epilogue->inv_LH;
+    return cuda_status(kvd::launch_epilogue(c, sp, s));
 }
 
 kvd_status kvd_combine_splits(const float* part_o, const float* part_lse, const int32_t* unit_first,
@@ -288,7 +303,7 @@ kvd_status kvd_accum_scores(const float* logits, int64_t logits_stride, const fl
     if (batch < 0 || n_q < 1 || logits_stride < 1 || scores_stride < 1) return KVD_ERR_INVALID;
     if (batch == 0) return KVD_OK;
     if (!logits || !lse || !seq_lens || !scores) return KVD_ERR_INVALID;
-    if (batch > 65535) return KVD_ERR_UNSUPPORTED;
+    if (batch > 65535 || n_q > 256) return KVD_ERR_UNSUPPORTED;
     kvd::ScoreParams p;
     p.logits = logits;
     p.logits_stride = logits_stride;

@@ -15,27 +15,21 @@
 
 namespace kvd {
 
-// One CTA of W warps (W = blockDim.x/32 ≤ 16, chosen from the expected partials per unit)
-// per (request, query head).  Warp w folds slots s ≡ w (mod W) in one online pass
-// (running max, rescaled sum and accumulator; lane l owns dims 4l..4l+3), then warp 0
-// merges the warps' states: a unit split 76 ways takes about one memory round trip with
-// W = 16, while two or three partials need a single warp.  A unit whose output the decode
+// Merge of one (request, query head) by the nw warps of a CTA.  Warp w folds slots
+// s ≡ w (mod nw) in one online pass (running max, rescaled sum and accumulator; lane l owns
+// dims 4l..4l+3), then warp 0 merges the warps' states.  A unit whose output the decode
 // kernel already wrote (count < 0) is skipped; a unit with no partial (count 0) gets
 // out = 0 and lse = −inf.
-constexpr int kCombineWarps = 16;
+constexpr int kMaxWarps = 16;
 
-__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const CombineParams p) {
-    __shared__ float s_m[kCombineWarps];
-    __shared__ float s_l[kCombineWarps];
-    __shared__ float4 s_acc[kCombineWarps][32];
-    const int bh = blockIdx.x;
+__device__ void combine_bh(const CombineParams& p, int bh, int nw, int warp, int lane) {
+    __shared__ float s_m[kMaxWarps];
+    __shared__ float s_l[kMaxWarps];
+    __shared__ float4 s_acc[kMaxWarps][32];
     const int b = bh / p.n_q;
     const int h = bh % p.n_q;
     const int u = b * p.n_kv + h / p.g;
     const int hg = h % p.g;
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int nw = blockDim.x >> 5;
     const int cnt = p.unit_count[u];
     if (cnt < 0) return;
     const int first = p.unit_first[u];
@@ -97,37 +91,110 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
     if (p.lse_out && lane == 0) p.lse_out[orow] = L > 0.f ? M + logf(L) : -INFINITY;
 }
 
-cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
-    // about four partials per warp: expected partials per unit ≈ splits / units + 2
-    const int expect = (p.slots_hint > 0 ? p.slots_hint : 1);
+// One CTA of W warps (W from the expected partials per unit) per (request, query head).
+__global__ void __launch_bounds__(kMaxWarps * 32) combine_kernel(const CombineParams p) {
+    combine_bh(p, blockIdx.x, blockDim.x >> 5, threadIdx.x >> 5, threadIdx.x & 31);
+}
+
+static int combine_warps(int slots_hint) {
+    // about four partials per warp: a unit split 76 ways takes about one memory round trip
+    const int expect = slots_hint > 0 ? slots_hint : 1;
     int warps = 1;
-    while (warps < kCombineWarps && warps * 4 < expect) warps <<= 1;
-    combine_kernel<<<static_cast<unsigned>(p.B * p.n_q), warps * 32, 0, stream>>>(p);
+    while (warps < kMaxWarps && warps * 4 < expect) warps <<= 1;
+    return warps;
+}
+
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
+    combine_kernel<<<static_cast<unsigned>(p.B * p.n_q), combine_warps(p.slots_hint) * 32, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
-// One thread per (request, position); heads are summed in order h = 0 .. n_q-1.
-__global__ void __launch_bounds__(256) scores_kernel(const ScoreParams p) {
-    const int b = blockIdx.y;
-    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+// Importance-score update of positions [t0, t0 + blockDim.x) of request b, one thread per
+// position: scores[b][t] += inv_LH · Σ_h exp(logits[b][h][t] − lse[h]), heads in order
+// h = 0 .. n_q-1, with the n_q final LSEs staged in shared memory.
+constexpr int kScoreThreads = 256;
+constexpr int kMaxHeads = 256;
+
+__device__ void scores_tile(const ScoreParams& p, const float* s_lse, int b, int t0) {
+    const int t = t0 + threadIdx.x;
     const int len = p.seq_lens[b];
     if (t >= len || t >= p.logits_stride || t >= p.scores_stride) return;
     const float* lrow = p.logits + static_cast<int64_t>(b) * p.n_q * p.logits_stride + t;
-    const float* lse = p.lse + static_cast<int64_t>(b) * p.n_q;
     float acc = 0.f;
+    #pragma unroll 8
     for (int h = 0; h < p.n_q; ++h) {
-        const float m = lse[h];
-        if (m == -INFINITY) continue;
-        acc += expf(lrow[static_cast<int64_t>(h) * p.logits_stride] - m);
+        const float m = s_lse[h];
+        const float x = lrow[static_cast<int64_t>(h) * p.logits_stride];
+        acc += m == -INFINITY ? 0.f : expf(x - m);
     }
     p.scores[static_cast<int64_t>(b) * p.scores_stride + t] += acc * p.inv_LH;
 }
 
+__global__ void __launch_bounds__(kScoreThreads) scores_kernel(const ScoreParams p) {
+    __shared__ float s_lse[kMaxHeads];
+    const int b = blockIdx.y;
+    for (int h = threadIdx.x; h < p.n_q; h += blockDim.x) s_lse[h] = p.lse[static_cast<int64_t>(b) * p.n_q + h];
+    __syncthreads();
+    scores_tile(p, s_lse, b, blockIdx.x * blockDim.x);
+}
+
 cudaError_t launch_scores(const ScoreParams& p, cudaStream_t stream) {
-    const int blk = 256;
     const int64_t extent = p.logits_stride < p.scores_stride ? p.logits_stride : p.scores_stride;
-    dim3 grid(static_cast<unsigned>((extent + blk - 1) / blk), p.B);
-    scores_kernel<<<grid, blk, 0, stream>>>(p);
+    dim3 grid(static_cast<unsigned>((extent + kScoreThreads - 1) / kScoreThreads), p.B);
+    scores_kernel<<<grid, kScoreThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+// Split merge and score update of one layer in one launch.  CTAs [0, B·n_q) merge one
+// (request, head) each; the rest each update a tile of positions of one request.  A score
+// CTA derives the final LSE of every head of its request from the split partials itself
+// (the merge CTAs of the same launch write lse_out concurrently), or reads lse_out where
+// the decode kernel already finished the unit.
+__global__ void __launch_bounds__(kScoreThreads) epilogue_kernel(const CombineParams c, const ScoreParams sp,
+                                                                  int tiles_per_req) {
+    const int bid = blockIdx.x;
+    const int ncomb = c.B * c.n_q;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (bid < ncomb) {
+        combine_bh(c, bid, blockDim.x >> 5, warp, lane);
+        return;
+    }
+    __shared__ float s_lse[kMaxHeads];
+    const int b = (bid - ncomb) / tiles_per_req;
+    const int tile = (bid - ncomb) % tiles_per_req;
+    for (int h = warp; h < c.n_q; h += blockDim.x >> 5) {
+        const int u = b * c.n_kv + h / c.g, hg = h % c.g;
+        const int cnt = c.unit_count[u];
+        float lse = -INFINITY;
+        if (cnt < 0) {
+            lse = c.lse_out[static_cast<int64_t>(b) * c.n_q + h];
+        } else if (cnt > 0) {
+            const int first = c.unit_first[u];
+            float M = -INFINITY;
+            for (int s = lane; s < cnt; s += 32) M = fmaxf(M, c.part_lse[static_cast<int64_t>(first + s) * c.g + hg]);
+            #pragma unroll
+            for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+            float L = 0.f;
+            if (M != -INFINITY)
+                for (int s = lane; s < cnt; s += 32) {
+                    const float ls = c.part_lse[static_cast<int64_t>(first + s) * c.g + hg];
+                    L += ls == -INFINITY ? 0.f : expf(ls - M);
+                }
+            #pragma unroll
+            for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
+            lse = L > 0.f ? M + logf(L) : -INFINITY;
+        }
+        if (lane == 0) s_lse[h] = lse;
+    }
+    __syncthreads();
+    scores_tile(sp, s_lse, b, tile * kScoreThreads);
+}
+
+cudaError_t launch_epilogue(const CombineParams& c, const ScoreParams& sp, cudaStream_t stream) {
+    const int64_t extent = sp.logits_stride < sp.scores_stride ? sp.logits_stride : sp.scores_stride;
+    const int tiles = static_cast<int>((extent + kScoreThreads - 1) / kScoreThreads);
+    const int64_t ctas = static_cast<int64_t>(c.B) * c.n_q + static_cast<int64_t>(c.B) * tiles;
+    epilogue_kernel<<<static_cast<unsigned>(ctas), kScoreThreads, 0, stream>>>(c, sp, tiles);
     return cudaGetLastError();
 }
 

@@ -441,15 +441,11 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
             }
 
             // ---- O^T += V^T · P^T ----
+            // A block with an invalid slot (context tail, evicted) zeroes that slot's V in
+            // this lane's fragment, so garbage (NaN) in unused slots cannot reach the output
+            // through 0·NaN; full blocks (warp-uniform test) skip the masking.
             const bool partial = (m & 0xFFFFu) != 0xFFFFu;
-            // halves of this lane's V fragment that belong to invalid tokens are zeroed,
-            // so garbage (NaN) in unused slots cannot reach the output through 0·NaN
-            uint32_t zlo = 0xFFFFFFFFu, zhi = 0xFFFFFFFFu;
-            if (partial) {
-                const int ta = 2 * tq;
-                zlo = (((m >> ta) & 1u) ? 0x0000FFFFu : 0u) | (((m >> (ta + 1)) & 1u) ? 0xFFFF0000u : 0u);
-                zhi = (((m >> (ta + 8)) & 1u) ? 0x0000FFFFu : 0u) | (((m >> (ta + 9)) & 1u) ? 0xFFFF0000u : 0u);
-            }
+            const int ta = 2 * tq;
             if constexpr (!FP8) {
                 const uint4* vt = reinterpret_cast<const uint4*>(st + Cfg<FP8>::kTile);
                 uint4 vv[8];
@@ -457,26 +453,61 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
                 for (int i = 0; i < 8; ++i) vv[i] = vt[i * 32 + lane];
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
+                if (partial) {   // 16-bit halves: tokens (2tq, 2tq+1) in .x/.y, (2tq+8, 2tq+9) in .z/.w
+                    const uint32_t zlo = (((m >> ta) & 1u) ? 0x0000FFFFu : 0u) | (((m >> (ta + 1)) & 1u) ? 0xFFFF0000u : 0u);
+                    const uint32_t zhi =
+                        (((m >> (ta + 8)) & 1u) ? 0x0000FFFFu : 0u) | (((m >> (ta + 9)) & 1u) ? 0xFFFF0000u : 0u);
+                    #pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        vv[i].x &= zlo;
+                        vv[i].y &= zlo;
+                        vv[i].z &= zhi;
+                        vv[i].w &= zhi;
+                    }
+                }
                 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const uint32_t fa[4] = {vv[i].x & zlo, vv[i].y & zlo, vv[i].z & zhi, vv[i].w & zhi};
+                    const uint32_t fa[4] = {vv[i].x, vv[i].y, vv[i].z, vv[i].w};
                     mma_bf16(o[i], fa, pb0, pb1);
                 }
             } else {
                 const uint4* vt = reinterpret_cast<const uint4*>(st + Cfg<FP8>::kTile);
-                uint4 vv[4];
+                uint32_t zlo = 0xFFFFFFFFu, zhi = 0xFFFFFFFFu;
+                if (partial) {   // bytes: tokens (2tq, 2tq+1) in .x/.z, (2tq+8, 2tq+9) in .y/.w; code 0 = +0
+                    zlo = (((m >> ta) & 1u) ? 0x00FFu : 0u) | (((m >> (ta + 1)) & 1u) ? 0xFF00u : 0u);
+                    zhi = (((m >> (ta + 8)) & 1u) ? 0x00FFu : 0u) | (((m >> (ta + 9)) & 1u) ? 0xFF00u : 0u);
+                    zlo |= zlo << 16;
+                    zhi |= zhi << 16;
+                }
+                // two halves of four m-tiles each keep fewer V registers live
                 #pragma unroll
-                for (int i = 0; i < 4; ++i) vv[i] = vt[i * 32 + lane];
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-                #pragma unroll
-                for (int u4 = 0; u4 < 4; ++u4) {
-                    const uint32_t fa[4] = {e4m3x2_to_f16x2(vv[u4].x & 0xffff) & zlo, e4m3x2_to_f16x2(vv[u4].x >> 16) & zlo,
-                                            e4m3x2_to_f16x2(vv[u4].y & 0xffff) & zhi, e4m3x2_to_f16x2(vv[u4].y >> 16) & zhi};
-                    const uint32_t fb[4] = {e4m3x2_to_f16x2(vv[u4].z & 0xffff) & zlo, e4m3x2_to_f16x2(vv[u4].z >> 16) & zlo,
-                                            e4m3x2_to_f16x2(vv[u4].w & 0xffff) & zhi, e4m3x2_to_f16x2(vv[u4].w >> 16) & zhi};
-                    mma_f16(o[2 * u4], fa, pb0, pb1);
-                    mma_f16(o[2 * u4 + 1], fb, pb0, pb1);
+                for (int half = 0; half < 2; ++half) {
+                    uint4 vv[2];
+                    vv[0] = vt[(2 * half) * 32 + lane];
+                    vv[1] = vt[(2 * half + 1) * 32 + lane];
+                    if (half == 1) {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&empty[s]);
+                    }
+                    if (partial) {
+                        #pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            vv[i].x &= zlo;
+                            vv[i].y &= zhi;
+                            vv[i].z &= zlo;
+                            vv[i].w &= zhi;
+                        }
+                    }
+                    #pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const int u4 = 2 * half + i;
+                        const uint32_t fa[4] = {e4m3x2_to_f16x2(vv[i].x & 0xffff), e4m3x2_to_f16x2(vv[i].x >> 16),
+                                                e4m3x2_to_f16x2(vv[i].y & 0xffff), e4m3x2_to_f16x2(vv[i].y >> 16)};
+                        const uint32_t fb[4] = {e4m3x2_to_f16x2(vv[i].z & 0xffff), e4m3x2_to_f16x2(vv[i].z >> 16),
+                                                e4m3x2_to_f16x2(vv[i].w & 0xffff), e4m3x2_to_f16x2(vv[i].w >> 16)};
+                        mma_f16(o[2 * u4], fa, pb0, pb1);
+                        mma_f16(o[2 * u4 + 1], fb, pb0, pb1);
+                    }
                 }
             }
         }

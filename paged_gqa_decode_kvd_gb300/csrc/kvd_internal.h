@@ -78,6 +78,7 @@ int decode_ctas_per_sm(bool fp8, int batch, int g);
 cudaError_t launch_decode(const DecodeParams& p, bool fp8, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 cudaError_t launch_scores(const ScoreParams& p, cudaStream_t stream);
+cudaError_t launch_epilogue(const CombineParams& c, const ScoreParams& sp, cudaStream_t stream);
 cudaError_t launch_wait_timeout(int32_t* err, int64_t timeout_ns, cudaStream_t stream);
 
 }  // namespace kvd

@@ -128,9 +128,13 @@ def test_tiered_scores_over_64_steps(cuda_device):
             ks, vs = zip(*[w.kv(layer, b, pos[b], pos[b] + 1, dev) for b in range(w.batch)])
             slots = torch.cat([w.slot_mapping(b, pos[b], pos[b] + 1, bt) for b in range(w.batch)]).to(dev)
             kvd.kvd_append_kv(pool.handle, layer, torch.cat(ks), torch.cat(vs), slots)
-            kvd.kvd_decode_attn(pool.handle, layer, w.q(layer, t, dev), bt_d, seq_d, max_len, ws, out,
-                                retain_mask=ret_d, lse_out=lse, logits_out=logits)
-            kvd.kvd_accum_scores(logits, lse, seq_d, inv, scores)
+            if layer % 2:   # both forms of the score update: fused into the call, or separate
+                kvd.kvd_decode_attn(pool.handle, layer, w.q(layer, t, dev), bt_d, seq_d, max_len, ws, out,
+                                    retain_mask=ret_d, lse_out=lse, logits_out=logits, scores=scores, inv_LH=inv)
+            else:
+                kvd.kvd_decode_attn(pool.handle, layer, w.q(layer, t, dev), bt_d, seq_d, max_len, ws, out,
+                                    retain_mask=ret_d, lse_out=lse, logits_out=logits)
+                kvd.kvd_accum_scores(logits, lse, seq_d, inv, scores)
         if t == 1:
             kept_s = scores.clone()
     assert kvd.kvd_get_device_error(pool.handle) == 0

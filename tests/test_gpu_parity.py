@@ -395,3 +395,35 @@ def test_fused_combine_matches_standalone_combine(cuda_device):
         assert kvd.kvd_get_device_error(pool.handle) == 0
         np.testing.assert_allclose(fused.cpu().numpy(), sep.cpu().numpy(), rtol=1e-5, atol=1e-6)
         np.testing.assert_allclose(flse.cpu().numpy(), slse.cpu().numpy(), rtol=1e-6, atol=1e-5)
+
+
+def test_fused_score_epilogue_matches_accum_scores(cuda_device):
+    """The score update fused into kvd_decode_attn's merge launch equals kvd_accum_scores
+    applied to the same call's logits and LSE, and both match the oracle's α sum."""
+    w = _custom("fusedscore", 28, 4, [3000, 700, 16, 4100], evict_frac=0.05, protect_prompt=64, protect_recent=32,
+                scores=True)
+    dev = cuda_device
+    bt, bt_d, seq, seq_d, ret_d = H.device_inputs(w, dev)
+    pool = H.make_pool(w)
+    H.fill_layer(pool, w, 0, bt, w.seq_lens(), dev)
+    q = w.q(0, 0, dev)
+    S = max(w.seq_lens())
+    inv = 1.0 / (3 * w.n_q)
+    for splits in (0, 3, 1):
+        _, ws = H.workspace(pool, w.n_q, w.batch, S, splits, dev)
+        out = torch.empty(w.batch, w.n_q, 128, dtype=torch.float32, device=dev)
+        lse = torch.empty(w.batch, w.n_q, dtype=torch.float32, device=dev)
+        logits = torch.full((w.batch, w.n_q, S), float("nan"), dtype=torch.float32, device=dev)
+        base = torch.rand(w.batch, S + 3, dtype=torch.float32, device=dev)
+        fused = base.clone()
+        kvd.kvd_decode_attn(pool.handle, 0, q, bt_d, seq_d, S, ws, out, num_splits=splits, retain_mask=ret_d,
+                            lse_out=lse, logits_out=logits, scores=fused, inv_LH=inv)
+        sep = base.clone()
+        kvd.kvd_accum_scores(logits, lse, seq_d, inv, sep)
+        assert kvd.kvd_get_device_error(pool.handle) == 0
+        np.testing.assert_allclose(fused.cpu().numpy(), sep.cpu().numpy(), rtol=2e-6, atol=1e-9)
+    ref = H.oracle_layer(w, 0, bt, w.seq_lens(), retain=w.retain_mask(bt), want_alpha=True)
+    got = (fused - base).double().cpu().numpy()
+    for b, n in enumerate(w.seq_lens()):
+        want = ref["alpha"][b, :, :n].sum(0) * inv
+        assert np.all(np.abs(got[b, :n] - want) <= H.SCORE_RTOL * want + 2 ** -22 * base[b, :n].double().cpu().numpy())
