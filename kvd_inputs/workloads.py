@@ -106,6 +106,8 @@ class Workload:
         lo = self.protect_prompt
         hi = self._ctx0[b] - self.protect_recent
         n = hi - lo
+        if n <= 0:                       # a context shorter than its protected parts: nothing evictable
+            return torch.zeros(0, dtype=torch.int64)
         k = int(round(self.evict_frac * n))
         pick = gen.choose(gen.stream_key(self.seed, self.name, "evict", b), n, k)
         return pick + lo
