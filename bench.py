@@ -54,6 +54,23 @@ def decode_intensity(g: int, w_kv: float) -> float:
     return 2 * g / w_kv
 
 
+def recorded_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on the
+    current decode kernel source (matched by its sha256); otherwise None."""
+    import hashlib
+
+    src = os.path.join(ROOT, "paged_gqa_decode_kvd_gb300", "csrc", "kvd_decode.cu")
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not (os.path.exists(src) and os.path.exists(path)):
+        return None
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload and parts[1] == digest:
+            return float(parts[2])
+    return None
+
+
 def measured_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -328,7 +345,8 @@ def gpu_arm(args, w, rank, world, local):
     layer_bytes = (st.kv_bytes(0) + st.scale_bytes(0)) / w.L
     achieved = layer_bytes / (dec_ms * 1e-3) / 1e9
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": args.traffic,
+            "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "traffic": args.traffic if args.traffic is not None else recorded_traffic(w.name) if not args.layers else None,
             "kernel": "kvd::decode_kernel", "peak_source": peaks["source"] + " (copy, MEASURED_PEAKS.json hbm_gbs)",
             "bytes_per_launch": layer_bytes, "launch_ms": round(dec_ms, 5)}
 
