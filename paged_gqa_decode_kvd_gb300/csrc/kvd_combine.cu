@@ -93,6 +93,7 @@ __device__ void combine_bh(const CombineParams& p, int bh, int nw, int warp, int
 
 // One CTA of W warps (W from the expected partials per unit) per (request, query head).
 __global__ void __launch_bounds__(kMaxWarps * 32) combine_kernel(const CombineParams p) {
+    pdl_wait();
     combine_bh(p, blockIdx.x, blockDim.x >> 5, threadIdx.x >> 5, threadIdx.x & 31);
 }
 
@@ -105,8 +106,8 @@ static int combine_warps(int slots_hint) {
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
-    combine_kernel<<<static_cast<unsigned>(p.B * p.n_q), combine_warps(p.slots_hint) * 32, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(combine_kernel, dim3(static_cast<unsigned>(p.B * p.n_q)),
+                            dim3(combine_warps(p.slots_hint) * 32), 0, stream, p);
 }
 
 // Importance-score update of positions [t0, t0 + blockDim.x) of request b, one thread per
@@ -152,6 +153,7 @@ cudaError_t launch_scores(const ScoreParams& p, cudaStream_t stream) {
 // the decode kernel already finished the unit.
 __global__ void __launch_bounds__(kScoreThreads) epilogue_kernel(const CombineParams c, const ScoreParams sp,
                                                                   int tiles_per_req) {
+    pdl_wait();
     const int bid = blockIdx.x;
     const int ncomb = c.B * c.n_q;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -194,8 +196,8 @@ cudaError_t launch_epilogue(const CombineParams& c, const ScoreParams& sp, cudaS
     const int64_t extent = sp.logits_stride < sp.scores_stride ? sp.logits_stride : sp.scores_stride;
     const int tiles = static_cast<int>((extent + kScoreThreads - 1) / kScoreThreads);
     const int64_t ctas = static_cast<int64_t>(c.B) * c.n_q + static_cast<int64_t>(c.B) * tiles;
-    epilogue_kernel<<<static_cast<unsigned>(ctas), kScoreThreads, 0, stream>>>(c, sp, tiles);
-    return cudaGetLastError();
+    return launch_dependent(epilogue_kernel, dim3(static_cast<unsigned>(ctas)), dim3(kScoreThreads), 0, stream, c, sp,
+                            tiles);
 }
 
 }  // namespace kvd

@@ -228,6 +228,13 @@ __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Programmatic dependent launch: the split merge is launched as a dependent of the decode
+// kernel.  The decode kernel signals once a CTA has streamed its last block, so the merge
+// grid can be scheduled while the decode grid drains; the merge kernel's first statement
+// waits until the decode grid has completed and its writes are visible.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 __device__ __forceinline__ void named_barrier(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }

@@ -512,6 +512,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
             }
         }
         k += nseg;
+        if (sg.end == hi) pdl_trigger();   // this CTA's last piece has been streamed
 
         // ---- merge the consumer warps' states (register tree: 3+2 -> 1+0, then 1 -> 0) ----
         #pragma unroll

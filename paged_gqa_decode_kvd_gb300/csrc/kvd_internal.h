@@ -72,6 +72,23 @@ struct ScoreParams {
     float inv_LH;
 };
 
+// Launch `kernel` as a programmatic dependent of the preceding kernel in the stream.
+template <typename... P>
+inline cudaError_t launch_dependent(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                    const P&... params) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, params...);
+}
+
 cudaError_t launch_append(const AppendParams& p, bool fp8, cudaStream_t stream);
 size_t decode_smem_bytes(bool fp8, int batch, int g);
 int decode_ctas_per_sm(bool fp8, int batch, int g);
