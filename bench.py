@@ -464,6 +464,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama8b")
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling captures)")
+    ap.add_argument("--context", type=int, default=0, help="override every request's context (size sweeps)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -480,6 +481,11 @@ def main(argv=None):
     if args.layers:
         w.L = args.layers
         w.description += f" [reduced to {args.layers} layers for profiling]"
+    if args.context:
+        if w.steps > 1:
+            ap.error("--context applies to fixed-context workloads only")
+        w._ctx0 = [args.context] * w.batch
+        w.description += f" [context set to {args.context} for a size sweep]"
     if world > 1:
         import torch.distributed as dist
 

@@ -94,6 +94,7 @@ __device__ void combine_bh(const CombineParams& p, int bh, int nw, int warp, int
 // One CTA of W warps (W from the expected partials per unit) per (request, query head).
 __global__ void __launch_bounds__(kMaxWarps * 32) combine_kernel(const CombineParams p) {
     pdl_wait();
+    pdl_trigger();
     combine_bh(p, blockIdx.x, blockDim.x >> 5, threadIdx.x >> 5, threadIdx.x & 31);
 }
 
@@ -154,6 +155,7 @@ cudaError_t launch_scores(const ScoreParams& p, cudaStream_t stream) {
 __global__ void __launch_bounds__(kScoreThreads) epilogue_kernel(const CombineParams c, const ScoreParams sp,
                                                                   int tiles_per_req) {
     pdl_wait();
+    pdl_trigger();
     const int bid = blockIdx.x;
     const int ncomb = c.B * c.n_q;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

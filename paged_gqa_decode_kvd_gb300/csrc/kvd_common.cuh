@@ -228,10 +228,13 @@ __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// Programmatic dependent launch: the split merge is launched as a dependent of the decode
-// kernel.  The decode kernel signals once a CTA has streamed its last block, so the merge
-// grid can be scheduled while the decode grid drains; the merge kernel's first statement
-// waits until the decode grid has completed and its writes are visible.
+// Programmatic dependent launch.  Every kernel of a decode call is launched as a
+// programmatic dependent of the kernel before it in the stream and starts with pdl_wait(),
+// which returns once that kernel has completed and its writes are visible (at once when
+// there is no such kernel), so its CTAs can be resident before the predecessor ends.  The
+// decode kernel signals its dependents once a CTA has streamed its last block; the small
+// merge kernels signal at their start, so the next layer's decode CTAs are scheduled
+// while the merge runs.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 

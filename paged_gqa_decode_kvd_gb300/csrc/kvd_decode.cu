@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int cta = blockIdx.x;
+    pdl_wait();   // the previous kernel of the stream may write any of this kernel's inputs
 
     // ---- plan: blocks per request, prefix sums, this CTA's range -----------------
     for (int b = tid; b < p.B; b += kThreads) {
@@ -673,11 +674,8 @@ cudaError_t launch_decode(const DecodeParams& p, bool fp8, cudaStream_t stream) 
     const size_t smem = decode_smem_bytes(fp8, p.B, p.g);
     cudaError_t e = fp8 ? ensure_smem_attr<true>() : ensure_smem_attr<false>();
     if (e != cudaSuccess) return e;
-    if (fp8)
-        decode_kernel<true><<<p.nsplit, kThreads, smem, stream>>>(p);
-    else
-        decode_kernel<false><<<p.nsplit, kThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    if (fp8) return launch_dependent(decode_kernel<true>, dim3(p.nsplit), dim3(kThreads), smem, stream, p);
+    return launch_dependent(decode_kernel<false>, dim3(p.nsplit), dim3(kThreads), smem, stream, p);
 }
 
 // ---------------------------------------------------------------- wait self-test
