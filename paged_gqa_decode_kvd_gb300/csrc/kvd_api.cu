@@ -241,6 +241,7 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     p.g = g;
     p.n_q = n_q;
     p.nsplit = S;
+    p.max_seq_len = max_seq_len;
     p.scale_log2 = softmax_scale * kvd::kLog2e;
     cudaError_t e = kvd::launch_decode(p, fp8, s);
     if (e != cudaSuccess) return KVD_ERR_CUDA;

@@ -55,7 +55,7 @@ struct Cfg {
 };
 
 struct Smem {
-    int ring_off, full_off, empty_off, meta_off, merge_off, pref_off, abort_off, flag_off, total;
+    int ring_off, full_off, empty_off, meta_off, merge_off, pref_off, lens_off, abort_off, flag_off, total;
 };
 
 template <bool FP8>
@@ -76,6 +76,8 @@ __host__ __device__ inline Smem smem_layout(int batch, int g) {
     o += 2 * merge_floats(g) * 4;
     s.pref_off = o;
     o += (batch + 1) * 4;
+    s.lens_off = o;
+    o += batch * 4;
     s.abort_off = o;
     o += 4;
     s.flag_off = o;
@@ -134,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
     int* meta = reinterpret_cast<int*>(smem + L.meta_off);
     float* merge = reinterpret_cast<float*>(smem + L.merge_off);
     int* pref = reinterpret_cast<int*>(smem + L.pref_off);
+    int* lens = reinterpret_cast<int*>(smem + L.lens_off);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_off);
 
     const int tid = threadIdx.x;
@@ -141,10 +144,28 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
     const int lane = tid & 31;
     const int cta = blockIdx.x;
     pdl_wait();   // the previous kernel of the stream may write any of this kernel's inputs
+    if (warp == kNcw) {
+        // Warm L2 with the block-table row this CTA would start on if every request had
+        // max_seq_len tokens (exact for uniform batches, a harmless miss otherwise); the real
+        // loads come after the plan below.
+        const int64_t nbg = (static_cast<int64_t>(p.max_seq_len) + kBs - 1) / kBs;
+        const int64_t tg = nbg * p.n_kv * p.B;
+        const int64_t lg = ((tg + p.nsplit - 1) / p.nsplit) * cta;
+        if (nbg > 0 && lg < tg && lane < 2) {
+            const int64_t ug = lg / nbg;
+            const int64_t bg = ug / p.n_kv;
+            const int64_t jg = lg % nbg + 32 * lane;
+            if (bg < p.B && jg < p.max_blocks) {
+                const int32_t* a = p.block_table + bg * p.max_blocks + jg;
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+            }
+        }
+    }
 
     // ---- plan: blocks per request, prefix sums, this CTA's range -----------------
     for (int b = tid; b < p.B; b += kThreads) {
         const int len = p.seq_lens[b];
+        lens[b] = len;
         int n = (len + kBs - 1) / kBs;
         if (len < 1 || n > p.max_blocks) {
             n = 0;
@@ -207,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
         for (int64_t x = lo; x < hi && !aborted;) {
             const Segment sg = find_segment(pref, p.B, p.n_kv, x, hi);
             const int32_t* bt = p.block_table + static_cast<int64_t>(sg.b) * p.max_blocks;
-            const int len = p.seq_lens[sg.b];
+            const int len = lens[sg.b];
             if (p.k_new && sg.j1 == sg.nblk) {
                 // Fused append: this CTA owns the unit's last block, so it writes the new token
                 // (position len-1) into the pool before it bulk-copies that block.
@@ -290,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
     for (int64_t x = lo; x < hi;) {
         const Segment sg = find_segment(pref, p.B, p.n_kv, x, hi);
         const int nseg = sg.j1 - sg.j0;
-        const int len = p.seq_lens[sg.b];
+        const int len = lens[sg.b];
         const int u = sg.b * p.n_kv + sg.kvh;
 
         // Q^T fragments (B operand): head gid, dims 16i + 2tq + {0,1,8,9}.

@@ -42,6 +42,7 @@ struct DecodeParams {
     int g;
     int n_q;
     int nsplit;
+    int max_seq_len;             // host bound on seq_lens (only used to warm L2)
     float scale_log2;            // softmax_scale * log2(e)
 };
 
