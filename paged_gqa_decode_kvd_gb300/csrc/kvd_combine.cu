@@ -111,38 +111,57 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
                             dim3(combine_warps(p.slots_hint) * 32), 0, stream, p);
 }
 
-// Importance-score update of positions [t0, t0 + blockDim.x) of request b, one thread per
-// position: scores[b][t] += inv_LH · Σ_h exp(logits[b][h][t] − lse[h]), heads in order
-// h = 0 .. n_q-1, with the n_q final LSEs staged in shared memory.
+// Importance-score update of a tile of kScorePos·blockDim.x positions of request b, each
+// thread taking kScorePos positions blockDim.x apart (warp loads stay coalesced):
+// scores[b][t] += inv_LH · Σ_h exp(logits[b][h][t] − lse[h]), heads in order h = 0..n_q-1.
+// The n_q final LSEs are staged in shared memory in the exp2 domain, so each term is one
+// FFMA and one ex2.approx (relative error about 1e-6, well inside the 1e-5 score bound).
 constexpr int kScoreThreads = 256;
+constexpr int kScorePos = 1;
+constexpr int kScoreTile = kScoreThreads * kScorePos;
 constexpr int kMaxHeads = 256;
 
-__device__ void scores_tile(const ScoreParams& p, const float* s_lse, int b, int t0) {
-    const int t = t0 + threadIdx.x;
+__device__ void scores_tile(const ScoreParams& p, const float* s_lse2, int b, int t0) {
     const int len = p.seq_lens[b];
-    if (t >= len || t >= p.logits_stride || t >= p.scores_stride) return;
-    const float* lrow = p.logits + static_cast<int64_t>(b) * p.n_q * p.logits_stride + t;
-    float acc = 0.f;
-    #pragma unroll 8
-    for (int h = 0; h < p.n_q; ++h) {
-        const float m = s_lse[h];
-        const float x = lrow[static_cast<int64_t>(h) * p.logits_stride];
-        acc += m == -INFINITY ? 0.f : expf(x - m);
+    int64_t lim = p.logits_stride < p.scores_stride ? p.logits_stride : p.scores_stride;
+    if (len < lim) lim = len;
+    const float* lrow = p.logits + static_cast<int64_t>(b) * p.n_q * p.logits_stride;
+    float acc[kScorePos];
+    int tt[kScorePos];
+    #pragma unroll
+    for (int k = 0; k < kScorePos; ++k) {
+        acc[k] = 0.f;
+        tt[k] = t0 + threadIdx.x + k * kScoreThreads;
     }
-    p.scores[static_cast<int64_t>(b) * p.scores_stride + t] += acc * p.inv_LH;
+    if (tt[0] >= lim) return;
+    #pragma unroll 4
+    for (int h = 0; h < p.n_q; ++h) {
+        const float m2 = s_lse2[h];
+        if (m2 == -INFINITY) continue;                 // head with no retained position
+        const float* hrow = lrow + static_cast<int64_t>(h) * p.logits_stride;
+        #pragma unroll
+        for (int k = 0; k < kScorePos; ++k)
+            if (tt[k] < lim) acc[k] += ex2(fmaf(hrow[tt[k]], kLog2e, -m2));
+    }
+    #pragma unroll
+    for (int k = 0; k < kScorePos; ++k)
+        if (tt[k] < lim) p.scores[static_cast<int64_t>(b) * p.scores_stride + tt[k]] += acc[k] * p.inv_LH;
 }
 
 __global__ void __launch_bounds__(kScoreThreads) scores_kernel(const ScoreParams p) {
-    __shared__ float s_lse[kMaxHeads];
+    __shared__ float s_lse2[kMaxHeads];
     const int b = blockIdx.y;
-    for (int h = threadIdx.x; h < p.n_q; h += blockDim.x) s_lse[h] = p.lse[static_cast<int64_t>(b) * p.n_q + h];
+    for (int h = threadIdx.x; h < p.n_q; h += blockDim.x) {
+        const float m = p.lse[static_cast<int64_t>(b) * p.n_q + h];
+        s_lse2[h] = m == -INFINITY ? -INFINITY : m * kLog2e;
+    }
     __syncthreads();
-    scores_tile(p, s_lse, b, blockIdx.x * blockDim.x);
+    scores_tile(p, s_lse2, b, blockIdx.x * kScoreTile);
 }
 
 cudaError_t launch_scores(const ScoreParams& p, cudaStream_t stream) {
     const int64_t extent = p.logits_stride < p.scores_stride ? p.logits_stride : p.scores_stride;
-    dim3 grid(static_cast<unsigned>((extent + kScoreThreads - 1) / kScoreThreads), p.B);
+    dim3 grid(static_cast<unsigned>((extent + kScoreTile - 1) / kScoreTile), p.B);
     scores_kernel<<<grid, kScoreThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
@@ -188,15 +207,15 @@ __global__ void __launch_bounds__(kScoreThreads) epilogue_kernel(const CombinePa
             for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
             lse = L > 0.f ? M + logf(L) : -INFINITY;
         }
-        if (lane == 0) s_lse[h] = lse;
+        if (lane == 0) s_lse[h] = lse == -INFINITY ? -INFINITY : lse * kLog2e;
     }
     __syncthreads();
-    scores_tile(sp, s_lse, b, tile * kScoreThreads);
+    scores_tile(sp, s_lse, b, tile * kScoreTile);
 }
 
 cudaError_t launch_epilogue(const CombineParams& c, const ScoreParams& sp, cudaStream_t stream) {
     const int64_t extent = sp.logits_stride < sp.scores_stride ? sp.logits_stride : sp.scores_stride;
-    const int tiles = static_cast<int>((extent + kScoreThreads - 1) / kScoreThreads);
+    const int tiles = static_cast<int>((extent + kScoreTile - 1) / kScoreTile);
     const int64_t ctas = static_cast<int64_t>(c.B) * c.n_q + static_cast<int64_t>(c.B) * tiles;
     return launch_dependent(epilogue_kernel, dim3(static_cast<unsigned>(ctas)), dim3(kScoreThreads), 0, stream, c, sp,
                             tiles);
