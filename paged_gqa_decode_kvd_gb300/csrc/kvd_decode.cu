@@ -392,10 +392,11 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
                 #pragma unroll
                 for (int u4 = 0; u4 < 4; ++u4) {
                     const uint4 w = kt[u4 * 32 + lane];
-                    const uint32_t fa[4] = {e4m3x2_to_f16x2(w.x & 0xffff), e4m3x2_to_f16x2(w.x >> 16),
-                                            e4m3x2_to_f16x2(w.y & 0xffff), e4m3x2_to_f16x2(w.y >> 16)};
-                    const uint32_t fb[4] = {e4m3x2_to_f16x2(w.z & 0xffff), e4m3x2_to_f16x2(w.z >> 16),
-                                            e4m3x2_to_f16x2(w.w & 0xffff), e4m3x2_to_f16x2(w.w >> 16)};
+                    uint32_t fa[4], fb[4];
+                    e4m3x4_to_f16x2x2(w.x, fa[0], fa[1]);
+                    e4m3x4_to_f16x2x2(w.y, fa[2], fa[3]);
+                    e4m3x4_to_f16x2x2(w.z, fb[0], fb[1]);
+                    e4m3x4_to_f16x2x2(w.w, fb[2], fb[3]);
                     mma_f16(ca, fa, qf[2 * u4][0], qf[2 * u4][1]);
                     mma_f16(cb, fb, qf[2 * u4 + 1][0], qf[2 * u4 + 1][1]);
                 }
@@ -523,10 +524,11 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
                     #pragma unroll
                     for (int i = 0; i < 2; ++i) {
                         const int u4 = 2 * half + i;
-                        const uint32_t fa[4] = {e4m3x2_to_f16x2(vv[i].x & 0xffff), e4m3x2_to_f16x2(vv[i].x >> 16),
-                                                e4m3x2_to_f16x2(vv[i].y & 0xffff), e4m3x2_to_f16x2(vv[i].y >> 16)};
-                        const uint32_t fb[4] = {e4m3x2_to_f16x2(vv[i].z & 0xffff), e4m3x2_to_f16x2(vv[i].z >> 16),
-                                                e4m3x2_to_f16x2(vv[i].w & 0xffff), e4m3x2_to_f16x2(vv[i].w >> 16)};
+                        uint32_t fa[4], fb[4];
+                        e4m3x4_to_f16x2x2(vv[i].x, fa[0], fa[1]);
+                        e4m3x4_to_f16x2x2(vv[i].y, fa[2], fa[3]);
+                        e4m3x4_to_f16x2x2(vv[i].z, fb[0], fb[1]);
+                        e4m3x4_to_f16x2x2(vv[i].w, fb[2], fb[3]);
                         mma_f16(o[2 * u4], fa, pb0, pb1);
                         mma_f16(o[2 * u4 + 1], fb, pb0, pb1);
                     }
