@@ -252,7 +252,7 @@ class Step:
                                  lse_out=self.lse if scores else None, logits_out=self.logits if scores else None,
                                  k_new=self.k_new[t][layer], v_new=self.v_new[t][layer],
                                  scores=self.scores if scores else None, inv_LH=1.0 / (self.w.L * self.w.n_q),
-                                 stream=stream)
+                                 early_start=True, stream=stream)
 
     def decode_kernel_only(self, layer: int, t: int = 0, stream=None):
         """The layer's decode kernel alone (fused append, partials, no merge launch)."""
@@ -260,7 +260,8 @@ class Step:
         self.kvd.kvd_decode_attn(self.pool.handle, layer, self.q[t][layer], self.bt, self.seq[t], self.max_len,
                                  self.ws, None, num_splits=self.splits, retain_mask=self.retain,
                                  logits_out=self.logits if scores else None,
-                                 k_new=self.k_new[t][layer], v_new=self.v_new[t][layer], stream=stream)
+                                 k_new=self.k_new[t][layer], v_new=self.v_new[t][layer], early_start=True,
+                                 stream=stream)
 
     def capture_decode_only(self):
         import torch

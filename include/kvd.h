@@ -89,6 +89,15 @@ typedef struct {
 
 typedef struct kvd_pool kvd_pool;  /* opaque */
 
+/* Flags of kvd_decode_attn.
+ * KVD_EARLY_START: the caller promises that block_table, seq_lens, retain_mask and the pool
+ *   contents (all but the slot the fused append writes) are not written by the kernel that
+ *   precedes this call in the stream.  The decode kernel, launched as a programmatic
+ *   dependent of that kernel, may then plan its split and start copying K/V while that
+ *   kernel is still running; reads of q, k_new, v_new and every write still wait for it to
+ *   complete.  Without the flag the kernel waits before touching any global memory. */
+#define KVD_EARLY_START 1u
+
 /* Optional score epilogue of kvd_decode_attn: adds this layer's share of the cumulative
  * importance score, scores[b][t] += inv_LH · Σ_h α_h[t], exactly as kvd_accum_scores would
  * from the call's logits and final LSE, but inside the call's merge launch. */
@@ -163,6 +172,7 @@ KVD_API kvd_status kvd_decode_workspace_bytes(const kvd_pool* pool, int n_q, int
  *               every attended position (−inf where evicted), input of kvd_accum_scores
  *  scores_epilogue  NULL, or the score update to fuse into the merge launch (needs out and
  *               logits_out; n_q ≤ 256)
+ *  flags        0 or KVD_EARLY_START (see above); other bits are KVD_ERR_INVALID
  * Query head h reads KV head h / g.  A head with no retained position gets out = 0 and
  * lse = −inf. */
 KVD_API kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q,
@@ -173,7 +183,7 @@ KVD_API kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int
                            void* workspace, size_t workspace_bytes,
                            void* out, int out_dtype, float* lse_out,
                            float* logits_out, int64_t logits_stride,
-                           const kvd_scores_desc* scores_epilogue, void* stream);
+                           const kvd_scores_desc* scores_epilogue, unsigned flags, void* stream);
 
 /* Size of the fixed device scratch array used by kvd_decode_attn_noalloc: 16 MiB, held on
  * every GPU that loads the library until the process exits. */
@@ -202,7 +212,8 @@ KVD_API kvd_status kvd_decode_attn_noalloc(kvd_pool* pool, int layer, const void
                                            const uint16_t* retain_mask, float softmax_scale,
                                            void* out, int out_dtype, float* lse_out,
                                            float* logits_out, int64_t logits_stride,
-                                           const kvd_scores_desc* scores_epilogue, void* stream);
+                                           const kvd_scores_desc* scores_epilogue, unsigned flags,
+                                           void* stream);
 
 /* Merge split partials by log-sum-exp.  For unit u = b·n_kv + h/g and head h:
  * LSE = log Σ_s exp(lse_s), out = Σ_s exp(lse_s − LSE)·o_s over the unit_count[u] slots

@@ -13,6 +13,7 @@ import os
 
 KVD_OK, KVD_ERR_INVALID, KVD_ERR_UNSUPPORTED, KVD_ERR_NOMEM, KVD_ERR_CUDA, KVD_ERR_OOB, KVD_ERR_TIMEOUT = range(7)
 KVD_BF16, KVD_FP8_E4M3, KVD_F32 = 0, 1, 2
+KVD_EARLY_START = 1   # kvd_decode_attn flag
 
 SYMBOLS = [
     "kvd_status_string", "kvd_pool_bytes", "kvd_pool_create", "kvd_pool_destroy", "kvd_append_kv",
@@ -71,7 +72,7 @@ def load(build_if_missing: bool = True):
     lib.kvd_decode_workspace_bytes.argtypes = [P, i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(sz)]
     lib.kvd_decode_attn.restype = i32
     lib.kvd_decode_attn.argtypes = [P, i32, P, i32, P, P, P, i32, P, i32, i32, i32, P, f32, P, sz, P, i32, P, P, i64,
-                                    P, P]
+                                    P, ctypes.c_uint, P]
     lib.kvd_combine_splits.restype = i32
     lib.kvd_combine_splits.argtypes = [P, P, P, P, i32, i32, i32, i32, P, i32, P, P]
     lib.kvd_accum_scores.restype = i32
@@ -82,7 +83,7 @@ def load(build_if_missing: bool = True):
     lib.kvd_selftest_wait_timeout.argtypes = [P, i64, P]
     lib.kvd_decode_attn_noalloc.restype = i32
     lib.kvd_decode_attn_noalloc.argtypes = [P, i32, P, i32, P, P, P, i32, P, i32, i32, i32, P, f32, P, i32, P, P,
-                                            i64, P, P]
+                                            i64, P, ctypes.c_uint, P]
     _lib = lib
     return lib
 
@@ -150,7 +151,7 @@ def _scores_desc(scores, inv_LH):
 
 def kvd_decode_attn(handle, layer, q, block_table, seq_lens, max_seq_len, workspace, out, num_splits=0,
                     retain_mask=None, softmax_scale=None, lse_out=None, logits_out=None, k_new=None, v_new=None,
-                    scores=None, inv_LH=None, stream=None):
+                    scores=None, inv_LH=None, early_start=False, stream=None):
     batch, n_q, d_h = q.shape
     if softmax_scale is None:
         softmax_scale = d_h ** -0.5
@@ -161,7 +162,7 @@ def kvd_decode_attn(handle, layer, q, block_table, seq_lens, max_seq_len, worksp
         _ptr(seq_lens), batch,
         int(max_seq_len), int(num_splits), _ptr(retain_mask), float(softmax_scale), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(out), out_dtype, _ptr(lse_out), _ptr(logits_out),
-        lstride, _scores_desc(scores, inv_LH), _stream(stream)))
+        lstride, _scores_desc(scores, inv_LH), KVD_EARLY_START if early_start else 0, _stream(stream)))
 
 
 def kvd_combine_splits(part_o, part_lse, unit_first, unit_count, batch, n_q, n_kv, out, lse_out=None, stream=None):
@@ -190,7 +191,7 @@ def kvd_selftest_wait_timeout(handle, timeout_ns, stream=None):
 
 def kvd_decode_attn_noalloc(handle, layer, q, block_table, seq_lens, max_seq_len, out, num_splits=0,
                             retain_mask=None, softmax_scale=None, lse_out=None, logits_out=None, k_new=None,
-                            v_new=None, scores=None, inv_LH=None, stream=None):
+                            v_new=None, scores=None, inv_LH=None, early_start=False, stream=None):
     """kvd_decode_attn without a workspace argument: the library's fixed device scratch array is used."""
     batch, n_q, d_h = q.shape
     if softmax_scale is None:
@@ -201,4 +202,5 @@ def kvd_decode_attn_noalloc(handle, layer, q, block_table, seq_lens, max_seq_len
         handle, layer, _ptr(q), n_q, _ptr(k_new), _ptr(v_new), _ptr(block_table), block_table.shape[1],
         _ptr(seq_lens), batch,
         int(max_seq_len), int(num_splits), _ptr(retain_mask), float(softmax_scale), _ptr(out), out_dtype,
-        _ptr(lse_out), _ptr(logits_out), lstride, _scores_desc(scores, inv_LH), _stream(stream)))
+        _ptr(lse_out), _ptr(logits_out), lstride, _scores_desc(scores, inv_LH),
+        KVD_EARLY_START if early_start else 0, _stream(stream)))

@@ -190,11 +190,13 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
                            int max_seq_len,
                            int num_splits, const uint16_t* retain_mask, float softmax_scale, void* workspace,
                            size_t workspace_bytes, void* out, int out_dtype, float* lse_out, float* logits_out,
-                           int64_t logits_stride, const kvd_scores_desc* scores_epilogue, void* stream) {
+                           int64_t logits_stride, const kvd_scores_desc* scores_epilogue, unsigned flags,
+                           void* stream) {
     kvd_status st = check_decode_shape(pool, n_q, batch, max_seq_len);
     if (st != KVD_OK) return st;
     if (layer < 0 || layer >= pool->desc.num_layers || num_splits < 0 || max_blocks_per_seq < 1) return KVD_ERR_INVALID;
     if (out_dtype != KVD_BF16 && out_dtype != KVD_F32) return KVD_ERR_INVALID;
+    if (flags & ~static_cast<unsigned>(KVD_EARLY_START)) return KVD_ERR_INVALID;
     if (batch == 0) return KVD_OK;
     if (!q || !block_table || !seq_lens || !workspace) return KVD_ERR_INVALID;
     if ((k_new == nullptr) != (v_new == nullptr)) return KVD_ERR_INVALID;
@@ -242,6 +244,7 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     p.n_q = n_q;
     p.nsplit = S;
     p.max_seq_len = max_seq_len;
+    p.early = (flags & KVD_EARLY_START) ? 1 : 0;
     p.scale_log2 = softmax_scale * kvd::kLog2e;
     cudaError_t e = kvd::launch_decode(p, fp8, s);
     if (e != cudaSuccess) return KVD_ERR_CUDA;

@@ -143,7 +143,11 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int cta = blockIdx.x;
-    pdl_wait();   // the previous kernel of the stream may write any of this kernel's inputs
+    // The previous kernel of the stream may write any input.  With p.early the caller has
+    // promised that the block table, lengths, retain mask and the pool (except the slot the
+    // fused append writes) are not among them: the plan and the K/V copies start at once,
+    // and only the reads of q / k_new / v_new and every global write wait below.
+    if (!p.early) pdl_wait();
     if (warp == kNcw) {
         // Warm L2 with the block-table row this CTA would start on if every request had
         // max_seq_len tokens (exact for uniform batches, a harmless miss otherwise); the real
@@ -208,10 +212,11 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
     const int64_t lo = chunk * cta;
     const int64_t hi = (lo + chunk < T) ? lo + chunk : T;
 
-    // Units with no block: no CTA covers them, so CTA 0 marks them empty.
-    if (cta == 0) {
+    // Units with no block: no CTA covers them, so CTA 0's consumer warps mark them empty.
+    if (cta == 0 && warp < kNcw) {
+        if (p.early) pdl_wait();
         const int U = p.B * p.n_kv;
-        for (int u = tid; u < U; u += kThreads) {
+        for (int u = tid; u < U; u += kNcw * 32) {
             const int b = u / p.n_kv;
             if (pref[b + 1] == pref[b]) {
                 p.unit_first[u] = 0;
@@ -234,6 +239,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
                 // (position len-1) into the pool before it bulk-copies that block.
                 const int pos = len - 1;
                 const int ph = bt[pos / kBs];
+                if (p.early) pdl_wait();   // k_new / v_new come from the previous kernel
                 if (ph >= 0 && ph < p.num_blocks) {
                     const int64_t row = (static_cast<int64_t>(sg.b) * p.n_kv + sg.kvh) * kDh;
                     uint8_t* rec = const_cast<uint8_t*>(p.kv) + (static_cast<int64_t>(ph) * p.n_kv + sg.kvh) * Cfg<FP8>::kRecord;
@@ -307,6 +313,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
     const int tq = lane & 3;     // head pair 2tq, 2tq+1
     const int h0 = 2 * tq, h1 = 2 * tq + 1;
     const int g = p.g;
+    if (p.early) pdl_wait();   // q and every output of this kernel
     uint32_t k = 0;
     for (int64_t x = lo; x < hi;) {
         const Segment sg = find_segment(pref, p.B, p.n_kv, x, hi);

@@ -43,6 +43,7 @@ struct DecodeParams {
     int n_q;
     int nsplit;
     int max_seq_len;             // host bound on seq_lens (only used to warm L2)
+    int early;                   // KVD_EARLY_START: plan and K/V copies before the grid dependency wait
     float scale_log2;            // softmax_scale * log2(e)
 };
 

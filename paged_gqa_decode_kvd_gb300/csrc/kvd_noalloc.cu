@@ -50,7 +50,7 @@ extern "C" kvd_status kvd_decode_attn_noalloc(kvd_pool* pool, int layer, const v
                                               const uint16_t* retain_mask, float softmax_scale, void* out,
                                               int out_dtype, float* lse_out, float* logits_out,
                                               int64_t logits_stride, const kvd_scores_desc* scores_epilogue,
-                                              void* stream) {
+                                              unsigned flags, void* stream) {
     if (!out && batch > 0) return KVD_ERR_INVALID;  // the partials would be unreachable
     int splits = 0;
     size_t need = 0;
@@ -63,5 +63,5 @@ extern "C" kvd_status kvd_decode_attn_noalloc(kvd_pool* pool, int layer, const v
     return kvd_decode_attn(pool, layer, q, n_q, k_new, v_new, block_table, max_blocks_per_seq, seq_lens, batch,
                            max_seq_len,
                            splits, retain_mask, softmax_scale, scratch, static_cast<size_t>(KVD_NOALLOC_SCRATCH_BYTES),
-                           out, out_dtype, lse_out, logits_out, logits_stride, scores_epilogue, stream);
+                           out, out_dtype, lse_out, logits_out, logits_stride, scores_epilogue, flags, stream);
 }

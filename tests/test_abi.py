@@ -76,9 +76,9 @@ def test_null_arguments_fail_before_any_launch():
     assert lib.kvd_pool_create(ctypes.byref(d), P(16), 10, ctypes.byref(h)) == kvd.KVD_ERR_NOMEM
     assert lib.kvd_pool_create(ctypes.byref(d), P(8), 1 << 30, ctypes.byref(h)) == kvd.KVD_ERR_INVALID
     assert lib.kvd_decode_attn(None, 0, None, 32, None, None, None, 1, None, 1, 1, 0, None, 0.1, None, 0, None, 0,
-                               None, None, 0, None, None) == kvd.KVD_ERR_INVALID
+                               None, None, 0, None, 0, None) == kvd.KVD_ERR_INVALID
     assert lib.kvd_decode_attn_noalloc(None, 0, None, 32, None, None, None, 1, None, 1, 1, 0, None, 0.1, None, 0,
-                                       None, None, 0, None, None) == kvd.KVD_ERR_INVALID
+                                       None, None, 0, None, 0, None) == kvd.KVD_ERR_INVALID
     assert lib.kvd_append_kv(None, 0, None, None, None, 1, None) == kvd.KVD_ERR_INVALID
     assert lib.kvd_combine_splits(None, None, None, None, 1, 32, 8, 64, None, 0, None, None) == \
         kvd.KVD_ERR_UNSUPPORTED

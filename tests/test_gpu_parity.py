@@ -427,3 +427,47 @@ def test_fused_score_epilogue_matches_accum_scores(cuda_device):
     for b, n in enumerate(w.seq_lens()):
         want = ref["alpha"][b, :, :n].sum(0) * inv
         assert np.all(np.abs(got[b, :n] - want) <= H.SCORE_RTOL * want + 2 ** -22 * base[b, :n].double().cpu().numpy())
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_early_start_is_bitwise_identical(cuda_device, kv_dtype):
+    """KVD_EARLY_START (plan and K/V copies before the grid-dependency wait) changes no bit, also
+    for back-to-back calls of two layers captured in one CUDA graph, where the overlap happens."""
+    w = _custom(f"early_{kv_dtype}", 32, 8, [3000, 17, 1200, 640], kv_dtype=kv_dtype, L=2, seed=8)
+    dev = cuda_device
+    bt, bt_d, seq, seq_d, _ = H.device_inputs(w, dev)
+    prefix = [c - 1 for c in w.seq_lens()]
+    pos = w.append_pos(0)
+    S = max(w.seq_lens())
+    results = []
+    for early in (False, True):
+        pool = H.make_pool(w, layers=2)
+        kn, vn, qs = [], [], []
+        for layer in range(2):
+            H.fill_layer(pool, w, layer, bt, prefix, dev)
+            ks, vs = zip(*[w.kv(layer, b, pos[b], pos[b] + 1, dev) for b in range(w.batch)])
+            kn.append(torch.cat(ks).contiguous())
+            vn.append(torch.cat(vs).contiguous())
+            qs.append(w.q(layer, 0, dev))
+        _, ws = H.workspace(pool, w.n_q, w.batch, S, 0, dev)
+        outs = [torch.empty(w.batch, w.n_q, 128, dtype=torch.float32, device=dev) for _ in range(2)]
+
+        def step():
+            for layer in range(2):
+                kvd.kvd_decode_attn(pool.handle, layer, qs[layer], bt_d, seq_d, S, ws, outs[layer],
+                                    k_new=kn[layer], v_new=vn[layer], early_start=early)
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            step()
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        assert kvd.kvd_get_device_error(pool.handle) == 0
+        results.append([o.cpu() for o in outs] + [pool.mem.cpu()])
+    for a, b in zip(*results):
+        assert torch.equal(a, b)
