@@ -179,13 +179,14 @@ class Step:
     per step index and the timed loop cycles through them.  With scores on, each layer
     also writes its logits and adds its share of the importance score."""
 
-    def __init__(self, w, dev, num_splits: int = 0):
+    def __init__(self, w, dev, num_splits: int = 0, early: bool = True):
         import numpy as np
         import torch
 
         import paged_gqa_decode_kvd_gb300 as kvd
 
         self.w, self.dev, self.kvd = w, dev, kvd
+        self.early = early   # KVD_EARLY_START: the step's tables and pool are not written by the previous kernel
         self.L = w.L
         self.fp8 = w.kv_dtype != "bf16"
         self.pool = kvd.KVPool(w.L, w.n_kv, w.num_blocks(), kvd.KVD_FP8_E4M3 if self.fp8 else kvd.KVD_BF16,
@@ -252,7 +253,7 @@ class Step:
                                  lse_out=self.lse if scores else None, logits_out=self.logits if scores else None,
                                  k_new=self.k_new[t][layer], v_new=self.v_new[t][layer],
                                  scores=self.scores if scores else None, inv_LH=1.0 / (self.w.L * self.w.n_q),
-                                 early_start=True, stream=stream)
+                                 early_start=self.early, stream=stream)
 
     def decode_kernel_only(self, layer: int, t: int = 0, stream=None):
         """The layer's decode kernel alone (fused append, partials, no merge launch)."""
@@ -260,7 +261,7 @@ class Step:
         self.kvd.kvd_decode_attn(self.pool.handle, layer, self.q[t][layer], self.bt, self.seq[t], self.max_len,
                                  self.ws, None, num_splits=self.splits, retain_mask=self.retain,
                                  logits_out=self.logits if scores else None,
-                                 k_new=self.k_new[t][layer], v_new=self.v_new[t][layer], early_start=True,
+                                 k_new=self.k_new[t][layer], v_new=self.v_new[t][layer], early_start=self.early,
                                  stream=stream)
 
     def capture_decode_only(self):
@@ -302,7 +303,7 @@ def gpu_arm(args, w, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     peaks = measured_peaks()
-    st = Step(w, dev, args.num_splits)
+    st = Step(w, dev, args.num_splits, early=not args.no_early_start)
     graphs = st.capture()
     stream = torch.cuda.current_stream(dev)
     # closed-form KV bytes of the timed steps (step t of the workload = graph t % steps)
@@ -466,6 +467,7 @@ def main(argv=None):
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling captures)")
     ap.add_argument("--context", type=int, default=0, help="override every request's context (size sweeps)")
+    ap.add_argument("--no-early-start", action="store_true", help="launch the decode kernel without KVD_EARLY_START")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")

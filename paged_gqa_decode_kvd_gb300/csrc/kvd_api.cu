@@ -246,7 +246,8 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     p.max_seq_len = max_seq_len;
     p.early = (flags & KVD_EARLY_START) ? 1 : 0;
     p.scale_log2 = softmax_scale * kvd::kLog2e;
-    cudaError_t e = kvd::launch_decode(p, fp8, s);
+    const int carveout = kvd::decode_carveout(fp8, batch, g);
+    cudaError_t e = kvd::launch_decode(p, fp8, carveout, s);
     if (e != cudaSuccess) return KVD_ERR_CUDA;
     if (!out) return KVD_OK;  // partials only: the caller merges them with kvd_combine_splits
 
@@ -263,7 +264,7 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     c.g = g;
     c.out_f32 = out_dtype == KVD_F32;
     c.slots_hint = S / U + 2;
-    if (!scores_epilogue) return cuda_status(kvd::launch_combine(c, s));
+    if (!scores_epilogue) return cuda_status(kvd::launch_combine(c, carveout, s));
     kvd::ScoreParams sp;
     sp.logits = logits_out;
     sp.logits_stride = logits_stride;
@@ -274,7 +275,7 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     sp.B = batch;
     sp.n_q = n_q;
     sp.inv_LH = scores_epilogue->inv_LH;
-    return cuda_status(kvd::launch_epilogue(c, sp, s));
+    return cuda_status(kvd::launch_epilogue(c, sp, carveout, s));
 }
 
 kvd_status kvd_combine_splits(const float* part_o, const float* part_lse, const int32_t* unit_first,
@@ -299,7 +300,7 @@ kvd_status kvd_combine_splits(const float* part_o, const float* part_lse, const 
     c.g = n_q / n_kv;
     c.out_f32 = out_dtype == KVD_F32;
     c.slots_hint = 64;   // counts unknown on the host: assume many partials per unit
-    return cuda_status(kvd::launch_combine(c, static_cast<cudaStream_t>(stream)));
+    return cuda_status(kvd::launch_combine(c, -1, static_cast<cudaStream_t>(stream)));
 }
 
 kvd_status kvd_accum_scores(const float* logits, int64_t logits_stride, const float* lse, const int32_t* seq_lens,

@@ -17,15 +17,19 @@ namespace kvd {
 
 // Merge of one (request, query head) by the nw warps of a CTA.  Warp w folds slots
 // s ≡ w (mod nw) in one online pass (running max, rescaled sum and accumulator; lane l owns
-// dims 4l..4l+3), then warp 0 merges the warps' states.  A unit whose output the decode
-// kernel already wrote (count < 0) is skipped; a unit with no partial (count 0) gets
+// dims 4l..4l+3); with several warps, warp 0 then merges their states, handed over in `red`
+// (red_bytes(nw) of shared memory; a single warp needs none).  A unit whose output the
+// decode kernel already wrote (count < 0) is skipped; a unit with no partial (count 0) gets
 // out = 0 and lse = −inf.
 constexpr int kMaxWarps = 16;
 
-__device__ void combine_bh(const CombineParams& p, int bh, int nw, int warp, int lane) {
-    __shared__ float s_m[kMaxWarps];
-    __shared__ float s_l[kMaxWarps];
-    __shared__ float4 s_acc[kMaxWarps][32];
+__host__ __device__ constexpr int red_bytes(int nw) {
+    return nw > 1 ? nw * 32 * static_cast<int>(sizeof(float4)) + 2 * nw * static_cast<int>(sizeof(float)) : 0;
+}
+
+extern __shared__ float4 dyn_smem[];
+
+__device__ void combine_bh(const CombineParams& p, int bh, int nw, int warp, int lane, float4* red) {
     const int b = bh / p.n_q;
     const int h = bh % p.n_q;
     const int u = b * p.n_kv + h / p.g;
@@ -52,26 +56,32 @@ __device__ void combine_bh(const CombineParams& p, int bh, int nw, int warp, int
         acc.w = acc.w * a + w * v.w;
         m = mn;
     }
-    s_acc[warp][lane] = acc;
-    if (lane == 0) {
-        s_m[warp] = m;
-        s_l[warp] = l;
-    }
-    __syncthreads();
-    if (warp != 0) return;
-    float M = -INFINITY;
-    for (int w = 0; w < nw; ++w) M = fmaxf(M, s_m[w]);
-    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-    float L = 0.f;
-    if (M != -INFINITY) {
-        for (int w = 0; w < nw; ++w) {
-            const float e = expf(s_m[w] - M);  // 0 for a warp that saw nothing
-            const float4 v = s_acc[w][lane];
-            L += s_l[w] * e;
-            t.x += v.x * e;
-            t.y += v.y * e;
-            t.z += v.z * e;
-            t.w += v.w * e;
+    float M = m, L = l;
+    float4 t = acc;
+    if (nw > 1) {
+        float* s_m = reinterpret_cast<float*>(red + nw * 32);
+        float* s_l = s_m + nw;
+        red[warp * 32 + lane] = acc;
+        if (lane == 0) {
+            s_m[warp] = m;
+            s_l[warp] = l;
+        }
+        __syncthreads();
+        if (warp != 0) return;
+        M = -INFINITY;
+        for (int w = 0; w < nw; ++w) M = fmaxf(M, s_m[w]);
+        t = make_float4(0.f, 0.f, 0.f, 0.f);
+        L = 0.f;
+        if (M != -INFINITY) {
+            for (int w = 0; w < nw; ++w) {
+                const float e = expf(s_m[w] - M);  // 0 for a warp that saw nothing
+                const float4 v = red[w * 32 + lane];
+                L += s_l[w] * e;
+                t.x += v.x * e;
+                t.y += v.y * e;
+                t.z += v.z * e;
+                t.w += v.w * e;
+            }
         }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
@@ -92,10 +102,12 @@ __device__ void combine_bh(const CombineParams& p, int bh, int nw, int warp, int
 }
 
 // One CTA of W warps (W from the expected partials per unit) per (request, query head).
+// It signals its dependents once its own wait has returned: the next decode kernel is then
+// scheduled while this merge runs.
 __global__ void __launch_bounds__(kMaxWarps * 32) combine_kernel(const CombineParams p) {
     pdl_wait();
     pdl_trigger();
-    combine_bh(p, blockIdx.x, blockDim.x >> 5, threadIdx.x >> 5, threadIdx.x & 31);
+    combine_bh(p, blockIdx.x, blockDim.x >> 5, threadIdx.x >> 5, threadIdx.x & 31, dyn_smem);
 }
 
 static int combine_warps(int slots_hint) {
@@ -106,57 +118,77 @@ static int combine_warps(int slots_hint) {
     return warps;
 }
 
-cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
-    return launch_dependent(combine_kernel, dim3(static_cast<unsigned>(p.B * p.n_q)),
-                            dim3(combine_warps(p.slots_hint) * 32), 0, stream, p);
+// Importance-score update of one position t of request b per thread (a CTA covers
+// kScoreTile consecutive positions, so warp loads stay coalesced):
+// scores[b][t] += inv_LH · Σ_h exp(logits[b][h][t] − lse[h]), heads in order h = 0..n_q-1.
+// score_load starts, before the final LSEs are known, asynchronous 4-byte copies of this
+// thread's logits of the first kPrefetchHeads heads into its own column of a shared tile
+// (no registers held) and loads the running score; score_add waits for its own copies and
+// finishes the sum.  The n_q final LSEs are staged in shared memory in the exp2 domain, so
+// each term is one FFMA and one ex2.approx (relative error about 1e-6, well inside the
+// 1e-5 score bound).
+constexpr int kScoreThreads = 256;
+constexpr int kScoreTile = kScoreThreads;
+constexpr int kMaxHeads = 256;
+constexpr int kPrefetchHeads = 32;
+constexpr int kPrefetchBytes = kPrefetchHeads * kScoreThreads * 4;
+
+__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 
-// Importance-score update of a tile of kScorePos·blockDim.x positions of request b, each
-// thread taking kScorePos positions blockDim.x apart (warp loads stay coalesced):
-// scores[b][t] += inv_LH · Σ_h exp(logits[b][h][t] − lse[h]), heads in order h = 0..n_q-1.
-// The n_q final LSEs are staged in shared memory in the exp2 domain, so each term is one
-// FFMA and one ex2.approx (relative error about 1e-6, well inside the 1e-5 score bound).
-constexpr int kScoreThreads = 256;
-constexpr int kScorePos = 1;
-constexpr int kScoreTile = kScoreThreads * kScorePos;
-constexpr int kMaxHeads = 256;
+struct ScoreLane {
+    float old;      // scores[b][t] before this update
+    int64_t t;
+    bool in_rows;   // t lies inside both row strides (every load is in bounds)
+};
 
-__device__ void scores_tile(const ScoreParams& p, const float* s_lse2, int b, int t0) {
-    const int len = p.seq_lens[b];
-    int64_t lim = p.logits_stride < p.scores_stride ? p.logits_stride : p.scores_stride;
-    if (len < lim) lim = len;
-    const float* lrow = p.logits + static_cast<int64_t>(b) * p.n_q * p.logits_stride;
-    float acc[kScorePos];
-    int tt[kScorePos];
-    #pragma unroll
-    for (int k = 0; k < kScorePos; ++k) {
-        acc[k] = 0.f;
-        tt[k] = t0 + threadIdx.x + k * kScoreThreads;
+// xs: shared [kPrefetchHeads][kScoreThreads] floats; this thread uses column threadIdx.x only.
+__device__ __forceinline__ ScoreLane score_load(const ScoreParams& p, int b, int64_t t, float* xs) {
+    ScoreLane r;
+    r.t = t;
+    r.in_rows = t < p.logits_stride && t < p.scores_stride;
+    if (r.in_rows) {
+        const float* col = p.logits + static_cast<int64_t>(b) * p.n_q * p.logits_stride + t;
+        const int nh = p.n_q < kPrefetchHeads ? p.n_q : kPrefetchHeads;
+        for (int h = 0; h < nh; ++h) cp_async4(xs + h * kScoreThreads + threadIdx.x, col + static_cast<int64_t>(h) * p.logits_stride);
     }
-    if (tt[0] >= lim) return;
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    r.old = r.in_rows ? p.scores[static_cast<int64_t>(b) * p.scores_stride + t] : 0.f;
+    return r;
+}
+
+__device__ __forceinline__ void score_add(const ScoreParams& p, const float* s_lse2, int b, const ScoreLane& r,
+                                          const float* xs) {
+    asm volatile("cp.async.wait_all;" ::: "memory");   // this thread's own copies only
+    if (!r.in_rows || r.t >= p.seq_lens[b]) return;
+    float acc = 0.f;
+    const int nh = p.n_q < kPrefetchHeads ? p.n_q : kPrefetchHeads;
     #pragma unroll 4
-    for (int h = 0; h < p.n_q; ++h) {
+    for (int h = 0; h < nh; ++h) {
         const float m2 = s_lse2[h];
-        if (m2 == -INFINITY) continue;                 // head with no retained position
-        const float* hrow = lrow + static_cast<int64_t>(h) * p.logits_stride;
-        #pragma unroll
-        for (int k = 0; k < kScorePos; ++k)
-            if (tt[k] < lim) acc[k] += ex2(fmaf(hrow[tt[k]], kLog2e, -m2));
+        if (m2 != -INFINITY) acc += ex2(fmaf(xs[h * kScoreThreads + threadIdx.x], kLog2e, -m2));   // -inf: no retained position
     }
-    #pragma unroll
-    for (int k = 0; k < kScorePos; ++k)
-        if (tt[k] < lim) p.scores[static_cast<int64_t>(b) * p.scores_stride + tt[k]] += acc[k] * p.inv_LH;
+    const float* col = p.logits + static_cast<int64_t>(b) * p.n_q * p.logits_stride + r.t;
+    #pragma unroll 4
+    for (int h = kPrefetchHeads; h < p.n_q; ++h) {
+        const float m2 = s_lse2[h];
+        if (m2 != -INFINITY) acc += ex2(fmaf(col[static_cast<int64_t>(h) * p.logits_stride], kLog2e, -m2));
+    }
+    p.scores[static_cast<int64_t>(b) * p.scores_stride + r.t] = r.old + acc * p.inv_LH;
 }
 
 __global__ void __launch_bounds__(kScoreThreads) scores_kernel(const ScoreParams p) {
     __shared__ float s_lse2[kMaxHeads];
+    __shared__ float xs[kPrefetchHeads * kScoreThreads];
     const int b = blockIdx.y;
+    const ScoreLane r = score_load(p, b, static_cast<int64_t>(blockIdx.x) * kScoreTile + threadIdx.x, xs);
     for (int h = threadIdx.x; h < p.n_q; h += blockDim.x) {
         const float m = p.lse[static_cast<int64_t>(b) * p.n_q + h];
         s_lse2[h] = m == -INFINITY ? -INFINITY : m * kLog2e;
     }
     __syncthreads();
-    scores_tile(p, s_lse2, b, blockIdx.x * kScoreTile);
+    score_add(p, s_lse2, b, r, xs);
 }
 
 cudaError_t launch_scores(const ScoreParams& p, cudaStream_t stream) {
@@ -171,7 +203,8 @@ cudaError_t launch_scores(const ScoreParams& p, cudaStream_t stream) {
 // CTA derives the final LSE of every head of its request from the split partials itself
 // (the merge CTAs of the same launch write lse_out concurrently), or reads lse_out where
 // the decode kernel already finished the unit.
-__global__ void __launch_bounds__(kScoreThreads) epilogue_kernel(const CombineParams c, const ScoreParams sp,
+// Six CTAs an SM (at most 42 registers a thread): about as many as the prefetch tiles allow.
+__global__ void __launch_bounds__(kScoreThreads, 6) epilogue_kernel(const CombineParams c, const ScoreParams sp,
                                                                   int tiles_per_req) {
     pdl_wait();
     pdl_trigger();
@@ -179,12 +212,14 @@ __global__ void __launch_bounds__(kScoreThreads) epilogue_kernel(const CombinePa
     const int ncomb = c.B * c.n_q;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (bid < ncomb) {
-        combine_bh(c, bid, blockDim.x >> 5, warp, lane);
+        combine_bh(c, bid, blockDim.x >> 5, warp, lane, dyn_smem);
         return;
     }
-    __shared__ float s_lse[kMaxHeads];
+    float* s_lse = reinterpret_cast<float*>(dyn_smem);   // kMaxHeads floats, then the prefetch tile
+    float* xs = s_lse + kMaxHeads;
     const int b = (bid - ncomb) / tiles_per_req;
     const int tile = (bid - ncomb) % tiles_per_req;
+    const ScoreLane r = score_load(sp, b, static_cast<int64_t>(tile) * kScoreTile + threadIdx.x, xs);
     for (int h = warp; h < c.n_q; h += blockDim.x >> 5) {
         const int u = b * c.n_kv + h / c.g, hg = h % c.g;
         const int cnt = c.unit_count[u];
@@ -210,15 +245,23 @@ __global__ void __launch_bounds__(kScoreThreads) epilogue_kernel(const CombinePa
         if (lane == 0) s_lse[h] = lse == -INFINITY ? -INFINITY : lse * kLog2e;
     }
     __syncthreads();
-    scores_tile(sp, s_lse, b, tile * kScoreTile);
+    score_add(sp, s_lse, b, r, xs);
 }
 
-cudaError_t launch_epilogue(const CombineParams& c, const ScoreParams& sp, cudaStream_t stream) {
+cudaError_t launch_combine(const CombineParams& p, int carveout, cudaStream_t stream) {
+    const int w = combine_warps(p.slots_hint);
+    return launch_dependent(combine_kernel, dim3(static_cast<unsigned>(p.B * p.n_q)), dim3(w * 32),
+                            static_cast<size_t>(red_bytes(w)), carveout, stream, p);
+}
+
+cudaError_t launch_epilogue(const CombineParams& c, const ScoreParams& sp, int carveout, cudaStream_t stream) {
     const int64_t extent = sp.logits_stride < sp.scores_stride ? sp.logits_stride : sp.scores_stride;
     const int tiles = static_cast<int>((extent + kScoreTile - 1) / kScoreTile);
     const int64_t ctas = static_cast<int64_t>(c.B) * c.n_q + static_cast<int64_t>(c.B) * tiles;
-    return launch_dependent(epilogue_kernel, dim3(static_cast<unsigned>(ctas)), dim3(kScoreThreads), 0, stream, c, sp,
-                            tiles);
+    constexpr int kScoreSmem = kMaxHeads * 4 + kPrefetchBytes;
+    constexpr int kSmem = red_bytes(kScoreThreads / 32) > kScoreSmem ? red_bytes(kScoreThreads / 32) : kScoreSmem;
+    return launch_dependent(epilogue_kernel, dim3(static_cast<unsigned>(ctas)), dim3(kScoreThreads),
+                            static_cast<size_t>(kSmem), carveout, stream, c, sp, tiles);
 }
 
 }  // namespace kvd

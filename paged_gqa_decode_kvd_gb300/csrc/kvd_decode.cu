@@ -700,12 +700,33 @@ static cudaError_t ensure_smem_attr() {
     return e;
 }
 
-cudaError_t launch_decode(const DecodeParams& p, bool fp8, cudaStream_t stream) {
+// Shared-memory carveout (percent of the SM's shared memory) that holds a full complement
+// of decode CTAs, each with the per-block reservation; -1 if the device cannot be queried.
+int decode_carveout(bool fp8, int batch, int g) {
+    static int cached_dev = -1, per_sm = 0, reserved = 0;   // attributes of the last device asked
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (dev != cached_dev) {
+        int a = 0, r = 0;
+        if (cudaDeviceGetAttribute(&a, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess) return -1;
+        if (cudaDeviceGetAttribute(&r, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) return -1;
+        per_sm = a;
+        reserved = r;
+        cached_dev = dev;
+    }
+    if (per_sm <= 0) return -1;
+    const int64_t need = static_cast<int64_t>(decode_ctas_per_sm(fp8, batch, g)) *
+                         (static_cast<int64_t>(decode_smem_bytes(fp8, batch, g)) + reserved);
+    const int64_t pct = (100 * need + per_sm - 1) / per_sm;
+    return static_cast<int>(pct > 100 ? 100 : pct);
+}
+
+cudaError_t launch_decode(const DecodeParams& p, bool fp8, int carveout, cudaStream_t stream) {
     const size_t smem = decode_smem_bytes(fp8, p.B, p.g);
     cudaError_t e = fp8 ? ensure_smem_attr<true>() : ensure_smem_attr<false>();
     if (e != cudaSuccess) return e;
-    if (fp8) return launch_dependent(decode_kernel<true>, dim3(p.nsplit), dim3(kThreads), smem, stream, p);
-    return launch_dependent(decode_kernel<false>, dim3(p.nsplit), dim3(kThreads), smem, stream, p);
+    if (fp8) return launch_dependent(decode_kernel<true>, dim3(p.nsplit), dim3(kThreads), smem, carveout, stream, p);
+    return launch_dependent(decode_kernel<false>, dim3(p.nsplit), dim3(kThreads), smem, carveout, stream, p);
 }
 
 // ---------------------------------------------------------------- wait self-test

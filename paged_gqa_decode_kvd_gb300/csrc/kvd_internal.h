@@ -74,30 +74,39 @@ struct ScoreParams {
     float inv_LH;
 };
 
-// Launch `kernel` as a programmatic dependent of the preceding kernel in the stream.
+// Launch `kernel` as a programmatic dependent of the preceding kernel in the stream, with
+// a preferred shared-memory carveout (percent of the SM's shared memory) when carveout ≥ 0.
+// The kernels of one decode call share the decode kernel's carveout, so an SM moving from
+// one to the next keeps its L1/shared-memory split.
 template <typename... P>
-inline cudaError_t launch_dependent(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                                    const P&... params) {
+inline cudaError_t launch_dependent(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, int carveout,
+                                    cudaStream_t stream, const P&... params) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (carveout >= 0) {
+        attr[1].id = cudaLaunchAttributePreferredSharedMemoryCarveout;
+        attr[1].val.sharedMemCarveout = static_cast<unsigned>(carveout);
+        cfg.numAttrs = 2;
+    }
     return cudaLaunchKernelEx(&cfg, kernel, params...);
 }
 
 cudaError_t launch_append(const AppendParams& p, bool fp8, cudaStream_t stream);
 size_t decode_smem_bytes(bool fp8, int batch, int g);
 int decode_ctas_per_sm(bool fp8, int batch, int g);
-cudaError_t launch_decode(const DecodeParams& p, bool fp8, cudaStream_t stream);
-cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+int decode_carveout(bool fp8, int batch, int g);   // percent, for the decode call's launches
+cudaError_t launch_decode(const DecodeParams& p, bool fp8, int carveout, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, int carveout, cudaStream_t stream);
 cudaError_t launch_scores(const ScoreParams& p, cudaStream_t stream);
-cudaError_t launch_epilogue(const CombineParams& c, const ScoreParams& sp, cudaStream_t stream);
+cudaError_t launch_epilogue(const CombineParams& c, const ScoreParams& sp, int carveout, cudaStream_t stream);
 cudaError_t launch_wait_timeout(int32_t* err, int64_t timeout_ns, cudaStream_t stream);
 
 }  // namespace kvd
