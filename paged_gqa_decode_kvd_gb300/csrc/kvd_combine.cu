@@ -131,7 +131,7 @@ constexpr int kScoreThreads = 256;
 constexpr int kScoreTile = kScoreThreads;
 constexpr int kMaxHeads = 256;
 constexpr int kPrefetchHeads = 32;
-constexpr int kPrefetchBytes = kPrefetchHeads * kScoreThreads * 4;
+constexpr int kLseValues = 1024;   // partial LSEs a score CTA stages in shared memory
 
 __device__ __forceinline__ void cp_async4(float* dst, const float* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
@@ -203,7 +203,8 @@ cudaError_t launch_scores(const ScoreParams& p, cudaStream_t stream) {
 // CTA derives the final LSE of every head of its request from the split partials itself
 // (the merge CTAs of the same launch write lse_out concurrently), or reads lse_out where
 // the decode kernel already finished the unit.
-// Six CTAs an SM (at most 42 registers a thread): about as many as the prefetch tiles allow.
+// Six CTAs an SM (at most 42 registers a thread): as many as the score CTAs' shared memory
+// allows with up to 28 heads (about 37 KB each).
 __global__ void __launch_bounds__(kScoreThreads, 6) epilogue_kernel(const CombineParams c, const ScoreParams sp,
                                                                   int tiles_per_req) {
     pdl_wait();
@@ -215,34 +216,118 @@ __global__ void __launch_bounds__(kScoreThreads, 6) epilogue_kernel(const Combin
         combine_bh(c, bid, blockDim.x >> 5, warp, lane, dyn_smem);
         return;
     }
-    float* s_lse = reinterpret_cast<float*>(dyn_smem);   // kMaxHeads floats, then the prefetch tile
-    float* xs = s_lse + kMaxHeads;
+    // Score CTA.  Shared memory: the heads' final LSEs (exp2 domain), the request's unit
+    // tables and value offsets, each head's unit, the values the LSEs need, then the logit
+    // prefetch tile.
+    const int nw = blockDim.x >> 5;
+    const int nkv = c.n_kv, g = c.g;
+    float* s_lse = reinterpret_cast<float*>(dyn_smem);          // kMaxHeads
+    int* s_cnt = reinterpret_cast<int*>(s_lse + kMaxHeads);     // kMaxHeads
+    int* s_first = s_cnt + kMaxHeads;                           // kMaxHeads
+    int* s_off = s_first + kMaxHeads;                           // kMaxHeads + 1
+    float* vals = reinterpret_cast<float*>(s_off + kMaxHeads + 1);   // kLseValues
+    float* xs = vals + kLseValues;                              // min(n_q, kPrefetchHeads) rows
+    uint8_t* s_unit = reinterpret_cast<uint8_t*>(xs + (c.n_q < kPrefetchHeads ? c.n_q : kPrefetchHeads) * kScoreThreads);
+                                                                // kMaxHeads bytes: h / g (< 256)
     const int b = (bid - ncomb) / tiles_per_req;
     const int tile = (bid - ncomb) % tiles_per_req;
+    // unit tables first: the prefetch below would queue ahead of them
+    int cnt0 = 0, first0 = 0;
+    if (threadIdx.x < nkv) {
+        cnt0 = c.unit_count[b * nkv + threadIdx.x];
+        first0 = c.unit_first[b * nkv + threadIdx.x];
+    }
     const ScoreLane r = score_load(sp, b, static_cast<int64_t>(tile) * kScoreTile + threadIdx.x, xs);
-    for (int h = warp; h < c.n_q; h += blockDim.x >> 5) {
-        const int u = b * c.n_kv + h / c.g, hg = h % c.g;
-        const int cnt = c.unit_count[u];
-        float lse = -INFINITY;
-        if (cnt < 0) {
-            lse = c.lse_out[static_cast<int64_t>(b) * c.n_q + h];
-        } else if (cnt > 0) {
-            const int first = c.unit_first[u];
-            float M = -INFINITY;
-            for (int s = lane; s < cnt; s += 32) M = fmaxf(M, c.part_lse[static_cast<int64_t>(first + s) * c.g + hg]);
-            #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-            float L = 0.f;
-            if (M != -INFINITY)
-                for (int s = lane; s < cnt; s += 32) {
-                    const float ls = c.part_lse[static_cast<int64_t>(first + s) * c.g + hg];
-                    L += ls == -INFINITY ? 0.f : expf(ls - M);
-                }
-            #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
-            lse = L > 0.f ? M + logf(L) : -INFINITY;
+    if (threadIdx.x < nkv) {
+        s_cnt[threadIdx.x] = cnt0;
+        s_first[threadIdx.x] = first0;
+    }
+    for (int k = kScoreThreads + threadIdx.x; k < nkv; k += kScoreThreads) {
+        s_cnt[k] = c.unit_count[b * nkv + k];
+        s_first[k] = c.unit_first[b * nkv + k];
+    }
+    for (int h = threadIdx.x; h < c.n_q; h += kScoreThreads) s_unit[h] = static_cast<uint8_t>(h / g);
+    __syncthreads();
+    if (threadIdx.x == 0) {   // unit k contributes g·count partial LSEs, or g finished LSEs (count < 0)
+        int acc = 0;
+        for (int k = 0; k < nkv; ++k) {
+            s_off[k] = acc;
+            const int cnt = s_cnt[k];
+            acc += cnt > 0 ? g * cnt : (cnt < 0 ? g : 0);
         }
-        if (lane == 0) s_lse[h] = lse == -INFINITY ? -INFINITY : lse * kLog2e;
+        s_off[nkv] = acc;
+    }
+    __syncthreads();
+    const int total = s_off[nkv];
+    // Final LSE of each head in the exp2 domain: LSE2 = M2 + log2 Σ_s 2^(lse_s·log2e − M2),
+    // M2 = max_s lse_s·log2e (ex2/lg2.approx: about 1e-6, inside the score bound).
+    auto head_lse2 = [&](int cnt, auto value) {   // value(s): natural-log LSE of partial s
+        float M = -INFINITY;
+        for (int s2 = lane; s2 < cnt; s2 += 32) M = fmaxf(M, value(s2));
+        #pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+        if (M == -INFINITY) return -INFINITY;
+        const float M2 = M * kLog2e;
+        float L = 0.f;
+        for (int s2 = lane; s2 < cnt; s2 += 32) {
+            const float ls = value(s2);
+            L += ls == -INFINITY ? 0.f : ex2(fmaf(ls, kLog2e, -M2));
+        }
+        #pragma unroll
+        for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
+        return M2 + lg2(L);
+    };
+    if (total <= kLseValues) {
+        // Every value at once (independent loads, one memory round trip): a unit's partial
+        // LSEs are slot-major with its g heads contiguous, so value j of unit k sits at
+        // part_lse[first·g + j]; a unit the decode kernel finished reads lse_out.
+        float v[kLseValues / kScoreThreads];
+        #pragma unroll
+        for (int m = 0; m < kLseValues / kScoreThreads; ++m) {
+            const int i = threadIdx.x + m * kScoreThreads;
+            v[m] = 0.f;
+            if (i < total) {
+                int lo = 0, hi = nkv - 1;   // the last unit with s_off[k] <= i
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (s_off[mid] <= i) lo = mid; else hi = mid - 1;
+                }
+                const int j = i - s_off[lo];
+                v[m] = s_cnt[lo] < 0 ? c.lse_out[static_cast<int64_t>(b) * c.n_q + lo * g + j]
+                                     : c.part_lse[static_cast<int64_t>(s_first[lo]) * g + j];
+            }
+        }
+        #pragma unroll
+        for (int m = 0; m < kLseValues / kScoreThreads; ++m) {
+            const int i = threadIdx.x + m * kScoreThreads;
+            if (i < total) vals[i] = v[m];
+        }
+        __syncthreads();
+        for (int h = warp; h < c.n_q; h += nw) {
+            const int k = s_unit[h], cnt = s_cnt[k];
+            const float* hv = vals + s_off[k] + (h - k * g);   // value s of head h at hv[s·g]
+            float lse2 = -INFINITY;
+            if (cnt < 0) {
+                lse2 = hv[0] == -INFINITY ? -INFINITY : hv[0] * kLog2e;
+            } else if (cnt > 0) {
+                lse2 = head_lse2(cnt, [&](int s2) { return hv[s2 * g]; });
+            }
+            if (lane == 0) s_lse[h] = lse2;
+        }
+    } else {
+        // more values than the buffer holds: each warp walks its heads' partials in global memory
+        for (int h = warp; h < c.n_q; h += nw) {
+            const int k = s_unit[h], hg = h - k * g, cnt = s_cnt[k];
+            float lse2 = -INFINITY;
+            if (cnt < 0) {
+                const float l = c.lse_out[static_cast<int64_t>(b) * c.n_q + h];
+                lse2 = l == -INFINITY ? -INFINITY : l * kLog2e;
+            } else if (cnt > 0) {
+                const float* col = c.part_lse + static_cast<int64_t>(s_first[k]) * g + hg;
+                lse2 = head_lse2(cnt, [&](int s2) { return col[static_cast<int64_t>(s2) * g]; });
+            }
+            if (lane == 0) s_lse[h] = lse2;
+        }
     }
     __syncthreads();
     score_add(sp, s_lse, b, r, xs);
@@ -258,10 +343,11 @@ cudaError_t launch_epilogue(const CombineParams& c, const ScoreParams& sp, int c
     const int64_t extent = sp.logits_stride < sp.scores_stride ? sp.logits_stride : sp.scores_stride;
     const int tiles = static_cast<int>((extent + kScoreTile - 1) / kScoreTile);
     const int64_t ctas = static_cast<int64_t>(c.B) * c.n_q + static_cast<int64_t>(c.B) * tiles;
-    constexpr int kScoreSmem = kMaxHeads * 4 + kPrefetchBytes;
-    constexpr int kSmem = red_bytes(kScoreThreads / 32) > kScoreSmem ? red_bytes(kScoreThreads / 32) : kScoreSmem;
+    const int npre = sp.n_q < kPrefetchHeads ? sp.n_q : kPrefetchHeads;
+    const int score_smem = (4 * kMaxHeads + 1) * 4 + kLseValues * 4 + npre * kScoreThreads * 4 + kMaxHeads;
+    const int smem = red_bytes(kScoreThreads / 32) > score_smem ? red_bytes(kScoreThreads / 32) : score_smem;
     return launch_dependent(epilogue_kernel, dim3(static_cast<unsigned>(ctas)), dim3(kScoreThreads),
-                            static_cast<size_t>(kSmem), carveout, stream, c, sp, tiles);
+                            static_cast<size_t>(smem), carveout, stream, c, sp, tiles);
 }
 
 }  // namespace kvd

@@ -397,11 +397,20 @@ def test_fused_combine_matches_standalone_combine(cuda_device):
         np.testing.assert_allclose(flse.cpu().numpy(), slse.cpu().numpy(), rtol=1e-6, atol=1e-5)
 
 
-def test_fused_score_epilogue_matches_accum_scores(cuda_device):
+@pytest.mark.parametrize("shape", ["mixed", "many_partials"])
+def test_fused_score_epilogue_matches_accum_scores(cuda_device, shape):
     """The score update fused into kvd_decode_attn's merge launch equals kvd_accum_scores
-    applied to the same call's logits and LSE, and both match the oracle's α sum."""
-    w = _custom("fusedscore", 28, 4, [3000, 700, 16, 4100], evict_frac=0.05, protect_prompt=64, protect_recent=32,
-                scores=True)
+    applied to the same call's logits and LSE, and both match the oracle's α sum.  The
+    "many_partials" shape (64 heads, 200 splits of one context) needs more partial LSEs per
+    request than a score CTA stages in shared memory, so it takes the per-warp path."""
+    if shape == "mixed":
+        w = _custom("fusedscore", 28, 4, [3000, 700, 16, 4100], evict_frac=0.05, protect_prompt=64,
+                    protect_recent=32, scores=True)
+        split_list = (0, 3, 1)
+    else:
+        w = _custom("fusedscore_many", 64, 8, [8000], evict_frac=0.05, protect_prompt=64, protect_recent=32,
+                    scores=True)
+        split_list = (200, 0)
     dev = cuda_device
     bt, bt_d, seq, seq_d, ret_d = H.device_inputs(w, dev)
     pool = H.make_pool(w)
@@ -409,7 +418,7 @@ def test_fused_score_epilogue_matches_accum_scores(cuda_device):
     q = w.q(0, 0, dev)
     S = max(w.seq_lens())
     inv = 1.0 / (3 * w.n_q)
-    for splits in (0, 3, 1):
+    for splits in split_list:
         _, ws = H.workspace(pool, w.n_q, w.batch, S, splits, dev)
         out = torch.empty(w.batch, w.n_q, 128, dtype=torch.float32, device=dev)
         lse = torch.empty(w.batch, w.n_q, dtype=torch.float32, device=dev)
