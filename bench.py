@@ -54,16 +54,30 @@ def decode_intensity(g: int, w_kv: float) -> float:
     return 2 * g / w_kv
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on the
-    current decode kernel source (matched by its sha256); otherwise None."""
+DECODE_SOURCES = ("kvd_decode.cu", "kvd_common.cuh", "kvd_internal.h")
+
+
+def decode_source_digest():
+    """sha256 of the decode kernel's sources (kvd_decode.cu, kvd_common.cuh, kvd_internal.h,
+    concatenated in that order), or None if one is missing."""
     import hashlib
 
-    src = os.path.join(ROOT, "paged_gqa_decode_kvd_gb300", "csrc", "kvd_decode.cu")
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        src = os.path.join(ROOT, "paged_gqa_decode_kvd_gb300", "csrc", name)
+        if not os.path.exists(src):
+            return None
+        h.update(open(src, "rb").read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on the
+    current decode kernel sources (matched by decode_source_digest); otherwise None."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
-    if not (os.path.exists(src) and os.path.exists(path)):
+    digest = decode_source_digest()
+    if digest is None or not os.path.exists(path):
         return None
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
     for line in open(path):
         parts = line.split()
         if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload and parts[1] == digest:
