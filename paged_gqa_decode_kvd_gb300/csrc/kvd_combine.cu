@@ -132,9 +132,13 @@ constexpr int kScoreTile = kScoreThreads;
 constexpr int kMaxHeads = 256;
 constexpr int kPrefetchHeads = 32;
 constexpr int kLseValues = 1024;   // partial LSEs a score CTA stages in shared memory
+constexpr int kOffSlots = kMaxHeads + 4;   // value offsets per unit, padded to keep 16-byte alignment
 
 __device__ __forceinline__ void cp_async4(float* dst, const float* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(float* dst, const float* src) {   // both 16-byte aligned
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 
 struct ScoreLane {
@@ -143,24 +147,36 @@ struct ScoreLane {
     bool in_rows;   // t lies inside both row strides (every load is in bounds)
 };
 
-// xs: shared [kPrefetchHeads][kScoreThreads] floats; this thread uses column threadIdx.x only.
-__device__ __forceinline__ ScoreLane score_load(const ScoreParams& p, int b, int64_t t, float* xs) {
+// xs: shared [kPrefetchHeads][kScoreThreads] floats, column j = position t0 + j (t0 a multiple
+// of kScoreTile).  With a logits row stride that is a multiple of 4 floats and a 16-byte
+// aligned buffer, the rows are copied in 16-byte chunks (a chunk never crosses the end of a
+// row), a quarter of the copy instructions of 4-byte copies.  Every thread must then wait
+// for its copies before a CTA barrier that precedes score_add.
+__device__ __forceinline__ ScoreLane score_load(const ScoreParams& p, int b, int64_t t0, float* xs) {
     ScoreLane r;
-    r.t = t;
-    r.in_rows = t < p.logits_stride && t < p.scores_stride;
-    if (r.in_rows) {
-        const float* col = p.logits + static_cast<int64_t>(b) * p.n_q * p.logits_stride + t;
-        const int nh = p.n_q < kPrefetchHeads ? p.n_q : kPrefetchHeads;
-        for (int h = 0; h < nh; ++h) cp_async4(xs + h * kScoreThreads + threadIdx.x, col + static_cast<int64_t>(h) * p.logits_stride);
+    r.t = t0 + threadIdx.x;
+    r.in_rows = r.t < p.logits_stride && r.t < p.scores_stride;
+    const float* rows = p.logits + static_cast<int64_t>(b) * p.n_q * p.logits_stride;
+    const int nh = p.n_q < kPrefetchHeads ? p.n_q : kPrefetchHeads;
+    if ((p.logits_stride & 3) == 0 && (reinterpret_cast<uintptr_t>(p.logits) & 15u) == 0) {
+        constexpr int kChunks = kScoreThreads / 4;
+        for (int i = threadIdx.x; i < nh * kChunks; i += kScoreThreads) {
+            const int h = i / kChunks, c = i % kChunks;
+            const int64_t t = t0 + 4 * c;
+            if (t < p.logits_stride)
+                cp_async16(xs + h * kScoreThreads + 4 * c, rows + static_cast<int64_t>(h) * p.logits_stride + t);
+        }
+    } else if (r.in_rows) {
+        for (int h = 0; h < nh; ++h)
+            cp_async4(xs + h * kScoreThreads + threadIdx.x, rows + static_cast<int64_t>(h) * p.logits_stride + r.t);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
-    r.old = r.in_rows ? p.scores[static_cast<int64_t>(b) * p.scores_stride + t] : 0.f;
+    r.old = r.in_rows ? p.scores[static_cast<int64_t>(b) * p.scores_stride + r.t] : 0.f;
     return r;
 }
 
 __device__ __forceinline__ void score_add(const ScoreParams& p, const float* s_lse2, int b, const ScoreLane& r,
                                           const float* xs) {
-    asm volatile("cp.async.wait_all;" ::: "memory");   // this thread's own copies only
     if (!r.in_rows || r.t >= p.seq_lens[b]) return;
     float acc = 0.f;
     const int nh = p.n_q < kPrefetchHeads ? p.n_q : kPrefetchHeads;
@@ -180,14 +196,15 @@ __device__ __forceinline__ void score_add(const ScoreParams& p, const float* s_l
 
 __global__ void __launch_bounds__(kScoreThreads) scores_kernel(const ScoreParams p) {
     __shared__ float s_lse2[kMaxHeads];
-    __shared__ float xs[kPrefetchHeads * kScoreThreads];
+    __shared__ __align__(16) float xs[kPrefetchHeads * kScoreThreads];
     const int b = blockIdx.y;
-    const ScoreLane r = score_load(p, b, static_cast<int64_t>(blockIdx.x) * kScoreTile + threadIdx.x, xs);
+    const ScoreLane r = score_load(p, b, static_cast<int64_t>(blockIdx.x) * kScoreTile, xs);
     for (int h = threadIdx.x; h < p.n_q; h += blockDim.x) {
         const float m = p.lse[static_cast<int64_t>(b) * p.n_q + h];
         s_lse2[h] = m == -INFINITY ? -INFINITY : m * kLog2e;
     }
-    __syncthreads();
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();   // every thread's copies and LSEs visible to all
     score_add(p, s_lse2, b, r, xs);
 }
 
@@ -224,8 +241,8 @@ __global__ void __launch_bounds__(kScoreThreads, 6) epilogue_kernel(const Combin
     float* s_lse = reinterpret_cast<float*>(dyn_smem);          // kMaxHeads
     int* s_cnt = reinterpret_cast<int*>(s_lse + kMaxHeads);     // kMaxHeads
     int* s_first = s_cnt + kMaxHeads;                           // kMaxHeads
-    int* s_off = s_first + kMaxHeads;                           // kMaxHeads + 1
-    float* vals = reinterpret_cast<float*>(s_off + kMaxHeads + 1);   // kLseValues
+    int* s_off = s_first + kMaxHeads;                           // kOffSlots (≥ kMaxHeads + 1)
+    float* vals = reinterpret_cast<float*>(s_off + kOffSlots);  // kLseValues (16-byte aligned)
     float* xs = vals + kLseValues;                              // min(n_q, kPrefetchHeads) rows
     uint8_t* s_unit = reinterpret_cast<uint8_t*>(xs + (c.n_q < kPrefetchHeads ? c.n_q : kPrefetchHeads) * kScoreThreads);
                                                                 // kMaxHeads bytes: h / g (< 256)
@@ -237,7 +254,7 @@ __global__ void __launch_bounds__(kScoreThreads, 6) epilogue_kernel(const Combin
         cnt0 = c.unit_count[b * nkv + threadIdx.x];
         first0 = c.unit_first[b * nkv + threadIdx.x];
     }
-    const ScoreLane r = score_load(sp, b, static_cast<int64_t>(tile) * kScoreTile + threadIdx.x, xs);
+    const ScoreLane r = score_load(sp, b, static_cast<int64_t>(tile) * kScoreTile, xs);
     if (threadIdx.x < nkv) {
         s_cnt[threadIdx.x] = cnt0;
         s_first[threadIdx.x] = first0;
@@ -329,7 +346,8 @@ __global__ void __launch_bounds__(kScoreThreads, 6) epilogue_kernel(const Combin
             if (lane == 0) s_lse[h] = lse2;
         }
     }
-    __syncthreads();
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();   // every thread's copies and the LSEs visible to all
     score_add(sp, s_lse, b, r, xs);
 }
 
@@ -344,7 +362,7 @@ cudaError_t launch_epilogue(const CombineParams& c, const ScoreParams& sp, int c
     const int tiles = static_cast<int>((extent + kScoreTile - 1) / kScoreTile);
     const int64_t ctas = static_cast<int64_t>(c.B) * c.n_q + static_cast<int64_t>(c.B) * tiles;
     const int npre = sp.n_q < kPrefetchHeads ? sp.n_q : kPrefetchHeads;
-    const int score_smem = (4 * kMaxHeads + 1) * 4 + kLseValues * 4 + npre * kScoreThreads * 4 + kMaxHeads;
+    const int score_smem = (3 * kMaxHeads + kOffSlots) * 4 + kLseValues * 4 + npre * kScoreThreads * 4 + kMaxHeads;
     const int smem = red_bytes(kScoreThreads / 32) > score_smem ? red_bytes(kScoreThreads / 32) : score_smem;
     return launch_dependent(epilogue_kernel, dim3(static_cast<unsigned>(ctas)), dim3(kScoreThreads),
                             static_cast<size_t>(smem), carveout, stream, c, sp, tiles);

@@ -397,13 +397,16 @@ def test_fused_combine_matches_standalone_combine(cuda_device):
         np.testing.assert_allclose(flse.cpu().numpy(), slse.cpu().numpy(), rtol=1e-6, atol=1e-5)
 
 
-@pytest.mark.parametrize("shape", ["mixed", "many_partials"])
+@pytest.mark.parametrize("shape", ["mixed", "many_partials", "odd_stride"])
 def test_fused_score_epilogue_matches_accum_scores(cuda_device, shape):
     """The score update fused into kvd_decode_attn's merge launch equals kvd_accum_scores
     applied to the same call's logits and LSE, and both match the oracle's α sum.  The
     "many_partials" shape (64 heads, 200 splits of one context) needs more partial LSEs per
-    request than a score CTA stages in shared memory, so it takes the per-warp path."""
-    if shape == "mixed":
+    request than a score CTA stages in shared memory, so it takes the per-warp path; the
+    "odd_stride" shape gives the logits rows an odd stride, so the score CTAs prefetch them
+    with 4-byte copies instead of 16-byte ones."""
+    extra_cols = 1 if shape == "odd_stride" else 0
+    if shape in ("mixed", "odd_stride"):
         w = _custom("fusedscore", 28, 4, [3000, 700, 16, 4100], evict_frac=0.05, protect_prompt=64,
                     protect_recent=32, scores=True)
         split_list = (0, 3, 1)
@@ -422,7 +425,7 @@ def test_fused_score_epilogue_matches_accum_scores(cuda_device, shape):
         _, ws = H.workspace(pool, w.n_q, w.batch, S, splits, dev)
         out = torch.empty(w.batch, w.n_q, 128, dtype=torch.float32, device=dev)
         lse = torch.empty(w.batch, w.n_q, dtype=torch.float32, device=dev)
-        logits = torch.full((w.batch, w.n_q, S), float("nan"), dtype=torch.float32, device=dev)
+        logits = torch.full((w.batch, w.n_q, S + extra_cols), float("nan"), dtype=torch.float32, device=dev)
         base = torch.rand(w.batch, S + 3, dtype=torch.float32, device=dev)
         fused = base.clone()
         kvd.kvd_decode_attn(pool.handle, 0, q, bt_d, seq_d, S, ws, out, num_splits=splits, retain_mask=ret_d,
