@@ -193,7 +193,7 @@ class Step:
     per step index and the timed loop cycles through them.  With scores on, each layer
     also writes its logits and adds its share of the importance score."""
 
-    def __init__(self, w, dev, num_splits: int = 0, early: bool = True):
+    def __init__(self, w, dev, num_splits: int = 0, early: bool = True, fused_scores: bool = False):
         import numpy as np
         import torch
 
@@ -241,11 +241,22 @@ class Step:
                                                              num_splits)
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         self.scores = None
+        # Score update: by default each layer's share is added on a second stream (the score
+        # array is read only when tokens are re-tiered, so no later layer waits for it); the
+        # layer's logits and LSE go to a ring of three buffers, and a layer waits only for the
+        # score update that last used its slot.  fused_scores: one stream, score update inside
+        # the layer's merge launch.
+        self.overlap = bool(w.scores) and not fused_scores
         if w.scores:
-            self.lse = torch.empty(w.batch, w.n_q, dtype=torch.float32, device=dev)
-            self.logits = torch.empty(w.batch, w.n_q, self.max_len, dtype=torch.float32, device=dev)
+            nbuf = 3 if self.overlap else 1
+            self.lse = torch.empty(nbuf, w.batch, w.n_q, dtype=torch.float32, device=dev)
+            self.logits = torch.empty(nbuf, w.batch, w.n_q, self.max_len, dtype=torch.float32, device=dev)
             self.scores = torch.zeros(w.batch, self.max_len, dtype=torch.float32, device=dev)
-        self.launches_per_step = 2 * w.L   # decode kernel + merge (with the fused score update)
+            if self.overlap:
+                self.side = torch.cuda.Stream(device=dev)
+                self.score_done = [None] * nbuf
+        # decode kernel + merge per layer (+ the score kernel when it runs on its own stream)
+        self.launches_per_step = (3 if self.overlap else 2) * w.L
         torch.cuda.synchronize()
         err = kvd.kvd_get_device_error(self.pool.handle)
         if err:
@@ -260,13 +271,32 @@ class Step:
         return 0 if w.kv_dtype == "bf16" else int(2 * w.L * w.n_kv * 4 * sum(self.lens[t]))
 
     def layer_call(self, layer: int, t: int = 0, stream=None):
-        """One layer's decode: fused append of the new token, attention, split merge (one launch)."""
+        """One layer's decode: fused append of the new token, attention, split merge, and (with
+        scores) this layer's share of the importance score."""
+        import torch
+
+        inv = 1.0 / (self.w.L * self.w.n_q)
+        if self.overlap:
+            i = layer % len(self.score_done)
+            cur = stream if stream is not None else torch.cuda.current_stream(self.dev)
+            if self.score_done[i] is not None:
+                cur.wait_event(self.score_done[i])   # the slot's previous score update is done
+            self.kvd.kvd_decode_attn(self.pool.handle, layer, self.q[t][layer], self.bt, self.seq[t], self.max_len,
+                                     self.ws, self.out[layer], num_splits=self.splits, retain_mask=self.retain,
+                                     lse_out=self.lse[i], logits_out=self.logits[i], k_new=self.k_new[t][layer],
+                                     v_new=self.v_new[t][layer], early_start=self.early, stream=cur)
+            self.side.wait_stream(cur)
+            self.kvd.kvd_accum_scores(self.logits[i], self.lse[i], self.seq[t], inv, self.scores, stream=self.side)
+            ev = torch.cuda.Event()
+            ev.record(self.side)
+            self.score_done[i] = ev
+            return
         scores = self.scores is not None
         self.kvd.kvd_decode_attn(self.pool.handle, layer, self.q[t][layer], self.bt, self.seq[t], self.max_len,
                                  self.ws, self.out[layer], num_splits=self.splits, retain_mask=self.retain,
-                                 lse_out=self.lse if scores else None, logits_out=self.logits if scores else None,
+                                 lse_out=self.lse[0] if scores else None, logits_out=self.logits[0] if scores else None,
                                  k_new=self.k_new[t][layer], v_new=self.v_new[t][layer],
-                                 scores=self.scores if scores else None, inv_LH=1.0 / (self.w.L * self.w.n_q),
+                                 scores=self.scores if scores else None, inv_LH=inv,
                                  early_start=self.early, stream=stream)
 
     def decode_kernel_only(self, layer: int, t: int = 0, stream=None):
@@ -274,7 +304,7 @@ class Step:
         scores = self.scores is not None
         self.kvd.kvd_decode_attn(self.pool.handle, layer, self.q[t][layer], self.bt, self.seq[t], self.max_len,
                                  self.ws, None, num_splits=self.splits, retain_mask=self.retain,
-                                 logits_out=self.logits if scores else None,
+                                 logits_out=self.logits[0] if scores else None,
                                  k_new=self.k_new[t][layer], v_new=self.v_new[t][layer], early_start=self.early,
                                  stream=stream)
 
@@ -289,8 +319,15 @@ class Step:
         return g
 
     def run(self, t: int = 0, stream=None):
+        import torch
+
+        if self.overlap:
+            self.score_done = [None] * len(self.score_done)   # a step depends on nothing of the last
         for layer in range(self.L):
             self.layer_call(layer, t, stream)
+        if self.overlap:   # the step ends when its last score update has
+            cur = stream if stream is not None else torch.cuda.current_stream(self.dev)
+            cur.wait_stream(self.side)
 
     def capture(self):
         import torch
@@ -317,7 +354,7 @@ def gpu_arm(args, w, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     peaks = measured_peaks()
-    st = Step(w, dev, args.num_splits, early=not args.no_early_start)
+    st = Step(w, dev, args.num_splits, early=not args.no_early_start, fused_scores=args.fused_scores)
     graphs = st.capture()
     stream = torch.cuda.current_stream(dev)
     # closed-form KV bytes of the timed steps (step t of the workload = graph t % steps)
@@ -401,6 +438,8 @@ def gpu_arm(args, w, rank, world, local):
                    "kv_bytes_per_step": kv_bytes, "fp8_scale_bytes_per_step": st.scale_bytes(0),
                    "num_splits": st.splits, "seed": w.seed,
                    "decode_steps_cycled": st.nsteps, "scores": bool(w.scores),
+                   "score_update": ("second stream (off the layer chain)" if st.overlap else
+                                    "fused into the merge launch" if w.scores else None),
                    "l2": "inputs larger than L2 (KV pool streamed every step)", "parallelism": f"replicas x{world}"},
         "steps_per_s": round(1e3 / ms_per_step, 2),
         "hbm_frac_of_measured": round(value / world / peaks["hbm_gbs"], 4),
@@ -482,6 +521,8 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling captures)")
     ap.add_argument("--context", type=int, default=0, help="override every request's context (size sweeps)")
     ap.add_argument("--no-early-start", action="store_true", help="launch the decode kernel without KVD_EARLY_START")
+    ap.add_argument("--fused-scores", action="store_true",
+                    help="score update inside each layer's merge launch (one stream) instead of on a second stream")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
