@@ -159,6 +159,12 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
 }
+
+// The two f16 halves of a packed pair as floats (lo, hi).
+__device__ __forceinline__ float2 unpack_f16(uint32_t v) {
+    const __half2 h = *reinterpret_cast<const __half2*>(&v);
+    return __half22float2(h);
+}
 // Two E4M3 codes (low byte = lower element) -> f16x2 in one instruction; exact, since
 // every E4M3 value is an f16 value.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {

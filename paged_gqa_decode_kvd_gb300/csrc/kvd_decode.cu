@@ -41,7 +41,7 @@ constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s
 // slots suffice for the register tree merge of the four consumer warps.
 __host__ __device__ inline int merge_floats(int g) { return g * kMergeStride + 2 * kMaxG; }
 
-template <bool FP8>
+template <bool FP8, int STAGES>
 struct Cfg {
     static constexpr int kTile = FP8 ? kTileFp8 : kTileBf16;
     static constexpr int kRecord = FP8 ? kRecordFp8 : kRecordBf16;   // one bulk copy per (block, head)
@@ -50,7 +50,7 @@ struct Cfg {
     // multiple of kNcw every reuse of a stage inside a segment belongs to the same warp,
     // and across segments the merge barrier orders it, so a consumer never waits on a
     // phase whose predecessor is still incomplete (mbarrier parity cannot alias).
-    static constexpr int kStages = 8;
+    static constexpr int kStages = STAGES;
     static_assert(kStages % kNcw == 0, "stages must be a multiple of the consumer warps");
 };
 
@@ -58,13 +58,13 @@ struct Smem {
     int ring_off, full_off, empty_off, meta_off, merge_off, pref_off, lens_off, abort_off, flag_off, total;
 };
 
-template <bool FP8>
+template <bool FP8, int S>
 __host__ __device__ inline Smem smem_layout(int batch, int g) {
-    constexpr int kStages = Cfg<FP8>::kStages;
+    constexpr int kStages = Cfg<FP8, S>::kStages;
     Smem s;
     int o = 0;
     s.ring_off = o;
-    o += kStages * Cfg<FP8>::kStage;
+    o += kStages * Cfg<FP8, S>::kStage;
     s.full_off = o;
     o += kStages * 8;
     s.empty_off = o;
@@ -125,11 +125,12 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, int64_t idx, fl
     }
 }
 
-template <bool FP8>
+template <bool FP8, int S>
 __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int kStages = Cfg<FP8>::kStages;
-    const Smem L = smem_layout<FP8>(p.B, p.g);
+    using C = Cfg<FP8, S>;
+    constexpr int kStages = C::kStages;
+    const Smem L = smem_layout<FP8, S>(p.B, p.g);
     uint8_t* ring = smem + L.ring_off;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full_off);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty_off);
@@ -242,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
                 if (p.early) pdl_wait();   // k_new / v_new come from the previous kernel
                 if (ph >= 0 && ph < p.num_blocks) {
                     const int64_t row = (static_cast<int64_t>(sg.b) * p.n_kv + sg.kvh) * kDh;
-                    uint8_t* rec = const_cast<uint8_t*>(p.kv) + (static_cast<int64_t>(ph) * p.n_kv + sg.kvh) * Cfg<FP8>::kRecord;
+                    uint8_t* rec = const_cast<uint8_t*>(p.kv) + (static_cast<int64_t>(ph) * p.n_kv + sg.kvh) * C::kRecord;
                     write_token<FP8>(rec, pos % kBs, p.k_new + row, p.v_new + row, lane);
                     fence_proxy_async_global();
                 }
@@ -276,10 +277,10 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
                             meta[s] = static_cast<int>(m);
                             if (m >> 16) {
                                 const uint8_t* rec =
-                                    p.kv + (static_cast<int64_t>(ph) * p.n_kv + sg.kvh) * Cfg<FP8>::kRecord;
-                                uint8_t* dst = ring + s * Cfg<FP8>::kStage;
-                                mbar_arrive_expect_tx(&full[s], Cfg<FP8>::kRecord);
-                                bulk_g2s(dst, rec, Cfg<FP8>::kRecord, &full[s], policy);
+                                    p.kv + (static_cast<int64_t>(ph) * p.n_kv + sg.kvh) * C::kRecord;
+                                uint8_t* dst = ring + s * C::kStage;
+                                mbar_arrive_expect_tx(&full[s], C::kRecord);
+                                bulk_g2s(dst, rec, C::kRecord, &full[s], policy);
                             } else {
                                 mbar_arrive(&full[s]);
                             }
@@ -376,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
                 if (lane == 0) mbar_arrive(&empty[s]);
                 continue;
             }
-            const uint8_t* st = ring + s * Cfg<FP8>::kStage;
+            const uint8_t* st = ring + s * C::kStage;
             const int j = sg.j0 + kk;
 
             // ---- S^T = K · Q^T  (16 tokens × 8 heads) ----
@@ -460,14 +461,23 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
             }
 
             // ---- P^T fragment: rows = tokens, cols = heads -> transpose ----
-            uint32_t pb0, pb1;
+            // FP8: the V scale is folded into p and p·s goes to the MMA as an f16 pair plus the
+            // f16 of its rounding remainder (two MMAs), about 2^-22 relative per term: with a
+            // single f16 (2^-11) a channel whose values are 20x the rest can lose more than the
+            // output tolerance to cancellation.
+            uint32_t pb0, pb1, pl0 = 0, pl1 = 0;
             if constexpr (!FP8) {
                 pb0 = movmatrix_t(pack_bf16(p0, p1));
                 pb1 = movmatrix_t(pack_bf16(p2, p3));
             } else {
                 const float w0 = v0 ? fv0 : 0.f, w1 = v1 ? fv1 : 0.f;
-                pb0 = movmatrix_t(pack_f16(p0 * w0, p1 * w0));
-                pb1 = movmatrix_t(pack_f16(p2 * w1, p3 * w1));
+                const float a0 = p0 * w0, a1 = p1 * w0, a2 = p2 * w1, a3 = p3 * w1;
+                const uint32_t h01 = pack_f16(a0, a1), h23 = pack_f16(a2, a3);
+                const float2 r01 = unpack_f16(h01), r23 = unpack_f16(h23);
+                pb0 = movmatrix_t(h01);
+                pb1 = movmatrix_t(h23);
+                pl0 = movmatrix_t(pack_f16(a0 - r01.x, a1 - r01.y));
+                pl1 = movmatrix_t(pack_f16(a2 - r23.x, a3 - r23.y));
             }
 
             // ---- O^T += V^T · P^T ----
@@ -477,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
             const bool partial = (m & 0xFFFFu) != 0xFFFFu;
             const int ta = 2 * tq;
             if constexpr (!FP8) {
-                const uint4* vt = reinterpret_cast<const uint4*>(st + Cfg<FP8>::kTile);
+                const uint4* vt = reinterpret_cast<const uint4*>(st + C::kTile);
                 uint4 vv[8];
                 #pragma unroll
                 for (int i = 0; i < 8; ++i) vv[i] = vt[i * 32 + lane];
@@ -501,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
                     mma_bf16(o[i], fa, pb0, pb1);
                 }
             } else {
-                const uint4* vt = reinterpret_cast<const uint4*>(st + Cfg<FP8>::kTile);
+                const uint4* vt = reinterpret_cast<const uint4*>(st + C::kTile);
                 uint32_t zlo = 0xFFFFFFFFu, zhi = 0xFFFFFFFFu;
                 if (partial) {   // bytes: tokens (2tq, 2tq+1) in .x/.z, (2tq+8, 2tq+9) in .y/.w; code 0 = +0
                     zlo = (((m >> ta) & 1u) ? 0x00FFu : 0u) | (((m >> (ta + 1)) & 1u) ? 0xFF00u : 0u);
@@ -538,6 +548,8 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
                         e4m3x4_to_f16x2x2(vv[i].w, fb[2], fb[3]);
                         mma_f16(o[2 * u4], fa, pb0, pb1);
                         mma_f16(o[2 * u4 + 1], fb, pb0, pb1);
+                        mma_f16(o[2 * u4], fa, pl0, pl1);
+                        mma_f16(o[2 * u4 + 1], fb, pl0, pl1);
                     }
                 }
             }
@@ -664,69 +676,96 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
     }
 }
 
-size_t decode_smem_bytes(bool fp8, int batch, int g) {
-    return fp8 ? smem_layout<true>(batch, g).total : smem_layout<false>(batch, g).total;
+// Shared memory per SM and per-block reservation of the current device (cached per device).
+static bool smem_attrs(int* per_sm, int* reserved) {
+    static int cached_dev = -1, c_per_sm = 0, c_reserved = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (dev != cached_dev) {
+        int a = 0, r = 0;
+        if (cudaDeviceGetAttribute(&a, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess) return false;
+        if (cudaDeviceGetAttribute(&r, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) return false;
+        c_per_sm = a;
+        c_reserved = r;
+        cached_dev = dev;
+    }
+    *per_sm = c_per_sm;
+    *reserved = c_reserved;
+    return c_per_sm > 0;
 }
 
-template <bool FP8>
-static cudaError_t ensure_smem_attr();
-
-template <bool FP8>
-static int ctas_per_sm_impl(int batch, int g) {
-    const int smem = smem_layout<FP8>(batch, g).total;
-    if (ensure_smem_attr<FP8>() != cudaSuccess) return 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<FP8>, kThreads, smem) != cudaSuccess)
-        return 1;
-    return n > 0 ? n : 1;
-}
-
-int decode_ctas_per_sm(bool fp8, int batch, int g) {
-    return fp8 ? ctas_per_sm_impl<true>(batch, g) : ctas_per_sm_impl<false>(batch, g);
+// Ring depth of a call.  BF16: 8 stages (8 KB records, 3 CTAs/SM).  FP8: 16 stages when three
+// such CTAs fit an SM (the per-request arrays are small enough), else 8 stages (4 CTAs/SM).
+// With 16 the CTA keeps twice the bytes in flight; measured on GB300 it is 1% faster for one
+// or eight long requests and equal for 32 requests of 8,192 tokens.
+static int decode_stages(bool fp8, int batch, int g) {
+    if (!fp8) return 8;
+    int per_sm = 0, reserved = 0;
+    if (!smem_attrs(&per_sm, &reserved)) return 8;
+    const int64_t need = 3 * (static_cast<int64_t>(smem_layout<true, 16>(batch, g).total) + reserved);
+    return need <= per_sm ? 16 : 8;
 }
 
 // Raise the kernel's dynamic shared-memory limit once per device to the largest
 // layout any batch size can need (batch ≤ kMaxBatch).
-template <bool FP8>
+template <bool FP8, int S>
 static cudaError_t ensure_smem_attr() {
     static int done_for_device = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (done_for_device == dev) return cudaSuccess;
-    e = cudaFuncSetAttribute(decode_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_layout<FP8>(kMaxBatch, kMaxG).total);
+    e = cudaFuncSetAttribute(decode_kernel<FP8, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_layout<FP8, S>(kMaxBatch, kMaxG).total);
     if (e == cudaSuccess) done_for_device = dev;
     return e;
+}
+
+template <bool FP8, int S>
+static int ctas_per_sm_impl(int batch, int g) {
+    const int smem = smem_layout<FP8, S>(batch, g).total;
+    if (ensure_smem_attr<FP8, S>() != cudaSuccess) return 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<FP8, S>, kThreads, smem) != cudaSuccess)
+        return 1;
+    return n > 0 ? n : 1;
+}
+
+size_t decode_smem_bytes(bool fp8, int batch, int g) {
+    if (!fp8) return smem_layout<false, 8>(batch, g).total;
+    return decode_stages(true, batch, g) == 16 ? smem_layout<true, 16>(batch, g).total
+                                               : smem_layout<true, 8>(batch, g).total;
+}
+
+int decode_ctas_per_sm(bool fp8, int batch, int g) {
+    if (!fp8) return ctas_per_sm_impl<false, 8>(batch, g);
+    return decode_stages(true, batch, g) == 16 ? ctas_per_sm_impl<true, 16>(batch, g)
+                                               : ctas_per_sm_impl<true, 8>(batch, g);
 }
 
 // Shared-memory carveout (percent of the SM's shared memory) that holds a full complement
 // of decode CTAs, each with the per-block reservation; -1 if the device cannot be queried.
 int decode_carveout(bool fp8, int batch, int g) {
-    static int cached_dev = -1, per_sm = 0, reserved = 0;   // attributes of the last device asked
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
-    if (dev != cached_dev) {
-        int a = 0, r = 0;
-        if (cudaDeviceGetAttribute(&a, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess) return -1;
-        if (cudaDeviceGetAttribute(&r, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) return -1;
-        per_sm = a;
-        reserved = r;
-        cached_dev = dev;
-    }
-    if (per_sm <= 0) return -1;
+    int per_sm = 0, reserved = 0;
+    if (!smem_attrs(&per_sm, &reserved)) return -1;
     const int64_t need = static_cast<int64_t>(decode_ctas_per_sm(fp8, batch, g)) *
                          (static_cast<int64_t>(decode_smem_bytes(fp8, batch, g)) + reserved);
     const int64_t pct = (100 * need + per_sm - 1) / per_sm;
     return static_cast<int>(pct > 100 ? 100 : pct);
 }
 
-cudaError_t launch_decode(const DecodeParams& p, bool fp8, int carveout, cudaStream_t stream) {
-    const size_t smem = decode_smem_bytes(fp8, p.B, p.g);
-    cudaError_t e = fp8 ? ensure_smem_attr<true>() : ensure_smem_attr<false>();
+template <bool FP8, int S>
+static cudaError_t launch_variant(const DecodeParams& p, int carveout, cudaStream_t stream) {
+    const cudaError_t e = ensure_smem_attr<FP8, S>();
     if (e != cudaSuccess) return e;
-    if (fp8) return launch_dependent(decode_kernel<true>, dim3(p.nsplit), dim3(kThreads), smem, carveout, stream, p);
-    return launch_dependent(decode_kernel<false>, dim3(p.nsplit), dim3(kThreads), smem, carveout, stream, p);
+    const size_t smem = smem_layout<FP8, S>(p.B, p.g).total;
+    return launch_dependent(decode_kernel<FP8, S>, dim3(p.nsplit), dim3(kThreads), smem, carveout, stream, p);
+}
+
+cudaError_t launch_decode(const DecodeParams& p, bool fp8, int carveout, cudaStream_t stream) {
+    if (!fp8) return launch_variant<false, 8>(p, carveout, stream);
+    return decode_stages(true, p.B, p.g) == 16 ? launch_variant<true, 16>(p, carveout, stream)
+                                               : launch_variant<true, 8>(p, carveout, stream);
 }
 
 // ---------------------------------------------------------------- wait self-test

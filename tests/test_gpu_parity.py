@@ -188,6 +188,18 @@ def test_fp8_decode_parity(cuda_device):
     np.testing.assert_allclose(res["lse"], ref["lse"], rtol=1e-5, atol=1e-4)
 
 
+def test_fp8_many_requests_parity(cuda_device):
+    """48 FP8 requests at g = 8: the per-request arrays leave no room for three 16-stage CTAs
+    an SM, so this call runs the FP8 kernel with the 8-stage ring (small batches run 16)."""
+    lens = [int(x) for x in np.random.default_rng(3).integers(40, 700, size=48)]
+    w = _custom("fp8many", 64, 8, lens, kv_dtype="fp8_e4m3", outlier_p=0.01, outlier_factor=20.0, seed=4)
+    res = _run(w, cuda_device, out_f32=True)
+    assert res["err"] == 0
+    ref = H.oracle_layer(w, 0, res["bt"], w.seq_lens())
+    H.assert_out_close(res["out"], ref["out"])
+    np.testing.assert_allclose(res["lse"], ref["lse"], rtol=1e-5, atol=1e-4)
+
+
 def test_evicted_slots_logits_and_scores(cuda_device):
     """Retain mask, per-position logits and the score epilogue against the oracle."""
     w = _custom("evict", 28, 4, [1500, 900, 2100], evict_frac=0.1, protect_prompt=64, protect_recent=32,
