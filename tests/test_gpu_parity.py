@@ -170,6 +170,21 @@ def test_ragged_lengths_every_group_size(cuda_device, g):
         np.testing.assert_allclose(res["lse"], ref["lse"], rtol=1e-5, atol=1e-4)
 
 
+@pytest.mark.parametrize("g", [1, 2, 4, 7, 8])
+def test_fp8_ragged_lengths_every_group_size(cuda_device, g):
+    """The FP8 pool (E4M3 codes, per-(token, head) scales, 20x outlier channels) for every group
+    size, lengths around the block edges, one CTA, the planned split and 13 splits."""
+    lens = [1, 15, 16, 17, 31, 33, 250, 1000, 2047, 5]
+    w = _custom(f"fp8_ragged_g{g}", 2 * g, 2, lens, kv_dtype="fp8_e4m3", outlier_p=0.01, outlier_factor=20.0,
+                seed=10 + g)
+    for splits in (0, 1, 13):
+        res = _run(w, cuda_device, num_splits=splits, out_f32=True)
+        assert res["err"] == 0
+        ref = H.oracle_layer(w, 0, res["bt"], lens)
+        H.assert_out_close(res["out"], ref["out"], what=f"fp8 g={g} splits={splits}")
+        np.testing.assert_allclose(res["lse"], ref["lse"], rtol=1e-5, atol=1e-4)
+
+
 def test_split_and_non_split_agree(cuda_device):
     w = _custom("splits", 32, 8, [4000, 2500, 16, 1234])
     one = _run(w, cuda_device, num_splits=1, out_f32=True)
