@@ -160,6 +160,12 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// The two bf16 halves of a packed pair as floats (lo, hi).
+__device__ __forceinline__ float2 unpack_bf16(uint32_t v) {
+    const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&v);
+    return __bfloat1622float2(h);
+}
+
 // The two f16 halves of a packed pair as floats (lo, hi).
 __device__ __forceinline__ float2 unpack_f16(uint32_t v) {
     const __half2 h = *reinterpret_cast<const __half2*>(&v);

@@ -461,14 +461,19 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
             }
 
             // ---- P^T fragment: rows = tokens, cols = heads -> transpose ----
-            // FP8: the V scale is folded into p and p·s goes to the MMA as an f16 pair plus the
-            // f16 of its rounding remainder (two MMAs), about 2^-22 relative per term: with a
-            // single f16 (2^-11) a channel whose values are 20x the rest can lose more than the
-            // output tolerance to cancellation.
-            uint32_t pb0, pb1, pl0 = 0, pl1 = 0;
+            // p goes to the MMA as a 16-bit value plus the 16-bit value of its rounding remainder
+            // (two MMAs): about 2^-17 (bf16) or 2^-22 (f16) relative per term.  A single 16-bit
+            // p (2^-9 bf16, 2^-11 f16) lets outputs that cancel (few dominant positions, or FP8
+            // channels 20x the others) lose more than the output tolerance.  FP8 folds the V
+            // scale into p first.
+            uint32_t pb0, pb1, pl0, pl1;
             if constexpr (!FP8) {
-                pb0 = movmatrix_t(pack_bf16(p0, p1));
-                pb1 = movmatrix_t(pack_bf16(p2, p3));
+                const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
+                const float2 r01 = unpack_bf16(h01), r23 = unpack_bf16(h23);
+                pb0 = movmatrix_t(h01);
+                pb1 = movmatrix_t(h23);
+                pl0 = movmatrix_t(pack_bf16(p0 - r01.x, p1 - r01.y));
+                pl1 = movmatrix_t(pack_bf16(p2 - r23.x, p3 - r23.y));
             } else {
                 const float w0 = v0 ? fv0 : 0.f, w1 = v1 ? fv1 : 0.f;
                 const float a0 = p0 * w0, a1 = p1 * w0, a2 = p2 * w1, a3 = p3 * w1;
@@ -509,6 +514,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
                 for (int i = 0; i < 8; ++i) {
                     const uint32_t fa[4] = {vv[i].x, vv[i].y, vv[i].z, vv[i].w};
                     mma_bf16(o[i], fa, pb0, pb1);
+                    mma_bf16(o[i], fa, pl0, pl1);
                 }
             } else {
                 const uint4* vt = reinterpret_cast<const uint4*>(st + C::kTile);

@@ -185,6 +185,20 @@ def test_fp8_ragged_lengths_every_group_size(cuda_device, g):
         np.testing.assert_allclose(res["lse"], ref["lse"], rtol=1e-5, atol=1e-4)
 
 
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_maximum_batch(cuda_device, kv_dtype):
+    """The largest supported batch (2,048 requests, lengths 1..48 around the block edges): the
+    per-request length and prefix arrays fill 16 KB of each CTA's shared memory, and units
+    of one to three blocks mostly lie inside one CTA (finished there, no merge)."""
+    lens = [int(x) for x in np.random.default_rng(7).integers(1, 49, size=2048)]
+    w = _custom(f"maxbatch_{kv_dtype}", 8, 2, lens, kv_dtype=kv_dtype, seed=21)
+    res = _run(w, cuda_device, out_f32=True)
+    assert res["err"] == 0
+    ref = H.oracle_layer(w, 0, res["bt"], lens)
+    H.assert_out_close(res["out"], ref["out"], what=f"{kv_dtype} batch 2048")
+    np.testing.assert_allclose(res["lse"], ref["lse"], rtol=1e-5, atol=1e-4)
+
+
 def test_split_and_non_split_agree(cuda_device):
     w = _custom("splits", 32, 8, [4000, 2500, 16, 1234])
     one = _run(w, cuda_device, num_splits=1, out_f32=True)
