@@ -125,13 +125,48 @@ KVD_API kvd_status kvd_pool_create(const kvd_pool_desc* desc, void* mem, size_t 
 /* Free the handle and its error word (not the caller's pool memory).  NULL is a no-op. */
 KVD_API void kvd_pool_destroy(kvd_pool* pool);
 
+/* Host tier (T1) of a pool.  Page "기술 요약: 모든 사고가 HBM 을 필요로 하는 것은 아님",
+ * section "1. 4 단계 분류": mid-importance tokens (tier T1) live at full precision in host
+ * memory and are brought to the GPU before every attention step; section "3. 제로-근사오차
+ * 오프로딩", Prop. 1: the attention output does not depend on how tokens are split between
+ * HBM (T0) and host memory (T1).
+ * A pool with a host tier has host_blocks more physical blocks, ids num_blocks ..
+ * num_blocks + host_blocks - 1, whose records (same record layout; per layer ℓ the record of
+ * host block i, head h sits at ((ℓ·host_blocks + i)·n_kv + h)·record_bytes) live in pinned
+ * host memory.  kvd_tier_prefetch copies one layer's host records into one of two HBM
+ * staging slots (slot layer % 2); kvd_decode_attn reads a host-tier block from that staged
+ * copy, so the staged layer must be the one attended.  A retain_mask then has
+ * num_blocks + host_blocks entries.  Block tables may mix both kinds of ids freely. */
+
+/* host_bytes = L·host_blocks·n_kv·record_bytes (pinned host memory); staging_bytes =
+ * 2·host_blocks·n_kv·record_bytes (device).  host_blocks ≥ 0.  Host only. */
+KVD_API kvd_status kvd_tier_bytes(const kvd_pool_desc* desc, int64_t host_blocks, size_t* host_bytes,
+                                  size_t* staging_bytes);
+
+/* Give the pool a host tier of host_blocks blocks (0 removes it).  host_mem: host memory the
+ * device can address — page-locked (cudaHostAlloc or registered), or on systems where the
+ * device reads pageable memory any host memory — 16-byte aligned, ≥ host_bytes; its device
+ * address is looked up here (KVD_ERR_INVALID if there is none).  staging_mem: device,
+ * 16-byte aligned, ≥ staging_bytes.  Both stay caller-owned; the host records are written by
+ * kvd_append_kv (slots in host blocks) and by the fused append of kvd_decode_attn. */
+KVD_API kvd_status kvd_pool_attach_host_tier(kvd_pool* pool, void* host_mem, size_t host_len, void* staging_mem,
+                                             size_t staging_len, int64_t host_blocks);
+
+/* Copy layer's host-tier records into staging slot layer % 2 (host_blocks·n_kv·record_bytes
+ * bytes over the host link) on `stream`.  It must complete before a kvd_decode_attn of that
+ * layer reads a host-tier block (same stream, or an event), and a slot is refilled two layers
+ * later, so the prefetch of layer ℓ+2 must wait for the attention of layer ℓ.  A no-op
+ * without a host tier. */
+KVD_API kvd_status kvd_tier_prefetch(kvd_pool* pool, int layer, void* stream);
+
 /* Decode-step append ("reshape and cache").  Token n's keys k_new[n][h][:] and values
  * v_new[n][h][:] (bf16, [n_tokens][n_kv][d_h], device) are written for every KV head h of
  * `layer` at slot s = slot_mapping[n] (int64, device) = physical_block·16 + offset;
  * s < 0 skips the token.  FP8 pools store per (token, head) and separately for K and V:
  * scale = fp32(absmax/448) (1 when the row is zero), code = e4m3 round-to-nearest-even,
- * saturating, of the fp32 quotient x/scale.  n_tokens = 0 is a no-op.  A slot beyond the
- * pool sets KVD_ERR_OOB on the device and that token is skipped. */
+ * saturating, of the fp32 quotient x/scale.  n_tokens = 0 is a no-op.  A slot in a host-tier
+ * block writes that block's host record.  A slot beyond the pool (and its host tier) sets
+ * KVD_ERR_OOB on the device and that token is skipped. */
 KVD_API kvd_status kvd_append_kv(kvd_pool* pool, int layer, const void* k_new, const void* v_new,
                          const int64_t* slot_mapping, int n_tokens, void* stream);
 
@@ -148,6 +183,7 @@ KVD_API kvd_status kvd_decode_workspace_bytes(const kvd_pool* pool, int n_q, int
  *               block_table[b][(len-1)/16]·16 + (len-1)%16 — is written into the pool (FP8
  *               quantised as kvd_append_kv does) by the CTA that attends that block, before
  *               it reads it.  That block must not be shared with another request of the call.
+ *               A host-tier block gets the token in its host record and in its staged copy.
  *  block_table  int32 [batch][max_blocks_per_seq], device; entry j of request b is the
  *               physical block of its logical block j (entries past the context unread)
  *  seq_lens     int32 [batch], device; positions 0 .. seq_lens[b]-1 are attended (the
@@ -157,8 +193,8 @@ KVD_API kvd_status kvd_decode_workspace_bytes(const kvd_pool* pool, int n_q, int
  *               (request, KV head, block) work is cut into num_splits equal contiguous
  *               ranges, one CTA each; partial results are merged by log-sum-exp (a unit
  *               that lies inside one CTA is finished by that CTA directly)
- *  retain_mask  uint16 [num_blocks] or NULL; bit o of retain_mask[p] clear = slot o of
- *               physical block p is evicted (logit −inf, weight 0) in every layer
+ *  retain_mask  uint16 [num_blocks + host_blocks] or NULL; bit o of retain_mask[p] clear =
+ *               slot o of physical block p is evicted (logit −inf, weight 0) in every layer
  *  softmax_scale  multiplies q·k (1/√d_h for the plain definition)
  *  workspace    device scratch of workspace_bytes ≥ kvd_decode_workspace_bytes, no
  *               initialisation needed; layout: part_o f32 [S + U][g][d_h], part_lse f32

@@ -25,6 +25,9 @@ from ._lib import (  # noqa: F401
     KvdError,
     kvd_accum_scores,
     kvd_append_kv,
+    kvd_pool_attach_host_tier,
+    kvd_tier_bytes,
+    kvd_tier_prefetch,
     kvd_combine_splits,
     kvd_decode_attn,
     kvd_decode_attn_noalloc,
@@ -55,6 +58,18 @@ class KVPool:
     def record_bytes(self) -> int:
         """Bytes of one (layer, block, KV head) record: K tile, V tile and (FP8) 32 fp32 scales."""
         return 8192 if self.kv_dtype == KVD_BF16 else 4096 + 128
+
+    def attach_host_tier(self, host_blocks: int):
+        """Give the pool host_blocks host-tier blocks (ids num_blocks ..): their records in
+        pinned host memory, plus two HBM staging slots for kvd_tier_prefetch."""
+        import torch
+
+        host_bytes, staging_bytes = kvd_tier_bytes(self.num_layers, self.n_kv, self.num_blocks, self.kv_dtype,
+                                                   host_blocks)
+        self.host_mem = torch.empty(host_bytes, dtype=torch.uint8, pin_memory=True)
+        self.staging = torch.empty(staging_bytes, dtype=torch.uint8, device=self.mem.device)
+        kvd_pool_attach_host_tier(self.handle, self.host_mem, self.staging, host_blocks)
+        self.host_blocks = host_blocks
 
     def close(self):
         if self.handle is not None:

@@ -19,6 +19,7 @@ SYMBOLS = [
     "kvd_status_string", "kvd_pool_bytes", "kvd_pool_create", "kvd_pool_destroy", "kvd_append_kv",
     "kvd_decode_workspace_bytes", "kvd_decode_attn", "kvd_combine_splits", "kvd_accum_scores",
     "kvd_get_device_error", "kvd_selftest_wait_timeout", "kvd_decode_attn_noalloc",
+    "kvd_tier_bytes", "kvd_pool_attach_host_tier", "kvd_tier_prefetch",
 ]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -66,6 +67,12 @@ def load(build_if_missing: bool = True):
     lib.kvd_pool_create.argtypes = [ctypes.POINTER(PoolDesc), P, sz, ctypes.POINTER(P)]
     lib.kvd_pool_destroy.restype = None
     lib.kvd_pool_destroy.argtypes = [P]
+    lib.kvd_tier_bytes.restype = i32
+    lib.kvd_tier_bytes.argtypes = [ctypes.POINTER(PoolDesc), i64, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+    lib.kvd_pool_attach_host_tier.restype = i32
+    lib.kvd_pool_attach_host_tier.argtypes = [P, P, sz, P, sz, i64]
+    lib.kvd_tier_prefetch.restype = i32
+    lib.kvd_tier_prefetch.argtypes = [P, i32, P]
     lib.kvd_append_kv.restype = i32
     lib.kvd_append_kv.argtypes = [P, i32, P, P, P, i32, P]
     lib.kvd_decode_workspace_bytes.restype = i32
@@ -114,6 +121,26 @@ def kvd_pool_bytes(num_layers: int, n_kv: int, num_blocks: int, kv_dtype: int, d
     pool, kv = ctypes.c_size_t(), ctypes.c_size_t()
     _check("kvd_pool_bytes", load().kvd_pool_bytes(ctypes.byref(d), ctypes.byref(pool), ctypes.byref(kv)))
     return pool.value, kv.value
+
+
+def kvd_tier_bytes(num_layers: int, n_kv: int, num_blocks: int, kv_dtype: int, host_blocks: int, d_h: int = 128,
+                   block_size: int = 16):
+    """(host_bytes, staging_bytes) of a host tier of host_blocks blocks; host only."""
+    d = PoolDesc(num_layers, n_kv, d_h, block_size, num_blocks, kv_dtype)
+    h, st = ctypes.c_size_t(), ctypes.c_size_t()
+    _check("kvd_tier_bytes", load().kvd_tier_bytes(ctypes.byref(d), int(host_blocks), ctypes.byref(h), ctypes.byref(st)))
+    return h.value, st.value
+
+
+def kvd_pool_attach_host_tier(handle, host_mem, staging, host_blocks):
+    """host_mem: pinned host tensor; staging: device tensor (both caller-owned, sized by kvd_tier_bytes)."""
+    _check("kvd_pool_attach_host_tier", load().kvd_pool_attach_host_tier(
+        handle, _ptr(host_mem), 0 if host_mem is None else host_mem.numel() * host_mem.element_size(),
+        _ptr(staging), 0 if staging is None else staging.numel() * staging.element_size(), int(host_blocks)))
+
+
+def kvd_tier_prefetch(handle, layer, stream=None):
+    _check("kvd_tier_prefetch", load().kvd_tier_prefetch(handle, int(layer), _stream(stream)))
 
 
 def kvd_pool_create(num_layers, n_kv, num_blocks, kv_dtype, mem, d_h=128, block_size=16):

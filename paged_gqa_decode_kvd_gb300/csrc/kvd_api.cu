@@ -16,6 +16,11 @@ struct kvd_pool {
     int device;
     int num_sms;
     size_t layer_bytes;
+    // host tier (T1): records in pinned host memory (device address) and two HBM staging slots
+    uint8_t* host_kv;
+    uint8_t* staging;
+    int64_t host_blocks;
+    size_t host_layer_bytes;
 };
 
 namespace {
@@ -128,6 +133,10 @@ kvd_status kvd_pool_create(const kvd_pool_desc* desc, void* mem, size_t len, kvd
     p->mem = static_cast<uint8_t*>(mem);
     p->layer_bytes = need / desc->num_layers;
     p->err = nullptr;
+    p->host_kv = nullptr;
+    p->staging = nullptr;
+    p->host_blocks = 0;
+    p->host_layer_bytes = 0;
     const size_t state_bytes = sizeof(int32_t);
     if (cudaGetDevice(&p->device) != cudaSuccess ||
         cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess ||
@@ -139,6 +148,56 @@ kvd_status kvd_pool_create(const kvd_pool_desc* desc, void* mem, size_t len, kvd
     }
     *out = p;
     return KVD_OK;
+}
+
+kvd_status kvd_tier_bytes(const kvd_pool_desc* desc, int64_t host_blocks, size_t* host_bytes, size_t* staging_bytes) {
+    kvd_status st = check_desc(desc);
+    if (st != KVD_OK) return st;
+    if (host_blocks < 0 || !host_bytes || !staging_bytes) return KVD_ERR_INVALID;
+    const size_t rec = desc->kv_dtype == KVD_FP8_E4M3 ? kvd::kRecordFp8 : kvd::kRecordBf16;
+    size_t layer = 0, all = 0;
+    if (!mul_ok(static_cast<size_t>(host_blocks), static_cast<size_t>(desc->n_kv), &layer)) return KVD_ERR_INVALID;
+    if (!mul_ok(layer, rec, &layer)) return KVD_ERR_INVALID;
+    if (!mul_ok(layer, static_cast<size_t>(desc->num_layers), &all)) return KVD_ERR_INVALID;
+    *host_bytes = all;
+    *staging_bytes = 2 * layer;
+    return KVD_OK;
+}
+
+kvd_status kvd_pool_attach_host_tier(kvd_pool* pool, void* host_mem, size_t host_len, void* staging_mem,
+                                     size_t staging_len, int64_t host_blocks) {
+    if (!pool || host_blocks < 0) return KVD_ERR_INVALID;
+    if (host_blocks == 0) {
+        pool->host_kv = nullptr;
+        pool->staging = nullptr;
+        pool->host_blocks = 0;
+        pool->host_layer_bytes = 0;
+        return KVD_OK;
+    }
+    size_t need_host = 0, need_stage = 0;
+    kvd_status st = kvd_tier_bytes(&pool->desc, host_blocks, &need_host, &need_stage);
+    if (st != KVD_OK) return st;
+    if (!host_mem || !staging_mem || !aligned16(host_mem) || !aligned16(staging_mem)) return KVD_ERR_INVALID;
+    if (host_len < need_host || staging_len < need_stage) return KVD_ERR_NOMEM;
+    void* dev = nullptr;
+    if (cudaHostGetDevicePointer(&dev, host_mem, 0) != cudaSuccess || !dev || !aligned16(dev)) {
+        cudaGetLastError();
+        return KVD_ERR_INVALID;   // host memory this device cannot address
+    }
+    pool->host_kv = static_cast<uint8_t*>(dev);
+    pool->staging = static_cast<uint8_t*>(staging_mem);
+    pool->host_blocks = host_blocks;
+    pool->host_layer_bytes = need_stage / 2;
+    return KVD_OK;
+}
+
+kvd_status kvd_tier_prefetch(kvd_pool* pool, int layer, void* stream) {
+    if (!pool || layer < 0 || layer >= pool->desc.num_layers) return KVD_ERR_INVALID;
+    if (pool->host_blocks == 0) return KVD_OK;
+    const uint8_t* src = pool->host_kv + static_cast<size_t>(layer) * pool->host_layer_bytes;
+    uint8_t* dst = pool->staging + static_cast<size_t>(layer % 2) * pool->host_layer_bytes;
+    return cuda_status(kvd::launch_tier_copy(src, dst, pool->host_layer_bytes, pool->num_sms,
+                                             static_cast<cudaStream_t>(stream)));
 }
 
 void kvd_pool_destroy(kvd_pool* pool) {
@@ -158,9 +217,11 @@ kvd_status kvd_append_kv(kvd_pool* pool, int layer, const void* k_new, const voi
     p.v_new = static_cast<const uint16_t*>(v_new);
     p.slot_mapping = slot_mapping;
     p.kv = pool->mem + static_cast<size_t>(layer) * pool->layer_bytes;
+    p.host_kv = pool->host_kv ? pool->host_kv + static_cast<size_t>(layer) * pool->host_layer_bytes : nullptr;
     p.err = pool->err;
     p.n_tokens = n_tokens;
     p.num_blocks = pool->desc.num_blocks;
+    p.host_blocks = pool->host_blocks;
     p.n_kv = pool->desc.n_kv;
     return cuda_status(kvd::launch_append(p, pool->desc.kv_dtype == KVD_FP8_E4M3, static_cast<cudaStream_t>(stream)));
 }
@@ -220,6 +281,9 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
 
     kvd::DecodeParams p;
     p.kv = pool->mem + static_cast<size_t>(layer) * pool->layer_bytes;
+    p.host_blocks = pool->host_blocks;
+    p.stage = pool->host_blocks ? pool->staging + static_cast<size_t>(layer % 2) * pool->host_layer_bytes : nullptr;
+    p.host_kv = pool->host_blocks ? pool->host_kv + static_cast<size_t>(layer) * pool->host_layer_bytes : nullptr;
     p.q = static_cast<const uint16_t*>(q);
     p.k_new = static_cast<const uint16_t*>(k_new);
     p.v_new = static_cast<const uint16_t*>(v_new);

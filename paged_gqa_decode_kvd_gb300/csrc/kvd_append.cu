@@ -9,7 +9,8 @@
 // scale = absmax/448, or 1 for an all-zero row.
 //
 // One warp per (token, KV head).  Lane l holds dims 4l..4l+3 (an 8-byte
-// coalesced load) and scatters them to their fragment-order positions.
+// coalesced load) and scatters them to their fragment-order positions.  A slot in a
+// host-tier block is written to that block's record in host memory.
 #include "kvd_common.cuh"
 #include "kvd_internal.h"
 
@@ -26,12 +27,15 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
     if (slot < 0) return;
     const int64_t blk = slot / kBs;
     const int t = static_cast<int>(slot % kBs);
-    if (blk >= p.num_blocks) {
+    if (blk >= p.num_blocks + p.host_blocks) {
         if (lane == 0) report(p.err, KVD_ERR_OOB);
         return;
     }
     const int64_t row = (n * p.n_kv + h) * kDh;
-    uint8_t* record = p.kv + (blk * p.n_kv + h) * (FP8 ? kRecordFp8 : kRecordBf16);
+    constexpr int64_t kRec = FP8 ? kRecordFp8 : kRecordBf16;
+    // a host-tier block (id ≥ num_blocks) keeps its record in host memory
+    uint8_t* record = blk < p.num_blocks ? p.kv + (blk * p.n_kv + h) * kRec
+                                         : p.host_kv + ((blk - p.num_blocks) * p.n_kv + h) * kRec;
     write_token<FP8>(record, t, p.k_new + row, p.v_new + row, lane);
 }
 

@@ -94,6 +94,14 @@ struct Segment {
     int64_t unit_end; // flattened index one past the unit
 };
 
+// Record of (physical block ph, KV head h) to read: a pool block, or the staged copy of a
+// host-tier block (ids num_blocks and up).
+template <int64_t kRec>
+__device__ __forceinline__ const uint8_t* record_of(const DecodeParams& p, int ph, int h) {
+    return ph < p.num_blocks ? p.kv + (static_cast<int64_t>(ph) * p.n_kv + h) * kRec
+                             : p.stage + ((static_cast<int64_t>(ph) - p.num_blocks) * p.n_kv + h) * kRec;
+}
+
 // Unit holding flattened block index x: units are ordered (b, kvh); unit (b, kvh)
 // covers [n_kv·pref[b] + kvh·n_b, n_kv·pref[b] + (kvh+1)·n_b).
 __device__ __forceinline__ Segment find_segment(const int* pref, int B, int n_kv, int64_t x, int64_t hi) {
@@ -241,10 +249,14 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
                 const int pos = len - 1;
                 const int ph = bt[pos / kBs];
                 if (p.early) pdl_wait();   // k_new / v_new come from the previous kernel
-                if (ph >= 0 && ph < p.num_blocks) {
+                if (ph >= 0 && ph < p.num_blocks + p.host_blocks) {
                     const int64_t row = (static_cast<int64_t>(sg.b) * p.n_kv + sg.kvh) * kDh;
-                    uint8_t* rec = const_cast<uint8_t*>(p.kv) + (static_cast<int64_t>(ph) * p.n_kv + sg.kvh) * C::kRecord;
+                    uint8_t* rec = const_cast<uint8_t*>(record_of<C::kRecord>(p, ph, sg.kvh));
                     write_token<FP8>(rec, pos % kBs, p.k_new + row, p.v_new + row, lane);
+                    if (ph >= p.num_blocks)   // a host-tier block: its host record too
+                        write_token<FP8>(p.host_kv + ((static_cast<int64_t>(ph) - p.num_blocks) * p.n_kv + sg.kvh) *
+                                                         C::kRecord,
+                                         pos % kBs, p.k_new + row, p.v_new + row, lane);
                     fence_proxy_async_global();
                 }
                 __syncwarp();
@@ -253,9 +265,13 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
                 const int j = jb + lane;
                 int phys = -1;
                 uint32_t vm = 0;
+                unsigned long long raddr = 0;
                 if (j < sg.j1) {
                     phys = bt[j];
-                    if (phys >= 0 && phys < p.num_blocks) {
+                    if (phys >= 0 && phys < p.num_blocks + p.host_blocks) {
+                        // each lane forms its block's record address here, in parallel, so that
+                        // lane 0's serial issue loop below only shuffles it in
+                        raddr = reinterpret_cast<unsigned long long>(record_of<C::kRecord>(p, phys, sg.kvh));
                         const int valid = len - j * kBs;
                         vm = valid >= kBs ? 0xFFFFu : ((1u << valid) - 1u);
                         if (p.retain) vm &= p.retain[phys];
@@ -268,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
                 for (int i = 0; i < cnt; ++i) {
                     const int ph = __shfl_sync(kFull, phys, i);
                     const uint32_t m = __shfl_sync(kFull, vm, i);
+                    const unsigned long long ra = __shfl_sync(kFull, raddr, i);
                     const int s = k % kStages;
                     const uint32_t par = (k / kStages) & 1u;
                     int ok = 1;
@@ -276,8 +293,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
                         if (ok) {
                             meta[s] = static_cast<int>(m);
                             if (m >> 16) {
-                                const uint8_t* rec =
-                                    p.kv + (static_cast<int64_t>(ph) * p.n_kv + sg.kvh) * C::kRecord;
+                                const uint8_t* rec = reinterpret_cast<const uint8_t*>(ra);
                                 uint8_t* dst = ring + s * C::kStage;
                                 mbar_arrive_expect_tx(&full[s], C::kRecord);
                                 bulk_g2s(dst, rec, C::kRecord, &full[s], policy);

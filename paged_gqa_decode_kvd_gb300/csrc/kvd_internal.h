@@ -11,14 +11,19 @@ struct AppendParams {
     const uint16_t* v_new;
     const int64_t* slot_mapping; // [n_tokens]
     uint8_t* kv;                 // this layer's records
+    uint8_t* host_kv;            // this layer's host-tier records (device address), or null
     int32_t* err;
     int64_t n_tokens;
     int64_t num_blocks;
+    int64_t host_blocks;         // host-tier blocks: ids num_blocks .. num_blocks + host_blocks - 1
     int n_kv;
 };
 
 struct DecodeParams {
     const uint8_t* kv;           // this layer's records (FP8: scales inline after the tiles)
+    const uint8_t* stage;        // staged copy of this layer's host-tier records, or null
+    uint8_t* host_kv;            // this layer's host-tier records (device address), or null
+    int64_t host_blocks;         // host-tier blocks: ids num_blocks .. num_blocks + host_blocks - 1
     const uint16_t* q;           // bf16 bits [B][n_q][128]
     const uint16_t* k_new;       // fused append: bf16 [B][n_kv][128] new token, or null
     const uint16_t* v_new;
@@ -100,6 +105,8 @@ inline cudaError_t launch_dependent(void (*kernel)(P...), dim3 grid, dim3 block,
 }
 
 cudaError_t launch_append(const AppendParams& p, bool fp8, cudaStream_t stream);
+// Copy `bytes` (a multiple of 16, both pointers 16-byte aligned) from src to dst.
+cudaError_t launch_tier_copy(const uint8_t* src, uint8_t* dst, size_t bytes, int num_sms, cudaStream_t stream);
 size_t decode_smem_bytes(bool fp8, int batch, int g);
 int decode_ctas_per_sm(bool fp8, int batch, int g);
 int decode_carveout(bool fp8, int batch, int g);   // percent, for the decode call's launches

@@ -52,6 +52,19 @@ def test_fp8_scale_bytes():
     assert pool == kv == 32 * 8192 * 131072 // 8192 * 8192     # 32 GiB: 128 KiB per token
 
 
+def test_host_tier_bytes():
+    """A host tier of hb blocks holds every layer's records of those blocks in host memory;
+    its HBM staging area holds two layers' worth (the prefetch of the next layer overlaps the
+    attention of this one)."""
+    for dtype, rec in ((kvd.KVD_BF16, 8192), (kvd.KVD_FP8_E4M3, 4224)):
+        for hb in (0, 1, 37):
+            host, staging = kvd.kvd_tier_bytes(28, 4, 1000, dtype, hb)
+            assert host == 28 * hb * 4 * rec
+            assert staging == 2 * hb * 4 * rec
+    with pytest.raises(kvd.KvdError):
+        kvd.kvd_tier_bytes(28, 4, 1000, kvd.KVD_BF16, -1)
+
+
 def test_bad_descriptors_are_rejected():
     with pytest.raises(kvd.KvdError) as e:
         kvd.kvd_pool_bytes(32, 8, 16, kvd.KVD_BF16, d_h=64)
