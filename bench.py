@@ -193,7 +193,8 @@ class Step:
     per step index and the timed loop cycles through them.  With scores on, each layer
     also writes its logits and adds its share of the importance score."""
 
-    def __init__(self, w, dev, num_splits: int = 0, early: bool = True, fused_scores: bool = False):
+    def __init__(self, w, dev, num_splits: int = 0, early: bool = True, fused_scores: bool = False,
+                 host_tier: float = 0.0):
         import numpy as np
         import torch
 
@@ -222,6 +223,9 @@ class Step:
                     k, v = w.kv(layer, b, 0, first[b], dev)
                     kvd.kvd_append_kv(self.pool.handle, layer, k.contiguous(), v.contiguous(),
                                       w.slot_mapping(b, 0, first[b], bt).to(dev))
+        self.host_blocks = 0
+        if host_tier > 0:
+            bt = self._host_tier(host_tier, bt)
         # per-step inputs: the appended token of every request, q, context lengths
         self.seq, self.slots, self.k_new, self.v_new, self.q = [], [], [], [], []
         for t in range(self.nsteps):
@@ -261,6 +265,49 @@ class Step:
         err = kvd.kvd_get_device_error(self.pool.handle)
         if err:
             raise RuntimeError(f"device error during setup: {kvd.status_string(err)}")
+
+    def _host_tier(self, frac: float, bt):
+        """Host tier (T1): the tier plan, on seeded synthetic scores, picks the frac·nb least
+        important unprotected blocks of every request; kvd_tier_move copies them to host-tier
+        ids and the block tables and retain mask are patched.  In the step, each layer's host
+        records are staged by a copy-engine DMA on a copy stream, two layers ahead of use."""
+        import torch
+
+        w, kvd, dev = self.w, self.kvd, self.dev
+        g = torch.Generator().manual_seed(w.seed + 7)
+        scores = torch.empty(w.batch, self.max_len).exponential_(generator=g).to(dev)
+        lens = torch.tensor(self.lens[0], dtype=torch.int32, device=dev)
+        mb = bt.shape[1]
+        t1 = int(frac * (max(self.lens[0]) + 15) // 16)
+        plan = torch.empty(w.batch, mb, dtype=torch.int8, device=dev)
+        kvd.kvd_tier_plan(scores, lens, mb, w.protect_prompt, w.protect_recent, t1, plan)
+        plan = plan.cpu()
+        nb = w.num_blocks()
+        bt2 = bt.clone()
+        src = []
+        for b, j in (plan == 1).nonzero().tolist():
+            src.append(int(bt[b, j]))
+            bt2[b, j] = nb + len(src) - 1
+        self.host_blocks = len(src)
+        if not src:
+            return bt
+        self.pool.attach_host_tier(len(src))
+        kvd.kvd_tier_move(self.pool.handle, torch.tensor(src, dtype=torch.int32, device=dev),
+                          torch.arange(nb, nb + len(src), dtype=torch.int32, device=dev))
+        self.bt = bt2.to(dev)
+        if self.retain is not None:
+            self.retain = torch.cat([self.retain, self.retain[torch.tensor(src, device=dev)]])
+        self.copy = torch.cuda.Stream(device=dev)
+        self.host_layer_bytes = self.host_blocks * w.n_kv * self.pool.record_bytes
+        return bt2
+
+    def _prefetch(self, layer: int):
+        import torch
+
+        self.kvd.kvd_tier_prefetch(self.pool.handle, layer, stream=self.copy)
+        ev = torch.cuda.Event()
+        ev.record(self.copy)
+        self.staged[layer] = ev
 
     def kv_bytes(self, t: int) -> int:
         w = self.w
@@ -321,12 +368,24 @@ class Step:
     def run(self, t: int = 0, stream=None):
         import torch
 
+        cur = stream if stream is not None else torch.cuda.current_stream(self.dev)
         if self.overlap:
             self.score_done = [None] * len(self.score_done)   # a step depends on nothing of the last
+        if self.host_blocks:   # staging slots 0 and 1 are free at the start of a step
+            self.copy.wait_stream(cur)
+            self.staged = [None] * self.L
+            for layer in range(min(2, self.L)):
+                self._prefetch(layer)
         for layer in range(self.L):
+            if self.host_blocks:
+                cur.wait_event(self.staged[layer])
             self.layer_call(layer, t, stream)
+            if self.host_blocks and layer + 2 < self.L:   # refill this layer's slot once it is read
+                done = torch.cuda.Event()
+                done.record(cur)
+                self.copy.wait_event(done)
+                self._prefetch(layer + 2)
         if self.overlap:   # the step ends when its last score update has
-            cur = stream if stream is not None else torch.cuda.current_stream(self.dev)
             cur.wait_stream(self.side)
 
     def capture(self):
@@ -354,7 +413,8 @@ def gpu_arm(args, w, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     peaks = measured_peaks()
-    st = Step(w, dev, args.num_splits, early=not args.no_early_start, fused_scores=args.fused_scores)
+    st = Step(w, dev, args.num_splits, early=not args.no_early_start, fused_scores=args.fused_scores,
+              host_tier=args.host_tier)
     graphs = st.capture()
     stream = torch.cuda.current_stream(dev)
     # closed-form KV bytes of the timed steps (step t of the workload = graph t % steps)
@@ -440,7 +500,11 @@ def gpu_arm(args, w, rank, world, local):
                    "decode_steps_cycled": st.nsteps, "scores": bool(w.scores),
                    "score_update": ("second stream (off the layer chain)" if st.overlap else
                                     "fused into the merge launch" if w.scores else None),
-                   "l2": "inputs larger than L2 (KV pool streamed every step)", "parallelism": f"replicas x{world}"},
+                   "l2": "inputs larger than L2 (KV pool streamed every step)", "parallelism": f"replicas x{world}",
+                   "host_tier": None if not st.host_blocks else {
+                       "fraction": args.host_tier, "host_blocks": st.host_blocks,
+                       "host_bytes_per_step": st.host_layer_bytes * w.L,
+                       "prefetch": "copy-engine DMA per layer on a copy stream, two layers ahead"}},
         "steps_per_s": round(1e3 / ms_per_step, 2),
         "hbm_frac_of_measured": round(value / world / peaks["hbm_gbs"], 4),
         "hbm_frac_of_datasheet_8tbs": round(value / world / 8000.0, 4),
@@ -523,6 +587,8 @@ def main(argv=None):
     ap.add_argument("--no-early-start", action="store_true", help="launch the decode kernel without KVD_EARLY_START")
     ap.add_argument("--fused-scores", action="store_true",
                     help="score update inside each layer's merge launch (one stream) instead of on a second stream")
+    ap.add_argument("--host-tier", type=float, default=0.0,
+                    help="fraction of each request's blocks the tier plan moves to the host tier (T1)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")

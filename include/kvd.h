@@ -153,11 +153,43 @@ KVD_API kvd_status kvd_pool_attach_host_tier(kvd_pool* pool, void* host_mem, siz
                                              size_t staging_len, int64_t host_blocks);
 
 /* Copy layer's host-tier records into staging slot layer % 2 (host_blocks·n_kv·record_bytes
- * bytes over the host link) on `stream`.  It must complete before a kvd_decode_attn of that
+ * bytes over the host link, one asynchronous DMA on a copy engine, so that it overlaps a
+ * decode kernel running on another stream) on `stream`.  It must complete before a kvd_decode_attn of that
  * layer reads a host-tier block (same stream, or an event), and a slot is refilled two layers
  * later, so the prefetch of layer ℓ+2 must wait for the attention of layer ℓ.  A no-op
  * without a host tier. */
 KVD_API kvd_status kvd_tier_prefetch(kvd_pool* pool, int layer, void* stream);
+
+/* Tier plan from the cumulative importance scores (same page, section "4. 시스템 구현":
+ * tiers are reassigned every Δ = 64 decode steps; section "1. 4 단계 분류": protected
+ * tokens — prompt, attention sinks, recent window — and the most important ones stay in HBM,
+ * mid-importance ones go to host memory).  For request b with seq_lens[b] = len and
+ * nb = ⌈len/16⌉ logical blocks (nb = 0 for a length outside [1, max_blocks_per_seq·16]):
+ *   importance[b][j] = Σ_{o=0..15, 16j+o < len} scores[b][16j+o], added in that order in fp32
+ *   (positions at or past scores_stride count 0);
+ *   block j is protected if it holds a position < protect_prompt or ≥ len - protect_recent;
+ *   tier[b][j] = 1 (host tier) for the t1_blocks unprotected blocks of smallest
+ *   (importance, j) — all unprotected blocks if there are fewer — else 0; tier[b][j] = -1
+ *   for j ≥ nb.  Evicted slots (tier T3, the retain mask) carry score 0 and are not treated
+ *   specially.
+ *  scores      f32 [batch][scores_stride], device (as accumulated by kvd_accum_scores)
+ *  importance  f32 [batch][max_blocks_per_seq] out (0 for j ≥ nb), or NULL
+ *  tier        int8 [batch][max_blocks_per_seq] out, device
+ * Moving the blocks (kvd_tier_move) and patching the block tables is the caller's: only
+ * blocks whose tier changed need to move.  Needs max_blocks_per_seq ≤ 16384
+ * (KVD_ERR_UNSUPPORTED otherwise); work per request grows as nb².  Negative protect_*,
+ * t1_blocks or batch, scores_stride < 1 or max_blocks_per_seq < 1: KVD_ERR_INVALID; batch = 0
+ * is a no-op. */
+KVD_API kvd_status kvd_tier_plan(const float* scores, int64_t scores_stride, const int32_t* seq_lens, int batch,
+                                 int max_blocks_per_seq, int protect_prompt, int protect_recent, int t1_blocks,
+                                 float* importance, int8_t* tier, void* stream);
+
+/* Copy every layer's and KV head's record of physical block from_ids[i] to physical block
+ * to_ids[i], i < n (int32 device arrays; ids of either tier).  No block may be both a source
+ * and a destination of the same call.  An id outside the pool and its host tier sets
+ * KVD_ERR_OOB on the device and that pair is skipped. */
+KVD_API kvd_status kvd_tier_move(kvd_pool* pool, const int32_t* from_ids, const int32_t* to_ids, int n,
+                                 void* stream);
 
 /* Decode-step append ("reshape and cache").  Token n's keys k_new[n][h][:] and values
  * v_new[n][h][:] (bf16, [n_tokens][n_kv][d_h], device) are written for every KV head h of

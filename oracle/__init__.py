@@ -6,7 +6,8 @@ library (``paged_gqa_decode_kvd_gb300``) and neither imports the other.
 
 Parity pins (all in ``tests/test_oracle.py``, run with ``-m "not gpu"``):
 e4m3 decode/encode, row quantise, the paged gather, decode attention, the
-split-free softmax statistics and the importance-score update are each pinned
+split-free softmax statistics, the importance-score update and the block tier
+plan are each pinned
 to something other than the oracle itself; no function here is "parity
 unpinned".
 """
@@ -20,5 +21,6 @@ from .oracle import (  # noqa: F401
     OraclePool,
     decode,
     score_update,
+    tier_plan,
     decode_dense_inputs,
 )

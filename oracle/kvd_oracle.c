@@ -238,3 +238,66 @@ void kvdo_score_update(const double* alpha, int L, int B, int H, const int32_t* 
         }
     }
 }
+
+/* ------------------------------------------------------------- tier plan */
+
+/* Tier assignment every Δ steps: page "기술 요약: 모든 사고가 HBM 을 필요로 하는 것은
+ * 아님", section "1. 4 단계 분류" (protected tokens — prompt, sinks, recent window — stay
+ * in HBM; mid-importance tokens go to host memory, T1) and section "4. 시스템 구현"
+ * (reassignment every Δ = 64 steps), at the granularity of a 16-token block.
+ *
+ * For request b of length len, block j covers positions [bs·j, min(bs·j+bs, len)).
+ *   importance[b][j] = the fp32 sum of scores[b][pos] over those positions, added in
+ *     position order (positions at or past `stride` count 0);
+ *   block j is protected when one of its positions is < protect_prompt or
+ *     ≥ len − protect_recent;
+ *   the unprotected blocks, sorted by (importance, j) ascending, give their first t1
+ *     entries tier 1 and the rest tier 0; protected blocks get 0; j ≥ ⌈len/bs⌉ gets −1.
+ * A length outside [1, max_blocks·bs] counts as 0 blocks.  The sum is single precision
+ * because the tier is an integer decided by comparing sums: both sides of a parity test
+ * take that decision in the same precision. */
+typedef struct {
+    float imp;
+    int j;
+} kvdo_block_key;
+
+static int kvdo_block_key_cmp(const void* a, const void* b) {
+    const kvdo_block_key* x = (const kvdo_block_key*)a;
+    const kvdo_block_key* y = (const kvdo_block_key*)b;
+    if (x->imp < y->imp) return -1;
+    if (x->imp > y->imp) return 1;
+    return (x->j > y->j) - (x->j < y->j);
+}
+
+void kvdo_tier_plan(const float* scores, int64_t stride, const int32_t* seq_lens, int B, int max_blocks,
+                    int block_size, int protect_prompt, int protect_recent, int t1, float* importance,
+                    int8_t* tier) {
+    kvdo_block_key* keys = (kvdo_block_key*)malloc(sizeof(kvdo_block_key) * (size_t)(max_blocks > 0 ? max_blocks : 1));
+    for (int b = 0; b < B; ++b) {
+        const int64_t len = seq_lens[b];
+        int64_t nb = (len + block_size - 1) / block_size;
+        if (len < 1 || nb > max_blocks) nb = 0;
+        float* imp = importance + (int64_t)b * max_blocks;
+        int8_t* tr = tier + (int64_t)b * max_blocks;
+        int n_free = 0;
+        for (int j = 0; j < max_blocks; ++j) {
+            imp[j] = 0.0f;
+            tr[j] = -1;
+            if (j >= nb) continue;
+            int prot = 0;
+            for (int64_t pos = (int64_t)j * block_size; pos < (int64_t)(j + 1) * block_size && pos < len; ++pos) {
+                if (pos < stride) imp[j] += scores[(int64_t)b * stride + pos];
+                if (pos < protect_prompt || pos >= len - protect_recent) prot = 1;
+            }
+            tr[j] = 0;
+            if (!prot) {
+                keys[n_free].imp = imp[j];
+                keys[n_free].j = j;
+                ++n_free;
+            }
+        }
+        qsort(keys, (size_t)n_free, sizeof(kvdo_block_key), kvdo_block_key_cmp);
+        for (int r = 0; r < n_free && r < t1; ++r) tr[keys[r].j] = 1;
+    }
+    free(keys);
+}

@@ -63,6 +63,7 @@ def _load():
             lib.kvdo_decode.argtypes = [i32, i32, i32, i32, i64, P, P, P, P, i32, P, i32, P, f64,
                                         P, P, P, P, i64]
             lib.kvdo_score_update.argtypes = [P, i32, i32, i32, P, i64, P]
+            lib.kvdo_tier_plan.argtypes = [P, i64, P, i32, i32, i32, i32, i32, i32, P, P]
             _lib = lib
     return _lib
 
@@ -180,6 +181,21 @@ def score_update(s, alpha_layers, seq_lens) -> np.ndarray:
     sl = _c(seq_lens, np.int32)
     _load().kvdo_score_update(_p(a), L, B, H, _p(sl), stride, _p(out))
     return out
+
+
+def tier_plan(scores, seq_lens, max_blocks: int, protect_prompt: int, protect_recent: int, t1: int,
+              block_size: int = 16) -> tuple[np.ndarray, np.ndarray]:
+    """Per-block importance (fp32 [B][max_blocks]) and tier (int8: 1 host, 0 HBM, -1 past the
+    context) from cumulative scores [B][stride] (fp32)."""
+    sc = _c(scores, np.float32)
+    B, stride = sc.shape
+    sl = _c(seq_lens, np.int32)
+    assert sl.shape == (B,)
+    imp = np.zeros((B, max_blocks), np.float32)
+    tier = np.zeros((B, max_blocks), np.int8)
+    _load().kvdo_tier_plan(_p(sc), stride, _p(sl), B, int(max_blocks), int(block_size), int(protect_prompt),
+                           int(protect_recent), int(t1), _p(imp), _p(tier))
+    return imp, tier
 
 
 def decode_dense_inputs(k_logical, v_logical, q, seq_lens, n_q, evicted=None, fp8=False, softmax_scale=None):

@@ -28,6 +28,8 @@ from ._lib import (  # noqa: F401
     kvd_pool_attach_host_tier,
     kvd_tier_bytes,
     kvd_tier_prefetch,
+    kvd_tier_plan,
+    kvd_tier_move,
     kvd_combine_splits,
     kvd_decode_attn,
     kvd_decode_attn_noalloc,

@@ -19,7 +19,7 @@ SYMBOLS = [
     "kvd_status_string", "kvd_pool_bytes", "kvd_pool_create", "kvd_pool_destroy", "kvd_append_kv",
     "kvd_decode_workspace_bytes", "kvd_decode_attn", "kvd_combine_splits", "kvd_accum_scores",
     "kvd_get_device_error", "kvd_selftest_wait_timeout", "kvd_decode_attn_noalloc",
-    "kvd_tier_bytes", "kvd_pool_attach_host_tier", "kvd_tier_prefetch",
+    "kvd_tier_bytes", "kvd_pool_attach_host_tier", "kvd_tier_prefetch", "kvd_tier_plan", "kvd_tier_move",
 ]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -73,6 +73,10 @@ def load(build_if_missing: bool = True):
     lib.kvd_pool_attach_host_tier.argtypes = [P, P, sz, P, sz, i64]
     lib.kvd_tier_prefetch.restype = i32
     lib.kvd_tier_prefetch.argtypes = [P, i32, P]
+    lib.kvd_tier_plan.restype = i32
+    lib.kvd_tier_plan.argtypes = [P, i64, P, i32, i32, i32, i32, i32, P, P, P]
+    lib.kvd_tier_move.restype = i32
+    lib.kvd_tier_move.argtypes = [P, P, P, i32, P]
     lib.kvd_append_kv.restype = i32
     lib.kvd_append_kv.argtypes = [P, i32, P, P, P, i32, P]
     lib.kvd_decode_workspace_bytes.restype = i32
@@ -141,6 +145,25 @@ def kvd_pool_attach_host_tier(handle, host_mem, staging, host_blocks):
 
 def kvd_tier_prefetch(handle, layer, stream=None):
     _check("kvd_tier_prefetch", load().kvd_tier_prefetch(handle, int(layer), _stream(stream)))
+
+
+def kvd_tier_plan(scores, seq_lens, max_blocks_per_seq, protect_prompt, protect_recent, t1_blocks, tier,
+                  importance=None, stream=None):
+    """Tier plan: tier (int8 [B][max_blocks], device) gets 1 for the t1_blocks least important
+    unprotected blocks of each request, 0 for the others, -1 past the context; importance
+    (f32, same shape, optional) gets the per-block score sums.  scores: f32 [B][stride]."""
+    _check("kvd_tier_plan", load().kvd_tier_plan(_ptr(scores), int(scores.stride(0)), _ptr(seq_lens),
+                                                 int(seq_lens.shape[0]), int(max_blocks_per_seq),
+                                                 int(protect_prompt), int(protect_recent), int(t1_blocks),
+                                                 _ptr(importance), _ptr(tier), _stream(stream)))
+
+
+def kvd_tier_move(handle, from_ids, to_ids, stream=None):
+    """Copy every layer's records of physical block from_ids[i] to to_ids[i] (int32 device tensors)."""
+    n = int(from_ids.numel())
+    if int(to_ids.numel()) != n:
+        raise ValueError("from_ids and to_ids differ in length")
+    _check("kvd_tier_move", load().kvd_tier_move(handle, _ptr(from_ids), _ptr(to_ids), n, _stream(stream)))
 
 
 def kvd_pool_create(num_layers, n_kv, num_blocks, kv_dtype, mem, d_h=128, block_size=16):

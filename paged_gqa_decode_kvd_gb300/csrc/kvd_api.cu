@@ -17,7 +17,8 @@ struct kvd_pool {
     int num_sms;
     size_t layer_bytes;
     // host tier (T1): records in pinned host memory (device address) and two HBM staging slots
-    uint8_t* host_kv;
+    uint8_t* host_kv;      // device address of the host records
+    uint8_t* host_mem;     // the same records' host address (the prefetch's DMA source)
     uint8_t* staging;
     int64_t host_blocks;
     size_t host_layer_bytes;
@@ -134,6 +135,7 @@ kvd_status kvd_pool_create(const kvd_pool_desc* desc, void* mem, size_t len, kvd
     p->layer_bytes = need / desc->num_layers;
     p->err = nullptr;
     p->host_kv = nullptr;
+    p->host_mem = nullptr;
     p->staging = nullptr;
     p->host_blocks = 0;
     p->host_layer_bytes = 0;
@@ -169,6 +171,7 @@ kvd_status kvd_pool_attach_host_tier(kvd_pool* pool, void* host_mem, size_t host
     if (!pool || host_blocks < 0) return KVD_ERR_INVALID;
     if (host_blocks == 0) {
         pool->host_kv = nullptr;
+        pool->host_mem = nullptr;
         pool->staging = nullptr;
         pool->host_blocks = 0;
         pool->host_layer_bytes = 0;
@@ -185,6 +188,7 @@ kvd_status kvd_pool_attach_host_tier(kvd_pool* pool, void* host_mem, size_t host
         return KVD_ERR_INVALID;   // host memory this device cannot address
     }
     pool->host_kv = static_cast<uint8_t*>(dev);
+    pool->host_mem = static_cast<uint8_t*>(host_mem);
     pool->staging = static_cast<uint8_t*>(staging_mem);
     pool->host_blocks = host_blocks;
     pool->host_layer_bytes = need_stage / 2;
@@ -194,10 +198,54 @@ kvd_status kvd_pool_attach_host_tier(kvd_pool* pool, void* host_mem, size_t host
 kvd_status kvd_tier_prefetch(kvd_pool* pool, int layer, void* stream) {
     if (!pool || layer < 0 || layer >= pool->desc.num_layers) return KVD_ERR_INVALID;
     if (pool->host_blocks == 0) return KVD_OK;
-    const uint8_t* src = pool->host_kv + static_cast<size_t>(layer) * pool->host_layer_bytes;
+    // One DMA on a copy engine: the decode kernel holds every SM while it runs, so a copy
+    // made by SMs could not overlap it.
+    const uint8_t* src = pool->host_mem + static_cast<size_t>(layer) * pool->host_layer_bytes;
     uint8_t* dst = pool->staging + static_cast<size_t>(layer % 2) * pool->host_layer_bytes;
-    return cuda_status(kvd::launch_tier_copy(src, dst, pool->host_layer_bytes, pool->num_sms,
-                                             static_cast<cudaStream_t>(stream)));
+    return cuda_status(cudaMemcpyAsync(dst, src, pool->host_layer_bytes, cudaMemcpyHostToDevice,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+kvd_status kvd_tier_plan(const float* scores, int64_t scores_stride, const int32_t* seq_lens, int batch,
+                         int max_blocks_per_seq, int protect_prompt, int protect_recent, int t1_blocks,
+                         float* importance, int8_t* tier, void* stream) {
+    if (batch < 0 || scores_stride < 1 || max_blocks_per_seq < 1 || protect_prompt < 0 || protect_recent < 0 ||
+        t1_blocks < 0)
+        return KVD_ERR_INVALID;
+    if (max_blocks_per_seq > kvd::kMaxPlanBlocks) return KVD_ERR_UNSUPPORTED;
+    if (batch == 0) return KVD_OK;
+    if (!scores || !seq_lens || !tier) return KVD_ERR_INVALID;
+    kvd::TierPlanParams p;
+    p.scores = scores;
+    p.scores_stride = scores_stride;
+    p.seq_lens = seq_lens;
+    p.importance = importance;
+    p.tier = tier;
+    p.B = batch;
+    p.max_blocks = max_blocks_per_seq;
+    p.protect_prompt = protect_prompt;
+    p.protect_recent = protect_recent;
+    p.t1 = t1_blocks;
+    return cuda_status(kvd::launch_tier_plan(p, static_cast<cudaStream_t>(stream)));
+}
+
+kvd_status kvd_tier_move(kvd_pool* pool, const int32_t* from_ids, const int32_t* to_ids, int n, void* stream) {
+    if (!pool || n < 0) return KVD_ERR_INVALID;
+    if (n == 0) return KVD_OK;
+    if (!from_ids || !to_ids) return KVD_ERR_INVALID;
+    kvd::TierMoveParams p;
+    p.from_ids = from_ids;
+    p.to_ids = to_ids;
+    p.kv = pool->mem;
+    p.host_kv = pool->host_kv;
+    p.err = pool->err;
+    p.num_blocks = pool->desc.num_blocks;
+    p.host_blocks = pool->host_blocks;
+    p.record_bytes = pool->desc.kv_dtype == KVD_FP8_E4M3 ? kvd::kRecordFp8 : kvd::kRecordBf16;
+    p.n = n;
+    p.L = pool->desc.num_layers;
+    p.n_kv = pool->desc.n_kv;
+    return cuda_status(kvd::launch_tier_move(p, pool->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
 void kvd_pool_destroy(kvd_pool* pool) {

@@ -105,8 +105,36 @@ inline cudaError_t launch_dependent(void (*kernel)(P...), dim3 grid, dim3 block,
 }
 
 cudaError_t launch_append(const AppendParams& p, bool fp8, cudaStream_t stream);
-// Copy `bytes` (a multiple of 16, both pointers 16-byte aligned) from src to dst.
-cudaError_t launch_tier_copy(const uint8_t* src, uint8_t* dst, size_t bytes, int num_sms, cudaStream_t stream);
+constexpr int kMaxPlanBlocks = 16384;   // the plan keeps a request's importances in shared memory
+
+struct TierPlanParams {
+    const float* scores;
+    int64_t scores_stride;
+    const int32_t* seq_lens;
+    float* importance;           // [B][max_blocks] or null
+    int8_t* tier;                // [B][max_blocks]
+    int B;
+    int max_blocks;
+    int protect_prompt;
+    int protect_recent;
+    int t1;
+};
+cudaError_t launch_tier_plan(const TierPlanParams& p, cudaStream_t stream);
+
+struct TierMoveParams {
+    const int32_t* from_ids;
+    const int32_t* to_ids;
+    uint8_t* kv;                 // the whole pool (every layer)
+    uint8_t* host_kv;            // the whole host tier (device address), or null
+    int32_t* err;
+    int64_t num_blocks;
+    int64_t host_blocks;
+    int64_t record_bytes;
+    int n;
+    int L;
+    int n_kv;
+};
+cudaError_t launch_tier_move(const TierMoveParams& p, int num_sms, cudaStream_t stream);
 size_t decode_smem_bytes(bool fp8, int batch, int g);
 int decode_ctas_per_sm(bool fp8, int batch, int g);
 int decode_carveout(bool fp8, int batch, int g);   // percent, for the decode call's launches

@@ -357,3 +357,75 @@ def test_score_sum_grows_by_one_per_step_and_single_head_is_softmax():
     s1 = oracle.score_update(np.zeros((1, 30)), res["alpha"][None], [30])
     lg = (q[0, 0].astype(np.float64) @ ks[0][:, 0].astype(np.float64).T) / 4.0
     np.testing.assert_allclose(s1[0], torch.softmax(torch.from_numpy(lg), 0).numpy(), rtol=1e-12)
+
+
+# ------------------------------------------------------------------ tier plan
+def _tier_of(imp_per_block, length, max_blocks, pp, pr, t1):
+    """Scores that put imp_per_block[j] on the first position of block j (the rest 0)."""
+    s = np.zeros((1, max_blocks * 16), np.float32)
+    for j, x in enumerate(imp_per_block):
+        s[0, 16 * j] = x
+    return oracle.tier_plan(s, [length], max_blocks, pp, pr, t1)
+
+
+def test_tier_plan_worked_example():
+    # length 100: blocks 0..6, the last holding positions 96..99.  protect_prompt 20 covers
+    # blocks 0 and 1 (block 1 holds 16..19); protect_recent 5 covers positions 95..99, i.e.
+    # block 5 (80..95) and block 6.  Unprotected: 2, 3, 4 with importances 3, 1, 2.
+    imp, tier = _tier_of([9, 9, 3, 1, 2, 9, 9], 100, 8, 20, 5, 2)
+    assert tier[0].tolist() == [0, 0, 0, 1, 1, 0, 0, -1]
+    assert imp[0].tolist() == [9, 9, 3, 1, 2, 9, 9, 0]
+    # protect_recent 4 leaves block 5 free (its last position 95 < 96); importance 0.5 ranks first
+    _, tier = _tier_of([9, 9, 3, 1, 2, 0.5, 9], 100, 8, 20, 4, 2)
+    assert tier[0].tolist() == [0, 0, 0, 1, 0, 1, 0, -1]
+    # no recent window: the partial last block is free too (it holds no position ≥ 100)
+    _, tier = _tier_of([9, 9, 3, 1, 2, 9, 0.25], 100, 8, 20, 0, 1)
+    assert tier[0].tolist() == [0, 0, 0, 0, 0, 0, 1, -1]
+    # t1 above the free count: every free block goes to the host tier
+    _, tier = _tier_of([9, 9, 3, 1, 2, 9, 9], 100, 8, 20, 5, 10)
+    assert tier[0].tolist() == [0, 0, 1, 1, 1, 0, 0, -1]
+    # t1 = 0 keeps everything in HBM; ties go to the lower block index
+    _, tier = _tier_of([9, 9, 3, 1, 2, 9, 9], 100, 8, 20, 5, 0)
+    assert tier[0].tolist() == [0, 0, 0, 0, 0, 0, 0, -1]
+    _, tier = _tier_of([1, 1, 1, 1, 1, 1, 1], 112, 8, 0, 0, 3)
+    assert tier[0].tolist() == [1, 1, 1, 0, 0, 0, 0, -1]
+
+
+def test_tier_plan_importance_closed_forms():
+    # unit scores: block j's importance is its number of positions (16, or the tail)
+    s = np.ones((3, 64), np.float32)
+    imp, tier = oracle.tier_plan(s, [37, 64, 0], 5, 0, 0, 0)
+    assert imp[0].tolist() == [16, 16, 5, 0, 0]
+    assert imp[1].tolist() == [16, 16, 16, 16, 0]
+    assert tier[2].tolist() == [-1] * 5 and imp[2].tolist() == [0] * 5   # empty request
+    # positions at or past the score stride count 0
+    imp, _ = oracle.tier_plan(np.ones((1, 40), np.float32), [64], 4, 0, 0, 0)
+    assert imp[0].tolist() == [16, 16, 8, 0]
+    # a length beyond max_blocks·16 is treated as empty
+    _, tier = oracle.tier_plan(np.ones((1, 64), np.float32), [49], 3, 0, 0, 1)
+    assert tier[0].tolist() == [-1, -1, -1]
+
+
+def test_tier_plan_matches_sorting_and_fp64_sums():
+    rng = _rng(7)
+    lens = [1, 16, 17, 300, 1023, 2048]
+    mb = 128
+    s = rng.exponential(1e-3, size=(len(lens), mb * 16)).astype(np.float32)
+    s[:, ::5] = np.round(s[:, ::5], 4)              # some equal values, so ties occur
+    s[3, 16:48] = 0.0                               # two all-zero blocks: a tie on importance 0
+    for pp, pr, t1 in [(0, 0, 3), (64, 32, 10), (5, 1, 1000), (2048, 0, 4)]:
+        imp, tier = oracle.tier_plan(s, lens, mb, pp, pr, t1)
+        for b, ln in enumerate(lens):
+            nb = (ln + 15) // 16
+            assert np.all(tier[b, nb:] == -1) and np.all(imp[b, nb:] == 0)
+            exact = np.array([np.sum(s[b, 16 * j:min(16 * j + 16, ln)].astype(np.float64)) for j in range(nb)])
+            mag = np.array([np.sum(np.abs(s[b, 16 * j:min(16 * j + 16, ln)].astype(np.float64))) for j in range(nb)])
+            assert np.all(np.abs(imp[b, :nb] - exact) <= 16 * 2.0 ** -24 * mag + 1e-30)
+            prot = np.array([any(p < pp or p >= ln - pr for p in range(16 * j, min(16 * j + 16, ln)))
+                             for j in range(nb)], bool)
+            free = np.nonzero(~prot)[0]
+            order = free[np.lexsort((free, imp[b, free]))]   # by importance, then block index
+            want = np.zeros(nb, np.int8)
+            want[order[:t1]] = 1
+            assert tier[b, :nb].tolist() == want.tolist()
+            assert int((tier[b] == 1).sum()) == min(t1, len(free))
