@@ -194,7 +194,7 @@ class Step:
     also writes its logits and adds its share of the importance score."""
 
     def __init__(self, w, dev, num_splits: int = 0, early: bool = True, fused_scores: bool = False,
-                 host_tier: float = 0.0):
+                 host_tier: float = 0.0, host_staged: bool = False):
         import numpy as np
         import torch
 
@@ -224,6 +224,7 @@ class Step:
                     kvd.kvd_append_kv(self.pool.handle, layer, k.contiguous(), v.contiguous(),
                                       w.slot_mapping(b, 0, first[b], bt).to(dev))
         self.host_blocks = 0
+        self.host_staged = host_staged
         if host_tier > 0:
             bt = self._host_tier(host_tier, bt)
         # per-step inputs: the appended token of every request, q, context lengths
@@ -269,8 +270,9 @@ class Step:
     def _host_tier(self, frac: float, bt):
         """Host tier (T1): the tier plan, on seeded synthetic scores, picks the frac·nb least
         important unprotected blocks of every request; kvd_tier_move copies them to host-tier
-        ids and the block tables and retain mask are patched.  In the step, each layer's host
-        records are staged by a copy-engine DMA on a copy stream, two layers ahead of use."""
+        ids and the block tables and retain mask are patched.  In the step the decode kernel
+        reads them in place over the host link, or (staged) each layer's host records are
+        copied by a copy-engine DMA on a copy stream, two layers ahead of use."""
         import torch
 
         w, kvd, dev = self.w, self.kvd, self.dev
@@ -281,6 +283,7 @@ class Step:
         t1 = int(frac * (max(self.lens[0]) + 15) // 16)
         plan = torch.empty(w.batch, mb, dtype=torch.int8, device=dev)
         kvd.kvd_tier_plan(scores, lens, mb, w.protect_prompt, w.protect_recent, t1, plan)
+        self.plan_args = (scores, lens, mb, w.protect_prompt, w.protect_recent, t1, plan.clone())
         plan = plan.cpu()
         nb = w.num_blocks()
         bt2 = bt.clone()
@@ -291,15 +294,52 @@ class Step:
         self.host_blocks = len(src)
         if not src:
             return bt
-        self.pool.attach_host_tier(len(src))
-        kvd.kvd_tier_move(self.pool.handle, torch.tensor(src, dtype=torch.int32, device=dev),
-                          torch.arange(nb, nb + len(src), dtype=torch.int32, device=dev))
+        self.pool.attach_host_tier(len(src), staged=self.host_staged)
+        self.move_ids = (torch.tensor(src, dtype=torch.int32, device=dev),
+                         torch.arange(nb, nb + len(src), dtype=torch.int32, device=dev))
+        kvd.kvd_tier_move(self.pool.handle, *self.move_ids)
         self.bt = bt2.to(dev)
         if self.retain is not None:
             self.retain = torch.cat([self.retain, self.retain[torch.tensor(src, device=dev)]])
         self.copy = torch.cuda.Stream(device=dev)
         self.host_layer_bytes = self.host_blocks * w.n_kv * self.pool.record_bytes
         return bt2
+
+    def time_host_tier(self, reps: int = 5) -> dict:
+        """Host-tier costs measured alone on the copy stream: one step's staging copies, one
+        tier plan, and one move of the planned blocks HBM → host (a reassignment that demotes
+        them all; the vacated HBM blocks still hold the same records, so repeating it changes
+        nothing)."""
+        import torch
+
+        kvd, s = self.kvd, self.copy
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+        def timed(fn, n):
+            torch.cuda.synchronize()
+            e0.record(s)
+            for _ in range(n):
+                fn()
+            e1.record(s)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / n
+
+        def stage():
+            for layer in range(self.L):
+                kvd.kvd_tier_prefetch(self.pool.handle, layer, stream=s)
+
+        stage_ms = timed(stage, reps) if self.host_staged else None
+        plan_ms = timed(lambda: kvd.kvd_tier_plan(*self.plan_args, stream=s), reps)
+        move_ms = timed(lambda: kvd.kvd_tier_move(self.pool.handle, *self.move_ids, stream=s), reps)
+        err = kvd.kvd_get_device_error(self.pool.handle)
+        if err:
+            raise RuntimeError(f"device error in the host-tier timing: {kvd.status_string(err)}")
+        step_bytes = self.host_layer_bytes * self.L
+        return {"staging_ms_per_step_alone": round(stage_ms, 4) if stage_ms else None,
+                "staging_gbs_alone": round(step_bytes / (stage_ms * 1e-3) / 1e9, 1) if stage_ms else None,
+                "plan_ms": round(plan_ms, 4), "move_ms": round(move_ms, 4),
+                "move_gbs": round(step_bytes / (move_ms * 1e-3) / 1e9, 1),
+                "retier_ms_per_step_at_delta_64": round((plan_ms + move_ms) / 64, 4)}
 
     def _prefetch(self, layer: int):
         import torch
@@ -371,16 +411,17 @@ class Step:
         cur = stream if stream is not None else torch.cuda.current_stream(self.dev)
         if self.overlap:
             self.score_done = [None] * len(self.score_done)   # a step depends on nothing of the last
-        if self.host_blocks:   # staging slots 0 and 1 are free at the start of a step
+        staged = self.host_blocks and self.host_staged
+        if staged:   # staging slots 0 and 1 are free at the start of a step
             self.copy.wait_stream(cur)
             self.staged = [None] * self.L
             for layer in range(min(2, self.L)):
                 self._prefetch(layer)
         for layer in range(self.L):
-            if self.host_blocks:
+            if staged:
                 cur.wait_event(self.staged[layer])
             self.layer_call(layer, t, stream)
-            if self.host_blocks and layer + 2 < self.L:   # refill this layer's slot once it is read
+            if staged and layer + 2 < self.L:   # refill this layer's slot once it is read
                 done = torch.cuda.Event()
                 done.record(cur)
                 self.copy.wait_event(done)
@@ -414,7 +455,7 @@ def gpu_arm(args, w, rank, world, local):
     torch.cuda.set_device(dev)
     peaks = measured_peaks()
     st = Step(w, dev, args.num_splits, early=not args.no_early_start, fused_scores=args.fused_scores,
-              host_tier=args.host_tier)
+              host_tier=args.host_tier, host_staged=args.host_tier_staged)
     graphs = st.capture()
     stream = torch.cuda.current_stream(dev)
     # closed-form KV bytes of the timed steps (step t of the workload = graph t % steps)
@@ -504,7 +545,9 @@ def gpu_arm(args, w, rank, world, local):
                    "host_tier": None if not st.host_blocks else {
                        "fraction": args.host_tier, "host_blocks": st.host_blocks,
                        "host_bytes_per_step": st.host_layer_bytes * w.L,
-                       "prefetch": "copy-engine DMA per layer on a copy stream, two layers ahead"}},
+                       "read": ("staged: copy-engine DMA per layer on a copy stream, two layers ahead"
+                                if st.host_staged else "direct: the decode kernel reads host records in place"),
+                       **st.time_host_tier()}},
         "steps_per_s": round(1e3 / ms_per_step, 2),
         "hbm_frac_of_measured": round(value / world / peaks["hbm_gbs"], 4),
         "hbm_frac_of_datasheet_8tbs": round(value / world / 8000.0, 4),
@@ -589,6 +632,8 @@ def main(argv=None):
                     help="score update inside each layer's merge launch (one stream) instead of on a second stream")
     ap.add_argument("--host-tier", type=float, default=0.0,
                     help="fraction of each request's blocks the tier plan moves to the host tier (T1)")
+    ap.add_argument("--host-tier-staged", action="store_true",
+                    help="stage each layer's host-tier records in HBM (DMA) instead of reading them in place")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -27,7 +27,8 @@
  *    wait that ran out) records the first error code in the pool's error word;
  *    the affected work item is treated as empty.  Read it with
  *    kvd_get_device_error.
- *  - Supported set: d_h = 128, block_size = 16, 1 ≤ g ≤ 8, batch ≤ 2048.
+ *  - Supported set: d_h = 128, block_size = 16, 1 ≤ g ≤ 8, batch ≤ 2048, at most 64 GiB
+ *    of pool (and of host tier) per layer.
  *    Anything else valid returns KVD_ERR_UNSUPPORTED before any launch.
  *
  * Pool layout (per layer ℓ, physical block p, KV head h)
@@ -133,10 +134,15 @@ KVD_API void kvd_pool_destroy(kvd_pool* pool);
  * A pool with a host tier has host_blocks more physical blocks, ids num_blocks ..
  * num_blocks + host_blocks - 1, whose records (same record layout; per layer ℓ the record of
  * host block i, head h sits at ((ℓ·host_blocks + i)·n_kv + h)·record_bytes) live in pinned
- * host memory.  kvd_tier_prefetch copies one layer's host records into one of two HBM
- * staging slots (slot layer % 2); kvd_decode_attn reads a host-tier block from that staged
- * copy, so the staged layer must be the one attended.  A retain_mask then has
- * num_blocks + host_blocks entries.  Block tables may mix both kinds of ids freely. */
+ * host memory.  Two ways to bring them to the GPU:
+ *  - direct (attached without staging memory): the decode kernel copies each host-tier
+ *    block it attends straight from host memory into shared memory, over the host link,
+ *    while it streams the HBM blocks; nothing else is needed per step.
+ *  - staged: kvd_tier_prefetch copies one layer's host records into one of two HBM staging
+ *    slots (slot layer % 2); kvd_decode_attn reads a host-tier block from that staged copy,
+ *    so the staged layer must be the one attended.
+ * A retain_mask then has num_blocks + host_blocks entries.  Block tables may mix both kinds
+ * of ids freely. */
 
 /* host_bytes = L·host_blocks·n_kv·record_bytes (pinned host memory); staging_bytes =
  * 2·host_blocks·n_kv·record_bytes (device).  host_blocks ≥ 0.  Host only. */
@@ -147,8 +153,9 @@ KVD_API kvd_status kvd_tier_bytes(const kvd_pool_desc* desc, int64_t host_blocks
  * device can address — page-locked (cudaHostAlloc or registered), or on systems where the
  * device reads pageable memory any host memory — 16-byte aligned, ≥ host_bytes; its device
  * address is looked up here (KVD_ERR_INVALID if there is none).  staging_mem: device,
- * 16-byte aligned, ≥ staging_bytes.  Both stay caller-owned; the host records are written by
- * kvd_append_kv (slots in host blocks) and by the fused append of kvd_decode_attn. */
+ * 16-byte aligned, ≥ staging_bytes; or NULL with staging_len = 0 for direct reads.  Both stay
+ * caller-owned; the host records are written by kvd_append_kv (slots in host blocks) and by
+ * the fused append of kvd_decode_attn. */
 KVD_API kvd_status kvd_pool_attach_host_tier(kvd_pool* pool, void* host_mem, size_t host_len, void* staging_mem,
                                              size_t staging_len, int64_t host_blocks);
 
@@ -157,7 +164,7 @@ KVD_API kvd_status kvd_pool_attach_host_tier(kvd_pool* pool, void* host_mem, siz
  * decode kernel running on another stream) on `stream`.  It must complete before a kvd_decode_attn of that
  * layer reads a host-tier block (same stream, or an event), and a slot is refilled two layers
  * later, so the prefetch of layer ℓ+2 must wait for the attention of layer ℓ.  A no-op
- * without a host tier. */
+ * without a host tier or with direct reads. */
 KVD_API kvd_status kvd_tier_prefetch(kvd_pool* pool, int layer, void* stream);
 
 /* Tier plan from the cumulative importance scores (same page, section "4. 시스템 구현":
@@ -215,7 +222,8 @@ KVD_API kvd_status kvd_decode_workspace_bytes(const kvd_pool* pool, int n_q, int
  *               block_table[b][(len-1)/16]·16 + (len-1)%16 — is written into the pool (FP8
  *               quantised as kvd_append_kv does) by the CTA that attends that block, before
  *               it reads it.  That block must not be shared with another request of the call.
- *               A host-tier block gets the token in its host record and in its staged copy.
+ *               A host-tier block gets the token in its host record (and, staged, in its
+ *               staged copy).
  *  block_table  int32 [batch][max_blocks_per_seq], device; entry j of request b is the
  *               physical block of its logical block j (entries past the context unread)
  *  seq_lens     int32 [batch], device; positions 0 .. seq_lens[b]-1 are attended (the

@@ -61,15 +61,16 @@ class KVPool:
         """Bytes of one (layer, block, KV head) record: K tile, V tile and (FP8) 32 fp32 scales."""
         return 8192 if self.kv_dtype == KVD_BF16 else 4096 + 128
 
-    def attach_host_tier(self, host_blocks: int):
+    def attach_host_tier(self, host_blocks: int, staged: bool = False):
         """Give the pool host_blocks host-tier blocks (ids num_blocks ..): their records in
-        pinned host memory, plus two HBM staging slots for kvd_tier_prefetch."""
+        pinned host memory, read by the decode kernel in place over the host link, or
+        (staged) copied per layer by kvd_tier_prefetch into two HBM staging slots."""
         import torch
 
         host_bytes, staging_bytes = kvd_tier_bytes(self.num_layers, self.n_kv, self.num_blocks, self.kv_dtype,
                                                    host_blocks)
         self.host_mem = torch.empty(host_bytes, dtype=torch.uint8, pin_memory=True)
-        self.staging = torch.empty(staging_bytes, dtype=torch.uint8, device=self.mem.device)
+        self.staging = torch.empty(staging_bytes, dtype=torch.uint8, device=self.mem.device) if staged else None
         kvd_pool_attach_host_tier(self.handle, self.host_mem, self.staging, host_blocks)
         self.host_blocks = host_blocks
 

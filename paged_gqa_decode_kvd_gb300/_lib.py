@@ -137,7 +137,8 @@ def kvd_tier_bytes(num_layers: int, n_kv: int, num_blocks: int, kv_dtype: int, h
 
 
 def kvd_pool_attach_host_tier(handle, host_mem, staging, host_blocks):
-    """host_mem: pinned host tensor; staging: device tensor (both caller-owned, sized by kvd_tier_bytes)."""
+    """host_mem: pinned host tensor; staging: device tensor, or None for direct reads (both
+    caller-owned, sized by kvd_tier_bytes)."""
     _check("kvd_pool_attach_host_tier", load().kvd_pool_attach_host_tier(
         handle, _ptr(host_mem), 0 if host_mem is None else host_mem.numel() * host_mem.element_size(),
         _ptr(staging), 0 if staging is None else staging.numel() * staging.element_size(), int(host_blocks)))

@@ -22,6 +22,7 @@ struct kvd_pool {
     uint8_t* staging;
     int64_t host_blocks;
     size_t host_layer_bytes;
+    int host_direct;       // no staging: the decode kernel reads host records over the host link
 };
 
 namespace {
@@ -139,6 +140,7 @@ kvd_status kvd_pool_create(const kvd_pool_desc* desc, void* mem, size_t len, kvd
     p->staging = nullptr;
     p->host_blocks = 0;
     p->host_layer_bytes = 0;
+    p->host_direct = 0;
     const size_t state_bytes = sizeof(int32_t);
     if (cudaGetDevice(&p->device) != cudaSuccess ||
         cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess ||
@@ -175,13 +177,16 @@ kvd_status kvd_pool_attach_host_tier(kvd_pool* pool, void* host_mem, size_t host
         pool->staging = nullptr;
         pool->host_blocks = 0;
         pool->host_layer_bytes = 0;
+        pool->host_direct = 0;
         return KVD_OK;
     }
     size_t need_host = 0, need_stage = 0;
     kvd_status st = kvd_tier_bytes(&pool->desc, host_blocks, &need_host, &need_stage);
     if (st != KVD_OK) return st;
-    if (!host_mem || !staging_mem || !aligned16(host_mem) || !aligned16(staging_mem)) return KVD_ERR_INVALID;
-    if (host_len < need_host || staging_len < need_stage) return KVD_ERR_NOMEM;
+    const bool direct = !staging_mem && staging_len == 0;
+    if (!host_mem || !aligned16(host_mem) || (!direct && (!staging_mem || !aligned16(staging_mem))))
+        return KVD_ERR_INVALID;
+    if (host_len < need_host || (!direct && staging_len < need_stage)) return KVD_ERR_NOMEM;
     void* dev = nullptr;
     if (cudaHostGetDevicePointer(&dev, host_mem, 0) != cudaSuccess || !dev || !aligned16(dev)) {
         cudaGetLastError();
@@ -192,12 +197,13 @@ kvd_status kvd_pool_attach_host_tier(kvd_pool* pool, void* host_mem, size_t host
     pool->staging = static_cast<uint8_t*>(staging_mem);
     pool->host_blocks = host_blocks;
     pool->host_layer_bytes = need_stage / 2;
+    pool->host_direct = direct ? 1 : 0;
     return KVD_OK;
 }
 
 kvd_status kvd_tier_prefetch(kvd_pool* pool, int layer, void* stream) {
     if (!pool || layer < 0 || layer >= pool->desc.num_layers) return KVD_ERR_INVALID;
-    if (pool->host_blocks == 0) return KVD_OK;
+    if (pool->host_blocks == 0 || pool->host_direct) return KVD_OK;
     // One DMA on a copy engine: the decode kernel holds every SM while it runs, so a copy
     // made by SMs could not overlap it.
     const uint8_t* src = pool->host_mem + static_cast<size_t>(layer) * pool->host_layer_bytes;
@@ -279,6 +285,8 @@ static kvd_status check_decode_shape(const kvd_pool* pool, int n_q, int batch, i
     if (n_q % pool->desc.n_kv != 0) return KVD_ERR_INVALID;
     const int g = n_q / pool->desc.n_kv;
     if (g > kvd::kMaxG || batch > kvd::kMaxBatch) return KVD_ERR_UNSUPPORTED;
+    // the decode kernel addresses a record by its offset in 16-byte units, 32 bits wide
+    if (pool->layer_bytes / 16 > UINT32_MAX || pool->host_layer_bytes / 16 > UINT32_MAX) return KVD_ERR_UNSUPPORTED;
     return KVD_OK;
 }
 
@@ -330,8 +338,11 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     kvd::DecodeParams p;
     p.kv = pool->mem + static_cast<size_t>(layer) * pool->layer_bytes;
     p.host_blocks = pool->host_blocks;
-    p.stage = pool->host_blocks ? pool->staging + static_cast<size_t>(layer % 2) * pool->host_layer_bytes : nullptr;
     p.host_kv = pool->host_blocks ? pool->host_kv + static_cast<size_t>(layer) * pool->host_layer_bytes : nullptr;
+    p.host_direct = pool->host_direct;
+    p.stage = !pool->host_blocks ? nullptr
+              : pool->host_direct ? p.host_kv
+                                  : pool->staging + static_cast<size_t>(layer % 2) * pool->host_layer_bytes;
     p.q = static_cast<const uint16_t*>(q);
     p.k_new = static_cast<const uint16_t*>(k_new);
     p.v_new = static_cast<const uint16_t*>(v_new);

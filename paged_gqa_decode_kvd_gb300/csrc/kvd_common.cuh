@@ -241,6 +241,21 @@ __device__ __forceinline__ void write_token(uint8_t* record, int t, const uint16
     }
 }
 
+// 16-byte asynchronous copy global → shared through the load path (any global address the
+// GPU maps, host memory included).  Both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async16_g2s(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+// Raise the mbarrier's pending count by one now and lower it once every cp.async this thread
+// issued before has landed: the current phase cannot complete before those copies.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// Order generic-proxy shared-memory writes before this thread's later bulk (async-proxy) copies.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Make this thread's generic-proxy global writes visible to its later bulk copies.
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");

@@ -102,6 +102,74 @@ __device__ __forceinline__ const uint8_t* record_of(const DecodeParams& p, int p
                              : p.stage + ((static_cast<int64_t>(ph) - p.num_blocks) * p.n_kv + h) * kRec;
 }
 
+// A ring stage filled from a host-tier record in place, by the whole producer warp: 16-byte
+// cp.async copies over the host link.  Each lane's copies hold the stage's phase open until
+// they land, and lane 0's arrive (after every lane has registered) is the one arrival the
+// phase expects.
+template <int kRec>
+__device__ __forceinline__ void lsu_fill(uint8_t* dst, const uint8_t* rec, uint64_t* full, int lane) {
+    for (int c = lane; c < kRec / 16; c += 32) cp_async16_g2s(dst + 16 * c, rec + 16 * c);
+    cp_async_mbar_arrive(full);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(full);
+}
+
+struct IssueState {
+    uint32_t k;            // copies issued so far (stage k % stages is next)
+    uint32_t lsu_filled;   // lane 0: stages whose last fill was cp.async (generic proxy)
+    int aborted;
+};
+
+// The producer's issue loop for a 32-block batch that holds host-tier blocks read in place:
+// pool blocks by one bulk copy from lane 0, host-tier blocks copied by the whole warp
+// (lsu_fill).  Out of line so that the plain loop, which every other batch runs, keeps its
+// code as it is.
+template <int kRec, int kStages>
+__device__ __noinline__ IssueState issue_batch_with_hosts(const DecodeParams& p, uint8_t* ring, int stage_bytes,
+                                                          uint64_t* full, uint64_t* empty, int* meta,
+                                                          volatile int* abort_flag, uint64_t policy, int phys,
+                                                          uint32_t vm, unsigned long long raddr, int cnt, int lane,
+                                                          IssueState st) {
+    for (int i = 0; i < cnt; ++i) {
+        const int ph = __shfl_sync(kFull, phys, i);
+        const uint32_t m = __shfl_sync(kFull, vm, i);
+        const unsigned long long ra = __shfl_sync(kFull, raddr, i);
+        const int s = st.k % kStages;
+        const uint32_t par = (st.k / kStages) & 1u;
+        const bool lsu = ph >= p.num_blocks && (m >> 16);   // warp-uniform
+        int ok = 1;
+        if (lane == 0) {
+            ok = mbar_wait(&empty[s], par ^ 1u, abort_flag, kWaitNs);
+            if (ok) {
+                meta[s] = static_cast<int>(m);
+                if (lsu) {
+                    st.lsu_filled |= 1u << s;
+                } else if (m >> 16) {
+                    if (st.lsu_filled >> s & 1u) {   // the stage's last writes were generic
+                        fence_proxy_async_shared();
+                        st.lsu_filled &= ~(1u << s);
+                    }
+                    mbar_arrive_expect_tx(&full[s], kRec);
+                    bulk_g2s(ring + s * stage_bytes, reinterpret_cast<const uint8_t*>(ra), kRec, &full[s], policy);
+                } else {
+                    mbar_arrive(&full[s]);
+                }
+            } else {
+                report(p.err, KVD_ERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+        }
+        ok = __shfl_sync(kFull, ok, 0);
+        if (!ok) {
+            st.aborted = 1;
+            break;
+        }
+        if (lsu) lsu_fill<kRec>(ring + s * stage_bytes, reinterpret_cast<const uint8_t*>(ra), &full[s], lane);
+        ++st.k;
+    }
+    return st;
+}
+
 // Unit holding flattened block index x: units are ordered (b, kvh); unit (b, kvh)
 // covers [n_kv·pref[b] + kvh·n_b, n_kv·pref[b] + (kvh+1)·n_b).
 __device__ __forceinline__ Segment find_segment(const int* pref, int B, int n_kv, int64_t x, int64_t hi) {
@@ -133,8 +201,10 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, int64_t idx, fl
     }
 }
 
-template <bool FP8, int S>
-__global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const DecodeParams p) {
+// DIRECT: the pool's host-tier blocks are read in place from host memory (lsu_fill); only
+// pools with such a tier launch this variant, so the others carry none of its code.
+template <bool FP8, int S, bool DIRECT>
+__global__ void __launch_bounds__(kThreads, FP8 && S == 8 ? 4 : 3) decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     using C = Cfg<FP8, S>;
     constexpr int kStages = C::kStages;
@@ -238,6 +308,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
         // =========================== producer warp ===========================
         const uint64_t policy = policy_evict_first();
         uint32_t k = 0;
+        uint32_t lsu_filled = 0;   // lane 0: stages whose last fill was cp.async (generic proxy)
         bool aborted = false;
         for (int64_t x = lo; x < hi && !aborted;) {
             const Segment sg = find_segment(pref, p.B, p.n_kv, x, hi);
@@ -253,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
                     const int64_t row = (static_cast<int64_t>(sg.b) * p.n_kv + sg.kvh) * kDh;
                     uint8_t* rec = const_cast<uint8_t*>(record_of<C::kRecord>(p, ph, sg.kvh));
                     write_token<FP8>(rec, pos % kBs, p.k_new + row, p.v_new + row, lane);
-                    if (ph >= p.num_blocks)   // a host-tier block: its host record too
+                    if (ph >= p.num_blocks && !p.host_direct)   // a staged host-tier block: its host record too
                         write_token<FP8>(p.host_kv + ((static_cast<int64_t>(ph) - p.num_blocks) * p.n_kv + sg.kvh) *
                                                          C::kRecord,
                                          pos % kBs, p.k_new + row, p.v_new + row, lane);
@@ -281,8 +352,18 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
                     }
                 }
                 const int cnt = min(32, sg.j1 - jb);
+                if (DIRECT && __any_sync(kFull, phys >= p.num_blocks)) {
+                    // a batch holding host-tier blocks read in place: issued out of line, so the
+                    // loop below stays the plain pool-block loop
+                    const IssueState st = issue_batch_with_hosts<C::kRecord, kStages>(
+                        p, ring, C::kStage, full, empty, meta, abort_flag, policy, phys, vm, raddr, cnt, lane,
+                        IssueState{k, lsu_filled, aborted ? 1 : 0});
+                    k = st.k;
+                    lsu_filled = st.lsu_filled;
+                    aborted = st.aborted != 0;
+                    continue;
+                }
                 for (int i = 0; i < cnt; ++i) {
-                    const int ph = __shfl_sync(kFull, phys, i);
                     const uint32_t m = __shfl_sync(kFull, vm, i);
                     const unsigned long long ra = __shfl_sync(kFull, raddr, i);
                     const int s = k % kStages;
@@ -295,6 +376,10 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 4 : 3) decode_kernel(const Dec
                             if (m >> 16) {
                                 const uint8_t* rec = reinterpret_cast<const uint8_t*>(ra);
                                 uint8_t* dst = ring + s * C::kStage;
+                                if (DIRECT && (lsu_filled >> s & 1u)) {   // the stage's last writes were generic
+                                    fence_proxy_async_shared();
+                                    lsu_filled &= ~(1u << s);
+                                }
                                 mbar_arrive_expect_tx(&full[s], C::kRecord);
                                 bulk_g2s(dst, rec, C::kRecord, &full[s], policy);
                             } else {
@@ -719,7 +804,9 @@ static bool smem_attrs(int* per_sm, int* reserved) {
 // Ring depth of a call.  BF16: 8 stages (8 KB records, 3 CTAs/SM).  FP8: 16 stages when three
 // such CTAs fit an SM (the per-request arrays are small enough), else 8 stages (4 CTAs/SM).
 // With 16 the CTA keeps twice the bytes in flight; measured on GB300 it is 1% faster for one
-// or eight long requests and equal for 32 requests of 8,192 tokens.
+// or eight long requests and equal for 32 requests of 8,192 tokens.  The 16-stage variant runs
+// three CTAs per SM anyway, so its launch bounds let it use 128 registers (the 8-stage one,
+// four per SM, gets 96); without spills it is another 1% faster on one long request.
 static int decode_stages(bool fp8, int batch, int g) {
     if (!fp8) return 8;
     int per_sm = 0, reserved = 0;
@@ -730,14 +817,14 @@ static int decode_stages(bool fp8, int batch, int g) {
 
 // Raise the kernel's dynamic shared-memory limit once per device to the largest
 // layout any batch size can need (batch ≤ kMaxBatch).
-template <bool FP8, int S>
+template <bool FP8, int S, bool DIRECT>
 static cudaError_t ensure_smem_attr() {
     static int done_for_device = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (done_for_device == dev) return cudaSuccess;
-    e = cudaFuncSetAttribute(decode_kernel<FP8, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(decode_kernel<FP8, S, DIRECT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem_layout<FP8, S>(kMaxBatch, kMaxG).total);
     if (e == cudaSuccess) done_for_device = dev;
     return e;
@@ -746,9 +833,9 @@ static cudaError_t ensure_smem_attr() {
 template <bool FP8, int S>
 static int ctas_per_sm_impl(int batch, int g) {
     const int smem = smem_layout<FP8, S>(batch, g).total;
-    if (ensure_smem_attr<FP8, S>() != cudaSuccess) return 1;
+    if (ensure_smem_attr<FP8, S, false>() != cudaSuccess) return 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<FP8, S>, kThreads, smem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<FP8, S, false>, kThreads, smem) != cudaSuccess)
         return 1;
     return n > 0 ? n : 1;
 }
@@ -776,18 +863,25 @@ int decode_carveout(bool fp8, int batch, int g) {
     return static_cast<int>(pct > 100 ? 100 : pct);
 }
 
-template <bool FP8, int S>
+template <bool FP8, int S, bool DIRECT>
 static cudaError_t launch_variant(const DecodeParams& p, int carveout, cudaStream_t stream) {
-    const cudaError_t e = ensure_smem_attr<FP8, S>();
+    const cudaError_t e = ensure_smem_attr<FP8, S, DIRECT>();
     if (e != cudaSuccess) return e;
     const size_t smem = smem_layout<FP8, S>(p.B, p.g).total;
-    return launch_dependent(decode_kernel<FP8, S>, dim3(p.nsplit), dim3(kThreads), smem, carveout, stream, p);
+    return launch_dependent(decode_kernel<FP8, S, DIRECT>, dim3(p.nsplit), dim3(kThreads), smem, carveout, stream,
+                            p);
+}
+
+template <bool DIRECT>
+static cudaError_t launch_decode_impl(const DecodeParams& p, bool fp8, int carveout, cudaStream_t stream) {
+    if (!fp8) return launch_variant<false, 8, DIRECT>(p, carveout, stream);
+    return decode_stages(true, p.B, p.g) == 16 ? launch_variant<true, 16, DIRECT>(p, carveout, stream)
+                                               : launch_variant<true, 8, DIRECT>(p, carveout, stream);
 }
 
 cudaError_t launch_decode(const DecodeParams& p, bool fp8, int carveout, cudaStream_t stream) {
-    if (!fp8) return launch_variant<false, 8>(p, carveout, stream);
-    return decode_stages(true, p.B, p.g) == 16 ? launch_variant<true, 16>(p, carveout, stream)
-                                               : launch_variant<true, 8>(p, carveout, stream);
+    return p.host_direct && p.host_blocks > 0 ? launch_decode_impl<true>(p, fp8, carveout, stream)
+                                              : launch_decode_impl<false>(p, fp8, carveout, stream);
 }
 
 // ---------------------------------------------------------------- wait self-test

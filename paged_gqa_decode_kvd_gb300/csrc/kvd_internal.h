@@ -21,7 +21,9 @@ struct AppendParams {
 
 struct DecodeParams {
     const uint8_t* kv;           // this layer's records (FP8: scales inline after the tiles)
-    const uint8_t* stage;        // staged copy of this layer's host-tier records, or null
+    const uint8_t* stage;        // where the decode reads this layer's host-tier records: their
+                                 // staged copy in HBM, or (host_direct) the host records themselves
+    int host_direct;             // 1: host-tier blocks are read from host memory by cp.async
     uint8_t* host_kv;            // this layer's host-tier records (device address), or null
     int64_t host_blocks;         // host-tier blocks: ids num_blocks .. num_blocks + host_blocks - 1
     const uint16_t* q;           // bf16 bits [B][n_q][128]

@@ -1,5 +1,6 @@
-"""Host tier (T1): blocks whose records live in pinned host memory and are staged into HBM
-before each layer's attention give outputs bit-identical to the same blocks kept in HBM
+"""Host tier (T1): blocks whose records live in pinned host memory — read by the decode kernel
+in place, or staged into HBM before each layer's attention — give outputs bit-identical to the
+same blocks kept in HBM
 (page "기술 요약: 모든 사고가 HBM 을 필요로 하는 것은 아님", section "3. 제로-근사오차
 오프로딩", Prop. 1: the output depends on the evicted set only, not on the HBM/host split)."""
 
@@ -53,8 +54,9 @@ def _run_layer(pool, w, layer, bt_d, seq_d, ret_d, k_new, v_new, dev, splits):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("staged", [False, True], ids=["direct", "staged"])
 @pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
-def test_host_tier_is_bitwise_identical_to_hbm(cuda_device, kv_dtype):
+def test_host_tier_is_bitwise_identical_to_hbm(cuda_device, kv_dtype, staged):
     dev = cuda_device
     w = _workload(kv_dtype)
     lens = w.seq_lens()
@@ -66,7 +68,7 @@ def test_host_tier_is_bitwise_identical_to_hbm(cuda_device, kv_dtype):
 
     hbm = H.make_pool(w)
     tier = H.make_pool(w)
-    tier.attach_host_tier(len(moved))
+    tier.attach_host_tier(len(moved), staged=staged)
     tier.host_mem.fill_(0xFF)   # unwritten host slots hold NaN, like the poisoned pool
     for layer in range(w.L):
         H.fill_layer(hbm, w, layer, bt, prefix, dev)
@@ -123,6 +125,8 @@ def test_host_tier_attach_checks_its_buffers(cuda_device):
     kvd.kvd_tier_prefetch(pool.handle, 0)
     torch.cuda.synchronize()
     assert kvd.kvd_get_device_error(pool.handle) == 0
+    kvd.kvd_pool_attach_host_tier(pool.handle, pinned, None, 4)   # direct reads: no staging, prefetch a no-op
+    kvd.kvd_tier_prefetch(pool.handle, 0)
     kvd.kvd_pool_attach_host_tier(pool.handle, None, None, 0)   # detach
 
 
@@ -218,8 +222,9 @@ def test_tier_move_copies_whole_records(cuda_device, dtype_code):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("staged", [False, True], ids=["direct", "staged"])
 @pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
-def test_plan_move_decode_is_bitwise_identical_to_hbm(cuda_device, kv_dtype):
+def test_plan_move_decode_is_bitwise_identical_to_hbm(cuda_device, kv_dtype, staged):
     """A re-tiering round as a caller runs it: plan from the scores, move the planned blocks to
     host-tier ids, patch the block tables, poison the vacated HBM blocks; the next decode step
     is bit-identical to the all-HBM pool."""
@@ -251,7 +256,7 @@ def test_plan_move_decode_is_bitwise_identical_to_hbm(cuda_device, kv_dtype):
                 bt2[b, j] = moved[-1][1]
     assert len(moved) > 10 and all(plan[b, (lens[b] - 1) // 16] == 0 for b in range(w.batch))
 
-    tier.attach_host_tier(len(moved))
+    tier.attach_host_tier(len(moved), staged=staged)
     tier.host_mem.fill_(0xFF)
     frm = torch.tensor([a for a, _ in moved], dtype=torch.int32, device=dev)
     to = torch.tensor([h for _, h in moved], dtype=torch.int32, device=dev)
