@@ -184,7 +184,8 @@ KVD_API kvd_status kvd_tier_prefetch(kvd_pool* pool, int layer, void* stream);
  *  tier        int8 [batch][max_blocks_per_seq] out, device
  * Moving the blocks (kvd_tier_move) and patching the block tables is the caller's: only
  * blocks whose tier changed need to move.  Needs max_blocks_per_seq ≤ 16384
- * (KVD_ERR_UNSUPPORTED otherwise); work per request grows as nb².  Negative protect_*,
+ * (KVD_ERR_UNSUPPORTED otherwise); one CTA per request, work O(nb).  Scores must be finite
+ * (a NaN has no place in the order).  Negative protect_*,
  * t1_blocks or batch, scores_stride < 1 or max_blocks_per_seq < 1: KVD_ERR_INVALID; batch = 0
  * is a no-op. */
 KVD_API kvd_status kvd_tier_plan(const float* scores, int64_t scores_stride, const int32_t* seq_lens, int batch,
