@@ -199,6 +199,33 @@ KVD_API kvd_status kvd_tier_plan(const float* scores, int64_t scores_stride, con
 KVD_API kvd_status kvd_tier_move(kvd_pool* pool, const int32_t* from_ids, const int32_t* to_ids, int n,
                                  void* stream);
 
+/* One tier reassignment, on the host (same page, section "4. 시스템 구현": only blocks whose
+ * tier changed move).  For request b and logical block j with tier[b][j] ≥ 0, the block's
+ * current id p = block_table[b][j] is a host-tier id when p ≥ num_blocks.  Where that differs
+ * from tier[b][j] = 1, the last id of the planned tier's free list becomes its destination d:
+ * block_table[b][j] = d, the pair (p, d) is appended to from_ids/to_ids, and, with a retain
+ * mask, retain_mask[d] = retain_mask[p].  A block id shared by several table entries moves
+ * once and every entry follows it (the first entry's plan decides).  Once all destinations
+ * are taken, each source id is appended to its own tier's free list.  Entries with tier < 0
+ * are left alone.  num_blocks, host_blocks: the pool's (ids num_blocks .. + host_blocks - 1
+ * are host-tier ids).
+ *  tier          int8 [batch][max_blocks_per_seq] (kvd_tier_plan's output copied to the host)
+ *  block_table   int32 [batch][max_blocks_per_seq], in/out
+ *  hbm_free      int32, capacity num_blocks, the first *hbm_free_n entries free pool ids (in/out)
+ *  host_free     int32, capacity host_blocks, the first *host_free_n entries free host-tier ids
+ *  retain_mask   uint16 [num_blocks + host_blocks] or NULL (in/out)
+ *  from_ids, to_ids  int32 [batch·max_blocks_per_seq] out; *n_moves out
+ * All host memory.  Afterwards the caller copies block_table (and retain_mask) to the device
+ * and runs kvd_tier_move(from_ids, to_ids) on the stream before the next decode.  A block whose
+ * planned tier has no free id stays where it is (KVD_ERR_NOMEM once the rest is done); a table
+ * id outside the pool and its host tier is skipped (KVD_ERR_OOB likewise); a free list holding
+ * an id of the other tier, or more ids than its tier has, is KVD_ERR_INVALID.  Host only, no
+ * GPU needed. */
+KVD_API kvd_status kvd_tier_reassign(int64_t num_blocks, int64_t host_blocks, const int8_t* tier,
+                                     int32_t* block_table, int batch, int max_blocks_per_seq, int32_t* hbm_free,
+                                     int32_t* hbm_free_n, int32_t* host_free, int32_t* host_free_n,
+                                     uint16_t* retain_mask, int32_t* from_ids, int32_t* to_ids, int32_t* n_moves);
+
 /* Decode-step append ("reshape and cache").  Token n's keys k_new[n][h][:] and values
  * v_new[n][h][:] (bf16, [n_tokens][n_kv][d_h], device) are written for every KV head h of
  * `layer` at slot s = slot_mapping[n] (int64, device) = physical_block·16 + offset;

@@ -30,6 +30,7 @@ from ._lib import (  # noqa: F401
     kvd_tier_prefetch,
     kvd_tier_plan,
     kvd_tier_move,
+    kvd_tier_reassign,
     kvd_combine_splits,
     kvd_decode_attn,
     kvd_decode_attn_noalloc,

@@ -20,6 +20,7 @@ SYMBOLS = [
     "kvd_decode_workspace_bytes", "kvd_decode_attn", "kvd_combine_splits", "kvd_accum_scores",
     "kvd_get_device_error", "kvd_selftest_wait_timeout", "kvd_decode_attn_noalloc",
     "kvd_tier_bytes", "kvd_pool_attach_host_tier", "kvd_tier_prefetch", "kvd_tier_plan", "kvd_tier_move",
+    "kvd_tier_reassign",
 ]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -77,6 +78,8 @@ def load(build_if_missing: bool = True):
     lib.kvd_tier_plan.argtypes = [P, i64, P, i32, i32, i32, i32, i32, P, P, P]
     lib.kvd_tier_move.restype = i32
     lib.kvd_tier_move.argtypes = [P, P, P, i32, P]
+    lib.kvd_tier_reassign.restype = i32
+    lib.kvd_tier_reassign.argtypes = [i64, i64, P, P, i32, i32, P, P, P, P, P, P, P, P]
     lib.kvd_append_kv.restype = i32
     lib.kvd_append_kv.argtypes = [P, i32, P, P, P, i32, P]
     lib.kvd_decode_workspace_bytes.restype = i32
@@ -165,6 +168,36 @@ def kvd_tier_move(handle, from_ids, to_ids, stream=None):
     if int(to_ids.numel()) != n:
         raise ValueError("from_ids and to_ids differ in length")
     _check("kvd_tier_move", load().kvd_tier_move(handle, _ptr(from_ids), _ptr(to_ids), n, _stream(stream)))
+
+
+def kvd_tier_reassign(num_blocks, host_blocks, tier, block_table, hbm_free, hbm_free_n, host_free, host_free_n,
+                      retain_mask=None):
+    """Host-side reassignment (numpy arrays, updated in place: block_table, hbm_free, host_free,
+    retain_mask).  Returns (status, from_ids, to_ids, hbm_free_n, host_free_n); raises only for
+    KVD_ERR_INVALID."""
+    import numpy as np
+
+    tier = np.ascontiguousarray(tier, dtype=np.int8)
+    for a, dt in ((block_table, np.int32), (hbm_free, np.int32), (host_free, np.int32)):
+        if a.dtype != dt or not a.flags.c_contiguous:
+            raise TypeError("block_table, hbm_free and host_free must be contiguous int32 arrays")
+    if retain_mask is not None and (retain_mask.dtype != np.uint16 or not retain_mask.flags.c_contiguous):
+        raise TypeError("retain_mask must be a contiguous uint16 array")
+    if tier.shape != block_table.shape or tier.ndim != 2:
+        raise ValueError("tier and block_table must both be [batch][max_blocks_per_seq]")
+    if hbm_free.size < num_blocks or host_free.size < host_blocks:
+        raise ValueError("free lists need capacity num_blocks and host_blocks")
+    batch, mb = block_table.shape
+    frm = np.empty(max(1, batch * mb), np.int32)
+    to = np.empty(max(1, batch * mb), np.int32)
+    hn, tn, n = ctypes.c_int32(int(hbm_free_n)), ctypes.c_int32(int(host_free_n)), ctypes.c_int32()
+    ptr = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+    st = load().kvd_tier_reassign(int(num_blocks), int(host_blocks), ptr(tier), ptr(block_table), batch, mb,
+                                  ptr(hbm_free), ctypes.byref(hn), ptr(host_free), ctypes.byref(tn),
+                                  ptr(retain_mask), ptr(frm), ptr(to), ctypes.byref(n))
+    if st == KVD_ERR_INVALID:
+        raise KvdError("kvd_tier_reassign", st, status_string(st))
+    return st, frm[:n.value].copy(), to[:n.value].copy(), hn.value, tn.value
 
 
 def kvd_pool_create(num_layers, n_kv, num_blocks, kv_dtype, mem, d_h=128, block_size=16):

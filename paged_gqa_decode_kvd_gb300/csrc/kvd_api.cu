@@ -254,6 +254,73 @@ kvd_status kvd_tier_move(kvd_pool* pool, const int32_t* from_ids, const int32_t*
     return cuda_status(kvd::launch_tier_move(p, pool->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
+kvd_status kvd_tier_reassign(int64_t num_blocks, int64_t host_blocks, const int8_t* tier, int32_t* block_table,
+                             int batch, int max_blocks_per_seq, int32_t* hbm_free, int32_t* hbm_free_n,
+                             int32_t* host_free, int32_t* host_free_n, uint16_t* retain_mask, int32_t* from_ids,
+                             int32_t* to_ids, int32_t* n_moves) {
+    if (num_blocks < 1 || host_blocks < 0 || num_blocks + host_blocks > INT32_MAX || batch < 0 ||
+        max_blocks_per_seq < 1 || !n_moves)
+        return KVD_ERR_INVALID;
+    *n_moves = 0;
+    if (batch == 0) return KVD_OK;
+    if (!tier || !block_table || !hbm_free || !hbm_free_n || !host_free || !host_free_n || !from_ids || !to_ids)
+        return KVD_ERR_INVALID;
+    const int64_t nb = num_blocks, ids = num_blocks + host_blocks;
+    if (*hbm_free_n < 0 || *hbm_free_n > nb || *host_free_n < 0 || *host_free_n > host_blocks) return KVD_ERR_INVALID;
+    // remap[p]: where block p is after this call, decided by its first table entry (-1: not seen)
+    int32_t* remap = static_cast<int32_t*>(std::malloc(sizeof(int32_t) * static_cast<size_t>(ids)));
+    if (!remap) return KVD_ERR_NOMEM;
+    for (int64_t i = 0; i < ids; ++i) remap[i] = -1;
+    kvd_status st = KVD_OK;
+    int32_t n = 0;
+    const int64_t entries = static_cast<int64_t>(batch) * max_blocks_per_seq;
+    for (int64_t e = 0; e < entries; ++e) {
+        if (tier[e] < 0) continue;
+        const int32_t p = block_table[e];
+        if (p < 0 || p >= ids) {
+            st = KVD_ERR_OOB;
+            continue;
+        }
+        if (remap[p] >= 0) {   // shared with an entry already decided
+            block_table[e] = remap[p];
+            continue;
+        }
+        remap[p] = p;
+        const bool in_host = p >= nb, want_host = tier[e] == 1;
+        if (in_host == want_host) continue;
+        int32_t* list = want_host ? host_free : hbm_free;
+        int32_t* len = want_host ? host_free_n : hbm_free_n;
+        if (*len == 0) {
+            if (st == KVD_OK) st = KVD_ERR_NOMEM;
+            continue;
+        }
+        const int32_t d = list[--*len];
+        if (d < (want_host ? nb : 0) || d >= (want_host ? ids : nb)) {   // a free list holding a wrong id
+            std::free(remap);
+            return KVD_ERR_INVALID;
+        }
+        remap[p] = d;
+        block_table[e] = d;
+        if (retain_mask) retain_mask[d] = retain_mask[p];
+        from_ids[n] = p;
+        to_ids[n] = d;
+        ++n;
+    }
+    for (int32_t i = 0; i < n; ++i) {   // the sources are free once their copies have run
+        const int32_t p = from_ids[i];
+        int32_t* list = p >= nb ? host_free : hbm_free;
+        int32_t* len = p >= nb ? host_free_n : hbm_free_n;
+        if (*len >= (p >= nb ? host_blocks : nb)) {   // more free ids than the tier has: inconsistent input
+            st = KVD_ERR_INVALID;
+            continue;
+        }
+        list[(*len)++] = p;
+    }
+    std::free(remap);
+    *n_moves = n;
+    return st;
+}
+
 void kvd_pool_destroy(kvd_pool* pool) {
     if (!pool) return;
     if (pool->err) cudaFree(pool->err);

@@ -99,7 +99,7 @@ def _compare_layers(hbm, tier, w, bt, bt2, retain, ret2, moved, dev):
         ref = H.oracle_layer(w, layer, bt, lens, retain=retain)
         H.assert_out_close(b[0].numpy(), ref["out"])
 
-    rb, nkv, nb, nh = hbm.record_bytes, w.n_kv, w.num_blocks(), len(moved)
+    rb, nkv, nb, nh = hbm.record_bytes, w.n_kv, w.num_blocks(), tier.host_blocks
     host = tier.host_mem
     for layer in range(w.L):
         for orig, hid in moved:
@@ -270,3 +270,70 @@ def test_plan_move_decode_is_bitwise_identical_to_hbm(cuda_device, kv_dtype, sta
     assert kvd.kvd_get_device_error(tier.handle) == 0
     ret2 = torch.cat([retain, retain[[p for p, _ in moved]]])
     _compare_layers(hbm, tier, w, bt, bt2, retain, ret2, moved, dev)
+
+
+def _poison(pool, w, ids):
+    """NaN bytes into every layer's records of the given block ids (pool or host tier)."""
+    torch.cuda.synchronize()   # host-tier bytes are written by the CPU: the moves must have run
+    nb, rb = w.num_blocks(), pool.record_bytes
+    for layer in range(w.L):
+        for p in ids:
+            if p < nb:
+                off = (layer * nb + p) * w.n_kv * rb
+                pool.mem[off:off + w.n_kv * rb].fill_(0xFF)
+            else:
+                off = (layer * pool.host_blocks + (p - nb)) * w.n_kv * rb
+                pool.host_mem[off:off + w.n_kv * rb].fill_(0xFF)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_reassignment_rounds_are_bitwise_identical_to_hbm(cuda_device, kv_dtype):
+    """Two reassignment rounds as a serving loop runs them every Δ steps: plan on the device,
+    kvd_tier_reassign on the host (free lists, table and retain patch), kvd_tier_move, vacated
+    blocks poisoned.  The second round's plan differs, so blocks are promoted back to HBM and
+    others demoted; after each round the decode is bit-identical to the all-HBM pool."""
+    dev = cuda_device
+    w = _workload(kv_dtype)
+    lens = w.seq_lens()
+    bt = w.block_table()
+    retain = w.retain_mask(bt)
+    prefix = [c - 1 for c in lens]
+    mb, nb, nh = bt.shape[1], w.num_blocks(), 64
+    hbm = H.make_pool(w)
+    tier = H.make_pool(w)
+    for layer in range(w.L):
+        H.fill_layer(hbm, w, layer, bt, prefix, dev)
+        H.fill_layer(tier, w, layer, bt, prefix, dev)
+    tier.attach_host_tier(nh)
+    tier.host_mem.fill_(0xFF)
+
+    bt_host = bt.numpy().astype(np.int32).copy()
+    used = set(int(x) for x in bt_host.ravel() if x >= 0)
+    hbm_free = np.zeros(nb, np.int32)
+    free = [i for i in range(nb) if i not in used]
+    hbm_free[:len(free)] = free
+    hn = len(free)
+    host_free = np.arange(nb, nb + nh, dtype=np.int32)
+    tn = nh
+    ret_host = np.concatenate([retain.numpy().astype(np.uint16), np.full(nh, 0xFFFF, np.uint16)])
+    seq_d = torch.tensor(lens, dtype=torch.int32, device=dev)
+    promoted = 0
+    for seed in (17, 23):
+        rng = np.random.default_rng(seed)
+        scores = torch.from_numpy(rng.exponential(1e-3, size=(w.batch, max(lens))).astype(np.float32)).to(dev)
+        plan = torch.empty(w.batch, mb, dtype=torch.int8, device=dev)
+        kvd.kvd_tier_plan(scores, seq_d, mb, 32, 16, 6, plan)
+        st, frm, to, hn, tn = kvd.kvd_tier_reassign(nb, nh, plan.cpu().numpy(), bt_host, hbm_free, hn, host_free, tn,
+                                                     ret_host)
+        assert st == kvd.KVD_OK and len(frm) > 0
+        promoted += int(((frm >= nb) & (to < nb)).sum())
+        kvd.kvd_tier_move(tier.handle, torch.from_numpy(frm).to(dev), torch.from_numpy(to).to(dev))
+        _poison(tier, w, frm.tolist())
+        torch.cuda.synchronize()
+        assert kvd.kvd_get_device_error(tier.handle) == 0
+        moved = [(int(bt[b, j]), int(bt_host[b, j])) for b in range(w.batch) for j in range(mb)
+                 if bt_host[b, j] >= nb]
+        _compare_layers(hbm, tier, w, bt, torch.from_numpy(bt_host.copy()), retain,
+                        torch.from_numpy(ret_host.astype(np.int32)), moved, dev)
+    assert promoted > 0
