@@ -194,7 +194,7 @@ class Step:
     also writes its logits and adds its share of the importance score."""
 
     def __init__(self, w, dev, num_splits: int = 0, early: bool = True, fused_scores: bool = False,
-                 host_tier: float = 0.0, host_staged: bool = False):
+                 host_tier: float = 0.0, host_staged: bool = False, retier: bool = False):
         import numpy as np
         import torch
 
@@ -225,8 +225,11 @@ class Step:
                                       w.slot_mapping(b, 0, first[b], bt).to(dev))
         self.host_blocks = 0
         self.host_staged = host_staged
+        if retier and (host_staged or not w.scores or host_tier <= 0):
+            raise ValueError("--retier needs --host-tier, a workload with scores, and in-place T1 reads")
+        self.retier_on = retier
         if host_tier > 0:
-            bt = self._host_tier(host_tier, bt)
+            bt = self._host_tier(host_tier, bt, retier)
         # per-step inputs: the appended token of every request, q, context lengths
         self.seq, self.slots, self.k_new, self.v_new, self.q = [], [], [], [], []
         for t in range(self.nsteps):
@@ -267,12 +270,16 @@ class Step:
         if err:
             raise RuntimeError(f"device error during setup: {kvd.status_string(err)}")
 
-    def _host_tier(self, frac: float, bt):
+    def _host_tier(self, frac: float, bt, retier: bool):
         """Host tier (T1): the tier plan, on seeded synthetic scores, picks the frac·nb least
-        important unprotected blocks of every request; kvd_tier_move copies them to host-tier
-        ids and the block tables and retain mask are patched.  In the step the decode kernel
-        reads them in place over the host link, or (staged) each layer's host records are
-        copied by a copy-engine DMA on a copy stream, two layers ahead of use."""
+        important unprotected blocks of every request; kvd_tier_reassign gives them host-tier
+        ids (free lists, tables and retain mask kept on the host) and kvd_tier_move copies
+        them.  In the step the decode kernel reads them in place over the host link, or
+        (staged) each layer's host records are copied by a copy-engine DMA on a copy stream,
+        two layers ahead of use.  With retier the host tier has room for a reassignment's
+        destinations before its sources are freed, and retier() reassigns from the live
+        scores."""
+        import numpy as np
         import torch
 
         w, kvd, dev = self.w, self.kvd, self.dev
@@ -284,26 +291,111 @@ class Step:
         plan = torch.empty(w.batch, mb, dtype=torch.int8, device=dev)
         kvd.kvd_tier_plan(scores, lens, mb, w.protect_prompt, w.protect_recent, t1, plan)
         self.plan_args = (scores, lens, mb, w.protect_prompt, w.protect_recent, t1, plan.clone())
-        plan = plan.cpu()
-        nb = w.num_blocks()
-        bt2 = bt.clone()
-        src = []
-        for b, j in (plan == 1).nonzero().tolist():
-            src.append(int(bt[b, j]))
-            bt2[b, j] = nb + len(src) - 1
-        self.host_blocks = len(src)
-        if not src:
+        n_t1 = int((plan == 1).sum())
+        if n_t1 == 0:
             return bt
-        self.pool.attach_host_tier(len(src), staged=self.host_staged)
-        self.move_ids = (torch.tensor(src, dtype=torch.int32, device=dev),
-                         torch.arange(nb, nb + len(src), dtype=torch.int32, device=dev))
-        kvd.kvd_tier_move(self.pool.handle, *self.move_ids)
-        self.bt = bt2.to(dev)
+        nb = w.num_blocks()
+        nh = 2 * n_t1 if retier else n_t1
+        self.pool.attach_host_tier(nh, staged=self.host_staged)
+        self.tier_shape = (nb, nh, mb, t1)
+        self.bt_host = bt.numpy().astype(np.int32).copy()
+        used = np.zeros(nb, bool)
+        used[self.bt_host[self.bt_host >= 0]] = True
+        free = np.nonzero(~used)[0].astype(np.int32)
+        self.hbm_free = np.zeros(nb, np.int32)
+        self.hbm_free[:len(free)] = free
+        self.hbm_n = len(free)
+        self.host_free = np.arange(nb, nb + nh, dtype=np.int32)
+        self.host_n = nh
+        self.ret_host = None
         if self.retain is not None:
-            self.retain = torch.cat([self.retain, self.retain[torch.tensor(src, device=dev)]])
+            self.ret_host = np.concatenate([self.retain.cpu().numpy().view(np.uint16), np.full(nh, 0xFFFF, np.uint16)])
+        st, frm, to, self.hbm_n, self.host_n = kvd.kvd_tier_reassign(
+            nb, nh, plan.cpu().numpy(), self.bt_host, self.hbm_free, self.hbm_n, self.host_free, self.host_n,
+            self.ret_host)
+        if st != kvd.KVD_OK:
+            raise RuntimeError(f"initial tier assignment: {kvd.status_string(st)}")
+        self.move_ids = (torch.from_numpy(frm).to(dev), torch.from_numpy(to).to(dev))
+        kvd.kvd_tier_move(self.pool.handle, *self.move_ids)
+        self.bt = torch.from_numpy(self.bt_host.copy()).to(dev)
+        if self.ret_host is not None:
+            self.retain = torch.from_numpy(self.ret_host.view(np.int16).copy()).to(dev)
+        self.host_blocks = nh
         self.copy = torch.cuda.Stream(device=dev)
-        self.host_layer_bytes = self.host_blocks * w.n_kv * self.pool.record_bytes
-        return bt2
+        self.host_layer_bytes = nh * w.n_kv * self.pool.record_bytes
+        self.plan_dev = torch.empty(w.batch, mb, dtype=torch.int8, device=dev)
+        self.retiers, self.retier_moves = 0, 0
+        return torch.from_numpy(self.bt_host.copy())
+
+    def t1_bytes_per_step(self) -> int:
+        """K/V bytes of the blocks the step reads from the host tier (every layer)."""
+        nb = self.tier_shape[0]
+        ids = set()
+        for b, ln in enumerate(self.lens[0]):
+            ids.update(int(x) for x in self.bt_host[b, :(ln + 15) // 16] if x >= nb)
+        return len(ids) * self.w.n_kv * self.pool.record_bytes * self.L
+
+    def retier_begin(self, t: int):
+        """Start a reassignment (every Δ = 64 steps): the plan from the live importance scores
+        and its copy to pinned host memory are queued behind the steps so far; retier_poll
+        applies it once the copy has landed, while the GPU keeps running steps."""
+        import torch
+
+        w, kvd = self.w, self.kvd
+        nb, nh, mb, t1 = self.tier_shape
+        if not hasattr(self, "plan_pinned"):
+            import numpy as np
+
+            self.plan_pinned = torch.empty(w.batch, mb, dtype=torch.int8, pin_memory=True)
+            self.bt_pinned = torch.empty(self.bt_host.shape, dtype=torch.int32, pin_memory=True)
+            self.ret_pinned = (None if self.ret_host is None else
+                               torch.empty(self.ret_host.shape, dtype=torch.int16, pin_memory=True))
+            self.moves_pinned = torch.empty(2, self.bt_host.size, dtype=torch.int32, pin_memory=True)
+            self.moves_dev = torch.empty(2, self.bt_host.size, dtype=torch.int32, device=self.dev)
+            self.upload_done = None
+        self.retier_poll(wait=True)   # one still pending is applied first (the host waits, the GPU has steps queued)
+        kvd.kvd_tier_plan(self.scores, self.seq[t], mb, w.protect_prompt, w.protect_recent, t1, self.plan_dev)
+        self.plan_pinned.copy_(self.plan_dev, non_blocking=True)
+        self.plan_ready = torch.cuda.Event()
+        self.plan_ready.record()
+
+    def retier_poll(self, wait: bool = False) -> bool:
+        """Apply a started reassignment if its plan has reached the host (or, with wait, once
+        it has): host-side reassignment, then the table and retain uploads and the block moves,
+        queued in stream order before the next step.  Returns whether one was applied."""
+        import numpy as np
+        import torch
+
+        if getattr(self, "plan_ready", None) is None or (not wait and not self.plan_ready.query()):
+            return False
+        self.plan_ready.synchronize()
+        self.plan_ready = None
+        kvd = self.kvd
+        nb, nh, mb, t1 = self.tier_shape
+        st, frm, to, self.hbm_n, self.host_n = kvd.kvd_tier_reassign(
+            nb, nh, self.plan_pinned.numpy(), self.bt_host, self.hbm_free, self.hbm_n, self.host_free, self.host_n,
+            self.ret_host)
+        if st != kvd.KVD_OK:
+            raise RuntimeError(f"tier reassignment: {kvd.status_string(st)}")
+        if len(frm):
+            if self.upload_done is not None:
+                self.upload_done.synchronize()   # the pinned sources of the last upload are free again
+            self.bt_pinned.numpy()[...] = self.bt_host
+            self.bt.copy_(self.bt_pinned, non_blocking=True)
+            if self.ret_host is not None:
+                self.ret_pinned.numpy()[...] = self.ret_host.view(np.int16)
+                self.retain.copy_(self.ret_pinned, non_blocking=True)
+            n = len(frm)   # pageable sources would synchronise the stream: everything goes through pinned buffers
+            self.moves_pinned.numpy()[0, :n] = frm
+            self.moves_pinned.numpy()[1, :n] = to
+            for r in range(2):   # contiguous rows
+                self.moves_dev[r, :n].copy_(self.moves_pinned[r, :n], non_blocking=True)
+            kvd.kvd_tier_move(self.pool.handle, self.moves_dev[0, :n], self.moves_dev[1, :n])
+            self.upload_done = torch.cuda.Event()
+            self.upload_done.record()
+        self.retiers += 1
+        self.retier_moves += len(frm)
+        return True
 
     def time_host_tier(self, reps: int = 5) -> dict:
         """Host-tier costs measured alone on the copy stream: one step's staging copies, one
@@ -455,7 +547,7 @@ def gpu_arm(args, w, rank, world, local):
     torch.cuda.set_device(dev)
     peaks = measured_peaks()
     st = Step(w, dev, args.num_splits, early=not args.no_early_start, fused_scores=args.fused_scores,
-              host_tier=args.host_tier, host_staged=args.host_tier_staged)
+              host_tier=args.host_tier, host_staged=args.host_tier_staged, retier=args.retier)
     graphs = st.capture()
     stream = torch.cuda.current_stream(dev)
     # closed-form KV bytes of the timed steps (step t of the workload = graph t % steps)
@@ -465,12 +557,26 @@ def gpu_arm(args, w, rank, world, local):
     t1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         for i in range(args.warmup):
+            if st.retier_on:
+                st.retier_poll()
+                if i % st.nsteps == 0 and i > 0:
+                    st.retier_begin(0)
             graphs[i % st.nsteps].replay()
+        if st.retier_on:
+            st.retier_poll(wait=True)
         torch.cuda.synchronize()
+        if st.retier_on:
+            st.retiers, st.retier_moves = 0, 0
         barrier(world)
         t0.record(stream)
         for i in range(args.steps):
+            if st.retier_on:   # every Δ = 64 steps (the step cycle), applied without stopping the GPU
+                st.retier_poll()
+                if i % st.nsteps == 0 and i > 0:
+                    st.retier_begin(0)
             graphs[i % st.nsteps].replay()
+        if st.retier_on:
+            st.retier_poll(wait=True)
         t1.record(stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -544,7 +650,10 @@ def gpu_arm(args, w, rank, world, local):
                    "l2": "inputs larger than L2 (KV pool streamed every step)", "parallelism": f"replicas x{world}",
                    "host_tier": None if not st.host_blocks else {
                        "fraction": args.host_tier, "host_blocks": st.host_blocks,
-                       "host_bytes_per_step": st.host_layer_bytes * w.L,
+                       "host_bytes_per_step": st.t1_bytes_per_step(),
+                       "retier": None if not st.retier_on else {
+                           "every_steps": st.nsteps, "in_timed_region": st.retiers,
+                           "blocks_moved": st.retier_moves},
                        "read": ("staged: copy-engine DMA per layer on a copy stream, two layers ahead"
                                 if st.host_staged else "direct: the decode kernel reads host records in place"),
                        **st.time_host_tier()}},
@@ -632,6 +741,8 @@ def main(argv=None):
                     help="score update inside each layer's merge launch (one stream) instead of on a second stream")
     ap.add_argument("--host-tier", type=float, default=0.0,
                     help="fraction of each request's blocks the tier plan moves to the host tier (T1)")
+    ap.add_argument("--retier", action="store_true",
+                    help="reassign tiers from the live scores every 64 steps inside the timed loop")
     ap.add_argument("--host-tier-staged", action="store_true",
                     help="stage each layer's host-tier records in HBM (DMA) instead of reading them in place")
     ap.add_argument("--seed", type=int, default=0)
