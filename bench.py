@@ -13,6 +13,14 @@ with every input resident in HBM.  Default workload: Llama-3.1-8B shape, 32 laye
 batch 32, context 8,192, BF16 KV (34.4 GB of KV per step, far larger than L2).
 
 `--impl reference` times the fp64 CPU oracle instead, on a bounded sample.
+
+Host tier (T1): `--host-tier F` moves the fraction F of each request's least important
+unprotected blocks to pinned host memory before timing; the decode kernel reads them in
+place over the host link (`--host-tier-staged`: copied per layer into HBM by a DMA on a
+copy stream instead).  `--retier` (tiered workload) reassigns tiers from the live
+importance scores every 64 steps inside the timed loop.  The K/V bytes counted per step
+are the same as without a tier; `config.host_tier` reports the host-tier bytes per step and
+the costs of the plan and the moves.
 """
 
 from __future__ import annotations

@@ -232,7 +232,8 @@ KVD_API kvd_status kvd_tier_reassign(int64_t num_blocks, int64_t host_blocks, co
  * s < 0 skips the token.  FP8 pools store per (token, head) and separately for K and V:
  * scale = fp32(absmax/448) (1 when the row is zero), code = e4m3 round-to-nearest-even,
  * saturating, of the fp32 quotient x/scale.  n_tokens = 0 is a no-op.  A slot in a host-tier
- * block writes that block's host record.  A slot beyond the pool (and its host tier) sets
+ * block writes that block's host record (with a staged host tier, before that layer's
+ * kvd_tier_prefetch: the staged copy is not updated).  A slot beyond the pool (and its host tier) sets
  * KVD_ERR_OOB on the device and that token is skipped. */
 KVD_API kvd_status kvd_append_kv(kvd_pool* pool, int layer, const void* k_new, const void* v_new,
                          const int64_t* slot_mapping, int n_tokens, void* stream);
