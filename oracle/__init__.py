@@ -5,7 +5,8 @@ Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 library (``paged_gqa_decode_kvd_gb300``) and neither imports the other.
 
 Parity pins (all in ``tests/test_oracle.py``, run with ``-m "not gpu"``):
-e4m3 decode/encode, row quantise, the paged gather, decode attention, the
+e4m3 and e5m2 decode/encode, row quantise in both formats, the mixed-precision
+pool, the paged gather, decode attention, the
 split-free softmax statistics, the importance-score update and the block tier
 plan are each pinned
 to something other than the oracle itself; no function here is "parity
@@ -18,6 +19,12 @@ from .oracle import (  # noqa: F401
     e4m3_decode,
     e4m3_encode,
     quantize_rows,
+    quantize_rows_fmt,
+    e5m2_decode,
+    e5m2_encode,
+    FMT_BF16,
+    FMT_E4M3,
+    FMT_E5M2,
     OraclePool,
     decode,
     score_update,

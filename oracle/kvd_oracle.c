@@ -7,9 +7,12 @@
  * from the definitions on the pages:
  *
  *  - FP8 E4M3 storage (1 sign, 4 exponent, 3 mantissa bits, max 448; store
- *    x / scale, multiply the scale back on read): page "LLM에서 KV 캐시는
- *    얼마나 생길까" (froggydisk.github.io/kv-cache-per-request), section
- *    "KV 캐시를 줄이는 기법", FP8 format table and the paragraph after it.
+ *    x / scale, multiply the scale back on read) and E5M2 (1·5·2 bits, max
+ *    57,344): page "LLM에서 KV 캐시는 얼마나 생길까"
+ *    (froggydisk.github.io/kv-cache-per-request), section "KV 캐시를 줄이는
+ *    기법", FP8 format table and the paragraph after it.
+ *  - Mixed-precision pages, one precision per block with the retention mask
+ *    beside it: page "The KV Cache Is the New Memory Wall", §5.5.
  *  - Paged cache: fixed 16-token blocks and a per-request block table that
  *    maps the request's j-th block to a physical block; the kernel walks the
  *    table in order, so scattered blocks give the same result: same page and
@@ -104,6 +107,81 @@ void kvdo_quantize_rows(const float* x, int64_t rows, int d, uint8_t* codes, flo
     for (int64_t r = 0; r < rows; ++r) kvdo_quantize_row(x + r * d, d, codes + r * d, scales + r);
 }
 
+/* ------------------------------------------------------------------ e5m2 */
+
+/* Value of an E5M2 code: sign, 5-bit exponent with bias 15, 2-bit mantissa.
+ * Exponent field 0 holds subnormals m·2^-16; field 31 holds infinity (mantissa
+ * 0) and NaN, so the largest finite magnitude is 1.75·2^15 = 57,344 (the
+ * page's format table: 1·5·2 bits, 57,344). */
+double kvdo_e5m2_decode(uint8_t code) {
+    int sign = code >> 7;
+    int e = (code >> 2) & 0x1F;
+    int m = code & 0x3;
+    double v;
+    if (e == 0x1F) v = (m == 0) ? INFINITY : NAN;
+    else if (e == 0) v = ldexp((double)m, -16);
+    else v = ldexp(1.0 + m / 4.0, e - 15);
+    return sign ? -v : v;
+}
+
+/* Nearest finite E5M2 code to y: enumeration of the 124 non-negative finite
+ * codes, a tie goes to the even mantissa, magnitudes beyond 57,344 saturate. */
+uint8_t kvdo_e5m2_encode(float y) {
+    if (isnan(y)) return 0x7F;
+    int neg = signbit(y) ? 1 : 0;
+    double a = fabs((double)y);
+    int best = 0;
+    double best_d = INFINITY;
+    for (int c = 0; c <= 0x7B; ++c) {
+        double d = fabs(a - kvdo_e5m2_decode((uint8_t)c));
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    if (a > 57344.0) best = 0x7B;
+    return (uint8_t)((neg << 7) | best);
+}
+
+void kvdo_e5m2_decode_array(const uint8_t* codes, int64_t n, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = kvdo_e5m2_decode(codes[i]);
+}
+
+void kvdo_e5m2_encode_array(const float* y, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = kvdo_e5m2_encode(y[i]);
+}
+
+/* Block precision codes of a mixed pool: 0 = BF16 values, 1 = E4M3 codes,
+ * 2 = E5M2 codes, each 8-bit format with a per-(token, head) fp32 scale. */
+#define KVDO_FMT_BF16 0
+#define KVDO_FMT_E4M3 1
+#define KVDO_FMT_E5M2 2
+
+static double fmt_decode(int fmt, uint8_t code) {
+    return fmt == KVDO_FMT_E5M2 ? kvdo_e5m2_decode(code) : kvdo_e4m3_decode(code);
+}
+
+/* A row in an 8-bit format: scale = absmax / (the format's largest value) in
+ * fp32 (1 for an all-zero row), code_i = nearest code of the fp32 x_i/scale. */
+void kvdo_quantize_row_fmt(const float* x, int d, int fmt, uint8_t* codes, float* scale_out) {
+    const float top = fmt == KVDO_FMT_E5M2 ? 57344.0f : 448.0f;
+    float amax = 0.0f;
+    for (int i = 0; i < d; ++i) {
+        float a = fabsf(x[i]);
+        if (a > amax) amax = a;
+    }
+    float scale = (amax == 0.0f) ? 1.0f : amax / top;
+    for (int i = 0; i < d; ++i) {
+        float y = x[i] / scale;
+        codes[i] = fmt == KVDO_FMT_E5M2 ? kvdo_e5m2_encode(y) : kvdo_e4m3_encode(y);
+    }
+    *scale_out = scale;
+}
+
+void kvdo_quantize_rows_fmt(const float* x, int64_t rows, int d, int fmt, uint8_t* codes, float* scales) {
+    for (int64_t r = 0; r < rows; ++r) kvdo_quantize_row_fmt(x + r * d, d, fmt, codes + r * d, scales + r);
+}
+
 /* ----------------------------------------------------------- paged cache */
 
 /* Write N new tokens into the pool.  Token n goes to slot slot_mapping[n] =
@@ -132,6 +210,43 @@ int kvdo_append(int n_kv, int d_h, int block_size, int64_t num_blocks, int fp8,
             } else {
                 kvdo_quantize_row(ks, d_h, k_codes + row * d_h, k_scales + row);
                 kvdo_quantize_row(vs, d_h, v_codes + row * d_h, v_scales + row);
+            }
+        }
+    }
+    return KVDO_OK;
+}
+
+/* Append into a mixed-precision pool: block p holds its tokens in format
+ * block_fmt[p] (BF16 values, or E4M3 / E5M2 codes with a row scale).  k_val,
+ * v_val receive what attention reads (the value, or code value × scale), and
+ * for 8-bit blocks the codes and scales are kept too.  Layout as kvdo_append. */
+int kvdo_append_mixed(int n_kv, int d_h, int block_size, int64_t num_blocks, const uint8_t* block_fmt,
+                      const float* k_new, const float* v_new, const int64_t* slot_mapping, int64_t N,
+                      double* k_val, double* v_val, uint8_t* k_codes, uint8_t* v_codes, float* k_scales,
+                      float* v_scales) {
+    for (int64_t n = 0; n < N; ++n) {
+        int64_t slot = slot_mapping[n];
+        if (slot < 0) continue;
+        int64_t blk = slot / block_size;
+        int64_t off = slot % block_size;
+        if (blk >= num_blocks) return KVDO_ERR_INDEX;
+        int fmt = block_fmt[blk];
+        for (int h = 0; h < n_kv; ++h) {
+            const float* ks = k_new + (n * n_kv + h) * d_h;
+            const float* vs = v_new + (n * n_kv + h) * d_h;
+            int64_t row = (blk * n_kv + h) * block_size + off;
+            if (fmt == KVDO_FMT_BF16) {
+                for (int i = 0; i < d_h; ++i) {
+                    k_val[row * d_h + i] = ks[i];
+                    v_val[row * d_h + i] = vs[i];
+                }
+                continue;
+            }
+            kvdo_quantize_row_fmt(ks, d_h, fmt, k_codes + row * d_h, k_scales + row);
+            kvdo_quantize_row_fmt(vs, d_h, fmt, v_codes + row * d_h, v_scales + row);
+            for (int i = 0; i < d_h; ++i) {
+                k_val[row * d_h + i] = fmt_decode(fmt, k_codes[row * d_h + i]) * (double)k_scales[row];
+                v_val[row * d_h + i] = fmt_decode(fmt, v_codes[row * d_h + i]) * (double)v_scales[row];
             }
         }
     }

@@ -64,6 +64,15 @@ def _load():
                                         P, P, P, P, i64]
             lib.kvdo_score_update.argtypes = [P, i32, i32, i32, P, i64, P]
             lib.kvdo_tier_plan.argtypes = [P, i64, P, i32, i32, i32, i32, i32, i32, P, P]
+            lib.kvdo_e5m2_decode.restype = f64
+            lib.kvdo_e5m2_decode.argtypes = [ctypes.c_uint8]
+            lib.kvdo_e5m2_encode.restype = ctypes.c_uint8
+            lib.kvdo_e5m2_encode.argtypes = [ctypes.c_float]
+            lib.kvdo_e5m2_decode_array.argtypes = [P, i64, P]
+            lib.kvdo_e5m2_encode_array.argtypes = [P, i64, P]
+            lib.kvdo_quantize_rows_fmt.argtypes = [P, i64, i32, i32, P, P]
+            lib.kvdo_append_mixed.restype = i32
+            lib.kvdo_append_mixed.argtypes = [i32, i32, i32, i64, P, P, P, P, i64, P, P, P, P, P, P]
             _lib = lib
     return _lib
 
@@ -92,6 +101,34 @@ def e4m3_encode(y) -> np.ndarray:
     return out
 
 
+FMT_BF16, FMT_E4M3, FMT_E5M2 = 0, 1, 2   # block precision codes of a mixed pool
+
+
+def e5m2_decode(codes) -> np.ndarray:
+    c = _c(codes, np.uint8)
+    out = np.empty(c.shape, np.float64)
+    _load().kvdo_e5m2_decode_array(_p(c), c.size, _p(out))
+    return out
+
+
+def e5m2_encode(y) -> np.ndarray:
+    a = _c(y, np.float32)
+    out = np.empty(a.shape, np.uint8)
+    _load().kvdo_e5m2_encode_array(_p(a), a.size, _p(out))
+    return out
+
+
+def quantize_rows_fmt(x, fmt: int) -> tuple[np.ndarray, np.ndarray]:
+    """Per-row absmax quantise of float32 [..., d] to E4M3 (fmt 1) or E5M2 (fmt 2)."""
+    a = _c(x, np.float32)
+    d = a.shape[-1]
+    rows = a.size // d
+    codes = np.empty(a.shape, np.uint8)
+    scales = np.empty(a.shape[:-1], np.float32)
+    _load().kvdo_quantize_rows_fmt(_p(a), rows, d, int(fmt), _p(codes), _p(scales))
+    return codes, scales
+
+
 def quantize_rows(x) -> tuple[np.ndarray, np.ndarray]:
     """Per-row absmax FP8 quantise of float32 [..., d]: (codes [..., d] uint8, scales [...] float32)."""
     a = _c(x, np.float32)
@@ -104,12 +141,26 @@ def quantize_rows(x) -> tuple[np.ndarray, np.ndarray]:
 
 
 class OraclePool:
-    """The oracle's own paged pool for one layer: [num_blocks][n_kv][block_size][d_h]."""
+    """The oracle's own paged pool for one layer: [num_blocks][n_kv][block_size][d_h].
 
-    def __init__(self, num_blocks: int, n_kv: int, d_h: int, block_size: int = 16, fp8: bool = False):
+    block_fmt (uint8 [num_blocks], optional) makes it a mixed-precision pool: block p holds
+    BF16 values (0), E4M3 codes (1) or E5M2 codes (2), each 8-bit row with its own scale."""
+
+    def __init__(self, num_blocks: int, n_kv: int, d_h: int, block_size: int = 16, fp8: bool = False,
+                 block_fmt=None):
         self.num_blocks, self.n_kv, self.d_h, self.block_size, self.fp8 = num_blocks, n_kv, d_h, block_size, fp8
         shape = (num_blocks, n_kv, block_size, d_h)
-        if fp8:
+        self.block_fmt = None
+        if block_fmt is not None:
+            self.block_fmt = _c(block_fmt, np.uint8)
+            assert self.block_fmt.shape == (num_blocks,) and int(self.block_fmt.max(initial=0)) <= FMT_E5M2
+            self.k = np.zeros(shape, np.float64)
+            self.v = np.zeros(shape, np.float64)
+            self.k_codes = np.zeros(shape, np.uint8)
+            self.v_codes = np.zeros(shape, np.uint8)
+            self.k_scales = np.ones(shape[:-1], np.float32)
+            self.v_scales = np.ones(shape[:-1], np.float32)
+        elif fp8:
             self.k_codes = np.zeros(shape, np.uint8)
             self.v_codes = np.zeros(shape, np.uint8)
             self.k_scales = np.ones(shape[:-1], np.float32)
@@ -125,6 +176,11 @@ class OraclePool:
         k = _c(k_new, np.float32)
         v = _c(v_new, np.float32)
         s = _c(slot_mapping, np.int64)
+        if self.block_fmt is not None:
+            return _load().kvdo_append_mixed(self.n_kv, self.d_h, self.block_size, self.num_blocks,
+                                             _p(self.block_fmt), _p(k), _p(v), _p(s), s.size, _p(self.k), _p(self.v),
+                                             _p(self.k_codes), _p(self.v_codes), _p(self.k_scales),
+                                             _p(self.v_scales))
         return _load().kvdo_append(self.n_kv, self.d_h, self.block_size, self.num_blocks, int(self.fp8),
                                    _p(k), _p(v), _p(s), s.size,
                                    _p(self.k), _p(self.v), _p(self.k_codes), _p(self.v_codes),
@@ -132,7 +188,7 @@ class OraclePool:
 
     def values(self) -> tuple[np.ndarray, np.ndarray]:
         """fp64 K and V as read by attention (FP8: code value × row scale)."""
-        if not self.fp8:
+        if not self.fp8 or self.block_fmt is not None:
             return self.k, self.v
         rows = self.num_blocks * self.n_kv * self.block_size
         kd = np.empty(self.k_codes.shape, np.float64)

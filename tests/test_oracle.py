@@ -429,3 +429,144 @@ def test_tier_plan_matches_sorting_and_fp64_sums():
             want[order[:t1]] = 1
             assert tier[b, :nb].tolist() == want.tolist()
             assert int((tier[b] == 1).sum()) == min(t1, len(free))
+
+
+# ------------------------------------------------------------------ e5m2 codec
+def test_e5m2_page_facts():
+    for line in open(os.path.join(GOLDEN, "e5m2_page_vectors.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        kind, *vals = line.split()
+        if kind == "bits":
+            s_bits, e_bits, m_bits = map(int, vals)
+            assert (s_bits, e_bits, m_bits) == (1, 5, 2)
+            # largest finite: all-ones exponent is reserved (inf/NaN), bias 2^(e-1)-1
+            top = (2 - 2.0 ** -m_bits) * 2.0 ** ((2 ** e_bits - 2) - (2 ** (e_bits - 1) - 1))
+            assert oracle.e5m2_decode(np.uint8(0x7B)) == top
+        elif kind == "max":
+            assert oracle.e5m2_decode(np.uint8(0x7B)) == float(vals[0])
+            assert int(oracle.e5m2_encode(np.float32(vals[0]))) == 0x7B
+            assert int(oracle.e5m2_encode(np.float32(1e9))) == 0x7B     # saturates
+
+
+def test_e5m2_decode_all_codes_match_torch_and_f16_high_byte():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e5m2_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e5m2).to(torch.float64).numpy()
+    # closed form: an E5M2 code is the high byte of an IEEE half with the low byte zero
+    half = (codes.astype(np.uint16) << 8).view(np.float16).astype(np.float64)
+    for other in (ref, half):
+        assert np.array_equal(np.isnan(ours), np.isnan(other))
+        ok = ~np.isnan(other)
+        assert np.array_equal(ours[ok], other[ok])
+        assert np.array_equal(np.signbit(ours[ok]), np.signbit(other[ok]))
+
+
+def _e5m2_test_values():
+    r = _rng(11)
+    mag = np.exp2(r.uniform(-18, 16, 200000)).astype(np.float32)
+    sgn = np.where(r.random(mag.size) < 0.5, -1, 1).astype(np.float32)
+    d = oracle.e5m2_decode(np.arange(124, dtype=np.uint8))
+    mids = ((d[1:] + d[:-1]) / 2).astype(np.float32)
+    return np.concatenate([mag * sgn, mids, -mids, d.astype(np.float32),
+                           np.array([0.0, -0.0, 57344, 57345, 61439, 61441, 1e9, -1e9], np.float32)])
+
+
+def test_e5m2_encode_matches_torch_cast_and_half_spacing():
+    y = _e5m2_test_values()
+    ours = oracle.e5m2_encode(y)
+    ref = torch.from_numpy(np.clip(y, -57344, 57344)).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+    fin = np.abs(y) <= 57344
+    back = oracle.e5m2_decode(ours[fin])
+    a = np.abs(y[fin].astype(np.float64))
+    spacing = np.exp2(np.floor(np.log2(np.maximum(a, 2.0 ** -14))) - 2)   # 2^-16 below 2^-14
+    assert np.all(np.abs(back - y[fin]) <= spacing / 2)
+
+
+def test_quantize_rows_in_both_formats():
+    r = _rng(12)
+    x = _bf16(r.standard_normal((300, 128)).astype(np.float32) * np.exp2(r.uniform(-8, 8, (300, 1))))
+    x[5] = 0.0
+    c4, s4 = oracle.quantize_rows_fmt(x, oracle.FMT_E4M3)
+    c_ref, s_ref = oracle.quantize_rows(x)
+    assert np.array_equal(c4, c_ref) and np.array_equal(s4.view(np.uint32), s_ref.view(np.uint32))
+    c5, s5 = oracle.quantize_rows_fmt(x, oracle.FMT_E5M2)
+    amax = np.abs(x).max(axis=1)
+    want = np.where(amax == 0, np.float32(1), (amax / np.float32(57344)).astype(np.float32))
+    assert np.array_equal(s5.view(np.uint32), want.view(np.uint32))
+    # the row's absmax element maps to the largest code, and codes are torch's cast of x/scale
+    i = np.abs(x).argmax(axis=1)
+    nz = amax > 0
+    assert np.all((c5[np.arange(300), i] & 0x7F)[nz] == 0x7B)
+    q = torch.from_numpy((x / s5[:, None]).astype(np.float32)).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    assert np.array_equal(c5, q)
+    assert np.all(c5[5] == 0) and s5[5] == 1.0
+
+
+def _mixed_pools(seed, fmt):
+    """Three single-format pools and one mixed pool fed the same tokens."""
+    r = _rng(seed)
+    nb, n_kv, d_h, bs = len(fmt), 2, 32, 16
+    n = nb * bs - 5
+    k = _bf16(r.standard_normal((n, n_kv, d_h)).astype(np.float32))
+    v = _bf16(r.standard_normal((n, n_kv, d_h)).astype(np.float32))
+    slots = r.permutation(nb * bs)[:n].astype(np.int64)
+    pools = {}
+    for f in (oracle.FMT_BF16, oracle.FMT_E4M3, oracle.FMT_E5M2):
+        p = oracle.OraclePool(nb, n_kv, d_h, bs, block_fmt=np.full(nb, f, np.uint8))
+        assert p.append(k, v, slots) == 0
+        pools[f] = p
+    mixed = oracle.OraclePool(nb, n_kv, d_h, bs, block_fmt=np.array(fmt, np.uint8))
+    assert mixed.append(k, v, slots) == 0
+    return pools, mixed, k, v, slots
+
+
+def test_mixed_pool_blocks_match_their_single_format_pools():
+    fmt = [0, 1, 2, 2, 1, 0, 1, 2]
+    pools, mixed, k, v, slots = _mixed_pools(13, fmt)
+    km, vm = mixed.values()
+    for p, f in enumerate(fmt):
+        kf, vf = pools[f].values()
+        assert np.array_equal(km[p], kf[p]) and np.array_equal(vm[p], vf[p])
+        if f:
+            assert np.array_equal(mixed.k_codes[p], pools[f].k_codes[p])
+    # an all-BF16 mixed pool is the plain BF16 pool; an all-E4M3 one the FP8 pool, bit for bit
+    plain = oracle.OraclePool(len(fmt), 2, 32, 16)
+    fp8 = oracle.OraclePool(len(fmt), 2, 32, 16, fp8=True)
+    assert plain.append(k, v, slots) == 0 and fp8.append(k, v, slots) == 0
+    assert np.array_equal(pools[0].values()[0], plain.values()[0])
+    assert np.array_equal(pools[1].values()[1], fp8.values()[1])
+    assert np.array_equal(pools[1].v_codes, fp8.v_codes)
+
+
+def test_mixed_pool_attention_matches_torch_casts_and_sdpa():
+    fmt = [2, 0, 1, 2, 0, 1, 1, 2]
+    nb, n_kv, d_h, bs, n_q = len(fmt), 2, 32, 16, 4
+    pools, mixed, k, v, slots = _mixed_pools(14, fmt)
+    # expected values from torch's float8 casts of x/scale, block by block
+    def via_torch(x, f):
+        if f == oracle.FMT_BF16:
+            return x.astype(np.float64)
+        top, dt = (448.0, torch.float8_e4m3fn) if f == oracle.FMT_E4M3 else (57344.0, torch.float8_e5m2)
+        amax = np.abs(x).max(axis=-1, keepdims=True)
+        sc = np.where(amax == 0, np.float32(1), (amax / np.float32(top)).astype(np.float32))
+        c = torch.from_numpy((x / sc).astype(np.float32)).to(dt).to(torch.float64).numpy()
+        return c * sc.astype(np.float64)
+    km, vm = mixed.values()
+    for t, s in enumerate(slots):
+        p, o = divmod(int(s), bs)
+        for h in range(n_kv):
+            assert np.array_equal(km[p, h, o], via_torch(k[t, h], fmt[p]))
+            assert np.array_equal(vm[p, h, o], via_torch(v[t, h], fmt[p]))
+    # attention over the mixed pool: one request whose table walks every block
+    r = _rng(15)
+    q = _bf16(r.standard_normal((1, n_q, d_h)).astype(np.float32))
+    table = np.array([r.permutation(nb)], np.int32)
+    ln = nb * bs
+    res = oracle.decode(mixed, q, n_q, table, np.array([ln], np.int32))
+    kl = np.stack([km[table[0, t // bs], :, t % bs] for t in range(ln)])   # [ln][n_kv][d_h]
+    vl = np.stack([vm[table[0, t // bs], :, t % bs] for t in range(ln)])
+    # the 5 slots never written hold zeros in every format and are attended like any other
+    ref = _dense_sdpa(q[0].astype(np.float64), kl, vl, 1 / np.sqrt(d_h))
+    np.testing.assert_allclose(res["out"][0], ref, rtol=1e-12, atol=1e-12)
