@@ -1,25 +1,31 @@
 """Benchmark: paged GQA decode attention steps on GB300 through the C ABI.
 
 One step = one decode step of every layer of the workload: per layer one
-kvd_decode_attn call: the decode kernel appends the new token's K/V of every request
-and runs paged decode attention with split-KV; a second launch merges the splits (and,
-for the tiered workload, adds the layer's share of the importance score).  Layers run in order, as in a model where layer
-ℓ+1's query depends on layer ℓ.  The L-layer step is captured as a CUDA graph and
-replayed.
+kvd_decode_attn call, one kernel launch: the decode kernel appends the new token's K/V of
+every request, runs paged decode attention with split-KV, and the CTA that finishes a
+unit's last piece merges its splits (--separate-merge: a second launch merges them).  The
+tiered workload adds each layer's share of the importance score (a score launch on a second
+stream, or --fused-scores: an epilogue launch on the same stream).  Layers run in order, as
+in a model where layer ℓ+1's query depends on layer ℓ.  The L-layer step is captured as a
+CUDA graph and replayed.
 
 Prints one JSON line.  `value` is the closed-form K/V bytes attended per step,
 2·L·n_kv·d_h·w_kv per token (FP8 scales excluded), divided by the step time, in GB/s,
 with every input resident in HBM.  Default workload: Llama-3.1-8B shape, 32 layers,
-batch 32, context 8,192, BF16 KV (34.4 GB of KV per step, far larger than L2).
+batch 32, context 8,192, BF16 KV (34.4 GB of KV per step, far larger than L2).  The
+default run also times the ragged, 70B FP8 and tiered workloads (key `workloads`, each
+with its own value, roofline and clocks), and measures the read-only HBM stream
+(`hbm_read_peak`) beside the copy peak of MEASURED_PEAKS.json.
 
-`--impl reference` times the fp64 CPU oracle instead, on a bounded sample.
+`--impl reference` times the fp64 CPU oracle instead: each step is a bounded sample of the
+workload, one whole (layer, request) unit per host thread.
 
 Host tier (T1): `--host-tier F` moves the fraction F of each request's least important
 unprotected blocks to pinned host memory before timing; the decode kernel reads them in
 place over the host link (`--host-tier-staged`: copied per layer into HBM by a DMA on a
 copy stream instead).  `--retier` (tiered workload) reassigns tiers from the live
 importance scores every 64 steps inside the timed loop.  The K/V bytes counted per step
-are the same as without a tier; `config.host_tier` reports the host-tier bytes per step and
+are the same as without a tier; `launch.host_tier` reports the host-tier bytes per step and
 the costs of the plan and the moves.
 """
 
@@ -202,7 +208,8 @@ class Step:
     also writes its logits and adds its share of the importance score."""
 
     def __init__(self, w, dev, num_splits: int = 0, early: bool = True, fused_scores: bool = False,
-                 host_tier: float = 0.0, host_staged: bool = False, retier: bool = False):
+                 host_tier: float = 0.0, host_staged: bool = False, retier: bool = False,
+                 separate_merge: bool = False):
         import numpy as np
         import torch
 
@@ -210,6 +217,7 @@ class Step:
 
         self.w, self.dev, self.kvd = w, dev, kvd
         self.early = early   # KVD_EARLY_START: the step's tables and pool are not written by the previous kernel
+        self.separate_merge = separate_merge   # KVD_SEPARATE_MERGE: splits merged by a second launch
         self.L = w.L
         self.fp8 = w.kv_dtype != "bf16"
         self.pool = kvd.KVPool(w.L, w.n_kv, w.num_blocks(), kvd.KVD_FP8_E4M3 if self.fp8 else kvd.KVD_BF16,
@@ -271,8 +279,12 @@ class Step:
             if self.overlap:
                 self.side = torch.cuda.Stream(device=dev)
                 self.score_done = [None] * nbuf
-        # decode kernel + merge per layer (+ the score kernel when it runs on its own stream)
-        self.launches_per_step = (3 if self.overlap else 2) * w.L
+        # per layer: the decode kernel (which merges the splits itself), + the merge launch with
+        # separate_merge, + the score update (own stream, or the epilogue launch when fused)
+        per_layer = 1 + (1 if separate_merge else 0) + (1 if w.scores else 0)
+        if w.scores and not self.overlap and separate_merge:
+            per_layer = 2   # merge and score update share the epilogue launch
+        self.launches_per_step = per_layer * w.L
         torch.cuda.synchronize()
         err = kvd.kvd_get_device_error(self.pool.handle)
         if err:
@@ -471,7 +483,8 @@ class Step:
             self.kvd.kvd_decode_attn(self.pool.handle, layer, self.q[t][layer], self.bt, self.seq[t], self.max_len,
                                      self.ws, self.out[layer], num_splits=self.splits, retain_mask=self.retain,
                                      lse_out=self.lse[i], logits_out=self.logits[i], k_new=self.k_new[t][layer],
-                                     v_new=self.v_new[t][layer], early_start=self.early, stream=cur)
+                                     v_new=self.v_new[t][layer], early_start=self.early,
+                                     separate_merge=self.separate_merge, stream=cur)
             self.side.wait_stream(cur)
             self.kvd.kvd_accum_scores(self.logits[i], self.lse[i], self.seq[t], inv, self.scores, stream=self.side)
             ev = torch.cuda.Event()
@@ -484,7 +497,7 @@ class Step:
                                  lse_out=self.lse[0] if scores else None, logits_out=self.logits[0] if scores else None,
                                  k_new=self.k_new[t][layer], v_new=self.v_new[t][layer],
                                  scores=self.scores if scores else None, inv_LH=inv,
-                                 early_start=self.early, stream=stream)
+                                 early_start=self.early, separate_merge=self.separate_merge, stream=stream)
 
     def decode_kernel_only(self, layer: int, t: int = 0, stream=None):
         """The layer's decode kernel alone (fused append, partials, no merge launch)."""
@@ -548,18 +561,63 @@ class Step:
         return graphs
 
 
-def gpu_arm(args, w, rank, world, local):
+
+
+# ------------------------------------------------------------------ shared descriptions
+def workload_config(w) -> dict:
+    """The `config` of a JSON line: the workload and its sizes, identical for both arms."""
+    return {"workload": f"{w.name}: {w.description}", "layers": w.L, "batch": w.batch, "n_q": w.n_q,
+            "n_kv": w.n_kv, "d_h": w.d_h, "kv_dtype": w.kv_dtype,
+            "context": w.seq_lens(0)[:4] if w.batch > 4 else w.seq_lens(0),
+            "kv_bytes_per_step": w.kv_bytes_per_step(), "fp8_scale_bytes_per_step": w.scale_bytes_per_step(),
+            "decode_steps_cycled": w.steps, "scores": bool(w.scores), "seed": w.seed,
+            "l2": "inputs larger than L2 (KV pool streamed every step)"}
+
+
+def read_stream_peak(dev, gib: int = 4, reps: int = 10) -> dict:
+    """Read-only HBM bandwidth: kvd_measure_read_stream over a `gib` GiB buffer, best of `reps`
+    CUDA-event-timed passes after 3 warm-up passes (the buffer is 30x the L2)."""
+    import torch
+
+    import paged_gqa_decode_kvd_gb300 as kvd
+
+    buf = torch.empty(gib << 30, dtype=torch.uint8, device=dev)
+    buf.fill_(0x5A)
+    sink = torch.empty(1 << 15, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        kvd.kvd_measure_read_stream(buf, sink, stream=s)
+    best = None
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        kvd.kvd_measure_read_stream(buf, sink, stream=s)
+        e1.record(s)
+        e1.synchronize()
+        ms = e0.elapsed_time(e1)
+        best = ms if best is None else min(best, ms)
+    nbytes = buf.numel()
+    del buf, sink
+    torch.cuda.empty_cache()
+    return {"gbs": round(nbytes / (best * 1e-3) / 1e9, 1), "bytes": nbytes, "best_ms": round(best, 4),
+            "how": f"kvd_measure_read_stream: {gib} GiB read once with 16-byte streaming loads, best of {reps}"}
+
+
+# ------------------------------------------------------------------ the GPU arm
+def gpu_workload(args, w, rank, world, local, peaks, headline: bool) -> dict:
+    """Time one workload's decode steps (CUDA graph per step, W warm-up + K timed replays,
+    events on the stream, clocks sampled), its decode kernel alone (roofline) and, for the
+    headline line, the end-to-end steps through the public API with host copies."""
     import torch
 
     dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    peaks = measured_peaks()
     st = Step(w, dev, args.num_splits, early=not args.no_early_start, fused_scores=args.fused_scores,
-              host_tier=args.host_tier, host_staged=args.host_tier_staged, retier=args.retier)
+              host_tier=args.host_tier if headline else 0.0, host_staged=args.host_tier_staged,
+              retier=args.retier and headline, separate_merge=args.separate_merge)
     graphs = st.capture()
     stream = torch.cuda.current_stream(dev)
-    # closed-form KV bytes of the timed steps (step t of the workload = graph t % steps)
-    kv_bytes = sum(st.kv_bytes(t % st.nsteps) for t in range(args.steps)) / args.steps
+    steps = args.steps
+    kv_bytes = sum(st.kv_bytes(t % st.nsteps) for t in range(steps)) / steps
 
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
@@ -577,7 +635,7 @@ def gpu_arm(args, w, rank, world, local):
             st.retiers, st.retier_moves = 0, 0
         barrier(world)
         t0.record(stream)
-        for i in range(args.steps):
+        for i in range(steps):
             if st.retier_on:   # every Δ = 64 steps (the step cycle), applied without stopping the GPU
                 st.retier_poll()
                 if i % st.nsteps == 0 and i > 0:
@@ -590,18 +648,18 @@ def gpu_arm(args, w, rank, world, local):
         barrier(world)
     ms = t0.elapsed_time(t1)
     ms_max = max_over_ranks(ms, world)
-    ms_per_step = ms_max / args.steps
+    ms_per_step = ms_max / steps
     value = kv_bytes * world / (ms_per_step * 1e-3) / 1e9
     err = st.kvd.kvd_get_device_error(st.pool.handle)
     if err:
-        raise RuntimeError(f"device error after timed steps: {st.kvd.status_string(err)}")
+        raise RuntimeError(f"device error after timed steps of {w.name}: {st.kvd.status_string(err)}")
 
     # per-launch time of the dominant kernel (the decode kernel), from a graph of its L
     # launches alone replayed on the same stream, so host enqueue time cannot inflate it
     dgraph = st.capture_decode_only()
     dgraph.replay()
     torch.cuda.synchronize()
-    reps = max(3, min(50, args.steps // 4))
+    reps = max(3, min(50, steps // 4))
     d0 = torch.cuda.Event(enable_timing=True)
     d1 = torch.cuda.Event(enable_timing=True)
     d0.record(stream)
@@ -614,122 +672,239 @@ def gpu_arm(args, w, rank, world, local):
     achieved = layer_bytes / (dec_ms * 1e-3) / 1e9
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(achieved / peaks["hbm_gbs"], 4),
-            "traffic": args.traffic if args.traffic is not None else recorded_traffic(w.name) if not args.layers else None,
+            "traffic": (args.traffic if args.traffic is not None else
+                        recorded_traffic(w.name) if not args.layers and not args.context else None),
             "kernel": "kvd::decode_kernel", "peak_source": peaks["source"] + " (copy, MEASURED_PEAKS.json hbm_gbs)",
             "bytes_per_launch": layer_bytes, "launch_ms": round(dec_ms, 5)}
+    if peaks.get("read_gbs"):
+        roof["frac_of_read_peak"] = round(achieved / peaks["read_gbs"], 4)
+    del dgraph
 
-    # end to end: per-step inputs from pinned host memory, outputs back to pinned host memory
-    h_q = st.q[0].cpu().pin_memory()
-    h_k = st.k_new[0].cpu().pin_memory()
-    h_v = st.v_new[0].cpu().pin_memory()
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8_e4m3",
+        "data": "synthetic (seeded counter-hash generator)",
+        "config": workload_config(w),
+        "launch": {"num_splits": st.splits, "merge": "separate launch" if st.separate_merge else "in the decode kernel",
+                   "early_start": st.early,
+                   "score_update": ("second stream (off the layer chain)" if st.overlap else
+                                    "fused into the call's epilogue launch" if w.scores else None),
+                   "parallelism": f"replicas x{world}"},
+        "steps_per_s": round(1e3 / ms_per_step, 2),
+        "hbm_frac_of_measured": round(value / world / peaks["hbm_gbs"], 4),
+        "hbm_frac_of_datasheet_8tbs": round(value / world / 8000.0, 4),
+        "roofline": roof,
+        "gpu_launches": st.launches_per_step * steps,
+        "clocks": clk.summary(),
+    }
+    if peaks.get("read_gbs"):
+        line["hbm_frac_of_read_peak"] = round(value / world / peaks["read_gbs"], 4)
+    if st.host_blocks:
+        line["launch"]["host_tier"] = {
+            "fraction": args.host_tier, "host_blocks": st.host_blocks,
+            "host_bytes_per_step": st.t1_bytes_per_step(),
+            "retier": None if not st.retier_on else {
+                "every_steps": st.nsteps, "in_timed_region": st.retiers, "blocks_moved": st.retier_moves},
+            "read": ("staged: copy-engine DMA per layer on a copy stream, two layers ahead"
+                     if st.host_staged else "direct: the decode kernel reads host records in place"),
+            **st.time_host_tier()}
+    if headline:
+        line["e2e"] = e2e_steps(st, args, world)
+    del graphs
+    st.pool.close()
+    return line
+
+
+def e2e_steps(st, args, world) -> dict:
+    """The same steps end to end through the public API: per step, the step's q and new K/V
+    copied from pinned host memory, one kvd_decode_attn call per layer issued from the host
+    (no graph), and the outputs copied back to pinned host memory; K steps after W warm-up."""
+    import torch
+
+    stream = torch.cuda.current_stream(st.dev)
+    h_q = [q.cpu().pin_memory() for q in st.q]
+    h_k = [k.cpu().pin_memory() for k in st.k_new]
+    h_v = [v.cpu().pin_memory() for v in st.v_new]
     h_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
-    e2e_steps = max(1, min(args.steps, 10))
+
+    def one(t):
+        i = t % st.nsteps
+        st.q[i].copy_(h_q[i], non_blocking=True)
+        st.k_new[i].copy_(h_k[i], non_blocking=True)
+        st.v_new[i].copy_(h_v[i], non_blocking=True)
+        st.run(i)
+        h_out.copy_(st.out, non_blocking=True)
+
+    for t in range(args.warmup):
+        one(t)
     torch.cuda.synchronize()
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e2e_steps):
-        st.q[0].copy_(h_q, non_blocking=True)
-        st.k_new[0].copy_(h_k, non_blocking=True)
-        st.v_new[0].copy_(h_v, non_blocking=True)
-        graphs[0].replay()
-        h_out.copy_(st.out, non_blocking=True)
+    for t in range(args.steps):
+        one(t)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
-    h2d = (h_q.numel() * h_q.element_size() + h_k.numel() * h_k.element_size() + h_v.numel() * h_v.element_size())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+    i = 0
+    h2d = (h_q[i].numel() * h_q[i].element_size() + h_k[i].numel() * h_k[i].element_size()
+           + h_v[i].numel() * h_v[i].element_size())
     d2h = h_out.numel() * h_out.element_size()
-    e2e = {"value": round(st.kv_bytes(0) * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
+    kv = sum(st.kv_bytes(t % st.nsteps) for t in range(args.steps)) / args.steps
+    return {"value": round(kv * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+            "how": "eager per-layer kvd_decode_attn calls from the host (no graph), the step's inputs "
+                   "copied from pinned host memory and its outputs back, every step"}
 
-    line = {
-        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8_e4m3",
-        "data": "synthetic (seeded counter-hash generator)",
-        "config": {"workload": f"{w.name}: {w.description}", "layers": w.L, "batch": w.batch, "n_q": w.n_q,
-                   "n_kv": w.n_kv, "d_h": w.d_h, "context": w.seq_lens(0)[:4] if w.batch > 4 else w.seq_lens(0),
-                   "kv_bytes_per_step": kv_bytes, "fp8_scale_bytes_per_step": st.scale_bytes(0),
-                   "num_splits": st.splits, "seed": w.seed,
-                   "decode_steps_cycled": st.nsteps, "scores": bool(w.scores),
-                   "score_update": ("second stream (off the layer chain)" if st.overlap else
-                                    "fused into the merge launch" if w.scores else None),
-                   "l2": "inputs larger than L2 (KV pool streamed every step)", "parallelism": f"replicas x{world}",
-                   "host_tier": None if not st.host_blocks else {
-                       "fraction": args.host_tier, "host_blocks": st.host_blocks,
-                       "host_bytes_per_step": st.t1_bytes_per_step(),
-                       "retier": None if not st.retier_on else {
-                           "every_steps": st.nsteps, "in_timed_region": st.retiers,
-                           "blocks_moved": st.retier_moves},
-                       "read": ("staged: copy-engine DMA per layer on a copy stream, two layers ahead"
-                                if st.host_staged else "direct: the decode kernel reads host records in place"),
-                       **st.time_host_tier()}},
-        "steps_per_s": round(1e3 / ms_per_step, 2),
-        "hbm_frac_of_measured": round(value / world / peaks["hbm_gbs"], 4),
-        "hbm_frac_of_datasheet_8tbs": round(value / world / 8000.0, 4),
-        "roofline": roof,
-        "e2e": e2e,
-        "gpu_launches": st.launches_per_step * args.steps,
-        "clocks": clk.summary(),
-    }
+
+EXTRA_WORKLOADS = ("ragged", "llama70b_fp8", "tiered")
+
+
+def gpu_arm(args, w, rank, world, local):
+    import gc
+
+    import torch
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks = measured_peaks()
+    if not args.no_read_peak:
+        peaks["read"] = read_stream_peak(dev)
+        peaks["read_gbs"] = peaks["read"]["gbs"]
+    line = gpu_workload(args, w, rank, world, local, peaks, headline=True)
+    if "read" in peaks:
+        line["hbm_read_peak"] = peaks["read"]
+    # the default run also measures the other full-size workloads on one GPU (the headline
+    # `value` stays the default workload's)
+    if world == 1 and args.workload == "llama8b" and not args.only:
+        others = {}
+        for name in EXTRA_WORKLOADS:
+            gc.collect()
+            torch.cuda.empty_cache()
+            from kvd_inputs import get
+
+            sub = gpu_workload(args, get(name, args.seed), rank, world, local, peaks, headline=False)
+            for k in ("metric", "unit", "n_gpus", "warmup", "higher_is_better", "scaling", "vs_baseline", "data"):
+                sub.pop(k, None)
+            others[name] = sub
+        line["workloads"] = others
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
     return line
 
 
 # ------------------------------------------------------------------ the CPU oracle arm
-def cpu_baseline(w, budget_s: float = 15.0) -> dict:
-    """Time the fp64 oracle (as it stands, one thread) on a bounded sample of the workload.
-
-    The sample is one (layer 0, request 0) unit of the workload — append of its context
-    into the oracle's pool, then decode of all its query heads — repeated until
-    `budget_s` seconds of oracle time are spent; the rate is scaled by KV bytes."""
+def _oracle_unit(w, layer: int, b: int, kf, vf, q):
+    """The oracle on one (layer, request) unit: append of its context into the oracle's own pool,
+    then decode of all its query heads (fp64)."""
     import numpy as np
 
     import oracle
 
-    oracle.build()
-    n = w.seq_lens(0)[0]
-    k, v = w.kv(0, 0, 0, n)
-    kf, vf = k.float().numpy(), v.float().numpy()
-    q = w.q(0, 0)[0:1].float().numpy()
+    n = kf.shape[0]
     nblk = -(-n // 16)
-    pos = np.arange(n)
-    slots = (pos // 16) * 16 + pos % 16
+    slots = np.arange(n, dtype=np.int64)
     table = np.arange(nblk, dtype=np.int32)[None, :]
-    t_used, units = 0.0, 0
-    while t_used < budget_s or units == 0:
+    pool = oracle.OraclePool(nblk, w.n_kv, w.d_h, 16, w.kv_dtype != "bf16")
+    pool.append(kf, vf, slots)
+    oracle.decode(pool, q, w.n_q, table, [n])
+
+
+def _unit_inputs(w, b: int):
+    n = w.seq_lens(0)[b]
+    k, v = w.kv(0, b, 0, n)
+    return k.float().numpy(), v.float().numpy(), w.q(0, 0)[b:b + 1].float().numpy()
+
+
+def host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(w, threads: int, budget_s: float) -> dict:
+    """Time the oracle (as it stands) on `threads` host threads, each running whole (layer 0,
+    request b) units of the workload (b = thread index mod batch), until `budget_s` seconds of
+    wall time have passed; returns KV bytes attended per second over the units completed."""
+    import concurrent.futures as cf
+
+    import oracle
+
+    oracle.build()
+    ins = [_unit_inputs(w, b % w.batch) for b in range(min(threads, w.batch))]
+    per_unit = [kv_bytes_per_token(1, w.n_kv, w.d_h, w.w_kv) * x[0].shape[0] for x in ins]
+
+    def worker(i):
+        units, done = 0, 0.0
         t0 = time.perf_counter()
-        pool = oracle.OraclePool(nblk, w.n_kv, w.d_h, 16, w.kv_dtype != "bf16")
-        pool.append(kf, vf, slots)
-        oracle.decode(pool, q, w.n_q, table, [n])
-        t_used += time.perf_counter() - t0
-        units += 1
-    bytes_done = kv_bytes_per_token(1, w.n_kv, w.d_h, w.w_kv) * n * units
-    gbs = bytes_done / t_used / 1e9
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{units} x one (layer, request) unit of {w.name}: {n} tokens, {w.n_q} query heads "
-                      f"(append + decode, fp64, one thread), {t_used:.1f} s, scaled by KV bytes",
-            "steps_per_s": round(gbs * 1e9 / w.kv_bytes_per_step(), 6)}
+        while True:
+            _oracle_unit(w, 0, i, *ins[i % len(ins)])
+            units += 1
+            done += per_unit[i % len(ins)]
+            if time.perf_counter() - t0 >= budget_s:
+                return units, done
+
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:   # ctypes releases the GIL in the C oracle
+        res = list(ex.map(worker, range(threads)))
+    wall = time.perf_counter() - t0
+    units = sum(r[0] for r in res)
+    nbytes = sum(r[1] for r in res)
+    return {"gbs": nbytes / wall / 1e9, "units": units, "wall_s": wall, "bytes": nbytes}
+
+
+def cpu_baseline(w, budget_s: float = 15.0) -> dict:
+    """The fp64 oracle timed on the host cores on a bounded sample of the workload: whole
+    (layer 0, request) units, first on one thread, then on every core the process may use."""
+    n = host_threads()
+    one = oracle_sample(w, 1, budget_s / 2)
+    allc = oracle_sample(w, n, budget_s / 2)
+    return {"value": round(allc["gbs"], 4), "unit": "GB/s", "cores": n, "kind": "oracle",
+            "sample": f"{allc['units']} whole (layer 0, request) units of {w.name} (append + decode of every "
+                      f"query head, fp64) on {n} host threads in {allc['wall_s']:.1f} s; KV bytes attended / wall time",
+            "steps_per_s": round(allc["gbs"] * 1e9 / w.kv_bytes_per_step(), 6),
+            "single_thread": {"value": round(one["gbs"], 4), "unit": "GB/s", "cores": 1,
+                              "sample": f"{one['units']} units on one thread in {one['wall_s']:.1f} s"}}
 
 
 def reference_arm(args, w, rank, world):
+    """The oracle as the reference arm: each step is one bounded sample of the workload, one
+    whole (layer 0, request b) unit per host thread, run in parallel; value = KV bytes the
+    sample attended / its wall time (the rate is measured, not extrapolated)."""
     if rank != 0:
         return None
-    budget = max(2.0, args.cpu_budget / max(1, args.steps + args.warmup))
+    import oracle
+
+    oracle.build()
+    n = host_threads()
+    ins = [_unit_inputs(w, b % w.batch) for b in range(min(n, w.batch))]
+    import concurrent.futures as cf
+
+    def sample():
+        t0 = time.perf_counter()
+        with cf.ThreadPoolExecutor(max_workers=n) as ex:
+            list(ex.map(lambda i: _oracle_unit(w, 0, i, *ins[i % len(ins)]), range(n)))
+        return time.perf_counter() - t0
+
     for _ in range(args.warmup):
-        cpu_baseline(w, budget_s=budget)
-    vals = [cpu_baseline(w, budget_s=budget) for _ in range(args.steps)]
-    gbs = statistics.mean(v["value"] for v in vals)
-    ms = w.kv_bytes_per_step() / (gbs * 1e9) * 1e3
+        sample()
+    walls = [sample() for _ in range(args.steps)]
+    per_sample = sum(kv_bytes_per_token(1, w.n_kv, w.d_h, w.w_kv) * ins[i % len(ins)][0].shape[0] for i in range(n))
+    total_s = sum(walls)
+    gbs = per_sample * args.steps / total_s / 1e9
     return {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded counter-hash generator)",
-            "config": {"workload": f"{w.name}: {w.description}", "layers": w.L, "batch": w.batch,
-                       "kv_bytes_per_step": w.kv_bytes_per_step(), "seed": w.seed},
-            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": vals[0]["sample"]},
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total_s / args.steps, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded counter-hash generator)", "config": workload_config(w),
+            "step": f"one bounded sample: {n} whole (layer 0, request) units of {w.name} in parallel on {n} host "
+                    f"threads ({per_sample / 1e6:.1f} MB of KV attended)",
+            "extrapolated": False,
+            "full_step_s_at_this_rate": round(w.kv_bytes_per_step() / (gbs * 1e9), 1),
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": n, "kind": "oracle",
+                             "sample": f"{args.steps} samples of {n} (layer 0, request) units, fp64"},
             "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
 
@@ -741,12 +916,17 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="llama8b")
+    ap.add_argument("--only", action="store_true",
+                    help="time the chosen workload alone (the default run also times the ragged, 70B FP8 and "
+                         "tiered workloads)")
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling captures)")
     ap.add_argument("--context", type=int, default=0, help="override every request's context (size sweeps)")
     ap.add_argument("--no-early-start", action="store_true", help="launch the decode kernel without KVD_EARLY_START")
+    ap.add_argument("--separate-merge", action="store_true",
+                    help="merge the splits in a second launch (KVD_SEPARATE_MERGE) instead of in the decode kernel")
     ap.add_argument("--fused-scores", action="store_true",
-                    help="score update inside each layer's merge launch (one stream) instead of on a second stream")
+                    help="score update inside each layer's epilogue launch (one stream) instead of on a second stream")
     ap.add_argument("--host-tier", type=float, default=0.0,
                     help="fraction of each request's blocks the tier plan moves to the host tier (T1)")
     ap.add_argument("--retier", action="store_true",
@@ -754,8 +934,9 @@ def main(argv=None):
     ap.add_argument("--host-tier-staged", action="store_true",
                     help="stage each layer's host-tier records in HBM (DMA) instead of reading them in place")
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
+    ap.add_argument("--cpu-budget", type=float, default=16.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-read-peak", action="store_true", help="skip the read-only HBM stream measurement")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes read+write per decode launch from an ncu capture of the current kernel")
     args = ap.parse_args(argv)
@@ -769,11 +950,13 @@ def main(argv=None):
     if args.layers:
         w.L = args.layers
         w.description += f" [reduced to {args.layers} layers for profiling]"
+        args.only = True
     if args.context:
         if w.steps > 1:
             ap.error("--context applies to fixed-context workloads only")
         w._ctx0 = [args.context] * w.batch
         w.description += f" [context set to {args.context} for a size sweep]"
+        args.only = True
     if world > 1:
         import torch.distributed as dist
 

@@ -17,8 +17,9 @@
  *
  * Conventions for every entry point
  *  - Device pointers are caller-owned CUDA device memory; the library never
- *    frees them.  The library itself allocates only the pool handle (host) and a
- *    4-byte device error word inside kvd_pool_create.
+ *    frees them.  The library itself allocates only the pool handle (host) and,
+ *    inside kvd_pool_create, a small device state block: the error word and one
+ *    32-bit split-merge counter per possible unit (2048·n_kv of them).
  *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
  *    stream.  Calls are asynchronous: the return status covers argument
  *    validation and kernel launch only.
@@ -98,6 +99,12 @@ typedef struct kvd_pool kvd_pool;  /* opaque */
  *   kernel is still running; reads of q, k_new, v_new and every write still wait for it to
  *   complete.  Without the flag the kernel waits before touching any global memory. */
 #define KVD_EARLY_START 1u
+/* KVD_SEPARATE_MERGE: merge the KV splits in a second launch after the decode kernel (the
+ *   standalone combine kernel) instead of inside it.  By default the CTA whose piece completes
+ *   a unit's count merges that unit's partials, so a call is one launch (two with a score
+ *   epilogue).  Results are identical up to the merge's rounding; the flag exists to compare
+ *   the two schedules. */
+#define KVD_SEPARATE_MERGE 2u
 
 /* Optional score epilogue of kvd_decode_attn: adds this layer's share of the cumulative
  * importance score, scores[b][t] += inv_LH · Σ_h α_h[t], exactly as kvd_accum_scores would
@@ -118,12 +125,12 @@ KVD_API const char* kvd_status_string(kvd_status s);
 KVD_API kvd_status kvd_pool_bytes(const kvd_pool_desc* desc, size_t* pool_bytes, size_t* kv_bytes);
 
 /* Wrap caller memory as a pool.  mem is a device buffer of len ≥ pool_bytes bytes,
- * 16-byte aligned (else KVD_ERR_NOMEM / KVD_ERR_INVALID).  Allocates the handle and a
- * 4-byte device error word on the current device (KVD_ERR_CUDA if that fails).  *out is
- * set on success. */
+ * 16-byte aligned (else KVD_ERR_NOMEM / KVD_ERR_INVALID).  Allocates the handle and the
+ * pool's device state (error word and split-merge counters, 256 + 8192·n_kv bytes, zeroed) on
+ * the current device (KVD_ERR_CUDA if that fails).  *out is set on success. */
 KVD_API kvd_status kvd_pool_create(const kvd_pool_desc* desc, void* mem, size_t len, kvd_pool** out);
 
-/* Free the handle and its error word (not the caller's pool memory).  NULL is a no-op. */
+/* Free the handle and its device state (not the caller's pool memory).  NULL is a no-op. */
 KVD_API void kvd_pool_destroy(kvd_pool* pool);
 
 /* Host tier (T1) of a pool.  Page "기술 요약: 모든 사고가 HBM 을 필요로 하는 것은 아님",
@@ -277,9 +284,15 @@ KVD_API kvd_status kvd_decode_workspace_bytes(const kvd_pool* pool, int n_q, int
  *               every attended position (−inf where evicted), input of kvd_accum_scores
  *  scores_epilogue  NULL, or the score update to fuse into the merge launch (needs out and
  *               logits_out; n_q ≤ 256)
- *  flags        0 or KVD_EARLY_START (see above); other bits are KVD_ERR_INVALID
+ *  flags        KVD_EARLY_START and / or KVD_SEPARATE_MERGE (see above); other bits are
+ *               KVD_ERR_INVALID
  * Query head h reads KV head h / g.  A head with no retained position gets out = 0 and
- * lse = −inf. */
+ * lse = −inf.
+ * With out given, the splits of a unit are merged inside the decode kernel by the CTA that
+ * finishes the unit's last piece, counted in the pool's merge counters (each call leaves them
+ * zero again).  Two calls on one pool whose kernels run at the same time on the GPU (on two
+ * streams at once) would share those counters: serialise decode calls on a pool (stream order
+ * is enough), or give concurrent streams pools of their own. */
 KVD_API kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q,
                            const void* k_new, const void* v_new,
                            const int32_t* block_table, int max_blocks_per_seq,
@@ -349,6 +362,15 @@ KVD_API kvd_status kvd_get_device_error(kvd_pool* pool, void* stream, int32_t* c
  * KVD_ERR_TIMEOUT in the pool's error word and returns.  Lets a caller check that device
  * waits give up and report instead of hanging. */
 KVD_API kvd_status kvd_selftest_wait_timeout(kvd_pool* pool, int64_t timeout_ns, void* stream);
+
+/* Measurement helper, not part of the method (the pages have no counterpart): reads every
+ * byte of the device buffer buf (bytes > 0, a multiple of 16, 16-byte aligned) once with
+ * 16-byte streaming loads, on `stream`, one CTA per resident slot of every SM, and writes one
+ * 32-bit fold per CTA into sink (device, 4-byte aligned).  It gives the read-only HBM
+ * bandwidth a decode kernel, which only reads, is compared with.  KVD_ERR_NOMEM if sink_bytes
+ * is smaller than 4 bytes per CTA (4·SMs·resident CTAs ≤ 32 KiB on any current GPU). */
+KVD_API kvd_status kvd_measure_read_stream(const void* buf, size_t bytes, void* sink, size_t sink_bytes,
+                                           void* stream);
 
 #ifdef __cplusplus
 }

@@ -11,6 +11,7 @@ from __future__ import annotations
 from ._lib import (  # noqa: F401
     KVD_BF16,
     KVD_EARLY_START,
+    KVD_SEPARATE_MERGE,
     KVD_F32,
     KVD_FP8_E4M3,
     KVD_OK,
@@ -35,6 +36,7 @@ from ._lib import (  # noqa: F401
     kvd_decode_attn,
     kvd_decode_attn_noalloc,
     kvd_decode_workspace_bytes,
+    kvd_measure_read_stream,
     kvd_get_device_error,
     kvd_pool_bytes,
     kvd_pool_create,

@@ -13,14 +13,15 @@ import os
 
 KVD_OK, KVD_ERR_INVALID, KVD_ERR_UNSUPPORTED, KVD_ERR_NOMEM, KVD_ERR_CUDA, KVD_ERR_OOB, KVD_ERR_TIMEOUT = range(7)
 KVD_BF16, KVD_FP8_E4M3, KVD_F32 = 0, 1, 2
-KVD_EARLY_START = 1   # kvd_decode_attn flag
+KVD_EARLY_START = 1   # kvd_decode_attn flags
+KVD_SEPARATE_MERGE = 2
 
 SYMBOLS = [
     "kvd_status_string", "kvd_pool_bytes", "kvd_pool_create", "kvd_pool_destroy", "kvd_append_kv",
     "kvd_decode_workspace_bytes", "kvd_decode_attn", "kvd_combine_splits", "kvd_accum_scores",
     "kvd_get_device_error", "kvd_selftest_wait_timeout", "kvd_decode_attn_noalloc",
     "kvd_tier_bytes", "kvd_pool_attach_host_tier", "kvd_tier_prefetch", "kvd_tier_plan", "kvd_tier_move",
-    "kvd_tier_reassign",
+    "kvd_tier_reassign", "kvd_measure_read_stream",
 ]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -98,6 +99,8 @@ def load(build_if_missing: bool = True):
     lib.kvd_decode_attn_noalloc.restype = i32
     lib.kvd_decode_attn_noalloc.argtypes = [P, i32, P, i32, P, P, P, i32, P, i32, i32, i32, P, f32, P, i32, P, P,
                                             i64, P, ctypes.c_uint, P]
+    lib.kvd_measure_read_stream.restype = i32
+    lib.kvd_measure_read_stream.argtypes = [P, sz, P, sz, P]
     _lib = lib
     return lib
 
@@ -233,9 +236,13 @@ def _scores_desc(scores, inv_LH):
     return ctypes.byref(ScoresDesc(scores.data_ptr(), scores.shape[-1], float(inv_LH)))
 
 
+def _flags(early_start, separate_merge):
+    return (KVD_EARLY_START if early_start else 0) | (KVD_SEPARATE_MERGE if separate_merge else 0)
+
+
 def kvd_decode_attn(handle, layer, q, block_table, seq_lens, max_seq_len, workspace, out, num_splits=0,
                     retain_mask=None, softmax_scale=None, lse_out=None, logits_out=None, k_new=None, v_new=None,
-                    scores=None, inv_LH=None, early_start=False, stream=None):
+                    scores=None, inv_LH=None, early_start=False, separate_merge=False, stream=None):
     batch, n_q, d_h = q.shape
     if softmax_scale is None:
         softmax_scale = d_h ** -0.5
@@ -246,7 +253,7 @@ def kvd_decode_attn(handle, layer, q, block_table, seq_lens, max_seq_len, worksp
         _ptr(seq_lens), batch,
         int(max_seq_len), int(num_splits), _ptr(retain_mask), float(softmax_scale), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(out), out_dtype, _ptr(lse_out), _ptr(logits_out),
-        lstride, _scores_desc(scores, inv_LH), KVD_EARLY_START if early_start else 0, _stream(stream)))
+        lstride, _scores_desc(scores, inv_LH), _flags(early_start, separate_merge), _stream(stream)))
 
 
 def kvd_combine_splits(part_o, part_lse, unit_first, unit_count, batch, n_q, n_kv, out, lse_out=None, stream=None):
@@ -275,7 +282,8 @@ def kvd_selftest_wait_timeout(handle, timeout_ns, stream=None):
 
 def kvd_decode_attn_noalloc(handle, layer, q, block_table, seq_lens, max_seq_len, out, num_splits=0,
                             retain_mask=None, softmax_scale=None, lse_out=None, logits_out=None, k_new=None,
-                            v_new=None, scores=None, inv_LH=None, early_start=False, stream=None):
+                            v_new=None, scores=None, inv_LH=None, early_start=False, separate_merge=False,
+                            stream=None):
     """kvd_decode_attn without a workspace argument: the library's fixed device scratch array is used."""
     batch, n_q, d_h = q.shape
     if softmax_scale is None:
@@ -287,4 +295,12 @@ def kvd_decode_attn_noalloc(handle, layer, q, block_table, seq_lens, max_seq_len
         _ptr(seq_lens), batch,
         int(max_seq_len), int(num_splits), _ptr(retain_mask), float(softmax_scale), _ptr(out), out_dtype,
         _ptr(lse_out), _ptr(logits_out), lstride, _scores_desc(scores, inv_LH),
-        KVD_EARLY_START if early_start else 0, _stream(stream)))
+        _flags(early_start, separate_merge), _stream(stream)))
+
+
+def kvd_measure_read_stream(buf, sink, stream=None):
+    """Read every byte of the device tensor buf once (read-only HBM stream); sink: device
+    tensor of at least 32 KiB that receives one word per CTA."""
+    _check("kvd_measure_read_stream", load().kvd_measure_read_stream(
+        _ptr(buf), buf.numel() * buf.element_size(), _ptr(sink), sink.numel() * sink.element_size(),
+        _stream(stream)))

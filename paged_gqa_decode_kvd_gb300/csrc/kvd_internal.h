@@ -39,6 +39,8 @@ struct DecodeParams {
     float* part_lse;             // [S + U][g]
     int32_t* unit_first;         // [U]
     int32_t* unit_count;         // [U]
+    uint32_t* merge_ctr;         // [U] pieces of each unit seen so far (the pool's; zero between calls)
+    int merge;                   // 1: the CTA whose piece completes a unit merges it (needs out)
     float* logits;               // [B][n_q][logits_stride] or null
     int64_t logits_stride;
     int32_t* err;
@@ -67,6 +69,7 @@ struct CombineParams {
     int g;
     int out_f32;
     int slots_hint;              // expected partials per unit (sizes the combine CTA), 0 = unknown
+    int merged;                  // 1: the decode kernel already merged every unit (epilogue: scores only)
 };
 
 struct ScoreParams {
