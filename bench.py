@@ -1,11 +1,10 @@
 """Benchmark: paged GQA decode attention steps on GB300 through the C ABI.
 
 One step = one decode step of every layer of the workload: per layer one
-kvd_decode_attn call, one kernel launch: the decode kernel appends the new token's K/V of
-every request, runs paged decode attention with split-KV, and the CTA that finishes a
-unit's last piece merges its splits (--separate-merge: a second launch merges them).  The
-tiered workload adds each layer's share of the importance score (a score launch on a second
-stream, or --fused-scores: an epilogue launch on the same stream).  Layers run in order, as
+kvd_decode_attn call: the decode kernel appends the new token's K/V of every request and
+runs paged decode attention with split-KV; a second launch merges the splits.  The tiered
+workload adds each layer's share of the importance score (a score launch on a second
+stream, or --fused-scores: inside the merge launch).  Layers run in order, as
 in a model where layer ℓ+1's query depends on layer ℓ.  The L-layer step is captured as a
 CUDA graph and replayed.
 
@@ -208,8 +207,7 @@ class Step:
     also writes its logits and adds its share of the importance score."""
 
     def __init__(self, w, dev, num_splits: int = 0, early: bool = True, fused_scores: bool = False,
-                 host_tier: float = 0.0, host_staged: bool = False, retier: bool = False,
-                 separate_merge: bool = False):
+                 host_tier: float = 0.0, host_staged: bool = False, retier: bool = False):
         import numpy as np
         import torch
 
@@ -217,7 +215,6 @@ class Step:
 
         self.w, self.dev, self.kvd = w, dev, kvd
         self.early = early   # KVD_EARLY_START: the step's tables and pool are not written by the previous kernel
-        self.separate_merge = separate_merge   # KVD_SEPARATE_MERGE: splits merged by a second launch
         self.L = w.L
         self.fp8 = w.kv_dtype != "bf16"
         self.pool = kvd.KVPool(w.L, w.n_kv, w.num_blocks(), kvd.KVD_FP8_E4M3 if self.fp8 else kvd.KVD_BF16,
@@ -279,12 +276,9 @@ class Step:
             if self.overlap:
                 self.side = torch.cuda.Stream(device=dev)
                 self.score_done = [None] * nbuf
-        # per layer: the decode kernel (which merges the splits itself), + the merge launch with
-        # separate_merge, + the score update (own stream, or the epilogue launch when fused)
-        per_layer = 1 + (1 if separate_merge else 0) + (1 if w.scores else 0)
-        if w.scores and not self.overlap and separate_merge:
-            per_layer = 2   # merge and score update share the epilogue launch
-        self.launches_per_step = per_layer * w.L
+        # per layer: the decode kernel and the merge launch (which also updates the scores when
+        # fused), + the score kernel when it runs on its own stream
+        self.launches_per_step = (3 if self.overlap else 2) * w.L
         torch.cuda.synchronize()
         err = kvd.kvd_get_device_error(self.pool.handle)
         if err:
@@ -483,8 +477,7 @@ class Step:
             self.kvd.kvd_decode_attn(self.pool.handle, layer, self.q[t][layer], self.bt, self.seq[t], self.max_len,
                                      self.ws, self.out[layer], num_splits=self.splits, retain_mask=self.retain,
                                      lse_out=self.lse[i], logits_out=self.logits[i], k_new=self.k_new[t][layer],
-                                     v_new=self.v_new[t][layer], early_start=self.early,
-                                     separate_merge=self.separate_merge, stream=cur)
+                                     v_new=self.v_new[t][layer], early_start=self.early, stream=cur)
             self.side.wait_stream(cur)
             self.kvd.kvd_accum_scores(self.logits[i], self.lse[i], self.seq[t], inv, self.scores, stream=self.side)
             ev = torch.cuda.Event()
@@ -497,7 +490,7 @@ class Step:
                                  lse_out=self.lse[0] if scores else None, logits_out=self.logits[0] if scores else None,
                                  k_new=self.k_new[t][layer], v_new=self.v_new[t][layer],
                                  scores=self.scores if scores else None, inv_LH=inv,
-                                 early_start=self.early, separate_merge=self.separate_merge, stream=stream)
+                                 early_start=self.early, stream=stream)
 
     def decode_kernel_only(self, layer: int, t: int = 0, stream=None):
         """The layer's decode kernel alone (fused append, partials, no merge launch)."""
@@ -613,7 +606,7 @@ def gpu_workload(args, w, rank, world, local, peaks, headline: bool) -> dict:
     dev = torch.device("cuda", local)
     st = Step(w, dev, args.num_splits, early=not args.no_early_start, fused_scores=args.fused_scores,
               host_tier=args.host_tier if headline else 0.0, host_staged=args.host_tier_staged,
-              retier=args.retier and headline, separate_merge=args.separate_merge)
+              retier=args.retier and headline)
     graphs = st.capture()
     stream = torch.cuda.current_stream(dev)
     steps = args.steps
@@ -686,8 +679,7 @@ def gpu_workload(args, w, rank, world, local, peaks, headline: bool) -> dict:
         "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8_e4m3",
         "data": "synthetic (seeded counter-hash generator)",
         "config": workload_config(w),
-        "launch": {"num_splits": st.splits, "merge": "separate launch" if st.separate_merge else "in the decode kernel",
-                   "early_start": st.early,
+        "launch": {"num_splits": st.splits, "early_start": st.early,
                    "score_update": ("second stream (off the layer chain)" if st.overlap else
                                     "fused into the call's epilogue launch" if w.scores else None),
                    "parallelism": f"replicas x{world}"},
@@ -923,8 +915,6 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling captures)")
     ap.add_argument("--context", type=int, default=0, help="override every request's context (size sweeps)")
     ap.add_argument("--no-early-start", action="store_true", help="launch the decode kernel without KVD_EARLY_START")
-    ap.add_argument("--separate-merge", action="store_true",
-                    help="merge the splits in a second launch (KVD_SEPARATE_MERGE) instead of in the decode kernel")
     ap.add_argument("--fused-scores", action="store_true",
                     help="score update inside each layer's epilogue launch (one stream) instead of on a second stream")
     ap.add_argument("--host-tier", type=float, default=0.0,

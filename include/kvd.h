@@ -17,9 +17,8 @@
  *
  * Conventions for every entry point
  *  - Device pointers are caller-owned CUDA device memory; the library never
- *    frees them.  The library itself allocates only the pool handle (host) and,
- *    inside kvd_pool_create, a small device state block: the error word and one
- *    32-bit split-merge counter per possible unit (2048·n_kv of them).
+ *    frees them.  The library itself allocates only the pool handle (host) and a
+ *    4-byte device error word inside kvd_pool_create.
  *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
  *    stream.  Calls are asynchronous: the return status covers argument
  *    validation and kernel launch only.
@@ -99,12 +98,6 @@ typedef struct kvd_pool kvd_pool;  /* opaque */
  *   kernel is still running; reads of q, k_new, v_new and every write still wait for it to
  *   complete.  Without the flag the kernel waits before touching any global memory. */
 #define KVD_EARLY_START 1u
-/* KVD_SEPARATE_MERGE: merge the KV splits in a second launch after the decode kernel (the
- *   standalone combine kernel) instead of inside it.  By default the CTA whose piece completes
- *   a unit's count merges that unit's partials, so a call is one launch (two with a score
- *   epilogue).  Results are identical up to the merge's rounding; the flag exists to compare
- *   the two schedules. */
-#define KVD_SEPARATE_MERGE 2u
 
 /* Optional score epilogue of kvd_decode_attn: adds this layer's share of the cumulative
  * importance score, scores[b][t] += inv_LH · Σ_h α_h[t], exactly as kvd_accum_scores would
@@ -125,12 +118,12 @@ KVD_API const char* kvd_status_string(kvd_status s);
 KVD_API kvd_status kvd_pool_bytes(const kvd_pool_desc* desc, size_t* pool_bytes, size_t* kv_bytes);
 
 /* Wrap caller memory as a pool.  mem is a device buffer of len ≥ pool_bytes bytes,
- * 16-byte aligned (else KVD_ERR_NOMEM / KVD_ERR_INVALID).  Allocates the handle and the
- * pool's device state (error word and split-merge counters, 256 + 8192·n_kv bytes, zeroed) on
- * the current device (KVD_ERR_CUDA if that fails).  *out is set on success. */
+ * 16-byte aligned (else KVD_ERR_NOMEM / KVD_ERR_INVALID).  Allocates the handle and a
+ * 4-byte device error word on the current device (KVD_ERR_CUDA if that fails).  *out is
+ * set on success. */
 KVD_API kvd_status kvd_pool_create(const kvd_pool_desc* desc, void* mem, size_t len, kvd_pool** out);
 
-/* Free the handle and its device state (not the caller's pool memory).  NULL is a no-op. */
+/* Free the handle and its error word (not the caller's pool memory).  NULL is a no-op. */
 KVD_API void kvd_pool_destroy(kvd_pool* pool);
 
 /* Host tier (T1) of a pool.  Page "기술 요약: 모든 사고가 HBM 을 필요로 하는 것은 아님",
@@ -233,7 +226,11 @@ KVD_API kvd_status kvd_tier_reassign(int64_t num_blocks, int64_t host_blocks, co
                                      int32_t* hbm_free_n, int32_t* host_free, int32_t* host_free_n,
                                      uint16_t* retain_mask, int32_t* from_ids, int32_t* to_ids, int32_t* n_moves);
 
-/* Decode-step append ("reshape and cache").  Token n's keys k_new[n][h][:] and values
+/* Decode-step append ("reshape and cache").  Page "LLM에서 KV 캐시는 얼마나 생길까", section
+ * "KV 캐시란": every decode step writes the new token's K and V into the cache before its
+ * attention; section "KV 캐시를 줄이는 기법": the cache lives in fixed 16-token blocks, and FP8
+ * E4M3 storage divides a value by a scale before rounding and multiplies it back on read.
+ * Token n's keys k_new[n][h][:] and values
  * v_new[n][h][:] (bf16, [n_tokens][n_kv][d_h], device) are written for every KV head h of
  * `layer` at slot s = slot_mapping[n] (int64, device) = physical_block·16 + offset;
  * s < 0 skips the token.  FP8 pools store per (token, head) and separately for K and V:
@@ -252,6 +249,13 @@ KVD_API kvd_status kvd_decode_workspace_bytes(const kvd_pool* pool, int n_q, int
                                       int num_splits, int* splits_out, size_t* bytes_out);
 
 /* Paged GQA decode attention for one layer (the decode kernel, then the split merge).
+ * Page "LLM에서 KV 캐시는 얼마나 생길까", section "KV 캐시란": a query head scores every cached
+ * key, q·kᵀ/√128, takes the softmax and sums the values, and several query heads share one
+ * KV head (GQA); section "KV 캐시를 줄이는 기법": the kernel follows the request's block table
+ * to blocks scattered anywhere in the pool.  Page "The KV Cache Is the New Memory Wall", §3.2:
+ * at decode this is a stream of the whole cache at about g FLOP per byte, bound by memory
+ * bandwidth.  Page "기술 요약: 모든 사고가 HBM 을 필요로 하는 것은 아님", section "3.
+ * 제로-근사오차 오프로딩": an evicted token is left out of the softmax (the retain mask).
  *  q            bf16 [batch][n_q][d_h], device
  *  k_new, v_new bf16 [batch][n_kv][d_h] or both NULL: the fused decode-step append.  The
  *               token at position seq_lens[b]-1 of request b — slot
@@ -284,15 +288,9 @@ KVD_API kvd_status kvd_decode_workspace_bytes(const kvd_pool* pool, int n_q, int
  *               every attended position (−inf where evicted), input of kvd_accum_scores
  *  scores_epilogue  NULL, or the score update to fuse into the merge launch (needs out and
  *               logits_out; n_q ≤ 256)
- *  flags        KVD_EARLY_START and / or KVD_SEPARATE_MERGE (see above); other bits are
- *               KVD_ERR_INVALID
+ *  flags        0 or KVD_EARLY_START (see above); other bits are KVD_ERR_INVALID
  * Query head h reads KV head h / g.  A head with no retained position gets out = 0 and
- * lse = −inf.
- * With out given, the splits of a unit are merged inside the decode kernel by the CTA that
- * finishes the unit's last piece, counted in the pool's merge counters (each call leaves them
- * zero again).  Two calls on one pool whose kernels run at the same time on the GPU (on two
- * streams at once) would share those counters: serialise decode calls on a pool (stream order
- * is enough), or give concurrent streams pools of their own. */
+ * lse = −inf. */
 KVD_API kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q,
                            const void* k_new, const void* v_new,
                            const int32_t* block_table, int max_blocks_per_seq,
@@ -316,9 +314,12 @@ KVD_API kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int
  * It allocates nothing (no cudaMalloc, no cudaFree, no allocating library routine).
  *  - A shape whose workspace (kvd_decode_workspace_bytes) exceeds KVD_NOALLOC_SCRATCH_BYTES
  *    is rejected with KVD_ERR_NOMEM before any launch; `out` may not be NULL.
- *  - The first call on a device, with that device current, looks up the array's device
- *    address (cudaGetSymbolAddress) once for that device; make that first call before any
- *    stream capture begins.
+ *  - The current device must be the pool's device (else KVD_ERR_INVALID).  The first call on
+ *    a device, with that device current, looks up the array's device address
+ *    (cudaGetSymbolAddress) once for that device and keeps it for the lifetime of the
+ *    device's primary context: make that first call before any stream capture begins, and
+ *    do not call this entry point again in a process that has reset the device
+ *    (cudaDeviceReset) after its first call there.
  *  - Every call on a device shares the one array, and it keeps the previous call's
  *    contents; every partial and unit-table entry is written before it is read, so nothing
  *    needs clearing.  Calls whose kernels overlap on the GPU (e.g. on two streams at once)
@@ -333,7 +334,10 @@ KVD_API kvd_status kvd_decode_attn_noalloc(kvd_pool* pool, int layer, const void
                                            const kvd_scores_desc* scores_epilogue, unsigned flags,
                                            void* stream);
 
-/* Merge split partials by log-sum-exp.  For unit u = b·n_kv + h/g and head h:
+/* Merge split partials by log-sum-exp.  The pages describe no split of a request's context
+ * across CTAs; this is the exact identity for the softmax over a union of disjoint position
+ * sets, each summarised by its normalised output o_s and its log-sum-exp lse_s.
+ * For unit u = b·n_kv + h/g and head h:
  * LSE = log Σ_s exp(lse_s), out = Σ_s exp(lse_s − LSE)·o_s over the unit_count[u] slots
  * starting at unit_first[u] of part_o f32 [slots][g][d_h] and part_lse f32 [slots][g]
  * (device).  Slots with lse = −inf are skipped; a unit with none (or count 0) yields
@@ -344,7 +348,10 @@ KVD_API kvd_status kvd_combine_splits(const float* part_o, const float* part_lse
                               int batch, int n_q, int n_kv, int d_h,
                               void* out, int out_dtype, float* lse_out, void* stream);
 
-/* Score epilogue: scores[b][t] += inv_LH · Σ_h exp(logits[b][h][t] − lse[b][h]) for
+/* Score epilogue.  Page "기술 요약: 모든 사고가 HBM 을 필요로 하는 것은 아님", section
+ * "2. 중요도 점수화": a token's importance s_i accumulates, every decode step, its attention
+ * weight averaged over the heads H and the layers L.
+ * scores[b][t] += inv_LH · Σ_h exp(logits[b][h][t] − lse[b][h]) for
  * t < seq_lens[b], i.e. this layer's share (1/(L·H))·Σ_h α_h[t] of the cumulative
  * importance score update.  logits f32 [batch][n_q][logits_stride], lse f32 [batch][n_q]
  * (both as written by kvd_decode_attn), scores f32 [batch][scores_stride]; all device.

@@ -11,7 +11,6 @@ from __future__ import annotations
 from ._lib import (  # noqa: F401
     KVD_BF16,
     KVD_EARLY_START,
-    KVD_SEPARATE_MERGE,
     KVD_F32,
     KVD_FP8_E4M3,
     KVD_OK,

@@ -13,8 +13,7 @@ import os
 
 KVD_OK, KVD_ERR_INVALID, KVD_ERR_UNSUPPORTED, KVD_ERR_NOMEM, KVD_ERR_CUDA, KVD_ERR_OOB, KVD_ERR_TIMEOUT = range(7)
 KVD_BF16, KVD_FP8_E4M3, KVD_F32 = 0, 1, 2
-KVD_EARLY_START = 1   # kvd_decode_attn flags
-KVD_SEPARATE_MERGE = 2
+KVD_EARLY_START = 1   # kvd_decode_attn flag
 
 SYMBOLS = [
     "kvd_status_string", "kvd_pool_bytes", "kvd_pool_create", "kvd_pool_destroy", "kvd_append_kv",
@@ -236,13 +235,9 @@ def _scores_desc(scores, inv_LH):
     return ctypes.byref(ScoresDesc(scores.data_ptr(), scores.shape[-1], float(inv_LH)))
 
 
-def _flags(early_start, separate_merge):
-    return (KVD_EARLY_START if early_start else 0) | (KVD_SEPARATE_MERGE if separate_merge else 0)
-
-
 def kvd_decode_attn(handle, layer, q, block_table, seq_lens, max_seq_len, workspace, out, num_splits=0,
                     retain_mask=None, softmax_scale=None, lse_out=None, logits_out=None, k_new=None, v_new=None,
-                    scores=None, inv_LH=None, early_start=False, separate_merge=False, stream=None):
+                    scores=None, inv_LH=None, early_start=False, stream=None):
     batch, n_q, d_h = q.shape
     if softmax_scale is None:
         softmax_scale = d_h ** -0.5
@@ -253,7 +248,7 @@ def kvd_decode_attn(handle, layer, q, block_table, seq_lens, max_seq_len, worksp
         _ptr(seq_lens), batch,
         int(max_seq_len), int(num_splits), _ptr(retain_mask), float(softmax_scale), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(out), out_dtype, _ptr(lse_out), _ptr(logits_out),
-        lstride, _scores_desc(scores, inv_LH), _flags(early_start, separate_merge), _stream(stream)))
+        lstride, _scores_desc(scores, inv_LH), KVD_EARLY_START if early_start else 0, _stream(stream)))
 
 
 def kvd_combine_splits(part_o, part_lse, unit_first, unit_count, batch, n_q, n_kv, out, lse_out=None, stream=None):
@@ -282,8 +277,7 @@ def kvd_selftest_wait_timeout(handle, timeout_ns, stream=None):
 
 def kvd_decode_attn_noalloc(handle, layer, q, block_table, seq_lens, max_seq_len, out, num_splits=0,
                             retain_mask=None, softmax_scale=None, lse_out=None, logits_out=None, k_new=None,
-                            v_new=None, scores=None, inv_LH=None, early_start=False, separate_merge=False,
-                            stream=None):
+                            v_new=None, scores=None, inv_LH=None, early_start=False, stream=None):
     """kvd_decode_attn without a workspace argument: the library's fixed device scratch array is used."""
     batch, n_q, d_h = q.shape
     if softmax_scale is None:
@@ -295,7 +289,7 @@ def kvd_decode_attn_noalloc(handle, layer, q, block_table, seq_lens, max_seq_len
         _ptr(seq_lens), batch,
         int(max_seq_len), int(num_splits), _ptr(retain_mask), float(softmax_scale), _ptr(out), out_dtype,
         _ptr(lse_out), _ptr(logits_out), lstride, _scores_desc(scores, inv_LH),
-        _flags(early_start, separate_merge), _stream(stream)))
+        KVD_EARLY_START if early_start else 0, _stream(stream)))
 
 
 def kvd_measure_read_stream(buf, sink, stream=None):

@@ -13,7 +13,6 @@ struct kvd_pool {
     kvd_pool_desc desc;
     uint8_t* mem;
     int32_t* err;       // device error word
-    uint32_t* merge_ctr;   // per-unit piece counters of the in-kernel split merge [kMaxBatch·n_kv]
     int device;
     int num_sms;
     size_t layer_bytes;
@@ -85,6 +84,8 @@ kvd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVD_OK : KVD_E
 
 }  // namespace
 
+int kvd::pool_device(const kvd_pool* pool) { return pool ? pool->device : -1; }
+
 extern "C" {
 
 const char* kvd_status_string(kvd_status s) {
@@ -136,15 +137,13 @@ kvd_status kvd_pool_create(const kvd_pool_desc* desc, void* mem, size_t len, kvd
     p->mem = static_cast<uint8_t*>(mem);
     p->layer_bytes = need / desc->num_layers;
     p->err = nullptr;
-    p->merge_ctr = nullptr;
     p->host_kv = nullptr;
     p->host_mem = nullptr;
     p->staging = nullptr;
     p->host_blocks = 0;
     p->host_layer_bytes = 0;
     p->host_direct = 0;
-    // device state: the error word, then (at byte 256) one merge counter per possible unit
-    const size_t state_bytes = 256 + static_cast<size_t>(kvd::kMaxBatch) * desc->n_kv * sizeof(uint32_t);
+    const size_t state_bytes = sizeof(int32_t);
     if (cudaGetDevice(&p->device) != cudaSuccess ||
         cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess ||
         cudaMalloc(&p->err, state_bytes) != cudaSuccess || cudaMemset(p->err, 0, state_bytes) != cudaSuccess) {
@@ -153,7 +152,6 @@ kvd_status kvd_pool_create(const kvd_pool_desc* desc, void* mem, size_t len, kvd
         cudaGetLastError();
         return KVD_ERR_CUDA;
     }
-    p->merge_ctr = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(p->err) + 256);
     *out = p;
     return KVD_OK;
 }
@@ -384,7 +382,7 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     if (st != KVD_OK) return st;
     if (layer < 0 || layer >= pool->desc.num_layers || num_splits < 0 || max_blocks_per_seq < 1) return KVD_ERR_INVALID;
     if (out_dtype != KVD_BF16 && out_dtype != KVD_F32) return KVD_ERR_INVALID;
-    if (flags & ~static_cast<unsigned>(KVD_EARLY_START | KVD_SEPARATE_MERGE)) return KVD_ERR_INVALID;
+    if (flags & ~static_cast<unsigned>(KVD_EARLY_START)) return KVD_ERR_INVALID;
     if (batch == 0) return KVD_OK;
     if (!q || !block_table || !seq_lens || !workspace) return KVD_ERR_INVALID;
     if ((k_new == nullptr) != (v_new == nullptr)) return KVD_ERR_INVALID;
@@ -427,8 +425,6 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     p.part_lse = reinterpret_cast<float*>(ws + w.part_lse);
     p.unit_first = reinterpret_cast<int32_t*>(ws + w.unit_first);
     p.unit_count = reinterpret_cast<int32_t*>(ws + w.unit_count);
-    p.merge_ctr = pool->merge_ctr;
-    p.merge = out != nullptr && !(flags & KVD_SEPARATE_MERGE);
     p.logits = logits_out;
     p.logits_stride = logits_stride;
     p.err = pool->err;
@@ -460,8 +456,7 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     c.g = g;
     c.out_f32 = out_dtype == KVD_F32;
     c.slots_hint = S / U + 2;
-    c.merged = p.merge;
-    if (!scores_epilogue) return p.merge ? KVD_OK : cuda_status(kvd::launch_combine(c, carveout, s));
+    if (!scores_epilogue) return cuda_status(kvd::launch_combine(c, carveout, s));
     kvd::ScoreParams sp;
     sp.logits = logits_out;
     sp.logits_stride = logits_stride;
@@ -497,7 +492,6 @@ kvd_status kvd_combine_splits(const float* part_o, const float* part_lse, const 
     c.g = n_q / n_kv;
     c.out_f32 = out_dtype == KVD_F32;
     c.slots_hint = 64;   // counts unknown on the host: assume many partials per unit
-    c.merged = 0;
     return cuda_status(kvd::launch_combine(c, -1, static_cast<cudaStream_t>(stream)));
 }
 

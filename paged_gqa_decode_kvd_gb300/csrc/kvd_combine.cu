@@ -216,8 +216,7 @@ cudaError_t launch_scores(const ScoreParams& p, cudaStream_t stream) {
 }
 
 // Split merge and score update of one layer in one launch.  CTAs [0, B·n_q) merge one
-// (request, head) each (none when the decode kernel merged every unit itself); the rest
-// each update a tile of positions of one request.  A score
+// (request, head) each; the rest each update a tile of positions of one request.  A score
 // CTA derives the final LSE of every head of its request from the split partials itself
 // (the merge CTAs of the same launch write lse_out concurrently), or reads lse_out where
 // the decode kernel already finished the unit.
@@ -228,7 +227,7 @@ __global__ void __launch_bounds__(kScoreThreads, 6) epilogue_kernel(const Combin
     pdl_wait();
     pdl_trigger();
     const int bid = blockIdx.x;
-    const int ncomb = c.merged ? 0 : c.B * c.n_q;
+    const int ncomb = c.B * c.n_q;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (bid < ncomb) {
         combine_bh(c, bid, blockDim.x >> 5, warp, lane, dyn_smem);
@@ -361,7 +360,7 @@ cudaError_t launch_combine(const CombineParams& p, int carveout, cudaStream_t st
 cudaError_t launch_epilogue(const CombineParams& c, const ScoreParams& sp, int carveout, cudaStream_t stream) {
     const int64_t extent = sp.logits_stride < sp.scores_stride ? sp.logits_stride : sp.scores_stride;
     const int tiles = static_cast<int>((extent + kScoreTile - 1) / kScoreTile);
-    const int64_t ctas = (c.merged ? 0 : static_cast<int64_t>(c.B) * c.n_q) + static_cast<int64_t>(c.B) * tiles;
+    const int64_t ctas = static_cast<int64_t>(c.B) * c.n_q + static_cast<int64_t>(c.B) * tiles;
     const int npre = sp.n_q < kPrefetchHeads ? sp.n_q : kPrefetchHeads;
     const int score_smem = (3 * kMaxHeads + kOffSlots) * 4 + kLseValues * 4 + npre * kScoreThreads * 4 + kMaxHeads;
     const int smem = red_bytes(kScoreThreads / 32) > score_smem ? red_bytes(kScoreThreads / 32) : score_smem;

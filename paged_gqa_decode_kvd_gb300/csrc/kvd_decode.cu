@@ -12,10 +12,8 @@
 //  * Work = the flattened sequence of (request, KV head, logical block); it is
 //    cut into `nsplit` equal contiguous ranges, one CTA each, so every CTA
 //    streams the same number of blocks whatever the length mix.  A CTA writes
-//    one partial (o, lse) per unit segment it touches into slot u + cta and
-//    counts it in the unit's counter; the CTA whose piece completes the count
-//    merges the unit's partials by log-sum-exp and writes the output (or, on
-//    request, a separate combine launch merges them).
+//    one partial (o, lse) per unit segment it touches into slot u + cta, and
+//    the combine kernel merges the partials of each unit by log-sum-exp.
 //  * One producer warp reads the block table (32 entries per coalesced load)
 //    and issues 1-D bulk copies (TMA engine) of each (block, KV head) record —
 //    K tile + V tile, 8 KiB BF16 or 4 KiB FP8 (+128 B of scales) — into a ring
@@ -203,63 +201,6 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, int64_t idx, fl
     }
 }
 
-// Log-sum-exp merge of one unit's n partials (slots first .. first+n-1) by the consumer warps
-// of the CTA whose piece completed the unit:
-//   LSE = M + log Σ_s exp(lse_s − M),  out = Σ_s exp(lse_s − M)·o_s / Σ_s exp(lse_s − M),
-// M = max_s lse_s.  Warp w takes heads w, w + kNcw, ...; lane l owns dims 4l..4l+3.  A piece's
-// weight is computed once, by lane s % 32, and handed to the other lanes by shuffle; the
-// pieces' o rows are independent 16-byte loads through L2 (written by other SMs).  Pieces are
-// added in slot order, so the result does not depend on which CTA merges.
-__device__ __noinline__ void merge_unit(const DecodeParams& p, int first, int n, int64_t orow0, int warp,
-                                        int lane) {
-    const int g = p.g;
-    for (int h = warp; h < g; h += kNcw) {
-        const float* lse = p.part_lse + static_cast<int64_t>(first) * g + h;   // piece s at lse[s·g]
-        float M = -INFINITY;
-        for (int s = lane; s < n; s += 32) M = fmaxf(M, __ldcg(lse + static_cast<int64_t>(s) * g));
-        #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        float Ls = 0.f;
-        if (M != -INFINITY) {
-            for (int c0 = 0; c0 < n; c0 += 32) {
-                const int s = c0 + lane;
-                const float ls = s < n ? __ldcg(lse + static_cast<int64_t>(s) * g) : -INFINITY;
-                const float w = ls == -INFINITY ? 0.f : expf(ls - M);
-                Ls += w;
-                const int cnt = n - c0 < 32 ? n - c0 : 32;
-                const float4* po =
-                    reinterpret_cast<const float4*>(p.part_o + (static_cast<int64_t>(first + c0) * g + h) * kDh) + lane;
-                #pragma unroll 8
-                for (int j = 0; j < cnt; ++j) {
-                    const float wj = __shfl_sync(kFull, w, j);
-                    const float4 v = __ldcg(po + static_cast<int64_t>(j) * g * (kDh / 4));
-                    if (wj != 0.f) {
-                        acc.x = fmaf(wj, v.x, acc.x);
-                        acc.y = fmaf(wj, v.y, acc.y);
-                        acc.z = fmaf(wj, v.z, acc.z);
-                        acc.w = fmaf(wj, v.w, acc.w);
-                    }
-                }
-            }
-            #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) Ls += __shfl_xor_sync(kFull, Ls, off);
-        }
-        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-        const int64_t orow = orow0 + h;
-        if (p.out_f32) {
-            reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * kDh)[lane] =
-                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-        } else {
-            uint2 v;
-            v.x = pack_bf16(acc.x * inv, acc.y * inv);
-            v.y = pack_bf16(acc.z * inv, acc.w * inv);
-            reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + orow * kDh)[lane] = v;
-        }
-        if (p.lse_out && lane == 0) p.lse_out[orow] = Ls > 0.f ? M + logf(Ls) : -INFINITY;
-    }
-}
-
 // DIRECT: the pool's host-tier blocks are read in place from host memory (lsu_fill); only
 // pools with such a tier launch this variant, so the others carry none of its code.
 template <bool FP8, int S, bool DIRECT>
@@ -276,7 +217,6 @@ __global__ void __launch_bounds__(kThreads, FP8 && S == 8 ? 4 : 3) decode_kernel
     int* pref = reinterpret_cast<int*>(smem + L.pref_off);
     int* lens = reinterpret_cast<int*>(smem + L.lens_off);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_off);
-    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L.flag_off);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -351,8 +291,7 @@ __global__ void __launch_bounds__(kThreads, FP8 && S == 8 ? 4 : 3) decode_kernel
     const int64_t lo = chunk * cta;
     const int64_t hi = (lo + chunk < T) ? lo + chunk : T;
 
-    // Units with no block: no CTA covers them, so CTA 0's consumer warps mark them empty (and,
-    // when this kernel merges, write their output: 0, lse −inf).
+    // Units with no block: no CTA covers them, so CTA 0's consumer warps mark them empty.
     if (cta == 0 && warp < kNcw) {
         if (p.early) pdl_wait();
         const int U = p.B * p.n_kv;
@@ -361,12 +300,6 @@ __global__ void __launch_bounds__(kThreads, FP8 && S == 8 ? 4 : 3) decode_kernel
             if (pref[b + 1] == pref[b]) {
                 p.unit_first[u] = 0;
                 p.unit_count[u] = 0;
-                if (p.merge) {
-                    const int64_t row0 = static_cast<int64_t>(b) * p.n_q + (u % p.n_kv) * p.g;
-                    for (int r = 0; r < p.g * kDh; ++r) store_out(p, row0 * kDh + r, 0.f);
-                    if (p.lse_out)
-                        for (int h = 0; h < p.g; ++h) p.lse_out[row0 + h] = -INFINITY;
-                }
             }
         }
     }
@@ -791,9 +724,6 @@ __global__ void __launch_bounds__(kThreads, FP8 && S == 8 ? 4 : 3) decode_kernel
         // A unit that lies in this CTA alone is final here: write the output straight from
         // registers and mark it done (unit_count = -1) so the combine kernel skips it.
         const bool whole = p.out != nullptr && sg.j0 == 0 && sg.end == sg.unit_end;
-        // CTAs c_first .. c_first + npieces - 1 each hold one piece of the unit
-        const int c_first = static_cast<int>((sg.unit_end - sg.nblk) / chunk);
-        const int npieces = static_cast<int>((sg.unit_end - 1) / chunk) - c_first + 1;
         if (warp == 0) {
             fold(merge);
             const float i0 = s0 > 0.f ? 1.f / s0 : 0.f, i1 = s1 > 0.f ? 1.f / s1 : 0.f;
@@ -842,30 +772,13 @@ __global__ void __launch_bounds__(kThreads, FP8 && S == 8 ? 4 : 3) decode_kernel
                     if (h0 < g) pl[h0] = ls0;
                     if (h1 < g) pl[h1] = ls1;
                 }
-                if (p.merge) {
-                    // publish the partial, then count it: the piece that completes the unit's
-                    // count (atomicInc wraps the counter back to 0 for the next call) merges
-                    __threadfence();
-                    __syncwarp();
-                    if (lane == 0) {
-                        const uint32_t old = atomicInc(p.merge_ctr + u, static_cast<uint32_t>(npieces - 1));
-                        *last_flag = old == static_cast<uint32_t>(npieces - 1) ? 1 : 0;
-                    }
-                } else if (sg.j0 == 0 && lane == 0) {
+                if (sg.j0 == 0 && lane == 0) {
                     p.unit_first[u] = slot;
-                    p.unit_count[u] = npieces;
+                    p.unit_count[u] = static_cast<int>((sg.unit_end - 1) / chunk - cta + 1);
                 }
             }
         }
         named_barrier(1, kNcw * 32);   // the buffer is free again for the next segment
-        if (p.merge && !whole && *last_flag) {
-            __threadfence();
-            merge_unit(p, u + c_first, npieces, static_cast<int64_t>(sg.b) * p.n_q + sg.kvh * g, warp, lane);
-            if (tid == 0) {
-                p.unit_first[u] = u + c_first;
-                p.unit_count[u] = -1;
-            }
-        }
         x = sg.end;
     }
 }

@@ -4,7 +4,12 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+struct kvd_pool;
+
 namespace kvd {
+
+// Device ordinal the pool was created on (its memory and state live there).
+int pool_device(const kvd_pool* pool);
 
 struct AppendParams {
     const uint16_t* k_new;       // bf16 bits [n_tokens][n_kv][128]
@@ -39,8 +44,6 @@ struct DecodeParams {
     float* part_lse;             // [S + U][g]
     int32_t* unit_first;         // [U]
     int32_t* unit_count;         // [U]
-    uint32_t* merge_ctr;         // [U] pieces of each unit seen so far (the pool's; zero between calls)
-    int merge;                   // 1: the CTA whose piece completes a unit merges it (needs out)
     float* logits;               // [B][n_q][logits_stride] or null
     int64_t logits_stride;
     int32_t* err;
@@ -69,7 +72,6 @@ struct CombineParams {
     int g;
     int out_f32;
     int slots_hint;              // expected partials per unit (sizes the combine CTA), 0 = unknown
-    int merged;                  // 1: the decode kernel already merged every unit (epilogue: scores only)
 };
 
 struct ScoreParams {

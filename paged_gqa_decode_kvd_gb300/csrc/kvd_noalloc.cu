@@ -13,6 +13,7 @@
 #include <mutex>
 
 #include "../../include/kvd.h"
+#include "kvd_internal.h"
 
 namespace {
 
@@ -23,10 +24,9 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device, looked up once per device.
-kvd_status scratch_for_current_device(void** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return KVD_ERR_CUDA;
+// Device address of the scratch array on device `dev` (the current device), looked up once
+// per device and kept for the lifetime of that device's primary context.
+kvd_status scratch_for_device(int dev, void** out) {
     if (dev < 0 || dev >= kMaxDevices) return KVD_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!g_scratch_addr[dev]) {
@@ -51,14 +51,19 @@ extern "C" kvd_status kvd_decode_attn_noalloc(kvd_pool* pool, int layer, const v
                                               int out_dtype, float* lse_out, float* logits_out,
                                               int64_t logits_stride, const kvd_scores_desc* scores_epilogue,
                                               unsigned flags, void* stream) {
+    if (!pool) return KVD_ERR_INVALID;
     if (!out && batch > 0) return KVD_ERR_INVALID;  // the partials would be unreachable
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KVD_ERR_CUDA;
+    // the scratch address below is the current device's: it must be the pool's device
+    if (dev != kvd::pool_device(pool)) return KVD_ERR_INVALID;
     int splits = 0;
     size_t need = 0;
     kvd_status st = kvd_decode_workspace_bytes(pool, n_q, batch, max_seq_len, num_splits, &splits, &need);
     if (st != KVD_OK) return st;
     if (need > static_cast<size_t>(KVD_NOALLOC_SCRATCH_BYTES)) return KVD_ERR_NOMEM;
     void* scratch = nullptr;
-    st = scratch_for_current_device(&scratch);
+    st = scratch_for_device(dev, &scratch);
     if (st != KVD_OK) return st;
     return kvd_decode_attn(pool, layer, q, n_q, k_new, v_new, block_table, max_blocks_per_seq, seq_lens, batch,
                            max_seq_len,

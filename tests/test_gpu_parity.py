@@ -525,39 +525,3 @@ def test_early_start_is_bitwise_identical(cuda_device, kv_dtype):
     for a, b in zip(*results):
         assert torch.equal(a, b)
 
-
-@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
-def test_in_kernel_merge_matches_separate_merge_and_oracle(cuda_device, kv_dtype):
-    """The split merge done by the CTA that completes each unit equals the separate merge
-    launch (KVD_SEPARATE_MERGE) and the oracle.  Calls alternate between split counts, so a
-    unit's piece count changes from call to call: the pool's merge counters must come back to
-    zero after every call, and repeating a call must give the same bits."""
-    w = _custom(f"inmerge_{kv_dtype}", 64, 8, [9000, 33, 1500, 4096, 16], kv_dtype=kv_dtype, seed=21)
-    dev = cuda_device
-    bt, bt_d, seq, seq_d, _ = H.device_inputs(w, dev)
-    pool = H.make_pool(w)
-    H.fill_layer(pool, w, 0, bt, w.seq_lens(), dev)
-    q = w.q(0, 0, dev)
-    S = max(w.seq_lens())
-    ref = H.oracle_layer(w, 0, bt, w.seq_lens())
-    first = {}
-    for rnd in range(2):
-        for splits in (0, 7, 301, 1):
-            _, ws = H.workspace(pool, w.n_q, w.batch, S, splits, dev)
-            res = []
-            for sep in (False, True):
-                out = torch.full((w.batch, w.n_q, 128), float("nan"), dtype=torch.float32, device=dev)
-                lse = torch.full((w.batch, w.n_q), float("nan"), dtype=torch.float32, device=dev)
-                kvd.kvd_decode_attn(pool.handle, 0, q, bt_d, seq_d, S, ws, out, num_splits=splits, lse_out=lse,
-                                    separate_merge=sep)
-                assert kvd.kvd_get_device_error(pool.handle) == 0
-                res.append((out.cpu(), lse.cpu()))
-            (o_in, l_in), (o_sep, l_sep) = res
-            np.testing.assert_allclose(o_in.numpy(), o_sep.numpy(), rtol=1e-5, atol=1e-6)
-            np.testing.assert_allclose(l_in.numpy(), l_sep.numpy(), rtol=1e-6, atol=1e-5)
-            H.assert_out_close(o_in.numpy(), ref["out"], what=f"splits {splits}")
-            np.testing.assert_allclose(l_in.numpy(), ref["lse"], rtol=1e-5, atol=1e-4)
-            if rnd == 0:
-                first[splits] = o_in
-            else:
-                assert torch.equal(first[splits], o_in)

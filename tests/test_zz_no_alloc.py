@@ -2,9 +2,11 @@
 
 Such callers (a host framework whose allocator owns all device memory, a latency-critical
 loop that cannot take cudaMalloc's synchronisation) pass only inputs and outputs; the split
-scratch lives in a fixed array inside the library.  Two calls in a row, with different
-shapes, must each match the workspace-taking entry point, so nothing stale from the first
-call leaks into the second.  This file is collected last on purpose.
+scratch lives in a fixed array inside the library.  The entry point runs the same kernels
+with the same split plan as kvd_decode_attn, so its results must be the same bits.  Two
+calls in a row, with different shapes, pool types and a fused score update, must each match
+the workspace-taking entry point, so nothing stale from one call leaks into the next.  This
+file is collected last on purpose.
 """
 
 import numpy as np
@@ -18,39 +20,76 @@ from tests import harness as H
 pytestmark = pytest.mark.gpu
 
 
-def _workload(name, n_q, n_kv, lens, seed):
-    w = Workload(name, L=1, n_q=n_q, n_kv=n_kv, d_h=128, batch=len(lens), kv_dtype="bf16", seed=seed)
+def _workload(name, n_q, n_kv, lens, seed, kv_dtype="bf16", **kw):
+    w = Workload(name, L=1, n_q=n_q, n_kv=n_kv, d_h=128, batch=len(lens), kv_dtype=kv_dtype, seed=seed, **kw)
     w._ctx0 = list(lens)
     return w
 
 
-def _both(w, dev):
-    bt, bt_d, seq, seq_d, _ = H.device_inputs(w, dev)
+def _both(w, dev, scores=False):
+    """The same call through both entry points; returns each one's (out, lse[, scores])."""
+    bt, bt_d, seq, seq_d, ret_d = H.device_inputs(w, dev)
     pool = H.make_pool(w)
     H.fill_layer(pool, w, 0, bt, w.seq_lens(), dev)
     q = w.q(0, 0, dev)
     max_len = max(w.seq_lens())
     _, ws = H.workspace(pool, w.n_q, w.batch, max_len, 0, dev)
-    ref = torch.empty(w.batch, w.n_q, 128, dtype=torch.float32, device=dev)
-    ref_lse = torch.empty(w.batch, w.n_q, dtype=torch.float32, device=dev)
-    kvd.kvd_decode_attn(pool.handle, 0, q, bt_d, seq_d, max_len, ws, ref, lse_out=ref_lse)
-    out = torch.full_like(ref, float("nan"))
-    lse = torch.full_like(ref_lse, float("nan"))
-    kvd.kvd_decode_attn_noalloc(pool.handle, 0, q, bt_d, seq_d, max_len, out, lse_out=lse)
-    assert kvd.kvd_get_device_error(pool.handle) == 0
-    return out.cpu().numpy(), lse.cpu().numpy(), ref.cpu().numpy(), ref_lse.cpu().numpy()
+    base = torch.rand(w.batch, max_len, dtype=torch.float32, device=dev) if scores else None
+    res = []
+    for noalloc in (False, True):
+        out = torch.full((w.batch, w.n_q, 128), float("nan"), dtype=torch.float32, device=dev)
+        lse = torch.full((w.batch, w.n_q), float("nan"), dtype=torch.float32, device=dev)
+        kw = dict(retain_mask=ret_d, lse_out=lse)
+        sc = None
+        if scores:
+            sc = base.clone()
+            kw.update(logits_out=torch.empty(w.batch, w.n_q, max_len, dtype=torch.float32, device=dev), scores=sc,
+                      inv_LH=1.0 / w.n_q)
+        if noalloc:
+            kvd.kvd_decode_attn_noalloc(pool.handle, 0, q, bt_d, seq_d, max_len, out, **kw)
+        else:
+            kvd.kvd_decode_attn(pool.handle, 0, q, bt_d, seq_d, max_len, ws, out, **kw)
+        assert kvd.kvd_get_device_error(pool.handle) == 0
+        res.append((out.cpu(), lse.cpu(), None if sc is None else sc.cpu()))
+    ref = H.oracle_layer(w, 0, bt, w.seq_lens(), retain=w.retain_mask(bt))
+    return res, ref, pool
 
 
 def test_noalloc_matches_workspace_entry_point_on_two_calls(cuda_device):
-    first = _workload("noalloc_a", 32, 8, [3000, 17, 1200, 640], seed=1)
-    second = _workload("noalloc_b", 16, 2, [5, 2047, 800], seed=2)
-    for w in (first, second):
-        out, lse, ref, ref_lse = _both(w, cuda_device)
-        H.assert_out_close(out, ref, what=f"{w.name} out")
-        np.testing.assert_allclose(lse, ref_lse, rtol=1e-5, atol=1e-4)
+    calls = [
+        (_workload("noalloc_a", 32, 8, [3000, 17, 1200, 640], seed=1), False),
+        (_workload("noalloc_b", 28, 4, [5, 2047, 800], seed=2, kv_dtype="fp8_e4m3", outlier_p=0.01,
+                   outlier_factor=20.0), False),
+        (_workload("noalloc_c", 28, 4, [3000, 700, 16], seed=3, evict_frac=0.05, protect_prompt=64,
+                   protect_recent=32, scores=True), True),
+    ]
+    for w, scores in calls:
+        (ws_res, na_res), ref, _ = _both(w, cuda_device, scores)
+        for a, b in zip(ws_res, na_res):
+            if a is not None:
+                assert torch.equal(a, b), f"{w.name}: the no-alloc result differs from the workspace path"
+        H.assert_out_close(na_res[0].numpy(), ref["out"], what=f"{w.name} out")
+        np.testing.assert_allclose(na_res[1].numpy(), ref["lse"], rtol=1e-5, atol=1e-4)
 
 
-def test_noalloc_rejects_shapes_beyond_its_scratch(cuda_device):
+def test_noalloc_call_allocates_no_device_memory(cuda_device):
+    w = _workload("noalloc_mem", 32, 8, [4000, 900], seed=4)
+    bt, bt_d, seq, seq_d, _ = H.device_inputs(w, cuda_device)
+    pool = H.make_pool(w)
+    H.fill_layer(pool, w, 0, bt, w.seq_lens(), cuda_device)
+    q = w.q(0, 0, cuda_device)
+    out = torch.empty(w.batch, w.n_q, 128, dtype=torch.bfloat16, device=cuda_device)
+    kvd.kvd_decode_attn_noalloc(pool.handle, 0, q, bt_d, seq_d, 4000, out)   # first call: address lookup
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info(cuda_device)[0]
+    for _ in range(3):
+        kvd.kvd_decode_attn_noalloc(pool.handle, 0, q, bt_d, seq_d, 4000, out)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info(cuda_device)[0] == free0
+    assert kvd.kvd_get_device_error(pool.handle) == 0
+
+
+def test_noalloc_rejects_shapes_beyond_its_scratch_and_a_null_output(cuda_device):
     w = _workload("noalloc_big", 64, 8, [16], seed=3)
     pool = H.make_pool(w)
     big_batch = 2048                                  # needs far more than the fixed scratch
@@ -63,3 +102,6 @@ def test_noalloc_rejects_shapes_beyond_its_scratch(cuda_device):
     with pytest.raises(kvd.KvdError) as e:
         kvd.kvd_decode_attn_noalloc(pool.handle, 0, q, bt, seq, 1 << 17, out, num_splits=4096)
     assert e.value.status == kvd.KVD_ERR_NOMEM
+    with pytest.raises(kvd.KvdError) as e:
+        kvd.kvd_decode_attn_noalloc(pool.handle, 0, q[:1], bt[:1], seq[:1], 16, None)
+    assert e.value.status == kvd.KVD_ERR_INVALID
