@@ -216,9 +216,12 @@ class Step:
         self.w, self.dev, self.kvd = w, dev, kvd
         self.early = early   # KVD_EARLY_START: the step's tables and pool are not written by the previous kernel
         self.L = w.L
-        self.fp8 = w.kv_dtype != "bf16"
-        self.pool = kvd.KVPool(w.L, w.n_kv, w.num_blocks(), kvd.KVD_FP8_E4M3 if self.fp8 else kvd.KVD_BF16,
-                               device=dev)
+        kind = {"bf16": kvd.KVD_BF16, "fp8_e4m3": kvd.KVD_FP8_E4M3, "mixed": kvd.KVD_MIXED}[w.kv_dtype]
+        self.pool = kvd.KVPool(w.L, w.n_kv, w.num_blocks(), kind, device=dev)
+        if w.kv_dtype == "mixed":   # a storage format per physical block
+            codes = [kvd.KVD_BF16, kvd.KVD_FP8_E4M3, kvd.KVD_FP8_E5M2]
+            fmt = torch.tensor([codes[f] for f in w.block_formats().tolist()], dtype=torch.uint8)
+            self.pool.set_block_formats(fmt.to(dev))
         bt = w.block_table()
         self.bt = bt.to(dev)
         self.nsteps = w.steps
@@ -456,12 +459,16 @@ class Step:
         self.staged[layer] = ev
 
     def kv_bytes(self, t: int) -> int:
-        w = self.w
-        return int(2 * w.L * w.n_kv * w.d_h * w.w_kv * sum(self.lens[t]))
+        """Closed-form K/V bytes attended by step t (all layers), FP8 scales excluded."""
+        if not hasattr(self, "_kvb"):
+            self._kvb = {}
+        if t not in self._kvb:
+            self._kvb[t] = (self.w.kv_bytes_per_step(t), self.w.scale_bytes_per_step(t))
+        return self._kvb[t][0]
 
     def scale_bytes(self, t: int) -> int:
-        w = self.w
-        return 0 if w.kv_dtype == "bf16" else int(2 * w.L * w.n_kv * 4 * sum(self.lens[t]))
+        self.kv_bytes(t)
+        return self._kvb[t][1]
 
     def layer_call(self, layer: int, t: int = 0, stream=None):
         """One layer's decode: fused append of the new token, attention, split merge, and (with
@@ -676,7 +683,8 @@ def gpu_workload(args, w, rank, world, local, peaks, headline: bool) -> dict:
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8_e4m3",
+        "vs_baseline": None, "dtype": {"bf16": "bf16", "fp8_e4m3": "fp8_e4m3",
+                                       "mixed": "mixed: bf16 / fp8_e4m3 / fp8_e5m2 per block"}[w.kv_dtype],
         "data": "synthetic (seeded counter-hash generator)",
         "config": workload_config(w),
         "launch": {"num_splits": st.splits, "early_start": st.early,
@@ -751,7 +759,7 @@ def e2e_steps(st, args, world) -> dict:
                    "copied from pinned host memory and its outputs back, every step"}
 
 
-EXTRA_WORKLOADS = ("ragged", "llama70b_fp8", "tiered")
+EXTRA_WORKLOADS = ("ragged", "llama70b_fp8", "tiered", "llama8b_mixed")
 
 
 def gpu_arm(args, w, rank, world, local):
@@ -788,9 +796,10 @@ def gpu_arm(args, w, rank, world, local):
 
 
 # ------------------------------------------------------------------ the CPU oracle arm
-def _oracle_unit(w, layer: int, b: int, kf, vf, q):
+def _oracle_unit(w, layer: int, b: int, kf, vf, q, fmt=None):
     """The oracle on one (layer, request) unit: append of its context into the oracle's own pool,
-    then decode of all its query heads (fp64)."""
+    then decode of all its query heads (fp64).  fmt: a mixed pool's formats of the request's
+    blocks, in table order."""
     import numpy as np
 
     import oracle
@@ -799,15 +808,28 @@ def _oracle_unit(w, layer: int, b: int, kf, vf, q):
     nblk = -(-n // 16)
     slots = np.arange(n, dtype=np.int64)
     table = np.arange(nblk, dtype=np.int32)[None, :]
-    pool = oracle.OraclePool(nblk, w.n_kv, w.d_h, 16, w.kv_dtype != "bf16")
+    if fmt is not None:
+        pool = oracle.OraclePool(nblk, w.n_kv, w.d_h, 16, block_fmt=fmt)
+    else:
+        pool = oracle.OraclePool(nblk, w.n_kv, w.d_h, 16, w.kv_dtype != "bf16")
     pool.append(kf, vf, slots)
     oracle.decode(pool, q, w.n_q, table, [n])
 
 
 def _unit_inputs(w, b: int):
+    """Inputs of the (layer 0, request b) unit: K, V, q, the block formats (mixed pools) and the
+    unit's closed-form K/V bytes."""
     n = w.seq_lens(0)[b]
     k, v = w.kv(0, b, 0, n)
-    return k.float().numpy(), v.float().numpy(), w.q(0, 0)[b:b + 1].float().numpy()
+    fmt = None
+    if w.kv_dtype == "mixed":
+        nblk = -(-n // 16)
+        fmt = w.block_formats()[w.block_table()[b, :nblk].numpy()]
+        wide = int((fmt == 0).sum()) * 16 - (16 * nblk - n if fmt[-1] == 0 else 0)
+        nbytes = 2 * w.n_kv * w.d_h * (2 * wide + (n - wide))
+    else:
+        nbytes = kv_bytes_per_token(1, w.n_kv, w.d_h, w.w_kv) * n
+    return k.float().numpy(), v.float().numpy(), w.q(0, 0)[b:b + 1].float().numpy(), fmt, nbytes
 
 
 def host_threads() -> int:
@@ -827,13 +849,13 @@ def oracle_sample(w, threads: int, budget_s: float) -> dict:
 
     oracle.build()
     ins = [_unit_inputs(w, b % w.batch) for b in range(min(threads, w.batch))]
-    per_unit = [kv_bytes_per_token(1, w.n_kv, w.d_h, w.w_kv) * x[0].shape[0] for x in ins]
+    per_unit = [x[4] for x in ins]
 
     def worker(i):
         units, done = 0, 0.0
         t0 = time.perf_counter()
         while True:
-            _oracle_unit(w, 0, i, *ins[i % len(ins)])
+            _oracle_unit(w, 0, i, *ins[i % len(ins)][:4])
             units += 1
             done += per_unit[i % len(ins)]
             if time.perf_counter() - t0 >= budget_s:
@@ -878,13 +900,13 @@ def reference_arm(args, w, rank, world):
     def sample():
         t0 = time.perf_counter()
         with cf.ThreadPoolExecutor(max_workers=n) as ex:
-            list(ex.map(lambda i: _oracle_unit(w, 0, i, *ins[i % len(ins)]), range(n)))
+            list(ex.map(lambda i: _oracle_unit(w, 0, i, *ins[i % len(ins)][:4]), range(n)))
         return time.perf_counter() - t0
 
     for _ in range(args.warmup):
         sample()
     walls = [sample() for _ in range(args.steps)]
-    per_sample = sum(kv_bytes_per_token(1, w.n_kv, w.d_h, w.w_kv) * ins[i % len(ins)][0].shape[0] for i in range(n))
+    per_sample = sum(ins[i % len(ins)][4] for i in range(n))
     total_s = sum(walls)
     gbs = per_sample * args.steps / total_s / 1e9
     return {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world,

@@ -46,6 +46,9 @@
  *      BF16 element index within the tile: (i·32 + lane)·8 + e
  *      FP8  byte index within the tile:   ((i/2)·32 + lane)·16 + (i%2)·8 + e
  *  - The pool is written only through kvd_append_kv.
+ *  - A mixed pool (KVD_MIXED) gives every record the BF16 size, 8192 bytes; a block stored
+ *    in E4M3 or E5M2 puts the 4224-byte FP8 record (codes of its own format, then the 32
+ *    scales) at the start of its slot and leaves the rest unused.
  */
 #ifndef KVD_H
 #define KVD_H
@@ -76,7 +79,9 @@ typedef enum {
 typedef enum {
     KVD_BF16 = 0,             /* w_kv = 2 bytes */
     KVD_FP8_E4M3 = 1,         /* w_kv = 1 byte, plus a per-(token, KV head) fp32 scale for K and for V */
-    KVD_F32 = 2               /* output only (full-precision check output) */
+    KVD_F32 = 2,              /* output only (full-precision check output) */
+    KVD_FP8_E5M2 = 3,         /* block format of a mixed pool: like E4M3, codes 1·5·2 bits, max 57,344 */
+    KVD_MIXED = 4             /* pool of mixed-precision blocks (kvd_pool_set_block_formats) */
 } kvd_dtype;
 
 typedef struct {
@@ -85,7 +90,7 @@ typedef struct {
     int32_t d_h;              /* head dimension; 128 */
     int32_t block_size;       /* tokens per block; 16 */
     int64_t num_blocks;       /* physical blocks per layer */
-    int32_t kv_dtype;         /* KVD_BF16 or KVD_FP8_E4M3 */
+    int32_t kv_dtype;         /* KVD_BF16, KVD_FP8_E4M3 or KVD_MIXED */
 } kvd_pool_desc;
 
 typedef struct kvd_pool kvd_pool;  /* opaque */
@@ -126,6 +131,23 @@ KVD_API kvd_status kvd_pool_create(const kvd_pool_desc* desc, void* mem, size_t 
 /* Free the handle and its error word (not the caller's pool memory).  NULL is a no-op. */
 KVD_API void kvd_pool_destroy(kvd_pool* pool);
 
+/* Mixed-precision pool, tier-homogeneous pages.  Page "The KV Cache Is the New Memory Wall",
+ * §5.5 (first open direction): one paged layout that carries a precision per block next to its
+ * retention mask; page "기술 요약: Spherical KV", §2.2 (tier-homogeneous pages): every entry of
+ * a page shares one precision tier, so the decode kernel reads a page in a single pass guided
+ * by its header.  A pool created with kv_dtype = KVD_MIXED stores physical block p in the
+ * format block_fmt[p]: KVD_BF16 (values), KVD_FP8_E4M3 or KVD_FP8_E5M2 (codes with a
+ * per-(token, KV head) fp32 scale for K and for V; scale = fp32(absmax/top), top = 448 or
+ * 57,344, code = round to nearest even, saturating, of the fp32 quotient x/scale).  The
+ * decode kernel reads a block's precision byte beside its retain bits and copies 8192 or 4224
+ * bytes.  block_fmt: uint8 [count ≥ num_blocks], device, caller-owned, read by every later
+ * kvd_append_kv and kvd_decode_attn of the pool (for every layer); change a block's format
+ * only while it holds no token.  A byte that is none of the three codes makes the block's
+ * tokens skipped (append) or treated as empty (decode) with KVD_ERR_OOB in the error word.
+ * KVD_ERR_INVALID for a pool that is not mixed, a NULL array or count < num_blocks.  A mixed
+ * pool takes no host tier (kvd_pool_attach_host_tier: KVD_ERR_UNSUPPORTED). */
+KVD_API kvd_status kvd_pool_set_block_formats(kvd_pool* pool, const uint8_t* block_fmt, int64_t count);
+
 /* Host tier (T1) of a pool.  Page "기술 요약: 모든 사고가 HBM 을 필요로 하는 것은 아님",
  * section "1. 4 단계 분류": mid-importance tokens (tier T1) live at full precision in host
  * memory and are brought to the GPU before every attention step; section "3. 제로-근사오차
@@ -142,7 +164,7 @@ KVD_API void kvd_pool_destroy(kvd_pool* pool);
  *    slots (slot layer % 2); kvd_decode_attn reads a host-tier block from that staged copy,
  *    so the staged layer must be the one attended.
  * A retain_mask then has num_blocks + host_blocks entries.  Block tables may mix both kinds
- * of ids freely. */
+ * of ids freely.  Mixed pools (KVD_MIXED) have no host tier. */
 
 /* host_bytes = L·host_blocks·n_kv·record_bytes (pinned host memory); staging_bytes =
  * 2·host_blocks·n_kv·record_bytes (device).  host_blocks ≥ 0.  Host only. */

@@ -30,7 +30,7 @@ class Workload:
     n_kv: int
     d_h: int
     batch: int
-    kv_dtype: str                       # "bf16" or "fp8_e4m3"
+    kv_dtype: str                       # "bf16", "fp8_e4m3" or "mixed" (a format per physical block)
     block_size: int = 16
     seed: int = 0
     steps: int = 1                      # decode steps in one unit of work
@@ -42,6 +42,7 @@ class Workload:
     protect_recent: int = 0             # trailing tokens never evicted
     scores: bool = False                # accumulate the importance score s_i
     pool_slack_blocks: int = 0          # unused physical blocks added to the pool
+    mixed_probs: tuple | None = None    # mixed pools: P(BF16), P(E4M3), P(E5M2) of a physical block
     description: str = ""
     _ctx0: list = field(default_factory=list)   # context before step 0's append
 
@@ -52,6 +53,9 @@ class Workload:
 
     @property
     def w_kv(self) -> int:
+        """Bytes per stored K or V element (a single-format pool)."""
+        if self.kv_dtype == "mixed":
+            raise ValueError("a mixed pool has a w_kv per block: use token_bytes()")
         return 2 if self.kv_dtype == "bf16" else 1
 
     def seq_lens(self, step: int = 0) -> list[int]:
@@ -77,15 +81,41 @@ class Workload:
         """Position written by the decode-step append of ``step``, per sequence."""
         return [c - 1 for c in self.seq_lens(step)]
 
-    def kv_bytes_per_step(self) -> int:
-        """Closed-form K/V bytes attended in one step over all layers: 2·L·n_kv·d_h·w_kv per token."""
-        tokens = sum(self.seq_lens(0))
-        return 2 * self.L * self.n_kv * self.d_h * self.w_kv * tokens
+    def _tokens_by_width(self, step: int = 0) -> tuple[int, int]:
+        """(tokens attended in 2-byte storage, tokens in 1-byte storage) at ``step``."""
+        tokens = sum(self.seq_lens(step))
+        if self.kv_dtype != "mixed":
+            return (tokens, 0) if self.kv_dtype == "bf16" else (0, tokens)
+        fmt = self.block_formats()
+        bt = self.block_table()
+        wide = 0
+        for b, n in enumerate(self.seq_lens(step)):
+            full, tail = divmod(n, self.block_size)
+            ids = bt[b, :full].numpy()
+            wide += int((fmt[ids] == 0).sum()) * self.block_size
+            if tail and fmt[int(bt[b, full])] == 0:
+                wide += tail
+        return wide, tokens - wide
 
-    def scale_bytes_per_step(self) -> int:
-        if self.kv_dtype == "bf16":
-            return 0
-        return 2 * self.L * self.n_kv * 4 * sum(self.seq_lens(0))
+    def kv_bytes_per_step(self, step: int = 0) -> int:
+        """Closed-form K/V bytes attended in one step over all layers: 2·L·n_kv·d_h·w_kv per token
+        (w_kv of the block that holds the token in a mixed pool)."""
+        wide, narrow = self._tokens_by_width(step)
+        return 2 * self.L * self.n_kv * self.d_h * (2 * wide + narrow)
+
+    def scale_bytes_per_step(self, step: int = 0) -> int:
+        """fp32 scales read with the 8-bit tokens: one for K and one for V per (token, KV head)."""
+        return 2 * self.L * self.n_kv * 4 * self._tokens_by_width(step)[1]
+
+    def block_formats(self):
+        """Mixed pools: uint8 numpy [num_blocks], the storage format of every physical block
+        (0 BF16, 1 E4M3, 2 E5M2), drawn per block with probabilities mixed_probs."""
+        import numpy as np
+
+        p = self.mixed_probs or (1.0, 0.0, 0.0)
+        u = gen.uniform(gen.stream_key(self.seed, self.name, "fmt"), gen.index_range(0, self.num_blocks(), "cpu"))
+        u = u.double().numpy()
+        return np.where(u < p[0], 0, np.where(u < p[0] + p[1], 1, 2)).astype(np.uint8)
 
     # ------------------------------------------------------------- structure
     def block_table(self) -> torch.Tensor:
@@ -194,6 +224,16 @@ def llama8b(seed: int = 0) -> Workload:
     return w
 
 
+def llama8b_mixed(seed: int = 0) -> Workload:
+    w = Workload("llama8b_mixed", L=32, n_q=32, n_kv=8, d_h=128, batch=32, kv_dtype="mixed", seed=seed,
+                 key_scale_range=(0.5, 2.0), mixed_probs=(0.25, 0.5, 0.25),
+                 description="Llama-3.1-8B shape decode step, mixed-precision pages: 32 layers, n_q 32, n_kv 8, "
+                             "d_h 128, batch 32, context 8,192, each physical block BF16 / FP8-E4M3 / FP8-E5M2 "
+                             "with probability 1/4, 1/2, 1/4")
+    w._ctx0 = [8192] * 32
+    return w
+
+
 def ragged(seed: int = 0) -> Workload:
     w = Workload("ragged", L=4, n_q=32, n_kv=8, d_h=128, batch=64, kv_dtype="bf16", seed=seed,
                  description="8B shape, 4 layers, 64 requests, context log-uniform in [256, 32,768], bf16 KV")
@@ -220,7 +260,7 @@ def tiered(seed: int = 0) -> Workload:
     return w
 
 
-WORKLOADS = {"tiny": tiny, "llama8b": llama8b, "ragged": ragged,
+WORKLOADS = {"tiny": tiny, "llama8b": llama8b, "llama8b_mixed": llama8b_mixed, "ragged": ragged,
              "llama70b_fp8": llama70b_fp8, "tiered": tiered}
 
 

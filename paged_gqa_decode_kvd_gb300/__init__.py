@@ -13,6 +13,8 @@ from ._lib import (  # noqa: F401
     KVD_EARLY_START,
     KVD_F32,
     KVD_FP8_E4M3,
+    KVD_FP8_E5M2,
+    KVD_MIXED,
     KVD_OK,
     KVD_ERR_CUDA,
     KVD_ERR_INVALID,
@@ -40,6 +42,7 @@ from ._lib import (  # noqa: F401
     kvd_pool_bytes,
     kvd_pool_create,
     kvd_pool_destroy,
+    kvd_pool_set_block_formats,
     kvd_selftest_wait_timeout,
     lib_path,
     load,
@@ -60,8 +63,14 @@ class KVPool:
 
     @property
     def record_bytes(self) -> int:
-        """Bytes of one (layer, block, KV head) record: K tile, V tile and (FP8) 32 fp32 scales."""
-        return 8192 if self.kv_dtype == KVD_BF16 else 4096 + 128
+        """Bytes of one (layer, block, KV head) record slot: K tile, V tile and (FP8) 32 fp32 scales;
+        a mixed pool sizes every slot for BF16."""
+        return 4096 + 128 if self.kv_dtype == KVD_FP8_E4M3 else 8192
+
+    def set_block_formats(self, block_fmt):
+        """Mixed pool: one precision code per physical block (uint8 device tensor, kept alive here)."""
+        self.block_fmt = block_fmt
+        kvd_pool_set_block_formats(self.handle, block_fmt)
 
     def attach_host_tier(self, host_blocks: int, staged: bool = False):
         """Give the pool host_blocks host-tier blocks (ids num_blocks ..): their records in

@@ -12,7 +12,7 @@ import ctypes
 import os
 
 KVD_OK, KVD_ERR_INVALID, KVD_ERR_UNSUPPORTED, KVD_ERR_NOMEM, KVD_ERR_CUDA, KVD_ERR_OOB, KVD_ERR_TIMEOUT = range(7)
-KVD_BF16, KVD_FP8_E4M3, KVD_F32 = 0, 1, 2
+KVD_BF16, KVD_FP8_E4M3, KVD_F32, KVD_FP8_E5M2, KVD_MIXED = 0, 1, 2, 3, 4
 KVD_EARLY_START = 1   # kvd_decode_attn flag
 
 SYMBOLS = [
@@ -20,7 +20,7 @@ SYMBOLS = [
     "kvd_decode_workspace_bytes", "kvd_decode_attn", "kvd_combine_splits", "kvd_accum_scores",
     "kvd_get_device_error", "kvd_selftest_wait_timeout", "kvd_decode_attn_noalloc",
     "kvd_tier_bytes", "kvd_pool_attach_host_tier", "kvd_tier_prefetch", "kvd_tier_plan", "kvd_tier_move",
-    "kvd_tier_reassign", "kvd_measure_read_stream",
+    "kvd_tier_reassign", "kvd_measure_read_stream", "kvd_pool_set_block_formats",
 ]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -98,6 +98,8 @@ def load(build_if_missing: bool = True):
     lib.kvd_decode_attn_noalloc.restype = i32
     lib.kvd_decode_attn_noalloc.argtypes = [P, i32, P, i32, P, P, P, i32, P, i32, i32, i32, P, f32, P, i32, P, P,
                                             i64, P, ctypes.c_uint, P]
+    lib.kvd_pool_set_block_formats.restype = i32
+    lib.kvd_pool_set_block_formats.argtypes = [P, P, i64]
     lib.kvd_measure_read_stream.restype = i32
     lib.kvd_measure_read_stream.argtypes = [P, sz, P, sz, P]
     _lib = lib
@@ -209,6 +211,14 @@ def kvd_pool_create(num_layers, n_kv, num_blocks, kv_dtype, mem, d_h=128, block_
     n = mem.numel() * mem.element_size()
     _check("kvd_pool_create", load().kvd_pool_create(ctypes.byref(d), _ptr(mem), n, ctypes.byref(h)))
     return h
+
+
+def kvd_pool_set_block_formats(handle, block_fmt):
+    """Mixed pool: block_fmt (uint8 device tensor, one KVD_BF16 / KVD_FP8_E4M3 / KVD_FP8_E5M2
+    code per physical block) gives every block's storage format; the pool reads it on every
+    later append and decode, so keep the tensor alive."""
+    _check("kvd_pool_set_block_formats", load().kvd_pool_set_block_formats(handle, _ptr(block_fmt),
+                                                                           int(block_fmt.numel())))
 
 
 def kvd_pool_destroy(handle):

@@ -23,6 +23,9 @@ struct kvd_pool {
     int64_t host_blocks;
     size_t host_layer_bytes;
     int host_direct;       // no staging: the decode kernel reads host records over the host link
+    // mixed pools: precision code of every physical block (device, caller-owned)
+    const uint8_t* block_fmt;
+    int64_t block_fmt_count;
 };
 
 namespace {
@@ -39,7 +42,7 @@ kvd_status check_desc(const kvd_pool_desc* d) {
     if (!d) return KVD_ERR_INVALID;
     if (d->num_layers < 1 || d->n_kv < 1 || d->num_blocks < 1 || d->d_h < 1 || d->block_size < 1)
         return KVD_ERR_INVALID;
-    if (d->kv_dtype != KVD_BF16 && d->kv_dtype != KVD_FP8_E4M3) return KVD_ERR_INVALID;
+    if (d->kv_dtype != KVD_BF16 && d->kv_dtype != KVD_FP8_E4M3 && d->kv_dtype != KVD_MIXED) return KVD_ERR_INVALID;
     if (d->d_h != kvd::kDh || d->block_size != kvd::kBs) return KVD_ERR_UNSUPPORTED;
     return KVD_OK;
 }
@@ -70,17 +73,29 @@ WsLayout ws_layout(int units, int nsplit, int g) {
 
 // Split count: enough CTAs to fill every SM at the kernel's occupancy, but no CTA
 // with fewer than kMinBlocksPerSplit blocks of the (upper-bound) total work.
+int pool_kind(const kvd_pool* pool);
+
 int plan_splits(const kvd_pool* pool, int batch, int max_seq_len, int g) {
-    const bool fp8 = pool->desc.kv_dtype == KVD_FP8_E4M3;
     const int64_t nblk = (static_cast<int64_t>(max_seq_len) + kvd::kBs - 1) / kvd::kBs;
     const int64_t total = nblk * batch * pool->desc.n_kv;
     const int64_t by_work = (total + kMinBlocksPerSplit - 1) / kMinBlocksPerSplit;
-    const int64_t by_sms = static_cast<int64_t>(pool->num_sms) * kvd::decode_ctas_per_sm(fp8, batch, g);
+    const int64_t by_sms = static_cast<int64_t>(pool->num_sms) * kvd::decode_ctas_per_sm(pool_kind(pool), batch, g);
     int64_t s = by_work < by_sms ? by_work : by_sms;
     return static_cast<int>(s < 1 ? 1 : s);
 }
 
 kvd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVD_OK : KVD_ERR_CUDA; }
+
+int pool_kind(const kvd_pool* pool) {
+    return pool->desc.kv_dtype == KVD_FP8_E4M3 ? kvd::kKindFp8
+           : pool->desc.kv_dtype == KVD_MIXED  ? kvd::kKindMixed
+                                               : kvd::kKindBf16;
+}
+
+// Bytes of one (layer, block, KV head) record slot.
+size_t record_bytes(const kvd_pool_desc* d) {
+    return d->kv_dtype == KVD_FP8_E4M3 ? kvd::kRecordFp8 : kvd::kRecordBf16;
+}
 
 }  // namespace
 
@@ -105,7 +120,8 @@ kvd_status kvd_pool_bytes(const kvd_pool_desc* desc, size_t* pool_bytes, size_t*
     kvd_status st = check_desc(desc);
     if (st != KVD_OK) return st;
     if (!kv_bytes || !pool_bytes) return KVD_ERR_INVALID;
-    const size_t w = desc->kv_dtype == KVD_BF16 ? 2 : 1;
+    // a mixed pool sizes every record slot for BF16 (an 8-bit block uses the first part of it)
+    const size_t w = desc->kv_dtype == KVD_FP8_E4M3 ? 1 : 2;
     size_t per_block = 0, rows = 0, total = 0;
     // 2 (K and V) · block_size · d_h · w_kv bytes per (layer, block, KV head)
     if (!mul_ok(2 * static_cast<size_t>(desc->block_size) * desc->d_h, w, &per_block)) return KVD_ERR_INVALID;
@@ -143,6 +159,8 @@ kvd_status kvd_pool_create(const kvd_pool_desc* desc, void* mem, size_t len, kvd
     p->host_blocks = 0;
     p->host_layer_bytes = 0;
     p->host_direct = 0;
+    p->block_fmt = nullptr;
+    p->block_fmt_count = 0;
     const size_t state_bytes = sizeof(int32_t);
     if (cudaGetDevice(&p->device) != cudaSuccess ||
         cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess ||
@@ -160,7 +178,7 @@ kvd_status kvd_tier_bytes(const kvd_pool_desc* desc, int64_t host_blocks, size_t
     kvd_status st = check_desc(desc);
     if (st != KVD_OK) return st;
     if (host_blocks < 0 || !host_bytes || !staging_bytes) return KVD_ERR_INVALID;
-    const size_t rec = desc->kv_dtype == KVD_FP8_E4M3 ? kvd::kRecordFp8 : kvd::kRecordBf16;
+    const size_t rec = record_bytes(desc);
     size_t layer = 0, all = 0;
     if (!mul_ok(static_cast<size_t>(host_blocks), static_cast<size_t>(desc->n_kv), &layer)) return KVD_ERR_INVALID;
     if (!mul_ok(layer, rec, &layer)) return KVD_ERR_INVALID;
@@ -170,9 +188,18 @@ kvd_status kvd_tier_bytes(const kvd_pool_desc* desc, int64_t host_blocks, size_t
     return KVD_OK;
 }
 
+kvd_status kvd_pool_set_block_formats(kvd_pool* pool, const uint8_t* block_fmt, int64_t count) {
+    if (!pool || pool->desc.kv_dtype != KVD_MIXED || !block_fmt || count < pool->desc.num_blocks)
+        return KVD_ERR_INVALID;
+    pool->block_fmt = block_fmt;
+    pool->block_fmt_count = count;
+    return KVD_OK;
+}
+
 kvd_status kvd_pool_attach_host_tier(kvd_pool* pool, void* host_mem, size_t host_len, void* staging_mem,
                                      size_t staging_len, int64_t host_blocks) {
     if (!pool || host_blocks < 0) return KVD_ERR_INVALID;
+    if (pool->desc.kv_dtype == KVD_MIXED && host_blocks > 0) return KVD_ERR_UNSUPPORTED;
     if (host_blocks == 0) {
         pool->host_kv = nullptr;
         pool->host_mem = nullptr;
@@ -249,7 +276,7 @@ kvd_status kvd_tier_move(kvd_pool* pool, const int32_t* from_ids, const int32_t*
     p.err = pool->err;
     p.num_blocks = pool->desc.num_blocks;
     p.host_blocks = pool->host_blocks;
-    p.record_bytes = pool->desc.kv_dtype == KVD_FP8_E4M3 ? kvd::kRecordFp8 : kvd::kRecordBf16;
+    p.record_bytes = static_cast<int64_t>(record_bytes(&pool->desc));
     p.n = n;
     p.L = pool->desc.num_layers;
     p.n_kv = pool->desc.n_kv;
@@ -335,18 +362,20 @@ kvd_status kvd_append_kv(kvd_pool* pool, int layer, const void* k_new, const voi
     if (n_tokens == 0) return KVD_OK;
     if (!k_new || !v_new || !slot_mapping) return KVD_ERR_INVALID;
     if ((reinterpret_cast<uintptr_t>(k_new) & 7u) || (reinterpret_cast<uintptr_t>(v_new) & 7u)) return KVD_ERR_INVALID;
+    if (pool->desc.kv_dtype == KVD_MIXED && !pool->block_fmt) return KVD_ERR_INVALID;
     kvd::AppendParams p;
     p.k_new = static_cast<const uint16_t*>(k_new);
     p.v_new = static_cast<const uint16_t*>(v_new);
     p.slot_mapping = slot_mapping;
     p.kv = pool->mem + static_cast<size_t>(layer) * pool->layer_bytes;
     p.host_kv = pool->host_kv ? pool->host_kv + static_cast<size_t>(layer) * pool->host_layer_bytes : nullptr;
+    p.block_fmt = pool->block_fmt;
     p.err = pool->err;
     p.n_tokens = n_tokens;
     p.num_blocks = pool->desc.num_blocks;
     p.host_blocks = pool->host_blocks;
     p.n_kv = pool->desc.n_kv;
-    return cuda_status(kvd::launch_append(p, pool->desc.kv_dtype == KVD_FP8_E4M3, static_cast<cudaStream_t>(stream)));
+    return cuda_status(kvd::launch_append(p, pool_kind(pool), static_cast<cudaStream_t>(stream)));
 }
 
 static kvd_status check_decode_shape(const kvd_pool* pool, int n_q, int batch, int max_seq_len) {
@@ -400,8 +429,9 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     const int S = num_splits > 0 ? num_splits : plan_splits(pool, batch, max_seq_len, g);
     const WsLayout w = ws_layout(U, S, g);
     if (workspace_bytes < w.total) return KVD_ERR_NOMEM;
+    if (pool->desc.kv_dtype == KVD_MIXED && !pool->block_fmt) return KVD_ERR_INVALID;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    const bool fp8 = pool->desc.kv_dtype == KVD_FP8_E4M3;
+    const int kind = pool_kind(pool);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     kvd::DecodeParams p;
@@ -421,6 +451,7 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     p.block_table = block_table;
     p.seq_lens = seq_lens;
     p.retain = retain_mask;
+    p.block_fmt = pool->block_fmt;
     p.part_o = reinterpret_cast<float*>(ws + w.part_o);
     p.part_lse = reinterpret_cast<float*>(ws + w.part_lse);
     p.unit_first = reinterpret_cast<int32_t*>(ws + w.unit_first);
@@ -438,8 +469,8 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     p.max_seq_len = max_seq_len;
     p.early = (flags & KVD_EARLY_START) ? 1 : 0;
     p.scale_log2 = softmax_scale * kvd::kLog2e;
-    const int carveout = kvd::decode_carveout(fp8, batch, g);
-    cudaError_t e = kvd::launch_decode(p, fp8, carveout, s);
+    const int carveout = kvd::decode_carveout(kind, batch, g);
+    cudaError_t e = kvd::launch_decode(p, kind, carveout, s);
     if (e != cudaSuccess) return KVD_ERR_CUDA;
     if (!out) return KVD_OK;  // partials only: the caller merges them with kvd_combine_splits
 

@@ -16,7 +16,10 @@
 
 namespace kvd {
 
-template <bool FP8>
+// KIND: kKindBf16 / kKindFp8 (every block in the pool's one format) or kKindMixed (each
+// block's format read from the pool's per-block precision array; such a pool has no host tier
+// and every record slot is sized for BF16).
+template <int KIND>
 __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
     const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -32,21 +35,31 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
         return;
     }
     const int64_t row = (n * p.n_kv + h) * kDh;
-    constexpr int64_t kRec = FP8 ? kRecordFp8 : kRecordBf16;
+    constexpr int64_t kRec = KIND == kKindFp8 ? kRecordFp8 : kRecordBf16;
     // a host-tier block (id ≥ num_blocks) keeps its record in host memory
     uint8_t* record = blk < p.num_blocks ? p.kv + (blk * p.n_kv + h) * kRec
                                          : p.host_kv + ((blk - p.num_blocks) * p.n_kv + h) * kRec;
-    write_token<FP8>(record, t, p.k_new + row, p.v_new + row, lane);
+    if constexpr (KIND == kKindMixed) {
+        const int fmt = block_format(p.block_fmt[blk]);
+        if (fmt == kFmtBf16) write_token<kFmtBf16>(record, t, p.k_new + row, p.v_new + row, lane);
+        else if (fmt == kFmtE4m3) write_token<kFmtE4m3>(record, t, p.k_new + row, p.v_new + row, lane);
+        else if (fmt == kFmtE5m2) write_token<kFmtE5m2>(record, t, p.k_new + row, p.v_new + row, lane);
+        else if (lane == 0) report(p.err, KVD_ERR_OOB);   // not a precision code: the token is skipped
+    } else {
+        write_token<KIND == kKindFp8 ? kFmtE4m3 : kFmtBf16>(record, t, p.k_new + row, p.v_new + row, lane);
+    }
 }
 
-cudaError_t launch_append(const AppendParams& p, bool fp8, cudaStream_t stream) {
+cudaError_t launch_append(const AppendParams& p, int kind, cudaStream_t stream) {
     const int64_t warps = p.n_tokens * p.n_kv;
     const int threads = 256;
     const int64_t blocks = (warps * 32 + threads - 1) / threads;
-    if (fp8)
-        append_kernel<true><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(p);
+    if (kind == kKindFp8)
+        append_kernel<kKindFp8><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(p);
+    else if (kind == kKindMixed)
+        append_kernel<kKindMixed><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(p);
     else
-        append_kernel<false><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(p);
+        append_kernel<kKindBf16><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

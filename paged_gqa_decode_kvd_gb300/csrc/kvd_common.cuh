@@ -26,6 +26,15 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned kFull = 0xffffffffu;
 
+// Storage format of one block's K/V: BF16 values, or 8-bit codes (E4M3 / E5M2) with one fp32
+// scale per (token, KV head) for K and one for V.
+constexpr int kFmtBf16 = 0, kFmtE4m3 = 1, kFmtE5m2 = 2;
+// Internal format of a per-block precision byte of a mixed pool (KVD_BF16, KVD_FP8_E4M3 or
+// KVD_FP8_E5M2), or -1 for any other value.
+__host__ __device__ __forceinline__ int block_format(int code) {
+    return code == KVD_BF16 ? kFmtBf16 : code == KVD_FP8_E4M3 ? kFmtE4m3 : code == KVD_FP8_E5M2 ? kFmtE5m2 : -1;
+}
+
 // ---------------------------------------------------------------- fragment order
 // A 16-token × 128-dim tile is stored so that lane `lane` of a warp finds the
 // A-operand fragment of k-step (or m-tile) i of mma.m16n8k16 in one 16-byte
@@ -181,12 +190,14 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
 }
 
 // Write one token's K and V rows (128 bf16 each) into slot t of a pool record, by one
-// warp: lane l holds dims 4l..4l+3.  BF16 records store the values in fragment order;
-// FP8 records store e4m3(x / scale) with scale = fp32(absmax/448) (1 for a zero row),
-// per K and per V, the scales after the two tiles.
-template <bool FP8>
+// warp: lane l holds dims 4l..4l+3.  BF16 records (FMT kFmtBf16) store the values in
+// fragment order; 8-bit records store code(x / scale) with scale = fp32(absmax/top) (1 for a
+// zero row), top = 448 (E4M3) or 57,344 (E5M2), the largest finite value of the format,
+// codes rounded to nearest even and saturated, per K and per V, the scales after the two tiles.
+template <int FMT>
 __device__ __forceinline__ void write_token(uint8_t* record, int t, const uint16_t* krow, const uint16_t* vrow,
                                             int lane) {
+    constexpr bool FP8 = FMT != kFmtBf16;
     const uint2 kraw = *reinterpret_cast<const uint2*>(krow + lane * 4);
     const uint2 vraw = *reinterpret_cast<const uint2*>(vrow + lane * 4);
     const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(&kraw);
@@ -218,15 +229,17 @@ __device__ __forceinline__ void write_token(uint8_t* record, int t, const uint16
             kmax = fmaxf(kmax, __shfl_xor_sync(kFull, kmax, o));
             vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, o));
         }
-        const float ks = (kmax == 0.f) ? 1.f : __fdiv_rn(kmax, 448.f);
-        const float vs = (vmax == 0.f) ? 1.f : __fdiv_rn(vmax, 448.f);
+        constexpr float kTop = FMT == kFmtE5m2 ? 57344.f : 448.f;
+        constexpr __nv_fp8_interpretation_t kInterp = FMT == kFmtE5m2 ? __NV_E5M2 : __NV_E4M3;
+        const float ks = (kmax == 0.f) ? 1.f : __fdiv_rn(kmax, kTop);
+        const float vs = (vmax == 0.f) ? 1.f : __fdiv_rn(vmax, kTop);
         uint8_t* ktile = record;
         uint8_t* vtile = record + kTileFp8;
         #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int d = lane * 4 + j;
-            const uint8_t kc = __nv_cvt_float_to_fp8(__fdiv_rn(kx[j], ks), __NV_SATFINITE, __NV_E4M3);
-            const uint8_t vc = __nv_cvt_float_to_fp8(__fdiv_rn(vx[j], vs), __NV_SATFINITE, __NV_E4M3);
+            const uint8_t kc = __nv_cvt_float_to_fp8(__fdiv_rn(kx[j], ks), __NV_SATFINITE, kInterp);
+            const uint8_t vc = __nv_cvt_float_to_fp8(__fdiv_rn(vx[j], vs), __NV_SATFINITE, kInterp);
             int fl, fe;
             int i = k_frag_i(t, d, &fl, &fe);
             ktile[fp8_tile_index(i, fl, fe)] = kc;
@@ -280,6 +293,21 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint
         "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
         : "=r"(lo), "=r"(hi)
         : "r"(w));
+}
+
+// The same for four E5M2 codes (an E5M2 value is the upper byte of an f16 value).
+__device__ __forceinline__ void e5m2x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 a, b;\n\t"
+        "mov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e5m2x2 %0, a;\n\t"
+        "cvt.rn.f16x2.e5m2x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+template <int FMT>
+__device__ __forceinline__ void f8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    if constexpr (FMT == kFmtE5m2) e5m2x4_to_f16x2x2(w, lo, hi);
+    else e4m3x4_to_f16x2x2(w, lo, hi);
 }
 
 __device__ __forceinline__ void named_barrier(int id, int threads) {

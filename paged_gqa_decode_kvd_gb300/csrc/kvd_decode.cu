@@ -41,10 +41,11 @@ constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s
 // slots suffice for the register tree merge of the four consumer warps.
 __host__ __device__ inline int merge_floats(int g) { return g * kMergeStride + 2 * kMaxG; }
 
-template <bool FP8, int STAGES>
+template <int KIND, int STAGES>
 struct Cfg {
-    static constexpr int kTile = FP8 ? kTileFp8 : kTileBf16;
-    static constexpr int kRecord = FP8 ? kRecordFp8 : kRecordBf16;   // one bulk copy per (block, head)
+    // record slot of one (block, KV head): a mixed pool sizes every slot for BF16 and an 8-bit
+    // block fills the first kRecordFp8 bytes of it
+    static constexpr int kRecord = KIND == kKindFp8 ? kRecordFp8 : kRecordBf16;
     static constexpr int kStage = kRecord;
     // Stage k%kStages is consumed by warp (k - segment start) % kNcw.  With kStages a
     // multiple of kNcw every reuse of a stage inside a segment belongs to the same warp,
@@ -58,13 +59,13 @@ struct Smem {
     int ring_off, full_off, empty_off, meta_off, merge_off, pref_off, lens_off, abort_off, flag_off, total;
 };
 
-template <bool FP8, int S>
+template <int KIND, int S>
 __host__ __device__ inline Smem smem_layout(int batch, int g) {
-    constexpr int kStages = Cfg<FP8, S>::kStages;
+    constexpr int kStages = Cfg<KIND, S>::kStages;
     Smem s;
     int o = 0;
     s.ring_off = o;
-    o += kStages * Cfg<FP8, S>::kStage;
+    o += kStages * Cfg<KIND, S>::kStage;
     s.full_off = o;
     o += kStages * 8;
     s.empty_off = o;
@@ -201,14 +202,209 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, int64_t idx, fl
     }
 }
 
+// One 16-token block of a unit by one consumer warp: S^T = K·Q^T for the g query heads of the
+// group, online softmax (fp32, exp2 domain) and O^T += V^T·P^T.  FMT is the block's storage:
+// kFmtBf16 (bf16 tiles, bf16 MMAs, qf in bf16) or kFmtE4m3 / kFmtE5m2 (8-bit codes converted
+// exactly to f16, f16 MMAs, qf in f16; the K scale multiplies the fp32 logit and the V scale
+// folds into p).  m: the block's valid-slot mask (bits 0..15).  lg0 / lg1: logit rows of heads
+// h0 / h1 (or null), written at positions tb + slot below lim.  The stage is released (arrive
+// on empty_s) as soon as its V tile is in registers.
+template <int FMT>
+__device__ __forceinline__ void consume_block(const uint8_t* st, const uint32_t (&qf)[8][2], float (&o)[8][4],
+                                              float& m0, float& m1, float& s0, float& s1, uint32_t m,
+                                              float scale_log2, float* lg0, float* lg1, int tb, int64_t lim,
+                                              uint64_t* empty_s, int lane) {
+    const int gid = lane >> 2;   // token row (S^T) / dim row (O^T) within an 8-row group
+    const int tq = lane & 3;     // head pair 2tq, 2tq+1
+    // ---- S^T = K · Q^T  (16 tokens × 8 heads) ----
+    float ca[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
+    float fk0, fk1, fv0 = 1.f, fv1 = 1.f;
+    if constexpr (FMT == kFmtBf16) {
+        const uint4* kt = reinterpret_cast<const uint4*>(st);
+        #pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            const uint4 a0 = kt[i * 32 + lane];
+            const uint4 a1 = kt[(i + 1) * 32 + lane];
+            const uint32_t fa[4] = {a0.x, a0.y, a0.z, a0.w};
+            const uint32_t fb[4] = {a1.x, a1.y, a1.z, a1.w};
+            mma_bf16(ca, fa, qf[i][0], qf[i][1]);
+            mma_bf16(cb, fb, qf[i + 1][0], qf[i + 1][1]);
+        }
+        fk0 = fk1 = scale_log2;
+    } else {
+        const uint4* kt = reinterpret_cast<const uint4*>(st);
+        #pragma unroll
+        for (int u4 = 0; u4 < 4; ++u4) {
+            const uint4 w = kt[u4 * 32 + lane];
+            uint32_t fa[4], fb[4];
+            f8x4_to_f16x2x2<FMT>(w.x, fa[0], fa[1]);
+            f8x4_to_f16x2x2<FMT>(w.y, fa[2], fa[3]);
+            f8x4_to_f16x2x2<FMT>(w.z, fb[0], fb[1]);
+            f8x4_to_f16x2x2<FMT>(w.w, fb[2], fb[3]);
+            mma_f16(ca, fa, qf[2 * u4][0], qf[2 * u4][1]);
+            mma_f16(cb, fb, qf[2 * u4 + 1][0], qf[2 * u4 + 1][1]);
+        }
+        const float* sc = reinterpret_cast<const float*>(st + 2 * kTileFp8);
+        fk0 = sc[gid] * scale_log2;
+        fk1 = sc[gid + 8] * scale_log2;
+        fv0 = sc[kBs + gid];
+        fv1 = sc[kBs + gid + 8];
+    }
+    const bool v0 = (m >> gid) & 1u;        // token gid
+    const bool v1 = (m >> (gid + 8)) & 1u;  // token gid + 8
+    float l0 = v0 ? (ca[0] + cb[0]) * fk0 : -INFINITY;  // (gid,   h0)
+    float l1 = v0 ? (ca[1] + cb[1]) * fk0 : -INFINITY;  // (gid,   h1)
+    float l2 = v1 ? (ca[2] + cb[2]) * fk1 : -INFINITY;  // (gid+8, h0)
+    float l3 = v1 ? (ca[3] + cb[3]) * fk1 : -INFINITY;  // (gid+8, h1)
+
+    {
+        const int t0 = tb + gid, t1 = t0 + 8;
+        if (lg0) {
+            if (t0 < lim) lg0[t0] = l0 * kLn2;
+            if (t1 < lim) lg0[t1] = l2 * kLn2;
+        }
+        if (lg1) {
+            if (t0 < lim) lg1[t0] = l1 * kLn2;
+            if (t1 < lim) lg1[t1] = l3 * kLn2;
+        }
+    }
+
+    // ---- online softmax (exp2 domain), heads h0 and h1 ----
+    float bm0 = fmaxf(l0, l2), bm1 = fmaxf(l1, l3);
+    #pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, off));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, off));
+    }
+    const float n0 = fmaxf(m0, bm0), n1 = fmaxf(m1, bm1);
+    const float z0 = n0 == -INFINITY ? 0.f : n0;
+    const float z1 = n1 == -INFINITY ? 0.f : n1;
+    const float c0 = ex2(m0 - z0), c1 = ex2(m1 - z1);   // 0 when m was −inf
+    const float p0 = ex2(l0 - z0), p1 = ex2(l1 - z1), p2 = ex2(l2 - z0), p3 = ex2(l3 - z1);
+    s0 = s0 * c0 + (p0 + p2);
+    s1 = s1 * c1 + (p1 + p3);
+    m0 = n0;
+    m1 = n1;
+    if (__any_sync(kFull, c0 != 1.f || c1 != 1.f)) {
+        #pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            o[i][0] *= c0;
+            o[i][1] *= c1;
+            o[i][2] *= c0;
+            o[i][3] *= c1;
+        }
+    }
+
+    // ---- P^T fragment: rows = tokens, cols = heads -> transpose ----
+    // p goes to the MMA as a 16-bit value plus the 16-bit value of its rounding remainder
+    // (two MMAs): about 2^-17 (bf16) or 2^-22 (f16) relative per term.  A single 16-bit
+    // p (2^-9 bf16, 2^-11 f16) lets outputs that cancel (few dominant positions, or FP8
+    // channels 20x the others) lose more than the output tolerance.  FP8 folds the V
+    // scale into p first.
+    uint32_t pb0, pb1, pl0, pl1;
+    if constexpr (FMT == kFmtBf16) {
+        const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
+        const float2 r01 = unpack_bf16(h01), r23 = unpack_bf16(h23);
+        pb0 = movmatrix_t(h01);
+        pb1 = movmatrix_t(h23);
+        pl0 = movmatrix_t(pack_bf16(p0 - r01.x, p1 - r01.y));
+        pl1 = movmatrix_t(pack_bf16(p2 - r23.x, p3 - r23.y));
+    } else {
+        const float w0 = v0 ? fv0 : 0.f, w1 = v1 ? fv1 : 0.f;
+        const float a0 = p0 * w0, a1 = p1 * w0, a2 = p2 * w1, a3 = p3 * w1;
+        const uint32_t h01 = pack_f16(a0, a1), h23 = pack_f16(a2, a3);
+        const float2 r01 = unpack_f16(h01), r23 = unpack_f16(h23);
+        pb0 = movmatrix_t(h01);
+        pb1 = movmatrix_t(h23);
+        pl0 = movmatrix_t(pack_f16(a0 - r01.x, a1 - r01.y));
+        pl1 = movmatrix_t(pack_f16(a2 - r23.x, a3 - r23.y));
+    }
+
+    // ---- O^T += V^T · P^T ----
+    // A block with an invalid slot (context tail, evicted) zeroes that slot's V in
+    // this lane's fragment, so garbage (NaN) in unused slots cannot reach the output
+    // through 0·NaN; full blocks (warp-uniform test) skip the masking.
+    const bool partial = (m & 0xFFFFu) != 0xFFFFu;
+    const int ta = 2 * tq;
+    if constexpr (FMT == kFmtBf16) {
+        const uint4* vt = reinterpret_cast<const uint4*>(st + kTileBf16);
+        uint4 vv[8];
+        #pragma unroll
+        for (int i = 0; i < 8; ++i) vv[i] = vt[i * 32 + lane];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_s);
+        if (partial) {   // 16-bit halves: tokens (2tq, 2tq+1) in .x/.y, (2tq+8, 2tq+9) in .z/.w
+            const uint32_t zlo = (((m >> ta) & 1u) ? 0x0000FFFFu : 0u) | (((m >> (ta + 1)) & 1u) ? 0xFFFF0000u : 0u);
+            const uint32_t zhi =
+                (((m >> (ta + 8)) & 1u) ? 0x0000FFFFu : 0u) | (((m >> (ta + 9)) & 1u) ? 0xFFFF0000u : 0u);
+            #pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                vv[i].x &= zlo;
+                vv[i].y &= zlo;
+                vv[i].z &= zhi;
+                vv[i].w &= zhi;
+            }
+        }
+        #pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t fa[4] = {vv[i].x, vv[i].y, vv[i].z, vv[i].w};
+            mma_bf16(o[i], fa, pb0, pb1);
+            mma_bf16(o[i], fa, pl0, pl1);
+        }
+    } else {
+        const uint4* vt = reinterpret_cast<const uint4*>(st + kTileFp8);
+        uint32_t zlo = 0xFFFFFFFFu, zhi = 0xFFFFFFFFu;
+        if (partial) {   // bytes: tokens (2tq, 2tq+1) in .x/.z, (2tq+8, 2tq+9) in .y/.w; code 0 = +0
+            zlo = (((m >> ta) & 1u) ? 0x00FFu : 0u) | (((m >> (ta + 1)) & 1u) ? 0xFF00u : 0u);
+            zhi = (((m >> (ta + 8)) & 1u) ? 0x00FFu : 0u) | (((m >> (ta + 9)) & 1u) ? 0xFF00u : 0u);
+            zlo |= zlo << 16;
+            zhi |= zhi << 16;
+        }
+        // two halves of four m-tiles each keep fewer V registers live
+        #pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            uint4 vv[2];
+            vv[0] = vt[(2 * half) * 32 + lane];
+            vv[1] = vt[(2 * half + 1) * 32 + lane];
+            if (half == 1) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_s);
+            }
+            if (partial) {
+                #pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    vv[i].x &= zlo;
+                    vv[i].y &= zhi;
+                    vv[i].z &= zlo;
+                    vv[i].w &= zhi;
+                }
+            }
+            #pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int u4 = 2 * half + i;
+                uint32_t fa[4], fb[4];
+                f8x4_to_f16x2x2<FMT>(vv[i].x, fa[0], fa[1]);
+                f8x4_to_f16x2x2<FMT>(vv[i].y, fa[2], fa[3]);
+                f8x4_to_f16x2x2<FMT>(vv[i].z, fb[0], fb[1]);
+                f8x4_to_f16x2x2<FMT>(vv[i].w, fb[2], fb[3]);
+                mma_f16(o[2 * u4], fa, pb0, pb1);
+                mma_f16(o[2 * u4 + 1], fb, pb0, pb1);
+                mma_f16(o[2 * u4], fa, pl0, pl1);
+                mma_f16(o[2 * u4 + 1], fb, pl0, pl1);
+            }
+        }
+    }
+}
+
 // DIRECT: the pool's host-tier blocks are read in place from host memory (lsu_fill); only
 // pools with such a tier launch this variant, so the others carry none of its code.
-template <bool FP8, int S, bool DIRECT>
-__global__ void __launch_bounds__(kThreads, FP8 && S == 8 ? 4 : 3) decode_kernel(const DecodeParams p) {
+template <int KIND, int S, bool DIRECT>
+__global__ void __launch_bounds__(kThreads, KIND == kKindFp8 && S == 8 ? 4 : KIND == kKindMixed ? 2 : 3)
+    decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    using C = Cfg<FP8, S>;
+    using C = Cfg<KIND, S>;
     constexpr int kStages = C::kStages;
-    const Smem L = smem_layout<FP8, S>(p.B, p.g);
+    const Smem L = smem_layout<KIND, S>(p.B, p.g);
     uint8_t* ring = smem + L.ring_off;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full_off);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty_off);
@@ -323,11 +519,19 @@ __global__ void __launch_bounds__(kThreads, FP8 && S == 8 ? 4 : 3) decode_kernel
                 if (ph >= 0 && ph < p.num_blocks + p.host_blocks) {
                     const int64_t row = (static_cast<int64_t>(sg.b) * p.n_kv + sg.kvh) * kDh;
                     uint8_t* rec = const_cast<uint8_t*>(record_of<C::kRecord>(p, ph, sg.kvh));
-                    write_token<FP8>(rec, pos % kBs, p.k_new + row, p.v_new + row, lane);
-                    if (ph >= p.num_blocks && !p.host_direct)   // a staged host-tier block: its host record too
-                        write_token<FP8>(p.host_kv + ((static_cast<int64_t>(ph) - p.num_blocks) * p.n_kv + sg.kvh) *
-                                                         C::kRecord,
-                                         pos % kBs, p.k_new + row, p.v_new + row, lane);
+                    if constexpr (KIND == kKindMixed) {   // the block's own format (no host tier)
+                        const int fmt = ph < p.num_blocks ? block_format(p.block_fmt[ph]) : -1;
+                        if (fmt == kFmtBf16) write_token<kFmtBf16>(rec, pos % kBs, p.k_new + row, p.v_new + row, lane);
+                        else if (fmt == kFmtE4m3) write_token<kFmtE4m3>(rec, pos % kBs, p.k_new + row, p.v_new + row, lane);
+                        else if (fmt == kFmtE5m2) write_token<kFmtE5m2>(rec, pos % kBs, p.k_new + row, p.v_new + row, lane);
+                    } else {
+                        constexpr int kF = KIND == kKindFp8 ? kFmtE4m3 : kFmtBf16;
+                        write_token<kF>(rec, pos % kBs, p.k_new + row, p.v_new + row, lane);
+                        if (ph >= p.num_blocks && !p.host_direct)   // a staged host-tier block: its host record too
+                            write_token<kF>(p.host_kv + ((static_cast<int64_t>(ph) - p.num_blocks) * p.n_kv + sg.kvh) *
+                                                            C::kRecord,
+                                            pos % kBs, p.k_new + row, p.v_new + row, lane);
+                    }
                     fence_proxy_async_global();
                 }
                 __syncwarp();
@@ -347,6 +551,15 @@ __global__ void __launch_bounds__(kThreads, FP8 && S == 8 ? 4 : 3) decode_kernel
                         vm = valid >= kBs ? 0xFFFFu : ((1u << valid) - 1u);
                         if (p.retain) vm &= p.retain[phys];
                         vm |= 1u << 16;
+                        if constexpr (KIND == kKindMixed) {   // the block's precision, bits 17-18
+                            const int fmt = block_format(p.block_fmt[phys]);
+                            if (fmt < 0) {
+                                vm = 0;
+                                report(p.err, KVD_ERR_OOB);
+                            } else {
+                                vm |= static_cast<uint32_t>(fmt) << 17;
+                            }
+                        }
                     } else {
                         report(p.err, KVD_ERR_OOB);
                     }
@@ -380,8 +593,11 @@ __global__ void __launch_bounds__(kThreads, FP8 && S == 8 ? 4 : 3) decode_kernel
                                     fence_proxy_async_shared();
                                     lsu_filled &= ~(1u << s);
                                 }
-                                mbar_arrive_expect_tx(&full[s], C::kRecord);
-                                bulk_g2s(dst, rec, C::kRecord, &full[s], policy);
+                                // a mixed pool's 8-bit block fills only the first kRecordFp8 bytes of its slot
+                                const uint32_t bytes =
+                                    KIND == kKindMixed && ((m >> 17) & 3u) != kFmtBf16 ? kRecordFp8 : C::kRecord;
+                                mbar_arrive_expect_tx(&full[s], bytes);
+                                bulk_g2s(dst, rec, bytes, &full[s], policy);
                             } else {
                                 mbar_arrive(&full[s]);
                             }
@@ -423,8 +639,10 @@ __global__ void __launch_bounds__(kThreads, FP8 && S == 8 ? 4 : 3) decode_kernel
         const int len = lens[sg.b];
         const int u = sg.b * p.n_kv + sg.kvh;
 
-        // Q^T fragments (B operand): head gid, dims 16i + 2tq + {0,1,8,9}.
+        // Q^T fragments (B operand): head gid, dims 16i + 2tq + {0,1,8,9}; in f16 for 8-bit
+        // blocks (qf), in bf16 for BF16 blocks (qf of a BF16 pool, qfb of a mixed pool).
         uint32_t qf[8][2];
+        uint32_t qfb[8][2];
         {
             const uint16_t* qh = p.q + (static_cast<int64_t>(sg.b) * p.n_q + sg.kvh * g + gid) * kDh;
             #pragma unroll
@@ -434,7 +652,11 @@ __global__ void __launch_bounds__(kThreads, FP8 && S == 8 ? 4 : 3) decode_kernel
                     lo2 = *reinterpret_cast<const uint32_t*>(qh + 16 * i + 2 * tq);
                     hi2 = *reinterpret_cast<const uint32_t*>(qh + 16 * i + 2 * tq + 8);
                 }
-                if constexpr (FP8) {  // bf16 -> f16 (exact inside the f16 range)
+                if constexpr (KIND == kKindMixed) {
+                    qfb[i][0] = lo2;
+                    qfb[i][1] = hi2;
+                }
+                if constexpr (KIND != kKindBf16) {  // bf16 -> f16 (exact inside the f16 range)
                     const __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&lo2);
                     const __nv_bfloat162 c = *reinterpret_cast<__nv_bfloat162*>(&hi2);
                     lo2 = pack_f16(__low2float(a), __high2float(a));
@@ -458,6 +680,7 @@ __global__ void __launch_bounds__(kThreads, FP8 && S == 8 ? 4 : 3) decode_kernel
             lg0 = h0 < g ? p.logits + (rowb + h0) * p.logits_stride : nullptr;
             lg1 = h1 < g ? p.logits + (rowb + h1) * p.logits_stride : nullptr;
         }
+        const int64_t lim = len < p.logits_stride ? len : p.logits_stride;
 
         for (int kk = warp; kk < nseg; kk += kNcw) {
             const uint32_t kg = k + kk;
@@ -481,184 +704,21 @@ __global__ void __launch_bounds__(kThreads, FP8 && S == 8 ? 4 : 3) decode_kernel
             const uint8_t* st = ring + s * C::kStage;
             const int j = sg.j0 + kk;
 
-            // ---- S^T = K · Q^T  (16 tokens × 8 heads) ----
-            float ca[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
-            float fk0, fk1, fv0 = 1.f, fv1 = 1.f;
-            if constexpr (!FP8) {
-                const uint4* kt = reinterpret_cast<const uint4*>(st);
-                #pragma unroll
-                for (int i = 0; i < 8; i += 2) {
-                    const uint4 a0 = kt[i * 32 + lane];
-                    const uint4 a1 = kt[(i + 1) * 32 + lane];
-                    const uint32_t fa[4] = {a0.x, a0.y, a0.z, a0.w};
-                    const uint32_t fb[4] = {a1.x, a1.y, a1.z, a1.w};
-                    mma_bf16(ca, fa, qf[i][0], qf[i][1]);
-                    mma_bf16(cb, fb, qf[i + 1][0], qf[i + 1][1]);
-                }
-                fk0 = fk1 = p.scale_log2;
+            const int tb = j * kBs;
+            if constexpr (KIND == kKindMixed) {
+                const uint32_t fmt = (m >> 17) & 3u;
+                if (fmt == kFmtBf16)
+                    consume_block<kFmtBf16>(st, qfb, o, m0, m1, s0, s1, m, p.scale_log2, lg0, lg1, tb, lim, &empty[s],
+                                            lane);
+                else if (fmt == kFmtE4m3)
+                    consume_block<kFmtE4m3>(st, qf, o, m0, m1, s0, s1, m, p.scale_log2, lg0, lg1, tb, lim, &empty[s],
+                                            lane);
+                else
+                    consume_block<kFmtE5m2>(st, qf, o, m0, m1, s0, s1, m, p.scale_log2, lg0, lg1, tb, lim, &empty[s],
+                                            lane);
             } else {
-                const uint4* kt = reinterpret_cast<const uint4*>(st);
-                #pragma unroll
-                for (int u4 = 0; u4 < 4; ++u4) {
-                    const uint4 w = kt[u4 * 32 + lane];
-                    uint32_t fa[4], fb[4];
-                    e4m3x4_to_f16x2x2(w.x, fa[0], fa[1]);
-                    e4m3x4_to_f16x2x2(w.y, fa[2], fa[3]);
-                    e4m3x4_to_f16x2x2(w.z, fb[0], fb[1]);
-                    e4m3x4_to_f16x2x2(w.w, fb[2], fb[3]);
-                    mma_f16(ca, fa, qf[2 * u4][0], qf[2 * u4][1]);
-                    mma_f16(cb, fb, qf[2 * u4 + 1][0], qf[2 * u4 + 1][1]);
-                }
-                const float* sc = reinterpret_cast<const float*>(st + 2 * kTileFp8);
-                fk0 = sc[gid] * p.scale_log2;
-                fk1 = sc[gid + 8] * p.scale_log2;
-                fv0 = sc[kBs + gid];
-                fv1 = sc[kBs + gid + 8];
-            }
-            const bool v0 = (m >> gid) & 1u;        // token gid
-            const bool v1 = (m >> (gid + 8)) & 1u;  // token gid + 8
-            float l0 = v0 ? (ca[0] + cb[0]) * fk0 : -INFINITY;  // (gid,   h0)
-            float l1 = v0 ? (ca[1] + cb[1]) * fk0 : -INFINITY;  // (gid,   h1)
-            float l2 = v1 ? (ca[2] + cb[2]) * fk1 : -INFINITY;  // (gid+8, h0)
-            float l3 = v1 ? (ca[3] + cb[3]) * fk1 : -INFINITY;  // (gid+8, h1)
-
-            if (p.logits) {
-                const int t0 = j * kBs + gid, t1 = t0 + 8;
-                const int64_t lim = len < p.logits_stride ? len : p.logits_stride;
-                if (lg0) {
-                    if (t0 < lim) lg0[t0] = l0 * kLn2;
-                    if (t1 < lim) lg0[t1] = l2 * kLn2;
-                }
-                if (lg1) {
-                    if (t0 < lim) lg1[t0] = l1 * kLn2;
-                    if (t1 < lim) lg1[t1] = l3 * kLn2;
-                }
-            }
-
-            // ---- online softmax (exp2 domain), heads h0 and h1 ----
-            float bm0 = fmaxf(l0, l2), bm1 = fmaxf(l1, l3);
-            #pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, off));
-                bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, off));
-            }
-            const float n0 = fmaxf(m0, bm0), n1 = fmaxf(m1, bm1);
-            const float z0 = n0 == -INFINITY ? 0.f : n0;
-            const float z1 = n1 == -INFINITY ? 0.f : n1;
-            const float c0 = ex2(m0 - z0), c1 = ex2(m1 - z1);   // 0 when m was −inf
-            const float p0 = ex2(l0 - z0), p1 = ex2(l1 - z1), p2 = ex2(l2 - z0), p3 = ex2(l3 - z1);
-            s0 = s0 * c0 + (p0 + p2);
-            s1 = s1 * c1 + (p1 + p3);
-            m0 = n0;
-            m1 = n1;
-            if (__any_sync(kFull, c0 != 1.f || c1 != 1.f)) {
-                #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    o[i][0] *= c0;
-                    o[i][1] *= c1;
-                    o[i][2] *= c0;
-                    o[i][3] *= c1;
-                }
-            }
-
-            // ---- P^T fragment: rows = tokens, cols = heads -> transpose ----
-            // p goes to the MMA as a 16-bit value plus the 16-bit value of its rounding remainder
-            // (two MMAs): about 2^-17 (bf16) or 2^-22 (f16) relative per term.  A single 16-bit
-            // p (2^-9 bf16, 2^-11 f16) lets outputs that cancel (few dominant positions, or FP8
-            // channels 20x the others) lose more than the output tolerance.  FP8 folds the V
-            // scale into p first.
-            uint32_t pb0, pb1, pl0, pl1;
-            if constexpr (!FP8) {
-                const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
-                const float2 r01 = unpack_bf16(h01), r23 = unpack_bf16(h23);
-                pb0 = movmatrix_t(h01);
-                pb1 = movmatrix_t(h23);
-                pl0 = movmatrix_t(pack_bf16(p0 - r01.x, p1 - r01.y));
-                pl1 = movmatrix_t(pack_bf16(p2 - r23.x, p3 - r23.y));
-            } else {
-                const float w0 = v0 ? fv0 : 0.f, w1 = v1 ? fv1 : 0.f;
-                const float a0 = p0 * w0, a1 = p1 * w0, a2 = p2 * w1, a3 = p3 * w1;
-                const uint32_t h01 = pack_f16(a0, a1), h23 = pack_f16(a2, a3);
-                const float2 r01 = unpack_f16(h01), r23 = unpack_f16(h23);
-                pb0 = movmatrix_t(h01);
-                pb1 = movmatrix_t(h23);
-                pl0 = movmatrix_t(pack_f16(a0 - r01.x, a1 - r01.y));
-                pl1 = movmatrix_t(pack_f16(a2 - r23.x, a3 - r23.y));
-            }
-
-            // ---- O^T += V^T · P^T ----
-            // A block with an invalid slot (context tail, evicted) zeroes that slot's V in
-            // this lane's fragment, so garbage (NaN) in unused slots cannot reach the output
-            // through 0·NaN; full blocks (warp-uniform test) skip the masking.
-            const bool partial = (m & 0xFFFFu) != 0xFFFFu;
-            const int ta = 2 * tq;
-            if constexpr (!FP8) {
-                const uint4* vt = reinterpret_cast<const uint4*>(st + C::kTile);
-                uint4 vv[8];
-                #pragma unroll
-                for (int i = 0; i < 8; ++i) vv[i] = vt[i * 32 + lane];
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-                if (partial) {   // 16-bit halves: tokens (2tq, 2tq+1) in .x/.y, (2tq+8, 2tq+9) in .z/.w
-                    const uint32_t zlo = (((m >> ta) & 1u) ? 0x0000FFFFu : 0u) | (((m >> (ta + 1)) & 1u) ? 0xFFFF0000u : 0u);
-                    const uint32_t zhi =
-                        (((m >> (ta + 8)) & 1u) ? 0x0000FFFFu : 0u) | (((m >> (ta + 9)) & 1u) ? 0xFFFF0000u : 0u);
-                    #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        vv[i].x &= zlo;
-                        vv[i].y &= zlo;
-                        vv[i].z &= zhi;
-                        vv[i].w &= zhi;
-                    }
-                }
-                #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t fa[4] = {vv[i].x, vv[i].y, vv[i].z, vv[i].w};
-                    mma_bf16(o[i], fa, pb0, pb1);
-                    mma_bf16(o[i], fa, pl0, pl1);
-                }
-            } else {
-                const uint4* vt = reinterpret_cast<const uint4*>(st + C::kTile);
-                uint32_t zlo = 0xFFFFFFFFu, zhi = 0xFFFFFFFFu;
-                if (partial) {   // bytes: tokens (2tq, 2tq+1) in .x/.z, (2tq+8, 2tq+9) in .y/.w; code 0 = +0
-                    zlo = (((m >> ta) & 1u) ? 0x00FFu : 0u) | (((m >> (ta + 1)) & 1u) ? 0xFF00u : 0u);
-                    zhi = (((m >> (ta + 8)) & 1u) ? 0x00FFu : 0u) | (((m >> (ta + 9)) & 1u) ? 0xFF00u : 0u);
-                    zlo |= zlo << 16;
-                    zhi |= zhi << 16;
-                }
-                // two halves of four m-tiles each keep fewer V registers live
-                #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint4 vv[2];
-                    vv[0] = vt[(2 * half) * 32 + lane];
-                    vv[1] = vt[(2 * half + 1) * 32 + lane];
-                    if (half == 1) {
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&empty[s]);
-                    }
-                    if (partial) {
-                        #pragma unroll
-                        for (int i = 0; i < 2; ++i) {
-                            vv[i].x &= zlo;
-                            vv[i].y &= zhi;
-                            vv[i].z &= zlo;
-                            vv[i].w &= zhi;
-                        }
-                    }
-                    #pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        const int u4 = 2 * half + i;
-                        uint32_t fa[4], fb[4];
-                        e4m3x4_to_f16x2x2(vv[i].x, fa[0], fa[1]);
-                        e4m3x4_to_f16x2x2(vv[i].y, fa[2], fa[3]);
-                        e4m3x4_to_f16x2x2(vv[i].z, fb[0], fb[1]);
-                        e4m3x4_to_f16x2x2(vv[i].w, fb[2], fb[3]);
-                        mma_f16(o[2 * u4], fa, pb0, pb1);
-                        mma_f16(o[2 * u4 + 1], fb, pb0, pb1);
-                        mma_f16(o[2 * u4], fa, pl0, pl1);
-                        mma_f16(o[2 * u4 + 1], fb, pl0, pl1);
-                    }
-                }
+                consume_block<KIND == kKindFp8 ? kFmtE4m3 : kFmtBf16>(st, qf, o, m0, m1, s0, s1, m, p.scale_log2, lg0,
+                                                                     lg1, tb, lim, &empty[s], lane);
             }
         }
         k += nseg;
@@ -801,87 +861,95 @@ static bool smem_attrs(int* per_sm, int* reserved) {
     return c_per_sm > 0;
 }
 
-// Ring depth of a call.  BF16: 8 stages (8 KB records, 3 CTAs/SM).  FP8: 16 stages when three
+// Mixed pools: 12 stages of 8 KB record slots, two CTAs an SM (the kernel holds a bf16 and an
+// f16 copy of q, 168 registers); an 8-bit block fills only half a stage.
+constexpr int kMixedStages = 12;
+
+// Ring depth of a call.  BF16: 8 stages (8 KB records).  FP8: 16 stages when three
 // such CTAs fit an SM (the per-request arrays are small enough), else 8 stages (4 CTAs/SM).
 // With 16 the CTA keeps twice the bytes in flight; measured on GB300 it is 1% faster for one
 // or eight long requests and equal for 32 requests of 8,192 tokens.  The 16-stage variant runs
 // three CTAs per SM anyway, so its launch bounds let it use 128 registers (the 8-stage one,
 // four per SM, gets 96); without spills it is another 1% faster on one long request.
-static int decode_stages(bool fp8, int batch, int g) {
-    if (!fp8) return 8;
+static int decode_stages(int kind, int batch, int g) {
+    if (kind != kKindFp8) return 8;
     int per_sm = 0, reserved = 0;
     if (!smem_attrs(&per_sm, &reserved)) return 8;
-    const int64_t need = 3 * (static_cast<int64_t>(smem_layout<true, 16>(batch, g).total) + reserved);
+    const int64_t need = 3 * (static_cast<int64_t>(smem_layout<kKindFp8, 16>(batch, g).total) + reserved);
     return need <= per_sm ? 16 : 8;
 }
 
 // Raise the kernel's dynamic shared-memory limit once per device to the largest
 // layout any batch size can need (batch ≤ kMaxBatch).
-template <bool FP8, int S, bool DIRECT>
+template <int KIND, int S, bool DIRECT>
 static cudaError_t ensure_smem_attr() {
     static int done_for_device = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (done_for_device == dev) return cudaSuccess;
-    e = cudaFuncSetAttribute(decode_kernel<FP8, S, DIRECT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_layout<FP8, S>(kMaxBatch, kMaxG).total);
+    e = cudaFuncSetAttribute(decode_kernel<KIND, S, DIRECT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_layout<KIND, S>(kMaxBatch, kMaxG).total);
     if (e == cudaSuccess) done_for_device = dev;
     return e;
 }
 
-template <bool FP8, int S>
+template <int KIND, int S>
 static int ctas_per_sm_impl(int batch, int g) {
-    const int smem = smem_layout<FP8, S>(batch, g).total;
-    if (ensure_smem_attr<FP8, S, false>() != cudaSuccess) return 1;
+    const int smem = smem_layout<KIND, S>(batch, g).total;
+    if (ensure_smem_attr<KIND, S, false>() != cudaSuccess) return 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<FP8, S, false>, kThreads, smem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<KIND, S, false>, kThreads, smem) != cudaSuccess)
         return 1;
     return n > 0 ? n : 1;
 }
 
-size_t decode_smem_bytes(bool fp8, int batch, int g) {
-    if (!fp8) return smem_layout<false, 8>(batch, g).total;
-    return decode_stages(true, batch, g) == 16 ? smem_layout<true, 16>(batch, g).total
-                                               : smem_layout<true, 8>(batch, g).total;
+size_t decode_smem_bytes(int kind, int batch, int g) {
+    if (kind == kKindBf16) return smem_layout<kKindBf16, 8>(batch, g).total;
+    if (kind == kKindMixed) return smem_layout<kKindMixed, kMixedStages>(batch, g).total;
+    return decode_stages(kind, batch, g) == 16 ? smem_layout<kKindFp8, 16>(batch, g).total
+                                               : smem_layout<kKindFp8, 8>(batch, g).total;
 }
 
-int decode_ctas_per_sm(bool fp8, int batch, int g) {
-    if (!fp8) return ctas_per_sm_impl<false, 8>(batch, g);
-    return decode_stages(true, batch, g) == 16 ? ctas_per_sm_impl<true, 16>(batch, g)
-                                               : ctas_per_sm_impl<true, 8>(batch, g);
+int decode_ctas_per_sm(int kind, int batch, int g) {
+    if (kind == kKindBf16) return ctas_per_sm_impl<kKindBf16, 8>(batch, g);
+    if (kind == kKindMixed) return ctas_per_sm_impl<kKindMixed, kMixedStages>(batch, g);
+    return decode_stages(kind, batch, g) == 16 ? ctas_per_sm_impl<kKindFp8, 16>(batch, g)
+                                               : ctas_per_sm_impl<kKindFp8, 8>(batch, g);
 }
 
 // Shared-memory carveout (percent of the SM's shared memory) that holds a full complement
 // of decode CTAs, each with the per-block reservation; -1 if the device cannot be queried.
-int decode_carveout(bool fp8, int batch, int g) {
+int decode_carveout(int kind, int batch, int g) {
     int per_sm = 0, reserved = 0;
     if (!smem_attrs(&per_sm, &reserved)) return -1;
-    const int64_t need = static_cast<int64_t>(decode_ctas_per_sm(fp8, batch, g)) *
-                         (static_cast<int64_t>(decode_smem_bytes(fp8, batch, g)) + reserved);
+    const int64_t need = static_cast<int64_t>(decode_ctas_per_sm(kind, batch, g)) *
+                         (static_cast<int64_t>(decode_smem_bytes(kind, batch, g)) + reserved);
     const int64_t pct = (100 * need + per_sm - 1) / per_sm;
     return static_cast<int>(pct > 100 ? 100 : pct);
 }
 
-template <bool FP8, int S, bool DIRECT>
+template <int KIND, int S, bool DIRECT>
 static cudaError_t launch_variant(const DecodeParams& p, int carveout, cudaStream_t stream) {
-    const cudaError_t e = ensure_smem_attr<FP8, S, DIRECT>();
+    const cudaError_t e = ensure_smem_attr<KIND, S, DIRECT>();
     if (e != cudaSuccess) return e;
-    const size_t smem = smem_layout<FP8, S>(p.B, p.g).total;
-    return launch_dependent(decode_kernel<FP8, S, DIRECT>, dim3(p.nsplit), dim3(kThreads), smem, carveout, stream,
+    const size_t smem = smem_layout<KIND, S>(p.B, p.g).total;
+    return launch_dependent(decode_kernel<KIND, S, DIRECT>, dim3(p.nsplit), dim3(kThreads), smem, carveout, stream,
                             p);
 }
 
 template <bool DIRECT>
-static cudaError_t launch_decode_impl(const DecodeParams& p, bool fp8, int carveout, cudaStream_t stream) {
-    if (!fp8) return launch_variant<false, 8, DIRECT>(p, carveout, stream);
-    return decode_stages(true, p.B, p.g) == 16 ? launch_variant<true, 16, DIRECT>(p, carveout, stream)
-                                               : launch_variant<true, 8, DIRECT>(p, carveout, stream);
+static cudaError_t launch_decode_impl(const DecodeParams& p, int kind, int carveout, cudaStream_t stream) {
+    if (kind == kKindBf16) return launch_variant<kKindBf16, 8, DIRECT>(p, carveout, stream);
+    return decode_stages(kind, p.B, p.g) == 16 ? launch_variant<kKindFp8, 16, DIRECT>(p, carveout, stream)
+                                               : launch_variant<kKindFp8, 8, DIRECT>(p, carveout, stream);
 }
 
-cudaError_t launch_decode(const DecodeParams& p, bool fp8, int carveout, cudaStream_t stream) {
-    return p.host_direct && p.host_blocks > 0 ? launch_decode_impl<true>(p, fp8, carveout, stream)
-                                              : launch_decode_impl<false>(p, fp8, carveout, stream);
+cudaError_t launch_decode(const DecodeParams& p, int kind, int carveout, cudaStream_t stream) {
+    // a mixed pool has no host tier
+    if (kind == kKindMixed) return launch_variant<kKindMixed, kMixedStages, false>(p, carveout, stream);
+    return p.host_direct && p.host_blocks > 0 ? launch_decode_impl<true>(p, kind, carveout, stream)
+                                              : launch_decode_impl<false>(p, kind, carveout, stream);
 }
 
 // ---------------------------------------------------------------- wait self-test

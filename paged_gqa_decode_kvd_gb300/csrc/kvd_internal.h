@@ -8,6 +8,9 @@ struct kvd_pool;
 
 namespace kvd {
 
+// Pool kinds: every block BF16, every block FP8-E4M3, or mixed (a precision byte per block).
+constexpr int kKindBf16 = 0, kKindFp8 = 1, kKindMixed = 2;
+
 // Device ordinal the pool was created on (its memory and state live there).
 int pool_device(const kvd_pool* pool);
 
@@ -17,6 +20,7 @@ struct AppendParams {
     const int64_t* slot_mapping; // [n_tokens]
     uint8_t* kv;                 // this layer's records
     uint8_t* host_kv;            // this layer's host-tier records (device address), or null
+    const uint8_t* block_fmt;    // mixed pools: precision code of every physical block
     int32_t* err;
     int64_t n_tokens;
     int64_t num_blocks;
@@ -40,6 +44,7 @@ struct DecodeParams {
     const int32_t* block_table;  // [B][max_blocks]
     const int32_t* seq_lens;     // [B]
     const uint16_t* retain;      // [num_blocks] or null
+    const uint8_t* block_fmt;    // mixed pools: [num_blocks] precision code (KVD_BF16 / _FP8_E4M3 / _FP8_E5M2)
     float* part_o;               // [S + U][g][128]
     float* part_lse;             // [S + U][g]
     int32_t* unit_first;         // [U]
@@ -111,7 +116,7 @@ inline cudaError_t launch_dependent(void (*kernel)(P...), dim3 grid, dim3 block,
     return cudaLaunchKernelEx(&cfg, kernel, params...);
 }
 
-cudaError_t launch_append(const AppendParams& p, bool fp8, cudaStream_t stream);
+cudaError_t launch_append(const AppendParams& p, int kind, cudaStream_t stream);
 constexpr int kMaxPlanBlocks = 16384;   // the plan keeps a request's importances in shared memory
 
 struct TierPlanParams {
@@ -142,10 +147,10 @@ struct TierMoveParams {
     int n_kv;
 };
 cudaError_t launch_tier_move(const TierMoveParams& p, int num_sms, cudaStream_t stream);
-size_t decode_smem_bytes(bool fp8, int batch, int g);
-int decode_ctas_per_sm(bool fp8, int batch, int g);
-int decode_carveout(bool fp8, int batch, int g);   // percent, for the decode call's launches
-cudaError_t launch_decode(const DecodeParams& p, bool fp8, int carveout, cudaStream_t stream);
+size_t decode_smem_bytes(int kind, int batch, int g);
+int decode_ctas_per_sm(int kind, int batch, int g);
+int decode_carveout(int kind, int batch, int g);   // percent, for the decode call's launches
+cudaError_t launch_decode(const DecodeParams& p, int kind, int carveout, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int carveout, cudaStream_t stream);
 cudaError_t launch_scores(const ScoreParams& p, cudaStream_t stream);
 cudaError_t launch_epilogue(const CombineParams& c, const ScoreParams& sp, int carveout, cudaStream_t stream);

@@ -31,13 +31,19 @@ def assert_out_close(gpu, ref, atol=OUT_ATOL, rtol=OUT_RTOL, what="out"):
 
 
 def dtype_code(w: Workload) -> int:
-    return kvd.KVD_BF16 if w.kv_dtype == "bf16" else kvd.KVD_FP8_E4M3
+    return {"bf16": kvd.KVD_BF16, "fp8_e4m3": kvd.KVD_FP8_E4M3, "mixed": kvd.KVD_MIXED}[w.kv_dtype]
+
+
+FORMAT_CODES = (kvd.KVD_BF16, kvd.KVD_FP8_E4M3, kvd.KVD_FP8_E5M2)   # index = oracle format code
 
 
 def make_pool(w: Workload, layers: int | None = None, poison: bool = True) -> kvd.KVPool:
     pool = kvd.KVPool(layers or w.L, w.n_kv, w.num_blocks(), dtype_code(w))
     if poison:   # NaN everywhere first (codes, bf16 values, fp32 scales): unwritten slots must never leak
         pool.mem.fill_(0xFF)
+    if w.kv_dtype == "mixed":
+        codes = torch.tensor([FORMAT_CODES[f] for f in w.block_formats().tolist()], dtype=torch.uint8)
+        pool.set_block_formats(codes.to(pool.mem.device))
     return pool
 
 
@@ -74,7 +80,10 @@ def workspace(pool: kvd.KVPool, n_q: int, batch: int, max_seq: int, num_splits: 
 def oracle_layer(w: Workload, layer: int, bt_cpu: torch.Tensor, seq_lens: list[int], retain=None, step: int = 0,
                  want_alpha=False, want_logits=False, q=None):
     """fp64 oracle over the oracle's own pool filled from the same seeded inputs."""
-    pool = oracle.OraclePool(w.num_blocks(), w.n_kv, w.d_h, 16, w.kv_dtype != "bf16")
+    if w.kv_dtype == "mixed":
+        pool = oracle.OraclePool(w.num_blocks(), w.n_kv, w.d_h, 16, block_fmt=w.block_formats())
+    else:
+        pool = oracle.OraclePool(w.num_blocks(), w.n_kv, w.d_h, 16, w.kv_dtype != "bf16")
     for b in range(w.batch):
         k, v = w.kv(layer, b, 0, seq_lens[b])
         slots = w.slot_mapping(b, 0, seq_lens[b], bt_cpu).numpy()

@@ -50,3 +50,28 @@ def test_kv_values_are_deterministic_and_slice_consistent():
     assert torch.equal(k1, k2[100:164]) and torch.equal(v1, v2[100:164])
     f = w._outlier_factor(3, "k", "cpu")
     assert set(f.unique().tolist()) <= {1.0, 20.0}
+
+
+def test_mixed_workload_bytes_count_each_token_at_its_blocks_width():
+    """K/V bytes of a mixed pool: 2·L·n_kv·d_h·w_kv per token with w_kv = 2 for a token in a BF16
+    block and 1 in an E4M3 / E5M2 block (scales counted apart: 8 B per token and KV head)."""
+    from kvd_inputs import Workload
+
+    w = Workload("mixed_bytes", L=3, n_q=8, n_kv=2, d_h=128, batch=3, kv_dtype="mixed", seed=4,
+                 mixed_probs=(0.3, 0.4, 0.3))
+    w._ctx0 = [37, 300, 16]
+    fmt = w.block_formats()
+    assert set(fmt.tolist()) <= {0, 1, 2} and len(fmt) == w.num_blocks()
+    bt = w.block_table()
+    wide = narrow = 0
+    for b, n in enumerate(w.seq_lens()):
+        for t in range(n):
+            if fmt[int(bt[b, t // 16])] == 0:
+                wide += 1
+            else:
+                narrow += 1
+    assert w.kv_bytes_per_step() == 2 * 3 * 2 * 128 * (2 * wide + narrow)
+    assert w.scale_bytes_per_step() == 2 * 3 * 2 * 4 * narrow
+    import pytest
+    with pytest.raises(ValueError):
+        w.w_kv
