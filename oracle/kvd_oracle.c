@@ -13,6 +13,10 @@
  *    기법", FP8 format table and the paragraph after it.
  *  - Mixed-precision pages, one precision per block with the retention mask
  *    beside it: page "The KV Cache Is the New Memory Wall", §5.5.
+ *  - Low-bit KV (INT4 / 2-bit codes with per-group scale and zero point): same
+ *    page, §3.2 (2-bit storage raises decode intensity to 64 FLOP/B), §4.2,
+ *    §4.6 and Tab. 7 (KIVI 2-bit, KVQuant INT4); the group layout is this
+ *    oracle's reading (the pages give none).
  *  - Paged cache: fixed 16-token blocks and a per-request block table that
  *    maps the request's j-th block to a physical block; the kernel walks the
  *    table in order, so scattered blocks give the same result: same page and
@@ -247,6 +251,103 @@ int kvdo_append_mixed(int n_kv, int d_h, int block_size, int64_t num_blocks, con
             for (int i = 0; i < d_h; ++i) {
                 k_val[row * d_h + i] = fmt_decode(fmt, k_codes[row * d_h + i]) * (double)k_scales[row];
                 v_val[row * d_h + i] = fmt_decode(fmt, v_codes[row * d_h + i]) * (double)v_scales[row];
+            }
+        }
+    }
+    return KVDO_OK;
+}
+
+/* ------------------------------------------------------------ low-bit KV */
+
+/* Nearest IEEE half-precision value to x, ties to the even significand, with
+ * magnitudes beyond the largest finite half (65,504) saturated to it: 10
+ * fraction bits, exponent bias 15, subnormal spacing 2^-24.  Written from the
+ * format definition (the result is returned as a double holding that value). */
+double kvdo_round_half_sat(double x) {
+    if (x == 0.0 || isnan(x)) return x;
+    double a = fabs(x);
+    int e = ilogb(a);               /* 2^e <= a < 2^(e+1) */
+    if (e < -14) e = -14;           /* below the normal range: fixed spacing 2^-24 */
+    double ulp = ldexp(1.0, e - 10);
+    double r = rint(a / ulp) * ulp; /* a / ulp is exact: ulp is a power of two */
+    if (r > 65504.0) r = 65504.0;
+    return x < 0 ? -r : r;
+}
+
+void kvdo_round_half_sat_array(const double* x, int64_t n, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = kvdo_round_half_sat(x[i]);
+}
+
+/* Low-bit row quantisation with per-group scale and zero point (the group
+ * layout is not on the pages; page "The KV Cache Is the New Memory Wall",
+ * §4.2, §4.6, Tab. 7, names INT4 / 2-bit KV with group scales).  For each group
+ * of `group` consecutive values of a (token, KV head) row, in single precision:
+ *   mn, mx   = min and max of the group,
+ *   scale    = half(fp32((mx - mn) / (2^bits - 1))), 1 if that rounds to 0,
+ *   zero     = half(mn),
+ *   code_i   = clamp(rint(fp32(fp32(x_i - zero) / scale)), 0, 2^bits - 1),
+ * half() = the nearest half-precision value, saturating; rint ties to even.
+ * The value read back is code·scale + zero.  codes [d], scales and zeros
+ * [d / group] (values that are exact half-precision numbers). */
+void kvdo_quantize_row_lowbit(const float* x, int d, int bits, int group, uint8_t* codes, float* scales,
+                              float* zeros) {
+    const int top = (1 << bits) - 1;
+    for (int g0 = 0, gi = 0; g0 < d; g0 += group, ++gi) {
+        float mn = x[g0], mx = x[g0];
+        for (int i = g0 + 1; i < g0 + group; ++i) {
+            if (x[i] < mn) mn = x[i];
+            if (x[i] > mx) mx = x[i];
+        }
+        float span = mx - mn;
+        float s = (float)kvdo_round_half_sat((double)(span / (float)top));
+        if (s == 0.0f) s = 1.0f;
+        float z = (float)kvdo_round_half_sat((double)mn);
+        for (int i = g0; i < g0 + group; ++i) {
+            float diff = x[i] - z;
+            float y = diff / s;
+            double r = rint((double)y);
+            if (r < 0.0) r = 0.0;
+            if (r > (double)top) r = (double)top;
+            codes[i] = (uint8_t)r;
+        }
+        scales[gi] = s;
+        zeros[gi] = z;
+    }
+}
+
+void kvdo_quantize_rows_lowbit(const float* x, int64_t rows, int d, int bits, int group, uint8_t* codes,
+                               float* scales, float* zeros) {
+    const int ng = d / group;
+    for (int64_t r = 0; r < rows; ++r)
+        kvdo_quantize_row_lowbit(x + r * d, d, bits, group, codes + r * d, scales + r * ng, zeros + r * ng);
+}
+
+/* Append into a low-bit pool: every (token, KV head) row of K and of V is
+ * quantised as above.  k_val, v_val [num_blocks][n_kv][block_size][d_h] receive
+ * the values attention reads (code·scale + zero, fp64); codes likewise, and
+ * scales / zeros [num_blocks][n_kv][block_size][d_h / group]. */
+int kvdo_append_lowbit(int n_kv, int d_h, int block_size, int64_t num_blocks, int bits, int group,
+                       const float* k_new, const float* v_new, const int64_t* slot_mapping, int64_t N,
+                       double* k_val, double* v_val, uint8_t* k_codes, uint8_t* v_codes, float* k_scales,
+                       float* k_zeros, float* v_scales, float* v_zeros) {
+    const int ng = d_h / group;
+    for (int64_t n = 0; n < N; ++n) {
+        int64_t slot = slot_mapping[n];
+        if (slot < 0) continue;
+        int64_t blk = slot / block_size;
+        int64_t off = slot % block_size;
+        if (blk >= num_blocks) return KVDO_ERR_INDEX;
+        for (int h = 0; h < n_kv; ++h) {
+            int64_t row = (blk * n_kv + h) * block_size + off;
+            kvdo_quantize_row_lowbit(k_new + (n * n_kv + h) * d_h, d_h, bits, group, k_codes + row * d_h,
+                                     k_scales + row * ng, k_zeros + row * ng);
+            kvdo_quantize_row_lowbit(v_new + (n * n_kv + h) * d_h, d_h, bits, group, v_codes + row * d_h,
+                                     v_scales + row * ng, v_zeros + row * ng);
+            for (int i = 0; i < d_h; ++i) {
+                k_val[row * d_h + i] = k_codes[row * d_h + i] * (double)k_scales[row * ng + i / group] +
+                                       (double)k_zeros[row * ng + i / group];
+                v_val[row * d_h + i] = v_codes[row * d_h + i] * (double)v_scales[row * ng + i / group] +
+                                       (double)v_zeros[row * ng + i / group];
             }
         }
     }

@@ -73,6 +73,12 @@ def _load():
             lib.kvdo_quantize_rows_fmt.argtypes = [P, i64, i32, i32, P, P]
             lib.kvdo_append_mixed.restype = i32
             lib.kvdo_append_mixed.argtypes = [i32, i32, i32, i64, P, P, P, P, i64, P, P, P, P, P, P]
+            lib.kvdo_round_half_sat.restype = f64
+            lib.kvdo_round_half_sat.argtypes = [f64]
+            lib.kvdo_round_half_sat_array.argtypes = [P, i64, P]
+            lib.kvdo_quantize_rows_lowbit.argtypes = [P, i64, i32, i32, i32, P, P, P]
+            lib.kvdo_append_lowbit.restype = i32
+            lib.kvdo_append_lowbit.argtypes = [i32, i32, i32, i64, i32, i32, P, P, P, i64, P, P, P, P, P, P, P, P]
             _lib = lib
     return _lib
 
@@ -140,18 +146,54 @@ def quantize_rows(x) -> tuple[np.ndarray, np.ndarray]:
     return codes, scales
 
 
+def round_half_sat(x) -> np.ndarray:
+    """Nearest IEEE half-precision value of each float64, ties to even, saturated at ±65,504."""
+    a = _c(x, np.float64)
+    out = np.empty(a.shape, np.float64)
+    _load().kvdo_round_half_sat_array(_p(a), a.size, _p(out))
+    return out
+
+
+def quantize_rows_lowbit(x, bits: int, group: int) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """Low-bit group quantise of float32 [..., d]: (codes [..., d] uint8 in [0, 2^bits - 1],
+    scales [..., d/group] float32, zeros [..., d/group] float32), value = code·scale + zero."""
+    a = _c(x, np.float32)
+    d = a.shape[-1]
+    rows = a.size // d
+    codes = np.empty(a.shape, np.uint8)
+    scales = np.empty(a.shape[:-1] + (d // group,), np.float32)
+    zeros = np.empty(a.shape[:-1] + (d // group,), np.float32)
+    _load().kvdo_quantize_rows_lowbit(_p(a), rows, d, int(bits), int(group), _p(codes), _p(scales), _p(zeros))
+    return codes, scales, zeros
+
+
 class OraclePool:
     """The oracle's own paged pool for one layer: [num_blocks][n_kv][block_size][d_h].
 
     block_fmt (uint8 [num_blocks], optional) makes it a mixed-precision pool: block p holds
-    BF16 values (0), E4M3 codes (1) or E5M2 codes (2), each 8-bit row with its own scale."""
+    BF16 values (0), E4M3 codes (1) or E5M2 codes (2), each 8-bit row with its own scale.
+    lowbit = (bits, group) makes it a low-bit pool: every row of K and V holds bits-wide codes
+    with a scale and a zero point per group of `group` values."""
 
     def __init__(self, num_blocks: int, n_kv: int, d_h: int, block_size: int = 16, fp8: bool = False,
-                 block_fmt=None):
+                 block_fmt=None, lowbit=None):
         self.num_blocks, self.n_kv, self.d_h, self.block_size, self.fp8 = num_blocks, n_kv, d_h, block_size, fp8
         shape = (num_blocks, n_kv, block_size, d_h)
         self.block_fmt = None
-        if block_fmt is not None:
+        self.lowbit = None
+        if lowbit is not None:
+            self.lowbit = (int(lowbit[0]), int(lowbit[1]))
+            ng = d_h // self.lowbit[1]
+            assert ng * self.lowbit[1] == d_h and self.lowbit[0] in (2, 4)
+            self.k = np.zeros(shape, np.float64)
+            self.v = np.zeros(shape, np.float64)
+            self.k_codes = np.zeros(shape, np.uint8)
+            self.v_codes = np.zeros(shape, np.uint8)
+            self.k_scales = np.ones(shape[:-1] + (ng,), np.float32)
+            self.k_zeros = np.zeros(shape[:-1] + (ng,), np.float32)
+            self.v_scales = np.ones(shape[:-1] + (ng,), np.float32)
+            self.v_zeros = np.zeros(shape[:-1] + (ng,), np.float32)
+        elif block_fmt is not None:
             self.block_fmt = _c(block_fmt, np.uint8)
             assert self.block_fmt.shape == (num_blocks,) and int(self.block_fmt.max(initial=0)) <= FMT_E5M2
             self.k = np.zeros(shape, np.float64)
@@ -176,6 +218,11 @@ class OraclePool:
         k = _c(k_new, np.float32)
         v = _c(v_new, np.float32)
         s = _c(slot_mapping, np.int64)
+        if self.lowbit is not None:
+            return _load().kvdo_append_lowbit(self.n_kv, self.d_h, self.block_size, self.num_blocks, self.lowbit[0],
+                                              self.lowbit[1], _p(k), _p(v), _p(s), s.size, _p(self.k), _p(self.v),
+                                              _p(self.k_codes), _p(self.v_codes), _p(self.k_scales),
+                                              _p(self.k_zeros), _p(self.v_scales), _p(self.v_zeros))
         if self.block_fmt is not None:
             return _load().kvdo_append_mixed(self.n_kv, self.d_h, self.block_size, self.num_blocks,
                                              _p(self.block_fmt), _p(k), _p(v), _p(s), s.size, _p(self.k), _p(self.v),
@@ -188,7 +235,7 @@ class OraclePool:
 
     def values(self) -> tuple[np.ndarray, np.ndarray]:
         """fp64 K and V as read by attention (FP8: code value × row scale)."""
-        if not self.fp8 or self.block_fmt is not None:
+        if not self.fp8 or self.block_fmt is not None or self.lowbit is not None:
             return self.k, self.v
         rows = self.num_blocks * self.n_kv * self.block_size
         kd = np.empty(self.k_codes.shape, np.float64)

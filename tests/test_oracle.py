@@ -570,3 +570,121 @@ def test_mixed_pool_attention_matches_torch_casts_and_sdpa():
     # the 5 slots never written hold zeros in every format and are attended like any other
     ref = _dense_sdpa(q[0].astype(np.float64), kl, vl, 1 / np.sqrt(d_h))
     np.testing.assert_allclose(res["out"][0], ref, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------------ low-bit KV (INT4 / 2-bit)
+def test_round_half_matches_numpy_float16_with_saturation():
+    """Half-precision rounding against numpy's IEEE float16 cast: random values over every
+    exponent, exact ties, subnormals and the overflow edge (saturated at 65,504 here)."""
+    r = _rng(40)
+    x = np.concatenate([
+        r.standard_normal(20000) * np.exp2(r.integers(-30, 20, 20000)),
+        (np.arange(1, 4000) + 0.5) * 2.0 ** -24,              # ties between subnormals
+        (1 + (2 * np.arange(1, 1024) + 1) / 2048.0) * 4.0,    # ties between normals
+        [0.0, -0.0, 65504.0, 65519.9, 65520.0, 1e6, -1e6, 2.0 ** -25, 3 * 2.0 ** -26],
+    ])
+    got = oracle.round_half_sat(x)
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).astype(np.float64)
+    ref = np.where(np.isinf(ref), np.sign(ref) * 65504.0, ref)
+    assert np.array_equal(got, ref)
+
+
+def _lowbit_case(seed, rows=400, d=128):
+    r = _rng(seed)
+    x = r.standard_normal((rows, d)).astype(np.float32)
+    x[5] = 0.0                                     # a zero row
+    x[6, :32] = 1.25                               # a constant group
+    x[7] *= 1000.0                                 # a wide row
+    x[8, 40] = 300.0                               # one outlier in group 1
+    x[9] = np.linspace(-3, 3, d, dtype=np.float32)
+    return _bf16(x)
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_lowbit_quantise_closed_forms(bits):
+    """Per group of 32: the scale is the group's span / (2^bits - 1) to half precision, the zero
+    point its minimum to half precision, codes span [0, 2^bits - 1] and reconstruct every value
+    to within half a scale (plus the half-precision rounding of the scale and zero)."""
+    G, top = 32, (1 << bits) - 1
+    x = _lowbit_case(41)
+    codes, scales, zeros = oracle.quantize_rows_lowbit(x, bits, G)
+    xg = x.reshape(x.shape[0], -1, G).astype(np.float64)
+    mn, mx = xg.min(-1), xg.max(-1)
+    span = (mx - mn) / top
+    assert codes.max() <= top and codes.dtype == np.uint8
+    # scale: the half-precision value nearest span (relative half-ulp 2^-11), 1 for a zero span
+    nz = span > 0
+    assert np.all(np.abs(scales[nz] - span[nz]) <= 2.0 ** -11 * span[nz] * (1 + 1e-6))
+    assert np.all(scales[~nz] == 1.0)
+    assert np.all(np.abs(zeros - mn) <= 2.0 ** -11 * np.abs(mn) + 2.0 ** -25)
+    # every scale and zero is a half-precision number
+    assert np.array_equal(scales.astype(np.float16).astype(np.float32), scales)
+    assert np.array_equal(zeros.astype(np.float16).astype(np.float32), zeros)
+    # reconstruction bound
+    rec = codes.reshape(xg.shape) * scales[..., None].astype(np.float64) + zeros[..., None].astype(np.float64)
+    slack = 2.0 ** -11 * (np.abs(mn) + top * span) + 1e-6 * np.abs(xg).max(-1)
+    err = np.abs(rec - xg)
+    assert np.all(err <= 0.5 * scales[..., None] + slack[..., None]), err.max()
+    # the minimum of a group lands on code 0 and its maximum on the top code (up to rounding)
+    cg = codes.reshape(xg.shape)
+    assert np.all(cg[np.arange(xg.shape[0])[:, None], np.arange(xg.shape[1]), xg.argmin(-1)][nz] == 0)
+    assert np.all(cg[np.arange(xg.shape[0])[:, None], np.arange(xg.shape[1]), xg.argmax(-1)][nz] >= top - 1)
+    # constant group: scale 1, code 0, value = the half-precision zero point
+    assert scales[6, 0] == 1.0 and np.all(codes[6, :32] == 0) and zeros[6, 0] == np.float32(1.25)
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_lowbit_codes_are_the_nearest_level(bits):
+    """Brute force: given the group's scale and zero, the stored code is the level c·scale + zero
+    nearest to x among all 2^bits levels (x below the lowest level takes code 0, above the highest
+    the top code); an exact tie may go either way only if the single-precision quotient rounded."""
+    G, top = 32, (1 << bits) - 1
+    x = _lowbit_case(42, rows=200)
+    codes, scales, zeros = oracle.quantize_rows_lowbit(x, bits, G)
+    lv = np.arange(top + 1, dtype=np.float64)
+    xs = x.reshape(x.shape[0], -1, G).astype(np.float64)
+    levels = lv[None, None, None, :] * scales[..., None, None] + zeros[..., None, None]   # [r][g][1][L]
+    dist = np.abs(xs[..., None] - levels)
+    best = dist.min(-1)
+    chosen = np.take_along_axis(dist, codes.reshape(xs.shape)[..., None].astype(np.int64), -1)[..., 0]
+    assert np.all(chosen <= best + 1e-6 * scales[..., None] + 1e-30)
+
+
+def test_lowbit_pool_attention_matches_sdpa_on_read_back_values():
+    """A low-bit pool reads back code·scale + zero for every (token, head) row, and decode over it
+    equals dense SDPA (fp64, torch) over those read-back values through the block table."""
+    bits, G = 4, 32
+    r = _rng(43)
+    nb, n_kv, d_h, bs, n_q = 9, 2, 128, 16, 8
+    n = nb * bs - 7
+    k = _bf16(r.standard_normal((n, n_kv, d_h)).astype(np.float32))
+    v = _bf16(r.standard_normal((n, n_kv, d_h)).astype(np.float32))
+    slots = r.permutation(nb * bs)[:n].astype(np.int64)
+    pool = oracle.OraclePool(nb, n_kv, d_h, bs, lowbit=(bits, G))
+    assert pool.append(k, v, slots) == 0
+    kc, ks, kz = oracle.quantize_rows_lowbit(k, bits, G)
+    for t, s in enumerate(slots):
+        p, o = divmod(int(s), bs)
+        assert np.array_equal(pool.k_codes[p, :, o], kc[t]) and np.array_equal(pool.k_scales[p, :, o], ks[t])
+        want = kc[t].reshape(n_kv, -1, G) * ks[t][..., None].astype(np.float64) + kz[t][..., None].astype(np.float64)
+        assert np.array_equal(pool.k[p, :, o], want.reshape(n_kv, d_h))
+    q = _bf16(r.standard_normal((1, n_q, d_h)).astype(np.float32))
+    table = np.array([r.permutation(nb)], np.int32)
+    ln = n - 3
+    res = oracle.decode(pool, q, n_q, table, np.array([ln], np.int32))
+    kv, vv = pool.values()
+    kl = np.stack([kv[table[0, t // bs], :, t % bs] for t in range(ln)])
+    vl = np.stack([vv[table[0, t // bs], :, t % bs] for t in range(ln)])
+    ref = _dense_sdpa(q[0].astype(np.float64), kl, vl, 1 / np.sqrt(d_h))
+    np.testing.assert_allclose(res["out"][0], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_lowbit_bytes_and_intensity_closed_forms():
+    """Bytes per (token, KV head) row: d_h·bits/8 of codes plus two half-precision numbers per
+    group; with the codes alone, 2-bit storage at g = 8 gives the page's 64 FLOP/B floor."""
+    import bench
+
+    for bits, row in ((4, 64 + 16), (2, 32 + 16)):
+        assert 128 * bits // 8 + (128 // 32) * 4 == row
+    assert bench.decode_intensity(8, 0.25) == 64 and bench.decode_intensity(8, 0.5) == 32
