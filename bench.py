@@ -67,12 +67,12 @@ def decode_intensity(g: int, w_kv: float) -> float:
     return 2 * g / w_kv
 
 
-DECODE_SOURCES = ("kvd_decode.cu", "kvd_common.cuh", "kvd_internal.h")
+DECODE_SOURCES = ("kvd_decode.cu", "kvd_common.cuh", "kvd_internal.h", "kvd_decode_kernel.cuh", "kvd_decode_lowbit.cu")
 
 
 def decode_source_digest():
-    """sha256 of the decode kernel's sources (kvd_decode.cu, kvd_common.cuh, kvd_internal.h,
-    concatenated in that order), or None if one is missing."""
+    """sha256 of the decode kernel's sources (DECODE_SOURCES concatenated in that order), or None if
+    one is missing."""
     import hashlib
 
     h = hashlib.sha256()

@@ -49,6 +49,16 @@
  *  - A mixed pool (KVD_MIXED) gives every record the BF16 size, 8192 bytes; a block stored
  *    in E4M3 or E5M2 puts the 4224-byte FP8 record (codes of its own format, then the 32
  *    scales) at the start of its slot and leaves the rest unused.
+ *  - A low-bit pool (KVD_INT4, KVD_INT2: bits = 4 or 2, group_size G ∈ {32, 64, 128}, NG =
+ *    128/G groups per row) has records of 2·(256·bits) + 2·(64·NG) bytes: the K code tile, the
+ *    V code tile (16·128 codes each, bits wide), then for K and then for V the table
+ *    [16 tokens][NG groups] of 32-bit entries (scale half-precision bits | zero-point bits << 16).
+ *    Value = code·scale + zero.  Codes: with P = 8/bits codes per byte, kg = d/(16·P),
+ *    h = (d/16) % P (the code sits in bits h·bits of its byte), c = d % 16:
+ *      K code of (t, d): lane = 4·(t%8) + (c%8)/2, th = t/8, j = (c%2) + 2·(c/8)
+ *      V code of (t, d): lane = 4·(c%8) + (t%8)/2, th = t/8, j = (t%2) + 2·(c/8)
+ *      byte index within the tile: (((kg/2)·32 + lane)·4 + (kg%2)·2 + th)·4 + j
+ *    so every byte holds codes of one token only.
  */
 #ifndef KVD_H
 #define KVD_H
@@ -81,7 +91,9 @@ typedef enum {
     KVD_FP8_E4M3 = 1,         /* w_kv = 1 byte, plus a per-(token, KV head) fp32 scale for K and for V */
     KVD_F32 = 2,              /* output only (full-precision check output) */
     KVD_FP8_E5M2 = 3,         /* block format of a mixed pool: like E4M3, codes 1·5·2 bits, max 57,344 */
-    KVD_MIXED = 4             /* pool of mixed-precision blocks (kvd_pool_set_block_formats) */
+    KVD_MIXED = 4,            /* pool of mixed-precision blocks (kvd_pool_set_block_formats) */
+    KVD_INT4 = 5,             /* w_kv = 1/2: 4-bit codes, half-precision scale and zero point per group */
+    KVD_INT2 = 6              /* w_kv = 1/4: 2-bit codes, likewise */
 } kvd_dtype;
 
 typedef struct {
@@ -90,7 +102,9 @@ typedef struct {
     int32_t d_h;              /* head dimension; 128 */
     int32_t block_size;       /* tokens per block; 16 */
     int64_t num_blocks;       /* physical blocks per layer */
-    int32_t kv_dtype;         /* KVD_BF16, KVD_FP8_E4M3 or KVD_MIXED */
+    int32_t kv_dtype;         /* KVD_BF16, KVD_FP8_E4M3, KVD_MIXED, KVD_INT4 or KVD_INT2 */
+    int32_t group_size;       /* KVD_INT4 / KVD_INT2: values per scale group, 32, 64 or 128; ignored
+                                 for the other types */
 } kvd_pool_desc;
 
 typedef struct kvd_pool kvd_pool;  /* opaque */
@@ -118,8 +132,19 @@ KVD_API const char* kvd_status_string(kvd_status s);
 
 /* Bytes of a pool.  kv_bytes = L·num_blocks·n_kv·2·block_size·d_h·w_kv, the closed form
  * 2·L·n_kv·d_h·w_kv bytes per token times num_blocks·block_size tokens (K and V elements
- * only); pool_bytes = kv_bytes plus, for FP8, L·num_blocks·n_kv·2·block_size·4 bytes of
- * scales: the size of the buffer kvd_pool_create needs.  Host only. */
+ * only; w_kv = 2, 1, 1/2 or 1/4 for BF16, FP8, INT4, INT2; a mixed pool counts 2); pool_bytes =
+ * kv_bytes plus, for FP8, L·num_blocks·n_kv·2·block_size·4 bytes of scales, for INT4 / INT2
+ * L·num_blocks·n_kv·2·block_size·(128/group_size)·4 bytes of group scales and zero points:
+ * the size of the buffer kvd_pool_create needs.  A low-bit type with a group_size other than
+ * 32, 64 or 128 is KVD_ERR_UNSUPPORTED.  Host only.
+ * Low-bit pools: page "The KV Cache Is the New Memory Wall", §4.2, §4.6 and Tab. 7 (INT4 and
+ * 2-bit KV with group-wise scales, KVQuant, KIVI), §3.2 (2-bit storage raises decode intensity
+ * to 2g/w_kv = 64 FLOP/B at g = 8).  The pages give no group layout; this library quantises
+ * each group of group_size consecutive dims of a (token, KV head) row, K and V alike:
+ * scale = half(fp32((max − min)/(2^bits − 1))) (1 if that is 0), zero = half(min), code =
+ * clamp(rint(fp32(fp32(x − zero)/scale)), 0, 2^bits − 1), half() = nearest half-precision
+ * value saturated at ±65,504, rint ties to even.  Low-bit pools take no host tier
+ * (kvd_pool_attach_host_tier: KVD_ERR_UNSUPPORTED). */
 KVD_API kvd_status kvd_pool_bytes(const kvd_pool_desc* desc, size_t* pool_bytes, size_t* kv_bytes);
 
 /* Wrap caller memory as a pool.  mem is a device buffer of len ≥ pool_bytes bytes,

@@ -30,7 +30,8 @@ class Workload:
     n_kv: int
     d_h: int
     batch: int
-    kv_dtype: str                       # "bf16", "fp8_e4m3" or "mixed" (a format per physical block)
+    kv_dtype: str                       # "bf16", "fp8_e4m3", "mixed" (a format per physical block),
+                                        # "int4" or "int2" (codes with a scale and zero per group)
     block_size: int = 16
     seed: int = 0
     steps: int = 1                      # decode steps in one unit of work
@@ -43,6 +44,7 @@ class Workload:
     scores: bool = False                # accumulate the importance score s_i
     pool_slack_blocks: int = 0          # unused physical blocks added to the pool
     mixed_probs: tuple | None = None    # mixed pools: P(BF16), P(E4M3), P(E5M2) of a physical block
+    group_size: int = 0                 # low-bit pools: values per scale group (32, 64 or 128)
     description: str = ""
     _ctx0: list = field(default_factory=list)   # context before step 0's append
 
@@ -52,11 +54,18 @@ class Workload:
         return self.n_q // self.n_kv
 
     @property
-    def w_kv(self) -> int:
+    def w_kv(self) -> float:
         """Bytes per stored K or V element (a single-format pool)."""
         if self.kv_dtype == "mixed":
             raise ValueError("a mixed pool has a w_kv per block: use token_bytes()")
-        return 2 if self.kv_dtype == "bf16" else 1
+        return {"bf16": 2, "fp8_e4m3": 1, "int4": 0.5, "int2": 0.25}[self.kv_dtype]
+
+    @property
+    def lowbit(self) -> tuple | None:
+        """(bits, group_size) of a low-bit pool, else None."""
+        if self.kv_dtype in ("int4", "int2"):
+            return (4 if self.kv_dtype == "int4" else 2, self.group_size)
+        return None
 
     def seq_lens(self, step: int = 0) -> list[int]:
         """Attended context of every sequence at ``step`` (includes the token appended in it)."""
@@ -100,11 +109,17 @@ class Workload:
     def kv_bytes_per_step(self, step: int = 0) -> int:
         """Closed-form K/V bytes attended in one step over all layers: 2·L·n_kv·d_h·w_kv per token
         (w_kv of the block that holds the token in a mixed pool)."""
+        if self.lowbit:
+            return 2 * self.L * self.n_kv * self.d_h * self.lowbit[0] * sum(self.seq_lens(step)) // 8
         wide, narrow = self._tokens_by_width(step)
         return 2 * self.L * self.n_kv * self.d_h * (2 * wide + narrow)
 
     def scale_bytes_per_step(self, step: int = 0) -> int:
-        """fp32 scales read with the 8-bit tokens: one for K and one for V per (token, KV head)."""
+        """Scale bytes read with the tokens: 8-bit tokens one fp32 scale for K and one for V per
+        (token, KV head); low-bit tokens a half-precision scale and zero point per group, for K
+        and for V."""
+        if self.lowbit:
+            return 2 * self.L * self.n_kv * 4 * (self.d_h // self.group_size) * sum(self.seq_lens(step))
         return 2 * self.L * self.n_kv * 4 * self._tokens_by_width(step)[1]
 
     def block_formats(self):
@@ -260,8 +275,29 @@ def tiered(seed: int = 0) -> Workload:
     return w
 
 
+def llama70b_int4(seed: int = 0) -> Workload:
+    w = Workload("llama70b_int4", L=80, n_q=64, n_kv=8, d_h=128, batch=1, kv_dtype="int4", seed=seed,
+                 outlier_p=0.001, outlier_factor=20.0, group_size=32,
+                 description="Llama-3-70B shape long context, 4-bit KV: 80 layers, n_q 64, n_kv 8, d_h 128, batch 1, "
+                             "context 131,072, 4-bit codes with a half-precision scale and zero point per group of "
+                             "32 values, 0.1% outlier channels x20")
+    w._ctx0 = [131072]
+    return w
+
+
+def llama70b_int2(seed: int = 0) -> Workload:
+    w = Workload("llama70b_int2", L=80, n_q=64, n_kv=8, d_h=128, batch=1, kv_dtype="int2", seed=seed,
+                 outlier_p=0.001, outlier_factor=20.0, group_size=32,
+                 description="Llama-3-70B shape long context, 2-bit KV: 80 layers, n_q 64, n_kv 8, d_h 128, batch 1, "
+                             "context 131,072, 2-bit codes with a half-precision scale and zero point per group of "
+                             "32 values, 0.1% outlier channels x20")
+    w._ctx0 = [131072]
+    return w
+
+
 WORKLOADS = {"tiny": tiny, "llama8b": llama8b, "llama8b_mixed": llama8b_mixed, "ragged": ragged,
-             "llama70b_fp8": llama70b_fp8, "tiered": tiered}
+             "llama70b_fp8": llama70b_fp8, "tiered": tiered, "llama70b_int4": llama70b_int4,
+             "llama70b_int2": llama70b_int2}
 
 
 def get(name: str, seed: int = 0) -> Workload:

@@ -14,6 +14,8 @@ from ._lib import (  # noqa: F401
     KVD_F32,
     KVD_FP8_E4M3,
     KVD_FP8_E5M2,
+    KVD_INT2,
+    KVD_INT4,
     KVD_MIXED,
     KVD_OK,
     KVD_ERR_CUDA,
@@ -53,18 +55,23 @@ from ._lib import (  # noqa: F401
 class KVPool:
     """Device memory for a paged KV pool (torch allocations) plus its library handle."""
 
-    def __init__(self, num_layers: int, n_kv: int, num_blocks: int, kv_dtype: int = KVD_BF16, device="cuda"):
+    def __init__(self, num_layers: int, n_kv: int, num_blocks: int, kv_dtype: int = KVD_BF16, device="cuda",
+                 group_size: int = 0):
         import torch
 
         self.num_layers, self.n_kv, self.num_blocks, self.kv_dtype = num_layers, n_kv, num_blocks, kv_dtype
-        pool_bytes, self.kv_bytes = kvd_pool_bytes(num_layers, n_kv, num_blocks, kv_dtype)
+        self.group_size = group_size
+        pool_bytes, self.kv_bytes = kvd_pool_bytes(num_layers, n_kv, num_blocks, kv_dtype, group_size=group_size)
         self.mem = torch.empty(pool_bytes, dtype=torch.uint8, device=device)
-        self.handle = kvd_pool_create(num_layers, n_kv, num_blocks, kv_dtype, self.mem)
+        self.handle = kvd_pool_create(num_layers, n_kv, num_blocks, kv_dtype, self.mem, group_size=group_size)
 
     @property
     def record_bytes(self) -> int:
-        """Bytes of one (layer, block, KV head) record slot: K tile, V tile and (FP8) 32 fp32 scales;
-        a mixed pool sizes every slot for BF16."""
+        """Bytes of one (layer, block, KV head) record slot: K tile, V tile and (FP8) 32 fp32 scales,
+        (INT4 / INT2) 2·16·(128/group_size) scale-and-zero words; a mixed pool sizes every slot for BF16."""
+        if self.kv_dtype in (KVD_INT4, KVD_INT2):
+            bits = 4 if self.kv_dtype == KVD_INT4 else 2
+            return 2 * 256 * bits + 2 * 64 * (128 // self.group_size)
         return 4096 + 128 if self.kv_dtype == KVD_FP8_E4M3 else 8192
 
     def set_block_formats(self, block_fmt):

@@ -12,7 +12,7 @@ import ctypes
 import os
 
 KVD_OK, KVD_ERR_INVALID, KVD_ERR_UNSUPPORTED, KVD_ERR_NOMEM, KVD_ERR_CUDA, KVD_ERR_OOB, KVD_ERR_TIMEOUT = range(7)
-KVD_BF16, KVD_FP8_E4M3, KVD_F32, KVD_FP8_E5M2, KVD_MIXED = 0, 1, 2, 3, 4
+KVD_BF16, KVD_FP8_E4M3, KVD_F32, KVD_FP8_E5M2, KVD_MIXED, KVD_INT4, KVD_INT2 = 0, 1, 2, 3, 4, 5, 6
 KVD_EARLY_START = 1   # kvd_decode_attn flag
 
 SYMBOLS = [
@@ -37,7 +37,8 @@ class ScoresDesc(ctypes.Structure):
 
 class PoolDesc(ctypes.Structure):
     _fields_ = [("num_layers", ctypes.c_int32), ("n_kv", ctypes.c_int32), ("d_h", ctypes.c_int32),
-                ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int64), ("kv_dtype", ctypes.c_int32)]
+                ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int64), ("kv_dtype", ctypes.c_int32),
+                ("group_size", ctypes.c_int32)]
 
 
 _lib = None
@@ -126,9 +127,11 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
-def kvd_pool_bytes(num_layers: int, n_kv: int, num_blocks: int, kv_dtype: int, d_h: int = 128, block_size: int = 16):
-    """(pool_bytes, kv_bytes) of a pool: buffer size to allocate, and closed-form K/V bytes; host only."""
-    d = PoolDesc(num_layers, n_kv, d_h, block_size, num_blocks, kv_dtype)
+def kvd_pool_bytes(num_layers: int, n_kv: int, num_blocks: int, kv_dtype: int, d_h: int = 128, block_size: int = 16,
+                   group_size: int = 0):
+    """(pool_bytes, kv_bytes) of a pool: buffer size to allocate, and closed-form K/V bytes; host only.
+    group_size: values per scale group of a KVD_INT4 / KVD_INT2 pool (32, 64 or 128)."""
+    d = PoolDesc(num_layers, n_kv, d_h, block_size, num_blocks, kv_dtype, group_size)
     pool, kv = ctypes.c_size_t(), ctypes.c_size_t()
     _check("kvd_pool_bytes", load().kvd_pool_bytes(ctypes.byref(d), ctypes.byref(pool), ctypes.byref(kv)))
     return pool.value, kv.value
@@ -204,9 +207,9 @@ def kvd_tier_reassign(num_blocks, host_blocks, tier, block_table, hbm_free, hbm_
     return st, frm[:n.value].copy(), to[:n.value].copy(), hn.value, tn.value
 
 
-def kvd_pool_create(num_layers, n_kv, num_blocks, kv_dtype, mem, d_h=128, block_size=16):
+def kvd_pool_create(num_layers, n_kv, num_blocks, kv_dtype, mem, d_h=128, block_size=16, group_size=0):
     """Wrap a caller-owned device tensor (any dtype, pool_bytes long) as a pool; returns the handle (c_void_p)."""
-    d = PoolDesc(num_layers, n_kv, d_h, block_size, num_blocks, kv_dtype)
+    d = PoolDesc(num_layers, n_kv, d_h, block_size, num_blocks, kv_dtype, group_size)
     h = ctypes.c_void_p()
     n = mem.numel() * mem.element_size()
     _check("kvd_pool_create", load().kvd_pool_create(ctypes.byref(d), _ptr(mem), n, ctypes.byref(h)))

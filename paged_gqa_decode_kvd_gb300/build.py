@@ -16,8 +16,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libkvd.so")
-SOURCES = ["kvd_api.cu", "kvd_append.cu", "kvd_decode.cu", "kvd_combine.cu", "kvd_noalloc.cu", "kvd_tier.cu", "kvd_measure.cu"]
-HEADERS = ["kvd_common.cuh", "kvd_internal.h", os.path.join("..", "..", "include", "kvd.h")]
+SOURCES = ["kvd_api.cu", "kvd_append.cu", "kvd_decode.cu", "kvd_decode_lowbit.cu", "kvd_combine.cu", "kvd_noalloc.cu",
+           "kvd_tier.cu", "kvd_measure.cu"]
+HEADERS = ["kvd_common.cuh", "kvd_internal.h", "kvd_decode_kernel.cuh", os.path.join("..", "..", "include", "kvd.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden", "--expt-relaxed-constexpr"]
 

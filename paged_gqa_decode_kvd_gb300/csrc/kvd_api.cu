@@ -42,10 +42,20 @@ kvd_status check_desc(const kvd_pool_desc* d) {
     if (!d) return KVD_ERR_INVALID;
     if (d->num_layers < 1 || d->n_kv < 1 || d->num_blocks < 1 || d->d_h < 1 || d->block_size < 1)
         return KVD_ERR_INVALID;
-    if (d->kv_dtype != KVD_BF16 && d->kv_dtype != KVD_FP8_E4M3 && d->kv_dtype != KVD_MIXED) return KVD_ERR_INVALID;
+    if (d->kv_dtype != KVD_BF16 && d->kv_dtype != KVD_FP8_E4M3 && d->kv_dtype != KVD_MIXED &&
+        d->kv_dtype != KVD_INT4 && d->kv_dtype != KVD_INT2)
+        return KVD_ERR_INVALID;
     if (d->d_h != kvd::kDh || d->block_size != kvd::kBs) return KVD_ERR_UNSUPPORTED;
+    if ((d->kv_dtype == KVD_INT4 || d->kv_dtype == KVD_INT2) && d->group_size != 32 && d->group_size != 64 &&
+        d->group_size != 128)
+        return KVD_ERR_UNSUPPORTED;
     return KVD_OK;
 }
+
+bool lowbit_dtype(int32_t t) { return t == KVD_INT4 || t == KVD_INT2; }
+
+// Groups per 128-value row of a low-bit pool (1 otherwise).
+int pool_ng(const kvd_pool_desc* d) { return lowbit_dtype(d->kv_dtype) ? kvd::kDh / d->group_size : 1; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -79,7 +89,8 @@ int plan_splits(const kvd_pool* pool, int batch, int max_seq_len, int g) {
     const int64_t nblk = (static_cast<int64_t>(max_seq_len) + kvd::kBs - 1) / kvd::kBs;
     const int64_t total = nblk * batch * pool->desc.n_kv;
     const int64_t by_work = (total + kMinBlocksPerSplit - 1) / kMinBlocksPerSplit;
-    const int64_t by_sms = static_cast<int64_t>(pool->num_sms) * kvd::decode_ctas_per_sm(pool_kind(pool), batch, g);
+    const int64_t by_sms =
+        static_cast<int64_t>(pool->num_sms) * kvd::decode_ctas_per_sm(pool_kind(pool), pool_ng(&pool->desc), batch, g);
     int64_t s = by_work < by_sms ? by_work : by_sms;
     return static_cast<int>(s < 1 ? 1 : s);
 }
@@ -87,13 +98,19 @@ int plan_splits(const kvd_pool* pool, int batch, int max_seq_len, int g) {
 kvd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVD_OK : KVD_ERR_CUDA; }
 
 int pool_kind(const kvd_pool* pool) {
-    return pool->desc.kv_dtype == KVD_FP8_E4M3 ? kvd::kKindFp8
-           : pool->desc.kv_dtype == KVD_MIXED  ? kvd::kKindMixed
-                                               : kvd::kKindBf16;
+    switch (pool->desc.kv_dtype) {
+        case KVD_FP8_E4M3: return kvd::kKindFp8;
+        case KVD_MIXED: return kvd::kKindMixed;
+        case KVD_INT4: return kvd::kKindInt4;
+        case KVD_INT2: return kvd::kKindInt2;
+        default: return kvd::kKindBf16;
+    }
 }
 
 // Bytes of one (layer, block, KV head) record slot.
 size_t record_bytes(const kvd_pool_desc* d) {
+    if (d->kv_dtype == KVD_INT4) return kvd::lowbit_record_bytes(4, pool_ng(d));
+    if (d->kv_dtype == KVD_INT2) return kvd::lowbit_record_bytes(2, pool_ng(d));
     return d->kv_dtype == KVD_FP8_E4M3 ? kvd::kRecordFp8 : kvd::kRecordBf16;
 }
 
@@ -120,16 +137,25 @@ kvd_status kvd_pool_bytes(const kvd_pool_desc* desc, size_t* pool_bytes, size_t*
     kvd_status st = check_desc(desc);
     if (st != KVD_OK) return st;
     if (!kv_bytes || !pool_bytes) return KVD_ERR_INVALID;
-    // a mixed pool sizes every record slot for BF16 (an 8-bit block uses the first part of it)
-    const size_t w = desc->kv_dtype == KVD_FP8_E4M3 ? 1 : 2;
+    // a mixed pool sizes every record slot for BF16 (an 8-bit block uses the first part of it);
+    // element bits: 16, 8, 4 or 2
+    const size_t bits = desc->kv_dtype == KVD_FP8_E4M3 ? 8 : desc->kv_dtype == KVD_INT4 ? 4
+                        : desc->kv_dtype == KVD_INT2   ? 2 : 16;
     size_t per_block = 0, rows = 0, total = 0;
     // 2 (K and V) · block_size · d_h · w_kv bytes per (layer, block, KV head)
-    if (!mul_ok(2 * static_cast<size_t>(desc->block_size) * desc->d_h, w, &per_block)) return KVD_ERR_INVALID;
+    if (!mul_ok(2 * static_cast<size_t>(desc->block_size) * desc->d_h, bits, &per_block)) return KVD_ERR_INVALID;
+    per_block /= 8;
     if (!mul_ok(static_cast<size_t>(desc->num_layers), static_cast<size_t>(desc->num_blocks), &rows)) return KVD_ERR_INVALID;
     if (!mul_ok(rows, static_cast<size_t>(desc->n_kv), &rows)) return KVD_ERR_INVALID;
     if (!mul_ok(rows, per_block, &total)) return KVD_ERR_INVALID;
     *kv_bytes = total;
     *pool_bytes = total;
+    if (lowbit_dtype(desc->kv_dtype)) {   // a (scale, zero) word per (token, group) for K and for V
+        size_t mb = 0;
+        if (!mul_ok(rows, 2 * static_cast<size_t>(desc->block_size) * pool_ng(desc) * 4, &mb)) return KVD_ERR_INVALID;
+        if (total > SIZE_MAX - mb) return KVD_ERR_INVALID;
+        *pool_bytes = total + mb;
+    }
     if (desc->kv_dtype == KVD_FP8_E4M3) {
         size_t sb = 0;
         if (!mul_ok(rows, 2 * static_cast<size_t>(desc->block_size) * sizeof(float), &sb)) return KVD_ERR_INVALID;
@@ -199,7 +225,8 @@ kvd_status kvd_pool_set_block_formats(kvd_pool* pool, const uint8_t* block_fmt, 
 kvd_status kvd_pool_attach_host_tier(kvd_pool* pool, void* host_mem, size_t host_len, void* staging_mem,
                                      size_t staging_len, int64_t host_blocks) {
     if (!pool || host_blocks < 0) return KVD_ERR_INVALID;
-    if (pool->desc.kv_dtype == KVD_MIXED && host_blocks > 0) return KVD_ERR_UNSUPPORTED;
+    if ((pool->desc.kv_dtype == KVD_MIXED || lowbit_dtype(pool->desc.kv_dtype)) && host_blocks > 0)
+        return KVD_ERR_UNSUPPORTED;
     if (host_blocks == 0) {
         pool->host_kv = nullptr;
         pool->host_mem = nullptr;
@@ -371,6 +398,7 @@ kvd_status kvd_append_kv(kvd_pool* pool, int layer, const void* k_new, const voi
     p.host_kv = pool->host_kv ? pool->host_kv + static_cast<size_t>(layer) * pool->host_layer_bytes : nullptr;
     p.block_fmt = pool->block_fmt;
     p.err = pool->err;
+    p.ng = pool_ng(&pool->desc);
     p.n_tokens = n_tokens;
     p.num_blocks = pool->desc.num_blocks;
     p.host_blocks = pool->host_blocks;
@@ -466,10 +494,11 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     p.g = g;
     p.n_q = n_q;
     p.nsplit = S;
+    p.ng = pool_ng(&pool->desc);
     p.max_seq_len = max_seq_len;
     p.early = (flags & KVD_EARLY_START) ? 1 : 0;
     p.scale_log2 = softmax_scale * kvd::kLog2e;
-    const int carveout = kvd::decode_carveout(kind, batch, g);
+    const int carveout = kvd::decode_carveout(kind, p.ng, batch, g);
     cudaError_t e = kvd::launch_decode(p, kind, carveout, s);
     if (e != cudaSuccess) return KVD_ERR_CUDA;
     if (!out) return KVD_OK;  // partials only: the caller merges them with kvd_combine_splits

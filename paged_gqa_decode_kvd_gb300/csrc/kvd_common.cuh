@@ -254,6 +254,140 @@ __device__ __forceinline__ void write_token(uint8_t* record, int t, const uint16
     }
 }
 
+// ------------------------------------------------------------------ low-bit records
+// A low-bit record holds BITS-wide codes (4 or 2) of the K tile and of the V tile, then for K
+// and for V a table [16 tokens][NG groups] of (scale, zero point) half-precision pairs (scale in
+// the low 16 bits); a value reads back as code·scale + zero.  A group is 128/NG consecutive
+// dims of one token's row.
+__host__ __device__ constexpr int lowbit_tile_bytes(int bits) { return kBs * kDh * bits / 8; }
+__host__ __device__ constexpr int lowbit_meta_bytes(int ng) { return kBs * ng * 4; }
+__host__ __device__ constexpr int lowbit_record_bytes(int bits, int ng) {
+    return 2 * lowbit_tile_bytes(bits) + 2 * lowbit_meta_bytes(ng);
+}
+
+// Code placement.  A byte holds 8/BITS codes of one token, in bit fields h·BITS (h < 8/BITS),
+// for dims 16 apart: the same fragment position of 8/BITS consecutive k-steps (K) or m-tiles
+// (V).  Masking field h of a word leaves one code in the low bits of each byte; as an E4M3
+// byte such a code c < 16 decodes exactly to c·2^-9, so one cvt turns bytes (0,1) and one bytes
+// (2,3) of the masked word into the f16 pairs of two fragment registers.  Words are grouped
+// four to a 16-byte chunk, chunk-major then lane, so a warp reads a chunk conflict-free.
+//   K (rows = tokens): word (kg, th) of lane = 4·(t%8) + tq holds token t = lane/4 + 8·th; byte
+//     j, field h: dim 16·(P·kg + h) + 2·tq + (j%2) + 8·(j/2), P = 8/BITS.  Fragment registers
+//     of k-step P·kg + h: a0 = bytes(0,1) of th 0, a1 = bytes(0,1) of th 1, a2/a3 = bytes(2,3).
+//   V (rows = dims): word (kg, th) of lane = 4·r + tq holds tokens 2·tq + (j%2) + 8·th; byte j,
+//     field h: dim 16·(P·kg + h) + r + 8·(j/2).  m-tile P·kg + h: a0 = bytes(0,1) of th 0,
+//     a1 = bytes(2,3) of th 0, a2/a3 the same of th 1.
+//   word index in the tile: ((kg/2)·32 + lane)·4 + (kg%2)·2 + th.
+__host__ __device__ __forceinline__ int lowbit_word(int kg, int lane, int th) {
+    return ((kg >> 1) * 32 + lane) * 4 + (kg & 1) * 2 + th;
+}
+// Byte of a K (V) tile that holds the code of token t, dim d; its field is (d/16) % (8/bits).
+__host__ __device__ __forceinline__ int lowbit_k_byte(int bits, int t, int d) {
+    const int kg = d / (16 * (8 / bits));
+    const int c = d & 15;
+    const int lane = 4 * (t & 7) + ((c & 7) >> 1);
+    return lowbit_word(kg, lane, t >> 3) * 4 + ((c & 1) | ((c >> 3) << 1));
+}
+__host__ __device__ __forceinline__ int lowbit_v_byte(int bits, int t, int d) {
+    const int kg = d / (16 * (8 / bits));
+    const int r = d & 15;
+    const int lane = 4 * (r & 7) + ((t & 7) >> 1);
+    return lowbit_word(kg, lane, t >> 3) * 4 + ((t & 1) | ((r >> 3) << 1));
+}
+
+// Nearest half-precision value, saturated to ±65,504 instead of overflowing.
+__device__ __forceinline__ __half half_sat(float v) {
+    const __half h = __float2half_rn(v);
+    if (__hisinf(h)) return __ushort_as_half(v > 0.f ? 0x7BFFu : 0xFBFFu);
+    return h;
+}
+
+// Quantise one group of a row held LPG lanes × 4 values (a group = 4·LPG consecutive dims):
+// mn, mx over the group; scale = half(fp32((mx − mn)/(2^BITS − 1))), 1 when that is 0;
+// zero = half(mn); code = clamp(rint(fp32(fp32(x − zero)/scale)), 0, 2^BITS − 1), single
+// precision, ties to even.  Returns the (scale, zero) bits packed as one word.
+template <int BITS, int LPG>
+__device__ __forceinline__ uint32_t lowbit_quantise(const float (&x)[4], int (&code)[4]) {
+    constexpr float kTop = static_cast<float>((1 << BITS) - 1);
+    float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
+    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+    #pragma unroll
+    for (int o = 1; o < LPG; o <<= 1) {
+        mn = fminf(mn, __shfl_xor_sync(kFull, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+    }
+    __half hs = half_sat(__fdiv_rn(__fsub_rn(mx, mn), kTop));
+    if (__half2float(hs) == 0.f) hs = __float2half_rn(1.f);
+    const __half hz = half_sat(mn);
+    const float s = __half2float(hs), z = __half2float(hz);
+    #pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float r = rintf(__fdiv_rn(__fsub_rn(x[k], z), s));
+        code[k] = static_cast<int>(fminf(fmaxf(r, 0.f), kTop));
+    }
+    return static_cast<uint32_t>(__half_as_ushort(hs)) | (static_cast<uint32_t>(__half_as_ushort(hz)) << 16);
+}
+
+// Write one token's K and V rows into slot t of a low-bit record, by one warp (lane l holds
+// dims 4l..4l+3).  A byte takes the codes of dims 16 apart from 8/BITS lanes; the lanes that
+// own its first dim gather them by shuffles and store whole bytes, so tokens written at the
+// same time never share a byte.
+template <int BITS, int NG>
+__device__ __forceinline__ void write_token_lowbit(uint8_t* record, int t, const uint16_t* krow, const uint16_t* vrow,
+                                                   int lane) {
+    constexpr int kLpg = 32 / NG;          // lanes per group
+    constexpr int kPer = 8 / BITS;         // codes per byte
+    constexpr int kTile = lowbit_tile_bytes(BITS);
+    const uint2 kraw = *reinterpret_cast<const uint2*>(krow + lane * 4);
+    const uint2 vraw = *reinterpret_cast<const uint2*>(vrow + lane * 4);
+    const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(&kraw);
+    const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(&vraw);
+    float kx[4], vx[4];
+    #pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        kx[j] = __bfloat162float(kb[j]);
+        vx[j] = __bfloat162float(vb[j]);
+    }
+    int kc[4], vc[4];
+    const uint32_t ksz = lowbit_quantise<BITS, kLpg>(kx, kc);
+    const uint32_t vsz = lowbit_quantise<BITS, kLpg>(vx, vc);
+    uint32_t kp = 0, vp = 0;   // this lane's 4 codes, code j in bits BITS·j
+    #pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        kp |= static_cast<uint32_t>(kc[j]) << (BITS * j);
+        vp |= static_cast<uint32_t>(vc[j]) << (BITS * j);
+    }
+    // field h of a byte comes from lane + 4h (dims 16h further on)
+    uint32_t kf[kPer], vf[kPer];
+    kf[0] = kp;
+    vf[0] = vp;
+    #pragma unroll
+    for (int h = 1; h < kPer; ++h) {
+        kf[h] = __shfl_down_sync(kFull, kp, 4 * h);
+        vf[h] = __shfl_down_sync(kFull, vp, 4 * h);
+    }
+    if ((lane & (4 * kPer - 4)) == 0) {
+        #pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t kbyte = 0, vbyte = 0;
+            #pragma unroll
+            for (int h = 0; h < kPer; ++h) {
+                kbyte |= ((kf[h] >> (BITS * j)) & ((1u << BITS) - 1)) << (BITS * h);
+                vbyte |= ((vf[h] >> (BITS * j)) & ((1u << BITS) - 1)) << (BITS * h);
+            }
+            const int d = 4 * lane + j;
+            record[lowbit_k_byte(BITS, t, d)] = static_cast<uint8_t>(kbyte);
+            record[kTile + lowbit_v_byte(BITS, t, d)] = static_cast<uint8_t>(vbyte);
+        }
+    }
+    if (lane % kLpg == 0) {
+        const int gi = lane / kLpg;
+        uint32_t* meta = reinterpret_cast<uint32_t*>(record + 2 * kTile);
+        meta[t * NG + gi] = ksz;
+        meta[kBs * NG + t * NG + gi] = vsz;
+    }
+}
+
 // 16-byte asynchronous copy global → shared through the load path (any global address the
 // GPU maps, host memory included).  Both addresses 16-byte aligned.
 __device__ __forceinline__ void cp_async16_g2s(void* dst, const void* src) {

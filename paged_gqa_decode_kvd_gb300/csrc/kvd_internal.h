@@ -8,8 +8,10 @@ struct kvd_pool;
 
 namespace kvd {
 
-// Pool kinds: every block BF16, every block FP8-E4M3, or mixed (a precision byte per block).
-constexpr int kKindBf16 = 0, kKindFp8 = 1, kKindMixed = 2;
+// Pool kinds: every block BF16, every block FP8-E4M3, mixed (a precision byte per block), or
+// low-bit (4-bit or 2-bit codes with a half-precision scale and zero point per group of values).
+constexpr int kKindBf16 = 0, kKindFp8 = 1, kKindMixed = 2, kKindInt4 = 3, kKindInt2 = 4;
+__host__ __device__ constexpr bool is_lowbit(int kind) { return kind == kKindInt4 || kind == kKindInt2; }
 
 // Device ordinal the pool was created on (its memory and state live there).
 int pool_device(const kvd_pool* pool);
@@ -22,6 +24,7 @@ struct AppendParams {
     uint8_t* host_kv;            // this layer's host-tier records (device address), or null
     const uint8_t* block_fmt;    // mixed pools: precision code of every physical block
     int32_t* err;
+    int ng;                      // low-bit pools: groups per 128-value row (128 / group size)
     int64_t n_tokens;
     int64_t num_blocks;
     int64_t host_blocks;         // host-tier blocks: ids num_blocks .. num_blocks + host_blocks - 1
@@ -59,6 +62,7 @@ struct DecodeParams {
     int g;
     int n_q;
     int nsplit;
+    int ng;                      // low-bit pools: groups per 128-value row (1, 2 or 4)
     int max_seq_len;             // host bound on seq_lens (only used to warm L2)
     int early;                   // KVD_EARLY_START: plan and K/V copies before the grid dependency wait
     float scale_log2;            // softmax_scale * log2(e)
@@ -147,10 +151,15 @@ struct TierMoveParams {
     int n_kv;
 };
 cudaError_t launch_tier_move(const TierMoveParams& p, int num_sms, cudaStream_t stream);
-size_t decode_smem_bytes(int kind, int batch, int g);
-int decode_ctas_per_sm(int kind, int batch, int g);
-int decode_carveout(int kind, int batch, int g);   // percent, for the decode call's launches
+// Decode launch geometry and launch for a pool kind (ng: groups per row of a low-bit pool, else 1).
+size_t decode_smem_bytes(int kind, int ng, int batch, int g);
+int decode_ctas_per_sm(int kind, int ng, int batch, int g);
+int decode_carveout(int kind, int ng, int batch, int g);   // percent, for the decode call's launches
 cudaError_t launch_decode(const DecodeParams& p, int kind, int carveout, cudaStream_t stream);
+// The low-bit kinds' variants (their own translation unit).
+size_t decode_smem_bytes_lowbit(int kind, int ng, int batch, int g);
+int decode_ctas_per_sm_lowbit(int kind, int ng, int batch, int g);
+cudaError_t launch_decode_lowbit(const DecodeParams& p, int kind, int carveout, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int carveout, cudaStream_t stream);
 cudaError_t launch_scores(const ScoreParams& p, cudaStream_t stream);
 cudaError_t launch_epilogue(const CombineParams& c, const ScoreParams& sp, int carveout, cudaStream_t stream);

@@ -31,14 +31,15 @@ def assert_out_close(gpu, ref, atol=OUT_ATOL, rtol=OUT_RTOL, what="out"):
 
 
 def dtype_code(w: Workload) -> int:
-    return {"bf16": kvd.KVD_BF16, "fp8_e4m3": kvd.KVD_FP8_E4M3, "mixed": kvd.KVD_MIXED}[w.kv_dtype]
+    return {"bf16": kvd.KVD_BF16, "fp8_e4m3": kvd.KVD_FP8_E4M3, "mixed": kvd.KVD_MIXED, "int4": kvd.KVD_INT4,
+            "int2": kvd.KVD_INT2}[w.kv_dtype]
 
 
 FORMAT_CODES = (kvd.KVD_BF16, kvd.KVD_FP8_E4M3, kvd.KVD_FP8_E5M2)   # index = oracle format code
 
 
 def make_pool(w: Workload, layers: int | None = None, poison: bool = True) -> kvd.KVPool:
-    pool = kvd.KVPool(layers or w.L, w.n_kv, w.num_blocks(), dtype_code(w))
+    pool = kvd.KVPool(layers or w.L, w.n_kv, w.num_blocks(), dtype_code(w), group_size=w.group_size)
     if poison:   # NaN everywhere first (codes, bf16 values, fp32 scales): unwritten slots must never leak
         pool.mem.fill_(0xFF)
     if w.kv_dtype == "mixed":
@@ -82,6 +83,8 @@ def oracle_layer(w: Workload, layer: int, bt_cpu: torch.Tensor, seq_lens: list[i
     """fp64 oracle over the oracle's own pool filled from the same seeded inputs."""
     if w.kv_dtype == "mixed":
         pool = oracle.OraclePool(w.num_blocks(), w.n_kv, w.d_h, 16, block_fmt=w.block_formats())
+    elif w.lowbit:
+        pool = oracle.OraclePool(w.num_blocks(), w.n_kv, w.d_h, 16, lowbit=w.lowbit)
     else:
         pool = oracle.OraclePool(w.num_blocks(), w.n_kv, w.d_h, 16, w.kv_dtype != "bf16")
     for b in range(w.batch):
@@ -133,3 +136,40 @@ def read_scales(pool: kvd.KVPool, layer: int, block: int, head: int):
     off = ((layer * pool.num_blocks + block) * pool.n_kv + head) * pool.record_bytes + 4096
     s = pool.mem[off:off + 128].cpu().view(torch.float32).numpy()
     return s[:16], s[16:]
+
+
+def _lowbit_positions(bits: int, kind: str):
+    """(byte index, bit shift) [16][128] of the code of (token t, dim d) in a low-bit K or V tile,
+    from the layout the header documents."""
+    t = np.arange(16)[:, None]
+    d = np.arange(128)[None, :]
+    per = 8 // bits
+    kg = d // (16 * per)
+    h = (d // 16) % per
+    c = d % 16
+    if kind == "k":
+        lane = 4 * (t % 8) + (c % 8) // 2
+        j = (c % 2) + 2 * (c // 8)
+    else:
+        lane = 4 * (c % 8) + (t % 8) // 2
+        j = (t % 2) + 2 * (c // 8)
+    th = t // 8
+    byte = (((kg // 2) * 32 + lane) * 4 + (kg % 2) * 2 + th) * 4 + j
+    return np.broadcast_to(byte, (16, 128)), np.broadcast_to(h * bits, (16, 128))
+
+
+def read_lowbit_record(pool: kvd.KVPool, layer: int, block: int, head: int):
+    """(K codes, V codes [16][128] uint8, K scales, K zeros, V scales, V zeros [16][ng] float32) of one
+    record of a low-bit pool, unpacked from the documented layout."""
+    bits = 4 if pool.kv_dtype == kvd.KVD_INT4 else 2
+    ng = 128 // pool.group_size
+    rb = pool.record_bytes
+    tile = 256 * bits
+    off = ((layer * pool.num_blocks + block) * pool.n_kv + head) * rb
+    raw = pool.mem[off:off + rb].cpu().numpy()
+    out = []
+    for kind, base in (("k", 0), ("v", tile)):
+        byte, shift = _lowbit_positions(bits, kind)
+        out.append(((raw[base + byte] >> shift) & ((1 << bits) - 1)).astype(np.uint8))
+    meta = raw[2 * tile:].view(np.float16).astype(np.float32).reshape(2, 16, ng, 2)
+    return out[0], out[1], meta[0, ..., 0], meta[0, ..., 1], meta[1, ..., 0], meta[1, ..., 1]

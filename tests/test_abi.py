@@ -52,6 +52,21 @@ def test_fp8_scale_bytes():
     assert pool == kv == 32 * 8192 * 131072 // 8192 * 8192     # 32 GiB: 128 KiB per token
 
 
+def test_lowbit_pool_bytes():
+    """Low-bit pools: codes at w_kv = bits/8 (the closed form 2·L·n_kv·d_h·w_kv per token), plus a
+    32-bit (scale, zero point) entry per (token, KV head, group) for K and for V."""
+    for dtype, bits in ((kvd.KVD_INT4, 4), (kvd.KVD_INT2, 2)):
+        for group in (32, 64, 128):
+            pool, kv = kvd.kvd_pool_bytes(80, 8, 8192, dtype, group_size=group)
+            tokens = 8192 * 16
+            assert kv == 2 * 80 * 8 * 128 * bits * tokens // 8
+            assert pool - kv == 2 * 80 * 8 * (128 // group) * 4 * tokens
+    # 70B shape, 128k context: 2-bit codes are an eighth of the BF16 bytes (the page's c = 8)
+    _, bf16 = kvd.kvd_pool_bytes(80, 8, 8192, kvd.KVD_BF16)
+    _, int2 = kvd.kvd_pool_bytes(80, 8, 8192, kvd.KVD_INT2, group_size=128)
+    assert bf16 == 8 * int2
+
+
 def test_host_tier_bytes():
     """A host tier of hb blocks holds every layer's records of those blocks in host memory;
     its HBM staging area holds two layers' worth (the prefetch of the next layer overlaps the

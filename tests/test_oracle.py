@@ -602,11 +602,12 @@ def _lowbit_case(seed, rows=400, d=128):
 
 
 @pytest.mark.parametrize("bits", [4, 2])
-def test_lowbit_quantise_closed_forms(bits):
-    """Per group of 32: the scale is the group's span / (2^bits - 1) to half precision, the zero
+@pytest.mark.parametrize("G", [32, 64, 128])
+def test_lowbit_quantise_closed_forms(bits, G):
+    """Per group of G values: the scale is the group's span / (2^bits - 1) to half precision, the zero
     point its minimum to half precision, codes span [0, 2^bits - 1] and reconstruct every value
     to within half a scale (plus the half-precision rounding of the scale and zero)."""
-    G, top = 32, (1 << bits) - 1
+    top = (1 << bits) - 1
     x = _lowbit_case(41)
     codes, scales, zeros = oracle.quantize_rows_lowbit(x, bits, G)
     xg = x.reshape(x.shape[0], -1, G).astype(np.float64)
@@ -630,16 +631,18 @@ def test_lowbit_quantise_closed_forms(bits):
     cg = codes.reshape(xg.shape)
     assert np.all(cg[np.arange(xg.shape[0])[:, None], np.arange(xg.shape[1]), xg.argmin(-1)][nz] == 0)
     assert np.all(cg[np.arange(xg.shape[0])[:, None], np.arange(xg.shape[1]), xg.argmax(-1)][nz] >= top - 1)
-    # constant group: scale 1, code 0, value = the half-precision zero point
-    assert scales[6, 0] == 1.0 and np.all(codes[6, :32] == 0) and zeros[6, 0] == np.float32(1.25)
+    # constant group (the first 32 values of row 6): scale 1, code 0, value = the half-precision zero point
+    if G == 32:
+        assert scales[6, 0] == 1.0 and np.all(codes[6, :32] == 0) and zeros[6, 0] == np.float32(1.25)
 
 
 @pytest.mark.parametrize("bits", [4, 2])
-def test_lowbit_codes_are_the_nearest_level(bits):
+@pytest.mark.parametrize("G", [32, 128])
+def test_lowbit_codes_are_the_nearest_level(bits, G):
     """Brute force: given the group's scale and zero, the stored code is the level c·scale + zero
     nearest to x among all 2^bits levels (x below the lowest level takes code 0, above the highest
     the top code); an exact tie may go either way only if the single-precision quotient rounded."""
-    G, top = 32, (1 << bits) - 1
+    top = (1 << bits) - 1
     x = _lowbit_case(42, rows=200)
     codes, scales, zeros = oracle.quantize_rows_lowbit(x, bits, G)
     lv = np.arange(top + 1, dtype=np.float64)
