@@ -12,9 +12,10 @@ Prints one JSON line.  `value` is the closed-form K/V bytes attended per step,
 2·L·n_kv·d_h·w_kv per token (FP8 scales excluded), divided by the step time, in GB/s,
 with every input resident in HBM.  Default workload: Llama-3.1-8B shape, 32 layers,
 batch 32, context 8,192, BF16 KV (34.4 GB of KV per step, far larger than L2).  The
-default run also times the ragged, 70B FP8 and tiered workloads (key `workloads`, each
-with its own value, roofline and clocks), and measures the read-only HBM stream
-(`hbm_read_peak`) beside the copy peak of MEASURED_PEAKS.json.
+default run also times the ragged, 70B FP8, tiered, mixed-precision and 70B INT4 / 2-bit
+workloads (key `workloads`, each with its own value, roofline and clocks), and measures the
+read-only HBM stream (`hbm_read_peak`) beside the copy peak of MEASURED_PEAKS.json.  For the
+8-bit and low-bit pools the roofline counts the scales (and zero points) with the codes.
 
 `--impl reference` times the fp64 CPU oracle instead: each step is a bounded sample of the
 workload, one whole (layer, request) unit per host thread.
@@ -216,8 +217,9 @@ class Step:
         self.w, self.dev, self.kvd = w, dev, kvd
         self.early = early   # KVD_EARLY_START: the step's tables and pool are not written by the previous kernel
         self.L = w.L
-        kind = {"bf16": kvd.KVD_BF16, "fp8_e4m3": kvd.KVD_FP8_E4M3, "mixed": kvd.KVD_MIXED}[w.kv_dtype]
-        self.pool = kvd.KVPool(w.L, w.n_kv, w.num_blocks(), kind, device=dev)
+        kind = {"bf16": kvd.KVD_BF16, "fp8_e4m3": kvd.KVD_FP8_E4M3, "mixed": kvd.KVD_MIXED, "int4": kvd.KVD_INT4,
+                "int2": kvd.KVD_INT2}[w.kv_dtype]
+        self.pool = kvd.KVPool(w.L, w.n_kv, w.num_blocks(), kind, device=dev, group_size=w.group_size)
         if w.kv_dtype == "mixed":   # a storage format per physical block
             codes = [kvd.KVD_BF16, kvd.KVD_FP8_E4M3, kvd.KVD_FP8_E5M2]
             fmt = torch.tensor([codes[f] for f in w.block_formats().tolist()], dtype=torch.uint8)
@@ -569,7 +571,8 @@ def workload_config(w) -> dict:
     return {"workload": f"{w.name}: {w.description}", "layers": w.L, "batch": w.batch, "n_q": w.n_q,
             "n_kv": w.n_kv, "d_h": w.d_h, "kv_dtype": w.kv_dtype,
             "context": w.seq_lens(0)[:4] if w.batch > 4 else w.seq_lens(0),
-            "kv_bytes_per_step": w.kv_bytes_per_step(), "fp8_scale_bytes_per_step": w.scale_bytes_per_step(),
+            "kv_bytes_per_step": w.kv_bytes_per_step(), "scale_bytes_per_step": w.scale_bytes_per_step(),
+            "group_size": w.group_size or None,
             "decode_steps_cycled": w.steps, "scores": bool(w.scores), "seed": w.seed,
             "l2": "inputs larger than L2 (KV pool streamed every step)"}
 
@@ -684,7 +687,9 @@ def gpu_workload(args, w, rank, world, local, peaks, headline: bool) -> dict:
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": {"bf16": "bf16", "fp8_e4m3": "fp8_e4m3",
-                                       "mixed": "mixed: bf16 / fp8_e4m3 / fp8_e5m2 per block"}[w.kv_dtype],
+                                       "mixed": "mixed: bf16 / fp8_e4m3 / fp8_e5m2 per block",
+                                       "int4": f"int4 (group {w.group_size}, f16 scale and zero)",
+                                       "int2": f"int2 (group {w.group_size}, f16 scale and zero)"}[w.kv_dtype],
         "data": "synthetic (seeded counter-hash generator)",
         "config": workload_config(w),
         "launch": {"num_splits": st.splits, "early_start": st.early,
@@ -759,7 +764,7 @@ def e2e_steps(st, args, world) -> dict:
                    "copied from pinned host memory and its outputs back, every step"}
 
 
-EXTRA_WORKLOADS = ("ragged", "llama70b_fp8", "tiered", "llama8b_mixed")
+EXTRA_WORKLOADS = ("ragged", "llama70b_fp8", "tiered", "llama8b_mixed", "llama70b_int4", "llama70b_int2")
 
 
 def gpu_arm(args, w, rank, world, local):
@@ -810,6 +815,8 @@ def _oracle_unit(w, layer: int, b: int, kf, vf, q, fmt=None):
     table = np.arange(nblk, dtype=np.int32)[None, :]
     if fmt is not None:
         pool = oracle.OraclePool(nblk, w.n_kv, w.d_h, 16, block_fmt=fmt)
+    elif w.lowbit:
+        pool = oracle.OraclePool(nblk, w.n_kv, w.d_h, 16, lowbit=w.lowbit)
     else:
         pool = oracle.OraclePool(nblk, w.n_kv, w.d_h, 16, w.kv_dtype != "bf16")
     pool.append(kf, vf, slots)
@@ -931,11 +938,13 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="llama8b")
     ap.add_argument("--only", action="store_true",
-                    help="time the chosen workload alone (the default run also times the ragged, 70B FP8 and "
-                         "tiered workloads)")
+                    help="time the chosen workload alone (the default run also times the ragged, 70B FP8, "
+                         "tiered, mixed-precision and 70B low-bit workloads)")
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling captures)")
     ap.add_argument("--context", type=int, default=0, help="override every request's context (size sweeps)")
+    ap.add_argument("--group-size", type=int, default=0,
+                    help="low-bit workloads: values per scale group (32, 64 or 128) instead of the workload's")
     ap.add_argument("--no-early-start", action="store_true", help="launch the decode kernel without KVD_EARLY_START")
     ap.add_argument("--fused-scores", action="store_true",
                     help="score update inside each layer's epilogue launch (one stream) instead of on a second stream")
@@ -968,6 +977,12 @@ def main(argv=None):
             ap.error("--context applies to fixed-context workloads only")
         w._ctx0 = [args.context] * w.batch
         w.description += f" [context set to {args.context} for a size sweep]"
+        args.only = True
+    if args.group_size:
+        if not w.lowbit:
+            ap.error("--group-size applies to the low-bit workloads only")
+        w.group_size = args.group_size
+        w.description += f" [group size set to {args.group_size}]"
         args.only = True
     if world > 1:
         import torch.distributed as dist
