@@ -7,7 +7,8 @@ library (``paged_gqa_decode_kvd_gb300``) and neither imports the other.
 Parity pins (all in ``tests/test_oracle.py``, run with ``-m "not gpu"``):
 e4m3 and e5m2 decode/encode, row quantise in both formats, the mixed-precision
 pool, half-precision rounding, the low-bit (INT4 / 2-bit) group quantise and
-its pool, the paged gather, decode attention, the
+its pool, the angle-domain key rows and query and their pool, the paged gather, decode
+attention, the
 split-free softmax statistics, the importance-score update and the block tier
 plan are each pinned
 to something other than the oracle itself; no function here is "parity
@@ -28,6 +29,8 @@ from .oracle import (  # noqa: F401
     FMT_E5M2,
     round_half_sat,
     quantize_rows_lowbit,
+    angle_key_rows,
+    angle_query,
     OraclePool,
     decode,
     score_update,

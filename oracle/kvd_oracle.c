@@ -17,6 +17,10 @@
  *    page, §3.2 (2-bit storage raises decode intensity to 64 FLOP/B), §4.2,
  *    §4.6 and Tab. 7 (KIVI 2-bit, KVQuant INT4); the group layout is this
  *    oracle's reading (the pages give none).
+ *  - Angle-domain keys (a radius and a code of the direction; the logit is
+ *    ||q||·r̃·cos of the two codes): page "기술 요약: Spherical KV"
+ *    (gist.science/ko/paper/2605.18856), §2.1; the direction code and the
+ *    cosine's form are this oracle's reading (the page defines neither).
  *  - Paged cache: fixed 16-token blocks and a per-request block table that
  *    maps the request's j-th block to a physical block; the kernel walks the
  *    table in order, so scattered blocks give the same result: same page and
@@ -349,6 +353,78 @@ int kvdo_append_lowbit(int n_kv, int d_h, int block_size, int64_t num_blocks, in
                 v_val[row * d_h + i] = v_codes[row * d_h + i] * (double)v_scales[row * ng + i / group] +
                                        (double)v_zeros[row * ng + i / group];
             }
+        }
+    }
+    return KVDO_OK;
+}
+
+/* ------------------------------------------------------- angle-domain keys */
+
+/* One key row in the angle domain (page "기술 요약: Spherical KV", §2.1, Angle-Domain
+ * Attention): the key k splits into a radius r = ||k|| and a direction; the cache keeps a
+ * quantised radius r̃ and a code of the direction, and a logit is ||q||·r̃·f_b(c_q, c_k), f_b
+ * the cosine of two direction codes.  The page defines neither the code nor f_b; this oracle
+ * reads them as:
+ *   c = the E4M3 codes of the row at its absmax scale (kvdo_quantize_row: they depend on the
+ *       direction only, not on ||k||), d = their values (kvdo_e4m3_decode);
+ *   r̃ = the nearest half-precision value of ||k|| (saturating);
+ *   f_b(c_q, c_k) = <d_q, d_k> / (||d_q||·||d_k||).
+ * So the key attention sees is w·d with w = fp32(r̃ / ||d||), computed in fp64 (w = 0 for a
+ * zero row); codes [d], *w_out, *r_out (r̃). */
+void kvdo_angle_key_row(const float* x, int d, uint8_t* codes, float* w_out, float* r_out) {
+    float scale;
+    kvdo_quantize_row(x, d, codes, &scale);
+    double r2 = 0.0, d2 = 0.0;
+    for (int i = 0; i < d; ++i) {
+        double c = kvdo_e4m3_decode(codes[i]);
+        r2 += (double)x[i] * (double)x[i];
+        d2 += c * c;
+    }
+    double rh = kvdo_round_half_sat(sqrt(r2));
+    *r_out = (float)rh;
+    *w_out = d2 > 0.0 ? (float)(rh / sqrt(d2)) : 0.0f;
+}
+
+void kvdo_angle_key_rows(const float* x, int64_t rows, int d, uint8_t* codes, float* w, float* r) {
+    for (int64_t i = 0; i < rows; ++i) kvdo_angle_key_row(x + i * d, d, codes + i * d, w + i, r + i);
+}
+
+/* The query side of the same cosine: each row q becomes (||q|| / ||d_q||)·d_q, d_q the values of
+ * its E4M3 codes at its absmax scale (0 for a zero row), so that <q', w·d_k> = ||q||·r̃·f_b. */
+void kvdo_angle_query(const float* q, int64_t rows, int d, double* out) {
+    uint8_t* codes = (uint8_t*)malloc((size_t)d);
+    for (int64_t i = 0; i < rows; ++i) {
+        float scale;
+        const float* x = q + i * d;
+        kvdo_quantize_row(x, d, codes, &scale);
+        double q2 = 0.0, d2 = 0.0;
+        for (int j = 0; j < d; ++j) {
+            double c = kvdo_e4m3_decode(codes[j]);
+            q2 += (double)x[j] * (double)x[j];
+            d2 += c * c;
+        }
+        double f = d2 > 0.0 ? sqrt(q2) / sqrt(d2) : 0.0;
+        for (int j = 0; j < d; ++j) out[i * d + j] = f * kvdo_e4m3_decode(codes[j]);
+    }
+    free(codes);
+}
+
+/* Append into an angle-domain pool: K rows as kvdo_angle_key_row (codes and the factor w in
+ * k_scales), V rows FP8 as kvdo_quantize_row (codes and scale).  Layout as kvdo_append. */
+int kvdo_append_angle(int n_kv, int d_h, int block_size, int64_t num_blocks, const float* k_new,
+                      const float* v_new, const int64_t* slot_mapping, int64_t N, uint8_t* k_codes,
+                      uint8_t* v_codes, float* k_scales, float* v_scales, float* k_radius) {
+    for (int64_t n = 0; n < N; ++n) {
+        int64_t slot = slot_mapping[n];
+        if (slot < 0) continue;
+        int64_t blk = slot / block_size;
+        int64_t off = slot % block_size;
+        if (blk >= num_blocks) return KVDO_ERR_INDEX;
+        for (int h = 0; h < n_kv; ++h) {
+            int64_t row = (blk * n_kv + h) * block_size + off;
+            kvdo_angle_key_row(k_new + (n * n_kv + h) * d_h, d_h, k_codes + row * d_h, k_scales + row,
+                               k_radius + row);
+            kvdo_quantize_row(v_new + (n * n_kv + h) * d_h, d_h, v_codes + row * d_h, v_scales + row);
         }
     }
     return KVDO_OK;

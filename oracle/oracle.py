@@ -73,6 +73,10 @@ def _load():
             lib.kvdo_quantize_rows_fmt.argtypes = [P, i64, i32, i32, P, P]
             lib.kvdo_append_mixed.restype = i32
             lib.kvdo_append_mixed.argtypes = [i32, i32, i32, i64, P, P, P, P, i64, P, P, P, P, P, P]
+            lib.kvdo_angle_key_rows.argtypes = [P, i64, i32, P, P, P]
+            lib.kvdo_angle_query.argtypes = [P, i64, i32, P]
+            lib.kvdo_append_angle.restype = i32
+            lib.kvdo_append_angle.argtypes = [i32, i32, i32, i64, P, P, P, i64, P, P, P, P, P]
             lib.kvdo_round_half_sat.restype = f64
             lib.kvdo_round_half_sat.argtypes = [f64]
             lib.kvdo_round_half_sat_array.argtypes = [P, i64, P]
@@ -167,21 +171,55 @@ def quantize_rows_lowbit(x, bits: int, group: int) -> tuple[np.ndarray, np.ndarr
     return codes, scales, zeros
 
 
+def angle_key_rows(x) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """Angle-domain key rows of float32 [..., d]: (E4M3 direction codes [..., d], the logit factor
+    w = fp32(r̃ / ||d||) [...], the half-precision radius r̃ [...]); the key attention sees is w·d."""
+    a = _c(x, np.float32)
+    d = a.shape[-1]
+    rows = a.size // d
+    codes = np.empty(a.shape, np.uint8)
+    w = np.empty(a.shape[:-1], np.float32)
+    r = np.empty(a.shape[:-1], np.float32)
+    _load().kvdo_angle_key_rows(_p(a), rows, d, _p(codes), _p(w), _p(r))
+    return codes, w, r
+
+
+def angle_query(q) -> np.ndarray:
+    """Each row q (float32 [..., d]) as (||q|| / ||d_q||)·d_q in fp64, d_q its E4M3 direction code's
+    values: the query of an angle-domain logit."""
+    a = _c(q, np.float32)
+    out = np.empty(a.shape, np.float64)
+    _load().kvdo_angle_query(_p(a), a.size // a.shape[-1], a.shape[-1], _p(out))
+    return out
+
+
 class OraclePool:
     """The oracle's own paged pool for one layer: [num_blocks][n_kv][block_size][d_h].
 
     block_fmt (uint8 [num_blocks], optional) makes it a mixed-precision pool: block p holds
     BF16 values (0), E4M3 codes (1) or E5M2 codes (2), each 8-bit row with its own scale.
     lowbit = (bits, group) makes it a low-bit pool: every row of K and V holds bits-wide codes
-    with a scale and a zero point per group of `group` values."""
+    with a scale and a zero point per group of `group` values.
+    angle=True makes it an angle-domain pool: K rows hold E4M3 direction codes with the factor
+    w = r̃/||d|| in k_scales (radius r̃ in k_radius), V rows FP8; decode it with a query passed
+    through angle_query."""
 
     def __init__(self, num_blocks: int, n_kv: int, d_h: int, block_size: int = 16, fp8: bool = False,
-                 block_fmt=None, lowbit=None):
+                 block_fmt=None, lowbit=None, angle: bool = False):
         self.num_blocks, self.n_kv, self.d_h, self.block_size, self.fp8 = num_blocks, n_kv, d_h, block_size, fp8
         shape = (num_blocks, n_kv, block_size, d_h)
         self.block_fmt = None
         self.lowbit = None
-        if lowbit is not None:
+        self.angle = bool(angle)
+        if self.angle:
+            self.fp8 = True
+            self.k_codes = np.zeros(shape, np.uint8)
+            self.v_codes = np.zeros(shape, np.uint8)
+            self.k_scales = np.zeros(shape[:-1], np.float32)
+            self.v_scales = np.ones(shape[:-1], np.float32)
+            self.k_radius = np.zeros(shape[:-1], np.float32)
+            self.k = self.v = None
+        elif lowbit is not None:
             self.lowbit = (int(lowbit[0]), int(lowbit[1]))
             ng = d_h // self.lowbit[1]
             assert ng * self.lowbit[1] == d_h and self.lowbit[0] in (2, 4)
@@ -218,6 +256,10 @@ class OraclePool:
         k = _c(k_new, np.float32)
         v = _c(v_new, np.float32)
         s = _c(slot_mapping, np.int64)
+        if self.angle:
+            return _load().kvdo_append_angle(self.n_kv, self.d_h, self.block_size, self.num_blocks, _p(k), _p(v),
+                                             _p(s), s.size, _p(self.k_codes), _p(self.v_codes), _p(self.k_scales),
+                                             _p(self.v_scales), _p(self.k_radius))
         if self.lowbit is not None:
             return _load().kvdo_append_lowbit(self.n_kv, self.d_h, self.block_size, self.num_blocks, self.lowbit[0],
                                               self.lowbit[1], _p(k), _p(v), _p(s), s.size, _p(self.k), _p(self.v),

@@ -691,3 +691,116 @@ def test_lowbit_bytes_and_intensity_closed_forms():
     for bits, row in ((4, 64 + 16), (2, 32 + 16)):
         assert 128 * bits // 8 + (128 // 32) * 4 == row
     assert bench.decode_intensity(8, 0.25) == 64 and bench.decode_intensity(8, 0.5) == 32
+
+
+# ------------------------------------------------------------- angle-domain keys
+def _angle_case(seed, rows=300, d=128):
+    r = _rng(seed)
+    x = r.standard_normal((rows, d)).astype(np.float32)
+    x[3] = 0.0                                     # a zero row
+    x[4] *= 1000.0                                 # a wide row
+    x[5, 7] = 250.0                                # one outlier
+    x[6] *= 1e-3                                   # a small row (subnormal codes)
+    return _bf16(x)
+
+
+def _torch_e4m3_codes(x):
+    """Codes of each row at its absmax scale through torch's float8_e4m3fn cast (fp32 quotient)."""
+    amax = np.abs(x).max(-1).astype(np.float32)
+    scale = np.where(amax == 0, np.float32(1), (amax / np.float32(448)).astype(np.float32)).astype(np.float32)
+    y = torch.from_numpy((x / scale[:, None]).astype(np.float32)).clamp(-448, 448)
+    c = y.to(torch.float8_e4m3fn)
+    return c.view(torch.uint8).numpy(), c.to(torch.float64).numpy()
+
+
+def test_angle_key_rows_radius_code_and_factor():
+    """Angle-domain keys ("기술 요약: Spherical KV", §2.1: radius r = ||k|| kept quantised, direction kept
+    as a code): r̃ is numpy's float16 of the fp64 norm; the direction code is torch's E4M3 cast of the
+    row at its absmax scale; the key attention sees, w·d, has the stored radius as its norm (to the fp32
+    rounding of w) and points within the E4M3 direction error of k (3 mantissa bits: cos >= 1 - 2^-7)."""
+    x = _angle_case(60)
+    codes, w, rad = oracle.angle_key_rows(x)
+    xd = x.astype(np.float64)
+    norm = np.linalg.norm(xd, axis=1)
+    assert np.array_equal(rad, norm.astype(np.float16).astype(np.float32))
+    tc, tv = _torch_e4m3_codes(x)
+    assert np.array_equal(codes, tc)
+    keff = w[:, None].astype(np.float64) * tv
+    nz = norm > 0
+    assert np.all(np.abs(np.linalg.norm(keff, axis=1)[nz] - rad[nz]) <= 2.0 ** -23 * rad[nz])
+    cos = (keff * xd).sum(1)[nz] / (np.linalg.norm(keff, axis=1)[nz] * norm[nz])
+    assert cos.min() >= 1 - 2.0 ** -7, cos.min()
+    assert w[3] == 0 and rad[3] == 0 and np.all(codes[3] == 0)
+
+
+def test_angle_direction_code_ignores_the_radius():
+    """Scaling a key by 2^j leaves its direction code unchanged and scales r̃ and w by 2^j."""
+    x = _angle_case(61, rows=50)
+    x = x[np.abs(x).max(1) < 100]
+    c0, w0, r0 = oracle.angle_key_rows(x)
+    for j in (-3, 2, 5):
+        c, w, r = oracle.angle_key_rows((x * np.float32(2.0 ** j)).astype(np.float32))
+        assert np.array_equal(c, c0)
+        assert np.array_equal(r, (r0 * np.float32(2.0 ** j)).astype(np.float32))
+        assert np.array_equal(w, (w0 * np.float32(2.0 ** j)).astype(np.float32))
+
+
+def test_angle_logit_is_the_cosine_form():
+    """<angle_query(q), w·d_k> = ||q||·r̃·<d_q, d_k>/(||d_q||·||d_k||), the page's ℓ̂ = ||q||·r̃·f_b(c_q, c_k)
+    with f_b the cosine of the two codes (codes decoded through torch, norms by numpy); for rows already on
+    the E4M3 grid at their absmax scale it is (r̃/||k||)·<q, k>."""
+    q = _angle_case(62, rows=40)
+    k = _angle_case(63, rows=40)
+    qe = oracle.angle_query(q)
+    kc, w, rad = oracle.angle_key_rows(k)
+    _, dq = _torch_e4m3_codes(q)
+    _, dk = _torch_e4m3_codes(k)
+    got = (qe * (w[:, None].astype(np.float64) * dk)).sum(1)
+    nq = np.linalg.norm(q.astype(np.float64), axis=1)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        cosf = (dq * dk).sum(1) / (np.linalg.norm(dq, axis=1) * np.linalg.norm(dk, axis=1))
+    want = np.where(np.isfinite(cosf), nq * rad * cosf, 0.0)
+    np.testing.assert_allclose(got, want, rtol=1e-6, atol=1e-12)
+    # on-grid rows: values e4m3 numbers times 2^j with absmax exactly 448·2^j
+    r = _rng(64)
+    grid = np.array([oracle.e4m3_decode(np.array([c], np.uint8))[0] for c in range(0, 127)])
+    for j in (-4, 0, 3):
+        qv = (r.choice(np.concatenate([grid, -grid]), size=128) * 2.0 ** j).astype(np.float32)
+        kv = (r.choice(np.concatenate([grid, -grid]), size=128) * 2.0 ** j).astype(np.float32)
+        qv[0], kv[5] = np.float32(448 * 2.0 ** j), np.float32(-448 * 2.0 ** j)
+        qa = oracle.angle_query(qv[None])[0]
+        _, wk, rk = oracle.angle_key_rows(kv[None])
+        np.testing.assert_array_equal(qa, qv.astype(np.float64))
+        lhs = float(qa @ (wk[0] * oracle.e4m3_decode(oracle.angle_key_rows(kv[None])[0][0]).astype(np.float64)))
+        rhs = float(rk[0]) / np.linalg.norm(kv.astype(np.float64)) * float(qv.astype(np.float64) @ kv.astype(np.float64))
+        assert abs(lhs - rhs) <= 1e-6 * abs(rhs) + 1e-9
+
+
+def test_angle_pool_attention_matches_sdpa():
+    """Decode over an angle-domain pool, with the query passed through angle_query, equals dense SDPA
+    (fp64, torch) over keys w·d_k and values v_scale·d_v decoded through torch's float8 cast."""
+    r = _rng(65)
+    nb, n_kv, d_h, bs, n_q = 7, 2, 128, 16, 8
+    n = nb * bs - 5
+    k = _bf16(r.standard_normal((n, n_kv, d_h)).astype(np.float32))
+    v = _bf16(r.standard_normal((n, n_kv, d_h)).astype(np.float32))
+    slots = r.permutation(nb * bs)[:n].astype(np.int64)
+    pool = oracle.OraclePool(nb, n_kv, d_h, bs, angle=True)
+    assert pool.append(k, v, slots) == 0
+    q = _bf16(r.standard_normal((1, n_q, d_h)).astype(np.float32))
+    table = np.array([r.permutation(nb)], np.int32)
+    res = oracle.decode(pool, oracle.angle_query(q), n_q, table, np.array([n], np.int32))
+    _, kw, _ = oracle.angle_key_rows(k.reshape(-1, d_h))
+    _, kd = _torch_e4m3_codes(k.reshape(-1, d_h))
+    vsc = np.where(np.abs(v).max(-1) == 0, 1, (np.abs(v).max(-1) / np.float32(448)).astype(np.float32))
+    _, vd = _torch_e4m3_codes(v.reshape(-1, d_h))
+    # per physical slot: token t was written at slot slots[t]; the 5 slots never written read as 0
+    kslot = np.zeros((nb * bs, n_kv, d_h))
+    vslot = np.zeros((nb * bs, n_kv, d_h))
+    kslot[slots] = (kw[:, None] * kd).reshape(n, n_kv, d_h)
+    vslot[slots] = (vsc.reshape(-1)[:, None].astype(np.float64) * vd).reshape(n, n_kv, d_h)
+    kl = np.stack([kslot[int(table[0, t // bs]) * bs + t % bs] for t in range(n)])
+    vl = np.stack([vslot[int(table[0, t // bs]) * bs + t % bs] for t in range(n)])
+    qa = oracle.angle_query(q)[0]
+    ref = _dense_sdpa(qa, kl, vl, 1 / np.sqrt(d_h))
+    np.testing.assert_allclose(res["out"][0], ref, rtol=1e-12, atol=1e-12)
