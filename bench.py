@@ -12,8 +12,8 @@ Prints one JSON line.  `value` is the closed-form K/V bytes attended per step,
 2·L·n_kv·d_h·w_kv per token (FP8 scales excluded), divided by the step time, in GB/s,
 with every input resident in HBM.  Default workload: Llama-3.1-8B shape, 32 layers,
 batch 32, context 8,192, BF16 KV (34.4 GB of KV per step, far larger than L2).  The
-default run also times the ragged, 70B FP8, tiered, mixed-precision and 70B INT4 / 2-bit
-workloads (key `workloads`, each with its own value, roofline and clocks), and measures the
+default run also times the ragged, 70B FP8, tiered, mixed-precision, 70B INT4 / 2-bit and
+70B angle-domain workloads (key `workloads`, each with its own value, roofline and clocks), and measures the
 read-only HBM stream (`hbm_read_peak`) beside the copy peak of MEASURED_PEAKS.json.  For the
 8-bit and low-bit pools the roofline counts the scales (and zero points) with the codes.
 
@@ -218,7 +218,7 @@ class Step:
         self.early = early   # KVD_EARLY_START: the step's tables and pool are not written by the previous kernel
         self.L = w.L
         kind = {"bf16": kvd.KVD_BF16, "fp8_e4m3": kvd.KVD_FP8_E4M3, "mixed": kvd.KVD_MIXED, "int4": kvd.KVD_INT4,
-                "int2": kvd.KVD_INT2}[w.kv_dtype]
+                "int2": kvd.KVD_INT2, "angle": kvd.KVD_ANGLE}[w.kv_dtype]
         self.pool = kvd.KVPool(w.L, w.n_kv, w.num_blocks(), kind, device=dev, group_size=w.group_size)
         if w.kv_dtype == "mixed":   # a storage format per physical block
             codes = [kvd.KVD_BF16, kvd.KVD_FP8_E4M3, kvd.KVD_FP8_E5M2]
@@ -689,7 +689,9 @@ def gpu_workload(args, w, rank, world, local, peaks, headline: bool) -> dict:
         "vs_baseline": None, "dtype": {"bf16": "bf16", "fp8_e4m3": "fp8_e4m3",
                                        "mixed": "mixed: bf16 / fp8_e4m3 / fp8_e5m2 per block",
                                        "int4": f"int4 (group {w.group_size}, f16 scale and zero)",
-                                       "int2": f"int2 (group {w.group_size}, f16 scale and zero)"}[w.kv_dtype],
+                                       "int2": f"int2 (group {w.group_size}, f16 scale and zero)",
+                                       "angle": "angle-domain keys (fp8_e4m3 direction codes), fp8_e4m3 values"}[
+                                           w.kv_dtype],
         "data": "synthetic (seeded counter-hash generator)",
         "config": workload_config(w),
         "launch": {"num_splits": st.splits, "early_start": st.early,
@@ -764,7 +766,8 @@ def e2e_steps(st, args, world) -> dict:
                    "copied from pinned host memory and its outputs back, every step"}
 
 
-EXTRA_WORKLOADS = ("ragged", "llama70b_fp8", "tiered", "llama8b_mixed", "llama70b_int4", "llama70b_int2")
+EXTRA_WORKLOADS = ("ragged", "llama70b_fp8", "tiered", "llama8b_mixed", "llama70b_int4", "llama70b_int2",
+                   "llama70b_angle")
 
 
 def gpu_arm(args, w, rank, world, local):
@@ -817,6 +820,9 @@ def _oracle_unit(w, layer: int, b: int, kf, vf, q, fmt=None):
         pool = oracle.OraclePool(nblk, w.n_kv, w.d_h, 16, block_fmt=fmt)
     elif w.lowbit:
         pool = oracle.OraclePool(nblk, w.n_kv, w.d_h, 16, lowbit=w.lowbit)
+    elif w.kv_dtype == "angle":
+        pool = oracle.OraclePool(nblk, w.n_kv, w.d_h, 16, angle=True)
+        q = oracle.angle_query(q)
     else:
         pool = oracle.OraclePool(nblk, w.n_kv, w.d_h, 16, w.kv_dtype != "bf16")
     pool.append(kf, vf, slots)
@@ -939,7 +945,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama8b")
     ap.add_argument("--only", action="store_true",
                     help="time the chosen workload alone (the default run also times the ragged, 70B FP8, "
-                         "tiered, mixed-precision and 70B low-bit workloads)")
+                         "tiered, mixed-precision, 70B low-bit and 70B angle-domain workloads)")
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling captures)")
     ap.add_argument("--context", type=int, default=0, help="override every request's context (size sweeps)")

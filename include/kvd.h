@@ -59,6 +59,10 @@
  *      V code of (t, d): lane = 4·(c%8) + (t%8)/2, th = t/8, j = (t%2) + 2·(c/8)
  *      byte index within the tile: (((kg/2)·32 + lane)·4 + (kg%2)·2 + th)·4 + j
  *    so every byte holds codes of one token only.
+ *  - An angle-domain pool (KVD_ANGLE) has FP8 records (4224 bytes, same tile layout): the K
+ *    tile holds the E4M3 codes of each key row's direction, the V tile FP8 values; of the 32
+ *    fp32 words after the tiles, index 0 holds per token the key's logit factor w (not a scale)
+ *    and index 1 the V scale.
  */
 #ifndef KVD_H
 #define KVD_H
@@ -93,7 +97,8 @@ typedef enum {
     KVD_FP8_E5M2 = 3,         /* block format of a mixed pool: like E4M3, codes 1·5·2 bits, max 57,344 */
     KVD_MIXED = 4,            /* pool of mixed-precision blocks (kvd_pool_set_block_formats) */
     KVD_INT4 = 5,             /* w_kv = 1/2: 4-bit codes, half-precision scale and zero point per group */
-    KVD_INT2 = 6              /* w_kv = 1/4: 2-bit codes, likewise */
+    KVD_INT2 = 6,             /* w_kv = 1/4: 2-bit codes, likewise */
+    KVD_ANGLE = 7             /* angle-domain keys (E4M3 direction code + radius factor), FP8 values */
 } kvd_dtype;
 
 typedef struct {
@@ -102,7 +107,7 @@ typedef struct {
     int32_t d_h;              /* head dimension; 128 */
     int32_t block_size;       /* tokens per block; 16 */
     int64_t num_blocks;       /* physical blocks per layer */
-    int32_t kv_dtype;         /* KVD_BF16, KVD_FP8_E4M3, KVD_MIXED, KVD_INT4 or KVD_INT2 */
+    int32_t kv_dtype;         /* KVD_BF16, KVD_FP8_E4M3, KVD_MIXED, KVD_INT4, KVD_INT2 or KVD_ANGLE */
     int32_t group_size;       /* KVD_INT4 / KVD_INT2: values per scale group, 32, 64 or 128; ignored
                                  for the other types */
 } kvd_pool_desc;
@@ -144,7 +149,17 @@ KVD_API const char* kvd_status_string(kvd_status s);
  * scale = half(fp32((max − min)/(2^bits − 1))) (1 if that is 0), zero = half(min), code =
  * clamp(rint(fp32(fp32(x − zero)/scale)), 0, 2^bits − 1), half() = nearest half-precision
  * value saturated at ±65,504, rint ties to even.  Low-bit pools take no host tier
- * (kvd_pool_attach_host_tier: KVD_ERR_UNSUPPORTED). */
+ * (kvd_pool_attach_host_tier: KVD_ERR_UNSUPPORTED).
+ * Angle-domain pools (KVD_ANGLE): page "기술 요약: Spherical KV", §2.1 (Angle-Domain Attention):
+ * a key is a radius r = ||k|| and a direction; the cache keeps a quantised radius r̃ and a code of
+ * the direction, and the decode kernel computes the logit ||q||·r̃·f_b(c_q, c_k) from the codes,
+ * f_b the cosine of two direction codes, without rebuilding a dense key.  The page defines
+ * neither the code nor f_b; this library takes the E4M3 codes of the row at its absmax scale as
+ * the direction code (they do not depend on ||k||), r̃ = the nearest half-precision value of
+ * ||k|| (saturating), and f_b = <d_q, d_k>/(||d_q||·||d_k||) with d the code values.  Each key row
+ * stores w = fp32(r̃/||d_k||) (computed in fp64; 0 for a zero row) where an FP8 record keeps its
+ * K scale; values are FP8-E4M3 as in an FP8 pool.  The query of each head is coded the same way
+ * inside kvd_decode_attn.  pool_bytes as for FP8.  No host tier. */
 KVD_API kvd_status kvd_pool_bytes(const kvd_pool_desc* desc, size_t* pool_bytes, size_t* kv_bytes);
 
 /* Wrap caller memory as a pool.  mem is a device buffer of len ≥ pool_bytes bytes,

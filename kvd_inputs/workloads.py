@@ -31,7 +31,8 @@ class Workload:
     d_h: int
     batch: int
     kv_dtype: str                       # "bf16", "fp8_e4m3", "mixed" (a format per physical block),
-                                        # "int4" or "int2" (codes with a scale and zero per group)
+                                        # "int4" or "int2" (codes with a scale and zero per group),
+                                        # "angle" (angle-domain keys, FP8 values)
     block_size: int = 16
     seed: int = 0
     steps: int = 1                      # decode steps in one unit of work
@@ -58,7 +59,7 @@ class Workload:
         """Bytes per stored K or V element (a single-format pool)."""
         if self.kv_dtype == "mixed":
             raise ValueError("a mixed pool has a w_kv per block: use token_bytes()")
-        return {"bf16": 2, "fp8_e4m3": 1, "int4": 0.5, "int2": 0.25}[self.kv_dtype]
+        return {"bf16": 2, "fp8_e4m3": 1, "int4": 0.5, "int2": 0.25, "angle": 1}[self.kv_dtype]
 
     @property
     def lowbit(self) -> tuple | None:
@@ -94,7 +95,7 @@ class Workload:
         """(tokens attended in 2-byte storage, tokens in 1-byte storage) at ``step``."""
         tokens = sum(self.seq_lens(step))
         if self.kv_dtype != "mixed":
-            return (tokens, 0) if self.kv_dtype == "bf16" else (0, tokens)
+            return (tokens, 0) if self.kv_dtype == "bf16" else (0, tokens)   # angle: FP8-sized records
         fmt = self.block_formats()
         bt = self.block_table()
         wide = 0
@@ -295,9 +296,19 @@ def llama70b_int2(seed: int = 0) -> Workload:
     return w
 
 
+def llama70b_angle(seed: int = 0) -> Workload:
+    w = Workload("llama70b_angle", L=80, n_q=64, n_kv=8, d_h=128, batch=1, kv_dtype="angle", seed=seed,
+                 outlier_p=0.001, outlier_factor=20.0,
+                 description="Llama-3-70B shape long context, angle-domain keys: 80 layers, n_q 64, n_kv 8, d_h 128, "
+                             "batch 1, context 131,072, keys as an FP8-e4m3 direction code plus a radius factor per "
+                             "(token, head), FP8-e4m3 values, 0.1% outlier channels x20")
+    w._ctx0 = [131072]
+    return w
+
+
 WORKLOADS = {"tiny": tiny, "llama8b": llama8b, "llama8b_mixed": llama8b_mixed, "ragged": ragged,
              "llama70b_fp8": llama70b_fp8, "tiered": tiered, "llama70b_int4": llama70b_int4,
-             "llama70b_int2": llama70b_int2}
+             "llama70b_int2": llama70b_int2, "llama70b_angle": llama70b_angle}
 
 
 def get(name: str, seed: int = 0) -> Workload:

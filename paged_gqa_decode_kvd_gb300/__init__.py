@@ -9,6 +9,7 @@ the library loads it and fails loudly if it is missing or cannot be built.
 from __future__ import annotations
 
 from ._lib import (  # noqa: F401
+    KVD_ANGLE,
     KVD_BF16,
     KVD_EARLY_START,
     KVD_F32,
@@ -72,7 +73,7 @@ class KVPool:
         if self.kv_dtype in (KVD_INT4, KVD_INT2):
             bits = 4 if self.kv_dtype == KVD_INT4 else 2
             return 2 * 256 * bits + 2 * 64 * (128 // self.group_size)
-        return 4096 + 128 if self.kv_dtype == KVD_FP8_E4M3 else 8192
+        return 4096 + 128 if self.kv_dtype in (KVD_FP8_E4M3, KVD_ANGLE) else 8192
 
     def set_block_formats(self, block_fmt):
         """Mixed pool: one precision code per physical block (uint8 device tensor, kept alive here)."""

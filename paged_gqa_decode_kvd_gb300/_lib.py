@@ -12,7 +12,7 @@ import ctypes
 import os
 
 KVD_OK, KVD_ERR_INVALID, KVD_ERR_UNSUPPORTED, KVD_ERR_NOMEM, KVD_ERR_CUDA, KVD_ERR_OOB, KVD_ERR_TIMEOUT = range(7)
-KVD_BF16, KVD_FP8_E4M3, KVD_F32, KVD_FP8_E5M2, KVD_MIXED, KVD_INT4, KVD_INT2 = 0, 1, 2, 3, 4, 5, 6
+KVD_BF16, KVD_FP8_E4M3, KVD_F32, KVD_FP8_E5M2, KVD_MIXED, KVD_INT4, KVD_INT2, KVD_ANGLE = 0, 1, 2, 3, 4, 5, 6, 7
 KVD_EARLY_START = 1   # kvd_decode_attn flag
 
 SYMBOLS = [

@@ -43,7 +43,7 @@ kvd_status check_desc(const kvd_pool_desc* d) {
     if (d->num_layers < 1 || d->n_kv < 1 || d->num_blocks < 1 || d->d_h < 1 || d->block_size < 1)
         return KVD_ERR_INVALID;
     if (d->kv_dtype != KVD_BF16 && d->kv_dtype != KVD_FP8_E4M3 && d->kv_dtype != KVD_MIXED &&
-        d->kv_dtype != KVD_INT4 && d->kv_dtype != KVD_INT2)
+        d->kv_dtype != KVD_INT4 && d->kv_dtype != KVD_INT2 && d->kv_dtype != KVD_ANGLE)
         return KVD_ERR_INVALID;
     if (d->d_h != kvd::kDh || d->block_size != kvd::kBs) return KVD_ERR_UNSUPPORTED;
     if ((d->kv_dtype == KVD_INT4 || d->kv_dtype == KVD_INT2) && d->group_size != 32 && d->group_size != 64 &&
@@ -103,6 +103,7 @@ int pool_kind(const kvd_pool* pool) {
         case KVD_MIXED: return kvd::kKindMixed;
         case KVD_INT4: return kvd::kKindInt4;
         case KVD_INT2: return kvd::kKindInt2;
+        case KVD_ANGLE: return kvd::kKindAngle;
         default: return kvd::kKindBf16;
     }
 }
@@ -111,7 +112,7 @@ int pool_kind(const kvd_pool* pool) {
 size_t record_bytes(const kvd_pool_desc* d) {
     if (d->kv_dtype == KVD_INT4) return kvd::lowbit_record_bytes(4, pool_ng(d));
     if (d->kv_dtype == KVD_INT2) return kvd::lowbit_record_bytes(2, pool_ng(d));
-    return d->kv_dtype == KVD_FP8_E4M3 ? kvd::kRecordFp8 : kvd::kRecordBf16;
+    return d->kv_dtype == KVD_FP8_E4M3 || d->kv_dtype == KVD_ANGLE ? kvd::kRecordFp8 : kvd::kRecordBf16;
 }
 
 }  // namespace
@@ -139,7 +140,8 @@ kvd_status kvd_pool_bytes(const kvd_pool_desc* desc, size_t* pool_bytes, size_t*
     if (!kv_bytes || !pool_bytes) return KVD_ERR_INVALID;
     // a mixed pool sizes every record slot for BF16 (an 8-bit block uses the first part of it);
     // element bits: 16, 8, 4 or 2
-    const size_t bits = desc->kv_dtype == KVD_FP8_E4M3 ? 8 : desc->kv_dtype == KVD_INT4 ? 4
+    const bool fp8_records = desc->kv_dtype == KVD_FP8_E4M3 || desc->kv_dtype == KVD_ANGLE;
+    const size_t bits = fp8_records ? 8 : desc->kv_dtype == KVD_INT4 ? 4
                         : desc->kv_dtype == KVD_INT2   ? 2 : 16;
     size_t per_block = 0, rows = 0, total = 0;
     // 2 (K and V) · block_size · d_h · w_kv bytes per (layer, block, KV head)
@@ -156,7 +158,7 @@ kvd_status kvd_pool_bytes(const kvd_pool_desc* desc, size_t* pool_bytes, size_t*
         if (total > SIZE_MAX - mb) return KVD_ERR_INVALID;
         *pool_bytes = total + mb;
     }
-    if (desc->kv_dtype == KVD_FP8_E4M3) {
+    if (fp8_records) {   // one fp32 word per (token, head) for K and for V
         size_t sb = 0;
         if (!mul_ok(rows, 2 * static_cast<size_t>(desc->block_size) * sizeof(float), &sb)) return KVD_ERR_INVALID;
         if (total > SIZE_MAX - sb) return KVD_ERR_INVALID;
@@ -225,7 +227,8 @@ kvd_status kvd_pool_set_block_formats(kvd_pool* pool, const uint8_t* block_fmt, 
 kvd_status kvd_pool_attach_host_tier(kvd_pool* pool, void* host_mem, size_t host_len, void* staging_mem,
                                      size_t staging_len, int64_t host_blocks) {
     if (!pool || host_blocks < 0) return KVD_ERR_INVALID;
-    if ((pool->desc.kv_dtype == KVD_MIXED || lowbit_dtype(pool->desc.kv_dtype)) && host_blocks > 0)
+    if ((pool->desc.kv_dtype == KVD_MIXED || pool->desc.kv_dtype == KVD_ANGLE || lowbit_dtype(pool->desc.kv_dtype)) &&
+        host_blocks > 0)
         return KVD_ERR_UNSUPPORTED;
     if (host_blocks == 0) {
         pool->host_kv = nullptr;

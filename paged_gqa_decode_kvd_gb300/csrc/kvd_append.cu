@@ -41,7 +41,7 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
     }
     const int64_t row = (n * p.n_kv + h) * kDh;
     constexpr int kBits = KIND == kKindInt4 ? 4 : 2;
-    constexpr int64_t kRec = KIND == kKindFp8    ? kRecordFp8
+    constexpr int64_t kRec = KIND == kKindFp8 || KIND == kKindAngle ? kRecordFp8
                              : is_lowbit(KIND) ? lowbit_record_bytes(kBits, NG)
                                                : kRecordBf16;
     // a host-tier block (id ≥ num_blocks) keeps its record in host memory
@@ -49,6 +49,8 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
                                          : p.host_kv + ((blk - p.num_blocks) * p.n_kv + h) * kRec;
     if constexpr (is_lowbit(KIND)) {
         write_token_lowbit<kBits, NG>(record, t, p.k_new + row, p.v_new + row, lane);
+    } else if constexpr (KIND == kKindAngle) {
+        write_token<kFmtE4m3, true>(record, t, p.k_new + row, p.v_new + row, lane);
     } else if constexpr (KIND == kKindMixed) {
         const int fmt = block_format(p.block_fmt[blk]);
         if (fmt == kFmtBf16) write_token<kFmtBf16>(record, t, p.k_new + row, p.v_new + row, lane);
@@ -75,7 +77,9 @@ cudaError_t launch_append(const AppendParams& p, int kind, cudaStream_t stream) 
             else if (p.ng == 2) append_kernel<kKindInt2, 2><<<grid, threads, 0, stream>>>(p);
             else append_kernel<kKindInt2, 1><<<grid, threads, 0, stream>>>(p);
         }
-    } else if (kind == kKindFp8)
+    } else if (kind == kKindAngle)
+        append_kernel<kKindAngle><<<grid, threads, 0, stream>>>(p);
+    else if (kind == kKindFp8)
         append_kernel<kKindFp8><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(p);
     else if (kind == kKindMixed)
         append_kernel<kKindMixed><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(p);

@@ -194,7 +194,10 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
 // fragment order; 8-bit records store code(x / scale) with scale = fp32(absmax/top) (1 for a
 // zero row), top = 448 (E4M3) or 57,344 (E5M2), the largest finite value of the format,
 // codes rounded to nearest even and saturated, per K and per V, the scales after the two tiles.
-template <int FMT>
+// ANGLE (E4M3 only): the K row's word after the tiles is its logit factor instead of its scale,
+// w = fp32(half(||k||) / ||d||) with d the values of its codes, in fp64 (0 for a zero row); the
+// direction code is the codes themselves (they depend on k/||k|| only).
+template <int FMT, bool ANGLE = false>
 __device__ __forceinline__ void write_token(uint8_t* record, int t, const uint16_t* krow, const uint16_t* vrow,
                                             int lane) {
     constexpr bool FP8 = FMT != kFmtBf16;
@@ -235,6 +238,7 @@ __device__ __forceinline__ void write_token(uint8_t* record, int t, const uint16
         const float vs = (vmax == 0.f) ? 1.f : __fdiv_rn(vmax, kTop);
         uint8_t* ktile = record;
         uint8_t* vtile = record + kTileFp8;
+        double r2 = 0.0, d2 = 0.0;   // ANGLE: squared radius and squared code norm, this lane's dims
         #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int d = lane * 4 + j;
@@ -245,10 +249,26 @@ __device__ __forceinline__ void write_token(uint8_t* record, int t, const uint16
             ktile[fp8_tile_index(i, fl, fe)] = kc;
             i = v_frag_i(t, d, &fl, &fe);
             vtile[fp8_tile_index(i, fl, fe)] = vc;
+            if constexpr (ANGLE) {
+                const double c = static_cast<double>(__half2float(__half(__nv_cvt_fp8_to_halfraw(kc, __NV_E4M3))));
+                r2 += static_cast<double>(kx[j]) * static_cast<double>(kx[j]);
+                d2 += c * c;   // exact: code values are multiples of 2^-9 below 2^9
+            }
+        }
+        float kw = ks;
+        if constexpr (ANGLE) {
+            #pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                r2 += __shfl_xor_sync(kFull, r2, o);
+                d2 += __shfl_xor_sync(kFull, d2, o);
+            }
+            __half rh = __double2half(__dsqrt_rn(r2));
+            if (__hisinf(rh)) rh = __ushort_as_half(0x7BFFu);
+            kw = d2 > 0.0 ? __double2float_rn(__ddiv_rn(static_cast<double>(__half2float(rh)), __dsqrt_rn(d2))) : 0.f;
         }
         if (lane == 0) {
             float* sc = reinterpret_cast<float*>(record + 2 * kTileFp8);
-            sc[t] = ks;
+            sc[t] = kw;
             sc[kBs + t] = vs;
         }
     }

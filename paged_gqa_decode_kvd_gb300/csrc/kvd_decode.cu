@@ -1,4 +1,5 @@
-// kvd_decode.cu — paged GQA decode attention for BF16, FP8-E4M3 and mixed-precision pools:
+// kvd_decode.cu — paged GQA decode attention for BF16, FP8-E4M3, mixed-precision and
+// angle-domain pools:
 // launch geometry and dispatch of the decode kernel (kvd_decode_kernel.cuh), and the self-test
 // of its bounded waits.
 #include "kvd_decode_kernel.cuh"
@@ -15,9 +16,10 @@ constexpr int kMixedStages = 12;
 // With 16 the CTA keeps twice the bytes in flight; measured on GB300 it is 1% faster for one
 // or eight long requests and equal for 32 requests of 8,192 tokens.  The 16-stage variant runs
 // three CTAs per SM anyway, so its launch bounds let it use 128 registers (the 8-stage one,
-// four per SM, gets 96); without spills it is another 1% faster on one long request.
+// four per SM, gets 96); without spills it is another 1% faster on one long request.  Angle-domain
+// pools have FP8 records and follow the same rule.
 static int decode_stages(int kind, int batch, int g) {
-    if (kind != kKindFp8) return 8;
+    if (kind != kKindFp8 && kind != kKindAngle) return 8;
     int per_sm = 0, reserved = 0;
     if (!smem_attrs(&per_sm, &reserved)) return 8;
     const int64_t need = 3 * (static_cast<int64_t>(smem_layout<kKindFp8, 16>(batch, g).total) + reserved);
@@ -28,6 +30,9 @@ size_t decode_smem_bytes(int kind, int ng, int batch, int g) {
     if (is_lowbit(kind)) return decode_smem_bytes_lowbit(kind, ng, batch, g);
     if (kind == kKindBf16) return smem_layout<kKindBf16, 8>(batch, g).total;
     if (kind == kKindMixed) return smem_layout<kKindMixed, kMixedStages>(batch, g).total;
+    if (kind == kKindAngle)
+        return decode_stages(kind, batch, g) == 16 ? smem_layout<kKindAngle, 16>(batch, g).total
+                                                   : smem_layout<kKindAngle, 8>(batch, g).total;
     return decode_stages(kind, batch, g) == 16 ? smem_layout<kKindFp8, 16>(batch, g).total
                                                : smem_layout<kKindFp8, 8>(batch, g).total;
 }
@@ -36,6 +41,9 @@ int decode_ctas_per_sm(int kind, int ng, int batch, int g) {
     if (is_lowbit(kind)) return decode_ctas_per_sm_lowbit(kind, ng, batch, g);
     if (kind == kKindBf16) return ctas_per_sm_impl<kKindBf16, 8>(batch, g);
     if (kind == kKindMixed) return ctas_per_sm_impl<kKindMixed, kMixedStages>(batch, g);
+    if (kind == kKindAngle)
+        return decode_stages(kind, batch, g) == 16 ? ctas_per_sm_impl<kKindAngle, 16>(batch, g)
+                                                   : ctas_per_sm_impl<kKindAngle, 8>(batch, g);
     return decode_stages(kind, batch, g) == 16 ? ctas_per_sm_impl<kKindFp8, 16>(batch, g)
                                                : ctas_per_sm_impl<kKindFp8, 8>(batch, g);
 }
@@ -60,6 +68,9 @@ static cudaError_t launch_decode_impl(const DecodeParams& p, int kind, int carve
 
 cudaError_t launch_decode(const DecodeParams& p, int kind, int carveout, cudaStream_t stream) {
     if (is_lowbit(kind)) return launch_decode_lowbit(p, kind, carveout, stream);   // no host tier
+    if (kind == kKindAngle)   // no host tier
+        return decode_stages(kind, p.B, p.g) == 16 ? launch_variant<kKindAngle, 16, false>(p, carveout, stream)
+                                                   : launch_variant<kKindAngle, 8, false>(p, carveout, stream);
     // a mixed pool has no host tier
     if (kind == kKindMixed) return launch_variant<kKindMixed, kMixedStages, false>(p, carveout, stream);
     return p.host_direct && p.host_blocks > 0 ? launch_decode_impl<true>(p, kind, carveout, stream)

@@ -26,6 +26,10 @@
 //    fp32 (exp2 domain), P^T built with movmatrix, O^T += V^T·P^T.
 //  * FP8: codes convert exactly to f16; the K scale multiplies the fp32 logit,
 //    the V scale folds into p before it is rounded to f16 for the MMA.
+//  * Angle-domain keys: the K codes are each row's direction code and the
+//    row's word is its logit factor r̃/||d_k||; the kernel codes q the same way
+//    (E4M3 at its absmax scale, per head) and multiplies the logit by the
+//    head's ||q||/||d_q||: the logit is ||q||·r̃·cos(d_q, d_k) from the codes.
 //  * Low-bit (4-bit / 2-bit codes, a scale and a zero point per group of a
 //    row): codes convert exactly to f16 through the E4M3 path; K accumulates
 //    one MMA sum per group, combined with the group's scale and zero point in
@@ -54,7 +58,7 @@ struct Cfg {
     // record slot of one (block, KV head): a mixed pool sizes every slot for BF16 and an 8-bit
     // block fills the first kRecordFp8 bytes of it
     static constexpr int kBits = KIND == kKindInt4 ? 4 : KIND == kKindInt2 ? 2 : 0;
-    static constexpr int kRecord = KIND == kKindFp8    ? kRecordFp8
+    static constexpr int kRecord = KIND == kKindFp8 || KIND == kKindAngle ? kRecordFp8
                                    : is_lowbit(KIND) ? lowbit_record_bytes(kBits, NG)
                                                      : kRecordBf16;
     static constexpr int kStage = kRecord;
@@ -220,11 +224,13 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, int64_t idx, fl
 // folds into p).  m: the block's valid-slot mask (bits 0..15).  lg0 / lg1: logit rows of heads
 // h0 / h1 (or null), written at positions tb + slot below lim.  The stage is released (arrive
 // on empty_s) as soon as its V tile is in registers.
-template <int FMT>
+// HF (angle-domain keys): the row's word is its logit factor, and hf0 / hf1 (softmax scale·log2(e)
+// times the head's ||q||/||d_q||) multiply the logits of heads h0 / h1.
+template <int FMT, bool HF = false>
 __device__ __forceinline__ void consume_block(const uint8_t* st, const uint32_t (&qf)[8][2], float (&o)[8][4],
                                               float& m0, float& m1, float& s0, float& s1, uint32_t m,
                                               float scale_log2, float* lg0, float* lg1, int tb, int64_t lim,
-                                              uint64_t* empty_s, int lane) {
+                                              uint64_t* empty_s, int lane, float hf0 = 1.f, float hf1 = 1.f) {
     const int gid = lane >> 2;   // token row (S^T) / dim row (O^T) within an 8-row group
     const int tq = lane & 3;     // head pair 2tq, 2tq+1
     // ---- S^T = K · Q^T  (16 tokens × 8 heads) ----
@@ -256,8 +262,8 @@ __device__ __forceinline__ void consume_block(const uint8_t* st, const uint32_t 
             mma_f16(cb, fb, qf[2 * u4 + 1][0], qf[2 * u4 + 1][1]);
         }
         const float* sc = reinterpret_cast<const float*>(st + 2 * kTileFp8);
-        fk0 = sc[gid] * scale_log2;
-        fk1 = sc[gid + 8] * scale_log2;
+        fk0 = HF ? sc[gid] : sc[gid] * scale_log2;
+        fk1 = HF ? sc[gid + 8] : sc[gid + 8] * scale_log2;
         fv0 = sc[kBs + gid];
         fv1 = sc[kBs + gid + 8];
     }
@@ -267,6 +273,12 @@ __device__ __forceinline__ void consume_block(const uint8_t* st, const uint32_t 
     float l1 = v0 ? (ca[1] + cb[1]) * fk0 : -INFINITY;  // (gid,   h1)
     float l2 = v1 ? (ca[2] + cb[2]) * fk1 : -INFINITY;  // (gid+8, h0)
     float l3 = v1 ? (ca[3] + cb[3]) * fk1 : -INFINITY;  // (gid+8, h1)
+    if constexpr (HF) {
+        l0 *= hf0;
+        l1 *= hf1;
+        l2 *= hf0;
+        l3 *= hf1;
+    }
 
     {
         const int t0 = tb + gid, t1 = t0 + 8;
@@ -592,7 +604,9 @@ __device__ __forceinline__ void consume_block_lowbit(const uint8_t* st, const ui
 // DIRECT: the pool's host-tier blocks are read in place from host memory (lsu_fill); only
 // pools with such a tier launch this variant, so the others carry none of its code.
 template <int KIND, int S, bool DIRECT, int NG = 1>
-__global__ void __launch_bounds__(kThreads, KIND == kKindFp8 && S == 8 ? 4 : KIND == kKindMixed ? 2 : 3)
+__global__ void __launch_bounds__(kThreads, (KIND == kKindFp8 || KIND == kKindAngle) && S == 8 ? 4
+                                           : KIND == kKindMixed                             ? 2
+                                                                                            : 3)
     decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     using C = Cfg<KIND, S, NG>;
@@ -714,6 +728,8 @@ __global__ void __launch_bounds__(kThreads, KIND == kKindFp8 && S == 8 ? 4 : KIN
                     uint8_t* rec = const_cast<uint8_t*>(record_of<C::kRecord>(p, ph, sg.kvh));
                     if constexpr (is_lowbit(KIND)) {      // no host tier
                         write_token_lowbit<C::kBits, NG>(rec, pos % kBs, p.k_new + row, p.v_new + row, lane);
+                    } else if constexpr (KIND == kKindAngle) {   // no host tier
+                        write_token<kFmtE4m3, true>(rec, pos % kBs, p.k_new + row, p.v_new + row, lane);
                     } else if constexpr (KIND == kKindMixed) {   // the block's own format (no host tier)
                         const int fmt = ph < p.num_blocks ? block_format(p.block_fmt[ph]) : -1;
                         if (fmt == kFmtBf16) write_token<kFmtBf16>(rec, pos % kBs, p.k_new + row, p.v_new + row, lane);
@@ -862,6 +878,43 @@ __global__ void __launch_bounds__(kThreads, KIND == kKindFp8 && S == 8 ? 4 : KIN
             }
         }
 
+        // Angle-domain keys: q of head gid becomes its E4M3 direction code at its absmax scale (the
+        // f16 fragments hold the code values, exactly) and hf0 / hf1 carry ||q||/||d_q|| of heads
+        // h0 / h1 times the softmax scale.
+        float hf0 = 1.f, hf1 = 1.f;
+        if constexpr (KIND == kKindAngle) {
+            float amax = 0.f;
+            #pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float2 a = unpack_f16(qf[i][0]), b = unpack_f16(qf[i][1]);
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(b.x), fabsf(b.y))));
+            }
+            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+            const float qs = amax == 0.f ? 1.f : __fdiv_rn(amax, 448.f);
+            float q2 = 0.f, d2 = 0.f;
+            #pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                #pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float2 a = unpack_f16(qf[i][r]);
+                    const uint32_t c0 = __nv_cvt_float_to_fp8(__fdiv_rn(a.x, qs), __NV_SATFINITE, __NV_E4M3);
+                    const uint32_t c1 = __nv_cvt_float_to_fp8(__fdiv_rn(a.y, qs), __NV_SATFINITE, __NV_E4M3);
+                    qf[i][r] = e4m3x2_to_f16x2(c0 | (c1 << 8));
+                    const float2 dv = unpack_f16(qf[i][r]);
+                    q2 = fmaf(a.x, a.x, fmaf(a.y, a.y, q2));
+                    d2 = fmaf(dv.x, dv.x, fmaf(dv.y, dv.y, d2));
+                }
+            }
+            q2 += __shfl_xor_sync(kFull, q2, 1);
+            q2 += __shfl_xor_sync(kFull, q2, 2);
+            d2 += __shfl_xor_sync(kFull, d2, 1);
+            d2 += __shfl_xor_sync(kFull, d2, 2);
+            const float f = d2 > 0.f ? sqrtf(q2) / sqrtf(d2) : 0.f;   // head gid
+            hf0 = p.scale_log2 * __shfl_sync(kFull, f, 4 * h0);
+            hf1 = p.scale_log2 * __shfl_sync(kFull, f, 4 * h1);
+        }
+
         float m0 = -INFINITY, m1 = -INFINITY;   // running max (log2 domain), heads h0, h1
         float s0 = 0.f, s1 = 0.f;               // running sum of p (this lane's tokens)
         float o[8][4];
@@ -918,6 +971,9 @@ __global__ void __launch_bounds__(kThreads, KIND == kKindFp8 && S == 8 ? 4 : KIN
             } else if constexpr (is_lowbit(KIND)) {
                 consume_block_lowbit<C::kBits, NG>(st, qf, qz, o, oz, m0, m1, s0, s1, m, p.scale_log2, lg0, lg1, tb,
                                                    lim, &empty[s], lane);
+            } else if constexpr (KIND == kKindAngle) {
+                consume_block<kFmtE4m3, true>(st, qf, o, m0, m1, s0, s1, m, p.scale_log2, lg0, lg1, tb, lim,
+                                              &empty[s], lane, hf0, hf1);
             } else {
                 consume_block<KIND == kKindFp8 ? kFmtE4m3 : kFmtBf16>(st, qf, o, m0, m1, s0, s1, m, p.scale_log2, lg0,
                                                                      lg1, tb, lim, &empty[s], lane);

@@ -11,6 +11,9 @@ namespace kvd {
 // Pool kinds: every block BF16, every block FP8-E4M3, mixed (a precision byte per block), or
 // low-bit (4-bit or 2-bit codes with a half-precision scale and zero point per group of values).
 constexpr int kKindBf16 = 0, kKindFp8 = 1, kKindMixed = 2, kKindInt4 = 3, kKindInt2 = 4;
+// Angle-domain keys: FP8 records whose K codes are the direction code of each key row and whose
+// K scale word is the row's logit factor w = r̃/||d||; the query is coded the same way in-kernel.
+constexpr int kKindAngle = 5;
 __host__ __device__ constexpr bool is_lowbit(int kind) { return kind == kKindInt4 || kind == kKindInt2; }
 
 // Device ordinal the pool was created on (its memory and state live there).

@@ -32,7 +32,7 @@ def assert_out_close(gpu, ref, atol=OUT_ATOL, rtol=OUT_RTOL, what="out"):
 
 def dtype_code(w: Workload) -> int:
     return {"bf16": kvd.KVD_BF16, "fp8_e4m3": kvd.KVD_FP8_E4M3, "mixed": kvd.KVD_MIXED, "int4": kvd.KVD_INT4,
-            "int2": kvd.KVD_INT2}[w.kv_dtype]
+            "int2": kvd.KVD_INT2, "angle": kvd.KVD_ANGLE}[w.kv_dtype]
 
 
 FORMAT_CODES = (kvd.KVD_BF16, kvd.KVD_FP8_E4M3, kvd.KVD_FP8_E5M2)   # index = oracle format code
@@ -85,6 +85,8 @@ def oracle_layer(w: Workload, layer: int, bt_cpu: torch.Tensor, seq_lens: list[i
         pool = oracle.OraclePool(w.num_blocks(), w.n_kv, w.d_h, 16, block_fmt=w.block_formats())
     elif w.lowbit:
         pool = oracle.OraclePool(w.num_blocks(), w.n_kv, w.d_h, 16, lowbit=w.lowbit)
+    elif w.kv_dtype == "angle":
+        pool = oracle.OraclePool(w.num_blocks(), w.n_kv, w.d_h, 16, angle=True)
     else:
         pool = oracle.OraclePool(w.num_blocks(), w.n_kv, w.d_h, 16, w.kv_dtype != "bf16")
     for b in range(w.batch):
@@ -93,7 +95,10 @@ def oracle_layer(w: Workload, layer: int, bt_cpu: torch.Tensor, seq_lens: list[i
         assert pool.append(k.float().numpy(), v.float().numpy(), slots) == 0
     if q is None:
         q = w.q(layer, step)
-    return oracle.decode(pool, q.float().numpy(), w.n_q, bt_cpu.numpy(), seq_lens,
+    qn = q.float().numpy()
+    if w.kv_dtype == "angle":   # the query of an angle-domain logit: its own direction code, rescaled
+        qn = oracle.angle_query(qn)
+    return oracle.decode(pool, qn, w.n_q, bt_cpu.numpy(), seq_lens,
                          None if retain is None else retain.numpy(), 1.0 / np.sqrt(w.d_h),
                          want_alpha=want_alpha, want_logits=want_logits)
 
@@ -119,7 +124,7 @@ def _tile_perm(kind: str, fp8: bool) -> np.ndarray:
 
 def read_record(pool: kvd.KVPool, layer: int, block: int, head: int):
     """(K, V) of one (layer, block, head) record, each [16][128], as stored (bf16 tensor or uint8 codes)."""
-    fp8 = pool.kv_dtype == kvd.KVD_FP8_E4M3
+    fp8 = pool.kv_dtype in (kvd.KVD_FP8_E4M3, kvd.KVD_ANGLE)
     rb = pool.record_bytes
     off = ((layer * pool.num_blocks + block) * pool.n_kv + head) * rb
     raw = pool.mem[off:off + rb].cpu()

@@ -61,6 +61,8 @@ def test_lowbit_pool_bytes():
             tokens = 8192 * 16
             assert kv == 2 * 80 * 8 * 128 * bits * tokens // 8
             assert pool - kv == 2 * 80 * 8 * (128 // group) * 4 * tokens
+    # angle-domain pools: FP8-sized records (codes, then one fp32 word per row for K and for V)
+    assert kvd.kvd_pool_bytes(80, 8, 8192, kvd.KVD_ANGLE) == kvd.kvd_pool_bytes(80, 8, 8192, kvd.KVD_FP8_E4M3)
     # 70B shape, 128k context: 2-bit codes are an eighth of the BF16 bytes (the page's c = 8)
     _, bf16 = kvd.kvd_pool_bytes(80, 8, 8192, kvd.KVD_BF16)
     _, int2 = kvd.kvd_pool_bytes(80, 8, 8192, kvd.KVD_INT2, group_size=128)
@@ -87,7 +89,7 @@ def test_bad_descriptors_are_rejected():
     with pytest.raises(kvd.KvdError) as e:
         kvd.kvd_pool_bytes(32, 8, 16, kvd.KVD_BF16, block_size=32)
     assert e.value.status == kvd.KVD_ERR_UNSUPPORTED
-    for bad in [dict(num_layers=0), dict(n_kv=0), dict(num_blocks=0), dict(kv_dtype=7)]:
+    for bad in [dict(num_layers=0), dict(n_kv=0), dict(num_blocks=0), dict(kv_dtype=99)]:
         args = dict(num_layers=2, n_kv=8, num_blocks=16, kv_dtype=kvd.KVD_BF16)
         args.update(bad)
         with pytest.raises(kvd.KvdError) as e:
