@@ -208,7 +208,7 @@ class Step:
     also writes its logits and adds its share of the importance score."""
 
     def __init__(self, w, dev, num_splits: int = 0, early: bool = True, fused_scores: bool = False,
-                 host_tier: float = 0.0, host_staged: bool = False, retier: bool = False):
+                 host_tier: float = 0.0, host_staged: bool = False, retier: bool = False, planned: bool = True):
         import numpy as np
         import torch
 
@@ -216,6 +216,7 @@ class Step:
 
         self.w, self.dev, self.kvd = w, dev, kvd
         self.early = early   # KVD_EARLY_START: the step's tables and pool are not written by the previous kernel
+        self.planned = planned   # one kvd_decode_plan per step, read by every layer's decode (KVD_PLANNED)
         self.L = w.L
         kind = {"bf16": kvd.KVD_BF16, "fp8_e4m3": kvd.KVD_FP8_E4M3, "mixed": kvd.KVD_MIXED, "int4": kvd.KVD_INT4,
                 "int2": kvd.KVD_INT2, "angle": kvd.KVD_ANGLE}[w.kv_dtype]
@@ -282,8 +283,8 @@ class Step:
                 self.side = torch.cuda.Stream(device=dev)
                 self.score_done = [None] * nbuf
         # per layer: the decode kernel and the merge launch (which also updates the scores when
-        # fused), + the score kernel when it runs on its own stream
-        self.launches_per_step = (3 if self.overlap else 2) * w.L
+        # fused), + the score kernel when it runs on its own stream; + the step's plan
+        self.launches_per_step = (3 if self.overlap else 2) * w.L + (1 if planned else 0)
         torch.cuda.synchronize()
         err = kvd.kvd_get_device_error(self.pool.handle)
         if err:
@@ -486,7 +487,8 @@ class Step:
             self.kvd.kvd_decode_attn(self.pool.handle, layer, self.q[t][layer], self.bt, self.seq[t], self.max_len,
                                      self.ws, self.out[layer], num_splits=self.splits, retain_mask=self.retain,
                                      lse_out=self.lse[i], logits_out=self.logits[i], k_new=self.k_new[t][layer],
-                                     v_new=self.v_new[t][layer], early_start=self.early, stream=cur)
+                                     v_new=self.v_new[t][layer], early_start=self.early, planned=self.planned,
+                                     stream=cur)
             self.side.wait_stream(cur)
             self.kvd.kvd_accum_scores(self.logits[i], self.lse[i], self.seq[t], inv, self.scores, stream=self.side)
             ev = torch.cuda.Event()
@@ -499,7 +501,7 @@ class Step:
                                  lse_out=self.lse[0] if scores else None, logits_out=self.logits[0] if scores else None,
                                  k_new=self.k_new[t][layer], v_new=self.v_new[t][layer],
                                  scores=self.scores if scores else None, inv_LH=inv,
-                                 early_start=self.early, stream=stream)
+                                 early_start=self.early, planned=self.planned, stream=stream)
 
     def decode_kernel_only(self, layer: int, t: int = 0, stream=None):
         """The layer's decode kernel alone (fused append, partials, no merge launch)."""
@@ -508,13 +510,20 @@ class Step:
                                  self.ws, None, num_splits=self.splits, retain_mask=self.retain,
                                  logits_out=self.logits[0] if scores else None,
                                  k_new=self.k_new[t][layer], v_new=self.v_new[t][layer], early_start=self.early,
-                                 stream=stream)
+                                 planned=self.planned, stream=stream)
+
+    def plan(self, t: int = 0, stream=None):
+        """The step's plan (block tables, lengths and retain mask are the same for all its layers)."""
+        if self.planned:
+            self.kvd.kvd_decode_plan(self.pool.handle, self.w.n_q, self.bt, self.seq[t], self.max_len, self.ws,
+                                     num_splits=self.splits, retain_mask=self.retain, stream=stream)
 
     def capture_decode_only(self):
         import torch
 
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
+            self.plan(0)
             for layer in range(self.L):
                 self.decode_kernel_only(layer)
         torch.cuda.synchronize()
@@ -527,6 +536,7 @@ class Step:
         if self.overlap:
             self.score_done = [None] * len(self.score_done)   # a step depends on nothing of the last
         staged = self.host_blocks and self.host_staged
+        self.plan(t, cur)
         if staged:   # staging slots 0 and 1 are free at the start of a step
             self.copy.wait_stream(cur)
             self.staged = [None] * self.L
@@ -616,7 +626,7 @@ def gpu_workload(args, w, rank, world, local, peaks, headline: bool) -> dict:
     dev = torch.device("cuda", local)
     st = Step(w, dev, args.num_splits, early=not args.no_early_start, fused_scores=args.fused_scores,
               host_tier=args.host_tier if headline else 0.0, host_staged=args.host_tier_staged,
-              retier=args.retier and headline)
+              retier=args.retier and headline, planned=not args.no_plan)
     graphs = st.capture()
     stream = torch.cuda.current_stream(dev)
     steps = args.steps
@@ -694,7 +704,7 @@ def gpu_workload(args, w, rank, world, local, peaks, headline: bool) -> dict:
                                            w.kv_dtype],
         "data": "synthetic (seeded counter-hash generator)",
         "config": workload_config(w),
-        "launch": {"num_splits": st.splits, "early_start": st.early,
+        "launch": {"num_splits": st.splits, "early_start": st.early, "step_plan": st.planned,
                    "score_update": ("second stream (off the layer chain)" if st.overlap else
                                     "fused into the call's epilogue launch" if w.scores else None),
                    "parallelism": f"replicas x{world}"},
@@ -952,6 +962,8 @@ def main(argv=None):
     ap.add_argument("--group-size", type=int, default=0,
                     help="low-bit workloads: values per scale group (32, 64 or 128) instead of the workload's")
     ap.add_argument("--no-early-start", action="store_true", help="launch the decode kernel without KVD_EARLY_START")
+    ap.add_argument("--no-plan", action="store_true",
+                    help="no step plan: every layer's decode kernel derives its split from the lengths and tables")
     ap.add_argument("--fused-scores", action="store_true",
                     help="score update inside each layer's epilogue launch (one stream) instead of on a second stream")
     ap.add_argument("--host-tier", type=float, default=0.0,

@@ -122,6 +122,11 @@ typedef struct kvd_pool kvd_pool;  /* opaque */
  *   kernel is still running; reads of q, k_new, v_new and every write still wait for it to
  *   complete.  Without the flag the kernel waits before touching any global memory. */
 #define KVD_EARLY_START 1u
+/* KVD_PLANNED: the workspace holds a step plan made by kvd_decode_plan for this call's shape
+ * (pool, n_q, batch, max_seq_len, num_splits) and for the block_table, seq_lens and retain_mask
+ * the call passes, which have not changed since; the decode kernel reads its split and its first
+ * blocks from it instead of deriving them. */
+#define KVD_PLANNED 2u
 
 /* Optional score epilogue of kvd_decode_attn: adds this layer's share of the cumulative
  * importance score, scores[b][t] += inv_LH · Σ_h α_h[t], exactly as kvd_accum_scores would
@@ -341,7 +346,8 @@ KVD_API kvd_status kvd_decode_workspace_bytes(const kvd_pool* pool, int n_q, int
  *  workspace    device scratch of workspace_bytes ≥ kvd_decode_workspace_bytes, no
  *               initialisation needed; layout: part_o f32 [S + U][g][d_h], part_lse f32
  *               [S + U][g], unit_first int32 [U], unit_count int32 [U] (−1 = output already
- *               final), each region on a 256-byte boundary (U = batch·n_kv, S splits)
+ *               final), then the step plan region (kvd_decode_plan), each region on a 256-byte
+ *               boundary (U = batch·n_kv, S splits)
  *  out          [batch][n_q][d_h] in out_dtype (KVD_BF16 rounds to nearest even, or KVD_F32);
  *               NULL = write only the partials and unit tables into the workspace (merge
  *               them later with kvd_combine_splits; lse_out is then unused)
@@ -350,7 +356,7 @@ KVD_API kvd_status kvd_decode_workspace_bytes(const kvd_pool* pool, int n_q, int
  *               every attended position (−inf where evicted), input of kvd_accum_scores
  *  scores_epilogue  NULL, or the score update to fuse into the merge launch (needs out and
  *               logits_out; n_q ≤ 256)
- *  flags        0 or KVD_EARLY_START (see above); other bits are KVD_ERR_INVALID
+ *  flags        0, KVD_EARLY_START and / or KVD_PLANNED (see above); other bits are KVD_ERR_INVALID
  * Query head h reads KV head h / g.  A head with no retained position gets out = 0 and
  * lse = −inf. */
 KVD_API kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q,
@@ -375,7 +381,8 @@ KVD_API kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int
  * go to a file-scope device array of KVD_NOALLOC_SCRATCH_BYTES bytes inside the library.
  * It allocates nothing (no cudaMalloc, no cudaFree, no allocating library routine).
  *  - A shape whose workspace (kvd_decode_workspace_bytes) exceeds KVD_NOALLOC_SCRATCH_BYTES
- *    is rejected with KVD_ERR_NOMEM before any launch; `out` may not be NULL.
+ *    is rejected with KVD_ERR_NOMEM before any launch; `out` may not be NULL; KVD_PLANNED is
+ *    KVD_ERR_INVALID (no step plan can have been made in the library's array).
  *  - The current device must be the pool's device (else KVD_ERR_INVALID).  The first call on
  *    a device, with that device current, looks up the array's device address
  *    (cudaGetSymbolAddress) once for that device and keeps it for the lifetime of the
@@ -395,6 +402,22 @@ KVD_API kvd_status kvd_decode_attn_noalloc(kvd_pool* pool, int layer, const void
                                            float* logits_out, int64_t logits_stride,
                                            const kvd_scores_desc* scores_epilogue, unsigned flags,
                                            void* stream);
+
+/* The step plan, for the layers of one decode step that share block tables and lengths.  The
+ * pages describe no split plan; this is an entry point of the library's own design.  Writes into
+ * the workspace's plan region (same workspace as the step's kvd_decode_attn calls, sized by
+ * kvd_decode_workspace_bytes) the per-request block counts' prefix sums and lengths, and, for each
+ * of the split count's CTAs, the physical ids and valid-slot masks of the first 32 blocks it will
+ * attend; kvd_decode_attn with KVD_PLANNED then starts copying K/V after one read of the plan
+ * instead of three dependent reads (lengths, block table, retain mask) per layer.  Arguments as
+ * kvd_decode_attn's; the plan stays valid while block_table, seq_lens, retain_mask (and a mixed
+ * pool's formats) are unchanged, for any layer of the pool.  Its kernel does not release a
+ * following launch before it completes, so the next kvd_decode_attn may pass KVD_EARLY_START.
+ * Bad lengths and block ids are reported on the device as kvd_decode_attn reports them. */
+KVD_API kvd_status kvd_decode_plan(kvd_pool* pool, int n_q, const int32_t* block_table, int max_blocks_per_seq,
+                                   const int32_t* seq_lens, int batch, int max_seq_len, int num_splits,
+                                   const uint16_t* retain_mask, void* workspace, size_t workspace_bytes,
+                                   void* stream);
 
 /* Merge split partials by log-sum-exp.  The pages describe no split of a request's context
  * across CTAs; this is the exact identity for the softmax over a union of disjoint position

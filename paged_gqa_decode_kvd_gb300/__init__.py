@@ -12,6 +12,7 @@ from ._lib import (  # noqa: F401
     KVD_ANGLE,
     KVD_BF16,
     KVD_EARLY_START,
+    KVD_PLANNED,
     KVD_F32,
     KVD_FP8_E4M3,
     KVD_FP8_E5M2,
@@ -39,6 +40,7 @@ from ._lib import (  # noqa: F401
     kvd_combine_splits,
     kvd_decode_attn,
     kvd_decode_attn_noalloc,
+    kvd_decode_plan,
     kvd_decode_workspace_bytes,
     kvd_measure_read_stream,
     kvd_get_device_error,

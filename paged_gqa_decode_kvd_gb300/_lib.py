@@ -13,14 +13,15 @@ import os
 
 KVD_OK, KVD_ERR_INVALID, KVD_ERR_UNSUPPORTED, KVD_ERR_NOMEM, KVD_ERR_CUDA, KVD_ERR_OOB, KVD_ERR_TIMEOUT = range(7)
 KVD_BF16, KVD_FP8_E4M3, KVD_F32, KVD_FP8_E5M2, KVD_MIXED, KVD_INT4, KVD_INT2, KVD_ANGLE = 0, 1, 2, 3, 4, 5, 6, 7
-KVD_EARLY_START = 1   # kvd_decode_attn flag
+KVD_EARLY_START = 1   # kvd_decode_attn flags
+KVD_PLANNED = 2
 
 SYMBOLS = [
     "kvd_status_string", "kvd_pool_bytes", "kvd_pool_create", "kvd_pool_destroy", "kvd_append_kv",
     "kvd_decode_workspace_bytes", "kvd_decode_attn", "kvd_combine_splits", "kvd_accum_scores",
     "kvd_get_device_error", "kvd_selftest_wait_timeout", "kvd_decode_attn_noalloc",
     "kvd_tier_bytes", "kvd_pool_attach_host_tier", "kvd_tier_prefetch", "kvd_tier_plan", "kvd_tier_move",
-    "kvd_tier_reassign", "kvd_measure_read_stream", "kvd_pool_set_block_formats",
+    "kvd_tier_reassign", "kvd_measure_read_stream", "kvd_pool_set_block_formats", "kvd_decode_plan",
 ]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -101,6 +102,8 @@ def load(build_if_missing: bool = True):
                                             i64, P, ctypes.c_uint, P]
     lib.kvd_pool_set_block_formats.restype = i32
     lib.kvd_pool_set_block_formats.argtypes = [P, P, i64]
+    lib.kvd_decode_plan.restype = i32
+    lib.kvd_decode_plan.argtypes = [P, i32, P, i32, P, i32, i32, i32, P, P, sz, P]
     lib.kvd_measure_read_stream.restype = i32
     lib.kvd_measure_read_stream.argtypes = [P, sz, P, sz, P]
     _lib = lib
@@ -248,9 +251,19 @@ def _scores_desc(scores, inv_LH):
     return ctypes.byref(ScoresDesc(scores.data_ptr(), scores.shape[-1], float(inv_LH)))
 
 
+def kvd_decode_plan(handle, n_q, block_table, seq_lens, max_seq_len, workspace, num_splits=0, retain_mask=None,
+                    stream=None):
+    """The step plan into the workspace's plan region, for kvd_decode_attn(..., planned=True) calls that
+    share block_table, seq_lens and retain_mask."""
+    _check("kvd_decode_plan", load().kvd_decode_plan(
+        handle, int(n_q), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), int(seq_lens.shape[0]),
+        int(max_seq_len), int(num_splits), _ptr(retain_mask), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
 def kvd_decode_attn(handle, layer, q, block_table, seq_lens, max_seq_len, workspace, out, num_splits=0,
                     retain_mask=None, softmax_scale=None, lse_out=None, logits_out=None, k_new=None, v_new=None,
-                    scores=None, inv_LH=None, early_start=False, stream=None):
+                    scores=None, inv_LH=None, early_start=False, planned=False, stream=None):
     batch, n_q, d_h = q.shape
     if softmax_scale is None:
         softmax_scale = d_h ** -0.5
@@ -261,7 +274,8 @@ def kvd_decode_attn(handle, layer, q, block_table, seq_lens, max_seq_len, worksp
         _ptr(seq_lens), batch,
         int(max_seq_len), int(num_splits), _ptr(retain_mask), float(softmax_scale), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(out), out_dtype, _ptr(lse_out), _ptr(logits_out),
-        lstride, _scores_desc(scores, inv_LH), KVD_EARLY_START if early_start else 0, _stream(stream)))
+        lstride, _scores_desc(scores, inv_LH), (KVD_EARLY_START if early_start else 0) | (KVD_PLANNED if planned else 0),
+        _stream(stream)))
 
 
 def kvd_combine_splits(part_o, part_lse, unit_first, unit_count, batch, n_q, n_kv, out, lse_out=None, stream=None):

@@ -62,10 +62,10 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
-    size_t part_o, part_lse, unit_first, unit_count, total;
+    size_t part_o, part_lse, unit_first, unit_count, plan, total;
 };
 
-WsLayout ws_layout(int units, int nsplit, int g) {
+WsLayout ws_layout(int units, int nsplit, int g, int batch) {
     WsLayout w;
     const size_t slots = static_cast<size_t>(units) + static_cast<size_t>(nsplit);
     size_t o = 0;
@@ -77,6 +77,8 @@ WsLayout ws_layout(int units, int nsplit, int g) {
     o = align256(o + static_cast<size_t>(units) * sizeof(int32_t));
     w.unit_count = o;
     o = align256(o + static_cast<size_t>(units) * sizeof(int32_t));
+    w.plan = o;
+    o = align256(o + static_cast<size_t>(kvd::decode_plan_words(batch, nsplit)) * sizeof(int32_t));
     w.total = o;
     return w;
 }
@@ -425,7 +427,7 @@ kvd_status kvd_decode_workspace_bytes(const kvd_pool* pool, int n_q, int batch, 
     if (st != KVD_OK) return st;
     if (num_splits < 0 || !bytes_out) return KVD_ERR_INVALID;
     const int S = num_splits > 0 ? num_splits : plan_splits(pool, batch, max_seq_len, n_q / pool->desc.n_kv);
-    const WsLayout w = ws_layout(batch * pool->desc.n_kv, S, n_q / pool->desc.n_kv);
+    const WsLayout w = ws_layout(batch * pool->desc.n_kv, S, n_q / pool->desc.n_kv, batch);
     if (splits_out) *splits_out = S;
     *bytes_out = w.total;
     return KVD_OK;
@@ -442,7 +444,7 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     if (st != KVD_OK) return st;
     if (layer < 0 || layer >= pool->desc.num_layers || num_splits < 0 || max_blocks_per_seq < 1) return KVD_ERR_INVALID;
     if (out_dtype != KVD_BF16 && out_dtype != KVD_F32) return KVD_ERR_INVALID;
-    if (flags & ~static_cast<unsigned>(KVD_EARLY_START)) return KVD_ERR_INVALID;
+    if (flags & ~static_cast<unsigned>(KVD_EARLY_START | KVD_PLANNED)) return KVD_ERR_INVALID;
     if (batch == 0) return KVD_OK;
     if (!q || !block_table || !seq_lens || !workspace) return KVD_ERR_INVALID;
     if ((k_new == nullptr) != (v_new == nullptr)) return KVD_ERR_INVALID;
@@ -458,7 +460,7 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     const int g = n_q / pool->desc.n_kv;
     const int U = batch * pool->desc.n_kv;
     const int S = num_splits > 0 ? num_splits : plan_splits(pool, batch, max_seq_len, g);
-    const WsLayout w = ws_layout(U, S, g);
+    const WsLayout w = ws_layout(U, S, g, batch);
     if (workspace_bytes < w.total) return KVD_ERR_NOMEM;
     if (pool->desc.kv_dtype == KVD_MIXED && !pool->block_fmt) return KVD_ERR_INVALID;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -487,6 +489,7 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     p.part_lse = reinterpret_cast<float*>(ws + w.part_lse);
     p.unit_first = reinterpret_cast<int32_t*>(ws + w.unit_first);
     p.unit_count = reinterpret_cast<int32_t*>(ws + w.unit_count);
+    p.plan = (flags & KVD_PLANNED) ? reinterpret_cast<const int32_t*>(ws + w.plan) : nullptr;
     p.logits = logits_out;
     p.logits_stride = logits_stride;
     p.err = pool->err;
@@ -531,6 +534,38 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     sp.n_q = n_q;
     sp.inv_LH = scores_epilogue->inv_LH;
     return cuda_status(kvd::launch_epilogue(c, sp, carveout, s));
+}
+
+kvd_status kvd_decode_plan(kvd_pool* pool, int n_q, const int32_t* block_table, int max_blocks_per_seq,
+                           const int32_t* seq_lens, int batch, int max_seq_len, int num_splits,
+                           const uint16_t* retain_mask, void* workspace, size_t workspace_bytes, void* stream) {
+    kvd_status st = check_decode_shape(pool, n_q, batch, max_seq_len);
+    if (st != KVD_OK) return st;
+    if (num_splits < 0 || max_blocks_per_seq < 1) return KVD_ERR_INVALID;
+    if (batch == 0) return KVD_OK;
+    if (!block_table || !seq_lens || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return KVD_ERR_INVALID;
+    if (pool->desc.kv_dtype == KVD_MIXED && !pool->block_fmt) return KVD_ERR_INVALID;
+    const int g = n_q / pool->desc.n_kv;
+    const int S = num_splits > 0 ? num_splits : plan_splits(pool, batch, max_seq_len, g);
+    const WsLayout w = ws_layout(batch * pool->desc.n_kv, S, g, batch);
+    if (workspace_bytes < w.total) return KVD_ERR_NOMEM;
+    kvd::DecodeParams p = {};
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.retain = retain_mask;
+    p.block_fmt = pool->block_fmt;
+    p.err = pool->err;
+    p.num_blocks = pool->desc.num_blocks;
+    p.host_blocks = pool->host_blocks;
+    p.max_blocks = max_blocks_per_seq;
+    p.B = batch;
+    p.n_kv = pool->desc.n_kv;
+    p.g = g;
+    p.n_q = n_q;
+    p.nsplit = S;
+    int32_t* plan = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + w.plan);
+    return cuda_status(kvd::launch_plan(p, plan, static_cast<cudaStream_t>(stream)));
 }
 
 kvd_status kvd_combine_splits(const float* part_o, const float* part_lse, const int32_t* unit_first,

@@ -77,6 +77,55 @@ cudaError_t launch_decode(const DecodeParams& p, int kind, int carveout, cudaStr
                                               : launch_decode_impl<false>(p, kind, carveout, stream);
 }
 
+// ---------------------------------------------------------------- step plan
+// One warp per decode CTA of the step: the prefix sums of blocks per request exactly as the
+// decode kernel forms them, and this CTA's first batch of (physical block, block word) pairs.
+// It never signals its dependents early, so a decode launched right after it sees the plan.
+__global__ void __launch_bounds__(32) plan_kernel(const DecodeParams p, int32_t* plan) {
+    extern __shared__ int plan_pref[];
+    const int lane = threadIdx.x;
+    const int cta = blockIdx.x;
+    for (int b = lane; b < p.B; b += 32) {
+        const int len = p.seq_lens[b];
+        int n = (len + kBs - 1) / kBs;
+        if (len < 1 || n > p.max_blocks) {
+            n = 0;
+            if (cta == 0) report(p.err, KVD_ERR_OOB);
+        }
+        plan_pref[b + 1] = n;
+        if (cta == 0) plan[p.B + 1 + b] = len;
+    }
+    if (lane == 0) plan_pref[0] = 0;
+    __syncwarp();
+    scan_pref(plan_pref, p.B, lane);
+    __syncwarp();
+    if (cta == 0)
+        for (int i = lane; i <= p.B; i += 32) plan[i] = plan_pref[i];
+    const int64_t T = static_cast<int64_t>(p.n_kv) * plan_pref[p.B];
+    const int64_t chunk = (T + p.nsplit - 1) / p.nsplit;
+    const int64_t lo = chunk * cta;
+    const int64_t hi = (lo + chunk < T) ? lo + chunk : T;
+    int phys = -1;
+    uint32_t vm = 0;
+    if (lo < hi) {
+        const Segment sg = find_segment(plan_pref, p.B, p.n_kv, lo, hi);
+        const int j = sg.j0 + lane;
+        if (j < sg.j1) {
+            phys = p.block_table[static_cast<int64_t>(sg.b) * p.max_blocks + j];
+            vm = block_word(phys, j, p.seq_lens[sg.b], p.num_blocks, p.host_blocks, p.retain, p.block_fmt, p.err);
+        }
+    }
+    reinterpret_cast<int2*>(plan + plan_cta_off(p.B) + static_cast<int64_t>(cta) * 2 * kPlanBatch)[lane] =
+        make_int2(phys, static_cast<int>(vm));
+}
+
+int64_t decode_plan_words(int batch, int nsplit) { return plan_words(batch, nsplit); }
+
+cudaError_t launch_plan(const DecodeParams& p, int32_t* plan, cudaStream_t stream) {
+    plan_kernel<<<p.nsplit, 32, (p.B + 1) * sizeof(int), stream>>>(p, plan);
+    return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- wait self-test
 __global__ void wait_timeout_kernel(int32_t* err, uint64_t limit_ns) {
     __shared__ __align__(8) uint64_t bar;

@@ -186,6 +186,60 @@ __device__ __noinline__ IssueState issue_batch_with_hosts(const DecodeParams& p,
     return st;
 }
 
+// The producer's word for logical block j of a request of length len whose physical block is phys:
+// bits 0-15 the slots to attend (valid positions, minus evicted ones), bit 16 set for a block
+// inside the pool (else KVD_ERR_OOB is reported and the block is empty), bits 17-18 a mixed pool
+// block's format.
+__device__ __forceinline__ uint32_t block_word(int phys, int j, int len, int64_t num_blocks, int64_t host_blocks,
+                                               const uint16_t* retain, const uint8_t* block_fmt, int32_t* err) {
+    if (phys < 0 || phys >= num_blocks + host_blocks) {
+        report(err, KVD_ERR_OOB);
+        return 0;
+    }
+    const int valid = len - j * kBs;
+    uint32_t vm = valid >= kBs ? 0xFFFFu : ((1u << valid) - 1u);
+    if (retain) vm &= retain[phys];
+    vm |= 1u << 16;
+    if (block_fmt) {   // a mixed pool: the block's precision, bits 17-18
+        const int fmt = block_format(block_fmt[phys]);
+        if (fmt < 0) {
+            report(err, KVD_ERR_OOB);
+            return 0;
+        }
+        vm |= static_cast<uint32_t>(fmt) << 17;
+    }
+    return vm;
+}
+
+// Inclusive scan of pref[1..B] in shared memory by one warp (pref[0] = 0 stays).
+__device__ __forceinline__ void scan_pref(int* pref, int B, int lane) {
+    const int per = (B + 31) / 32;
+    const int a = 1 + lane * per;
+    const int e = min(B + 1, a + per);
+    int run = 0;
+    for (int i = a; i < e; ++i) run += pref[i];
+    int incl = run;
+    #pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += v;
+    }
+    int acc = incl - run;
+    for (int i = a; i < e; ++i) {
+        acc += pref[i];
+        pref[i] = acc;
+    }
+}
+
+// A step's plan (kvd_decode_plan) in int32 words: pref [B + 1] (pref[b] = blocks of requests
+// before b), lens [B], then, from a 16-byte boundary, per CTA the (physical block, block word)
+// pairs of the first kPlanBatch blocks of its first segment.
+constexpr int kPlanBatch = 32;
+__host__ __device__ inline int64_t plan_cta_off(int B) { return (2 * static_cast<int64_t>(B) + 1 + 3) / 4 * 4; }
+__host__ __device__ inline int64_t plan_words(int B, int nsplit) {
+    return plan_cta_off(B) + static_cast<int64_t>(nsplit) * 2 * kPlanBatch;
+}
+
 // Unit holding flattened block index x: units are ordered (b, kvh); unit (b, kvh)
 // covers [n_kv·pref[b] + kvh·n_b, n_kv·pref[b] + (kvh+1)·n_b).
 __device__ __forceinline__ Segment find_segment(const int* pref, int B, int n_kv, int64_t x, int64_t hi) {
@@ -649,18 +703,33 @@ __global__ void __launch_bounds__(kThreads, (KIND == kKindFp8 || KIND == kKindAn
     }
 
     // ---- plan: blocks per request, prefix sums, this CTA's range -----------------
-    for (int b = tid; b < p.B; b += kThreads) {
-        const int len = p.seq_lens[b];
-        lens[b] = len;
-        int n = (len + kBs - 1) / kBs;
-        if (len < 1 || n > p.max_blocks) {
-            n = 0;
-            if (cta == 0) report(p.err, KVD_ERR_OOB);
+    // With a step plan (kvd_decode_plan) the prefix sums and lengths are read from it, and the
+    // producer takes its first batch of blocks from it below: one round trip instead of three.
+    int plan_phys = -1;
+    uint32_t plan_vm = 0;
+    if (p.plan) {
+        if (warp == kNcw) {
+            const int32_t* e = p.plan + plan_cta_off(p.B) + static_cast<int64_t>(cta) * 2 * kPlanBatch;
+            const int2 pv = reinterpret_cast<const int2*>(e)[lane];
+            plan_phys = pv.x;
+            plan_vm = static_cast<uint32_t>(pv.y);
         }
-        pref[b + 1] = n;
+        for (int i = tid; i <= p.B; i += kThreads) pref[i] = p.plan[i];
+        for (int b = tid; b < p.B; b += kThreads) lens[b] = p.plan[p.B + 1 + b];
+    } else {
+        for (int b = tid; b < p.B; b += kThreads) {
+            const int len = p.seq_lens[b];
+            lens[b] = len;
+            int n = (len + kBs - 1) / kBs;
+            if (len < 1 || n > p.max_blocks) {
+                n = 0;
+                if (cta == 0) report(p.err, KVD_ERR_OOB);
+            }
+            pref[b + 1] = n;
+        }
     }
     if (tid == 0) {
-        pref[0] = 0;
+        if (!p.plan) pref[0] = 0;
         *abort_flag = 0;
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
@@ -669,24 +738,7 @@ __global__ void __launch_bounds__(kThreads, (KIND == kKindFp8 || KIND == kKindAn
         mbar_fence_init();
     }
     __syncthreads();
-    if (warp == 0) {  // inclusive scan of pref[1..B]
-        const int per = (p.B + 31) / 32;
-        const int a = 1 + lane * per;
-        const int e = min(p.B + 1, a + per);
-        int run = 0;
-        for (int i = a; i < e; ++i) run += pref[i];
-        int incl = run;
-        #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o) incl += v;
-        }
-        int acc = incl - run;
-        for (int i = a; i < e; ++i) {
-            acc += pref[i];
-            pref[i] = acc;
-        }
-    }
+    if (!p.plan && warp == 0) scan_pref(pref, p.B, lane);
     __syncthreads();
 
     const int64_t T = static_cast<int64_t>(p.n_kv) * pref[p.B];
@@ -753,27 +805,17 @@ __global__ void __launch_bounds__(kThreads, (KIND == kKindFp8 || KIND == kKindAn
                 uint32_t vm = 0;
                 unsigned long long raddr = 0;
                 if (j < sg.j1) {
-                    phys = bt[j];
-                    if (phys >= 0 && phys < p.num_blocks + p.host_blocks) {
-                        // each lane forms its block's record address here, in parallel, so that
-                        // lane 0's serial issue loop below only shuffles it in
-                        raddr = reinterpret_cast<unsigned long long>(record_of<C::kRecord>(p, phys, sg.kvh));
-                        const int valid = len - j * kBs;
-                        vm = valid >= kBs ? 0xFFFFu : ((1u << valid) - 1u);
-                        if (p.retain) vm &= p.retain[phys];
-                        vm |= 1u << 16;
-                        if constexpr (KIND == kKindMixed) {   // the block's precision, bits 17-18
-                            const int fmt = block_format(p.block_fmt[phys]);
-                            if (fmt < 0) {
-                                vm = 0;
-                                report(p.err, KVD_ERR_OOB);
-                            } else {
-                                vm |= static_cast<uint32_t>(fmt) << 17;
-                            }
-                        }
+                    if (p.plan && k == 0) {   // the CTA's first batch, from the step plan
+                        phys = plan_phys;
+                        vm = plan_vm;
                     } else {
-                        report(p.err, KVD_ERR_OOB);
+                        phys = bt[j];
+                        vm = block_word(phys, j, len, p.num_blocks, p.host_blocks, p.retain,
+                                        KIND == kKindMixed ? p.block_fmt : nullptr, p.err);
                     }
+                    // each lane forms its block's record address here, in parallel, so that
+                    // lane 0's serial issue loop below only shuffles it in
+                    if (vm >> 16) raddr = reinterpret_cast<unsigned long long>(record_of<C::kRecord>(p, phys, sg.kvh));
                 }
                 const int cnt = min(32, sg.j1 - jb);
                 if (DIRECT && __any_sync(kFull, phys >= p.num_blocks)) {

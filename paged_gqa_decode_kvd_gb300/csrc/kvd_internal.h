@@ -55,6 +55,7 @@ struct DecodeParams {
     float* part_lse;             // [S + U][g]
     int32_t* unit_first;         // [U]
     int32_t* unit_count;         // [U]
+    const int32_t* plan;         // a step plan (kvd_decode_plan) in the workspace, or null
     float* logits;               // [B][n_q][logits_stride] or null
     int64_t logits_stride;
     int32_t* err;
@@ -164,6 +165,9 @@ size_t decode_smem_bytes_lowbit(int kind, int ng, int batch, int g);
 int decode_ctas_per_sm_lowbit(int kind, int ng, int batch, int g);
 cudaError_t launch_decode_lowbit(const DecodeParams& p, int kind, int carveout, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int carveout, cudaStream_t stream);
+// The step plan: prefix sums and lengths, and every decode CTA's first batch of blocks.
+int64_t decode_plan_words(int batch, int nsplit);
+cudaError_t launch_plan(const DecodeParams& p, int32_t* plan, cudaStream_t stream);
 cudaError_t launch_scores(const ScoreParams& p, cudaStream_t stream);
 cudaError_t launch_epilogue(const CombineParams& c, const ScoreParams& sp, int carveout, cudaStream_t stream);
 cudaError_t launch_wait_timeout(int32_t* err, int64_t timeout_ns, cudaStream_t stream);

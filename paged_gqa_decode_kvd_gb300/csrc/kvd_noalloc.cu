@@ -53,6 +53,7 @@ extern "C" kvd_status kvd_decode_attn_noalloc(kvd_pool* pool, int layer, const v
                                               unsigned flags, void* stream) {
     if (!pool) return KVD_ERR_INVALID;
     if (!out && batch > 0) return KVD_ERR_INVALID;  // the partials would be unreachable
+    if (flags & KVD_PLANNED) return KVD_ERR_INVALID;  // no step plan can be in the shared array
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return KVD_ERR_CUDA;
     // the scratch address below is the current device's: it must be the pool's device
