@@ -120,6 +120,15 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
+// A logit written for the score update: kept in L2 (evict-last) until the score kernel, which runs
+// about one layer later, reads it, so neither the write nor the read reaches DRAM.
+__device__ __forceinline__ void st_logit(float* p, float v) {
+    asm volatile(
+        "{\n\t.reg .b64 pol;\n\t"
+        "createpolicy.fractional.L2::evict_last.b64 pol, 1.0;\n\t"
+        "st.global.L2::cache_hint.f32 [%0], %1, pol;\n\t}" ::"l"(p), "f"(v)
+        : "memory");
+}
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

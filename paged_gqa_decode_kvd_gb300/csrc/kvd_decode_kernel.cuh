@@ -337,12 +337,12 @@ __device__ __forceinline__ void consume_block(const uint8_t* st, const uint32_t 
     {
         const int t0 = tb + gid, t1 = t0 + 8;
         if (lg0) {
-            if (t0 < lim) lg0[t0] = l0 * kLn2;
-            if (t1 < lim) lg0[t1] = l2 * kLn2;
+            if (t0 < lim) st_logit(lg0 + t0, l0 * kLn2);
+            if (t1 < lim) st_logit(lg0 + t1, l2 * kLn2);
         }
         if (lg1) {
-            if (t0 < lim) lg1[t0] = l1 * kLn2;
-            if (t1 < lim) lg1[t1] = l3 * kLn2;
+            if (t0 < lim) st_logit(lg1 + t0, l1 * kLn2);
+            if (t1 < lim) st_logit(lg1 + t1, l3 * kLn2);
         }
     }
 
@@ -573,12 +573,12 @@ __device__ __forceinline__ void consume_block_lowbit(const uint8_t* st, const ui
     {
         const int t0 = tb + gid, t1 = t0 + 8;
         if (lg0) {
-            if (t0 < lim) lg0[t0] = l0 * kLn2;
-            if (t1 < lim) lg0[t1] = l2 * kLn2;
+            if (t0 < lim) st_logit(lg0 + t0, l0 * kLn2);
+            if (t1 < lim) st_logit(lg0 + t1, l2 * kLn2);
         }
         if (lg1) {
-            if (t0 < lim) lg1[t0] = l1 * kLn2;
-            if (t1 < lim) lg1[t1] = l3 * kLn2;
+            if (t0 < lim) st_logit(lg1 + t0, l1 * kLn2);
+            if (t1 < lim) st_logit(lg1 + t1, l3 * kLn2);
         }
     }
 
