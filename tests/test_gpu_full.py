@@ -1,10 +1,15 @@
-"""Full-size workloads in the launch configuration the benchmark times, checked on
-sampled outputs the oracle computes one by one, and by properties that hold at any size.
+"""Full-size workloads in the launch configuration the benchmark times, checked against the
+oracle on whole layers (every request, or every KV head of a long request), and by properties
+that hold at any size.
 
 Every device pool is filled through kvd_append_kv from the seeded generator running on
-the GPU; the oracle regenerates the sampled requests' K/V on the host from the same
-counter-based generator (bit-identical) and never reads device memory.
+the GPU; the oracle regenerates each request's K/V on the host from the same counter-based
+generator (bit-identical) and never reads device memory.  Oracle units run on a thread pool
+(the C oracle releases the interpreter lock).
 """
+
+import concurrent.futures as cf
+import os
 
 import numpy as np
 import pytest
@@ -155,3 +160,148 @@ def test_tiered_scores_over_64_steps(cuda_device):
         s_ref = oracle.score_update(s_ref, np.stack(alphas), [n])
     got = kept_s[0].double().cpu().numpy()
     assert np.all(np.abs(got - s_ref[0]) <= H.SCORE_RTOL * np.abs(s_ref[0]) + 1e-12)
+
+
+
+# ------------------------------------------------------------- whole layers, benchmark configuration
+def _bench_layer(w, dev, layer, step=0, logits=False):
+    """One layer as the benchmark runs it: a one-layer pool holding the context before the step,
+    the step plan, then kvd_decode_attn appending the step's token itself (k_new, v_new) with early
+    start and the automatic split count."""
+    bt, bt_d, seq, seq_d, ret_d = H.device_inputs(w, dev, step)
+    lens = w.seq_lens(step)
+    pool = H.make_pool(w, layers=1)
+    H.fill_layer(pool, w, layer, bt, [n - 1 for n in lens], dev, pool_layer=0)
+    kn, vn = zip(*[w.kv(layer, b, n - 1, n, dev) for b, n in enumerate(lens)])
+    kn, vn = torch.cat(kn).contiguous(), torch.cat(vn).contiguous()
+    max_len = max(w.seq_lens(w.steps - 1))
+    S, ws = H.workspace(pool, w.n_q, w.batch, max_len, 0, dev)
+    kvd.kvd_decode_plan(pool.handle, w.n_q, bt_d, seq_d, max_len, ws, retain_mask=ret_d)
+    out = torch.empty(w.batch, w.n_q, 128, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(w.batch, w.n_q, dtype=torch.float32, device=dev)
+    kvd.kvd_decode_attn(pool.handle, 0, w.q(layer, step, dev), bt_d, seq_d, max_len, ws, out, retain_mask=ret_d,
+                        lse_out=lse, k_new=kn, v_new=vn, early_start=True, planned=True)
+    assert kvd.kvd_get_device_error(pool.handle) == 0
+    return out.float().cpu().numpy(), lse.cpu().numpy(), S, pool
+
+
+def _oracle_unit(w, layer, b, n, step=0, heads=None):
+    """Oracle on one request of any pool kind: its regenerated K/V in an identity-ordered pool (a
+    mixed pool keeps each block's format from the request's block table), optionally only the query
+    heads of some KV heads."""
+    k, v = w.kv(layer, b, 0, n)
+    q = w.q(layer, step)[b:b + 1]
+    n_kv = w.n_kv
+    if heads is not None:
+        k, v = k[:, heads], v[:, heads]
+        q = torch.cat([q[:, h * w.g:(h + 1) * w.g] for h in heads], dim=1)
+        n_kv = len(heads)
+    q = q.float().numpy()
+    nb = -(-n // 16)
+    if w.lowbit:
+        pool = oracle.OraclePool(nb, n_kv, w.d_h, 16, lowbit=w.lowbit)
+    elif w.kv_dtype == "angle":
+        pool = oracle.OraclePool(nb, n_kv, w.d_h, 16, angle=True)
+        q = oracle.angle_query(q)
+    elif w.kv_dtype == "mixed":
+        pool = oracle.OraclePool(nb, n_kv, w.d_h, 16, block_fmt=w.block_formats()[w.block_table()[b, :nb].numpy()])
+    else:
+        pool = oracle.OraclePool(nb, n_kv, w.d_h, 16, w.kv_dtype != "bf16")
+    assert pool.append(k.float().numpy(), v.float().numpy(), np.arange(n, dtype=np.int64)) == 0
+    return oracle.decode(pool, q, w.g * n_kv, np.arange(nb, dtype=np.int32)[None], [n])
+
+
+def _pool_map(fn, items):
+    with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4)) as ex:
+        return list(ex.map(fn, items))
+
+
+@pytest.mark.parametrize("name", ["llama8b", "ragged"])
+def test_whole_layer_every_request(cuda_device, name):
+    """Every request of one layer (8B: 32 x 8,192 tokens; ragged: 64 contexts in [256, 32,768])."""
+    w = get(name)
+    layer = w.L - 1
+    out, lse, S, _ = _bench_layer(w, cuda_device, layer)
+    assert S > 1
+    lens = w.seq_lens()
+    refs = _pool_map(lambda b: _oracle_unit(w, layer, b, lens[b]), range(w.batch))
+    for b, ref in enumerate(refs):
+        H.assert_out_close(out[b], ref["out"][0], what=f"{name} layer {layer} request {b}")
+        np.testing.assert_allclose(lse[b], ref["lse"][0], rtol=1e-5, atol=1e-4)
+
+
+@pytest.mark.parametrize("name", ["llama70b_fp8", "llama70b_int4", "llama70b_int2", "llama70b_angle"])
+def test_long_context_every_head(cuda_device, name):
+    """Batch 1 x 131,072 tokens split across every SM: all 8 KV heads (64 query heads) of one layer."""
+    w = get(name)
+    layer = w.L - 1
+    out, lse, S, _ = _bench_layer(w, cuda_device, layer)
+    assert S >= 152
+    refs = _pool_map(lambda h: _oracle_unit(w, layer, 0, 131072, heads=[h]), range(w.n_kv))
+    for h, ref in enumerate(refs):
+        sl = slice(h * w.g, (h + 1) * w.g)
+        H.assert_out_close(out[0, sl], ref["out"][0], what=f"{name} KV head {h}")
+        np.testing.assert_allclose(lse[0, sl], ref["lse"][0], rtol=1e-5, atol=1e-4)
+
+
+def test_mixed_precision_whole_layer(cuda_device):
+    """8B shape with every physical block BF16 / E4M3 / E5M2: every request of one layer against the
+    oracle's mixed pool (each block in the format of the physical block it occupies on the GPU)."""
+    w = get("llama8b_mixed")
+    layer = w.L - 1
+    out, lse, S, _ = _bench_layer(w, cuda_device, layer)
+    lens = w.seq_lens()
+    refs = _pool_map(lambda b: _oracle_unit(w, layer, b, lens[b]), range(w.batch))
+    for b, ref in enumerate(refs):
+        H.assert_out_close(out[b], ref["out"][0], what=f"mixed layer request {b}")
+        np.testing.assert_allclose(lse[b], ref["lse"][0], rtol=1e-5, atol=1e-4)
+
+
+def test_tiered_scores_every_request_two_steps(cuda_device):
+    """The tiered workload's first two steps, every layer: the importance score of every request
+    and position against the oracle's (1/(L·H))·Σ_ℓ Σ_h α, evicted positions included."""
+    w = get("tiered")
+    dev = cuda_device
+    pool = H.make_pool(w)
+    bt = w.block_table()
+    prefill = [c - 1 for c in w.seq_lens(0)]
+    for layer in range(w.L):
+        H.fill_layer(pool, w, layer, bt, prefill, dev)
+    max_len = max(w.seq_lens(w.steps - 1))
+    S, ws = H.workspace(pool, w.n_q, w.batch, max_len, 0, dev)
+    ret_d = H.retain_bits(w.retain_mask(bt)).to(dev)
+    bt_d = bt.to(dev)
+    scores = torch.zeros(w.batch, max_len, dtype=torch.float32, device=dev)
+    lse = torch.empty(w.batch, w.n_q, dtype=torch.float32, device=dev)
+    logits = torch.empty(w.batch, w.n_q, max_len, dtype=torch.float32, device=dev)
+    out = torch.empty(w.batch, w.n_q, 128, dtype=torch.bfloat16, device=dev)
+    inv = 1.0 / (w.L * w.n_q)
+    for t in range(2):
+        pos = w.append_pos(t)
+        seq_d = torch.tensor(w.seq_lens(t), dtype=torch.int32, device=dev)
+        kvd.kvd_decode_plan(pool.handle, w.n_q, bt_d, seq_d, max_len, ws, retain_mask=ret_d)
+        for layer in range(w.L):
+            ks, vs = zip(*[w.kv(layer, b, pos[b], pos[b] + 1, dev) for b in range(w.batch)])
+            kvd.kvd_decode_attn(pool.handle, layer, w.q(layer, t, dev), bt_d, seq_d, max_len, ws, out,
+                                retain_mask=ret_d, lse_out=lse, logits_out=logits, k_new=torch.cat(ks).contiguous(),
+                                v_new=torch.cat(vs).contiguous(), early_start=True, planned=True)
+            kvd.kvd_accum_scores(logits, lse, seq_d, inv, scores)
+    assert kvd.kvd_get_device_error(pool.handle) == 0
+    got = scores.double().cpu().numpy()
+
+    def alpha(args):
+        layer, b, t = args
+        n = w.seq_lens(t)[b]
+        r = _oracle_request(w, layer, b, n, step=t, evicted=[w.evicted_positions(b).numpy()])
+        return r["alpha"][0]
+
+    for b in range(w.batch):
+        s_ref = np.zeros((1, max_len))
+        for t in range(2):
+            n = w.seq_lens(t)[b]
+            al = _pool_map(alpha, [(layer, b, t) for layer in range(w.L)])
+            a = np.zeros((w.L, 1, w.n_q, max_len))
+            for layer in range(w.L):
+                a[layer, 0, :, :n] = al[layer]
+            s_ref = oracle.score_update(s_ref, a, [n])
+        assert np.all(np.abs(got[b] - s_ref[0]) <= H.SCORE_RTOL * np.abs(s_ref[0]) + 1e-12), b
