@@ -354,8 +354,8 @@ KVD_API kvd_status kvd_decode_workspace_bytes(const kvd_pool* pool, int n_q, int
  *  lse_out      f32 [batch][n_q] natural-log log-sum-exp of the logits, or NULL
  *  logits_out   f32 [batch][n_q][logits_stride] or NULL: the scaled logit q·k·scale of
  *               every attended position (−inf where evicted), input of kvd_accum_scores
- *  scores_epilogue  NULL, or the score update to fuse into the merge launch (needs out and
- *               logits_out; n_q ≤ 256)
+ *  scores_epilogue  NULL, or the score update to fuse into the merge launch (needs out,
+ *               lse_out and logits_out, else KVD_ERR_INVALID; n_q ≤ 256)
  *  flags        0, KVD_EARLY_START and / or KVD_PLANNED (see above); other bits are KVD_ERR_INVALID
  * Query head h reads KV head h / g.  A head with no retained position gets out = 0 and
  * lse = −inf. */

@@ -451,7 +451,9 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     if ((reinterpret_cast<uintptr_t>(k_new) & 7u) || (reinterpret_cast<uintptr_t>(v_new) & 7u)) return KVD_ERR_INVALID;
     if (logits_out && logits_stride < 1) return KVD_ERR_INVALID;
     if (scores_epilogue) {
-        if (!out || !logits_out || !scores_epilogue->scores || scores_epilogue->scores_stride < 1) return KVD_ERR_INVALID;
+        // the score update reads every head's final LSE: lse_out is required
+        if (!out || !lse_out || !logits_out || !scores_epilogue->scores || scores_epilogue->scores_stride < 1)
+            return KVD_ERR_INVALID;
         if (n_q > 256 || batch > 65535) return KVD_ERR_UNSUPPORTED;
     }
     if ((reinterpret_cast<uintptr_t>(q) & 3u) || (reinterpret_cast<uintptr_t>(out) & 15u) ||

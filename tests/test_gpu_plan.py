@@ -134,3 +134,73 @@ def test_plan_arguments(cuda_device):
                                      1, 64, 0, None, 0.1, ctypes.c_void_p(out.data_ptr()), kvd.KVD_F32, None, None, 0,
                                      None, kvd.KVD_PLANNED, None)
     assert st == kvd.KVD_ERR_INVALID
+
+
+@pytest.mark.parametrize("kind,splits", [("bf16", 0), ("fp8_e4m3", 0), ("bf16", 1000)])
+def test_planned_units_spread_over_every_cta(cuda_device, kind, splits):
+    """One KV head per request and g = 8: request 0 (40,000 tokens) is one unit cut into hundreds of
+    pieces, request 1 (20,000 tokens) has every slot evicted (all its pieces have lse = -inf), and
+    1000 splits put more CTAs in the grid than fit at once.  Five launches share one plan and repeat
+    bit for bit; planned equals unplanned bit for bit; request 0 matches the oracle, request 1 is
+    out = 0, lse = -inf."""
+    w = _custom(f"spread_{kind}", 8, 1, [40000, 20000], kind, seed=11)
+    dev = cuda_device
+    bt, bt_d, seq, seq_d, _ = H.device_inputs(w, dev)
+    lens = w.seq_lens()
+    pool = H.make_pool(w)
+    H.fill_layer(pool, w, 0, bt, lens, dev)
+    mask = torch.full((w.num_blocks(),), 0xFFFF, dtype=torch.int32)
+    mask[bt[1, : (lens[1] + 15) // 16].long()] = 0
+    ret_d = H.retain_bits(mask).to(dev)
+    _, ws = H.workspace(pool, w.n_q, w.batch, max(lens), splits)
+    kvd.kvd_decode_plan(pool.handle, w.n_q, bt_d, seq_d, max(lens), ws, num_splits=splits, retain_mask=ret_d)
+    outs = [_run(pool, w, 0, bt_d, seq_d, ws, splits, True, ret_d) for _ in range(5)]
+    assert kvd.kvd_get_device_error(pool.handle) == 0
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+    out, lse = outs[0]
+    assert torch.all(out[1] == 0) and torch.all(torch.isneginf(lse[1]))
+    a, la = _run(pool, w, 0, bt_d, seq_d, ws, splits, False, ret_d)
+    assert torch.equal(out, a) and torch.equal(lse, la)
+    ref = H.oracle_layer(w, 0, bt, lens, retain=mask)
+    H.assert_out_close(out[0].cpu().numpy(), ref["out"][0], what=f"{kind} spread unit")
+    np.testing.assert_allclose(lse[0].cpu().numpy(), ref["lse"][0], rtol=1e-5, atol=1e-4)
+
+
+def test_planned_decode_with_fused_scores(cuda_device):
+    """The fused score update (merge launch) of a planned decode against the standalone score update
+    after an unplanned one; without lse_out the fused update is rejected before any launch (it reads
+    the LSEs the decode kernel finished there)."""
+    w = _custom("plan_scores", 28, 4, [5000, 700, 3100, 16], seed=12, evict_frac=0.04, protect_prompt=64,
+                protect_recent=32)
+    dev = cuda_device
+    bt, bt_d, seq, seq_d, ret_d = H.device_inputs(w, dev)
+    lens = w.seq_lens()
+    pool = H.make_pool(w)
+    H.fill_layer(pool, w, 0, bt, lens, dev)
+    _, ws = H.workspace(pool, w.n_q, w.batch, max(lens), 0)
+    stride = max(lens) + 5
+    base = torch.rand(w.batch, stride, generator=torch.Generator().manual_seed(5)).to(dev)
+    res = []
+    for planned in (False, True):
+        scores = base.clone()
+        logits = torch.empty(w.batch, w.n_q, stride, dtype=torch.float32, device=dev)
+        out = torch.empty(w.batch, w.n_q, 128, dtype=torch.float32, device=dev)
+        lse = torch.empty(w.batch, w.n_q, dtype=torch.float32, device=dev)
+        if planned:
+            kvd.kvd_decode_plan(pool.handle, w.n_q, bt_d, seq_d, max(lens), ws, retain_mask=ret_d)
+            kvd.kvd_decode_attn(pool.handle, 0, w.q(0, 0, dev), bt_d, seq_d, max(lens), ws, out, retain_mask=ret_d,
+                                lse_out=lse, logits_out=logits, scores=scores, inv_LH=1.0 / (3 * w.n_q),
+                                early_start=True, planned=True)
+        else:
+            kvd.kvd_decode_attn(pool.handle, 0, w.q(0, 0, dev), bt_d, seq_d, max(lens), ws, out, retain_mask=ret_d,
+                                lse_out=lse, logits_out=logits)
+            kvd.kvd_accum_scores(logits, lse, seq_d, 1.0 / (3 * w.n_q), scores)
+        assert kvd.kvd_get_device_error(pool.handle) == 0
+        res.append((out.cpu(), scores.cpu()))
+    assert torch.equal(res[1][0], res[0][0])
+    torch.testing.assert_close(res[1][1], res[0][1], rtol=1e-5, atol=1e-7)
+    with pytest.raises(kvd.KvdError) as e:
+        kvd.kvd_decode_attn(pool.handle, 0, w.q(0, 0, dev), bt_d, seq_d, max(lens), ws, out, logits_out=logits,
+                            scores=scores, inv_LH=1.0, planned=True)
+    assert e.value.status == kvd.KVD_ERR_INVALID
