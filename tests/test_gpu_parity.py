@@ -407,7 +407,8 @@ def test_fused_append_equals_separate_append(cuda_device, kv_dtype):
 
 
 def test_fused_combine_matches_standalone_combine(cuda_device):
-    """The in-kernel merge (last CTA of each unit) equals kvd_combine_splits on the partials."""
+    """kvd_decode_attn's own merge launch equals kvd_combine_splits run on the partials of a call
+    without output (out = NULL)."""
     w = _custom("fusedcomb", 32, 8, [5000, 77, 2048, 700])
     dev = cuda_device
     bt, bt_d, seq, seq_d, _ = H.device_inputs(w, dev)
