@@ -125,7 +125,12 @@ typedef struct kvd_pool kvd_pool;  /* opaque */
 /* KVD_PLANNED: the workspace holds a step plan made by kvd_decode_plan for this call's shape
  * (pool, n_q, batch, max_seq_len, num_splits) and for the block_table, seq_lens and retain_mask
  * the call passes, which have not changed since; the decode kernel reads its split and its first
- * blocks from it instead of deriving them. */
+ * blocks from it instead of deriving them.  With the plan the work of a BF16 pool is also balanced
+ * at run time: when each split's range holds 192 blocks or more, every CTA streams the first 5/6
+ * of its range, and the last sixth of every range is cut into four pieces (1/2, 1/4, 1/8 and the
+ * rest of it) that CTAs take from a counter in the plan once their own part is done, the largest
+ * first.  A piece's partial does not depend on the CTA that takes it, so results repeat bit for
+ * bit.  Calls that share one workspace's plan must not run concurrently. */
 #define KVD_PLANNED 2u
 
 /* Optional score epilogue of kvd_decode_attn: adds this layer's share of the cumulative
@@ -344,10 +349,11 @@ KVD_API kvd_status kvd_decode_workspace_bytes(const kvd_pool* pool, int n_q, int
  *               slot o of physical block p is evicted (logit −inf, weight 0) in every layer
  *  softmax_scale  multiplies q·k (1/√d_h for the plain definition)
  *  workspace    device scratch of workspace_bytes ≥ kvd_decode_workspace_bytes, no
- *               initialisation needed; layout: part_o f32 [S + U][g][d_h], part_lse f32
- *               [S + U][g], unit_first int32 [U], unit_count int32 [U] (−1 = output already
- *               final), then the step plan region (kvd_decode_plan), each region on a 256-byte
- *               boundary (U = batch·n_kv, S splits)
+ *               initialisation needed; layout: part_o f32 [U + 5·S][g][d_h], part_lse f32
+ *               [U + 5·S][g], unit_first int32 [U], unit_count int32 [U] (−1 = output already
+ *               final; a unit's partials are slots unit_first .. unit_first + count − 1), then
+ *               the step plan region (kvd_decode_plan), each region on a 256-byte boundary
+ *               (U = batch·n_kv, S splits; a split's range is one piece, or five with a plan)
  *  out          [batch][n_q][d_h] in out_dtype (KVD_BF16 rounds to nearest even, or KVD_F32);
  *               NULL = write only the partials and unit tables into the workspace (merge
  *               them later with kvd_combine_splits; lse_out is then unused)
@@ -413,7 +419,9 @@ KVD_API kvd_status kvd_decode_attn_noalloc(kvd_pool* pool, int layer, const void
  * kvd_decode_attn's; the plan stays valid while block_table, seq_lens, retain_mask (and a mixed
  * pool's formats) are unchanged, for any layer of the pool.  Its kernel does not release a
  * following launch before it completes, so the next kvd_decode_attn may pass KVD_EARLY_START.
- * Bad lengths and block ids are reported on the device as kvd_decode_attn reports them. */
+ * It also zeroes the two counters of the run-time balancing (each planned launch leaves them at
+ * zero again).  Bad lengths and block ids are reported on the device as kvd_decode_attn reports
+ * them. */
 KVD_API kvd_status kvd_decode_plan(kvd_pool* pool, int n_q, const int32_t* block_table, int max_blocks_per_seq,
                                    const int32_t* seq_lens, int batch, int max_seq_len, int num_splits,
                                    const uint16_t* retain_mask, void* workspace, size_t workspace_bytes,

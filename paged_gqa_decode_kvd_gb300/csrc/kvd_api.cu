@@ -67,7 +67,8 @@ struct WsLayout {
 
 WsLayout ws_layout(int units, int nsplit, int g, int batch) {
     WsLayout w;
-    const size_t slots = static_cast<size_t>(units) + static_cast<size_t>(nsplit);
+    // a partial slot per (unit, piece): nsplit ranges of kDecodePieces pieces with dynamic balancing
+    const size_t slots = static_cast<size_t>(units) + static_cast<size_t>(nsplit) * kvd::kDecodePieces;
     size_t o = 0;
     w.part_o = o;
     o = align256(o + slots * g * kvd::kDh * sizeof(float));
@@ -492,6 +493,13 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     p.unit_first = reinterpret_cast<int32_t*>(ws + w.unit_first);
     p.unit_count = reinterpret_cast<int32_t*>(ws + w.unit_count);
     p.plan = (flags & KVD_PLANNED) ? reinterpret_cast<const int32_t*>(ws + w.plan) : nullptr;
+    // Run-time balancing with a step plan (its counters live in the plan), for BF16 pools: there
+    // the decode kernel is bound by HBM and its consumer warps have time for the segment switch
+    // a taken piece costs; the 8-bit and low-bit kernels are bound by their consumers' instructions
+    // (measured: mixed pool 7.6% slower with it, 8B BF16 2.1% and ragged BF16 4.7% faster).
+    p.dyn = (flags & KVD_PLANNED) && kind == kvd::kKindBf16
+                ? reinterpret_cast<int32_t*>(ws + w.plan) + kvd::decode_plan_dyn_off(batch, S)
+                : nullptr;
     p.logits = logits_out;
     p.logits_stride = logits_stride;
     p.err = pool->err;
@@ -523,7 +531,7 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     c.n_kv = pool->desc.n_kv;
     c.g = g;
     c.out_f32 = out_dtype == KVD_F32;
-    c.slots_hint = S / U + 2;
+    c.slots_hint = (p.dyn ? S * kvd::kDecodePieces : S) / U + 2;
     if (!scores_epilogue) return cuda_status(kvd::launch_combine(c, carveout, s));
     kvd::ScoreParams sp;
     sp.logits = logits_out;

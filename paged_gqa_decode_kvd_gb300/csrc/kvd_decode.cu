@@ -117,9 +117,11 @@ __global__ void __launch_bounds__(32) plan_kernel(const DecodeParams p, int32_t*
     }
     reinterpret_cast<int2*>(plan + plan_cta_off(p.B) + static_cast<int64_t>(cta) * 2 * kPlanBatch)[lane] =
         make_int2(phys, static_cast<int>(vm));
+    if (cta == 0 && lane < 2) plan[plan_dyn_off(p.B, p.nsplit) + lane] = 0;
 }
 
 int64_t decode_plan_words(int batch, int nsplit) { return plan_words(batch, nsplit); }
+int64_t decode_plan_dyn_off(int batch, int nsplit) { return plan_dyn_off(batch, nsplit); }
 
 cudaError_t launch_plan(const DecodeParams& p, int32_t* plan, cudaStream_t stream) {
     plan_kernel<<<p.nsplit, 32, (p.B + 1) * sizeof(int), stream>>>(p, plan);

@@ -86,7 +86,7 @@ __host__ __device__ inline Smem smem_layout(int batch, int g) {
     s.empty_off = o;
     o += kStages * 8;
     s.meta_off = o;
-    o += kStages * 4;
+    o += 2 * kStages * 4;   // per stage: the block word, then the tag of a taken piece
     o = (o + 15) & ~15;
     s.merge_off = o;
     o += 2 * merge_floats(g) * 4;
@@ -134,6 +134,7 @@ struct IssueState {
     uint32_t k;            // copies issued so far (stage k % stages is next)
     uint32_t lsu_filled;   // lane 0: stages whose last fill was cp.async (generic proxy)
     int aborted;
+    int piece;             // taken piece the stages belong to (stage tag, see kPieces)
 };
 
 // The producer's issue loop for a 32-block batch that holds host-tier blocks read in place:
@@ -158,6 +159,7 @@ __device__ __noinline__ IssueState issue_batch_with_hosts(const DecodeParams& p,
             ok = mbar_wait(&empty[s], par ^ 1u, abort_flag, kWaitNs);
             if (ok) {
                 meta[s] = static_cast<int>(m);
+                meta[kStages + s] = st.piece;
                 if (lsu) {
                     st.lsu_filled |= 1u << s;
                 } else if (m >> 16) {
@@ -233,11 +235,66 @@ __device__ __forceinline__ void scan_pref(int* pref, int B, int lane) {
 
 // A step's plan (kvd_decode_plan) in int32 words: pref [B + 1] (pref[b] = blocks of requests
 // before b), lens [B], then, from a 16-byte boundary, per CTA the (physical block, block word)
-// pairs of the first kPlanBatch blocks of its first segment.
+// pairs of the first kPlanBatch blocks of its first segment, then the two counters of dynamic
+// balancing (zeroed by the plan; the last CTA of each launch puts them back to zero).
 constexpr int kPlanBatch = 32;
 __host__ __device__ inline int64_t plan_cta_off(int B) { return (2 * static_cast<int64_t>(B) + 1 + 3) / 4 * 4; }
-__host__ __device__ inline int64_t plan_words(int B, int nsplit) {
+__host__ __device__ inline int64_t plan_dyn_off(int B, int nsplit) {
     return plan_cta_off(B) + static_cast<int64_t>(nsplit) * 2 * kPlanBatch;
+}
+__host__ __device__ inline int64_t plan_words(int B, int nsplit) { return plan_dyn_off(B, nsplit) + 2; }
+
+// Dynamic balancing (with a step plan).  The flattened work is cut into nsplit equal ranges as
+// without it, and each range into parts: its own part (the first 5/6), then kDynLevels pieces
+// that make up the last sixth, of 1/2, 1/4, 1/8 and the rest of it.  A CTA streams its own part,
+// then takes pieces from a counter shared by the grid, every CTA's largest pieces first, until
+// none is left; early CTAs so take the work that late or slow ones would have finished last.
+// Part i of range c is piece c·kPieces + i; a unit's partial for piece π goes to slot u + π (the
+// pieces are in flattened order, so the slot is unique and a unit's slots are contiguous).
+// Without dynamic balancing a range is one piece, π = c.
+constexpr int kDynLevels = 4;
+constexpr int kPieces = kDynLevels + 1;
+constexpr int64_t kDynMinChunk = 192;
+static_assert(kPieces == kDecodePieces, "pieces per range");
+
+// Start of part i (0 ≤ i ≤ kPieces) inside a range of `chunk` blocks.
+__host__ __device__ inline int64_t part_off(int64_t chunk, int i) {
+    const int64_t d = chunk / 6;
+    const int64_t a = chunk - d;
+    switch (i) {
+        case 0: return 0;
+        case 1: return a;
+        case 2: return a + d / 2;
+        case 3: return a + d / 2 + d / 4;
+        case 4: return a + d / 2 + d / 4 + d / 8;
+        default: return chunk;
+    }
+}
+
+// Piece holding flattened index x.
+__device__ __forceinline__ int64_t piece_of(int64_t x, int64_t chunk, bool dyn) {
+    const int64_t c = x / chunk;
+    if (!dyn) return c;
+    const int64_t o = x - c * chunk;
+    const int i = (o >= part_off(chunk, 1)) + (o >= part_off(chunk, 2)) + (o >= part_off(chunk, 3)) +
+                  (o >= part_off(chunk, 4));
+    return c * kPieces + i;
+}
+
+// Flattened range [x0, x1) of piece π (empty past the end of the work).
+__device__ __forceinline__ void piece_range(int64_t piece, int64_t chunk, int64_t T, bool dyn, int64_t& x0,
+                                            int64_t& x1) {
+    const int64_t c = dyn ? piece / kPieces : piece;
+    const int i = dyn ? static_cast<int>(piece % kPieces) : 0;
+    x0 = c * chunk + part_off(chunk, dyn ? i : 0);
+    x1 = c * chunk + (dyn ? part_off(chunk, i + 1) : chunk);
+    if (x0 > T) x0 = T;
+    if (x1 > T) x1 = T;
+}
+
+// The piece behind taken number d (0 ≤ d < kDynLevels·nsplit): level d / nsplit of range d % nsplit.
+__device__ __forceinline__ int64_t taken_piece(int d, int nsplit) {
+    return static_cast<int64_t>(d % nsplit) * kPieces + 1 + d / nsplit;
 }
 
 // Unit holding flattened block index x: units are ordered (b, kvh); unit (b, kvh)
@@ -743,8 +800,15 @@ __global__ void __launch_bounds__(kThreads, (KIND == kKindFp8 || KIND == kKindAn
 
     const int64_t T = static_cast<int64_t>(p.n_kv) * pref[p.B];
     const int64_t chunk = (T + p.nsplit - 1) / p.nsplit;
-    const int64_t lo = chunk * cta;
-    const int64_t hi = (lo + chunk < T) ? lo + chunk : T;
+    // Dynamic balancing needs long ranges: a taken piece costs its CTA a segment switch (q reload,
+    // state merge, partial write, about 1.5 µs), which a piece of a few blocks does not repay
+    // (measured: 70B FP8 ranges of 144 blocks 24% slower, 8B BF16 ranges of 288 blocks 3% faster).
+    // From 48 blocks on no part is empty, so a unit's pieces have consecutive numbers.
+    const bool dyn = p.dyn != nullptr && chunk >= kDynMinChunk;
+    const int64_t lo = chunk * cta < T ? chunk * cta : T;
+    // the CTA's own part: all of its range, or with dynamic balancing the part before the pieces
+    const int64_t own = lo + (dyn ? part_off(chunk, 1) : chunk);
+    const int64_t hi = own < T ? own : T;
 
     // Units with no block: no CTA covers them, so CTA 0's consumer warps mark them empty.
     if (cta == 0 && warp < kNcw) {
@@ -765,8 +829,11 @@ __global__ void __launch_bounds__(kThreads, (KIND == kKindFp8 || KIND == kKindAn
         uint32_t k = 0;
         uint32_t lsu_filled = 0;   // lane 0: stages whose last fill was cp.async (generic proxy)
         bool aborted = false;
-        for (int64_t x = lo; x < hi && !aborted;) {
-            const Segment sg = find_segment(pref, p.B, p.n_kv, x, hi);
+        int64_t rx0 = lo, rx1 = hi;   // the range being issued: the own part, then each taken piece
+        int tag = -2;                 // stage tag: the taken piece the stages belong to
+        while (!aborted) {
+        for (int64_t x = rx0; x < rx1 && !aborted;) {
+            const Segment sg = find_segment(pref, p.B, p.n_kv, x, rx1);
             const int32_t* bt = p.block_table + static_cast<int64_t>(sg.b) * p.max_blocks;
             const int len = lens[sg.b];
             if (p.k_new && sg.j1 == sg.nblk) {
@@ -823,7 +890,7 @@ __global__ void __launch_bounds__(kThreads, (KIND == kKindFp8 || KIND == kKindAn
                     // loop below stays the plain pool-block loop
                     const IssueState st = issue_batch_with_hosts<C::kRecord, kStages>(
                         p, ring, C::kStage, full, empty, meta, abort_flag, policy, phys, vm, raddr, cnt, lane,
-                        IssueState{k, lsu_filled, aborted ? 1 : 0});
+                        IssueState{k, lsu_filled, aborted ? 1 : 0, tag});
                     k = st.k;
                     lsu_filled = st.lsu_filled;
                     aborted = st.aborted != 0;
@@ -839,6 +906,7 @@ __global__ void __launch_bounds__(kThreads, (KIND == kKindFp8 || KIND == kKindAn
                         ok = mbar_wait(&empty[s], par ^ 1u, abort_flag, kWaitNs);
                         if (ok) {
                             meta[s] = static_cast<int>(m);
+                            meta[kStages + s] = tag;
                             if (m >> 16) {
                                 const uint8_t* rec = reinterpret_cast<const uint8_t*>(ra);
                                 uint8_t* dst = ring + s * C::kStage;
@@ -869,6 +937,38 @@ __global__ void __launch_bounds__(kThreads, (KIND == kKindFp8 || KIND == kKindAn
             }
             x = sg.end;
         }
+        if (!dyn || aborted) break;
+        // Take the next piece.  A number past the last piece ends the CTA's work: one stage tagged
+        // -1 tells the consumer warps, and the last CTA to get here puts the counters back to zero
+        // for the next launch that shares the plan.
+        int d = 0;
+        if (lane == 0) d = atomicAdd(p.dyn, 1);
+        d = __shfl_sync(kFull, d, 0);
+        if (d >= kDynLevels * p.nsplit) {
+            int ok = 1;
+            if (lane == 0) {
+                const int s = k % kStages;
+                ok = mbar_wait(&empty[s], ((k / kStages) & 1u) ^ 1u, abort_flag, kWaitNs);
+                if (ok) {
+                    meta[s] = 0;
+                    meta[kStages + s] = -1;
+                    mbar_arrive(&full[s]);
+                } else {
+                    report(p.err, KVD_ERR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                if (atomicAdd(p.dyn + 1, 1) == p.nsplit - 1) {
+                    p.dyn[0] = 0;
+                    p.dyn[1] = 0;
+                }
+            }
+            if (__shfl_sync(kFull, ok, 0)) ++k;
+            break;
+        }
+        const int64_t pc = taken_piece(d, p.nsplit);
+        piece_range(pc, chunk, T, true, rx0, rx1);
+        tag = static_cast<int>(pc);
+        }
         // Drain: every issued copy must land before the CTA may exit.
         if (lane == 0) {
             const uint32_t first = k > static_cast<uint32_t>(kStages) ? k - kStages : 0u;
@@ -886,8 +986,11 @@ __global__ void __launch_bounds__(kThreads, (KIND == kKindFp8 || KIND == kKindAn
     const int g = p.g;
     if (p.early) pdl_wait();   // q and every output of this kernel
     uint32_t k = 0;
-    for (int64_t x = lo; x < hi;) {
-        const Segment sg = find_segment(pref, p.B, p.n_kv, x, hi);
+    int64_t rx0 = lo, rx1 = hi;                                  // the own part, then each taken piece
+    int64_t piece = dyn ? static_cast<int64_t>(cta) * kPieces : cta;
+    while (true) {
+    for (int64_t x = rx0; x < rx1;) {
+        const Segment sg = find_segment(pref, p.B, p.n_kv, x, rx1);
         const int nseg = sg.j1 - sg.j0;
         const int len = lens[sg.b];
         const int u = sg.b * p.n_kv + sg.kvh;
@@ -1043,7 +1146,7 @@ __global__ void __launch_bounds__(kThreads, (KIND == kKindFp8 || KIND == kKindAn
                 o[i][3] = fmaf(o[i][3], 512.f, oz[gi][1]);
             }
         }
-        if (sg.end == hi) pdl_trigger();   // this CTA's last piece has been streamed
+        if (!dyn && sg.end == hi) pdl_trigger();   // this CTA's last piece has been streamed
 
         // ---- merge the consumer warps' states (register tree: 3+2 -> 1+0, then 1 -> 0) ----
         #pragma unroll
@@ -1129,12 +1232,12 @@ __global__ void __launch_bounds__(kThreads, (KIND == kKindFp8 || KIND == kKindAn
                     if (h1 < g) p.lse_out[orow + h1] = ls1;
                 }
                 if (lane == 0) {
-                    p.unit_first[u] = u + cta;
+                    p.unit_first[u] = u + static_cast<int>(piece);
                     p.unit_count[u] = -1;
                 }
             } else {
                 // this unit piece's partial: o normalised over its own positions, and its lse
-                const int slot = u + cta;
+                const int slot = u + static_cast<int>(piece);
                 float* po = p.part_o + static_cast<int64_t>(slot) * g * kDh;
                 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -1155,13 +1258,30 @@ __global__ void __launch_bounds__(kThreads, (KIND == kKindFp8 || KIND == kKindAn
                 }
                 if (sg.j0 == 0 && lane == 0) {
                     p.unit_first[u] = slot;
-                    p.unit_count[u] = static_cast<int>((sg.unit_end - 1) / chunk - cta + 1);
+                    p.unit_count[u] = static_cast<int>(piece_of(sg.unit_end - 1, chunk, dyn) - piece + 1);
                 }
             }
         }
         named_barrier(1, kNcw * 32);   // the buffer is free again for the next segment
         x = sg.end;
     }
+    if (!dyn) break;
+    // The next taken piece: its first stage carries the piece's number (-1: none left).
+    const int s = k % kStages;
+    const bool got = mbar_wait(&full[s], (k / kStages) & 1u, abort_flag, kWaitNs);
+    if (!__all_sync(kFull, got)) {
+        if (lane == 0) {
+            report(p.err, KVD_ERR_TIMEOUT);
+            *abort_flag = 1;
+        }
+        break;
+    }
+    const int t = meta[kStages + s];
+    if (t < 0) break;
+    piece = t;
+    piece_range(piece, chunk, T, true, rx0, rx1);
+    }
+    if (dyn) pdl_trigger();   // every piece of this CTA has been streamed
 }
 
 // Shared memory per SM and per-block reservation of the current device (cached per device).

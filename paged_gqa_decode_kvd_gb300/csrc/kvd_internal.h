@@ -56,6 +56,8 @@ struct DecodeParams {
     int32_t* unit_first;         // [U]
     int32_t* unit_count;         // [U]
     const int32_t* plan;         // a step plan (kvd_decode_plan) in the workspace, or null
+    int32_t* dyn;                // dynamic balancing: the plan's piece counter and finished-CTA count,
+                                 // or null (each CTA streams its whole range)
     float* logits;               // [B][n_q][logits_stride] or null
     int64_t logits_stride;
     int32_t* err;
@@ -167,6 +169,8 @@ cudaError_t launch_decode_lowbit(const DecodeParams& p, int kind, int carveout, 
 cudaError_t launch_combine(const CombineParams& p, int carveout, cudaStream_t stream);
 // The step plan: prefix sums and lengths, and every decode CTA's first batch of blocks.
 int64_t decode_plan_words(int batch, int nsplit);
+int64_t decode_plan_dyn_off(int batch, int nsplit);
+constexpr int kDecodePieces = 5;   // pieces per CTA range with dynamic balancing
 cudaError_t launch_plan(const DecodeParams& p, int32_t* plan, cudaStream_t stream);
 cudaError_t launch_scores(const ScoreParams& p, cudaStream_t stream);
 cudaError_t launch_epilogue(const CombineParams& c, const ScoreParams& sp, int carveout, cudaStream_t stream);
