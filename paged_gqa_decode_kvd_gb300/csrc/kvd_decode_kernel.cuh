@@ -568,6 +568,25 @@ __device__ __forceinline__ void lowbit_regs(uint32_t w0, uint32_t w1, int h, uin
     e4m3x4_to_f16x2x2(m1, b01, b23);
 }
 
+// The NG metadata words (scale | zero << 16) of one token, one per group, in one shared-memory load
+// (a token's words are contiguous and 4·NG-byte aligned).
+template <int NG>
+__device__ __forceinline__ void load_meta(const uint32_t* row, uint32_t (&w)[NG]) {
+    if constexpr (NG == 4) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row);
+        w[0] = v.x;
+        w[1] = v.y;
+        w[2] = v.z;
+        w[3] = v.w;
+    } else if constexpr (NG == 2) {
+        const uint2 v = *reinterpret_cast<const uint2*>(row);
+        w[0] = v.x;
+        w[1] = v.y;
+    } else {
+        w[0] = row[0];
+    }
+}
+
 // One 16-token block of a low-bit unit by one consumer warp (see consume_block for the fragment
 // roles).  K: S^T accumulates one MMA sum per group (codes·2^-9 against q), and the logit of
 // (token t, head h) is Σ_g scale_log2·(512·scale_K[t][g]·acc_g + zero_K[t][g]·Σ_{group} q_h).
@@ -614,10 +633,13 @@ __device__ __forceinline__ void consume_block_lowbit(const uint8_t* st, const ui
     const bool v0 = (m >> gid) & 1u;        // token gid
     const bool v1 = (m >> (gid + 8)) & 1u;  // token gid + 8
     float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+    uint32_t ka[NG], kb[NG];
+    load_meta<NG>(kmeta + gid * NG, ka);         // token gid
+    load_meta<NG>(kmeta + (gid + 8) * NG, kb);   // token gid + 8
     #pragma unroll
     for (int gi = 0; gi < NG; ++gi) {
-        const float2 a = unpack_f16(kmeta[gid * NG + gi]);        // (scale, zero) of token gid
-        const float2 b = unpack_f16(kmeta[(gid + 8) * NG + gi]);  // token gid + 8
+        const float2 a = unpack_f16(ka[gi]);   // (scale, zero) of token gid
+        const float2 b = unpack_f16(kb[gi]);
         const float sa = a.x * (512.f * scale_log2), sb = b.x * (512.f * scale_log2);
         l0 = fmaf(sa, acc[gi][0], fmaf(a.y, qz[gi][0], l0));
         l1 = fmaf(sa, acc[gi][1], fmaf(a.y, qz[gi][1], l1));
@@ -675,15 +697,18 @@ __device__ __forceinline__ void consume_block_lowbit(const uint8_t* st, const ui
     uint4 vw[kChunks];
     #pragma unroll
     for (int c = 0; c < kChunks; ++c) vw[c] = vt[c * 32 + lane];
+    uint32_t va_w[NG], vb_w[NG];
+    load_meta<NG>(vmeta + gid * NG, va_w);
+    load_meta<NG>(vmeta + (gid + 8) * NG, vb_w);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_s);
     float2 va[NG], vb[NG];
     #pragma unroll
     for (int gi = 0; gi < NG; ++gi) {
         // an invalid slot's scale and zero point may be garbage (NaN): its p is 0, keep it 0
-        va[gi] = v0 ? unpack_f16(vmeta[gid * NG + gi]) : make_float2(0.f, 0.f);
-        vb[gi] = v1 ? unpack_f16(vmeta[(gid + 8) * NG + gi]) : make_float2(0.f, 0.f);
+        va[gi] = unpack_f16(v0 ? va_w[gi] : 0u);
+        vb[gi] = unpack_f16(v1 ? vb_w[gi] : 0u);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty_s);
 
     // ---- O^T += V^T · P'^T per group; zero-point share in fp32 ----
     #pragma unroll
@@ -804,7 +829,9 @@ __global__ void __launch_bounds__(kThreads, (KIND == kKindFp8 || KIND == kKindAn
     // state merge, partial write, about 1.5 µs), which a piece of a few blocks does not repay
     // (measured: 70B FP8 ranges of 144 blocks 24% slower, 8B BF16 ranges of 288 blocks 3% faster).
     // From 48 blocks on no part is empty, so a unit's pieces have consecutive numbers.
-    const bool dyn = p.dyn != nullptr && chunk >= kDynMinChunk;
+    // (BF16 kernels only: the launch sets p.dyn for BF16 pools alone, and the other kinds carry
+    // none of its code)
+    const bool dyn = KIND == kKindBf16 && p.dyn != nullptr && chunk >= kDynMinChunk;
     const int64_t lo = chunk * cta < T ? chunk * cta : T;
     // the CTA's own part: all of its range, or with dynamic balancing the part before the pieces
     const int64_t own = lo + (dyn ? part_off(chunk, 1) : chunk);
@@ -906,7 +933,7 @@ __global__ void __launch_bounds__(kThreads, (KIND == kKindFp8 || KIND == kKindAn
                         ok = mbar_wait(&empty[s], par ^ 1u, abort_flag, kWaitNs);
                         if (ok) {
                             meta[s] = static_cast<int>(m);
-                            meta[kStages + s] = tag;
+                            if constexpr (KIND == kKindBf16) meta[kStages + s] = tag;   // run-time balancing
                             if (m >> 16) {
                                 const uint8_t* rec = reinterpret_cast<const uint8_t*>(ra);
                                 uint8_t* dst = ring + s * C::kStage;
