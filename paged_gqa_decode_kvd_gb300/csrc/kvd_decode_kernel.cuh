@@ -13,8 +13,11 @@
 //  * Work = the flattened sequence of (request, KV head, logical block); it is
 //    cut into `nsplit` equal contiguous ranges, one CTA each, so every CTA
 //    streams the same number of blocks whatever the length mix.  A CTA writes
-//    one partial (o, lse) per unit segment it touches into slot u + cta, and
+//    one partial (o, lse) per unit segment it touches into slot u + piece, and
 //    the combine kernel merges the partials of each unit by log-sum-exp.
+//    With a step plan, BF16 kernels balance the work at run time: the last
+//    sixth of every range is cut into pieces that CTAs done with their own part
+//    take from a counter (see kPieces).
 //  * One producer warp reads the block table (32 entries per coalesced load)
 //    and issues 1-D bulk copies (TMA engine) of each (block, KV head) record —
 //    K tile + V tile, 8 KiB BF16 or 4 KiB FP8 (+128 B of scales) — into a ring
