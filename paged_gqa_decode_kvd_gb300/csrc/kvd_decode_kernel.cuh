@@ -862,142 +862,146 @@ __global__ void __launch_bounds__(kThreads, (KIND == kKindFp8 || KIND == kKindAn
         int64_t rx0 = lo, rx1 = hi;   // the range being issued: the own part, then each taken piece
         int tag = -2;                 // stage tag: the taken piece the stages belong to
         while (!aborted) {
-        for (int64_t x = rx0; x < rx1 && !aborted;) {
-            const Segment sg = find_segment(pref, p.B, p.n_kv, x, rx1);
-            const int32_t* bt = p.block_table + static_cast<int64_t>(sg.b) * p.max_blocks;
-            const int len = lens[sg.b];
-            if (p.k_new && sg.j1 == sg.nblk) {
-                // Fused append: this CTA owns the unit's last block, so it writes the new token
-                // (position len-1) into the pool before it bulk-copies that block.
-                const int pos = len - 1;
-                const int ph = bt[pos / kBs];
-                if (p.early) pdl_wait();   // k_new / v_new come from the previous kernel
-                if (ph >= 0 && ph < p.num_blocks + p.host_blocks) {
-                    const int64_t row = (static_cast<int64_t>(sg.b) * p.n_kv + sg.kvh) * kDh;
-                    uint8_t* rec = const_cast<uint8_t*>(record_of<C::kRecord>(p, ph, sg.kvh));
-                    if constexpr (is_lowbit(KIND)) {      // no host tier
-                        write_token_lowbit<C::kBits, NG>(rec, pos % kBs, p.k_new + row, p.v_new + row, lane);
-                    } else if constexpr (KIND == kKindAngle) {   // no host tier
-                        write_token<kFmtE4m3, true>(rec, pos % kBs, p.k_new + row, p.v_new + row, lane);
-                    } else if constexpr (KIND == kKindMixed) {   // the block's own format (no host tier)
-                        const int fmt = ph < p.num_blocks ? block_format(p.block_fmt[ph]) : -1;
-                        if (fmt == kFmtBf16) write_token<kFmtBf16>(rec, pos % kBs, p.k_new + row, p.v_new + row, lane);
-                        else if (fmt == kFmtE4m3) write_token<kFmtE4m3>(rec, pos % kBs, p.k_new + row, p.v_new + row, lane);
-                        else if (fmt == kFmtE5m2) write_token<kFmtE5m2>(rec, pos % kBs, p.k_new + row, p.v_new + row, lane);
-                    } else {
-                        constexpr int kF = KIND == kKindFp8 ? kFmtE4m3 : kFmtBf16;
-                        write_token<kF>(rec, pos % kBs, p.k_new + row, p.v_new + row, lane);
-                        if (ph >= p.num_blocks && !p.host_direct)   // a staged host-tier block: its host record too
-                            write_token<kF>(p.host_kv + ((static_cast<int64_t>(ph) - p.num_blocks) * p.n_kv + sg.kvh) *
-                                                            C::kRecord,
-                                            pos % kBs, p.k_new + row, p.v_new + row, lane);
-                    }
-                    fence_proxy_async_global();
-                }
-                __syncwarp();
-            }
-            for (int jb = sg.j0; jb < sg.j1 && !aborted; jb += 32) {
-                const int j = jb + lane;
-                int phys = -1;
-                uint32_t vm = 0;
-                unsigned long long raddr = 0;
-                if (j < sg.j1) {
-                    if (p.plan && k == 0) {   // the CTA's first batch, from the step plan
-                        phys = plan_phys;
-                        vm = plan_vm;
-                    } else {
-                        phys = bt[j];
-                        vm = block_word(phys, j, len, p.num_blocks, p.host_blocks, p.retain,
-                                        KIND == kKindMixed ? p.block_fmt : nullptr, p.err);
-                    }
-                    // each lane forms its block's record address here, in parallel, so that
-                    // lane 0's serial issue loop below only shuffles it in
-                    if (vm >> 16) raddr = reinterpret_cast<unsigned long long>(record_of<C::kRecord>(p, phys, sg.kvh));
-                }
-                const int cnt = min(32, sg.j1 - jb);
-                if (DIRECT && __any_sync(kFull, phys >= p.num_blocks)) {
-                    // a batch holding host-tier blocks read in place: issued out of line, so the
-                    // loop below stays the plain pool-block loop
-                    const IssueState st = issue_batch_with_hosts<C::kRecord, kStages>(
-                        p, ring, C::kStage, full, empty, meta, abort_flag, policy, phys, vm, raddr, cnt, lane,
-                        IssueState{k, lsu_filled, aborted ? 1 : 0, tag});
-                    k = st.k;
-                    lsu_filled = st.lsu_filled;
-                    aborted = st.aborted != 0;
-                    continue;
-                }
-                for (int i = 0; i < cnt; ++i) {
-                    const uint32_t m = __shfl_sync(kFull, vm, i);
-                    const unsigned long long ra = __shfl_sync(kFull, raddr, i);
-                    const int s = k % kStages;
-                    const uint32_t par = (k / kStages) & 1u;
-                    int ok = 1;
-                    if (lane == 0) {
-                        ok = mbar_wait(&empty[s], par ^ 1u, abort_flag, kWaitNs);
-                        if (ok) {
-                            meta[s] = static_cast<int>(m);
-                            if constexpr (KIND == kKindBf16) meta[kStages + s] = tag;   // run-time balancing
-                            if (m >> 16) {
-                                const uint8_t* rec = reinterpret_cast<const uint8_t*>(ra);
-                                uint8_t* dst = ring + s * C::kStage;
-                                if (DIRECT && (lsu_filled >> s & 1u)) {   // the stage's last writes were generic
-                                    fence_proxy_async_shared();
-                                    lsu_filled &= ~(1u << s);
-                                }
-                                // a mixed pool's 8-bit block fills only the first kRecordFp8 bytes of its slot
-                                const uint32_t bytes =
-                                    KIND == kKindMixed && ((m >> 17) & 3u) != kFmtBf16 ? kRecordFp8 : C::kRecord;
-                                mbar_arrive_expect_tx(&full[s], bytes);
-                                bulk_g2s(dst, rec, bytes, &full[s], policy);
-                            } else {
-                                mbar_arrive(&full[s]);
-                            }
+            for (int64_t x = rx0; x < rx1 && !aborted;) {
+                const Segment sg = find_segment(pref, p.B, p.n_kv, x, rx1);
+                const int32_t* bt = p.block_table + static_cast<int64_t>(sg.b) * p.max_blocks;
+                const int len = lens[sg.b];
+                if (p.k_new && sg.j1 == sg.nblk) {
+                    // Fused append: this CTA owns the unit's last block, so it writes the new token
+                    // (position len-1) into the pool before it bulk-copies that block.
+                    const int pos = len - 1;
+                    const int ph = bt[pos / kBs];
+                    if (p.early) pdl_wait();   // k_new / v_new come from the previous kernel
+                    if (ph >= 0 && ph < p.num_blocks + p.host_blocks) {
+                        const int64_t row = (static_cast<int64_t>(sg.b) * p.n_kv + sg.kvh) * kDh;
+                        uint8_t* rec = const_cast<uint8_t*>(record_of<C::kRecord>(p, ph, sg.kvh));
+                        if constexpr (is_lowbit(KIND)) {      // no host tier
+                            write_token_lowbit<C::kBits, NG>(rec, pos % kBs, p.k_new + row, p.v_new + row, lane);
+                        } else if constexpr (KIND == kKindAngle) {   // no host tier
+                            write_token<kFmtE4m3, true>(rec, pos % kBs, p.k_new + row, p.v_new + row, lane);
+                        } else if constexpr (KIND == kKindMixed) {   // the block's own format (no host tier)
+                            const int fmt = ph < p.num_blocks ? block_format(p.block_fmt[ph]) : -1;
+                            const uint16_t* kn = p.k_new + row;
+                            const uint16_t* vn = p.v_new + row;
+                            if (fmt == kFmtBf16) write_token<kFmtBf16>(rec, pos % kBs, kn, vn, lane);
+                            else if (fmt == kFmtE4m3) write_token<kFmtE4m3>(rec, pos % kBs, kn, vn, lane);
+                            else if (fmt == kFmtE5m2) write_token<kFmtE5m2>(rec, pos % kBs, kn, vn, lane);
                         } else {
-                            report(p.err, KVD_ERR_TIMEOUT);
-                            *abort_flag = 1;
+                            constexpr int kF = KIND == kKindFp8 ? kFmtE4m3 : kFmtBf16;
+                            write_token<kF>(rec, pos % kBs, p.k_new + row, p.v_new + row, lane);
+                            if (ph >= p.num_blocks && !p.host_direct) {   // a staged host-tier block: its host copy too
+                                const int64_t hrec = (static_cast<int64_t>(ph) - p.num_blocks) * p.n_kv + sg.kvh;
+                                write_token<kF>(p.host_kv + hrec * C::kRecord, pos % kBs, p.k_new + row, p.v_new + row,
+                                                lane);
+                            }
                         }
+                        fence_proxy_async_global();
                     }
-                    ok = __shfl_sync(kFull, ok, 0);
-                    if (!ok) {
-                        aborted = true;
-                        break;
+                    __syncwarp();
+                }
+                for (int jb = sg.j0; jb < sg.j1 && !aborted; jb += 32) {
+                    const int j = jb + lane;
+                    int phys = -1;
+                    uint32_t vm = 0;
+                    unsigned long long raddr = 0;
+                    if (j < sg.j1) {
+                        if (p.plan && k == 0) {   // the CTA's first batch, from the step plan
+                            phys = plan_phys;
+                            vm = plan_vm;
+                        } else {
+                            phys = bt[j];
+                            vm = block_word(phys, j, len, p.num_blocks, p.host_blocks, p.retain,
+                                            KIND == kKindMixed ? p.block_fmt : nullptr, p.err);
+                        }
+                        // each lane forms its block's record address here, in parallel, so that
+                        // lane 0's serial issue loop below only shuffles it in
+                        if (vm >> 16)
+                            raddr = reinterpret_cast<unsigned long long>(record_of<C::kRecord>(p, phys, sg.kvh));
                     }
-                    ++k;
+                    const int cnt = min(32, sg.j1 - jb);
+                    if (DIRECT && __any_sync(kFull, phys >= p.num_blocks)) {
+                        // a batch holding host-tier blocks read in place: issued out of line, so the
+                        // loop below stays the plain pool-block loop
+                        const IssueState st = issue_batch_with_hosts<C::kRecord, kStages>(
+                            p, ring, C::kStage, full, empty, meta, abort_flag, policy, phys, vm, raddr, cnt, lane,
+                            IssueState{k, lsu_filled, aborted ? 1 : 0, tag});
+                        k = st.k;
+                        lsu_filled = st.lsu_filled;
+                        aborted = st.aborted != 0;
+                        continue;
+                    }
+                    for (int i = 0; i < cnt; ++i) {
+                        const uint32_t m = __shfl_sync(kFull, vm, i);
+                        const unsigned long long ra = __shfl_sync(kFull, raddr, i);
+                        const int s = k % kStages;
+                        const uint32_t par = (k / kStages) & 1u;
+                        int ok = 1;
+                        if (lane == 0) {
+                            ok = mbar_wait(&empty[s], par ^ 1u, abort_flag, kWaitNs);
+                            if (ok) {
+                                meta[s] = static_cast<int>(m);
+                                if constexpr (KIND == kKindBf16) meta[kStages + s] = tag;   // run-time balancing
+                                if (m >> 16) {
+                                    const uint8_t* rec = reinterpret_cast<const uint8_t*>(ra);
+                                    uint8_t* dst = ring + s * C::kStage;
+                                    if (DIRECT && (lsu_filled >> s & 1u)) {   // the stage's last writes were generic
+                                        fence_proxy_async_shared();
+                                        lsu_filled &= ~(1u << s);
+                                    }
+                                    // a mixed pool's 8-bit block fills only the first kRecordFp8 bytes of its slot
+                                    const uint32_t bytes =
+                                        KIND == kKindMixed && ((m >> 17) & 3u) != kFmtBf16 ? kRecordFp8 : C::kRecord;
+                                    mbar_arrive_expect_tx(&full[s], bytes);
+                                    bulk_g2s(dst, rec, bytes, &full[s], policy);
+                                } else {
+                                    mbar_arrive(&full[s]);
+                                }
+                            } else {
+                                report(p.err, KVD_ERR_TIMEOUT);
+                                *abort_flag = 1;
+                            }
+                        }
+                        ok = __shfl_sync(kFull, ok, 0);
+                        if (!ok) {
+                            aborted = true;
+                            break;
+                        }
+                        ++k;
+                    }
                 }
+                x = sg.end;
             }
-            x = sg.end;
-        }
-        if (!dyn || aborted) break;
-        // Take the next piece.  A number past the last piece ends the CTA's work: one stage tagged
-        // -1 tells the consumer warps, and the last CTA to get here puts the counters back to zero
-        // for the next launch that shares the plan.
-        int d = 0;
-        if (lane == 0) d = atomicAdd(p.dyn, 1);
-        d = __shfl_sync(kFull, d, 0);
-        if (d >= kDynLevels * p.nsplit) {
-            int ok = 1;
-            if (lane == 0) {
-                const int s = k % kStages;
-                ok = mbar_wait(&empty[s], ((k / kStages) & 1u) ^ 1u, abort_flag, kWaitNs);
-                if (ok) {
-                    meta[s] = 0;
-                    meta[kStages + s] = -1;
-                    mbar_arrive(&full[s]);
-                } else {
-                    report(p.err, KVD_ERR_TIMEOUT);
-                    *abort_flag = 1;
+            if (!dyn || aborted) break;
+            // Take the next piece.  A number past the last piece ends the CTA's work: one stage tagged
+            // -1 tells the consumer warps, and the last CTA to get here puts the counters back to zero
+            // for the next launch that shares the plan.
+            int d = 0;
+            if (lane == 0) d = atomicAdd(p.dyn, 1);
+            d = __shfl_sync(kFull, d, 0);
+            if (d >= kDynLevels * p.nsplit) {
+                int ok = 1;
+                if (lane == 0) {
+                    const int s = k % kStages;
+                    ok = mbar_wait(&empty[s], ((k / kStages) & 1u) ^ 1u, abort_flag, kWaitNs);
+                    if (ok) {
+                        meta[s] = 0;
+                        meta[kStages + s] = -1;
+                        mbar_arrive(&full[s]);
+                    } else {
+                        report(p.err, KVD_ERR_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                    if (atomicAdd(p.dyn + 1, 1) == p.nsplit - 1) {
+                        p.dyn[0] = 0;
+                        p.dyn[1] = 0;
+                    }
                 }
-                if (atomicAdd(p.dyn + 1, 1) == p.nsplit - 1) {
-                    p.dyn[0] = 0;
-                    p.dyn[1] = 0;
-                }
+                if (__shfl_sync(kFull, ok, 0)) ++k;
+                break;
             }
-            if (__shfl_sync(kFull, ok, 0)) ++k;
-            break;
-        }
-        const int64_t pc = taken_piece(d, p.nsplit);
-        piece_range(pc, chunk, T, true, rx0, rx1);
-        tag = static_cast<int>(pc);
+            const int64_t pc = taken_piece(d, p.nsplit);
+            piece_range(pc, chunk, T, true, rx0, rx1);
+            tag = static_cast<int>(pc);
         }
         // Drain: every issued copy must land before the CTA may exit.
         if (lane == 0) {
@@ -1019,297 +1023,297 @@ __global__ void __launch_bounds__(kThreads, (KIND == kKindFp8 || KIND == kKindAn
     int64_t rx0 = lo, rx1 = hi;                                  // the own part, then each taken piece
     int64_t piece = dyn ? static_cast<int64_t>(cta) * kPieces : cta;
     while (true) {
-    for (int64_t x = rx0; x < rx1;) {
-        const Segment sg = find_segment(pref, p.B, p.n_kv, x, rx1);
-        const int nseg = sg.j1 - sg.j0;
-        const int len = lens[sg.b];
-        const int u = sg.b * p.n_kv + sg.kvh;
+        for (int64_t x = rx0; x < rx1;) {
+            const Segment sg = find_segment(pref, p.B, p.n_kv, x, rx1);
+            const int nseg = sg.j1 - sg.j0;
+            const int len = lens[sg.b];
+            const int u = sg.b * p.n_kv + sg.kvh;
 
-        // Q^T fragments (B operand): head gid, dims 16i + 2tq + {0,1,8,9}; in f16 for 8-bit
-        // blocks (qf), in bf16 for BF16 blocks (qf of a BF16 pool, qfb of a mixed pool).
-        uint32_t qf[8][2];
-        uint32_t qfb[8][2];
-        {
-            const uint16_t* qh = p.q + (static_cast<int64_t>(sg.b) * p.n_q + sg.kvh * g + gid) * kDh;
-            #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                uint32_t lo2 = 0, hi2 = 0;
-                if (gid < g) {
-                    lo2 = *reinterpret_cast<const uint32_t*>(qh + 16 * i + 2 * tq);
-                    hi2 = *reinterpret_cast<const uint32_t*>(qh + 16 * i + 2 * tq + 8);
+            // Q^T fragments (B operand): head gid, dims 16i + 2tq + {0,1,8,9}; in f16 for 8-bit
+            // blocks (qf), in bf16 for BF16 blocks (qf of a BF16 pool, qfb of a mixed pool).
+            uint32_t qf[8][2];
+            uint32_t qfb[8][2];
+            {
+                const uint16_t* qh = p.q + (static_cast<int64_t>(sg.b) * p.n_q + sg.kvh * g + gid) * kDh;
+                #pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    uint32_t lo2 = 0, hi2 = 0;
+                    if (gid < g) {
+                        lo2 = *reinterpret_cast<const uint32_t*>(qh + 16 * i + 2 * tq);
+                        hi2 = *reinterpret_cast<const uint32_t*>(qh + 16 * i + 2 * tq + 8);
+                    }
+                    if constexpr (KIND == kKindMixed) {
+                        qfb[i][0] = lo2;
+                        qfb[i][1] = hi2;
+                    }
+                    if constexpr (KIND != kKindBf16) {  // bf16 -> f16 (exact inside the f16 range)
+                        const __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&lo2);
+                        const __nv_bfloat162 c = *reinterpret_cast<__nv_bfloat162*>(&hi2);
+                        lo2 = pack_f16(__low2float(a), __high2float(a));
+                        hi2 = pack_f16(__low2float(c), __high2float(c));
+                    }
+                    qf[i][0] = lo2;
+                    qf[i][1] = hi2;
                 }
+            }
+
+            // Angle-domain keys: q of head gid becomes its E4M3 direction code at its absmax scale (the
+            // f16 fragments hold the code values, exactly) and hf0 / hf1 carry ||q||/||d_q|| of heads
+            // h0 / h1 times the softmax scale.
+            float hf0 = 1.f, hf1 = 1.f;
+            if constexpr (KIND == kKindAngle) {
+                float amax = 0.f;
+                #pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float2 a = unpack_f16(qf[i][0]), b = unpack_f16(qf[i][1]);
+                    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(b.x), fabsf(b.y))));
+                }
+                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+                const float qs = amax == 0.f ? 1.f : __fdiv_rn(amax, 448.f);
+                float q2 = 0.f, d2 = 0.f;
+                #pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    #pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const float2 a = unpack_f16(qf[i][r]);
+                        const uint32_t c0 = __nv_cvt_float_to_fp8(__fdiv_rn(a.x, qs), __NV_SATFINITE, __NV_E4M3);
+                        const uint32_t c1 = __nv_cvt_float_to_fp8(__fdiv_rn(a.y, qs), __NV_SATFINITE, __NV_E4M3);
+                        qf[i][r] = e4m3x2_to_f16x2(c0 | (c1 << 8));
+                        const float2 dv = unpack_f16(qf[i][r]);
+                        q2 = fmaf(a.x, a.x, fmaf(a.y, a.y, q2));
+                        d2 = fmaf(dv.x, dv.x, fmaf(dv.y, dv.y, d2));
+                    }
+                }
+                q2 += __shfl_xor_sync(kFull, q2, 1);
+                q2 += __shfl_xor_sync(kFull, q2, 2);
+                d2 += __shfl_xor_sync(kFull, d2, 1);
+                d2 += __shfl_xor_sync(kFull, d2, 2);
+                const float f = d2 > 0.f ? sqrtf(q2) / sqrtf(d2) : 0.f;   // head gid
+                hf0 = p.scale_log2 * __shfl_sync(kFull, f, 4 * h0);
+                hf1 = p.scale_log2 * __shfl_sync(kFull, f, 4 * h1);
+            }
+
+            float m0 = -INFINITY, m1 = -INFINITY;   // running max (log2 domain), heads h0, h1
+            float s0 = 0.f, s1 = 0.f;               // running sum of p (this lane's tokens)
+            float o[8][4];
+            #pragma unroll
+            for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+            float qz[NG][2], oz[NG][2];             // low-bit pools: zero-point terms
+            #pragma unroll
+            for (int gi = 0; gi < NG; ++gi) oz[gi][0] = oz[gi][1] = 0.f;
+            if constexpr (is_lowbit(KIND)) lowbit_q_sums<NG>(qf, p.scale_log2, qz, lane);
+
+            float* lg0 = nullptr;
+            float* lg1 = nullptr;
+            if (p.logits) {
+                const int64_t rowb = static_cast<int64_t>(sg.b) * p.n_q + sg.kvh * g;
+                lg0 = h0 < g ? p.logits + (rowb + h0) * p.logits_stride : nullptr;
+                lg1 = h1 < g ? p.logits + (rowb + h1) * p.logits_stride : nullptr;
+            }
+            const int64_t lim = len < p.logits_stride ? len : p.logits_stride;
+
+            for (int kk = warp; kk < nseg; kk += kNcw) {
+                const uint32_t kg = k + kk;
+                const int s = kg % kStages;
+                // every lane observes the phase (acquire); the outcome is made warp-uniform so a
+                // timeout racing with completion cannot split the warp before the MMAs
+                const bool got = mbar_wait(&full[s], (kg / kStages) & 1u, abort_flag, kWaitNs);
+                if (!__all_sync(kFull, got)) {
+                    if (lane == 0) {
+                        report(p.err, KVD_ERR_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                    break;
+                }
+                const uint32_t m = static_cast<uint32_t>(meta[s]);
+                if (!(m >> 16)) {  // bad block id: reported by the producer, treated as empty
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[s]);
+                    continue;
+                }
+                const uint8_t* st = ring + s * C::kStage;
+                const int j = sg.j0 + kk;
+
+                const int tb = j * kBs;
                 if constexpr (KIND == kKindMixed) {
-                    qfb[i][0] = lo2;
-                    qfb[i][1] = hi2;
+                    const uint32_t fmt = (m >> 17) & 3u;
+                    if (fmt == kFmtBf16)
+                        consume_block<kFmtBf16>(st, qfb, o, m0, m1, s0, s1, m, p.scale_log2, lg0, lg1, tb, lim,
+                                                &empty[s], lane);
+                    else if (fmt == kFmtE4m3)
+                        consume_block<kFmtE4m3>(st, qf, o, m0, m1, s0, s1, m, p.scale_log2, lg0, lg1, tb, lim,
+                                                &empty[s], lane);
+                    else
+                        consume_block<kFmtE5m2>(st, qf, o, m0, m1, s0, s1, m, p.scale_log2, lg0, lg1, tb, lim,
+                                                &empty[s], lane);
+                } else if constexpr (is_lowbit(KIND)) {
+                    consume_block_lowbit<C::kBits, NG>(st, qf, qz, o, oz, m0, m1, s0, s1, m, p.scale_log2, lg0, lg1, tb,
+                                                       lim, &empty[s], lane);
+                } else if constexpr (KIND == kKindAngle) {
+                    consume_block<kFmtE4m3, true>(st, qf, o, m0, m1, s0, s1, m, p.scale_log2, lg0, lg1, tb, lim,
+                                                  &empty[s], lane, hf0, hf1);
+                } else {
+                    constexpr int kF = KIND == kKindFp8 ? kFmtE4m3 : kFmtBf16;
+                    consume_block<kF>(st, qf, o, m0, m1, s0, s1, m, p.scale_log2, lg0, lg1, tb, lim, &empty[s], lane);
                 }
-                if constexpr (KIND != kKindBf16) {  // bf16 -> f16 (exact inside the f16 range)
-                    const __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&lo2);
-                    const __nv_bfloat162 c = *reinterpret_cast<__nv_bfloat162*>(&hi2);
-                    lo2 = pack_f16(__low2float(a), __high2float(a));
-                    hi2 = pack_f16(__low2float(c), __high2float(c));
-                }
-                qf[i][0] = lo2;
-                qf[i][1] = hi2;
             }
-        }
-
-        // Angle-domain keys: q of head gid becomes its E4M3 direction code at its absmax scale (the
-        // f16 fragments hold the code values, exactly) and hf0 / hf1 carry ||q||/||d_q|| of heads
-        // h0 / h1 times the softmax scale.
-        float hf0 = 1.f, hf1 = 1.f;
-        if constexpr (KIND == kKindAngle) {
-            float amax = 0.f;
-            #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float2 a = unpack_f16(qf[i][0]), b = unpack_f16(qf[i][1]);
-                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(b.x), fabsf(b.y))));
-            }
-            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
-            const float qs = amax == 0.f ? 1.f : __fdiv_rn(amax, 448.f);
-            float q2 = 0.f, d2 = 0.f;
-            #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            k += nseg;
+            if constexpr (is_lowbit(KIND)) {
+                // o holds Σ p·scale·code·2^-9 per lane's fragment; add the zero-point share, summed
+                // over the eight lanes that hold the warp's tokens of heads h0, h1
+                constexpr int kStepsPerGroup = 8 / NG;
                 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    const float2 a = unpack_f16(qf[i][r]);
-                    const uint32_t c0 = __nv_cvt_float_to_fp8(__fdiv_rn(a.x, qs), __NV_SATFINITE, __NV_E4M3);
-                    const uint32_t c1 = __nv_cvt_float_to_fp8(__fdiv_rn(a.y, qs), __NV_SATFINITE, __NV_E4M3);
-                    qf[i][r] = e4m3x2_to_f16x2(c0 | (c1 << 8));
-                    const float2 dv = unpack_f16(qf[i][r]);
-                    q2 = fmaf(a.x, a.x, fmaf(a.y, a.y, q2));
-                    d2 = fmaf(dv.x, dv.x, fmaf(dv.y, dv.y, d2));
+                for (int gi = 0; gi < NG; ++gi) {
+                    #pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) {
+                        oz[gi][0] += __shfl_xor_sync(kFull, oz[gi][0], off);
+                        oz[gi][1] += __shfl_xor_sync(kFull, oz[gi][1], off);
+                    }
                 }
-            }
-            q2 += __shfl_xor_sync(kFull, q2, 1);
-            q2 += __shfl_xor_sync(kFull, q2, 2);
-            d2 += __shfl_xor_sync(kFull, d2, 1);
-            d2 += __shfl_xor_sync(kFull, d2, 2);
-            const float f = d2 > 0.f ? sqrtf(q2) / sqrtf(d2) : 0.f;   // head gid
-            hf0 = p.scale_log2 * __shfl_sync(kFull, f, 4 * h0);
-            hf1 = p.scale_log2 * __shfl_sync(kFull, f, 4 * h1);
-        }
-
-        float m0 = -INFINITY, m1 = -INFINITY;   // running max (log2 domain), heads h0, h1
-        float s0 = 0.f, s1 = 0.f;               // running sum of p (this lane's tokens)
-        float o[8][4];
-        #pragma unroll
-        for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-        float qz[NG][2], oz[NG][2];             // low-bit pools: zero-point terms
-        #pragma unroll
-        for (int gi = 0; gi < NG; ++gi) oz[gi][0] = oz[gi][1] = 0.f;
-        if constexpr (is_lowbit(KIND)) lowbit_q_sums<NG>(qf, p.scale_log2, qz, lane);
-
-        float* lg0 = nullptr;
-        float* lg1 = nullptr;
-        if (p.logits) {
-            const int64_t rowb = static_cast<int64_t>(sg.b) * p.n_q + sg.kvh * g;
-            lg0 = h0 < g ? p.logits + (rowb + h0) * p.logits_stride : nullptr;
-            lg1 = h1 < g ? p.logits + (rowb + h1) * p.logits_stride : nullptr;
-        }
-        const int64_t lim = len < p.logits_stride ? len : p.logits_stride;
-
-        for (int kk = warp; kk < nseg; kk += kNcw) {
-            const uint32_t kg = k + kk;
-            const int s = kg % kStages;
-            // every lane observes the phase (acquire); the outcome is made warp-uniform so a
-            // timeout racing with completion cannot split the warp before the MMAs
-            const bool got = mbar_wait(&full[s], (kg / kStages) & 1u, abort_flag, kWaitNs);
-            if (!__all_sync(kFull, got)) {
-                if (lane == 0) {
-                    report(p.err, KVD_ERR_TIMEOUT);
-                    *abort_flag = 1;
-                }
-                break;
-            }
-            const uint32_t m = static_cast<uint32_t>(meta[s]);
-            if (!(m >> 16)) {  // bad block id: reported by the producer, treated as empty
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-                continue;
-            }
-            const uint8_t* st = ring + s * C::kStage;
-            const int j = sg.j0 + kk;
-
-            const int tb = j * kBs;
-            if constexpr (KIND == kKindMixed) {
-                const uint32_t fmt = (m >> 17) & 3u;
-                if (fmt == kFmtBf16)
-                    consume_block<kFmtBf16>(st, qfb, o, m0, m1, s0, s1, m, p.scale_log2, lg0, lg1, tb, lim, &empty[s],
-                                            lane);
-                else if (fmt == kFmtE4m3)
-                    consume_block<kFmtE4m3>(st, qf, o, m0, m1, s0, s1, m, p.scale_log2, lg0, lg1, tb, lim, &empty[s],
-                                            lane);
-                else
-                    consume_block<kFmtE5m2>(st, qf, o, m0, m1, s0, s1, m, p.scale_log2, lg0, lg1, tb, lim, &empty[s],
-                                            lane);
-            } else if constexpr (is_lowbit(KIND)) {
-                consume_block_lowbit<C::kBits, NG>(st, qf, qz, o, oz, m0, m1, s0, s1, m, p.scale_log2, lg0, lg1, tb,
-                                                   lim, &empty[s], lane);
-            } else if constexpr (KIND == kKindAngle) {
-                consume_block<kFmtE4m3, true>(st, qf, o, m0, m1, s0, s1, m, p.scale_log2, lg0, lg1, tb, lim,
-                                              &empty[s], lane, hf0, hf1);
-            } else {
-                consume_block<KIND == kKindFp8 ? kFmtE4m3 : kFmtBf16>(st, qf, o, m0, m1, s0, s1, m, p.scale_log2, lg0,
-                                                                     lg1, tb, lim, &empty[s], lane);
-            }
-        }
-        k += nseg;
-        if constexpr (is_lowbit(KIND)) {
-            // o holds Σ p·scale·code·2^-9 per lane's fragment; add the zero-point share, summed
-            // over the eight lanes that hold the warp's tokens of heads h0, h1
-            constexpr int kStepsPerGroup = 8 / NG;
-            #pragma unroll
-            for (int gi = 0; gi < NG; ++gi) {
                 #pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
-                    oz[gi][0] += __shfl_xor_sync(kFull, oz[gi][0], off);
-                    oz[gi][1] += __shfl_xor_sync(kFull, oz[gi][1], off);
+                for (int i = 0; i < 8; ++i) {
+                    const int gi = i / kStepsPerGroup;
+                    o[i][0] = fmaf(o[i][0], 512.f, oz[gi][0]);
+                    o[i][2] = fmaf(o[i][2], 512.f, oz[gi][0]);
+                    o[i][1] = fmaf(o[i][1], 512.f, oz[gi][1]);
+                    o[i][3] = fmaf(o[i][3], 512.f, oz[gi][1]);
                 }
             }
-            #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int gi = i / kStepsPerGroup;
-                o[i][0] = fmaf(o[i][0], 512.f, oz[gi][0]);
-                o[i][2] = fmaf(o[i][2], 512.f, oz[gi][0]);
-                o[i][1] = fmaf(o[i][1], 512.f, oz[gi][1]);
-                o[i][3] = fmaf(o[i][3], 512.f, oz[gi][1]);
-            }
-        }
-        if (!dyn && sg.end == hi) pdl_trigger();   // this CTA's last piece has been streamed
+            if (!dyn && sg.end == hi) pdl_trigger();   // this CTA's last piece has been streamed
 
-        // ---- merge the consumer warps' states (register tree: 3+2 -> 1+0, then 1 -> 0) ----
-        #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            s0 += __shfl_xor_sync(kFull, s0, off);
-            s1 += __shfl_xor_sync(kFull, s1, off);
-        }
-        const int MF = merge_floats(g);
-        auto publish = [&](float* mb) {
+            // ---- merge the consumer warps' states (register tree: 3+2 -> 1+0, then 1 -> 0) ----
             #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int d0 = 16 * i + gid, d1 = d0 + 8;
-                if (h0 < g) {
-                    mb[h0 * kMergeStride + d0] = o[i][0];
-                    mb[h0 * kMergeStride + d1] = o[i][2];
-                }
-                if (h1 < g) {
-                    mb[h1 * kMergeStride + d0] = o[i][1];
-                    mb[h1 * kMergeStride + d1] = o[i][3];
-                }
+            for (int off = 4; off < 32; off <<= 1) {
+                s0 += __shfl_xor_sync(kFull, s0, off);
+                s1 += __shfl_xor_sync(kFull, s1, off);
             }
-            if (gid == 0) {
-                mb[g * kMergeStride + h0] = m0;
-                mb[g * kMergeStride + h1] = m1;
-                mb[g * kMergeStride + kMaxG + h0] = s0;
-                mb[g * kMergeStride + kMaxG + h1] = s1;
-            }
-        };
-        auto fold = [&](const float* mb) {
-            const float mo0 = mb[g * kMergeStride + h0], mo1 = mb[g * kMergeStride + h1];
-            const float so0 = mb[g * kMergeStride + kMaxG + h0], so1 = mb[g * kMergeStride + kMaxG + h1];
-            const float M0 = fmaxf(m0, mo0), M1 = fmaxf(m1, mo1);
-            const float z0 = M0 == -INFINITY ? 0.f : M0, z1 = M1 == -INFINITY ? 0.f : M1;
-            const float a0 = ex2(m0 - z0), b0 = ex2(mo0 - z0);   // 0 for a -inf side
-            const float a1 = ex2(m1 - z1), b1 = ex2(mo1 - z1);
-            s0 = s0 * a0 + so0 * b0;
-            s1 = s1 * a1 + so1 * b1;
-            m0 = M0;
-            m1 = M1;
-            #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int d0 = 16 * i + gid, d1 = d0 + 8;
-                const float p00 = h0 < g ? mb[h0 * kMergeStride + d0] : 0.f;
-                const float p02 = h0 < g ? mb[h0 * kMergeStride + d1] : 0.f;
-                const float p11 = h1 < g ? mb[h1 * kMergeStride + d0] : 0.f;
-                const float p13 = h1 < g ? mb[h1 * kMergeStride + d1] : 0.f;
-                o[i][0] = o[i][0] * a0 + p00 * b0;
-                o[i][2] = o[i][2] * a0 + p02 * b0;
-                o[i][1] = o[i][1] * a1 + p11 * b1;
-                o[i][3] = o[i][3] * a1 + p13 * b1;
-            }
-        };
-        if (warp >= 2) publish(merge + (warp - 2) * MF);
-        named_barrier(1, kNcw * 32);
-        if (warp < 2) fold(merge + warp * MF);
-        named_barrier(1, kNcw * 32);
-        if (warp == 1) publish(merge);
-        named_barrier(1, kNcw * 32);
-        // A unit that lies in this CTA alone is final here: write the output straight from
-        // registers and mark it done (unit_count = -1) so the combine kernel skips it.
-        const bool whole = p.out != nullptr && sg.j0 == 0 && sg.end == sg.unit_end;
-        if (warp == 0) {
-            fold(merge);
-            const float i0 = s0 > 0.f ? 1.f / s0 : 0.f, i1 = s1 > 0.f ? 1.f / s1 : 0.f;
-            const float ls0 = s0 > 0.f ? (m0 + log2f(s0)) * kLn2 : -INFINITY;
-            const float ls1 = s1 > 0.f ? (m1 + log2f(s1)) * kLn2 : -INFINITY;
-            if (whole) {
-                const int64_t orow = static_cast<int64_t>(sg.b) * p.n_q + sg.kvh * g;
+            const int MF = merge_floats(g);
+            auto publish = [&](float* mb) {
                 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int d0 = 16 * i + gid, d1 = d0 + 8;
                     if (h0 < g) {
-                        store_out(p, (orow + h0) * kDh + d0, o[i][0] * i0);
-                        store_out(p, (orow + h0) * kDh + d1, o[i][2] * i0);
+                        mb[h0 * kMergeStride + d0] = o[i][0];
+                        mb[h0 * kMergeStride + d1] = o[i][2];
                     }
                     if (h1 < g) {
-                        store_out(p, (orow + h1) * kDh + d0, o[i][1] * i1);
-                        store_out(p, (orow + h1) * kDh + d1, o[i][3] * i1);
-                    }
-                }
-                if (p.lse_out && gid == 0) {
-                    if (h0 < g) p.lse_out[orow + h0] = ls0;
-                    if (h1 < g) p.lse_out[orow + h1] = ls1;
-                }
-                if (lane == 0) {
-                    p.unit_first[u] = u + static_cast<int>(piece);
-                    p.unit_count[u] = -1;
-                }
-            } else {
-                // this unit piece's partial: o normalised over its own positions, and its lse
-                const int slot = u + static_cast<int>(piece);
-                float* po = p.part_o + static_cast<int64_t>(slot) * g * kDh;
-                #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int d0 = 16 * i + gid, d1 = d0 + 8;
-                    if (h0 < g) {
-                        po[h0 * kDh + d0] = o[i][0] * i0;
-                        po[h0 * kDh + d1] = o[i][2] * i0;
-                    }
-                    if (h1 < g) {
-                        po[h1 * kDh + d0] = o[i][1] * i1;
-                        po[h1 * kDh + d1] = o[i][3] * i1;
+                        mb[h1 * kMergeStride + d0] = o[i][1];
+                        mb[h1 * kMergeStride + d1] = o[i][3];
                     }
                 }
                 if (gid == 0) {
-                    float* pl = p.part_lse + static_cast<int64_t>(slot) * g;
-                    if (h0 < g) pl[h0] = ls0;
-                    if (h1 < g) pl[h1] = ls1;
+                    mb[g * kMergeStride + h0] = m0;
+                    mb[g * kMergeStride + h1] = m1;
+                    mb[g * kMergeStride + kMaxG + h0] = s0;
+                    mb[g * kMergeStride + kMaxG + h1] = s1;
                 }
-                if (sg.j0 == 0 && lane == 0) {
-                    p.unit_first[u] = slot;
-                    p.unit_count[u] = static_cast<int>(piece_of(sg.unit_end - 1, chunk, dyn) - piece + 1);
+            };
+            auto fold = [&](const float* mb) {
+                const float mo0 = mb[g * kMergeStride + h0], mo1 = mb[g * kMergeStride + h1];
+                const float so0 = mb[g * kMergeStride + kMaxG + h0], so1 = mb[g * kMergeStride + kMaxG + h1];
+                const float M0 = fmaxf(m0, mo0), M1 = fmaxf(m1, mo1);
+                const float z0 = M0 == -INFINITY ? 0.f : M0, z1 = M1 == -INFINITY ? 0.f : M1;
+                const float a0 = ex2(m0 - z0), b0 = ex2(mo0 - z0);   // 0 for a -inf side
+                const float a1 = ex2(m1 - z1), b1 = ex2(mo1 - z1);
+                s0 = s0 * a0 + so0 * b0;
+                s1 = s1 * a1 + so1 * b1;
+                m0 = M0;
+                m1 = M1;
+                #pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int d0 = 16 * i + gid, d1 = d0 + 8;
+                    const float p00 = h0 < g ? mb[h0 * kMergeStride + d0] : 0.f;
+                    const float p02 = h0 < g ? mb[h0 * kMergeStride + d1] : 0.f;
+                    const float p11 = h1 < g ? mb[h1 * kMergeStride + d0] : 0.f;
+                    const float p13 = h1 < g ? mb[h1 * kMergeStride + d1] : 0.f;
+                    o[i][0] = o[i][0] * a0 + p00 * b0;
+                    o[i][2] = o[i][2] * a0 + p02 * b0;
+                    o[i][1] = o[i][1] * a1 + p11 * b1;
+                    o[i][3] = o[i][3] * a1 + p13 * b1;
+                }
+            };
+            if (warp >= 2) publish(merge + (warp - 2) * MF);
+            named_barrier(1, kNcw * 32);
+            if (warp < 2) fold(merge + warp * MF);
+            named_barrier(1, kNcw * 32);
+            if (warp == 1) publish(merge);
+            named_barrier(1, kNcw * 32);
+            // A unit that lies in this CTA alone is final here: write the output straight from
+            // registers and mark it done (unit_count = -1) so the combine kernel skips it.
+            const bool whole = p.out != nullptr && sg.j0 == 0 && sg.end == sg.unit_end;
+            if (warp == 0) {
+                fold(merge);
+                const float i0 = s0 > 0.f ? 1.f / s0 : 0.f, i1 = s1 > 0.f ? 1.f / s1 : 0.f;
+                const float ls0 = s0 > 0.f ? (m0 + log2f(s0)) * kLn2 : -INFINITY;
+                const float ls1 = s1 > 0.f ? (m1 + log2f(s1)) * kLn2 : -INFINITY;
+                if (whole) {
+                    const int64_t orow = static_cast<int64_t>(sg.b) * p.n_q + sg.kvh * g;
+                    #pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int d0 = 16 * i + gid, d1 = d0 + 8;
+                        if (h0 < g) {
+                            store_out(p, (orow + h0) * kDh + d0, o[i][0] * i0);
+                            store_out(p, (orow + h0) * kDh + d1, o[i][2] * i0);
+                        }
+                        if (h1 < g) {
+                            store_out(p, (orow + h1) * kDh + d0, o[i][1] * i1);
+                            store_out(p, (orow + h1) * kDh + d1, o[i][3] * i1);
+                        }
+                    }
+                    if (p.lse_out && gid == 0) {
+                        if (h0 < g) p.lse_out[orow + h0] = ls0;
+                        if (h1 < g) p.lse_out[orow + h1] = ls1;
+                    }
+                    if (lane == 0) {
+                        p.unit_first[u] = u + static_cast<int>(piece);
+                        p.unit_count[u] = -1;
+                    }
+                } else {
+                    // this unit piece's partial: o normalised over its own positions, and its lse
+                    const int slot = u + static_cast<int>(piece);
+                    float* po = p.part_o + static_cast<int64_t>(slot) * g * kDh;
+                    #pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int d0 = 16 * i + gid, d1 = d0 + 8;
+                        if (h0 < g) {
+                            po[h0 * kDh + d0] = o[i][0] * i0;
+                            po[h0 * kDh + d1] = o[i][2] * i0;
+                        }
+                        if (h1 < g) {
+                            po[h1 * kDh + d0] = o[i][1] * i1;
+                            po[h1 * kDh + d1] = o[i][3] * i1;
+                        }
+                    }
+                    if (gid == 0) {
+                        float* pl = p.part_lse + static_cast<int64_t>(slot) * g;
+                        if (h0 < g) pl[h0] = ls0;
+                        if (h1 < g) pl[h1] = ls1;
+                    }
+                    if (sg.j0 == 0 && lane == 0) {
+                        p.unit_first[u] = slot;
+                        p.unit_count[u] = static_cast<int>(piece_of(sg.unit_end - 1, chunk, dyn) - piece + 1);
+                    }
                 }
             }
+            named_barrier(1, kNcw * 32);   // the buffer is free again for the next segment
+            x = sg.end;
         }
-        named_barrier(1, kNcw * 32);   // the buffer is free again for the next segment
-        x = sg.end;
-    }
-    if (!dyn) break;
-    // The next taken piece: its first stage carries the piece's number (-1: none left).
-    const int s = k % kStages;
-    const bool got = mbar_wait(&full[s], (k / kStages) & 1u, abort_flag, kWaitNs);
-    if (!__all_sync(kFull, got)) {
-        if (lane == 0) {
-            report(p.err, KVD_ERR_TIMEOUT);
-            *abort_flag = 1;
+        if (!dyn) break;
+        // The next taken piece: its first stage carries the piece's number (-1: none left).
+        const int s = k % kStages;
+        const bool got = mbar_wait(&full[s], (k / kStages) & 1u, abort_flag, kWaitNs);
+        if (!__all_sync(kFull, got)) {
+            if (lane == 0) {
+                report(p.err, KVD_ERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            break;
         }
-        break;
-    }
-    const int t = meta[kStages + s];
-    if (t < 0) break;
-    piece = t;
-    piece_range(piece, chunk, T, true, rx0, rx1);
+        const int t = meta[kStages + s];
+        if (t < 0) break;
+        piece = t;
+        piece_range(piece, chunk, T, true, rx0, rx1);
     }
     if (dyn) pdl_trigger();   // every piece of this CTA has been streamed
 }
