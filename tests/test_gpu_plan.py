@@ -79,8 +79,10 @@ def test_planned_decode_equals_unplanned(cuda_device, kind, group):
             np.testing.assert_allclose(res[1][0][1].numpy(), ref["lse"], rtol=1e-5, atol=1e-4)
 
 
-@pytest.mark.parametrize("staged", [False, True])
-def test_planned_decode_with_a_host_tier(cuda_device, staged):
+@pytest.mark.parametrize("staged,splits", [(False, 0), (True, 0), (False, 8)])
+def test_planned_decode_with_a_host_tier(cuda_device, staged, splits):
+    """8 splits: ranges of 373 blocks, so the run-time balancing's pieces (taken by any CTA) hold
+    host-tier blocks read in place."""
     w = _custom("plan_tier", 32, 8, [3000, 900, 2048], seed=4)
     dev = cuda_device
     bt, bt_d, seq, seq_d, _ = H.device_inputs(w, dev)
@@ -97,10 +99,10 @@ def test_planned_decode_with_a_host_tier(cuda_device, staged):
     bt2_d = bt2.to(dev)
     if staged:
         kvd.kvd_tier_prefetch(pool.handle, 0)
-    _, ws = H.workspace(pool, w.n_q, w.batch, max(w.seq_lens()), 0)
-    a, la = _run(pool, w, 0, bt2_d, seq_d, ws, 0, False)
-    kvd.kvd_decode_plan(pool.handle, w.n_q, bt2_d, seq_d, max(w.seq_lens()), ws)
-    b, lb = _run(pool, w, 0, bt2_d, seq_d, ws, 0, True)
+    _, ws = H.workspace(pool, w.n_q, w.batch, max(w.seq_lens()), splits)
+    a, la = _run(pool, w, 0, bt2_d, seq_d, ws, splits, False)
+    kvd.kvd_decode_plan(pool.handle, w.n_q, bt2_d, seq_d, max(w.seq_lens()), ws, num_splits=splits)
+    b, lb = _run(pool, w, 0, bt2_d, seq_d, ws, splits, True)
     assert kvd.kvd_get_device_error(pool.handle) == 0
     torch.testing.assert_close(b, a, rtol=0, atol=H.SPLIT_ATOL)
     torch.testing.assert_close(lb, la, rtol=1e-5, atol=1e-4)
@@ -181,10 +183,12 @@ def test_planned_units_spread_over_every_cta(cuda_device, kind, splits):
     np.testing.assert_allclose(lse[0].cpu().numpy(), ref["lse"][0], rtol=1e-5, atol=1e-4)
 
 
-def test_planned_decode_with_fused_scores(cuda_device):
+@pytest.mark.parametrize("splits", [0, 4])
+def test_planned_decode_with_fused_scores(cuda_device, splits):
     """The fused score update (merge launch) of a planned decode against the standalone score update
-    after an unplanned one; without lse_out the fused update is rejected before any launch (it reads
-    the LSEs the decode kernel finished there)."""
+    after an unplanned one (4 splits: ranges long enough for run-time balancing); without lse_out
+    the fused update is rejected before any launch (it reads the LSEs the decode kernel finished
+    there)."""
     w = _custom("plan_scores", 28, 4, [5000, 700, 3100, 16], seed=12, evict_frac=0.04, protect_prompt=64,
                 protect_recent=32)
     dev = cuda_device
@@ -192,7 +196,7 @@ def test_planned_decode_with_fused_scores(cuda_device):
     lens = w.seq_lens()
     pool = H.make_pool(w)
     H.fill_layer(pool, w, 0, bt, lens, dev)
-    _, ws = H.workspace(pool, w.n_q, w.batch, max(lens), 0)
+    _, ws = H.workspace(pool, w.n_q, w.batch, max(lens), splits)
     stride = max(lens) + 5
     base = torch.rand(w.batch, stride, generator=torch.Generator().manual_seed(5)).to(dev)
     res = []
@@ -202,19 +206,20 @@ def test_planned_decode_with_fused_scores(cuda_device):
         out = torch.empty(w.batch, w.n_q, 128, dtype=torch.float32, device=dev)
         lse = torch.empty(w.batch, w.n_q, dtype=torch.float32, device=dev)
         if planned:
-            kvd.kvd_decode_plan(pool.handle, w.n_q, bt_d, seq_d, max(lens), ws, retain_mask=ret_d)
-            kvd.kvd_decode_attn(pool.handle, 0, w.q(0, 0, dev), bt_d, seq_d, max(lens), ws, out, retain_mask=ret_d,
-                                lse_out=lse, logits_out=logits, scores=scores, inv_LH=1.0 / (3 * w.n_q),
-                                early_start=True, planned=True)
+            kvd.kvd_decode_plan(pool.handle, w.n_q, bt_d, seq_d, max(lens), ws, num_splits=splits,
+                                retain_mask=ret_d)
+            kvd.kvd_decode_attn(pool.handle, 0, w.q(0, 0, dev), bt_d, seq_d, max(lens), ws, out, num_splits=splits,
+                                retain_mask=ret_d, lse_out=lse, logits_out=logits, scores=scores,
+                                inv_LH=1.0 / (3 * w.n_q), early_start=True, planned=True)
         else:
-            kvd.kvd_decode_attn(pool.handle, 0, w.q(0, 0, dev), bt_d, seq_d, max(lens), ws, out, retain_mask=ret_d,
-                                lse_out=lse, logits_out=logits)
+            kvd.kvd_decode_attn(pool.handle, 0, w.q(0, 0, dev), bt_d, seq_d, max(lens), ws, out, num_splits=splits,
+                                retain_mask=ret_d, lse_out=lse, logits_out=logits)
             kvd.kvd_accum_scores(logits, lse, seq_d, 1.0 / (3 * w.n_q), scores)
         assert kvd.kvd_get_device_error(pool.handle) == 0
         res.append((out.cpu(), scores.cpu()))
     torch.testing.assert_close(res[1][0], res[0][0], rtol=0, atol=H.SPLIT_ATOL)
     torch.testing.assert_close(res[1][1], res[0][1], rtol=1e-5, atol=1e-7)
     with pytest.raises(kvd.KvdError) as e:
-        kvd.kvd_decode_attn(pool.handle, 0, w.q(0, 0, dev), bt_d, seq_d, max(lens), ws, out, logits_out=logits,
-                            scores=scores, inv_LH=1.0, planned=True)
+        kvd.kvd_decode_attn(pool.handle, 0, w.q(0, 0, dev), bt_d, seq_d, max(lens), ws, out, num_splits=splits,
+                            logits_out=logits, scores=scores, inv_LH=1.0, planned=True)
     assert e.value.status == kvd.KVD_ERR_INVALID
