@@ -343,8 +343,9 @@ KVD_API kvd_status kvd_decode_workspace_bytes(const kvd_pool* pool, int n_q, int
  *  max_seq_len  host upper bound on seq_lens, used only for the split plan
  *  num_splits   0 = automatic; else the number of KV splits: the flattened sequence of
  *               (request, KV head, block) work is cut into num_splits equal contiguous
- *               ranges, one CTA each; partial results are merged by log-sum-exp (a unit
- *               that lies inside one CTA is finished by that CTA directly)
+ *               ranges, one CTA each (with KVD_PLANNED a BF16 pool's long ranges are also
+ *               balanced at run time, see KVD_PLANNED); partial results are merged by
+ *               log-sum-exp (a unit that lies inside one piece is finished directly)
  *  retain_mask  uint16 [num_blocks + host_blocks] or NULL; bit o of retain_mask[p] clear =
  *               slot o of physical block p is evicted (logit −inf, weight 0) in every layer
  *  softmax_scale  multiplies q·k (1/√d_h for the plain definition)
