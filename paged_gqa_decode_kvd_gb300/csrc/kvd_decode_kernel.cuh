@@ -743,9 +743,11 @@ __device__ __forceinline__ void consume_block_lowbit(const uint8_t* st, const ui
 // DIRECT: the pool's host-tier blocks are read in place from host memory (lsu_fill); only
 // pools with such a tier launch this variant, so the others carry none of its code.
 template <int KIND, int S, bool DIRECT, int NG = 1>
-__global__ void __launch_bounds__(kThreads, (KIND == kKindFp8 || KIND == kKindAngle) && S == 8 ? 4
-                                           : KIND == kKindMixed                             ? 2
-                                                                                            : 3)
+__global__ void __launch_bounds__(kThreads, ((KIND == kKindFp8 || KIND == kKindAngle) && S == 8) ||
+                                                   (is_lowbit(KIND) && NG == 1)
+                                               ? 4
+                                           : KIND == kKindMixed ? 2
+                                                                : 3)
     decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     using C = Cfg<KIND, S, NG>;
