@@ -350,11 +350,12 @@ KVD_API kvd_status kvd_decode_workspace_bytes(const kvd_pool* pool, int n_q, int
  *               slot o of physical block p is evicted (logit −inf, weight 0) in every layer
  *  softmax_scale  multiplies q·k (1/√d_h for the plain definition)
  *  workspace    device scratch of workspace_bytes ≥ kvd_decode_workspace_bytes, no
- *               initialisation needed; layout: part_o f32 [U + 5·S][g][d_h], part_lse f32
- *               [U + 5·S][g], unit_first int32 [U], unit_count int32 [U] (−1 = output already
- *               final; a unit's partials are slots unit_first .. unit_first + count − 1), then
- *               the step plan region (kvd_decode_plan), each region on a 256-byte boundary
- *               (U = batch·n_kv, S splits; a split's range is one piece, or five with a plan)
+ *               initialisation needed; layout: part_o f32 [U + P·S][g][d_h], part_lse f32
+ *               [U + P·S][g], unit_first int32 [U], unit_count int32 [U] (−1 = output already
+ *               final; a unit's partials are slots unit_first .. unit_first + count − 1), then,
+ *               with KVD_PLANNED, the step plan region (kvd_decode_plan), each region on a
+ *               256-byte boundary (U = batch·n_kv, S splits, P = 5 pieces a split with
+ *               KVD_PLANNED, else 1; kvd_decode_workspace_bytes reports the planned size)
  *  out          [batch][n_q][d_h] in out_dtype (KVD_BF16 rounds to nearest even, or KVD_F32);
  *               NULL = write only the partials and unit tables into the workspace (merge
  *               them later with kvd_combine_splits; lse_out is then unused)
@@ -387,7 +388,8 @@ KVD_API kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int
  * Same arguments and results as kvd_decode_attn, minus the workspace: the split partials
  * go to a file-scope device array of KVD_NOALLOC_SCRATCH_BYTES bytes inside the library.
  * It allocates nothing (no cudaMalloc, no cudaFree, no allocating library routine).
- *  - A shape whose workspace (kvd_decode_workspace_bytes) exceeds KVD_NOALLOC_SCRATCH_BYTES
+ *  - A shape whose unplanned workspace (kvd_decode_attn's layout without KVD_PLANNED, at most
+ *    kvd_decode_workspace_bytes) exceeds KVD_NOALLOC_SCRATCH_BYTES
  *    is rejected with KVD_ERR_NOMEM before any launch; `out` may not be NULL; KVD_PLANNED is
  *    KVD_ERR_INVALID (no step plan can have been made in the library's array).
  *  - The current device must be the pool's device (else KVD_ERR_INVALID).  The first call on

@@ -65,10 +65,12 @@ struct WsLayout {
     size_t part_o, part_lse, unit_first, unit_count, plan, total;
 };
 
-WsLayout ws_layout(int units, int nsplit, int g, int batch) {
+// The workspace of a call: a partial slot per (unit, piece), a range being one piece, or with a
+// step plan (run-time balancing) kDecodePieces; then the unit tables and, for a planned call,
+// the plan.  kvd_decode_workspace_bytes reports the planned size, which serves both.
+WsLayout ws_layout(int units, int nsplit, int g, int batch, bool planned) {
     WsLayout w;
-    // a partial slot per (unit, piece): nsplit ranges of kDecodePieces pieces with dynamic balancing
-    const size_t slots = static_cast<size_t>(units) + static_cast<size_t>(nsplit) * kvd::kDecodePieces;
+    const size_t slots = static_cast<size_t>(units) + static_cast<size_t>(nsplit) * (planned ? kvd::kDecodePieces : 1);
     size_t o = 0;
     w.part_o = o;
     o = align256(o + slots * g * kvd::kDh * sizeof(float));
@@ -79,7 +81,7 @@ WsLayout ws_layout(int units, int nsplit, int g, int batch) {
     w.unit_count = o;
     o = align256(o + static_cast<size_t>(units) * sizeof(int32_t));
     w.plan = o;
-    o = align256(o + static_cast<size_t>(kvd::decode_plan_words(batch, nsplit)) * sizeof(int32_t));
+    if (planned) o = align256(o + static_cast<size_t>(kvd::decode_plan_words(batch, nsplit)) * sizeof(int32_t));
     w.total = o;
     return w;
 }
@@ -422,16 +424,29 @@ static kvd_status check_decode_shape(const kvd_pool* pool, int n_q, int batch, i
     return KVD_OK;
 }
 
-kvd_status kvd_decode_workspace_bytes(const kvd_pool* pool, int n_q, int batch, int max_seq_len, int num_splits,
-                                      int* splits_out, size_t* bytes_out) {
+}  // extern "C"
+
+namespace kvd {
+// Workspace bytes of a planned call (which also serve an unplanned one), or of an unplanned call
+// alone (the no-alloc entry point, which takes no plan).
+kvd_status decode_workspace_bytes(const kvd_pool* pool, int n_q, int batch, int max_seq_len, int num_splits,
+                                  bool planned, int* splits_out, size_t* bytes_out) {
     kvd_status st = check_decode_shape(pool, n_q, batch, max_seq_len);
     if (st != KVD_OK) return st;
     if (num_splits < 0 || !bytes_out) return KVD_ERR_INVALID;
     const int S = num_splits > 0 ? num_splits : plan_splits(pool, batch, max_seq_len, n_q / pool->desc.n_kv);
-    const WsLayout w = ws_layout(batch * pool->desc.n_kv, S, n_q / pool->desc.n_kv, batch);
+    const WsLayout w = ws_layout(batch * pool->desc.n_kv, S, n_q / pool->desc.n_kv, batch, planned);
     if (splits_out) *splits_out = S;
     *bytes_out = w.total;
     return KVD_OK;
+}
+}  // namespace kvd
+
+extern "C" {
+
+kvd_status kvd_decode_workspace_bytes(const kvd_pool* pool, int n_q, int batch, int max_seq_len, int num_splits,
+                                      int* splits_out, size_t* bytes_out) {
+    return kvd::decode_workspace_bytes(pool, n_q, batch, max_seq_len, num_splits, true, splits_out, bytes_out);
 }
 
 kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, const void* k_new, const void* v_new,
@@ -463,7 +478,7 @@ kvd_status kvd_decode_attn(kvd_pool* pool, int layer, const void* q, int n_q, co
     const int g = n_q / pool->desc.n_kv;
     const int U = batch * pool->desc.n_kv;
     const int S = num_splits > 0 ? num_splits : plan_splits(pool, batch, max_seq_len, g);
-    const WsLayout w = ws_layout(U, S, g, batch);
+    const WsLayout w = ws_layout(U, S, g, batch, (flags & KVD_PLANNED) != 0);
     if (workspace_bytes < w.total) return KVD_ERR_NOMEM;
     if (pool->desc.kv_dtype == KVD_MIXED && !pool->block_fmt) return KVD_ERR_INVALID;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -558,7 +573,7 @@ kvd_status kvd_decode_plan(kvd_pool* pool, int n_q, const int32_t* block_table, 
     if (pool->desc.kv_dtype == KVD_MIXED && !pool->block_fmt) return KVD_ERR_INVALID;
     const int g = n_q / pool->desc.n_kv;
     const int S = num_splits > 0 ? num_splits : plan_splits(pool, batch, max_seq_len, g);
-    const WsLayout w = ws_layout(batch * pool->desc.n_kv, S, g, batch);
+    const WsLayout w = ws_layout(batch * pool->desc.n_kv, S, g, batch, true);
     if (workspace_bytes < w.total) return KVD_ERR_NOMEM;
     kvd::DecodeParams p = {};
     p.block_table = block_table;

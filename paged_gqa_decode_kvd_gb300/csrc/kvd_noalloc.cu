@@ -43,6 +43,11 @@ kvd_status scratch_for_device(int dev, void** out) {
 
 }  // namespace
 
+namespace kvd {
+kvd_status decode_workspace_bytes(const kvd_pool* pool, int n_q, int batch, int max_seq_len, int num_splits,
+                                  bool planned, int* splits_out, size_t* bytes_out);   // kvd_api.cu
+}
+
 extern "C" kvd_status kvd_decode_attn_noalloc(kvd_pool* pool, int layer, const void* q, int n_q,
                                               const void* k_new, const void* v_new,
                                               const int32_t* block_table, int max_blocks_per_seq,
@@ -60,7 +65,7 @@ extern "C" kvd_status kvd_decode_attn_noalloc(kvd_pool* pool, int layer, const v
     if (dev != kvd::pool_device(pool)) return KVD_ERR_INVALID;
     int splits = 0;
     size_t need = 0;
-    kvd_status st = kvd_decode_workspace_bytes(pool, n_q, batch, max_seq_len, num_splits, &splits, &need);
+    kvd_status st = kvd::decode_workspace_bytes(pool, n_q, batch, max_seq_len, num_splits, false, &splits, &need);
     if (st != KVD_OK) return st;
     if (need > static_cast<size_t>(KVD_NOALLOC_SCRATCH_BYTES)) return KVD_ERR_NOMEM;
     void* scratch = nullptr;

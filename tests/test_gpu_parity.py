@@ -422,7 +422,7 @@ def test_fused_combine_matches_standalone_combine(cuda_device):
         kvd.kvd_decode_attn(pool.handle, 0, q, bt_d, seq_d, 5000, ws, fused, num_splits=splits, lse_out=flse)
         kvd.kvd_decode_attn(pool.handle, 0, q, bt_d, seq_d, 5000, ws, None, num_splits=splits)
         U, g = w.batch * w.n_kv, w.g
-        slots = U + 5 * S   # workspace layout (kvd.h): a partial slot per unit and per piece, 5 pieces a split
+        slots = U + S   # workspace layout of an unplanned call (kvd.h): a partial slot per unit and per split
         a256 = lambda x: (x + 255) // 256 * 256
         o_po, o_pl = 0, a256(slots * g * 128 * 4)
         o_uf = o_pl + a256(slots * g * 4)

@@ -105,3 +105,18 @@ def test_noalloc_rejects_shapes_beyond_its_scratch_and_a_null_output(cuda_device
     with pytest.raises(kvd.KvdError) as e:
         kvd.kvd_decode_attn_noalloc(pool.handle, 0, q[:1], bt[:1], seq[:1], 16, None)
     assert e.value.status == kvd.KVD_ERR_INVALID
+    # a shape whose planned workspace (five partial slots a split) exceeds the scratch but whose
+    # unplanned one fits: accepted, since the entry point never takes a plan
+    need_planned = kvd.kvd_decode_workspace_bytes(pool.handle, 64, 16, 16, 1500)[1]
+    assert need_planned > kvd.NOALLOC_SCRATCH_BYTES
+    bt_w = w.block_table()
+    H.fill_layer(pool, w, 0, bt_w, [16], cuda_device)            # request 0's 16 tokens, shared by all 16
+    bt16 = bt_w[:1].repeat(16, 1).to(cuda_device)
+    seq16 = torch.full((16,), 16, dtype=torch.int32, device=cuda_device)
+    q16 = w.q(0, 0, cuda_device).repeat(16, 1, 1).contiguous()
+    out16 = torch.empty(16, 64, 128, dtype=torch.float32, device=cuda_device)
+    kvd.kvd_decode_attn_noalloc(pool.handle, 0, q16, bt16, seq16, 16, out16, num_splits=1500)
+    assert kvd.kvd_get_device_error(pool.handle) == 0
+    ref = H.oracle_layer(w, 0, bt_w, [16])["out"][0]
+    for b in range(16):
+        H.assert_out_close(out16[b].cpu().numpy(), ref, what=f"request {b}")
