@@ -976,7 +976,9 @@ __global__ void __launch_bounds__(kThreads, ((KIND == kKindFp8 || KIND == kKindA
             if (!dyn || aborted) break;
             // Take the next piece.  A number past the last piece ends the CTA's work: one stage tagged
             // -1 tells the consumer warps, and the last CTA to get here puts the counters back to zero
-            // for the next launch that shares the plan.
+            // for the next launch that shares the plan.  That launch cannot take a piece earlier: its
+            // own part (at least 5/6 of kDynMinChunk blocks) outlasts its ring, so its producer waits
+            // for its consumers, and they wait for this launch to complete before their first block.
             int d = 0;
             if (lane == 0) d = atomicAdd(p.dyn, 1);
             d = __shfl_sync(kFull, d, 0);
