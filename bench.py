@@ -705,6 +705,11 @@ def gpu_workload(args, w, rank, world, local, peaks, headline: bool) -> dict:
         "data": "synthetic (seeded counter-hash generator)",
         "config": workload_config(w),
         "launch": {"num_splits": st.splits, "early_start": st.early, "step_plan": st.planned,
+                   # the decode kernel balances the last sixth of every split's range at run time for
+                   # planned BF16 calls whose ranges hold at least 192 blocks (computed here the same way)
+                   "run_time_balancing": bool(st.planned and w.kv_dtype == "bf16" and
+                                              -(-sum(-(-n // w.block_size) for n in w.seq_lens(0)) * w.n_kv
+                                                // st.splits) >= 192),
                    "score_update": ("second stream (off the layer chain)" if st.overlap else
                                     "fused into the call's epilogue launch" if w.scores else None),
                    "parallelism": f"replicas x{world}"},
